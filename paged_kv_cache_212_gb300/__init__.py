@@ -1,3 +1,246 @@
 """GB300-native paged KV cache: page write (bf16 / int8), gather, in-place paged
 decode attention with split-KV, and chunked paged prefill, as hand-written
-sm_103a CUDA kernels behind a C ABI (libpagedkv.so)."""
+sm_103a CUDA kernels behind the C ABI of ``libpagedkv.so`` (``include/pagedkv.h``).
+
+This module is argument marshalling only: it checks tensor shapes, dtypes and
+devices, passes raw device pointers and the current CUDA stream to the
+library, and turns a non-zero status into an exception.  Every step of the
+computation runs in the library's kernels; there is no CPU or PyTorch
+fallback, and using any call without the built library raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libpagedkv.so")
+
+PKV_KV_BF16, PKV_KV_INT8 = 0, 1
+DEV_BAD_BLOCK_ID, DEV_BAD_POSITION, DEV_BAD_LENGTH = 1, 2, 4
+DEV_WORKSPACE_OVERFLOW, DEV_TIMEOUT = 8, 16
+
+EXPORTS = ("pkv_status_string", "pkv_last_cuda_error", "paged_kv_write", "paged_kv_write_int8",
+           "paged_kv_gather", "pkv_decode_workspace_bytes", "paged_decode_attention",
+           "paged_prefill_attention")
+
+
+class PagedKVError(RuntimeError):
+    def __init__(self, fn, status, name, cuda_error=0):
+        msg = f"{fn} returned {name} ({status})"
+        if cuda_error:
+            msg += f", cudaError {cuda_error}"
+        super().__init__(msg)
+        self.status = status
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [("n_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def load_library(path: str = LIB_PATH):
+    """Load libpagedkv.so (raises if it has not been built)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with paged_kv_cache_212_gb300.build.build() "
+                           "(nvcc, sm_103a); there is no fallback path")
+    lib = ctypes.CDLL(path)
+    P, i32, i64, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+    lib.pkv_status_string.argtypes = [ctypes.c_int]
+    lib.pkv_status_string.restype = ctypes.c_char_p
+    lib.pkv_last_cuda_error.argtypes = []
+    lib.pkv_last_cuda_error.restype = ctypes.c_int
+    lib.paged_kv_write.argtypes = [P, P, P, P, Dims, P, i32, P, i32, i32, P, P]
+    lib.paged_kv_write_int8.argtypes = [P, P, P, P, P, P, Dims, P, i32, P, i32, i32, P, P]
+    lib.paged_kv_gather.argtypes = [P, P, Dims, P, i32, P, i32, i32, P, P, P, P]
+    lib.pkv_decode_workspace_bytes.argtypes = [i32, i32, i32, i64, i32]
+    lib.pkv_decode_workspace_bytes.restype = sz
+    lib.paged_decode_attention.argtypes = [P, i32, P, P, P, P, i32, Dims, P, i32, P, i32, ctypes.c_float,
+                                           i32, P, P, P, sz, P, P]
+    lib.paged_prefill_attention.argtypes = [P, i32, P, P, Dims, P, i32, P, i32, i32, ctypes.c_float, P, P,
+                                            P, P]
+    for fn in ("paged_kv_write", "paged_kv_write_int8", "paged_kv_gather", "paged_decode_attention",
+               "paged_prefill_attention"):
+        getattr(lib, fn).restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _check(fn, status):
+    if status != 0:
+        lib = load_library()
+        raise PagedKVError(fn, status, lib.pkv_status_string(status).decode(),
+                           lib.pkv_last_cuda_error())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _need(t, name, dtype=None, ndim=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def pool_dims(k_pool: torch.Tensor) -> Dims:
+    """Geometry of a [n_blocks + 1, block_size, n_kv_heads, head_dim] pool (the
+    last row is the scratch block)."""
+    nb1, bs, hkv, d = k_pool.shape
+    return Dims(nb1 - 1, bs, hkv, d)
+
+
+def paged_kv_write(k_new, v_new, k_pool, v_pool, block_tables, start_pos, dev_status=None, stream=None):
+    """Native bf16 page write: k_new/v_new [n_seqs, n_new, Hkv, D] to positions
+    start_pos[s] .. of each sequence."""
+    lib = load_library()
+    for t, n in ((k_new, "k_new"), (v_new, "v_new"), (k_pool, "k_pool"), (v_pool, "v_pool")):
+        _need(t, n, torch.bfloat16, 4, k_pool.device)
+    _need(block_tables, "block_tables", torch.int32, 2, k_pool.device)
+    _need(start_pos, "start_pos", torch.int32, 1, k_pool.device)
+    if dev_status is not None:
+        _need(dev_status, "dev_status", torch.int32, None, k_pool.device)
+    st = lib.paged_kv_write(_ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool), pool_dims(k_pool),
+                            _ptr(block_tables), block_tables.shape[1], _ptr(start_pos), k_new.shape[0],
+                            k_new.shape[1], _ptr(dev_status), _stream(stream))
+    _check("paged_kv_write", st)
+
+
+def paged_kv_write_int8(k_new, v_new, k_pool, v_pool, k_scales, v_scales, block_tables, start_pos,
+                        dev_status=None, stream=None):
+    """Quantised page write: int8 pools [NB+1, bs, Hkv, D], fp32 scales [NB+1, bs, Hkv]."""
+    lib = load_library()
+    dev = k_pool.device
+    _need(k_new, "k_new", torch.bfloat16, 4, dev)
+    _need(v_new, "v_new", torch.bfloat16, 4, dev)
+    _need(k_pool, "k_pool", torch.int8, 4, dev)
+    _need(v_pool, "v_pool", torch.int8, 4, dev)
+    _need(k_scales, "k_scales", torch.float32, 3, dev)
+    _need(v_scales, "v_scales", torch.float32, 3, dev)
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(start_pos, "start_pos", torch.int32, 1, dev)
+    st = lib.paged_kv_write_int8(_ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool), _ptr(k_scales),
+                                 _ptr(v_scales), pool_dims(k_pool), _ptr(block_tables), block_tables.shape[1],
+                                 _ptr(start_pos), k_new.shape[0], k_new.shape[1], _ptr(dev_status),
+                                 _stream(stream))
+    _check("paged_kv_write_int8", st)
+
+
+def paged_kv_gather(k_pool, v_pool, block_tables, lens, out_tokens, k_out=None, v_out=None, dev_status=None,
+                    stream=None):
+    """Contiguous copy [n_seqs, Hkv, out_tokens, D] of every sequence's pages
+    (zeros past its length).  Returns (k_out, v_out)."""
+    lib = load_library()
+    dev = k_pool.device
+    _need(k_pool, "k_pool", torch.bfloat16, 4, dev)
+    _need(v_pool, "v_pool", torch.bfloat16, 4, dev)
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(lens, "lens", torch.int32, 1, dev)
+    n_seqs = block_tables.shape[0]
+    shape = (n_seqs, k_pool.shape[2], int(out_tokens), k_pool.shape[3])
+    if k_out is None:
+        k_out = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+    if v_out is None:
+        v_out = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+    _need(k_out, "k_out", torch.bfloat16, 4, dev)
+    _need(v_out, "v_out", torch.bfloat16, 4, dev)
+    st = lib.paged_kv_gather(_ptr(k_pool), _ptr(v_pool), pool_dims(k_pool), _ptr(block_tables),
+                             block_tables.shape[1], _ptr(lens), n_seqs, int(out_tokens), _ptr(k_out), _ptr(v_out),
+                             _ptr(dev_status), _stream(stream))
+    _check("paged_kv_gather", st)
+    return k_out, v_out
+
+
+def decode_workspace_bytes(n_seqs, n_q_heads, head_dim, max_total_ctx_tokens, split_tokens=0) -> int:
+    n = load_library().pkv_decode_workspace_bytes(int(n_seqs), int(n_q_heads), int(head_dim),
+                                                  int(max_total_ctx_tokens), int(split_tokens))
+    if n == 0:
+        raise ValueError("invalid arguments to pkv_decode_workspace_bytes")
+    return int(n)
+
+
+def paged_decode_attention(q, k_pool, v_pool, block_tables, ctx_lens, softmax_scale, k_scales=None,
+                           v_scales=None, split_tokens=0, out=None, lse_out=None, workspace=None,
+                           max_total_ctx_tokens=None, dev_status=None, stream=None):
+    """In-place paged GQA decode attention.  q [n_seqs, Hq, D] bf16; bf16 pools,
+    or int8 pools with k_scales/v_scales.  Returns out [n_seqs, Hq, D] bf16.
+    ``workspace`` (uint8 CUDA tensor) is allocated when not given, sized from
+    max_total_ctx_tokens (default: every table entry full)."""
+    lib = load_library()
+    dev = q.device
+    _need(q, "q", torch.bfloat16, 3, dev)
+    int8 = k_pool.dtype == torch.int8
+    _need(k_pool, "k_pool", torch.int8 if int8 else torch.bfloat16, 4, dev)
+    _need(v_pool, "v_pool", torch.int8 if int8 else torch.bfloat16, 4, dev)
+    if int8:
+        _need(k_scales, "k_scales", torch.float32, 3, dev)
+        _need(v_scales, "v_scales", torch.float32, 3, dev)
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(ctx_lens, "ctx_lens", torch.int32, 1, dev)
+    n_seqs, n_q_heads, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, 3, dev)
+    if lse_out is not None:
+        _need(lse_out, "lse_out", torch.float32, 2, dev)
+    if workspace is None:
+        if max_total_ctx_tokens is None:
+            max_total_ctx_tokens = n_seqs * block_tables.shape[1] * k_pool.shape[1]
+        nbytes = decode_workspace_bytes(n_seqs, n_q_heads, D, max_total_ctx_tokens, split_tokens)
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", torch.uint8, 1, dev)
+    st = lib.paged_decode_attention(_ptr(q), n_q_heads, _ptr(k_pool), _ptr(v_pool), _ptr(k_scales),
+                                    _ptr(v_scales), PKV_KV_INT8 if int8 else PKV_KV_BF16, pool_dims(k_pool),
+                                    _ptr(block_tables), block_tables.shape[1], _ptr(ctx_lens), n_seqs,
+                                    float(softmax_scale), int(split_tokens), _ptr(out), _ptr(lse_out),
+                                    _ptr(workspace), workspace.numel(), _ptr(dev_status), _stream(stream))
+    _check("paged_decode_attention", st)
+    return out
+
+
+def paged_prefill_attention(q, k_pool, v_pool, block_tables, prefix_lens, softmax_scale, out=None,
+                            lse_out=None, dev_status=None, stream=None):
+    """Chunked paged prefill: q [n_seqs, chunk, Hq, D] bf16 (the chunk's K/V
+    already written at prefix_lens[s] ..).  Returns out, same shape as q."""
+    lib = load_library()
+    dev = q.device
+    _need(q, "q", torch.bfloat16, 4, dev)
+    _need(k_pool, "k_pool", torch.bfloat16, 4, dev)
+    _need(v_pool, "v_pool", torch.bfloat16, 4, dev)
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(prefix_lens, "prefix_lens", torch.int32, 1, dev)
+    n_seqs, chunk, n_q_heads, _ = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, 4, dev)
+    if lse_out is not None:
+        _need(lse_out, "lse_out", torch.float32, 3, dev)
+    st = lib.paged_prefill_attention(_ptr(q), n_q_heads, _ptr(k_pool), _ptr(v_pool), pool_dims(k_pool),
+                                     _ptr(block_tables), block_tables.shape[1], _ptr(prefix_lens), n_seqs,
+                                     chunk, float(softmax_scale), _ptr(out), _ptr(lse_out), _ptr(dev_status),
+                                     _stream(stream))
+    _check("paged_prefill_attention", st)
+    return out

@@ -1,0 +1,884 @@
+// decode.cu -- in-place paged GQA decode attention with split-KV and a
+// log-sum-exp merge, for bf16 pages and for int8 pages with fp32 per-(token,
+// kv head) scales.
+//
+// Three launches on the caller's stream, no host synchronisation:
+//   1. decode_plan_kernel (one CTA): cuts every sequence's context into
+//      logical ranges of split_tokens tokens (metrale high_speed_swap
+//      impl_more.rs, attend_layer_on_stream_with_q_pos: tiles of resident
+//      blocks), writes the (sequence, split) work list into the workspace and
+//      resets the work counter.
+//   2. decode_split_kernel (persistent, one or two CTAs per SM): a producer
+//      warp takes (split, kv-head group) items from the counter and streams the
+//      item's pages, 16 tokens per stage, into a shared-memory ring with TMA
+//      (cp.async.bulk.tensor, 128-byte swizzle), addressed through the block
+//      table.  One consumer warp per kv head contracts the stage with its GQA
+//      query group on the tensor cores (mma.sync m16n8k16: S^T = K Q^T with the
+//      16 tokens as M and the query heads as N, then O^T += V^T P^T) and keeps
+//      an online softmax (running max and sum in log2 units).  A sequence with
+//      one split writes its output directly; otherwise the item writes its
+//      partial (m, l, acc) to the workspace.
+//   3. decode_merge_kernel: for multi-split sequences, o = sum_k 2^(m_k - M)
+//      acc_k / sum_k 2^(m_k - M) l_k (the finalize step of the tiled
+//      attention), and lse = ln 2 (M + log2 L).
+//
+// Pool tiles in shared memory: for each stage and each 64-element half of
+// head_dim, a [heads][16 tokens][128 bytes] box with the TMA 128-byte swizzle
+// (16-byte chunk c of row r stored at chunk c ^ (r & 7)), so ldmatrix reads of
+// eight consecutive tokens hit eight different bank groups.
+#include <math.h>
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace pkv {
+
+namespace {
+
+constexpr int kStageTokens = 16;
+constexpr int kMaxStages = 8;
+constexpr uint32_t kHdrCounter = 0, kHdrTotal = 1, kHdrOverflow = 2;
+
+enum : int32_t { kMetaFirst = 1, kMetaLast = 2, kMetaBad = 4, kMetaStop = 8, kMetaFinal = 16 };
+
+struct StageMeta {
+    int32_t seq;
+    int32_t split_index;  // index into the workspace split list
+    int32_t n_valid;      // valid tokens in this stage (1..16)
+    int32_t flags;
+    int32_t head_group;   // which group of hpc kv heads the item covers
+    int32_t pad[3];
+};
+
+struct DecodeParams {
+    const __nv_bfloat16 *q;
+    int32_t n_q_heads, group, hpc, n_hg;
+    int32_t n_blocks, block_size, n_kv_heads;
+    const int32_t *tables;
+    int32_t max_blocks;
+    const int32_t *ctx_lens;
+    int32_t n_seqs;
+    float scale_log2;
+    int32_t split_tokens;
+    __nv_bfloat16 *out;
+    float *lse_out;
+    DecodeWorkspace ws;
+    int32_t *dev_status;
+    int32_t n_stages;
+    int32_t boxes_per_half;  // TMA boxes per (K or V, half): 1 (all heads) or hpc (one per head)
+    uint32_t stage_bytes, tx_bytes, kv_tile_bytes, scale_tile_bytes, q_slot_bytes, scratch_bytes;
+};
+
+// Shared-memory carve-up (dynamic smem, base rounded up to 1024 bytes).
+struct SmemLayout {
+    uint8_t *stages;     // n_stages * stage_bytes
+    uint8_t *q_slots;    // 2 * q_slot_bytes
+    uint8_t *scratch;    // per-consumer-warp fp16 tiles (int8 pages only)
+    uint64_t *full_bar, *empty_bar, *qfull_bar, *qempty_bar;
+    StageMeta *meta;
+    int32_t *abort_flag;
+};
+
+__device__ __forceinline__ SmemLayout carve(uint8_t *smem, const DecodeParams &p)
+{
+    SmemLayout L;
+    uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem) + 1023) &
+                                                ~uintptr_t(1023));
+    L.stages = base;
+    base += (size_t)p.n_stages * p.stage_bytes;
+    L.q_slots = base;
+    base += 2 * (size_t)p.q_slot_bytes;
+    L.scratch = base;
+    base += (size_t)p.hpc * p.scratch_bytes;
+    L.full_bar = reinterpret_cast<uint64_t *>(base);
+    L.empty_bar = L.full_bar + kMaxStages;
+    L.qfull_bar = L.empty_bar + kMaxStages;
+    L.qempty_bar = L.qfull_bar + 2;
+    L.meta = reinterpret_cast<StageMeta *>(L.qempty_bar + 2);
+    L.abort_flag = reinterpret_cast<int32_t *>(L.meta + kMaxStages);
+    return L;
+}
+
+__host__ __device__ constexpr size_t smem_tail_bytes()
+{
+    return (2 * kMaxStages + 4) * sizeof(uint64_t) + kMaxStages * sizeof(StageMeta) + 16;
+}
+
+// Exact int8 -> fp16 for four packed codes: (0x6400 | (b ^ 0x80)) is the fp16
+// value 1024 + b + 128, so subtracting 1152 leaves b exactly.
+__device__ __forceinline__ void int8x4_to_half2x2(uint32_t w, uint32_t &lo, uint32_t &hi)
+{
+    const uint32_t u = w ^ 0x80808080u;
+    uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);
+    uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);
+    const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6480));  // 1152
+    __half2 ha = __hsub2(*reinterpret_cast<__half2 *>(&a), bias);
+    __half2 hb = __hsub2(*reinterpret_cast<__half2 *>(&b), bias);
+    lo = *reinterpret_cast<uint32_t *>(&ha);
+    hi = *reinterpret_cast<uint32_t *>(&hb);
+}
+
+// Byte offset of the 16-byte chunk `chunk` (0..7) of row `row` in a
+// 128-byte-swizzled tile of 128-byte rows.
+__device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t chunk)
+{
+    return row * 128u + ((chunk ^ (row & 7u)) << 4);
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// 1. plan
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t *__restrict__ ctx_lens,
+                                                           int32_t n_seqs, int32_t split_tokens,
+                                                           int32_t max_tokens, DecodeWorkspace ws,
+                                                           int32_t *dev_status)
+{
+    __shared__ int32_t warp_sums[32];
+    __shared__ int32_t running_s;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) running_s = 0;
+    __syncthreads();
+    for (int32_t c0 = 0; c0 < n_seqs; c0 += blockDim.x) {
+        const int32_t s = c0 + tid;
+        int32_t n = 0;
+        if (s < n_seqs) {
+            const int32_t ctx = ctx_lens[s];
+            if (ctx < 0 || ctx > max_tokens)
+                report(dev_status, PKV_DEV_BAD_LENGTH);
+            else
+                n = (ctx + split_tokens - 1) / split_tokens;
+        }
+        int32_t incl = n;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            int32_t v = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += v;
+        }
+        if (lane == 31) warp_sums[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            int32_t v = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
+            int32_t vi = v;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                int32_t u = __shfl_up_sync(0xffffffffu, vi, off);
+                if (lane >= off) vi += u;
+            }
+            warp_sums[lane] = vi - v;  // exclusive prefix of warp totals
+        }
+        __syncthreads();
+        const int32_t base = running_s + warp_sums[warp] + incl - n;
+        if (s < n_seqs) {
+            ws.split_base[s] = base;
+            for (int32_t k = 0; k < n; ++k)
+                if (base + k < ws.capacity) ws.split_list[base + k] = make_int2(s, k);
+        }
+        __syncthreads();
+        if (tid == (int)blockDim.x - 1) running_s = base + n;
+        __syncthreads();
+    }
+    if (tid == 0) {
+        const int32_t total = running_s;
+        const bool overflow = total > ws.capacity;
+        if (overflow) report(dev_status, PKV_DEV_WORKSPACE_OVERFLOW);
+        ws.header[kHdrTotal] = overflow ? 0u : (uint32_t)total;
+        ws.header[kHdrOverflow] = overflow ? 1u : 0u;
+        ws.header[kHdrCounter] = 0u;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// 2. split kernel
+// ---------------------------------------------------------------------------
+template <int D, bool INT8>
+__global__ void __launch_bounds__(288, 1) decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
+                                                              const __grid_constant__ CUtensorMap v_map,
+                                                              const __grid_constant__ CUtensorMap ks_map,
+                                                              const __grid_constant__ CUtensorMap vs_map,
+                                                              const DecodeParams p)
+{
+    constexpr int HALVES = D / 64;      // 64-element (128-byte) column halves of a bf16 row
+    constexpr int KSTEPS = D / 16;      // mma k-steps over head_dim (QK) = m-tiles (PV)
+    extern __shared__ uint8_t smem_raw[];
+    SmemLayout L = carve(smem_raw, p);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int hpc = p.hpc;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < p.n_stages; ++i) {
+            mbar_init(&L.full_bar[i], 1);
+            mbar_init(&L.empty_bar[i], hpc);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&L.qfull_bar[i], 1);
+            mbar_init(&L.qempty_bar[i], hpc);
+        }
+        *L.abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    const uint32_t total_items = p.ws.header[kHdrTotal] * (uint32_t)p.n_hg;
+    volatile int32_t *abort_flag = L.abort_flag;
+
+    if (warp == hpc) {
+        // ===================== producer warp =====================
+        if (lane == 0) {
+            prefetch_tensormap(&k_map);
+            prefetch_tensormap(&v_map);
+            if (INT8) {
+                prefetch_tensormap(&ks_map);
+                prefetch_tensormap(&vs_map);
+            }
+        }
+        uint32_t stage_it = 0, item_it = 0;
+        uint32_t next = 0;
+        if (lane == 0) next = atomicAdd(&p.ws.header[kHdrCounter], 1u);
+        next = __shfl_sync(0xffffffffu, next, 0);
+        bool ok = true;
+        while (ok && next < total_items) {
+            const uint32_t it = next;
+            if (lane == 0) next = atomicAdd(&p.ws.header[kHdrCounter], 1u);
+            const int32_t sp = (int32_t)(it / p.n_hg), hg = (int32_t)(it % p.n_hg);
+            const int2 sk = p.ws.split_list[sp];
+            const int32_t s = sk.x;
+            const int32_t ctx = __ldg(p.ctx_lens + s);
+            const int32_t t0 = sk.y * p.split_tokens;
+            const int32_t t1 = min(t0 + p.split_tokens, ctx);
+            const bool final_out = ctx <= p.split_tokens;
+            const int32_t *trow = p.tables + (int64_t)s * p.max_blocks;
+            const int32_t blk0 = t0 / p.block_size;
+            // this item's queries: heads [hg*hpc*G, (hg+1)*hpc*G) of sequence s
+            const uint32_t qs = item_it & 1u;
+            if (lane == 0) {
+                if (!mbar_wait(&L.qempty_bar[qs], ((item_it >> 1) & 1u) ^ 1u, abort_flag)) {
+                    report(p.dev_status, PKV_DEV_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                if (!*abort_flag) {
+                    mbar_arrive_expect_tx(&L.qfull_bar[qs], p.q_slot_bytes);
+                    bulk_g2s(L.q_slots + qs * p.q_slot_bytes,
+                             p.q + ((int64_t)s * p.n_q_heads + (int64_t)hg * hpc * p.group) * D,
+                             p.q_slot_bytes, &L.qfull_bar[qs]);
+                }
+            }
+            ok = !__shfl_sync(0xffffffffu, *abort_flag, 0);
+            int32_t tbl = 0, tbl_base = -1;
+            for (int32_t t = t0; ok && t < t1; t += kStageTokens) {
+                const int32_t lb = t / p.block_size;
+                if (lb - blk0 >= tbl_base + 32 || tbl_base < 0) {
+                    tbl_base = lb - blk0;
+                    const int32_t j = blk0 + tbl_base + lane;
+                    tbl = j < p.max_blocks ? __ldg(trow + j) : -1;
+                }
+                const int32_t blk = __shfl_sync(0xffffffffu, tbl, lb - blk0 - tbl_base);
+                if (lane == 0) {
+                    const uint32_t st = stage_it % p.n_stages;
+                    if (!mbar_wait(&L.empty_bar[st], ((stage_it / p.n_stages) & 1u) ^ 1u, abort_flag)) {
+                        report(p.dev_status, PKV_DEV_TIMEOUT);
+                        *abort_flag = 1;
+                    } else {
+                        StageMeta m;
+                        m.seq = s;
+                        m.split_index = sp;
+                        m.n_valid = min(kStageTokens, t1 - t);
+                        m.flags = (t == t0 ? kMetaFirst : 0) | (t + kStageTokens >= t1 ? kMetaLast : 0) |
+                                  (final_out ? kMetaFinal : 0);
+                        m.head_group = hg;
+                        const bool bad = blk < 0 || blk > p.n_blocks;
+                        if (bad) {
+                            m.flags |= kMetaBad;
+                            report(p.dev_status, PKV_DEV_BAD_BLOCK_ID);
+                        }
+                        L.meta[st] = m;
+                        if (bad) {
+                            mbar_arrive(&L.full_bar[st]);
+                        } else {
+                            uint8_t *stg = L.stages + (size_t)st * p.stage_bytes;
+                            const int32_t row0 = blk * p.block_size + (t % p.block_size);
+                            const int32_t head0 = hg * hpc;
+                            mbar_arrive_expect_tx(&L.full_bar[st], p.tx_bytes);
+                            if (!INT8) {
+                                const uint32_t half_bytes = (uint32_t)hpc * kStageTokens * 128u;
+                                for (int h = 0; h < HALVES; ++h) {
+                                    for (int b = 0; b < p.boxes_per_half; ++b) {
+                                        const uint32_t off = h * half_bytes + b * (kStageTokens * 128u);
+                                        if (p.boxes_per_half == 1) {
+                                            tma_load_3d(stg + off, &k_map, h * 64, row0, head0, &L.full_bar[st]);
+                                            tma_load_3d(stg + p.kv_tile_bytes + off, &v_map, h * 64, row0, head0,
+                                                        &L.full_bar[st]);
+                                        } else {
+                                            tma_load_3d(stg + off, &k_map, h * 64, head0 + b, row0, &L.full_bar[st]);
+                                            tma_load_3d(stg + p.kv_tile_bytes + off, &v_map, h * 64, head0 + b, row0,
+                                                        &L.full_bar[st]);
+                                        }
+                                    }
+                                }
+                            } else {
+                                for (int b = 0; b < p.boxes_per_half; ++b) {
+                                    const uint32_t off = b * (kStageTokens * (uint32_t)D);
+                                    if (p.boxes_per_half == 1) {
+                                        tma_load_3d(stg + off, &k_map, 0, row0, head0, &L.full_bar[st]);
+                                        tma_load_3d(stg + p.kv_tile_bytes + off, &v_map, 0, row0, head0,
+                                                    &L.full_bar[st]);
+                                    } else {
+                                        tma_load_3d(stg + off, &k_map, 0, head0 + b, row0, &L.full_bar[st]);
+                                        tma_load_3d(stg + p.kv_tile_bytes + off, &v_map, 0, head0 + b, row0,
+                                                    &L.full_bar[st]);
+                                    }
+                                }
+                                uint8_t *sc = stg + 2 * p.kv_tile_bytes;
+                                tma_load_2d(sc, &ks_map, head0, row0, &L.full_bar[st]);
+                                tma_load_2d(sc + p.scale_tile_bytes, &vs_map, head0, row0, &L.full_bar[st]);
+                            }
+                        }
+                    }
+                }
+                ok = !__shfl_sync(0xffffffffu, *abort_flag, 0);
+                ++stage_it;
+            }
+            ++item_it;
+            next = __shfl_sync(0xffffffffu, next, 0);
+        }
+        // stop marker
+        if (lane == 0 && !*abort_flag) {
+            const uint32_t st = stage_it % p.n_stages;
+            if (mbar_wait(&L.empty_bar[st], ((stage_it / p.n_stages) & 1u) ^ 1u, abort_flag)) {
+                L.meta[st].flags = kMetaStop;
+                mbar_arrive(&L.full_bar[st]);
+            } else {
+                report(p.dev_status, PKV_DEV_TIMEOUT);
+                *abort_flag = 1;
+            }
+        }
+        if (lane == 0 && *abort_flag) {
+            // wind down: let every load already issued land before the CTA exits
+            const uint32_t first = stage_it > (uint32_t)p.n_stages ? stage_it - p.n_stages : 0;
+            for (uint32_t i = first; i < stage_it; ++i)
+                (void)mbar_wait(&L.full_bar[i % p.n_stages], (i / p.n_stages) & 1u);
+        }
+        return;
+    }
+    if (warp > hpc) return;
+
+    // ===================== consumer warps (one kv head each) =====================
+    const int g = lane >> 2, qd = lane & 3;   // mma fragment row group / column pair
+    const int G = p.group;
+    const int mi = lane >> 3, ri = lane & 7;  // ldmatrix matrix index / row within it
+    uint32_t qf[KSTEPS][2];                   // Q^T B-fragments (bf16, or fp16 for int8 pages)
+    float acc[KSTEPS][4];                     // O^T accumulators: rows d, columns query heads
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    uint32_t stage_it = 0, item_it = 0;
+    const uint32_t half_bytes = (uint32_t)hpc * kStageTokens * 128u;
+    uint8_t *scratch = L.scratch + (size_t)warp * p.scratch_bytes;
+
+    while (true) {
+        const uint32_t st = stage_it % p.n_stages;
+        if (!__all_sync(0xffffffffu, mbar_wait(&L.full_bar[st], (stage_it / p.n_stages) & 1u, abort_flag))) {
+            if (lane == 0) report(p.dev_status, PKV_DEV_TIMEOUT);
+            *abort_flag = 1;
+            break;
+        }
+        const StageMeta meta = L.meta[st];
+        if (meta.flags & kMetaStop) break;
+        uint8_t *stg = L.stages + (size_t)st * p.stage_bytes;
+
+        if (meta.flags & kMetaFirst) {
+            const uint32_t qs = item_it & 1u;
+            if (!__all_sync(0xffffffffu, mbar_wait(&L.qfull_bar[qs], (item_it >> 1) & 1u, abort_flag))) {
+                if (lane == 0) report(p.dev_status, PKV_DEV_TIMEOUT);
+                *abort_flag = 1;
+                break;
+            }
+            const __nv_bfloat16 *qsm =
+                reinterpret_cast<const __nv_bfloat16 *>(L.q_slots + qs * p.q_slot_bytes) +
+                (size_t)warp * G * D;
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS; ++kk) {
+                uint32_t b0 = 0, b1 = 0;
+                if (g < G) {
+                    const __nv_bfloat16 *qr = qsm + (size_t)g * D + kk * 16 + 2 * qd;
+                    __nv_bfloat162 x0 = *reinterpret_cast<const __nv_bfloat162 *>(qr);
+                    __nv_bfloat162 x1 = *reinterpret_cast<const __nv_bfloat162 *>(qr + 8);
+                    if (INT8) {
+                        float2 f0 = __bfloat1622float2(x0), f1 = __bfloat1622float2(x1);
+                        b0 = pack_f16x2(f0.x, f0.y);
+                        b1 = pack_f16x2(f1.x, f1.y);
+                    } else {
+                        b0 = *reinterpret_cast<uint32_t *>(&x0);
+                        b1 = *reinterpret_cast<uint32_t *>(&x1);
+                    }
+                }
+                qf[kk][0] = b0;
+                qf[kk][1] = b1;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&L.qempty_bar[qs]);
+#pragma unroll
+            for (int mt = 0; mt < KSTEPS; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
+            m0 = m1 = -INFINITY;
+            l0 = l1 = 0.f;
+        }
+
+        if (!(meta.flags & kMetaBad)) {
+            const int nv = meta.n_valid;
+            // --- tiles for this head: bf16 straight from the stage, int8 via fp16 scratch
+            uint32_t k_base, v_base;     // smem address of half 0 of this head's K / V tile
+            uint32_t half_stride;        // bytes between the two 64-column halves
+            float sk0 = 1.f, sk1 = 1.f, sv0 = 1.f, sv1 = 1.f;
+            if (!INT8) {
+                k_base = smem_u32(stg) + warp * (kStageTokens * 128u);
+                v_base = k_base + p.kv_tile_bytes;
+                half_stride = half_bytes;
+            } else {
+                // convert this head's codes to fp16 tiles laid out like the bf16 ones
+                const uint8_t *kc = stg + (size_t)warp * kStageTokens * D;
+                const uint8_t *vc = kc + p.kv_tile_bytes;
+                constexpr int CPR = D / 16;  // 16-code chunks per row
+#pragma unroll
+                for (int j = 0; j < (kStageTokens * CPR) / 32; ++j) {
+                    const int idx = j * 32 + lane;
+                    const int tok = idx / CPR, c = idx % CPR;
+                    const uint32_t src_off = D == 128 ? swz(tok, c) : (uint32_t)(tok * D + c * 16);
+                    const uint4 kw = *reinterpret_cast<const uint4 *>(kc + src_off);
+                    const uint4 vw = *reinterpret_cast<const uint4 *>(vc + src_off);
+                    uint4 klo, khi, vlo, vhi;
+                    int8x4_to_half2x2(kw.x, klo.x, klo.y);
+                    int8x4_to_half2x2(kw.y, klo.z, klo.w);
+                    int8x4_to_half2x2(kw.z, khi.x, khi.y);
+                    int8x4_to_half2x2(kw.w, khi.z, khi.w);
+                    int8x4_to_half2x2(vw.x, vlo.x, vlo.y);
+                    int8x4_to_half2x2(vw.y, vlo.z, vlo.w);
+                    int8x4_to_half2x2(vw.z, vhi.x, vhi.y);
+                    int8x4_to_half2x2(vw.w, vhi.z, vhi.w);
+                    // fp16 elements d = 16c .. 16c+15 -> half (16c)/64, chunks (c%4)*2, +1
+                    const uint32_t hoff = (uint32_t)((16 * c) / 64) * (kStageTokens * 128u);
+                    const uint32_t c0 = (uint32_t)((c % 4) * 2);
+                    uint8_t *ks_ = scratch + hoff;
+                    uint8_t *vs_ = scratch + HALVES * kStageTokens * 128u + hoff;
+                    *reinterpret_cast<uint4 *>(ks_ + swz(tok, c0)) = klo;
+                    *reinterpret_cast<uint4 *>(ks_ + swz(tok, c0 + 1)) = khi;
+                    *reinterpret_cast<uint4 *>(vs_ + swz(tok, c0)) = vlo;
+                    *reinterpret_cast<uint4 *>(vs_ + swz(tok, c0 + 1)) = vhi;
+                }
+                __syncwarp();
+                k_base = smem_u32(scratch);
+                v_base = k_base + HALVES * kStageTokens * 128u;
+                half_stride = kStageTokens * 128u;
+                const float *sc = reinterpret_cast<const float *>(stg + 2 * p.kv_tile_bytes);
+                sk0 = sc[g * hpc + warp];
+                sk1 = sc[(g + 8) * hpc + warp];
+                const float *scv = sc + p.scale_tile_bytes / 4;
+                sv0 = scv[g * hpc + warp];
+                sv1 = scv[(g + 8) * hpc + warp];
+            }
+
+            // --- S^T[16 tokens x 8 heads] = K Q^T
+            float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kk = 0; kk < KSTEPS; ++kk) {
+                const int tok = ri + 8 * (mi & 1);
+                const uint32_t chunk = (uint32_t)((kk % 4) * 2 + (mi >> 1));
+                uint32_t a[4];
+                ldmatrix_x4(a, k_base + (uint32_t)(kk / 4) * half_stride + swz(tok, chunk));
+                if (INT8)
+                    mma_f16_16816(s4, a, qf[kk][0], qf[kk][1]);
+                else
+                    mma_bf16_16816(s4, a, qf[kk][0], qf[kk][1]);
+            }
+            // scale to log2 units, dequantise K (int8), mask tokens past the context
+            const bool v0 = g < nv, v1 = g + 8 < nv;
+            float x0 = v0 ? s4[0] * sk0 * p.scale_log2 : -INFINITY;
+            float x1 = v0 ? s4[1] * sk0 * p.scale_log2 : -INFINITY;
+            float x2 = v1 ? s4[2] * sk1 * p.scale_log2 : -INFINITY;
+            float x3 = v1 ? s4[3] * sk1 * p.scale_log2 : -INFINITY;
+            float bm0 = fmaxf(x0, x2), bm1 = fmaxf(x1, x3);
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
+                bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
+            }
+            const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+            const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
+            const float p0 = fast_exp2(x0 - mn0), p1 = fast_exp2(x1 - mn1);
+            const float p2 = fast_exp2(x2 - mn0), p3 = fast_exp2(x3 - mn1);
+            m0 = mn0;
+            m1 = mn1;
+            l0 = l0 * al0 + p0 + p2;
+            l1 = l1 * al1 + p1 + p3;
+            if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+                for (int mt = 0; mt < KSTEPS; ++mt) {
+                    acc[mt][0] *= al0;
+                    acc[mt][1] *= al1;
+                    acc[mt][2] *= al0;
+                    acc[mt][3] *= al1;
+                }
+            }
+            // P^T as the B operand of O^T += V^T P^T (int8: fold the V scale into P)
+            uint32_t pb0, pb1;
+            if (INT8) {
+                pb0 = movmatrix_trans(pack_f16x2(v0 ? p0 * sv0 : 0.f, v0 ? p1 * sv0 : 0.f));
+                pb1 = movmatrix_trans(pack_f16x2(v1 ? p2 * sv1 : 0.f, v1 ? p3 * sv1 : 0.f));
+            } else {
+                pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
+                pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
+            }
+            // V rows past the context may hold anything (even NaN): zero them in the
+            // A fragments of a partial stage so 0 * NaN never reaches the sum.
+            uint32_t vmask0 = 0xffffffffu, vmask1 = 0xffffffffu;
+            if (!INT8 && nv < kStageTokens) {
+                const int ta = 2 * qd, tb = 2 * qd + 8;
+                vmask0 = (ta < nv ? 0x0000ffffu : 0u) | (ta + 1 < nv ? 0xffff0000u : 0u);
+                vmask1 = (tb < nv ? 0x0000ffffu : 0u) | (tb + 1 < nv ? 0xffff0000u : 0u);
+            }
+#pragma unroll
+            for (int mt = 0; mt < KSTEPS; ++mt) {
+                const int tok = ri + 8 * (mi >> 1);
+                const uint32_t chunk = (uint32_t)((mt % 4) * 2 + (mi & 1));
+                uint32_t a[4];
+                ldmatrix_x4_trans(a, v_base + (uint32_t)(mt / 4) * half_stride + swz(tok, chunk));
+                if (INT8) {
+                    mma_f16_16816(acc[mt], a, pb0, pb1);
+                } else {
+                    a[0] &= vmask0;
+                    a[1] &= vmask0;
+                    a[2] &= vmask1;
+                    a[3] &= vmask1;
+                    mma_bf16_16816(acc[mt], a, pb0, pb1);
+                }
+            }
+            if (INT8) __syncwarp();  // scratch is rewritten by the next stage
+        }
+
+        if (meta.flags & kMetaLast) {
+            float L0 = l0, L1 = l1;
+#pragma unroll
+            for (int off = 4; off < 32; off <<= 1) {
+                L0 += __shfl_xor_sync(0xffffffffu, L0, off);
+                L1 += __shfl_xor_sync(0xffffffffu, L1, off);
+            }
+            const int32_t s = meta.seq;
+            // first query head of this warp's group: columns 2qd, 2qd+1 are hbase + n0, n1
+            const int32_t hbase = (meta.head_group * hpc + warp) * G;
+            const int n0 = 2 * qd, n1 = 2 * qd + 1;
+            if (meta.flags & kMetaFinal) {
+                const float inv0 = 1.f / L0, inv1 = 1.f / L1;
+                __nv_bfloat16 *o = p.out + ((int64_t)s * p.n_q_heads + hbase) * D;
+#pragma unroll
+                for (int mt = 0; mt < KSTEPS; ++mt) {
+                    const int d = mt * 16 + g;
+                    if (n0 < G) {
+                        o[(size_t)n0 * D + d] = __float2bfloat16_rn(acc[mt][0] * inv0);
+                        o[(size_t)n0 * D + d + 8] = __float2bfloat16_rn(acc[mt][2] * inv0);
+                    }
+                    if (n1 < G) {
+                        o[(size_t)n1 * D + d] = __float2bfloat16_rn(acc[mt][1] * inv1);
+                        o[(size_t)n1 * D + d + 8] = __float2bfloat16_rn(acc[mt][3] * inv1);
+                    }
+                }
+                if (p.lse_out && g == 0) {
+                    float *lo = p.lse_out + (int64_t)s * p.n_q_heads + hbase;
+                    if (n0 < G) lo[n0] = (m0 + __log2f(L0)) * 0.69314718055994531f;
+                    if (n1 < G) lo[n1] = (m1 + __log2f(L1)) * 0.69314718055994531f;
+                }
+            } else {
+                const int64_t prow = (int64_t)meta.split_index * p.n_q_heads + hbase;
+                float *pa = p.ws.part_acc + prow * D;
+#pragma unroll
+                for (int mt = 0; mt < KSTEPS; ++mt) {
+                    const int d = mt * 16 + g;
+                    if (n0 < G) {
+                        pa[(size_t)n0 * D + d] = acc[mt][0];
+                        pa[(size_t)n0 * D + d + 8] = acc[mt][2];
+                    }
+                    if (n1 < G) {
+                        pa[(size_t)n1 * D + d] = acc[mt][1];
+                        pa[(size_t)n1 * D + d + 8] = acc[mt][3];
+                    }
+                }
+                if (g == 0) {
+                    if (n0 < G) p.ws.part_ml[prow + n0] = make_float2(m0, L0);
+                    if (n1 < G) p.ws.part_ml[prow + n1] = make_float2(m1, L1);
+                }
+            }
+            ++item_it;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&L.empty_bar[st]);
+        ++stage_it;
+    }
+}
+
+}  // namespace pkv
+
+namespace pkv {
+
+// ---------------------------------------------------------------------------
+// 3. merge of split partials
+// ---------------------------------------------------------------------------
+// One warp per (sequence, query head).  Sequences with exactly one split were
+// finished by the split kernel; an empty (or invalid) context gives o = 0,
+// lse = -inf.
+template <int D>
+__global__ void __launch_bounds__(128) decode_merge_kernel(
+    const int32_t *__restrict__ ctx_lens, int32_t n_seqs, int32_t n_q_heads, int32_t split_tokens,
+    int32_t max_tokens, DecodeWorkspace ws, __nv_bfloat16 *__restrict__ out, float *lse_out)
+{
+    constexpr int EPL = D / 32;
+    const int lane = threadIdx.x & 31;
+    const int64_t idx = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (idx >= (int64_t)n_seqs * n_q_heads) return;
+    const int32_t s = (int32_t)(idx / n_q_heads);
+    const int32_t ctx = __ldg(ctx_lens + s);
+    const int32_t n = (ctx > 0 && ctx <= max_tokens) ? (ctx + split_tokens - 1) / split_tokens : 0;
+    const bool overflow = ws.header[kHdrOverflow] != 0;
+    if (n == 1 && !overflow) return;
+    float o[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) o[e] = 0.f;
+    float lse = -INFINITY;
+    if (n > 1 && !overflow) {
+        const int64_t base = ws.split_base[s];
+        float M = -INFINITY;
+        for (int32_t k = 0; k < n; ++k) M = fmaxf(M, ws.part_ml[(base + k) * n_q_heads + idx % n_q_heads].x);
+        if (M != -INFINITY) {
+            float Lsum = 0.f;
+            for (int32_t k = 0; k < n; ++k) {
+                const int64_t row = (base + k) * n_q_heads + idx % n_q_heads;
+                const float2 ml = ws.part_ml[row];
+                const float w = exp2f(ml.x - M);
+                Lsum += ml.y * w;
+                const float *pa = ws.part_acc + row * D + lane * EPL;
+                if constexpr (EPL == 4) {
+                    const float4 a = *reinterpret_cast<const float4 *>(pa);
+                    o[0] += a.x * w;
+                    o[1] += a.y * w;
+                    o[2] += a.z * w;
+                    o[3] += a.w * w;
+                } else {
+                    const float2 a = *reinterpret_cast<const float2 *>(pa);
+                    o[0] += a.x * w;
+                    o[1] += a.y * w;
+                }
+            }
+            const float inv = 1.f / Lsum;
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) o[e] *= inv;
+            lse = (M + log2f(Lsum)) * 0.69314718055994531f;
+        }
+    }
+    __nv_bfloat16 *dst = out + idx * D + lane * EPL;
+    if constexpr (EPL == 4) {
+        uint2 v;
+        v.x = pack_bf16x2(o[0], o[1]);
+        v.y = pack_bf16x2(o[2], o[3]);
+        *reinterpret_cast<uint2 *>(dst) = v;
+    } else {
+        *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(o[0], o[1]);
+    }
+    if (lse_out && lane == 0) lse_out[idx] = lse;
+}
+
+// ---------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------
+
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+size_t decode_workspace_bytes(int32_t n_seqs, int32_t n_q_heads, int32_t head_dim, int64_t capacity)
+{
+    size_t b = 256;                                          // header
+    b += align_up((size_t)n_seqs * sizeof(int32_t), 256);    // split_base
+    b += align_up((size_t)capacity * sizeof(int2), 256);     // split_list
+    b += align_up((size_t)capacity * n_q_heads * sizeof(float2), 256);
+    b += align_up((size_t)capacity * n_q_heads * head_dim * sizeof(float), 256);
+    return b;
+}
+
+bool carve_decode_workspace(void *ws, size_t bytes, int32_t n_seqs, int32_t n_q_heads,
+                            int32_t head_dim, DecodeWorkspace *out)
+{
+    if (!ws) return false;
+    const size_t fixed = 256 + align_up((size_t)n_seqs * sizeof(int32_t), 256) + 3 * 256;
+    if (bytes < fixed) return false;
+    const size_t per = sizeof(int2) + (size_t)n_q_heads * sizeof(float2) +
+                       (size_t)n_q_heads * head_dim * sizeof(float);
+    int64_t cap = (int64_t)((bytes - fixed) / per);
+    while (cap > 0 && decode_workspace_bytes(n_seqs, n_q_heads, head_dim, cap) > bytes) --cap;
+    if (cap > (int64_t)0x7fffffff) cap = 0x7fffffff;
+    uint8_t *p = static_cast<uint8_t *>(ws);
+    out->header = reinterpret_cast<uint32_t *>(p);
+    p += 256;
+    out->split_base = reinterpret_cast<int32_t *>(p);
+    p += align_up((size_t)n_seqs * sizeof(int32_t), 256);
+    out->split_list = reinterpret_cast<int2 *>(p);
+    p += align_up((size_t)cap * sizeof(int2), 256);
+    out->part_ml = reinterpret_cast<float2 *>(p);
+    p += align_up((size_t)cap * n_q_heads * sizeof(float2), 256);
+    out->part_acc = reinterpret_cast<float *>(p);
+    out->capacity = (int32_t)cap;
+    return true;
+}
+
+namespace {
+
+int env_int(const char *name, int fallback)
+{
+    const char *v = getenv(name);
+    return (v && *v) ? atoi(v) : fallback;
+}
+
+// Pool tile map for TMA: preferred is a 3-D view {col, row, head} whose box
+// {box_cols, 16, hpc} fetches 16 token rows of hpc heads in one copy; if the
+// driver rejects the non-monotonic strides, a {col, head, row} view with one
+// box {box_cols, 1, 16} per head.  Returns boxes per column block (1 or hpc),
+// or -1 on failure.
+int encode_pool_map(CUtensorMap *map, const void *pool, CUtensorMapDataType dt, uint32_t elem_bytes,
+                    const pkv_dims &d, int hpc, uint32_t box_cols, CUtensorMapSwizzle swz)
+{
+    const uint64_t rows = (uint64_t)(d.n_blocks + 1) * d.block_size;
+    const uint64_t row_bytes = (uint64_t)d.n_kv_heads * d.head_dim * elem_bytes;
+    const uint64_t head_bytes = (uint64_t)d.head_dim * elem_bytes;
+    {
+        const uint64_t dims[3] = {(uint64_t)d.head_dim, rows, (uint64_t)d.n_kv_heads};
+        const uint64_t strides[2] = {row_bytes, head_bytes};
+        const uint32_t box[3] = {box_cols, 16u, (uint32_t)hpc};
+        if (encode_tensor_map(map, dt, 3, const_cast<void *>(pool), dims, strides, box, swz) ==
+            CUDA_SUCCESS)
+            return 1;
+    }
+    const uint64_t dims[3] = {(uint64_t)d.head_dim, (uint64_t)d.n_kv_heads, rows};
+    const uint64_t strides[2] = {head_bytes, row_bytes};
+    const uint32_t box[3] = {box_cols, 1u, 16u};
+    if (encode_tensor_map(map, dt, 3, const_cast<void *>(pool), dims, strides, box, swz) ==
+        CUDA_SUCCESS)
+        return hpc;
+    return -1;
+}
+
+template <int D, bool INT8>
+cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream)
+{
+    const pkv_dims &d = a.dims;
+    const int G = a.n_q_heads / d.n_kv_heads;
+    int hpc = env_int("PKV_DECODE_HPC", d.n_kv_heads <= 8 ? d.n_kv_heads : 8);
+    if (hpc <= 0 || hpc > 8 || d.n_kv_heads % hpc != 0) hpc = d.n_kv_heads <= 8 ? d.n_kv_heads : 8;
+    if (INT8 && hpc % 4 != 0) return cudaErrorInvalidValue;
+    int ctas_per_sm = env_int("PKV_DECODE_CTAS_PER_SM", 1);
+    if (ctas_per_sm < 1 || ctas_per_sm > 4) ctas_per_sm = 1;
+
+    DecodeParams p{};
+    p.q = static_cast<const __nv_bfloat16 *>(a.q);
+    p.n_q_heads = a.n_q_heads;
+    p.group = G;
+    p.hpc = hpc;
+    p.n_hg = d.n_kv_heads / hpc;
+    p.n_blocks = d.n_blocks;
+    p.block_size = d.block_size;
+    p.n_kv_heads = d.n_kv_heads;
+    p.tables = a.tables;
+    p.max_blocks = a.max_blocks;
+    p.ctx_lens = a.ctx_lens;
+    p.n_seqs = a.n_seqs;
+    p.scale_log2 = a.softmax_scale * 1.4426950408889634f;
+    p.split_tokens = a.split_tokens;
+    p.out = static_cast<__nv_bfloat16 *>(a.out);
+    p.lse_out = a.lse_out;
+    p.ws = a.ws;
+    p.dev_status = a.dev_status;
+    if (!INT8) {
+        p.kv_tile_bytes = (uint32_t)(D / 64) * hpc * 16u * 128u;
+        p.scale_tile_bytes = 0;
+        p.scratch_bytes = 0;
+        p.tx_bytes = 2 * p.kv_tile_bytes;
+    } else {
+        p.kv_tile_bytes = (uint32_t)hpc * 16u * D;
+        p.scale_tile_bytes = (uint32_t)hpc * 16u * 4u;
+        p.scratch_bytes = 2u * (D / 64) * 16u * 128u;
+        p.tx_bytes = 2 * p.kv_tile_bytes + 2 * p.scale_tile_bytes;
+    }
+    p.stage_bytes = (uint32_t)align_up(p.tx_bytes, 1024);
+    p.q_slot_bytes = (uint32_t)(hpc * G * D * 2);
+
+    CUtensorMap kmap, vmap, ksmap, vsmap;
+    memset(&ksmap, 0, sizeof ksmap);
+    memset(&vsmap, 0, sizeof vsmap);
+    const CUtensorMapDataType dt = INT8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const uint32_t eb = INT8 ? 1 : 2;
+    const uint32_t box_cols = INT8 ? (uint32_t)D : 64u;
+    const CUtensorMapSwizzle sw = (INT8 && D == 64) ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B;
+    const int bk = encode_pool_map(&kmap, a.k_pool, dt, eb, d, hpc, box_cols, sw);
+    const int bv = encode_pool_map(&vmap, a.v_pool, dt, eb, d, hpc, box_cols, sw);
+    if (bk < 0 || bv < 0 || bk != bv) return cudaErrorInvalidValue;
+    p.boxes_per_half = bk;
+    if (INT8) {
+        const uint64_t rows = (uint64_t)(d.n_blocks + 1) * d.block_size;
+        const uint64_t dims[2] = {(uint64_t)d.n_kv_heads, rows};
+        const uint64_t strides[1] = {(uint64_t)d.n_kv_heads * 4};
+        const uint32_t box[2] = {(uint32_t)hpc, 16u};
+        if (encode_tensor_map(&ksmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, (void *)a.k_scales, dims, strides,
+                              box, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS ||
+            encode_tensor_map(&vsmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, (void *)a.v_scales, dims, strides,
+                              box, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+
+    // shared memory: stages fill what one CTA may hold at ctas_per_sm per SM
+    const size_t max_smem = 232448;  // 227 KiB per CTA on sm_103
+    const size_t per_cta = max_smem / ctas_per_sm - (ctas_per_sm > 1 ? 1024 : 0);
+    const size_t fixed = 1024 + 2 * (size_t)p.q_slot_bytes + (size_t)hpc * p.scratch_bytes + smem_tail_bytes();
+    if (fixed + 2 * (size_t)p.stage_bytes > per_cta) return cudaErrorInvalidValue;
+    int stages = (int)((per_cta - fixed) / p.stage_bytes);
+    stages = stages > kMaxStages ? kMaxStages : stages;
+    const int want = env_int("PKV_DECODE_STAGES", 0);
+    if (want >= 2 && want < stages) stages = want;
+    p.n_stages = stages;
+    const size_t smem = fixed + (size_t)stages * p.stage_bytes;
+
+    auto kern = decode_split_kernel<D, INT8>;
+    static size_t configured = 0;
+    if (configured < smem) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        configured = smem;
+    }
+    const int threads = 32 * (hpc + 1);
+    int occ = 0;
+    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
+    if (e != cudaSuccess) return e;
+    if (occ < 1) return cudaErrorInvalidConfiguration;
+    const int grid = num_sms * (occ < ctas_per_sm ? occ : ctas_per_sm);
+    kern<<<grid, threads, smem, stream>>>(kmap, vmap, ksmap, vsmap, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const DecodeArgs &a, int num_sms, cudaStream_t stream)
+{
+    const int32_t max_tokens = a.max_blocks * a.dims.block_size;
+    decode_plan_kernel<<<1, 1024, 0, stream>>>(a.ctx_lens, a.n_seqs, a.split_tokens, max_tokens, a.ws,
+                                               a.dev_status);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const bool int8 = a.kv_dtype == PKV_KV_INT8;
+    if (a.dims.head_dim == 128)
+        e = int8 ? launch_split<128, true>(a, num_sms, stream) : launch_split<128, false>(a, num_sms, stream);
+    else
+        e = int8 ? launch_split<64, true>(a, num_sms, stream) : launch_split<64, false>(a, num_sms, stream);
+    if (e != cudaSuccess) return e;
+    const int64_t warps = (int64_t)a.n_seqs * a.n_q_heads;
+    const unsigned grid = (unsigned)((warps + 3) / 4);
+    if (a.dims.head_dim == 128)
+        decode_merge_kernel<128><<<grid, 128, 0, stream>>>(a.ctx_lens, a.n_seqs, a.n_q_heads, a.split_tokens,
+                                                           max_tokens, a.ws, (__nv_bfloat16 *)a.out, a.lse_out);
+    else
+        decode_merge_kernel<64><<<grid, 128, 0, stream>>>(a.ctx_lens, a.n_seqs, a.n_q_heads, a.split_tokens,
+                                                          max_tokens, a.ws, (__nv_bfloat16 *)a.out, a.lse_out);
+    return cudaGetLastError();
+}
+
+}  // namespace pkv

@@ -1,0 +1,106 @@
+// launch.h -- internal interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/pagedkv.h"
+
+namespace pkv {
+
+struct WriteArgs {
+    const void *k_new, *v_new;
+    void *k_pool, *v_pool;
+    pkv_dims dims;
+    const int32_t *tables;
+    int32_t max_blocks;
+    const int32_t *start_pos;
+    int32_t n_seqs, n_new;
+    int32_t *dev_status;
+};
+
+struct GatherArgs {
+    const void *k_pool, *v_pool;
+    pkv_dims dims;
+    const int32_t *tables;
+    int32_t max_blocks;
+    const int32_t *lens;
+    int32_t n_seqs, out_tokens;
+    void *k_out, *v_out;
+    int32_t *dev_status;
+};
+
+// Decode workspace layout (all offsets 256-byte aligned):
+//   header     : uint32 [64]      work counter, number of splits, capacity
+//   split_base : int32 [n_seqs]   first split index of each sequence
+//   split_list : int2  [cap]      (sequence, split) of every split
+//   part_ml    : float2[cap][Hq]  (running max in log2 units, running sum)
+//   part_acc   : float [cap][Hq][D] unnormalised partial outputs
+struct DecodeWorkspace {
+    uint32_t *header;
+    int32_t *split_base;
+    int2 *split_list;
+    float2 *part_ml;
+    float *part_acc;
+    int32_t capacity;  // splits the workspace can hold
+};
+
+constexpr int kDecodeMinAutoSplit = 128;   // automatic split never goes below this
+constexpr int kDecodeDefaultSplit = 256;
+
+size_t decode_workspace_bytes(int32_t n_seqs, int32_t n_q_heads, int32_t head_dim,
+                              int64_t capacity);
+bool carve_decode_workspace(void *ws, size_t bytes, int32_t n_seqs, int32_t n_q_heads,
+                            int32_t head_dim, DecodeWorkspace *out);
+
+struct DecodeArgs {
+    const void *q;
+    int32_t n_q_heads;
+    const void *k_pool, *v_pool;
+    const float *k_scales, *v_scales;
+    int32_t kv_dtype;
+    pkv_dims dims;
+    const int32_t *tables;
+    int32_t max_blocks;
+    const int32_t *ctx_lens;
+    int32_t n_seqs;
+    float softmax_scale;
+    int32_t split_tokens;
+    void *out;
+    float *lse_out;
+    DecodeWorkspace ws;
+    int32_t *dev_status;
+};
+
+struct PrefillArgs {
+    const void *q;
+    int32_t n_q_heads;
+    const void *k_pool, *v_pool;
+    pkv_dims dims;
+    const int32_t *tables;
+    int32_t max_blocks;
+    const int32_t *prefix_lens;
+    int32_t n_seqs, chunk;
+    float softmax_scale;
+    void *out;
+    float *lse_out;
+    int32_t *dev_status;
+};
+
+cudaError_t launch_write_bf16(const WriteArgs &a, cudaStream_t stream);
+cudaError_t launch_write_int8(const WriteArgs &a, float *k_scales, float *v_scales,
+                              cudaStream_t stream);
+cudaError_t launch_gather(const GatherArgs &a, int num_sms, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeArgs &a, int num_sms, cudaStream_t stream);
+cudaError_t launch_prefill(const PrefillArgs &a, int num_sms, cudaStream_t stream);
+
+// Driver entry point for tensor-map encoding (resolved once through cudart,
+// so the library does not link libcuda directly).  Returns CUDA_SUCCESS or
+// the driver error.
+CUresult encode_tensor_map(CUtensorMap *map, CUtensorMapDataType dtype, uint32_t rank,
+                           void *base, const uint64_t *dims, const uint64_t *strides_bytes,
+                           const uint32_t *box, CUtensorMapSwizzle swizzle);
+
+}  // namespace pkv

@@ -1,0 +1,141 @@
+"""The C ABI boundary on the CPU: the library builds, loads and exports every
+function include/pagedkv.h declares; host-side argument checks return their
+status codes before any CUDA call; workspace sizing is a pure host function.
+No kernel is launched here."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "pagedkv.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from paged_kv_cache_212_gb300 import build as B
+    try:
+        B.nvcc()
+    except RuntimeError:
+        pytest.skip("nvcc not available")
+    B.build()
+    import paged_kv_cache_212_gb300 as P
+    return P.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^[A-Za-z_][\w\s\*]*?\b([a-z_][a-z0-9_]*)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "defined")))
+
+
+def test_header_declares_the_five_calls_and_helpers():
+    names = declared_functions()
+    for n in ("paged_kv_write", "paged_kv_write_int8", "paged_kv_gather", "paged_decode_attention",
+              "paged_prefill_attention", "pkv_decode_workspace_bytes", "pkv_status_string",
+              "pkv_last_cuda_error"):
+        assert n in names, n
+
+
+def test_header_is_plain_c():
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-fsyntax-only", "-x", "c", HEADER],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
+def test_library_exports_every_declared_symbol(lib):
+    from paged_kv_cache_212_gb300 import EXPORTS
+    names = declared_functions()
+    assert set(EXPORTS) == set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", lib._name], capture_output=True, text=True).stdout
+    exported = set(line.split()[-1] for line in out.splitlines() if " T " in line)
+    assert set(names) <= exported
+
+
+def test_status_strings(lib):
+    assert lib.pkv_status_string(0) == b"PKV_OK"
+    assert lib.pkv_status_string(4) == b"PKV_ERR_WORKSPACE"
+    assert lib.pkv_status_string(99) == b"PKV_ERR_UNKNOWN"
+
+
+def _dims(P, nb=8, bs=16, hkv=2, d=64):
+    return P.Dims(nb, bs, hkv, d)
+
+
+FAKE = ctypes.c_void_p(0x1000)      # 16-byte aligned, never dereferenced
+MISALIGNED = ctypes.c_void_p(0x1008)
+
+
+def test_write_argument_checks(lib):
+    import paged_kv_cache_212_gb300 as P
+    d = _dims(P)
+    w = lib.paged_kv_write
+    # no-op sizes return OK without touching anything
+    assert w(None, None, None, None, d, None, 4, None, 0, 1, None, None) == 0
+    assert w(None, None, None, None, d, None, 4, None, 3, 0, None, None) == 0
+    # null pointers / bad sizes
+    assert w(None, FAKE, FAKE, FAKE, d, FAKE, 4, FAKE, 1, 1, None, None) == 1
+    assert w(FAKE, FAKE, FAKE, FAKE, d, FAKE, 0, FAKE, 1, 1, None, None) == 1
+    assert w(FAKE, FAKE, FAKE, FAKE, d, FAKE, 4, FAKE, -1, 1, None, None) == 1
+    assert w(MISALIGNED, FAKE, FAKE, FAKE, d, FAKE, 4, FAKE, 1, 1, None, None) == 1
+    # unsupported geometry
+    assert w(FAKE, FAKE, FAKE, FAKE, _dims(P, d=96), FAKE, 4, FAKE, 1, 1, None, None) == 2
+    assert w(FAKE, FAKE, FAKE, FAKE, _dims(P, bs=8), FAKE, 4, FAKE, 1, 1, None, None) == 2
+    assert w(FAKE, FAKE, FAKE, FAKE, _dims(P, nb=-1), FAKE, 4, FAKE, 1, 1, None, None) == 1
+    # more new tokens than a table row can hold
+    assert w(FAKE, FAKE, FAKE, FAKE, d, FAKE, 2, FAKE, 1, 33, None, None) == 3
+    wi = lib.paged_kv_write_int8
+    assert wi(FAKE, FAKE, FAKE, FAKE, None, FAKE, d, FAKE, 4, FAKE, 1, 1, None, None) == 1
+
+
+def test_decode_argument_checks(lib):
+    import paged_kv_cache_212_gb300 as P
+    d = _dims(P, hkv=2)
+    f = lib.paged_decode_attention
+    args = lambda **kw: [kw.get("q", FAKE), kw.get("hq", 8), FAKE, FAKE, kw.get("ks", None), kw.get("vs", None),
+                         kw.get("dt", 0), kw.get("dims", d), FAKE, 4, FAKE, kw.get("n", 2), 0.125,
+                         kw.get("split", 0), FAKE, None, kw.get("ws", FAKE), kw.get("wsb", 1 << 20), None,
+                         None]
+    assert f(*args(n=0)) == 0
+    assert f(*args(hq=7)) == 1                      # Hq % Hkv != 0
+    assert f(*args(hq=18 * 2)) == 2                 # G = 18 > 8
+    assert f(*args(dt=3)) == 2
+    assert f(*args(split=24)) == 2                  # not a multiple of 16
+    assert f(*args(q=None)) == 1
+    assert f(*args(q=MISALIGNED)) == 1
+    assert f(*args(dt=1, dims=_dims(P, hkv=4))) == 1  # int8 without scales
+    assert f(*args(dt=1, ks=FAKE, vs=FAKE)) == 2   # int8 needs Hkv % 4 == 0
+    assert f(*args(ws=None)) == 4
+    assert f(*args(wsb=64)) == 4
+
+
+def test_prefill_and_gather_argument_checks(lib):
+    import paged_kv_cache_212_gb300 as P
+    d = _dims(P, hkv=2)
+    f = lib.paged_prefill_attention
+    assert f(FAKE, 8, FAKE, FAKE, d, FAKE, 4, FAKE, 0, 16, 0.1, FAKE, None, None, None) == 0
+    assert f(FAKE, 8, FAKE, FAKE, d, FAKE, 4, FAKE, 1, 0, 0.1, FAKE, None, None, None) == 0
+    assert f(FAKE, 6, FAKE, FAKE, d, FAKE, 4, FAKE, 1, 16, 0.1, FAKE, None, None, None) == 2  # G = 3
+    assert f(FAKE, 8, FAKE, FAKE, d, FAKE, 4, FAKE, 1, 65, 0.1, FAKE, None, None, None) == 3
+    assert f(None, 8, FAKE, FAKE, d, FAKE, 4, FAKE, 1, 16, 0.1, FAKE, None, None, None) == 1
+    g = lib.paged_kv_gather
+    assert g(FAKE, FAKE, d, FAKE, 4, FAKE, 0, 16, FAKE, FAKE, None, None) == 0
+    assert g(FAKE, FAKE, d, FAKE, 4, FAKE, 2, 16, None, FAKE, None, None) == 1
+    assert g(FAKE, FAKE, d, FAKE, 4, FAKE, 2, -1, FAKE, FAKE, None, None) == 1
+
+
+def test_decode_workspace_sizing(lib):
+    f = lib.pkv_decode_workspace_bytes
+    assert f(4, 8, 64, 1000, 24) == 0             # split not a multiple of 16
+    assert f(-1, 8, 64, 1000, 0) == 0
+    small = f(64, 32, 128, 150_000, 512)
+    auto = f(64, 32, 128, 150_000, 0)
+    assert 0 < small < auto                       # auto covers the smallest automatic split
+    # capacity grows with the number of splits: ceil(total / split) + n_seqs partial rows
+    per_split = 8 + 32 * 8 + 32 * 128 * 4
+    assert f(64, 32, 128, 150_000 + 512 * 100, 512) - small >= 100 * per_split - 4 * 256

@@ -1,0 +1,394 @@
+"""Parity of the CUDA path (called through the C ABI) with the CPU oracle.
+
+Inputs are the seeded synthetic workloads; every pool the GPU reads is built
+by the ORACLE's own write from the drawn rows (unused memory poisoned with
+NaN / code 127 + NaN scales) and copied to the device, so no oracle input comes
+from the CUDA path.  Bars:
+  * write, int8 write (codes and scales) and gather: bit-exact, whole pools;
+  * attention, bf16 pages: max-abs <= 1e-2 and mean-abs <= 1e-3 against the
+    float64 oracle; int8 pages: max-abs <= 2e-2 against the oracle computed
+    from the same codes and scales; lse within 2e-3 (fp32 accumulation).
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_support import NTHREADS, attention_errors, dev, host, i32
+from oracle_pools import dims_of, empty_pools, oracle_pools_after_step, write_prefix
+from paged_kv_cache_212_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+BF16_MAX, BF16_MEAN, INT8_MAX, LSE_TOL = 1e-2, 1e-3, 2e-2, 2e-3
+
+
+@pytest.fixture(scope="session")
+def P():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from paged_kv_cache_212_gb300 import build
+    build.build()
+    import paged_kv_cache_212_gb300 as P
+    P.load_library()
+    return P
+
+
+_CACHE = {}
+
+
+def workload(name):
+    """Full-size named workloads are drawn once per session."""
+    if name not in _CACHE:
+        makers = {
+            "cfg0": W.config0, "cfg1": W.config1, "cfg2": W.config2, "cfg3": W.config3, "cfg4": W.config4,
+            "cfg2_gather": W.config2_gather,
+            "ragged_d64": lambda: W.decode_workload("ragged", 5, [1, 15, 16, 17, 31, 33, 200, 511], 16, 4, 64, 16),
+            "ragged_g8_bs32": lambda: W.decode_workload("g8", 6, [1, 31, 32, 33, 100, 700, 1500], 64, 8, 128, 32),
+            "ragged_g1": lambda: W.decode_workload("g1", 7, [3, 40, 129], 4, 4, 128, 16),
+            "int8_small": lambda: W.decode_workload("i8", 8, [0, 1, 15, 16, 100, 333], 16, 4, 128, 16, n_new=3,
+                                                    kv_format="int8"),
+            "int8_d64": lambda: W.decode_workload("i8d64", 9, [5, 77, 300], 8, 4, 64, 32, n_new=2,
+                                                  kv_format="int8"),
+            "prefill_small": lambda: W.prefill_workload("p", 10, [0, 5, 16, 100, 250], 40, 8, 2, 64, 16),
+            "prefill_g8": lambda: W.prefill_workload("p8", 11, [0, 33, 300], 37, 64, 8, 128, 16),
+            "prefill_g1": lambda: W.prefill_workload("p1", 12, [7, 64], 70, 4, 4, 128, 32),
+        }
+        _CACHE[name] = makers[name]()
+    return _CACHE[name]
+
+
+_POOLS = {}
+
+
+def pools(name, after_step=True):
+    key = (name, after_step)
+    if key not in _POOLS:
+        w = workload(name)
+        if after_step:
+            _POOLS[key] = oracle_pools_after_step(w, poison=True)
+        else:
+            kp, vp, ks, vs = empty_pools(w, poison=True)
+            write_prefix(w, kp, vp, ks, vs)
+            _POOLS[key] = (kp, vp, ks, vs)
+    return _POOLS[key]
+
+
+def status_tensor():
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+# ---------------------------------------------------------------------------
+# writes and gather: bit-exact
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["cfg0", "cfg1", "cfg3", "cfg4", "ragged_d64"])
+def test_write_bf16_bit_exact(P, name):
+    w = workload(name)
+    kp, vp, _, _ = pools(name, after_step=False)
+    gk, gv = dev(kp), dev(vp)
+    st = status_tensor()
+    P.paged_kv_write(w.k_new.cuda(), w.v_new.cuda(), gk, gv, i32(w.tables), i32(w.start_pos), dev_status=st)
+    torch.cuda.synchronize()
+    rk, rv, _, _ = pools(name, after_step=True)
+    assert int(st.item()) == 0
+    assert np.array_equal(host(gk), rk)
+    assert np.array_equal(host(gv), rv)
+
+
+@pytest.mark.parametrize("name", ["cfg2", "int8_small", "int8_d64"])
+def test_write_int8_bit_exact(P, name):
+    w = workload(name)
+    kp, vp, ks, vs = pools(name, after_step=False)
+    gk, gv, gks, gvs = dev(kp), dev(vp), dev(ks), dev(vs)
+    st = status_tensor()
+    P.paged_kv_write_int8(w.k_new.cuda(), w.v_new.cuda(), gk, gv, gks, gvs, i32(w.tables), i32(w.start_pos),
+                          dev_status=st)
+    torch.cuda.synchronize()
+    rk, rv, rks, rvs = pools(name, after_step=True)
+    assert int(st.item()) == 0
+    assert np.array_equal(host(gk), rk) and np.array_equal(host(gv), rv)
+    # scales compared as bit patterns (NaN poison included)
+    assert np.array_equal(host(gks).view(np.uint32), rks.view(np.uint32))
+    assert np.array_equal(host(gvs).view(np.uint32), rvs.view(np.uint32))
+
+
+def test_write_to_bad_slots_is_flagged_and_skipped(P):
+    w = workload("cfg0")
+    kp, vp, _, _ = pools("cfg0", after_step=False)
+    gk, gv = dev(kp), dev(vp)
+    tables = w.tables.clone()
+    tables[1, int(w.start_pos[1]) // w.block_size] = w.n_blocks + 5      # id out of range
+    start = w.start_pos.clone()
+    start[2] = w.max_blocks * w.block_size                                # past the table
+    st = status_tensor()
+    P.paged_kv_write(w.k_new.cuda(), w.v_new.cuda(), gk, gv, i32(tables), i32(start), dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == (P.DEV_BAD_BLOCK_ID | P.DEV_BAD_POSITION)
+    rk = kp.copy()
+    rv = vp.copy()
+    code = oracle.write_bf16(w.k_new, w.v_new, rk, rv, dims_of(w), tables, start)
+    assert code == oracle.BAD_INDEX
+    assert np.array_equal(host(gk), rk) and np.array_equal(host(gv), rv)
+
+
+@pytest.mark.parametrize("name,extra", [("cfg2_gather", 0), ("cfg0", 13), ("ragged_d64", 1)])
+def test_gather_bit_exact(P, name, extra):
+    w = workload(name)
+    kp, vp, _, _ = pools(name, after_step=w.kind != "gather")
+    lens = w.ctx_lens if w.kind != "gather" else w.stored_lens
+    out_tokens = int(lens.max()) + extra
+    st = status_tensor()
+    ko, vo = P.paged_kv_gather(dev(kp), dev(vp), i32(w.tables), i32(lens), out_tokens, dev_status=st)
+    torch.cuda.synchronize()
+    code, rk, rv = oracle.gather(kp, vp, dims_of(w), w.tables, lens, out_tokens)
+    assert code == oracle.OK and int(st.item()) == 0
+    assert np.array_equal(host(ko), rk) and np.array_equal(host(vo), rv)
+
+
+def test_gather_zero_length_and_bad_length(P):
+    w = workload("cfg0")
+    kp, vp, _, _ = pools("cfg0")
+    lens = torch.tensor([0, 5, 10**6, 65], dtype=torch.int32)
+    st = status_tensor()
+    ko, vo = P.paged_kv_gather(dev(kp), dev(vp), i32(w.tables), i32(lens), 70, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & P.DEV_BAD_LENGTH
+    ok_lens = lens.clone()
+    ok_lens[2] = 0  # the bad sequence's view is zero-filled, like an empty one
+    _, rk, rv = oracle.gather(kp, vp, dims_of(w), w.tables, ok_lens, 70)
+    assert np.array_equal(host(ko), rk) and np.array_equal(host(vo), rv)
+
+
+# ---------------------------------------------------------------------------
+# decode attention
+# ---------------------------------------------------------------------------
+
+def run_decode(P, w, kp, vp, ks=None, vs=None, split=None, tables=None, ctx=None, lse=True):
+    tables = w.tables if tables is None else tables
+    ctx = w.ctx_lens if ctx is None else ctx
+    q = w.q.cuda()
+    lse_t = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda") if lse else None
+    st = status_tensor()
+    out = P.paged_decode_attention(q, dev(kp), dev(vp), i32(tables), i32(ctx), w.softmax_scale,
+                                   k_scales=None if ks is None else dev(ks),
+                                   v_scales=None if vs is None else dev(vs),
+                                   split_tokens=w.split_tokens if split is None else split,
+                                   lse_out=lse_t, max_total_ctx_tokens=int(torch.as_tensor(ctx).sum()),
+                                   dev_status=st)
+    torch.cuda.synchronize()
+    return out, lse_t, int(st.item())
+
+
+def oracle_decode(w, kp, vp, ks=None, vs=None, tables=None, ctx=None):
+    tables = w.tables if tables is None else tables
+    ctx = w.ctx_lens if ctx is None else ctx
+    code, out, lse = oracle.decode(w.q, kp, vp, dims_of(w), tables, ctx, w.softmax_scale, ks, vs,
+                                   n_threads=NTHREADS)
+    assert code == oracle.OK
+    return out, lse
+
+
+def check_lse(lse_gpu, lse_ref):
+    g = lse_gpu.cpu().numpy().astype(np.float64)
+    fin = np.isfinite(lse_ref)
+    assert np.array_equal(np.isneginf(g), np.isneginf(lse_ref))
+    if fin.any():
+        assert np.abs(g[fin] - lse_ref[fin]).max() <= LSE_TOL
+
+
+@pytest.mark.parametrize("name", ["cfg0", "cfg1", "cfg4", "ragged_d64", "ragged_g8_bs32", "ragged_g1"])
+def test_decode_bf16_parity(P, name):
+    w = workload(name)
+    kp, vp, _, _ = pools(name)
+    out, lse, st = run_decode(P, w, kp, vp)
+    ref, ref_lse = oracle_decode(w, kp, vp)
+    assert st == 0
+    mx, mean = attention_errors(out, ref)
+    assert mx <= BF16_MAX and mean <= BF16_MEAN, (mx, mean)
+    check_lse(lse, ref_lse)
+
+
+@pytest.mark.parametrize("name", ["cfg2", "int8_small", "int8_d64"])
+def test_decode_int8_parity(P, name):
+    w = workload(name)
+    kp, vp, ks, vs = pools(name)
+    out, lse, st = run_decode(P, w, kp, vp, ks, vs)
+    ref, ref_lse = oracle_decode(w, kp, vp, ks, vs)
+    assert st == 0
+    mx, _ = attention_errors(out, ref)
+    assert mx <= INT8_MAX, mx
+    check_lse(lse, ref_lse)
+
+
+@pytest.mark.parametrize("split", [16, 48, 128, 512, 4096])
+def test_decode_split_sizes(P, split):
+    w = workload("ragged_g8_bs32")
+    kp, vp, _, _ = pools("ragged_g8_bs32")
+    out, lse, st = run_decode(P, w, kp, vp, split=split)
+    ref, ref_lse = oracle_decode(w, kp, vp)
+    assert st == 0
+    mx, mean = attention_errors(out, ref)
+    assert mx <= BF16_MAX and mean <= BF16_MEAN, (split, mx, mean)
+    check_lse(lse, ref_lse)
+
+
+@pytest.mark.parametrize("name", ["cfg1", "int8_small"])
+def test_decode_identity_vs_permuted_tables_bit_exact(P, name):
+    """Results do not depend on which physical pages the table names."""
+    w = workload(name)
+    kp, vp, ks, vs = pools(name)
+    out, lse, _ = run_decode(P, w, kp, vp, ks, vs)
+    perm = np.random.default_rng(1).permutation(w.n_blocks)
+    move = np.append(perm, w.n_blocks)
+    kp2, vp2 = np.empty_like(kp), np.empty_like(vp)
+    kp2[move], vp2[move] = kp, vp
+    ks2 = vs2 = None
+    if ks is not None:
+        ks2, vs2 = np.empty_like(ks), np.empty_like(vs)
+        ks2[move], vs2[move] = ks, vs
+    t2 = torch.from_numpy(move[w.tables.numpy()]).to(torch.int32)
+    out2, lse2, _ = run_decode(P, w, kp2, vp2, ks2, vs2, tables=t2)
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(lse, lse2)
+
+
+def test_decode_edge_lengths(P):
+    w = workload("ragged_d64")
+    kp, vp, _, _ = pools("ragged_d64")
+    ctx = w.ctx_lens.clone()
+    ctx[0] = 0            # empty context: o = 0, lse = -inf
+    ctx[1] = 1            # a single token: o = v_0
+    ctx[3] = 16           # exactly one block
+    out, lse, st = run_decode(P, w, kp, vp, ctx=ctx)
+    ref, ref_lse = oracle_decode(w, kp, vp, ctx=ctx)
+    assert st == 0
+    assert (out[0] == 0).all() and torch.isneginf(lse[0]).all()
+    mx, mean = attention_errors(out, ref)
+    assert mx <= BF16_MAX and mean <= BF16_MEAN
+    check_lse(lse, ref_lse)
+
+
+def test_decode_bad_table_and_length_are_flagged(P):
+    w = workload("ragged_d64")
+    kp, vp, _, _ = pools("ragged_d64")
+    tables = w.tables.clone()
+    tables[6, 3] = -7
+    ctx = w.ctx_lens.clone()
+    ctx[2] = w.max_blocks * w.block_size + 1
+    out, lse, st = run_decode(P, w, kp, vp, tables=tables, ctx=ctx)
+    assert st & P.DEV_BAD_BLOCK_ID and st & P.DEV_BAD_LENGTH
+    assert (out[2] == 0).all()
+    ref, _ = oracle_decode(w, kp, vp)
+    good = [0, 1, 3, 4, 5, 7]
+    mx, _ = attention_errors(out[good], ref[good])
+    assert mx <= BF16_MAX
+
+
+def test_decode_workspace_overflow_is_flagged(P):
+    w = workload("ragged_d64")
+    kp, vp, _, _ = pools("ragged_d64")
+    q = w.q.cuda()
+    small = P.decode_workspace_bytes(w.n_seqs, w.n_q_heads, w.head_dim, 16, 16)
+    ws = torch.empty(small, dtype=torch.uint8, device="cuda")
+    st = status_tensor()
+    out = P.paged_decode_attention(q, dev(kp), dev(vp), i32(w.tables), i32(w.ctx_lens), w.softmax_scale,
+                                   split_tokens=16, workspace=ws, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & P.DEV_WORKSPACE_OVERFLOW
+    assert (out == 0).all()
+
+
+# ---------------------------------------------------------------------------
+# the decode step as the benchmark runs it: GPU write, then GPU decode
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["cfg1", "cfg2"])
+def test_step_write_then_decode_full_size(P, name):
+    w = workload(name)
+    kp, vp, ks, vs = pools(name, after_step=False)
+    gk, gv = dev(kp), dev(vp)
+    tables, start, ctx = i32(w.tables), i32(w.start_pos), i32(w.ctx_lens)
+    st = status_tensor()
+    if w.kv_format == "int8":
+        gks, gvs = dev(ks), dev(vs)
+        P.paged_kv_write_int8(w.k_new.cuda(), w.v_new.cuda(), gk, gv, gks, gvs, tables, start, dev_status=st)
+    else:
+        gks = gvs = None
+        P.paged_kv_write(w.k_new.cuda(), w.v_new.cuda(), gk, gv, tables, start, dev_status=st)
+    out = P.paged_decode_attention(w.q.cuda(), gk, gv, tables, ctx, w.softmax_scale, k_scales=gks,
+                                   v_scales=gvs, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    rk, rv, rks, rvs = pools(name, after_step=True)
+    ref, _ = oracle_decode(w, rk, rv, rks, rvs)
+    mx, mean = attention_errors(out, ref)
+    if w.kv_format == "int8":
+        assert mx <= INT8_MAX, mx
+    else:
+        assert mx <= BF16_MAX and mean <= BF16_MEAN, (mx, mean)
+
+
+# ---------------------------------------------------------------------------
+# chunked prefill
+# ---------------------------------------------------------------------------
+
+def run_prefill(P, w, kp, vp, tables=None):
+    tables = w.tables if tables is None else tables
+    q = w.q.cuda()
+    lse = torch.empty(q.shape[:3], dtype=torch.float32, device="cuda")
+    st = status_tensor()
+    out = P.paged_prefill_attention(q, dev(kp), dev(vp), i32(tables), i32(w.stored_lens), w.softmax_scale,
+                                    lse_out=lse, dev_status=st)
+    torch.cuda.synchronize()
+    return out, lse, int(st.item())
+
+
+@pytest.mark.parametrize("name", ["prefill_small", "prefill_g8", "prefill_g1"])
+def test_prefill_parity_all_rows(P, name):
+    w = workload(name)
+    kp, vp, _, _ = pools(name)
+    out, lse, st = run_prefill(P, w, kp, vp)
+    code, ref, ref_lse = oracle.prefill(w.q, kp, vp, dims_of(w), w.tables, w.stored_lens, w.softmax_scale,
+                                        n_threads=NTHREADS)
+    assert code == 0 and st == 0
+    mx, mean = attention_errors(out, ref)
+    assert mx <= BF16_MAX and mean <= BF16_MEAN, (mx, mean)
+    assert np.abs(lse.cpu().numpy() - ref_lse).max() <= LSE_TOL
+
+
+def test_prefill_full_size_sampled_rows(P):
+    """Config 3 at full size: the GPU computes every row; the oracle checks a
+    sample of chunk rows (first, last, block boundaries, random) of every
+    sequence and head."""
+    w = workload("cfg3")
+    kp, vp, _, _ = pools("cfg3")
+    out, lse, st = run_prefill(P, w, kp, vp)
+    assert st == 0
+    rng = np.random.default_rng(0)
+    sel = np.zeros((w.n_seqs, w.n_new), bool)
+    for s in range(w.n_seqs):
+        rows = {0, 1, 15, 16, 17, 63, 64, 255, 256, w.n_new - 2, w.n_new - 1}
+        rows |= set(rng.integers(0, w.n_new, 6).tolist())
+        sel[s, sorted(r for r in rows if r < w.n_new)] = True
+    code, ref, ref_lse = oracle.prefill(w.q, kp, vp, dims_of(w), w.tables, w.stored_lens, w.softmax_scale,
+                                        row_select=sel, n_threads=NTHREADS)
+    assert code == 0
+    g = out.cpu().to(torch.float64).numpy()[sel]
+    err = np.abs(g - ref[sel])
+    assert err.max() <= BF16_MAX and err.mean() <= BF16_MEAN, (err.max(), err.mean())
+    assert np.abs(lse.cpu().numpy()[sel] - ref_lse[sel]).max() <= LSE_TOL
+    assert torch.isfinite(out).all()
+
+
+def test_prefill_identity_vs_permuted_tables_bit_exact(P):
+    w = workload("prefill_small")
+    kp, vp, _, _ = pools("prefill_small")
+    out, lse, _ = run_prefill(P, w, kp, vp)
+    perm = np.random.default_rng(2).permutation(w.n_blocks)
+    move = np.append(perm, w.n_blocks)
+    kp2, vp2 = np.empty_like(kp), np.empty_like(vp)
+    kp2[move], vp2[move] = kp, vp
+    t2 = torch.from_numpy(move[w.tables.numpy()]).to(torch.int32)
+    out2, lse2, _ = run_prefill(P, w, kp2, vp2, tables=t2)
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16)) and torch.equal(lse, lse2)
