@@ -1,0 +1,434 @@
+"""Benchmark of the paged KV-cache hot path on GB300.
+
+One step = one decode step of one layer of the Llama-3-8B-shaped workload
+(batch 64, stored lengths U[512, 4096], Hq 32 / Hkv 8 / head_dim 128 /
+block_size 16, pool 1.25x the blocks needed, random block tables): the paged
+write of each sequence's new K/V row, then in-place paged decode attention over
+len + 1 tokens.  Inputs are resident in HBM; the decode reads ~604 MB of K/V
+pages per step, far more than the 129 MB L2, so no flush is needed between
+steps.
+
+  python bench.py [--gpus N --steps K --warmup W] [--config 1] [--impl reference]
+
+Prints one JSON line (rank 0).  Under torchrun every rank runs its own replica
+(independent sequences, no collective in the data path: weak scaling) and the
+time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attention HBM GB/s (% of GB300 peak) and seq-steps/s per layer"
+FALLBACK_HBM_GBS = 6800.0
+
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of decode_split_kernel
+# on the config-1 workload, from the ncu capture summarised in
+# profiles/decode_split_cfg1.txt, valid while the kernel source hashes match.
+NCU_TRAFFIC = {"source_sha": None, "bytes_per_launch": None}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", type=int, default=1, choices=[1, 2, 4])
+    ap.add_argument("--split", type=int, default=0, help="decode split_tokens (0 = library default)")
+    ap.add_argument("--e2e-steps", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_sha():
+    import hashlib
+    h = hashlib.sha256()
+    for name in ("decode.cu", "common.cuh", "launch.h"):
+        with open(os.path.join(ROOT, "paged_kv_cache_212_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def make_workload(cfg, device):
+    from paged_kv_cache_212_gb300 import workloads as W
+    if cfg == 1:
+        w = W.config1(device=device)
+    elif cfg == 2:
+        w = W.config2(device=device)
+    else:
+        w = W.config4(device=device)
+    return w
+
+
+def algorithmic_bytes(w):
+    """Bytes the step must move at minimum: K/V of every attended token (int8:
+    codes + fp32 scales), Q and O, the table entries and lengths read; plus the
+    write's new rows in and out (int8: codes + scales out)."""
+    ctx = w.ctx_lens.long()
+    hkv, d, bs = w.n_kv_heads, w.head_dim, w.block_size
+    tokens = int(ctx.sum())
+    if w.kv_format == "int8":
+        kv = tokens * 2 * hkv * (d + 4)
+    else:
+        kv = tokens * 2 * hkv * d * 2
+    qo = 2 * w.n_seqs * w.n_q_heads * d * 2
+    tab = int(((ctx + bs - 1) // bs).sum()) * 4 + w.n_seqs * 4
+    decode = kv + qo + tab
+    rows = w.n_seqs * w.n_new * hkv
+    if w.kv_format == "int8":
+        write = 2 * rows * d * 2 + 2 * rows * (d + 4) + w.n_seqs * 8
+    else:
+        write = 2 * 2 * rows * d * 2 + w.n_seqs * 8
+    return decode, write
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 100 ms while running."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.uuid = uuid
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            cmd = ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100"]
+            if self.uuid:
+                cmd += ["-i", self.uuid]
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in (self.out or "").splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def fill_pool(P, w, device):
+    """Untimed set-up: allocate the pools and place the resident prefix with
+    the library's own write (int8 pages through the quantised write)."""
+    import torch
+    nb1 = w.n_blocks + 1
+    if w.kv_format == "int8":
+        kp = torch.zeros(w.pool_shape, dtype=torch.int8, device=device)
+        vp = torch.zeros(w.pool_shape, dtype=torch.int8, device=device)
+        ks = torch.zeros(w.scale_shape, dtype=torch.float32, device=device)
+        vs = torch.zeros(w.scale_shape, dtype=torch.float32, device=device)
+    else:
+        kp = torch.zeros(w.pool_shape, dtype=torch.bfloat16, device=device)
+        vp = torch.zeros(w.pool_shape, dtype=torch.bfloat16, device=device)
+        ks = vs = None
+    tables = w.tables.to(device)
+    for seg in w.prefix:
+        t = tables[seg.seq:seg.seq + 1]
+        sp = torch.tensor([seg.start], dtype=torch.int32, device=device)
+        if ks is not None:
+            P.paged_kv_write_int8(seg.k[None].contiguous(), seg.v[None].contiguous(), kp, vp, ks, vs, t, sp)
+        else:
+            P.paged_kv_write(seg.k[None].contiguous(), seg.v[None].contiguous(), kp, vp, t, sp)
+    torch.cuda.synchronize()
+    del nb1
+    return kp, vp, ks, vs
+
+
+def cpu_baseline(cfg, budget_s=12.0, threads=None):
+    """The float64 oracle, as it stands, on the host cores: write + decode of
+    the same workload's sequences, repeated until ~budget_s of wall time."""
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import numpy as np
+    import oracle
+    from oracle_pools import dims_of, empty_pools, write_prefix
+    w = make_workload(cfg, "cpu")
+    threads = threads or (os.cpu_count() or 1)
+    kp, vp, ks, vs = empty_pools(w, poison=False)
+    write_prefix(w, kp, vp, ks, vs)
+    decode_b, write_b = algorithmic_bytes(w)
+    d = dims_of(w)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        if w.kv_format == "int8":
+            oracle.write_int8(w.k_new, w.v_new, kp, vp, ks, vs, d, w.tables, w.start_pos)
+        else:
+            oracle.write_bf16(w.k_new, w.v_new, kp, vp, d, w.tables, w.start_pos)
+        oracle.decode(w.q, kp, vp, d, w.tables, w.ctx_lens, w.softmax_scale, ks, vs, n_threads=threads)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    gbs = reps * (decode_b + write_b) / el / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"{reps} full steps (write + float64 decode of all {w.n_seqs} sequences) in {el:.1f} s",
+            "seq_steps_per_s": round(reps * w.n_seqs / el, 2)}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the float64 oracle on the host cores, same metric and
+    workload; each step is a bounded sample (the first n sequences)."""
+    if rank != 0:
+        return
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import oracle
+    import torch
+    from oracle_pools import dims_of, empty_pools, write_prefix
+    w = make_workload(args.config, "cpu")
+    threads = os.cpu_count() or 1
+    kp, vp, ks, vs = empty_pools(w, poison=False)
+    write_prefix(w, kp, vp, ks, vs)
+    d = dims_of(w)
+
+    def step(n):
+        sl = slice(0, n)
+        if w.kv_format == "int8":
+            oracle.write_int8(w.k_new[sl], w.v_new[sl], kp, vp, ks, vs, d, w.tables[sl], w.start_pos[sl])
+        else:
+            oracle.write_bf16(w.k_new[sl], w.v_new[sl], kp, vp, d, w.tables[sl], w.start_pos[sl])
+        oracle.decode(w.q[sl], kp, vp, d, w.tables[sl], w.ctx_lens[sl], w.softmax_scale, ks, vs,
+                      n_threads=threads)
+
+    t0 = time.perf_counter()
+    step(w.n_seqs)
+    t_full = time.perf_counter() - t0
+    budget = 150.0 / max(1, args.steps + args.warmup)
+    n = max(1, min(w.n_seqs, int(w.n_seqs * budget / max(t_full, 1e-9))))
+    for _ in range(args.warmup):
+        step(n)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step(n)
+    el = time.perf_counter() - t0
+    sub = make_sub_bytes(w, n)
+    gbs = args.steps * sub / el / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": bench_config(w, args),
+            "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": f"each step: write + float64 decode of the first {n} of {w.n_seqs} "
+                                       "sequences"},
+            "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def make_sub_bytes(w, n):
+    import copy
+    sub = copy.copy(w)
+    sub.n_seqs = n
+    sub.stored_lens = w.stored_lens[:n]
+    sub.tables = w.tables[:n]
+    dec, wr = algorithmic_bytes(sub)
+    return dec + wr
+
+
+def bench_config(w, args):
+    ctx = w.ctx_lens
+    return {"workload": w.name, "n_seqs": w.n_seqs, "ctx_min": int(ctx.min()), "ctx_max": int(ctx.max()),
+            "ctx_total": int(ctx.sum()), "n_q_heads": w.n_q_heads, "n_kv_heads": w.n_kv_heads,
+            "head_dim": w.head_dim, "block_size": w.block_size, "kv_pages": w.kv_format,
+            "n_blocks": w.n_blocks, "layers_timed": 1, "split_tokens": args.split or "library default",
+            "l2": "inputs larger than L2 (K/V pages read per step far exceed the 129 MB L2); no flush"}
+
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+
+    import torch
+    import torch.distributed as dist
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+    from paged_kv_cache_212_gb300 import build as B
+    B.build()
+    import paged_kv_cache_212_gb300 as P
+    P.load_library()
+
+    w = make_workload(args.config, device)  # every rank owns an independent replica batch
+    kp, vp, ks, vs = fill_pool(P, w, device)
+    tables = w.tables.to(device)
+    start = w.start_pos.to(device)
+    ctx = w.ctx_lens.to(device)
+    k_new, v_new, q = w.k_new.to(device), w.v_new.to(device), w.q.to(device)
+    out = torch.empty_like(q)
+    split = args.split or w.split_tokens
+    ws_bytes = P.decode_workspace_bytes(w.n_seqs, w.n_q_heads, w.head_dim, int(w.ctx_lens.sum()), split)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream()
+    int8 = w.kv_format == "int8"
+
+    def write():
+        if int8:
+            P.paged_kv_write_int8(k_new, v_new, kp, vp, ks, vs, tables, start, dev_status=status)
+        else:
+            P.paged_kv_write(k_new, v_new, kp, vp, tables, start, dev_status=status)
+
+    def decode():
+        P.paged_decode_attention(q, kp, vp, tables, ctx, w.softmax_scale, k_scales=ks, v_scales=vs,
+                                 split_tokens=split, out=out, workspace=ws, dev_status=status)
+
+    for _ in range(max(3, args.warmup)):
+        write()
+        decode()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+
+    # ---- timed region: K steps, events around every decode call ----
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        pass
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(uuid) as clk:
+        time.sleep(0.25)  # let the sampler start before the timed work
+        t_start.record(stream)
+        for i in range(K):
+            write()
+            ev[i][0].record(stream)
+            decode()
+            ev[i][1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    decode_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    if world > 1:
+        tt = torch.tensor([elapsed_ms, decode_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms, decode_ms = float(tt[0]), float(tt[1])
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    ms_per_step = elapsed_ms / K
+
+    # ---- end to end through the public API with pinned host buffers ----
+    e2e_steps = args.e2e_steps or max(10, min(K, 2000))
+    h_k, h_v, h_q = (x.cpu().pin_memory() for x in (w.k_new, w.v_new, w.q))
+    h_tab, h_start, h_ctx = (x.cpu().pin_memory() for x in (w.tables, w.start_pos, w.ctx_lens))
+    h_out = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in (h_k, h_v, h_q, h_tab, h_start, h_ctx))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        k_new.copy_(h_k, non_blocking=True)
+        v_new.copy_(h_v, non_blocking=True)
+        q.copy_(h_q, non_blocking=True)
+        tables.copy_(h_tab, non_blocking=True)
+        start.copy_(h_start, non_blocking=True)
+        ctx.copy_(h_ctx, non_blocking=True)
+        write()
+        decode()
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        tt = torch.tensor([e2e_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        e2e_ms = float(tt[0])
+
+    decode_b, write_b = algorithmic_bytes(w)
+    step_b = decode_b + write_b
+    peak, peak_kind = measured_peaks()
+    value = world * step_b / (ms_per_step * 1e-3) / 1e9
+    achieved = decode_b / (decode_ms * 1e-3) / 1e9
+    traffic = NCU_TRAFFIC["bytes_per_launch"] if NCU_TRAFFIC["source_sha"] == kernel_source_sha() else None
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8" if int8 else "bf16", "data": "synthetic",
+        "config": bench_config(w, args),
+        "pct_of_peak": round(100 * value / world / peak, 2),
+        "seq_steps_per_s_per_layer": round(world * w.n_seqs / (ms_per_step * 1e-3), 1),
+        "seq_steps_per_s_decode_only": round(world * w.n_seqs / (decode_ms * 1e-3), 1),
+        "ms_per_32_layer_step": round(32 * ms_per_step, 4),
+        "roofline": {"bound": "hbm", "kernel": "paged_decode_attention (plan + split + merge launches)",
+                     "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes_per_launch": decode_b, "avg_launch_ms": round(decode_ms, 5),
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                     else "fallback 6.8 TB/s"},
+        "e2e": {"value": round(world * step_b / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5),
+                "steps": e2e_steps},
+        "gpu_launches": 4 * K,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.config)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
