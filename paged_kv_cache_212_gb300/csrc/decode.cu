@@ -2,7 +2,7 @@
 // log-sum-exp merge, for bf16 pages and for int8 pages with fp32 per-(token,
 // kv head) scales.
 //
-// Three launches on the caller's stream, no host synchronisation:
+// Two launches on the caller's stream, no host synchronisation:
 //   1. decode_plan_kernel (one CTA): cuts every sequence's context into
 //      logical ranges of split_tokens tokens (metrale high_speed_swap
 //      impl_more.rs, attend_layer_on_stream_with_q_pos: tiles of resident
@@ -18,9 +18,10 @@
 //      an online softmax (running max and sum in log2 units).  A sequence with
 //      one split writes its output directly; otherwise the item writes its
 //      partial (m, l, acc) to the workspace.
-//   3. decode_merge_kernel: for multi-split sequences, o = sum_k 2^(m_k - M)
-//      acc_k / sum_k 2^(m_k - M) l_k (the finalize step of the tiled
-//      attention), and lse = ln 2 (M + log2 L).
+//      The consumer warp that finishes the last split of a (sequence, kv head)
+//      -- an atomic counter per pair in the workspace -- merges the partials:
+//      o = sum_k 2^(m_k - M) acc_k / sum_k 2^(m_k - M) l_k (the finalize step
+//      of the tiled attention) and lse = ln 2 (M + log2 L).
 //
 // Pool tiles in shared memory: for each stage and each 64-element half of
 // head_dim, a [heads][16 tokens][128 bytes] box with the TMA 128-byte swizzle
@@ -47,7 +48,8 @@ struct StageMeta {
     int32_t n_valid;      // valid tokens in this stage (1..16)
     int32_t flags;
     int32_t head_group;   // which group of hpc kv heads the item covers
-    int32_t pad[3];
+    int32_t n_splits;     // splits of this sequence
+    int32_t pad[2];
 };
 
 struct DecodeParams {
@@ -132,8 +134,10 @@ __device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t chunk)
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t *__restrict__ ctx_lens,
                                                            int32_t n_seqs, int32_t split_tokens,
-                                                           int32_t max_tokens, DecodeWorkspace ws,
-                                                           int32_t *dev_status)
+                                                           int32_t max_tokens, int32_t n_q_heads,
+                                                           int32_t head_dim, int32_t n_kv_heads,
+                                                           DecodeWorkspace ws, __nv_bfloat16 *out,
+                                                           float *lse_out, int32_t *dev_status)
 {
     __shared__ int32_t warp_sums[32];
     __shared__ int32_t running_s;
@@ -179,14 +183,84 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t *__rest
         if (tid == (int)blockDim.x - 1) running_s = base + n;
         __syncthreads();
     }
+    const int32_t total = running_s;
+    const bool overflow = total > ws.capacity;
     if (tid == 0) {
-        const int32_t total = running_s;
-        const bool overflow = total > ws.capacity;
         if (overflow) report(dev_status, PKV_DEV_WORKSPACE_OVERFLOW);
         ws.header[kHdrTotal] = overflow ? 0u : (uint32_t)total;
         ws.header[kHdrOverflow] = overflow ? 1u : 0u;
         ws.header[kHdrCounter] = 0u;
     }
+    for (int64_t i = tid; i < (int64_t)n_seqs * n_kv_heads; i += blockDim.x) ws.done[i] = 0;
+    // Sequences no split will cover (empty or invalid context, or every
+    // sequence when the work list overflowed) get o = 0 and lse = -inf here.
+    for (int32_t s = 0; s < n_seqs; ++s) {
+        const int32_t ctx = ctx_lens[s];
+        if (!overflow && ctx > 0 && ctx <= max_tokens) continue;
+        const int64_t row = (int64_t)s * n_q_heads;
+        for (int32_t i = tid; i < n_q_heads * head_dim; i += blockDim.x)
+            out[row * head_dim + i] = __float2bfloat16_rn(0.f);
+        if (lse_out)
+            for (int32_t i = tid; i < n_q_heads; i += blockDim.x) lse_out[row + i] = -INFINITY;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// split merge, run by the one warp that finished a (sequence, kv head) last
+// ---------------------------------------------------------------------------
+// The G query heads are merged side by side: 32 / G lanes per head, each lane
+// owning D * G / 32 consecutive elements of its head's output, so all partial
+// loads of all heads are in flight together.  Partials are read with
+// ld.global.cg (L2): other SMs wrote them.
+template <int D>
+__device__ __noinline__ void merge_splits(const float2 *part_ml, const float *part_acc, __nv_bfloat16 *out,
+                                          float *lse_out, int32_t n_q_heads, int32_t s, int32_t hbase, int G,
+                                          int32_t base, int32_t n_splits, int lane)
+{
+    const int lph = 32 / G;                 // lanes per head
+    const int n = lane / lph, sub = lane % lph;
+    const int epl = D / lph;                // elements per lane: 4 .. 32
+    const int64_t hrow = hbase + n;
+    // running max over the splits, in lane groups
+    float M = -INFINITY;
+    for (int32_t k = sub; k < n_splits; k += lph)
+        M = fmaxf(M, __ldcg(&part_ml[(int64_t)(base + k) * n_q_heads + hrow]).x);
+    for (int off = 1; off < lph; off <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float o[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) o[e] = 0.f;
+    float Lsum = 0.f;
+    for (int32_t k = 0; k < n_splits; ++k) {
+        const int64_t row = (int64_t)(base + k) * n_q_heads + hrow;
+        const float2 ml = __ldcg(&part_ml[row]);
+        const float w = M == -INFINITY ? 0.f : exp2f(ml.x - M);
+        Lsum += ml.y * w;
+        const float4 *src = reinterpret_cast<const float4 *>(part_acc + row * D + sub * epl);
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+            if (v * 4 < epl) {
+                const float4 a = __ldcg(src + v);
+                o[4 * v + 0] += a.x * w;
+                o[4 * v + 1] += a.y * w;
+                o[4 * v + 2] += a.z * w;
+                o[4 * v + 3] += a.w * w;
+            }
+        }
+    }
+    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+    __nv_bfloat16 *dst = out + ((int64_t)s * n_q_heads + hrow) * D + sub * epl;
+#pragma unroll
+    for (int v = 0; v < 8; ++v) {
+        if (v * 4 < epl) {
+            uint2 pk;
+            pk.x = pack_bf16x2(o[4 * v] * inv, o[4 * v + 1] * inv);
+            pk.y = pack_bf16x2(o[4 * v + 2] * inv, o[4 * v + 3] * inv);
+            *reinterpret_cast<uint2 *>(dst + 4 * v) = pk;
+        }
+    }
+    if (lse_out && sub == 0)
+        lse_out[(int64_t)s * n_q_heads + hrow] =
+            Lsum > 0.f ? (M + __log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
 }
 
 // ---------------------------------------------------------------------------
@@ -287,6 +361,7 @@ __global__ void __launch_bounds__(288, 1) decode_split_kernel(const __grid_const
                         m.flags = (t == t0 ? kMetaFirst : 0) | (t + kStageTokens >= t1 ? kMetaLast : 0) |
                                   (final_out ? kMetaFinal : 0);
                         m.head_group = hg;
+                        m.n_splits = (ctx + p.split_tokens - 1) / p.split_tokens;
                         const bool bad = blk < 0 || blk > p.n_blocks;
                         if (bad) {
                             m.flags |= kMetaBad;
@@ -553,6 +628,11 @@ __global__ void __launch_bounds__(288, 1) decode_split_kernel(const __grid_const
             if (INT8) __syncwarp();  // scratch is rewritten by the next stage
         }
 
+        // the stage's tiles are no longer needed: hand the slot back before finalising
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&L.empty_bar[st]);
+        ++stage_it;
+
         if (meta.flags & kMetaLast) {
             float L0 = l0, L1 = l1;
 #pragma unroll
@@ -561,8 +641,9 @@ __global__ void __launch_bounds__(288, 1) decode_split_kernel(const __grid_const
                 L1 += __shfl_xor_sync(0xffffffffu, L1, off);
             }
             const int32_t s = meta.seq;
+            const int32_t kvh = meta.head_group * hpc + warp;
             // first query head of this warp's group: columns 2qd, 2qd+1 are hbase + n0, n1
-            const int32_t hbase = (meta.head_group * hpc + warp) * G;
+            const int32_t hbase = kvh * G;
             const int n0 = 2 * qd, n1 = 2 * qd + 1;
             if (meta.flags & kMetaFinal) {
                 const float inv0 = 1.f / L0, inv1 = 1.f / L1;
@@ -603,84 +684,27 @@ __global__ void __launch_bounds__(288, 1) decode_split_kernel(const __grid_const
                     if (n0 < G) p.ws.part_ml[prow + n0] = make_float2(m0, L0);
                     if (n1 < G) p.ws.part_ml[prow + n1] = make_float2(m1, L1);
                 }
+                // publish the partial; the warp that completes the last split of
+                // this (sequence, kv head) merges them all
+                __threadfence();
+                __syncwarp();
+                int32_t last = 0;
+                if (lane == 0) last = atomicAdd(&p.ws.done[(int64_t)s * p.n_kv_heads + kvh], 1) == meta.n_splits - 1;
+                last = __shfl_sync(0xffffffffu, last, 0);
+                if (last) {
+                    __threadfence();
+                    merge_splits<D>(p.ws.part_ml, p.ws.part_acc, p.out, p.lse_out, p.n_q_heads, s, hbase, G,
+                                    __ldcg(&p.ws.split_base[s]), meta.n_splits, lane);
+                }
             }
             ++item_it;
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&L.empty_bar[st]);
-        ++stage_it;
     }
 }
 
 }  // namespace pkv
 
 namespace pkv {
-
-// ---------------------------------------------------------------------------
-// 3. merge of split partials
-// ---------------------------------------------------------------------------
-// One warp per (sequence, query head).  Sequences with exactly one split were
-// finished by the split kernel; an empty (or invalid) context gives o = 0,
-// lse = -inf.
-template <int D>
-__global__ void __launch_bounds__(128) decode_merge_kernel(
-    const int32_t *__restrict__ ctx_lens, int32_t n_seqs, int32_t n_q_heads, int32_t split_tokens,
-    int32_t max_tokens, DecodeWorkspace ws, __nv_bfloat16 *__restrict__ out, float *lse_out)
-{
-    constexpr int EPL = D / 32;
-    const int lane = threadIdx.x & 31;
-    const int64_t idx = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (idx >= (int64_t)n_seqs * n_q_heads) return;
-    const int32_t s = (int32_t)(idx / n_q_heads);
-    const int32_t ctx = __ldg(ctx_lens + s);
-    const int32_t n = (ctx > 0 && ctx <= max_tokens) ? (ctx + split_tokens - 1) / split_tokens : 0;
-    const bool overflow = ws.header[kHdrOverflow] != 0;
-    if (n == 1 && !overflow) return;
-    float o[EPL];
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) o[e] = 0.f;
-    float lse = -INFINITY;
-    if (n > 1 && !overflow) {
-        const int64_t base = ws.split_base[s];
-        float M = -INFINITY;
-        for (int32_t k = 0; k < n; ++k) M = fmaxf(M, ws.part_ml[(base + k) * n_q_heads + idx % n_q_heads].x);
-        if (M != -INFINITY) {
-            float Lsum = 0.f;
-            for (int32_t k = 0; k < n; ++k) {
-                const int64_t row = (base + k) * n_q_heads + idx % n_q_heads;
-                const float2 ml = ws.part_ml[row];
-                const float w = exp2f(ml.x - M);
-                Lsum += ml.y * w;
-                const float *pa = ws.part_acc + row * D + lane * EPL;
-                if constexpr (EPL == 4) {
-                    const float4 a = *reinterpret_cast<const float4 *>(pa);
-                    o[0] += a.x * w;
-                    o[1] += a.y * w;
-                    o[2] += a.z * w;
-                    o[3] += a.w * w;
-                } else {
-                    const float2 a = *reinterpret_cast<const float2 *>(pa);
-                    o[0] += a.x * w;
-                    o[1] += a.y * w;
-                }
-            }
-            const float inv = 1.f / Lsum;
-#pragma unroll
-            for (int e = 0; e < EPL; ++e) o[e] *= inv;
-            lse = (M + log2f(Lsum)) * 0.69314718055994531f;
-        }
-    }
-    __nv_bfloat16 *dst = out + idx * D + lane * EPL;
-    if constexpr (EPL == 4) {
-        uint2 v;
-        v.x = pack_bf16x2(o[0], o[1]);
-        v.y = pack_bf16x2(o[2], o[3]);
-        *reinterpret_cast<uint2 *>(dst) = v;
-    } else {
-        *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(o[0], o[1]);
-    }
-    if (lse_out && lane == 0) lse_out[idx] = lse;
-}
 
 // ---------------------------------------------------------------------------
 // host side
@@ -692,6 +716,7 @@ size_t decode_workspace_bytes(int32_t n_seqs, int32_t n_q_heads, int32_t head_di
 {
     size_t b = 256;                                          // header
     b += align_up((size_t)n_seqs * sizeof(int32_t), 256);    // split_base
+    b += align_up((size_t)n_seqs * n_q_heads * sizeof(int32_t), 256);  // done counters
     b += align_up((size_t)capacity * sizeof(int2), 256);     // split_list
     b += align_up((size_t)capacity * n_q_heads * sizeof(float2), 256);
     b += align_up((size_t)capacity * n_q_heads * head_dim * sizeof(float), 256);
@@ -702,7 +727,8 @@ bool carve_decode_workspace(void *ws, size_t bytes, int32_t n_seqs, int32_t n_q_
                             int32_t head_dim, DecodeWorkspace *out)
 {
     if (!ws) return false;
-    const size_t fixed = 256 + align_up((size_t)n_seqs * sizeof(int32_t), 256) + 3 * 256;
+    const size_t fixed = 256 + align_up((size_t)n_seqs * sizeof(int32_t), 256) +
+                         align_up((size_t)n_seqs * n_q_heads * sizeof(int32_t), 256) + 3 * 256;
     if (bytes < fixed) return false;
     const size_t per = sizeof(int2) + (size_t)n_q_heads * sizeof(float2) +
                        (size_t)n_q_heads * head_dim * sizeof(float);
@@ -714,6 +740,8 @@ bool carve_decode_workspace(void *ws, size_t bytes, int32_t n_seqs, int32_t n_q_
     p += 256;
     out->split_base = reinterpret_cast<int32_t *>(p);
     p += align_up((size_t)n_seqs * sizeof(int32_t), 256);
+    out->done = reinterpret_cast<int32_t *>(p);
+    p += align_up((size_t)n_seqs * n_q_heads * sizeof(int32_t), 256);
     out->split_list = reinterpret_cast<int2 *>(p);
     p += align_up((size_t)cap * sizeof(int2), 256);
     out->part_ml = reinterpret_cast<float2 *>(p);
@@ -839,15 +867,11 @@ cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream)
     const size_t smem = fixed + (size_t)stages * p.stage_bytes;
 
     auto kern = decode_split_kernel<D, INT8>;
-    static size_t configured = 0;
-    if (configured < smem) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        configured = smem;
-    }
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
     const int threads = 32 * (hpc + 1);
     int occ = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
     if (e != cudaSuccess) return e;
     if (occ < 1) return cudaErrorInvalidConfiguration;
     const int grid = num_sms * (occ < ctas_per_sm ? occ : ctas_per_sm);
@@ -860,25 +884,15 @@ cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream)
 cudaError_t launch_decode(const DecodeArgs &a, int num_sms, cudaStream_t stream)
 {
     const int32_t max_tokens = a.max_blocks * a.dims.block_size;
-    decode_plan_kernel<<<1, 1024, 0, stream>>>(a.ctx_lens, a.n_seqs, a.split_tokens, max_tokens, a.ws,
-                                               a.dev_status);
+    decode_plan_kernel<<<1, 1024, 0, stream>>>(a.ctx_lens, a.n_seqs, a.split_tokens, max_tokens, a.n_q_heads,
+                                               a.dims.head_dim, a.dims.n_kv_heads, a.ws,
+                                               (__nv_bfloat16 *)a.out, a.lse_out, a.dev_status);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const bool int8 = a.kv_dtype == PKV_KV_INT8;
     if (a.dims.head_dim == 128)
-        e = int8 ? launch_split<128, true>(a, num_sms, stream) : launch_split<128, false>(a, num_sms, stream);
-    else
-        e = int8 ? launch_split<64, true>(a, num_sms, stream) : launch_split<64, false>(a, num_sms, stream);
-    if (e != cudaSuccess) return e;
-    const int64_t warps = (int64_t)a.n_seqs * a.n_q_heads;
-    const unsigned grid = (unsigned)((warps + 3) / 4);
-    if (a.dims.head_dim == 128)
-        decode_merge_kernel<128><<<grid, 128, 0, stream>>>(a.ctx_lens, a.n_seqs, a.n_q_heads, a.split_tokens,
-                                                           max_tokens, a.ws, (__nv_bfloat16 *)a.out, a.lse_out);
-    else
-        decode_merge_kernel<64><<<grid, 128, 0, stream>>>(a.ctx_lens, a.n_seqs, a.n_q_heads, a.split_tokens,
-                                                          max_tokens, a.ws, (__nv_bfloat16 *)a.out, a.lse_out);
-    return cudaGetLastError();
+        return int8 ? launch_split<128, true>(a, num_sms, stream) : launch_split<128, false>(a, num_sms, stream);
+    return int8 ? launch_split<64, true>(a, num_sms, stream) : launch_split<64, false>(a, num_sms, stream);
 }
 
 }  // namespace pkv

@@ -33,14 +33,16 @@ struct GatherArgs {
 };
 
 // Decode workspace layout (all offsets 256-byte aligned):
-//   header     : uint32 [64]      work counter, number of splits, capacity
+//   header     : uint32 [64]      work counter, number of splits, overflow flag
 //   split_base : int32 [n_seqs]   first split index of each sequence
+//   done       : int32 [n_seqs][Hq] finished-split counters per (sequence, kv head)
 //   split_list : int2  [cap]      (sequence, split) of every split
 //   part_ml    : float2[cap][Hq]  (running max in log2 units, running sum)
 //   part_acc   : float [cap][Hq][D] unnormalised partial outputs
 struct DecodeWorkspace {
     uint32_t *header;
     int32_t *split_base;
+    int32_t *done;
     int2 *split_list;
     float2 *part_ml;
     float *part_acc;
