@@ -197,6 +197,41 @@ int paged_prefill_attention(const pkv_bf16 *q, int32_t n_q_heads, const pkv_bf16
                             int32_t chunk, float softmax_scale, pkv_bf16 *out, float *lse_out,
                             int32_t *dev_status, pkv_stream_t stream);
 
+/*
+ * paged_decode_attention_noalloc -- paged_decode_attention for callers that
+ * cannot allocate device memory.  The pages have no counterpart: this entry
+ * point exists only for callers such as a plugin whose host framework owns all
+ * device memory, or a runtime with a fixed memory budget, which may not call
+ * cudaMalloc (or anything that allocates) to obtain a decode workspace.
+ *
+ * Arguments and results are those of paged_decode_attention, except that no
+ * workspace is passed: the split-KV scratch is a static device array of
+ * PKV_NOALLOC_DECODE_SCRATCH_BYTES (16 MiB) inside the library, which every
+ * GPU that loads the library holds until the process exits.  The call
+ * allocates nothing and frees nothing.
+ *   max_total_ctx_tokens  an upper bound on sum_s ctx_lens[s]; when the
+ *       scratch this needs (pkv_decode_workspace_bytes(n_seqs, n_q_heads,
+ *       head_dim, max_total_ctx_tokens, split_tokens)) exceeds the static
+ *       array, the call returns PKV_ERR_WORKSPACE and enqueues nothing.
+ * The first call on a device looks up the array's device address (one
+ * cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  All calls share the one array and it keeps the
+ * last call's contents (nothing in it needs to start at zero: each call
+ * rewrites what it reads).  Calls whose work overlaps on the GPU -- on
+ * different streams, or from different threads without ordering -- race on
+ * the scratch and give wrong results; order them on one stream.
+ */
+#define PKV_NOALLOC_DECODE_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+int paged_decode_attention_noalloc(const pkv_bf16 *q, int32_t n_q_heads, const void *k_pool,
+                                   const void *v_pool, const float *k_scales,
+                                   const float *v_scales, int32_t kv_dtype, pkv_dims dims,
+                                   const int32_t *block_tables, int32_t max_blocks,
+                                   const int32_t *ctx_lens, int32_t n_seqs, float softmax_scale,
+                                   int32_t split_tokens, int64_t max_total_ctx_tokens,
+                                   pkv_bf16 *out, float *lse_out, int32_t *dev_status,
+                                   pkv_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -24,7 +24,8 @@ DEV_WORKSPACE_OVERFLOW, DEV_TIMEOUT = 8, 16
 
 EXPORTS = ("pkv_status_string", "pkv_last_cuda_error", "paged_kv_write", "paged_kv_write_int8",
            "paged_kv_gather", "pkv_decode_workspace_bytes", "paged_decode_attention",
-           "paged_prefill_attention")
+           "paged_prefill_attention", "paged_decode_attention_noalloc")
+NOALLOC_DECODE_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
 class PagedKVError(RuntimeError):
@@ -67,8 +68,10 @@ def load_library(path: str = LIB_PATH):
                                            i32, P, P, P, sz, P, P]
     lib.paged_prefill_attention.argtypes = [P, i32, P, P, Dims, P, i32, P, i32, i32, ctypes.c_float, P, P,
                                             P, P]
+    lib.paged_decode_attention_noalloc.argtypes = [P, i32, P, P, P, P, i32, Dims, P, i32, P, i32,
+                                                   ctypes.c_float, i32, i64, P, P, P, P]
     for fn in ("paged_kv_write", "paged_kv_write_int8", "paged_kv_gather", "paged_decode_attention",
-               "paged_prefill_attention"):
+               "paged_prefill_attention", "paged_decode_attention_noalloc"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -218,6 +221,40 @@ def paged_decode_attention(q, k_pool, v_pool, block_tables, ctx_lens, softmax_sc
                                     float(softmax_scale), int(split_tokens), _ptr(out), _ptr(lse_out),
                                     _ptr(workspace), workspace.numel(), _ptr(dev_status), _stream(stream))
     _check("paged_decode_attention", st)
+    return out
+
+
+def paged_decode_attention_noalloc(q, k_pool, v_pool, block_tables, ctx_lens, softmax_scale,
+                                   max_total_ctx_tokens, out, k_scales=None, v_scales=None, split_tokens=0,
+                                   lse_out=None, dev_status=None, stream=None):
+    """paged_decode_attention for callers that cannot allocate device memory:
+    the split-KV scratch is the library's own static 16 MiB device array, so
+    no workspace is passed and the call allocates nothing (``out`` must be
+    given).  max_total_ctx_tokens bounds sum(ctx_lens); a request whose
+    scratch would not fit raises (PKV_ERR_WORKSPACE).  Calls share the one
+    array: do not let two of them overlap on the GPU."""
+    lib = load_library()
+    dev = q.device
+    _need(q, "q", torch.bfloat16, 3, dev)
+    int8 = k_pool.dtype == torch.int8
+    _need(k_pool, "k_pool", torch.int8 if int8 else torch.bfloat16, 4, dev)
+    _need(v_pool, "v_pool", torch.int8 if int8 else torch.bfloat16, 4, dev)
+    if int8:
+        _need(k_scales, "k_scales", torch.float32, 3, dev)
+        _need(v_scales, "v_scales", torch.float32, 3, dev)
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(ctx_lens, "ctx_lens", torch.int32, 1, dev)
+    _need(out, "out", torch.bfloat16, 3, dev)
+    if lse_out is not None:
+        _need(lse_out, "lse_out", torch.float32, 2, dev)
+    n_seqs, n_q_heads, _ = q.shape
+    st = lib.paged_decode_attention_noalloc(_ptr(q), n_q_heads, _ptr(k_pool), _ptr(v_pool), _ptr(k_scales),
+                                            _ptr(v_scales), PKV_KV_INT8 if int8 else PKV_KV_BF16,
+                                            pool_dims(k_pool), _ptr(block_tables), block_tables.shape[1],
+                                            _ptr(ctx_lens), n_seqs, float(softmax_scale), int(split_tokens),
+                                            int(max_total_ctx_tokens), _ptr(out), _ptr(lse_out),
+                                            _ptr(dev_status), _stream(stream))
+    _check("paged_decode_attention_noalloc", st)
     return out
 
 

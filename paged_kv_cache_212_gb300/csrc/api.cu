@@ -81,6 +81,8 @@ size_t decode_capacity_for(int32_t n_seqs, int64_t max_total_ctx_tokens, int32_t
 
 }  // namespace
 
+void record_cuda_error(int e) { g_last_cuda_error = e; }
+
 CUresult encode_tensor_map(CUtensorMap *map, CUtensorMapDataType dtype, uint32_t rank, void *base,
                            const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box,
                            CUtensorMapSwizzle swizzle)
