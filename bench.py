@@ -43,21 +43,21 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", type=int, default=1, choices=[1, 2, 4])
+    ap.add_argument("--config", type=int, default=1, choices=[1, 2, 3, 4])
     ap.add_argument("--split", type=int, default=0, help="decode split_tokens (0 = library default)")
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
 
-def measured_peaks():
+def measured_peaks(key="hbm_gbs"):
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
+        return float(d[key]), "measured"
     except Exception:
-        return FALLBACK_HBM_GBS, "fallback"
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": 1900.0}[key], "fallback"
 
 
 def kernel_source_sha():
@@ -73,6 +73,8 @@ def make_workload(cfg, device):
     from paged_kv_cache_212_gb300 import workloads as W
     if cfg == 1:
         w = W.config1(device=device)
+    elif cfg == 3:
+        w = W.config3(device=device)
     elif cfg == 2:
         w = W.config2(device=device)
     else:
@@ -276,6 +278,71 @@ def bench_config(w, args):
             "l2": "inputs larger than L2 (K/V pages read per step far exceed the 129 MB L2); no flush"}
 
 
+def prefill_flops(w):
+    """4 * Hq * D * sum over queries of the keys each attends (Q K^T and P V)."""
+    import torch
+    P = w.stored_lens.long()
+    keys = int((P[:, None] + torch.arange(w.n_new)[None, :] + 1).sum())
+    return 4 * w.n_q_heads * w.head_dim * keys
+
+
+def run_prefill_bench(args, P, w, device, rank, world):
+    """Config 3: paged write of each sequence's 512-token chunk, then chunked
+    paged prefill attention over prefix + chunk (tensor-core bound)."""
+    import torch
+    import torch.distributed as dist
+    kp, vp, _, _ = fill_pool(P, w, device)
+    tables, start = w.tables.to(device), w.start_pos.to(device)
+    k_new, v_new, q = w.k_new.to(device), w.v_new.to(device), w.q.to(device)
+    out = torch.empty_like(q)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        P.paged_kv_write(k_new, v_new, kp, vp, tables, start, dev_status=status)
+        if ev is not None:
+            ev[0].record(stream)
+        P.paged_prefill_attention(q, kp, vp, tables, start, w.softmax_scale, out=out, dev_status=status)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(uuid) as clk:
+        time.sleep(0.25)
+        t0.record(stream)
+        for i in range(K):
+            step(ev[i])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / K
+    pre_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    flops = prefill_flops(w)
+    peak, kind = measured_peaks("bf16_tflops")
+    ach = flops / (pre_ms * 1e-3) / 1e12
+    line = {"metric": "chunked paged prefill attention TFLOP/s (config 3)", "value": round(world * flops / (ms * 1e-3) / 1e12, 2),
+            "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "n_seqs": w.n_seqs, "chunk": w.n_new,
+                       "prefix": [int(x) for x in w.stored_lens], "impl": os.environ.get("PKV_PREFILL_IMPL", "tcgen05")},
+            "roofline": {"bound": "tensor", "kernel": "paged_prefill_attention", "achieved": round(ach, 2),
+                         "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4), "traffic": None,
+                         "flops_per_launch": flops, "avg_launch_ms": round(pre_ms, 5),
+                         "peak_source": f"{kind} bf16_tflops (burst)"},
+            "gpu_launches": 2 * K, "clocks": clk.summary()}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     rank = int(os.environ.get("RANK", "0"))
@@ -297,6 +364,11 @@ def main():
     P.load_library()
 
     w = make_workload(args.config, device)  # every rank owns an independent replica batch
+    if args.config == 3:
+        run_prefill_bench(args, P, w, device, rank, world)
+        if world > 1:
+            dist.destroy_process_group()
+        return
     kp, vp, ks, vs = fill_pool(P, w, device)
     tables = w.tables.to(device)
     start = w.start_pos.to(device)

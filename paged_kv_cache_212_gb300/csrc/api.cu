@@ -9,6 +9,7 @@
 namespace pkv {
 
 cudaError_t launch_prefill_mma(const PrefillArgs &a, cudaStream_t stream);
+cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream);
 
 namespace {
 
@@ -96,10 +97,16 @@ CUresult encode_tensor_map(CUtensorMap *map, CUtensorMapDataType dtype, uint32_t
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+// Prefill runs on the tcgen05 kernel; PKV_PREFILL_IMPL=mma selects the
+// warp-level mma.sync kernel instead (kept for comparison and for group sizes
+// the tcgen05 tiling does not take).
 cudaError_t launch_prefill(const PrefillArgs &a, int num_sms, cudaStream_t stream)
 {
     (void)num_sms;
-    return launch_prefill_mma(a, stream);
+    const char *impl = getenv("PKV_PREFILL_IMPL");
+    const int G = a.n_q_heads / a.dims.n_kv_heads;
+    if ((impl && impl[0] == 'm') || G > 16 || 128 % G != 0) return launch_prefill_mma(a, stream);
+    return launch_prefill_tc(a, stream);
 }
 
 }  // namespace pkv
