@@ -482,7 +482,7 @@ def main():
         "seq_steps_per_s_per_layer": round(world * w.n_seqs / (ms_per_step * 1e-3), 1),
         "seq_steps_per_s_decode_only": round(world * w.n_seqs / (decode_ms * 1e-3), 1),
         "ms_per_32_layer_step": round(32 * ms_per_step, 4),
-        "roofline": {"bound": "hbm", "kernel": "paged_decode_attention (plan + split launches)",
+        "roofline": {"bound": "hbm", "kernel": "paged_decode_attention (plan + split + merge launches)",
                      "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "algorithmic_bytes_per_launch": decode_b, "avg_launch_ms": round(decode_ms, 5),
@@ -491,7 +491,7 @@ def main():
         "e2e": {"value": round(world * step_b / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5),
                 "steps": e2e_steps},
-        "gpu_launches": 3 * K,
+        "gpu_launches": 4 * K,
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

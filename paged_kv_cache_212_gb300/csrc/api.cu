@@ -74,10 +74,13 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
+// Partial slots a call needs: fixed splits give one per split of every
+// sequence; balanced pieces give at most one per sequence plus one per item.
 size_t decode_capacity_for(int32_t n_seqs, int64_t max_total_ctx_tokens, int32_t split_tokens)
 {
-    const int64_t split = split_tokens > 0 ? split_tokens : kDecodeMinAutoSplit;
-    return (size_t)((max_total_ctx_tokens + split - 1) / split + n_seqs);
+    if (split_tokens > 0) return (size_t)((max_total_ctx_tokens + split_tokens - 1) / split_tokens + n_seqs);
+    const int64_t stages = (max_total_ctx_tokens + 15) / 16 + 1;
+    return (size_t)(n_seqs + (stages < kDecodeAutoMaxItems ? stages : kDecodeAutoMaxItems));
 }
 
 }  // namespace
@@ -244,7 +247,7 @@ int paged_decode_attention(const pkv_bf16 *q, int32_t n_q_heads, const void *k_p
     a.ctx_lens = ctx_lens;
     a.n_seqs = n_seqs;
     a.softmax_scale = softmax_scale;
-    a.split_tokens = split_tokens > 0 ? split_tokens : kDecodeDefaultSplit;
+    a.split_tokens = split_tokens;
     a.out = out;
     a.lse_out = lse_out;
     a.dev_status = dev_status;

@@ -71,6 +71,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
     return done != 0;
 }
 
+// Non-blocking test of the phase with the given parity.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
 // Waits for the phase with the given parity to complete.  Returns false when
 // the wait ran out of time or another warp of the CTA raised *abort (the
 // caller then reports PKV_DEV_TIMEOUT and winds down).
@@ -87,6 +101,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
         }
     }
 }
+
+// ---- programmatic dependent launch -------------------------------------------
+
+// Lets the next kernel on the stream (launched as a programmatic dependent)
+// start; it still waits for this grid in grid_dependency_wait().
+__device__ __forceinline__ void grid_dependents_launch()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Waits until the preceding grid has completed and its writes are visible
+// (returns at once when the kernel was not launched as a dependent).
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ---- TMA ------------------------------------------------------------------
 

@@ -2,26 +2,32 @@
 // log-sum-exp merge, for bf16 pages and for int8 pages with fp32 per-(token,
 // kv head) scales.
 //
-// Two launches on the caller's stream, no host synchronisation:
-//   1. decode_plan_kernel (one CTA): cuts every sequence's context into
-//      logical ranges of split_tokens tokens (metrale high_speed_swap
-//      impl_more.rs, attend_layer_on_stream_with_q_pos: tiles of resident
-//      blocks), writes the (sequence, split) work list into the workspace and
-//      resets the work counter.
+// Three launches on the caller's stream, no host synchronisation:
+//   1. decode_plan_kernel (one CTA) cuts the work into items.  With
+//      split_tokens > 0 an item is one logical range [k S, (k+1) S) of one
+//      sequence (metrale high_speed_swap impl_more.rs,
+//      attend_layer_on_stream_with_q_pos: tiles of resident blocks).  With
+//      split_tokens == 0 the concatenated 16-token stages of all sequences are
+//      cut into equal contiguous ranges, about one per CTA, so every CTA gets
+//      the same amount of work; a range may cover the end of one sequence and
+//      the start of the next.  Each (sequence, item) piece owns one partial
+//      slot.  The plan also resets the work counter and the merge counters.
 //   2. decode_split_kernel (persistent, one or two CTAs per SM): a producer
-//      warp takes (split, kv-head group) items from the counter and streams the
+//      warp takes (item, kv-head group) units from the counter and streams the
 //      item's pages, 16 tokens per stage, into a shared-memory ring with TMA
 //      (cp.async.bulk.tensor, 128-byte swizzle), addressed through the block
 //      table.  One consumer warp per kv head contracts the stage with its GQA
 //      query group on the tensor cores (mma.sync m16n8k16: S^T = K Q^T with the
 //      16 tokens as M and the query heads as N, then O^T += V^T P^T) and keeps
-//      an online softmax (running max and sum in log2 units).  A sequence with
-//      one split writes its output directly; otherwise the item writes its
+//      an online softmax (running max and sum in log2 units).  A sequence in
+//      one piece writes its output directly; otherwise each piece writes its
 //      partial (m, l, acc) to the workspace.
-//      The consumer warp that finishes the last split of a (sequence, kv head)
-//      -- an atomic counter per pair in the workspace -- merges the partials:
+//   3. decode_merge_kernel, for sequences in two or more pieces:
 //      o = sum_k 2^(m_k - M) acc_k / sum_k 2^(m_k - M) l_k (the finalize step
 //      of the tiled attention) and lse = ln 2 (M + log2 L).
+// The split and merge kernels are programmatic dependent launches: each
+// starts while its predecessor drains and waits (griddepcontrol.wait) before
+// reading the predecessor's results.
 //
 // Pool tiles in shared memory: for each stage and each 64-element half of
 // head_dim, a [heads][16 tokens][128 bytes] box with the TMA 128-byte swizzle
@@ -38,17 +44,18 @@ namespace {
 
 constexpr int kStageTokens = 16;
 constexpr int kMaxStages = 8;
-constexpr uint32_t kHdrCounter = 0, kHdrTotal = 1, kHdrOverflow = 2;
+constexpr uint32_t kHdrCounter = 0, kHdrTotal = 1, kHdrOverflow = 2, kHdrChunk = 3, kHdrStages = 4;
+constexpr int32_t kMinChunkStages = 4;   // balanced items hold at least 64 tokens
 
 enum : int32_t { kMetaFirst = 1, kMetaLast = 2, kMetaBad = 4, kMetaStop = 8, kMetaFinal = 16 };
 
 struct StageMeta {
     int32_t seq;
-    int32_t split_index;  // index into the workspace split list
+    int32_t split_index;  // the piece's partial slot
     int32_t n_valid;      // valid tokens in this stage (1..16)
     int32_t flags;
     int32_t head_group;   // which group of hpc kv heads the item covers
-    int32_t n_splits;     // splits of this sequence
+    int32_t n_splits;     // pieces of this sequence
     int32_t pad[2];
 };
 
@@ -61,7 +68,7 @@ struct DecodeParams {
     const int32_t *ctx_lens;
     int32_t n_seqs;
     float scale_log2;
-    int32_t split_tokens;
+    int32_t split_tokens;         // 0: balanced pieces
     __nv_bfloat16 *out;
     float *lse_out;
     DecodeWorkspace ws;
@@ -132,18 +139,53 @@ __device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t chunk)
 // ---------------------------------------------------------------------------
 // 1. plan
 // ---------------------------------------------------------------------------
+
+// Exclusive prefix sum of v over the CTA (blockDim.x a multiple of 32);
+// *total receives the CTA-wide sum.  scratch: 33 ints of shared memory.
+__device__ int32_t block_exclusive_scan(int32_t v, int32_t *total, int32_t *scratch)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int32_t incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int32_t u = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += u;
+    }
+    if (lane == 31) scratch[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const int32_t x = lane < (int)(blockDim.x >> 5) ? scratch[lane] : 0;
+        int32_t xi = x;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const int32_t u = __shfl_up_sync(0xffffffffu, xi, off);
+            if (lane >= off) xi += u;
+        }
+        scratch[lane] = xi - x;
+        if (lane == 31) scratch[32] = xi;
+    }
+    __syncthreads();
+    const int32_t r = scratch[warp] + incl - v;
+    *total = scratch[32];
+    __syncthreads();
+    return r;
+}
+
 __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t *__restrict__ ctx_lens,
                                                            int32_t n_seqs, int32_t split_tokens,
                                                            int32_t max_tokens, int32_t n_q_heads,
                                                            int32_t head_dim, int32_t n_kv_heads,
-                                                           DecodeWorkspace ws, __nv_bfloat16 *out,
-                                                           float *lse_out, int32_t *dev_status)
+                                                           int32_t items_target, DecodeWorkspace ws,
+                                                           __nv_bfloat16 *out, float *lse_out,
+                                                           int32_t *dev_status)
 {
-    __shared__ int32_t warp_sums[32];
-    __shared__ int32_t running_s;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (tid == 0) running_s = 0;
-    __syncthreads();
+    __shared__ int32_t scratch[33];
+    grid_dependents_launch();   // the split kernel may start; it waits for this grid's results
+    const int tid = threadIdx.x;
+    const bool balanced = split_tokens == 0;
+    const int32_t unit = balanced ? kStageTokens : split_tokens;
+    // pass 1: units (16-token stages, or fixed splits) per sequence and their prefix
+    int32_t running = 0;
     for (int32_t c0 = 0; c0 < n_seqs; c0 += blockDim.x) {
         const int32_t s = c0 + tid;
         int32_t n = 0;
@@ -152,47 +194,69 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t *__rest
             if (ctx < 0 || ctx > max_tokens)
                 report(dev_status, PKV_DEV_BAD_LENGTH);
             else
-                n = (ctx + split_tokens - 1) / split_tokens;
+                n = (ctx + unit - 1) / unit;
         }
-        int32_t incl = n;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            int32_t v = __shfl_up_sync(0xffffffffu, incl, off);
-            if (lane >= off) incl += v;
-        }
-        if (lane == 31) warp_sums[warp] = incl;
-        __syncthreads();
-        if (warp == 0) {
-            int32_t v = lane < (int)(blockDim.x >> 5) ? warp_sums[lane] : 0;
-            int32_t vi = v;
-#pragma unroll
-            for (int off = 1; off < 32; off <<= 1) {
-                int32_t u = __shfl_up_sync(0xffffffffu, vi, off);
-                if (lane >= off) vi += u;
-            }
-            warp_sums[lane] = vi - v;  // exclusive prefix of warp totals
-        }
-        __syncthreads();
-        const int32_t base = running_s + warp_sums[warp] + incl - n;
+        int32_t tot;
+        const int32_t ex = running + block_exclusive_scan(n, &tot, scratch);
         if (s < n_seqs) {
-            ws.split_base[s] = base;
-            for (int32_t k = 0; k < n; ++k)
-                if (base + k < ws.capacity) ws.split_list[base + k] = make_int2(s, k);
+            if (balanced) {
+                ws.seq_prefix[s] = ex;
+            } else {
+                ws.seg_base[s] = ex;
+                ws.n_seg[s] = n;
+                for (int32_t k = 0; k < n; ++k)
+                    if (ex + k < ws.capacity) ws.items[ex + k] = make_int2(s, k);
+            }
         }
-        __syncthreads();
-        if (tid == (int)blockDim.x - 1) running_s = base + n;
-        __syncthreads();
+        running += tot;
     }
-    const int32_t total = running_s;
-    const bool overflow = total > ws.capacity;
+    int32_t n_items = 0, chunk = 0;
+    bool overflow = false;
+    if (!balanced) {
+        n_items = running;
+        overflow = running > ws.capacity;
+    } else {
+        const int32_t total = running;
+        if (tid == 0) ws.seq_prefix[n_seqs] = total;
+        const int32_t room = ws.capacity - n_seqs;   // items the partial slots allow
+        overflow = room < 1 && total > 0;
+        if (total > 0 && !overflow) {
+            const int32_t want = max(1, min(items_target, room));
+            chunk = max(kMinChunkStages, (total + want - 1) / want);
+            n_items = (total + chunk - 1) / chunk;
+        }
+        // pass 2: pieces per sequence, their slots, and the first sequence of every item
+        running = 0;
+        for (int32_t c0 = 0; c0 < n_seqs; c0 += blockDim.x) {
+            const int32_t s = c0 + tid;
+            int32_t n = 0, pre = 0, st = 0;
+            if (s < n_seqs && chunk > 0) {
+                pre = ws.seq_prefix[s];
+                const int32_t ctx = ctx_lens[s];
+                st = (ctx < 0 || ctx > max_tokens) ? 0 : (ctx + kStageTokens - 1) / kStageTokens;
+                if (st > 0) n = (pre + st - 1) / chunk - pre / chunk + 1;
+            }
+            int32_t tot;
+            const int32_t ex = running + block_exclusive_scan(n, &tot, scratch);
+            if (s < n_seqs) {
+                ws.seg_base[s] = ex;
+                ws.n_seg[s] = n;
+                // items whose first stage lies in this sequence start with it
+                for (int32_t i = (pre + chunk - 1) / max(chunk, 1); st > 0 && i * chunk < pre + st; ++i)
+                    ws.items[i] = make_int2(s, 0);
+            }
+            running += tot;
+        }
+    }
     if (tid == 0) {
         if (overflow) report(dev_status, PKV_DEV_WORKSPACE_OVERFLOW);
-        ws.header[kHdrTotal] = overflow ? 0u : (uint32_t)total;
+        ws.header[kHdrTotal] = overflow ? 0u : (uint32_t)n_items;
         ws.header[kHdrOverflow] = overflow ? 1u : 0u;
+        ws.header[kHdrChunk] = (uint32_t)chunk;
+        ws.header[kHdrStages] = balanced && !overflow ? (uint32_t)ws.seq_prefix[n_seqs] : 0u;
         ws.header[kHdrCounter] = 0u;
     }
-    for (int64_t i = tid; i < (int64_t)n_seqs * n_kv_heads; i += blockDim.x) ws.done[i] = 0;
-    // Sequences no split will cover (empty or invalid context, or every
+    // Sequences no piece will cover (empty or invalid context, or every
     // sequence when the work list overflowed) get o = 0 and lse = -inf here.
     for (int32_t s = 0; s < n_seqs; ++s) {
         const int32_t ctx = ctx_lens[s];
@@ -206,61 +270,131 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t *__rest
 }
 
 // ---------------------------------------------------------------------------
-// split merge, run by the one warp that finished a (sequence, kv head) last
+// 3. merge of the pieces of a sequence
 // ---------------------------------------------------------------------------
 // The G query heads are merged side by side: 32 / G lanes per head, each lane
-// owning D * G / 32 consecutive elements of its head's output, so all partial
-// loads of all heads are in flight together.  Partials are read with
-// ld.global.cg (L2): other SMs wrote them.
-template <int D>
-__device__ __noinline__ void merge_splits(const float2 *part_ml, const float *part_acc, __nv_bfloat16 *out,
-                                          float *lse_out, int32_t n_q_heads, int32_t s, int32_t hbase, int G,
-                                          int32_t base, int32_t n_splits, int lane)
+// owning EPL = D * G / 32 consecutive elements of its head's output.  The
+// partials of a batch of pieces are all loaded before any is used, so a merge
+// costs about two L2 round trips.  Partials are read with ld.global.cg (L2):
+// other SMs wrote them.
+template <int D, int EPL>
+__device__ __forceinline__ void merge_pieces(const float2 *part_ml, const float *part_acc, __nv_bfloat16 *out,
+                                          float *lse_out, int32_t n_q_heads, int32_t s, int32_t hbase,
+                                          int32_t base, int32_t n_pieces, int lane)
 {
-    const int lph = 32 / G;                 // lanes per head
-    const int n = lane / lph, sub = lane % lph;
-    const int epl = D / lph;                // elements per lane: 4 .. 32
+    constexpr int LPH = D / EPL;                     // lanes per head
+    constexpr int VEC = EPL >= 4 ? 4 : 2;            // floats per load
+    constexpr int NV = EPL / VEC;                    // loads per piece and lane
+    constexpr int BATCH = EPL >= 32 ? 2 : (EPL >= 16 ? 4 : 8);
+    const int n = lane / LPH, sub = lane % LPH;
     const int64_t hrow = hbase + n;
-    // running max over the splits, in lane groups
     float M = -INFINITY;
-    for (int32_t k = sub; k < n_splits; k += lph)
+    for (int32_t k = sub; k < n_pieces; k += LPH)
         M = fmaxf(M, __ldcg(&part_ml[(int64_t)(base + k) * n_q_heads + hrow]).x);
-    for (int off = 1; off < lph; off <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    float o[32];
 #pragma unroll
-    for (int e = 0; e < 32; ++e) o[e] = 0.f;
+    for (int off = 1; off < LPH; off <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float o[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) o[e] = 0.f;
     float Lsum = 0.f;
-    for (int32_t k = 0; k < n_splits; ++k) {
-        const int64_t row = (int64_t)(base + k) * n_q_heads + hrow;
-        const float2 ml = __ldcg(&part_ml[row]);
-        const float w = M == -INFINITY ? 0.f : exp2f(ml.x - M);
-        Lsum += ml.y * w;
-        const float4 *src = reinterpret_cast<const float4 *>(part_acc + row * D + sub * epl);
+    for (int32_t k0 = 0; k0 < n_pieces; k0 += BATCH) {
+        float2 ml[BATCH];
+        float a[BATCH][EPL];
 #pragma unroll
-        for (int v = 0; v < 8; ++v) {
-            if (v * 4 < epl) {
-                const float4 a = __ldcg(src + v);
-                o[4 * v + 0] += a.x * w;
-                o[4 * v + 1] += a.y * w;
-                o[4 * v + 2] += a.z * w;
-                o[4 * v + 3] += a.w * w;
+        for (int i = 0; i < BATCH; ++i) {
+            if (k0 + i < n_pieces) {
+                const int64_t row = (int64_t)(base + k0 + i) * n_q_heads + hrow;
+                ml[i] = __ldcg(&part_ml[row]);
+                const float *src = part_acc + row * D + sub * EPL;
+#pragma unroll
+                for (int v = 0; v < NV; ++v) {
+                    if constexpr (VEC == 4) {
+                        const float4 x = __ldcg(reinterpret_cast<const float4 *>(src) + v);
+                        a[i][4 * v] = x.x;
+                        a[i][4 * v + 1] = x.y;
+                        a[i][4 * v + 2] = x.z;
+                        a[i][4 * v + 3] = x.w;
+                    } else {
+                        const float2 x = __ldcg(reinterpret_cast<const float2 *>(src) + v);
+                        a[i][2 * v] = x.x;
+                        a[i][2 * v + 1] = x.y;
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < BATCH; ++i) {
+            if (k0 + i < n_pieces) {
+                const float w = M == -INFINITY ? 0.f : exp2f(ml[i].x - M);
+                Lsum += ml[i].y * w;
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) o[e] += a[i][e] * w;
             }
         }
     }
     const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-    __nv_bfloat16 *dst = out + ((int64_t)s * n_q_heads + hrow) * D + sub * epl;
+    __nv_bfloat16 *dst = out + ((int64_t)s * n_q_heads + hrow) * D + sub * EPL;
 #pragma unroll
-    for (int v = 0; v < 8; ++v) {
-        if (v * 4 < epl) {
-            uint2 pk;
-            pk.x = pack_bf16x2(o[4 * v] * inv, o[4 * v + 1] * inv);
-            pk.y = pack_bf16x2(o[4 * v + 2] * inv, o[4 * v + 3] * inv);
-            *reinterpret_cast<uint2 *>(dst + 4 * v) = pk;
-        }
-    }
+    for (int e = 0; e < EPL; e += 2) *reinterpret_cast<uint32_t *>(dst + e) = pack_bf16x2(o[e] * inv, o[e + 1] * inv);
     if (lse_out && sub == 0)
-        lse_out[(int64_t)s * n_q_heads + hrow] =
-            Lsum > 0.f ? (M + __log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
+        lse_out[(int64_t)s * n_q_heads + hrow] = Lsum > 0.f ? (M + __log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
+}
+
+// One warp per (sequence, kv head) of every sequence cut into two or more
+// pieces; EPL = D * G / 32.  Launched after the split kernel as a programmatic
+// dependent: it waits for the split kernel's results before reading them.
+template <int D, int EPL>
+__global__ void __launch_bounds__(128) decode_merge_kernel(DecodeWorkspace ws, int32_t n_seqs, int32_t n_kv_heads,
+                                                           int32_t n_q_heads, int32_t group, __nv_bfloat16 *out,
+                                                           float *lse_out)
+{
+    grid_dependency_wait();
+    const int lane = threadIdx.x & 31;
+    const int64_t idx = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (idx >= (int64_t)n_seqs * n_kv_heads) return;
+    const int32_t s = (int32_t)(idx / n_kv_heads), kvh = (int32_t)(idx % n_kv_heads);
+    const int32_t n = ws.n_seg[s];
+    if (n < 2 || ws.header[kHdrOverflow] != 0) return;
+    merge_pieces<D, EPL>(ws.part_ml, ws.part_acc, out, lse_out, n_q_heads, s, kvh * group, ws.seg_base[s], n, lane);
+}
+
+// TMA copies of one 16-token stage (K and V tiles of hpc kv heads, int8 scales)
+template <int D, bool INT8>
+__device__ __forceinline__ void issue_stage_loads(uint8_t *stg, const DecodeParams &p, const CUtensorMap &k_map,
+                                                  const CUtensorMap &v_map, const CUtensorMap &ks_map,
+                                                  const CUtensorMap &vs_map, int32_t row0, int32_t head0,
+                                                  uint64_t *bar)
+{
+    constexpr int HALVES = D / 64;
+    if (!INT8) {
+        const uint32_t half_bytes = (uint32_t)p.hpc * kStageTokens * 128u;
+        for (int h = 0; h < HALVES; ++h) {
+            for (int b = 0; b < p.boxes_per_half; ++b) {
+                const uint32_t off = h * half_bytes + b * (kStageTokens * 128u);
+                if (p.boxes_per_half == 1) {
+                    tma_load_3d(stg + off, &k_map, h * 64, row0, head0, bar);
+                    tma_load_3d(stg + p.kv_tile_bytes + off, &v_map, h * 64, row0, head0, bar);
+                } else {
+                    tma_load_3d(stg + off, &k_map, h * 64, head0 + b, row0, bar);
+                    tma_load_3d(stg + p.kv_tile_bytes + off, &v_map, h * 64, head0 + b, row0, bar);
+                }
+            }
+        }
+    } else {
+        for (int b = 0; b < p.boxes_per_half; ++b) {
+            const uint32_t off = b * (kStageTokens * (uint32_t)D);
+            if (p.boxes_per_half == 1) {
+                tma_load_3d(stg + off, &k_map, 0, row0, head0, bar);
+                tma_load_3d(stg + p.kv_tile_bytes + off, &v_map, 0, row0, head0, bar);
+            } else {
+                tma_load_3d(stg + off, &k_map, 0, head0 + b, row0, bar);
+                tma_load_3d(stg + p.kv_tile_bytes + off, &v_map, 0, head0 + b, row0, bar);
+            }
+        }
+        uint8_t *sc = stg + 2 * p.kv_tile_bytes;
+        tma_load_2d(sc, &ks_map, head0, row0, bar);
+        tma_load_2d(sc + p.scale_tile_bytes, &vs_map, head0, row0, bar);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -293,6 +427,8 @@ __global__ void __launch_bounds__(288, 1) decode_split_kernel(const __grid_const
         fence_mbar_init();
     }
     __syncthreads();
+    grid_dependents_launch();
+    grid_dependency_wait();     // the plan kernel's work list is complete and visible
 
     const uint32_t total_items = p.ws.header[kHdrTotal] * (uint32_t)p.n_hg;
     volatile int32_t *abort_flag = L.abort_flag;
@@ -312,109 +448,115 @@ __global__ void __launch_bounds__(288, 1) decode_split_kernel(const __grid_const
         if (lane == 0) next = atomicAdd(&p.ws.header[kHdrCounter], 1u);
         next = __shfl_sync(0xffffffffu, next, 0);
         bool ok = true;
+        const bool balanced = p.split_tokens == 0;
+        const int32_t chunk = (int32_t)p.ws.header[kHdrChunk];
+        const int32_t total_stages = (int32_t)p.ws.header[kHdrStages];
         while (ok && next < total_items) {
             const uint32_t it = next;
             if (lane == 0) next = atomicAdd(&p.ws.header[kHdrCounter], 1u);
-            const int32_t sp = (int32_t)(it / p.n_hg), hg = (int32_t)(it % p.n_hg);
-            const int2 sk = p.ws.split_list[sp];
-            const int32_t s = sk.x;
-            const int32_t ctx = __ldg(p.ctx_lens + s);
-            const int32_t t0 = sk.y * p.split_tokens;
-            const int32_t t1 = min(t0 + p.split_tokens, ctx);
-            const bool final_out = ctx <= p.split_tokens;
-            const int32_t *trow = p.tables + (int64_t)s * p.max_blocks;
-            const int32_t blk0 = t0 / p.block_size;
-            // this item's queries: heads [hg*hpc*G, (hg+1)*hpc*G) of sequence s
-            const uint32_t qs = item_it & 1u;
-            if (lane == 0) {
-                if (!mbar_wait(&L.qempty_bar[qs], ((item_it >> 1) & 1u) ^ 1u, abort_flag)) {
-                    report(p.dev_status, PKV_DEV_TIMEOUT);
-                    *abort_flag = 1;
-                }
-                if (!*abort_flag) {
-                    mbar_arrive_expect_tx(&L.qfull_bar[qs], p.q_slot_bytes);
-                    bulk_g2s(L.q_slots + qs * p.q_slot_bytes,
-                             p.q + ((int64_t)s * p.n_q_heads + (int64_t)hg * hpc * p.group) * D,
-                             p.q_slot_bytes, &L.qfull_bar[qs]);
-                }
+            const int32_t item = (int32_t)(it / p.n_hg), hg = (int32_t)(it % p.n_hg);
+            // balanced: the item is the stage range [g0, g1) of the concatenated sequences
+            int32_t g0 = 0, g1 = 0, s = 0;
+            int2 fixed_sk = make_int2(0, 0);
+            if (balanced) {
+                g0 = item * chunk;
+                g1 = min(g0 + chunk, total_stages);
+                s = __ldg(&p.ws.items[item].x);
+            } else {
+                fixed_sk = __ldg(&p.ws.items[item]);
             }
-            ok = !__shfl_sync(0xffffffffu, *abort_flag, 0);
-            int32_t tbl = 0, tbl_base = -1;
-            for (int32_t t = t0; ok && t < t1; t += kStageTokens) {
-                const int32_t lb = t / p.block_size;
-                if (lb - blk0 >= tbl_base + 32 || tbl_base < 0) {
-                    tbl_base = lb - blk0;
-                    const int32_t j = blk0 + tbl_base + lane;
-                    tbl = j < p.max_blocks ? __ldg(trow + j) : -1;
+            bool more = true;
+            while (ok && more) {
+                // the next piece: sequence, token range, partial slot, pieces of that sequence
+                int32_t seq, t0, t1, slot, n_pieces;
+                if (balanced) {
+                    int32_t pre = __ldg(p.ws.seq_prefix + s), pre1 = __ldg(p.ws.seq_prefix + s + 1);
+                    while (pre1 == pre) {  // sequences without tokens
+                        ++s;
+                        pre = pre1;
+                        pre1 = __ldg(p.ws.seq_prefix + s + 1);
+                    }
+                    const int32_t e = min(g1, pre1);
+                    seq = s;
+                    t0 = (g0 - pre) * kStageTokens;
+                    t1 = min((e - pre) * kStageTokens, __ldg(p.ctx_lens + s));
+                    slot = __ldg(p.ws.seg_base + s) + (item - pre / chunk);
+                    n_pieces = __ldg(p.ws.n_seg + s);
+                    g0 = e;
+                    ++s;
+                    more = g0 < g1;
+                } else {
+                    seq = fixed_sk.x;
+                    t0 = fixed_sk.y * p.split_tokens;
+                    t1 = min(t0 + p.split_tokens, __ldg(p.ctx_lens + seq));
+                    slot = item;
+                    n_pieces = __ldg(p.ws.n_seg + seq);
+                    more = false;
                 }
-                const int32_t blk = __shfl_sync(0xffffffffu, tbl, lb - blk0 - tbl_base);
+                const bool final_out = n_pieces == 1;
+                const int32_t *trow = p.tables + (int64_t)seq * p.max_blocks;
+                const int32_t blk0 = t0 / p.block_size;
+                // this piece's queries: heads [hg*hpc*G, (hg+1)*hpc*G) of sequence seq
+                const uint32_t qs = item_it & 1u;
                 if (lane == 0) {
-                    const uint32_t st = stage_it % p.n_stages;
-                    if (!mbar_wait(&L.empty_bar[st], ((stage_it / p.n_stages) & 1u) ^ 1u, abort_flag)) {
+                    if (!mbar_wait(&L.qempty_bar[qs], ((item_it >> 1) & 1u) ^ 1u, abort_flag)) {
                         report(p.dev_status, PKV_DEV_TIMEOUT);
                         *abort_flag = 1;
-                    } else {
-                        StageMeta m;
-                        m.seq = s;
-                        m.split_index = sp;
-                        m.n_valid = min(kStageTokens, t1 - t);
-                        m.flags = (t == t0 ? kMetaFirst : 0) | (t + kStageTokens >= t1 ? kMetaLast : 0) |
-                                  (final_out ? kMetaFinal : 0);
-                        m.head_group = hg;
-                        m.n_splits = (ctx + p.split_tokens - 1) / p.split_tokens;
-                        const bool bad = blk < 0 || blk > p.n_blocks;
-                        if (bad) {
-                            m.flags |= kMetaBad;
-                            report(p.dev_status, PKV_DEV_BAD_BLOCK_ID);
-                        }
-                        L.meta[st] = m;
-                        if (bad) {
-                            mbar_arrive(&L.full_bar[st]);
-                        } else {
-                            uint8_t *stg = L.stages + (size_t)st * p.stage_bytes;
-                            const int32_t row0 = blk * p.block_size + (t % p.block_size);
-                            const int32_t head0 = hg * hpc;
-                            mbar_arrive_expect_tx(&L.full_bar[st], p.tx_bytes);
-                            if (!INT8) {
-                                const uint32_t half_bytes = (uint32_t)hpc * kStageTokens * 128u;
-                                for (int h = 0; h < HALVES; ++h) {
-                                    for (int b = 0; b < p.boxes_per_half; ++b) {
-                                        const uint32_t off = h * half_bytes + b * (kStageTokens * 128u);
-                                        if (p.boxes_per_half == 1) {
-                                            tma_load_3d(stg + off, &k_map, h * 64, row0, head0, &L.full_bar[st]);
-                                            tma_load_3d(stg + p.kv_tile_bytes + off, &v_map, h * 64, row0, head0,
-                                                        &L.full_bar[st]);
-                                        } else {
-                                            tma_load_3d(stg + off, &k_map, h * 64, head0 + b, row0, &L.full_bar[st]);
-                                            tma_load_3d(stg + p.kv_tile_bytes + off, &v_map, h * 64, head0 + b, row0,
-                                                        &L.full_bar[st]);
-                                        }
-                                    }
-                                }
-                            } else {
-                                for (int b = 0; b < p.boxes_per_half; ++b) {
-                                    const uint32_t off = b * (kStageTokens * (uint32_t)D);
-                                    if (p.boxes_per_half == 1) {
-                                        tma_load_3d(stg + off, &k_map, 0, row0, head0, &L.full_bar[st]);
-                                        tma_load_3d(stg + p.kv_tile_bytes + off, &v_map, 0, row0, head0,
-                                                    &L.full_bar[st]);
-                                    } else {
-                                        tma_load_3d(stg + off, &k_map, 0, head0 + b, row0, &L.full_bar[st]);
-                                        tma_load_3d(stg + p.kv_tile_bytes + off, &v_map, 0, head0 + b, row0,
-                                                    &L.full_bar[st]);
-                                    }
-                                }
-                                uint8_t *sc = stg + 2 * p.kv_tile_bytes;
-                                tma_load_2d(sc, &ks_map, head0, row0, &L.full_bar[st]);
-                                tma_load_2d(sc + p.scale_tile_bytes, &vs_map, head0, row0, &L.full_bar[st]);
-                            }
-                        }
+                    }
+                    if (!*abort_flag) {
+                        mbar_arrive_expect_tx(&L.qfull_bar[qs], p.q_slot_bytes);
+                        bulk_g2s(L.q_slots + qs * p.q_slot_bytes,
+                                 p.q + ((int64_t)seq * p.n_q_heads + (int64_t)hg * hpc * p.group) * D,
+                                 p.q_slot_bytes, &L.qfull_bar[qs]);
                     }
                 }
                 ok = !__shfl_sync(0xffffffffu, *abort_flag, 0);
-                ++stage_it;
+                int32_t tbl = 0, tbl_base = -1;
+                for (int32_t t = t0; ok && t < t1; t += kStageTokens) {
+                    const int32_t lb = t / p.block_size;
+                    if (lb - blk0 >= tbl_base + 32 || tbl_base < 0) {
+                        tbl_base = lb - blk0;
+                        const int32_t j = blk0 + tbl_base + lane;
+                        tbl = j < p.max_blocks ? __ldg(trow + j) : -1;
+                    }
+                    const int32_t blk = __shfl_sync(0xffffffffu, tbl, lb - blk0 - tbl_base);
+                    if (lane == 0) {
+                        const uint32_t st = stage_it % p.n_stages;
+                        if (!mbar_wait(&L.empty_bar[st], ((stage_it / p.n_stages) & 1u) ^ 1u, abort_flag)) {
+                            report(p.dev_status, PKV_DEV_TIMEOUT);
+                            *abort_flag = 1;
+                        } else {
+                            StageMeta m;
+                            m.seq = seq;
+                            m.split_index = slot;
+                            m.n_valid = min(kStageTokens, t1 - t);
+                            m.flags = (t == t0 ? kMetaFirst : 0) | (t + kStageTokens >= t1 ? kMetaLast : 0) |
+                                      (final_out ? kMetaFinal : 0);
+                            m.head_group = hg;
+                            m.n_splits = n_pieces;
+                            const bool bad = blk < 0 || blk > p.n_blocks;
+                            if (bad) {
+                                m.flags |= kMetaBad;
+                                report(p.dev_status, PKV_DEV_BAD_BLOCK_ID);
+                            }
+                            L.meta[st] = m;
+                            if (bad) {
+                                mbar_arrive(&L.full_bar[st]);
+                            } else {
+                                uint8_t *stg = L.stages + (size_t)st * p.stage_bytes;
+                                const int32_t row0 = blk * p.block_size + (t % p.block_size);
+                                const int32_t head0 = hg * hpc;
+                                mbar_arrive_expect_tx(&L.full_bar[st], p.tx_bytes);
+                                issue_stage_loads<D, INT8>(stg, p, k_map, v_map, ks_map, vs_map, row0, head0,
+                                                           &L.full_bar[st]);
+                            }
+                        }
+                    }
+                    ok = !__shfl_sync(0xffffffffu, *abort_flag, 0);
+                    ++stage_it;
+                }
+                ++item_it;
             }
-            ++item_it;
             next = __shfl_sync(0xffffffffu, next, 0);
         }
         // stop marker
@@ -442,7 +584,6 @@ __global__ void __launch_bounds__(288, 1) decode_split_kernel(const __grid_const
     const int g = lane >> 2, qd = lane & 3;   // mma fragment row group / column pair
     const int G = p.group;
     const int mi = lane >> 3, ri = lane & 7;  // ldmatrix matrix index / row within it
-    uint32_t qf[KSTEPS][2];                   // Q^T B-fragments (bf16, or fp16 for int8 pages)
     float acc[KSTEPS][4];                     // O^T accumulators: rows d, columns query heads
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     uint32_t stage_it = 0, item_it = 0;
@@ -467,30 +608,39 @@ __global__ void __launch_bounds__(288, 1) decode_split_kernel(const __grid_const
                 *abort_flag = 1;
                 break;
             }
-            const __nv_bfloat16 *qsm =
-                reinterpret_cast<const __nv_bfloat16 *>(L.q_slots + qs * p.q_slot_bytes) +
-                (size_t)warp * G * D;
+            // Rewrite this warp's G query rows in place: 16-byte chunk c of head row
+            // r moves to chunk c ^ r (so ldmatrix of 8 head rows is conflict-free),
+            // converted to fp16 for int8 pages.  The rows stay in the slot until
+            // the piece's last stage.
+            uint8_t *qrows = L.q_slots + qs * p.q_slot_bytes + (size_t)warp * G * D * 2;
+            {
+                constexpr int CPR = D / 8;            // 16-byte chunks per head row
+                uint4 tmp[(8 * CPR + 31) / 32];
 #pragma unroll
-            for (int kk = 0; kk < KSTEPS; ++kk) {
-                uint32_t b0 = 0, b1 = 0;
-                if (g < G) {
-                    const __nv_bfloat16 *qr = qsm + (size_t)g * D + kk * 16 + 2 * qd;
-                    __nv_bfloat162 x0 = *reinterpret_cast<const __nv_bfloat162 *>(qr);
-                    __nv_bfloat162 x1 = *reinterpret_cast<const __nv_bfloat162 *>(qr + 8);
-                    if (INT8) {
-                        float2 f0 = __bfloat1622float2(x0), f1 = __bfloat1622float2(x1);
-                        b0 = pack_f16x2(f0.x, f0.y);
-                        b1 = pack_f16x2(f1.x, f1.y);
-                    } else {
-                        b0 = *reinterpret_cast<uint32_t *>(&x0);
-                        b1 = *reinterpret_cast<uint32_t *>(&x1);
+                for (int i = 0; i < (8 * CPR + 31) / 32; ++i) {
+                    const int idx = i * 32 + lane;
+                    if (idx < G * CPR) tmp[i] = *reinterpret_cast<const uint4 *>(qrows + idx * 16);
+                }
+                __syncwarp();
+#pragma unroll
+                for (int i = 0; i < (8 * CPR + 31) / 32; ++i) {
+                    const int idx = i * 32 + lane;
+                    if (idx < G * CPR) {
+                        const int r = idx / CPR, c = idx % CPR;
+                        uint4 x = tmp[i];
+                        if (INT8) {
+                            uint32_t *w = reinterpret_cast<uint32_t *>(&x);
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&w[e]));
+                                w[e] = pack_f16x2(f.x, f.y);
+                            }
+                        }
+                        *reinterpret_cast<uint4 *>(qrows + (r * CPR + (c ^ (r & 7))) * 16) = x;
                     }
                 }
-                qf[kk][0] = b0;
-                qf[kk][1] = b1;
+                __syncwarp();
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&L.qempty_bar[qs]);
 #pragma unroll
             for (int mt = 0; mt < KSTEPS; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
             m0 = m1 = -INFINITY;
@@ -550,18 +700,29 @@ __global__ void __launch_bounds__(288, 1) decode_split_kernel(const __grid_const
                 sv1 = scv[(g + 8) * hpc + warp];
             }
 
-            // --- S^T[16 tokens x 8 heads] = K Q^T
+            // --- S^T[16 tokens x 8 heads] = K Q^T; Q^T B-fragments by ldmatrix from the
+            // swizzled query rows.  Padding columns (heads G..7) re-read row 0 of
+            // this warp: their results are never used, and every address stays
+            // inside this warp's G rows of the slot.
+            const uint32_t q_base = smem_u32(L.q_slots + (item_it & 1u) * p.q_slot_bytes) + warp * G * D * 2;
+            const uint32_t qrow = ri < G ? (uint32_t)ri : 0u;
             float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int kk = 0; kk < KSTEPS; ++kk) {
-                const int tok = ri + 8 * (mi & 1);
-                const uint32_t chunk = (uint32_t)((kk % 4) * 2 + (mi >> 1));
-                uint32_t a[4];
-                ldmatrix_x4(a, k_base + (uint32_t)(kk / 4) * half_stride + swz(tok, chunk));
-                if (INT8)
-                    mma_f16_16816(s4, a, qf[kk][0], qf[kk][1]);
-                else
-                    mma_bf16_16816(s4, a, qf[kk][0], qf[kk][1]);
+            for (int kk = 0; kk < KSTEPS; kk += 2) {
+                uint32_t qb[4];  // b0, b1 of k-step kk, then of kk + 1
+                ldmatrix_x4(qb, q_base + qrow * (D * 2) + (((uint32_t)(2 * kk + mi) ^ (qrow & 7u)) << 4));
+#pragma unroll
+                for (int k2 = 0; k2 < 2; ++k2) {
+                    const int k = kk + k2;
+                    const int tok = ri + 8 * (mi & 1);
+                    const uint32_t chunk = (uint32_t)((k % 4) * 2 + (mi >> 1));
+                    uint32_t a[4];
+                    ldmatrix_x4(a, k_base + (uint32_t)(k / 4) * half_stride + swz(tok, chunk));
+                    if (INT8)
+                        mma_f16_16816(s4, a, qb[2 * k2], qb[2 * k2 + 1]);
+                    else
+                        mma_bf16_16816(s4, a, qb[2 * k2], qb[2 * k2 + 1]);
+                }
             }
             // scale to log2 units, dequantise K (int8), mask tokens past the context
             const bool v0 = g < nv, v1 = g + 8 < nv;
@@ -628,9 +789,13 @@ __global__ void __launch_bounds__(288, 1) decode_split_kernel(const __grid_const
             if (INT8) __syncwarp();  // scratch is rewritten by the next stage
         }
 
-        // the stage's tiles are no longer needed: hand the slot back before finalising
+        // the stage's tiles (and, at a piece's end, its query rows) are no longer
+        // needed: hand them back before finalising
         __syncwarp();
-        if (lane == 0) mbar_arrive(&L.empty_bar[st]);
+        if (lane == 0) {
+            mbar_arrive(&L.empty_bar[st]);
+            if (meta.flags & kMetaLast) mbar_arrive(&L.qempty_bar[item_it & 1u]);
+        }
         ++stage_it;
 
         if (meta.flags & kMetaLast) {
@@ -684,18 +849,6 @@ __global__ void __launch_bounds__(288, 1) decode_split_kernel(const __grid_const
                     if (n0 < G) p.ws.part_ml[prow + n0] = make_float2(m0, L0);
                     if (n1 < G) p.ws.part_ml[prow + n1] = make_float2(m1, L1);
                 }
-                // publish the partial; the warp that completes the last split of
-                // this (sequence, kv head) merges them all
-                __threadfence();
-                __syncwarp();
-                int32_t last = 0;
-                if (lane == 0) last = atomicAdd(&p.ws.done[(int64_t)s * p.n_kv_heads + kvh], 1) == meta.n_splits - 1;
-                last = __shfl_sync(0xffffffffu, last, 0);
-                if (last) {
-                    __threadfence();
-                    merge_splits<D>(p.ws.part_ml, p.ws.part_acc, p.out, p.lse_out, p.n_q_heads, s, hbase, G,
-                                    __ldcg(&p.ws.split_base[s]), meta.n_splits, lane);
-                }
             }
             ++item_it;
         }
@@ -714,10 +867,10 @@ static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 size_t decode_workspace_bytes(int32_t n_seqs, int32_t n_q_heads, int32_t head_dim, int64_t capacity)
 {
-    size_t b = 256;                                          // header
-    b += align_up((size_t)n_seqs * sizeof(int32_t), 256);    // split_base
-    b += align_up((size_t)n_seqs * n_q_heads * sizeof(int32_t), 256);  // done counters
-    b += align_up((size_t)capacity * sizeof(int2), 256);     // split_list
+    size_t b = 256;                                                    // header
+    b += align_up((size_t)(n_seqs + 1) * sizeof(int32_t), 256);        // seq_prefix
+    b += 2 * align_up((size_t)n_seqs * sizeof(int32_t), 256);          // seg_base, n_seg
+    b += align_up((size_t)capacity * sizeof(int2), 256);               // items
     b += align_up((size_t)capacity * n_q_heads * sizeof(float2), 256);
     b += align_up((size_t)capacity * n_q_heads * head_dim * sizeof(float), 256);
     return b;
@@ -727,22 +880,22 @@ bool carve_decode_workspace(void *ws, size_t bytes, int32_t n_seqs, int32_t n_q_
                             int32_t head_dim, DecodeWorkspace *out)
 {
     if (!ws) return false;
-    const size_t fixed = 256 + align_up((size_t)n_seqs * sizeof(int32_t), 256) +
-                         align_up((size_t)n_seqs * n_q_heads * sizeof(int32_t), 256) + 3 * 256;
-    if (bytes < fixed) return false;
+    if (bytes < decode_workspace_bytes(n_seqs, n_q_heads, head_dim, 1)) return false;
     const size_t per = sizeof(int2) + (size_t)n_q_heads * sizeof(float2) +
                        (size_t)n_q_heads * head_dim * sizeof(float);
-    int64_t cap = (int64_t)((bytes - fixed) / per);
-    while (cap > 0 && decode_workspace_bytes(n_seqs, n_q_heads, head_dim, cap) > bytes) --cap;
+    int64_t cap = (int64_t)(bytes / per) + 1;
+    while (cap > 1 && decode_workspace_bytes(n_seqs, n_q_heads, head_dim, cap) > bytes) --cap;
     if (cap > (int64_t)0x7fffffff) cap = 0x7fffffff;
     uint8_t *p = static_cast<uint8_t *>(ws);
     out->header = reinterpret_cast<uint32_t *>(p);
     p += 256;
-    out->split_base = reinterpret_cast<int32_t *>(p);
+    out->seq_prefix = reinterpret_cast<int32_t *>(p);
+    p += align_up((size_t)(n_seqs + 1) * sizeof(int32_t), 256);
+    out->seg_base = reinterpret_cast<int32_t *>(p);
     p += align_up((size_t)n_seqs * sizeof(int32_t), 256);
-    out->done = reinterpret_cast<int32_t *>(p);
-    p += align_up((size_t)n_seqs * n_q_heads * sizeof(int32_t), 256);
-    out->split_list = reinterpret_cast<int2 *>(p);
+    out->n_seg = reinterpret_cast<int32_t *>(p);
+    p += align_up((size_t)n_seqs * sizeof(int32_t), 256);
+    out->items = reinterpret_cast<int2 *>(p);
     p += align_up((size_t)cap * sizeof(int2), 256);
     out->part_ml = reinterpret_cast<float2 *>(p);
     p += align_up((size_t)cap * n_q_heads * sizeof(float2), 256);
@@ -875,20 +1028,49 @@ cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream)
     if (e != cudaSuccess) return e;
     if (occ < 1) return cudaErrorInvalidConfiguration;
     const int grid = num_sms * (occ < ctas_per_sm ? occ : ctas_per_sm);
-    kern<<<grid, threads, smem, stream>>>(kmap, vmap, ksmap, vsmap, p);
-    return cudaGetLastError();
+    // balanced pieces: about items_per_cta items per CTA and kv-head group
+    int items_per_cta = env_int("PKV_DECODE_ITEMS_PER_CTA", 1);
+    if (items_per_cta < 1 || items_per_cta > 16) items_per_cta = 1;
+    const int items_target = (grid * items_per_cta + p.n_hg - 1) / p.n_hg;
+    const int32_t max_tokens = a.max_blocks * d.block_size;
+    decode_plan_kernel<<<1, 1024, 0, stream>>>(a.ctx_lens, a.n_seqs, a.split_tokens, max_tokens, a.n_q_heads, D,
+                                               d.n_kv_heads, items_target, a.ws, (__nv_bfloat16 *)a.out,
+                                               a.lse_out, a.dev_status);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t lc{};
+    lc.gridDim = dim3((unsigned)grid);
+    lc.blockDim = dim3((unsigned)threads);
+    lc.dynamicSmemBytes = smem;
+    lc.stream = stream;
+    lc.attrs = pdl;
+    lc.numAttrs = 1;
+    e = cudaLaunchKernelEx(&lc, kern, kmap, vmap, ksmap, vsmap, p);
+    if (e != cudaSuccess) return e;
+    // merge of multi-piece sequences: one warp per (sequence, kv head)
+    const int64_t warps = (int64_t)a.n_seqs * d.n_kv_heads;
+    cudaLaunchConfig_t mc{};
+    mc.gridDim = dim3((unsigned)((warps + 3) / 4));
+    mc.blockDim = dim3(128);
+    mc.stream = stream;
+    mc.attrs = pdl;
+    mc.numAttrs = 1;
+    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out);
+    switch (G) {
+    case 1: return cudaLaunchKernelEx(&mc, decode_merge_kernel<D, D / 32>, a.ws, a.n_seqs, d.n_kv_heads, a.n_q_heads, G, out, a.lse_out);
+    case 2: return cudaLaunchKernelEx(&mc, decode_merge_kernel<D, D / 16>, a.ws, a.n_seqs, d.n_kv_heads, a.n_q_heads, G, out, a.lse_out);
+    case 4: return cudaLaunchKernelEx(&mc, decode_merge_kernel<D, D / 8>, a.ws, a.n_seqs, d.n_kv_heads, a.n_q_heads, G, out, a.lse_out);
+    default: return cudaLaunchKernelEx(&mc, decode_merge_kernel<D, D / 4>, a.ws, a.n_seqs, d.n_kv_heads, a.n_q_heads, G, out, a.lse_out);
+    }
 }
 
 }  // namespace
 
 cudaError_t launch_decode(const DecodeArgs &a, int num_sms, cudaStream_t stream)
 {
-    const int32_t max_tokens = a.max_blocks * a.dims.block_size;
-    decode_plan_kernel<<<1, 1024, 0, stream>>>(a.ctx_lens, a.n_seqs, a.split_tokens, max_tokens, a.n_q_heads,
-                                               a.dims.head_dim, a.dims.n_kv_heads, a.ws,
-                                               (__nv_bfloat16 *)a.out, a.lse_out, a.dev_status);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
     const bool int8 = a.kv_dtype == PKV_KV_INT8;
     if (a.dims.head_dim == 128)
         return int8 ? launch_split<128, true>(a, num_sms, stream) : launch_split<128, false>(a, num_sms, stream);

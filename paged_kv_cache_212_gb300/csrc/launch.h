@@ -33,24 +33,27 @@ struct GatherArgs {
 };
 
 // Decode workspace layout (all offsets 256-byte aligned):
-//   header     : uint32 [64]      work counter, number of splits, overflow flag
-//   split_base : int32 [n_seqs]   first split index of each sequence
-//   done       : int32 [n_seqs][Hq] finished-split counters per (sequence, kv head)
-//   split_list : int2  [cap]      (sequence, split) of every split
-//   part_ml    : float2[cap][Hq]  (running max in log2 units, running sum)
+//   header     : uint32 [64]        work counter, items, overflow flag, stages per item, total stages
+//   seq_prefix : int32 [n_seqs + 1] 16-token stages before each sequence (balanced mode)
+//   seg_base   : int32 [n_seqs]     first partial slot of each sequence
+//   n_seg      : int32 [n_seqs]     pieces (partial slots) of each sequence
+//   items      : int2  [cap]        fixed splits: (sequence, split) per item; balanced: first sequence
+//   part_ml    : float2[cap][Hq]    (running max in log2 units, running sum)
 //   part_acc   : float [cap][Hq][D] unnormalised partial outputs
 struct DecodeWorkspace {
     uint32_t *header;
-    int32_t *split_base;
-    int32_t *done;
-    int2 *split_list;
+    int32_t *seq_prefix;
+    int32_t *seg_base;
+    int32_t *n_seg;
+    int2 *items;
     float2 *part_ml;
     float *part_acc;
-    int32_t capacity;  // splits the workspace can hold
+    int32_t capacity;  // partial slots (and items) the workspace can hold
 };
 
-constexpr int kDecodeMinAutoSplit = 128;   // automatic split never goes below this
-constexpr int kDecodeDefaultSplit = 256;
+// Automatic splitting cuts the concatenated token stream into equal pieces,
+// about one per CTA; the workspace for it holds n_seqs + this many slots.
+constexpr int kDecodeAutoMaxItems = 512;
 
 size_t decode_workspace_bytes(int32_t n_seqs, int32_t n_q_heads, int32_t head_dim,
                               int64_t capacity);
@@ -69,7 +72,7 @@ struct DecodeArgs {
     const int32_t *ctx_lens;
     int32_t n_seqs;
     float softmax_scale;
-    int32_t split_tokens;
+    int32_t split_tokens;  // 0: balanced pieces
     void *out;
     float *lse_out;
     DecodeWorkspace ws;

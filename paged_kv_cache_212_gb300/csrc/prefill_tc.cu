@@ -104,6 +104,21 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// Issue a load of 32 consecutive fp32 columns without waiting for it.
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t *r)
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32])
 {
     asm volatile(
@@ -258,18 +273,24 @@ __global__ void __launch_bounds__(192, 1) prefill_tc_kernel(const __grid_constan
         }
     } else if (warp == 5 && n_kt > 0) {
         // ===================== MMA issuer =====================
+        // One lane issues S_j = Q K_j^T as soon as K_j has landed and S buffer
+        // j & 1 is free, and O += P_j V_j as soon as P_j is written, whichever
+        // is ready first (non-blocking polls, bounded by the wait limit).
         const uint32_t idesc_s = umma_idesc_bf16(kTM, kTN, false, false);
         const uint32_t idesc_o = umma_idesc_bf16(kTM, D, false, true);
         bool ok = true;
-        if (lane == 0) ok = mbar_wait(q_full, 0, abort_flag);
-        const uint32_t q_addr = smem_u32(q_s), p_addr = smem_u32(p_s);
-        for (int j = 0; j <= n_kt && ok; ++j) {
-            if (j < n_kt) {
-                const int st = j % kKvStages, use = j / kKvStages, b = j & 1;
-                if (lane == 0) {
-                    ok = mbar_wait(&kv_full[st], use & 1, abort_flag) &&
-                         mbar_wait(&s_free[b], ((j >> 1) & 1) ^ 1, abort_flag);
-                    if (ok) {
+        if (lane == 0) {
+            ok = mbar_wait(q_full, 0, abort_flag);
+            const uint32_t q_addr = smem_u32(q_s), p_addr = smem_u32(p_s);
+            int js = 0, jp = 0;
+            unsigned long long t_last = global_timer_ns();
+            uint32_t spin = 0;
+            while (ok && jp < n_kt) {
+                bool progressed = false;
+                if (js < n_kt && js < jp + 2) {
+                    const int st = js % kKvStages, b = js & 1;
+                    if (mbar_test_wait(&kv_full[st], (js / kKvStages) & 1) &&
+                        mbar_test_wait(&s_free[b], ((js >> 1) & 1) ^ 1)) {
                         tc_fence_after();
                         const uint32_t k_addr = smem_u32(kv_s + st * kStageBytes);
 #pragma unroll
@@ -279,41 +300,44 @@ __global__ void __launch_bounds__(192, 1) prefill_tc_kernel(const __grid_constan
                                       umma_desc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0);
                         }
                         umma_commit(&s_full[b]);
+                        ++js;
+                        progressed = true;
                     }
                 }
-            }
-            if (j >= 1) {
-                const int jp = j - 1, st = jp % kKvStages;
-                if (lane == 0 && ok) {
-                    ok = mbar_wait(p_full, jp & 1, abort_flag);
-                    if (ok) {
-                        tc_fence_after();
-                        const uint32_t v_addr = smem_u32(kv_s + st * kStageBytes + kKBytes);
+                if (jp < js && mbar_test_wait(p_full, jp & 1)) {
+                    tc_fence_after();
+                    const int st = jp % kKvStages;
+                    const uint32_t v_addr = smem_u32(kv_s + st * kStageBytes + kKBytes);
 #pragma unroll
-                        for (int kk = 0; kk < kTN / 16; ++kk) {
-                            // A = P (K-major, keys kk*16..), B = V (MN-major: 8-key groups 1024 B apart,
-                            // 64-column panels kPanelRows128 apart)
-                            const uint32_t a_off = (kk / 4) * kPanelRows128 + (kk % 4) * 32;
-                            umma_bf16(tmem + kOCol, umma_desc_sw128(p_addr + a_off, 16, 1024),
-                                      umma_desc_sw128(v_addr + kk * 2048, kPanelRows128, 1024), idesc_o,
-                                      (jp > 0 || kk > 0) ? 1u : 0u);
-                        }
-                        umma_commit(o_done);
-                        umma_commit(&kv_empty[st]);
+                    for (int kk = 0; kk < kTN / 16; ++kk) {
+                        // A = P (K-major, keys kk*16..), B = V (MN-major: 8-key groups 1024 B
+                        // apart, 64-column panels kPanelRows128 apart)
+                        const uint32_t a_off = (kk / 4) * kPanelRows128 + (kk % 4) * 32;
+                        umma_bf16(tmem + kOCol, umma_desc_sw128(p_addr + a_off, 16, 1024),
+                                  umma_desc_sw128(v_addr + kk * 2048, kPanelRows128, 1024), idesc_o,
+                                  (jp > 0 || kk > 0) ? 1u : 0u);
                     }
+                    umma_commit(o_done);
+                    umma_commit(&kv_empty[st]);
+                    ++jp;
+                    progressed = true;
+                }
+                if (progressed) {
+                    spin = 0;
+                    t_last = global_timer_ns();
+                } else if ((++spin & 255u) == 0) {
+                    if (*abort_flag || global_timer_ns() - t_last > kWaitTimeoutNs) ok = false;
                 }
             }
-            ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-        }
-        if (!ok && lane == 0) {
-            report(p.dev_status, PKV_DEV_TIMEOUT);
-            *abort_flag = 1;
-        }
-        // every MMA this warp issued has retired before the TMEM is released
-        if (lane == 0) {
+            if (!ok) {
+                report(p.dev_status, PKV_DEV_TIMEOUT);
+                *abort_flag = 1;
+            }
+            // every MMA issued has retired before the TMEM is released
             umma_commit(fin_bar);
             (void)mbar_wait(fin_bar, 0);
         }
+        __syncwarp();
     } else if (warp < 4) {
         // ===================== softmax warpgroup: row r = TMEM lane r =====================
         const int r = threadIdx.x;
@@ -328,20 +352,23 @@ __global__ void __launch_bounds__(192, 1) prefill_tc_kernel(const __grid_constan
             tc_fence_after();
             const int32_t key_base = j * kTN;
             const bool masked = key_base + kTN - 1 > qpos;
-            // pass 1: row maximum of this tile
+            // one pass: the whole S row into registers (four loads, one wait)
+            uint32_t sv[kTN];
+#pragma unroll
+            for (int c = 0; c < kTN / 32; ++c) tmem_ld32_async(lane_base + b * kTN + c * 32, sv + c * 32);
+            tmem_wait_ld();
+            // S buffer b is read: the MMA warp may overwrite it with S_{j+2}
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&s_free[b]);
             float mx = -INFINITY;
-            float v[32];
 #pragma unroll
-            for (int c = 0; c < kTN / 32; ++c) {
-                tmem_ld32(lane_base + b * kTN + c * 32, v);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const bool valid = !masked || key_base + c * 32 + i <= qpos;
-                    mx = fmaxf(mx, valid ? v[i] : -INFINITY);
-                }
+            for (int i = 0; i < kTN; ++i) {
+                const bool valid = !masked || key_base + i <= qpos;
+                mx = fmaxf(mx, valid ? __uint_as_float(sv[i]) : -INFINITY);
             }
             mx *= p.scale_log2;
-            // wait until the previous P V product is done: P is overwritten, O may be rescaled
+            // the previous P V product must be done: P is overwritten, O may be rescaled
             if (j > 0) {
                 ok = __all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, abort_flag));
                 if (!ok) break;
@@ -354,27 +381,18 @@ __global__ void __launch_bounds__(192, 1) prefill_tc_kernel(const __grid_constan
                 alpha = fast_exp2(m - mx);
                 m = mx;
             }
-            if (__any_sync(0xffffffffu, alpha != 1.f) && j > 0) {
-#pragma unroll
-                for (int c = 0; c < D / 32; ++c) {
-                    tmem_ld32(lane_base + kOCol + c * 32, v);
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] *= alpha;
-                    tmem_st32(lane_base + kOCol + c * 32, v);
-                }
-            }
             l *= alpha;
-            // pass 2: probabilities, row sum, P (bf16) to shared memory
+            // probabilities, row sum, P (bf16) to shared memory
 #pragma unroll
             for (int c = 0; c < kTN / 32; ++c) {
-                tmem_ld32(lane_base + b * kTN + c * 32, v);
                 uint32_t pk[16];
 #pragma unroll
                 for (int i = 0; i < 32; i += 2) {
-                    const bool v0 = !masked || key_base + c * 32 + i <= qpos;
-                    const bool v1 = !masked || key_base + c * 32 + i + 1 <= qpos;
-                    const float e0 = v0 ? fast_exp2(v[i] * p.scale_log2 - m) : 0.f;
-                    const float e1 = v1 ? fast_exp2(v[i + 1] * p.scale_log2 - m) : 0.f;
+                    const int kidx = c * 32 + i;
+                    const bool v0 = !masked || key_base + kidx <= qpos;
+                    const bool v1 = !masked || key_base + kidx + 1 <= qpos;
+                    const float e0 = v0 ? fast_exp2(__uint_as_float(sv[kidx]) * p.scale_log2 - m) : 0.f;
+                    const float e1 = v1 ? fast_exp2(__uint_as_float(sv[kidx + 1]) * p.scale_log2 - m) : 0.f;
                     l += e0 + e1;
                     pk[i / 2] = pack_bf16x2(e0, e1);
                 }
@@ -385,10 +403,18 @@ __global__ void __launch_bounds__(192, 1) prefill_tc_kernel(const __grid_constan
                     *reinterpret_cast<uint4 *>(prow + swz128(r, (c % 2) * 4 + q4)) =
                         make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
             }
-            // S buffer b is read: the MMA warp may overwrite it with S_{j+2}
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s_free[b]);
+            // O row rescale (rare: the row maximum grew by more than 2^8), after the
+            // S row is dead; the next P V product is issued only after p_full below
+            if (__any_sync(0xffffffffu, alpha != 1.f) && j > 0) {
+                float v[32];
+#pragma unroll 1
+                for (int c = 0; c < D / 32; ++c) {
+                    tmem_ld32(lane_base + kOCol + c * 32, v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] *= alpha;
+                    tmem_st32(lane_base + kOCol + c * 32, v);
+                }
+            }
             // last tile: V rows of keys past the last one may hold anything; zero them
             if (j == n_kt - 1 && (n_keys & 15) != 0) {
                 const int first = n_keys - key_base, stop = ((n_keys + 15) & ~15) - key_base;
@@ -413,10 +439,15 @@ __global__ void __launch_bounds__(192, 1) prefill_tc_kernel(const __grid_constan
             const bool store = pos <= p_last;
             const float inv = 1.f / l;
             __nv_bfloat16 *o = p.out + (((int64_t)s * p.chunk + pos) * p.n_q_heads + h) * D;
-            float v[32];
+            uint32_t ov[D];
+#pragma unroll
+            for (int c = 0; c < D / 32; ++c) tmem_ld32_async(lane_base + kOCol + c * 32, ov + c * 32);
+            tmem_wait_ld();
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
-                tmem_ld32(lane_base + kOCol + c * 32, v);
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(ov[c * 32 + i]);
                 if (store) {
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
