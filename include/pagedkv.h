@@ -35,7 +35,8 @@
  *
  * Supported geometry: head_dim in {64, 128}; block_size a multiple of 16, at
  * most 256; n_q_heads % n_kv_heads == 0 and G = n_q_heads / n_kv_heads in
- * {1, 2, 4, 8}; query head h reads kv head h / G.
+ * {1, 2, 4, 8} for decode (1 .. 16 dividing 64 for prefill); query head h reads kv
+ * head h / G.
  */
 #ifndef PAGEDKV_H
 #define PAGEDKV_H
@@ -177,6 +178,24 @@ int paged_decode_attention(const pkv_bf16 *q, int32_t n_q_heads, const void *k_p
                            float softmax_scale, int32_t split_tokens, pkv_bf16 *out,
                            float *lse_out, void *workspace, size_t workspace_bytes,
                            int32_t *dev_status, pkv_stream_t stream);
+
+/*
+ * paged_decode_step -- one decode step of one layer in one call: the page
+ * write of this step's new rows (paged_kv_write, or paged_kv_write_int8 when
+ * kv_dtype is PKV_KV_INT8, with k_new / v_new / start_pos / n_new as there)
+ * followed by paged_decode_attention over ctx_lens tokens, which must count
+ * the rows just written.  Results are those of the two calls in sequence; the
+ * write runs inside the first kernel launch of the decode, saving one launch
+ * per layer (the per-layer step of tiny-llm paged_kv.py, PagedLayerKV.update:
+ * write, then attention).
+ */
+int paged_decode_step(const pkv_bf16 *k_new, const pkv_bf16 *v_new, const int32_t *start_pos,
+                      int32_t n_new, const pkv_bf16 *q, int32_t n_q_heads, void *k_pool,
+                      void *v_pool, float *k_scales, float *v_scales, int32_t kv_dtype,
+                      pkv_dims dims, const int32_t *block_tables, int32_t max_blocks,
+                      const int32_t *ctx_lens, int32_t n_seqs, float softmax_scale,
+                      int32_t split_tokens, pkv_bf16 *out, float *lse_out, void *workspace,
+                      size_t workspace_bytes, int32_t *dev_status, pkv_stream_t stream);
 
 /*
  * paged_prefill_attention -- chunked paged prefill (AstrAI cache.py,

@@ -24,7 +24,7 @@ DEV_WORKSPACE_OVERFLOW, DEV_TIMEOUT = 8, 16
 
 EXPORTS = ("pkv_status_string", "pkv_last_cuda_error", "paged_kv_write", "paged_kv_write_int8",
            "paged_kv_gather", "pkv_decode_workspace_bytes", "paged_decode_attention",
-           "paged_prefill_attention", "paged_decode_attention_noalloc")
+           "paged_prefill_attention", "paged_decode_attention_noalloc", "paged_decode_step")
 NOALLOC_DECODE_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
@@ -70,8 +70,10 @@ def load_library(path: str = LIB_PATH):
                                             P, P]
     lib.paged_decode_attention_noalloc.argtypes = [P, i32, P, P, P, P, i32, Dims, P, i32, P, i32,
                                                    ctypes.c_float, i32, i64, P, P, P, P]
+    lib.paged_decode_step.argtypes = [P, P, P, i32, P, i32, P, P, P, P, i32, Dims, P, i32, P, i32,
+                                      ctypes.c_float, i32, P, P, P, sz, P, P]
     for fn in ("paged_kv_write", "paged_kv_write_int8", "paged_kv_gather", "paged_decode_attention",
-               "paged_prefill_attention", "paged_decode_attention_noalloc"):
+               "paged_prefill_attention", "paged_decode_attention_noalloc", "paged_decode_step"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -221,6 +223,51 @@ def paged_decode_attention(q, k_pool, v_pool, block_tables, ctx_lens, softmax_sc
                                     float(softmax_scale), int(split_tokens), _ptr(out), _ptr(lse_out),
                                     _ptr(workspace), workspace.numel(), _ptr(dev_status), _stream(stream))
     _check("paged_decode_attention", st)
+    return out
+
+
+def paged_decode_step(k_new, v_new, start_pos, q, k_pool, v_pool, block_tables, ctx_lens, softmax_scale,
+                      k_scales=None, v_scales=None, split_tokens=0, out=None, lse_out=None, workspace=None,
+                      max_total_ctx_tokens=None, dev_status=None, stream=None):
+    """One decode step of one layer: the page write of k_new/v_new
+    [n_seqs, n_new, Hkv, D] at start_pos (int8 pools: quantised) and paged
+    decode attention over ctx_lens tokens (which count the new rows), in one
+    call.  Returns out [n_seqs, Hq, D] bf16."""
+    lib = load_library()
+    dev = q.device
+    _need(q, "q", torch.bfloat16, 3, dev)
+    _need(k_new, "k_new", torch.bfloat16, 4, dev)
+    _need(v_new, "v_new", torch.bfloat16, 4, dev)
+    _need(start_pos, "start_pos", torch.int32, 1, dev)
+    int8 = k_pool.dtype == torch.int8
+    _need(k_pool, "k_pool", torch.int8 if int8 else torch.bfloat16, 4, dev)
+    _need(v_pool, "v_pool", torch.int8 if int8 else torch.bfloat16, 4, dev)
+    if int8:
+        _need(k_scales, "k_scales", torch.float32, 3, dev)
+        _need(v_scales, "v_scales", torch.float32, 3, dev)
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(ctx_lens, "ctx_lens", torch.int32, 1, dev)
+    n_seqs, n_q_heads, D = q.shape
+    if k_new.shape[0] != n_seqs:
+        raise ValueError("k_new and q disagree on n_seqs")
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, 3, dev)
+    if lse_out is not None:
+        _need(lse_out, "lse_out", torch.float32, 2, dev)
+    if workspace is None:
+        if max_total_ctx_tokens is None:
+            max_total_ctx_tokens = n_seqs * block_tables.shape[1] * k_pool.shape[1]
+        nbytes = decode_workspace_bytes(n_seqs, n_q_heads, D, max_total_ctx_tokens, split_tokens)
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    _need(workspace, "workspace", torch.uint8, 1, dev)
+    st = lib.paged_decode_step(_ptr(k_new), _ptr(v_new), _ptr(start_pos), k_new.shape[1], _ptr(q), n_q_heads,
+                               _ptr(k_pool), _ptr(v_pool), _ptr(k_scales), _ptr(v_scales),
+                               PKV_KV_INT8 if int8 else PKV_KV_BF16, pool_dims(k_pool), _ptr(block_tables),
+                               block_tables.shape[1], _ptr(ctx_lens), n_seqs, float(softmax_scale),
+                               int(split_tokens), _ptr(out), _ptr(lse_out), _ptr(workspace), workspace.numel(),
+                               _ptr(dev_status), _stream(stream))
+    _check("paged_decode_step", st)
     return out
 
 

@@ -205,19 +205,19 @@ size_t pkv_decode_workspace_bytes(int32_t n_seqs, int32_t n_q_heads, int32_t hea
                                   (int64_t)decode_capacity_for(n_seqs, max_total_ctx_tokens, split_tokens));
 }
 
-int paged_decode_attention(const pkv_bf16 *q, int32_t n_q_heads, const void *k_pool, const void *v_pool,
-                           const float *k_scales, const float *v_scales, int32_t kv_dtype, pkv_dims dims,
-                           const int32_t *block_tables, int32_t max_blocks, const int32_t *ctx_lens,
-                           int32_t n_seqs, float softmax_scale, int32_t split_tokens, pkv_bf16 *out,
-                           float *lse_out, void *workspace, size_t workspace_bytes, int32_t *dev_status,
-                           pkv_stream_t stream)
+// Host checks of a decode call; on success fills *a (workspace carved).
+static int prepare_decode(const pkv_bf16 *q, int32_t n_q_heads, const void *k_pool, const void *v_pool,
+                          const float *k_scales, const float *v_scales, int32_t kv_dtype, const pkv_dims &dims,
+                          const int32_t *block_tables, int32_t max_blocks, const int32_t *ctx_lens, int32_t n_seqs,
+                          float softmax_scale, int32_t split_tokens, pkv_bf16 *out, float *lse_out,
+                          void *workspace, size_t workspace_bytes, int32_t *dev_status, DecodeArgs *a)
 {
     int st = check_dims(dims);
     if (st != PKV_OK) return st;
     if (n_seqs < 0 || n_q_heads <= 0 || max_blocks <= 0 || split_tokens < 0) return PKV_ERR_INVALID_ARG;
     if (n_q_heads % dims.n_kv_heads != 0) return PKV_ERR_INVALID_ARG;
     const int G = n_q_heads / dims.n_kv_heads;
-    if (G > 8) return PKV_ERR_UNSUPPORTED;
+    if (G > 8 || (G & (G - 1)) != 0) return PKV_ERR_UNSUPPORTED;
     if (kv_dtype != PKV_KV_BF16 && kv_dtype != PKV_KV_INT8) return PKV_ERR_UNSUPPORTED;
     if (split_tokens % 16 != 0) return PKV_ERR_UNSUPPORTED;
     if ((int64_t)max_blocks * dims.block_size > 0x7fffffffLL) return PKV_ERR_OUT_OF_RANGE;
@@ -228,30 +228,68 @@ int paged_decode_attention(const pkv_bf16 *q, int32_t n_q_heads, const void *k_p
     if (kv_dtype == PKV_KV_INT8 && (!k_scales || !v_scales || !aligned16(k_scales) || !aligned16(v_scales)))
         return PKV_ERR_INVALID_ARG;
     if (!std::isfinite(softmax_scale)) return PKV_ERR_INVALID_ARG;
-    DecodeArgs a{};
-    if (!carve_decode_workspace(workspace, workspace_bytes, n_seqs, n_q_heads, dims.head_dim, &a.ws))
+    if (!carve_decode_workspace(workspace, workspace_bytes, n_seqs, n_q_heads, dims.head_dim, &a->ws))
         return PKV_ERR_WORKSPACE;
+    a->q = q;
+    a->n_q_heads = n_q_heads;
+    a->k_pool = k_pool;
+    a->v_pool = v_pool;
+    a->k_scales = k_scales;
+    a->v_scales = v_scales;
+    a->kv_dtype = kv_dtype;
+    a->dims = dims;
+    a->tables = block_tables;
+    a->max_blocks = max_blocks;
+    a->ctx_lens = ctx_lens;
+    a->n_seqs = n_seqs;
+    a->softmax_scale = softmax_scale;
+    a->split_tokens = split_tokens;
+    a->out = out;
+    a->lse_out = lse_out;
+    a->dev_status = dev_status;
+    return PKV_OK;
+}
+
+int paged_decode_attention(const pkv_bf16 *q, int32_t n_q_heads, const void *k_pool, const void *v_pool,
+                           const float *k_scales, const float *v_scales, int32_t kv_dtype, pkv_dims dims,
+                           const int32_t *block_tables, int32_t max_blocks, const int32_t *ctx_lens,
+                           int32_t n_seqs, float softmax_scale, int32_t split_tokens, pkv_bf16 *out,
+                           float *lse_out, void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                           pkv_stream_t stream)
+{
+    DecodeArgs a{};
+    int st = prepare_decode(q, n_q_heads, k_pool, v_pool, k_scales, v_scales, kv_dtype, dims, block_tables,
+                            max_blocks, ctx_lens, n_seqs, softmax_scale, split_tokens, out, lse_out, workspace,
+                            workspace_bytes, dev_status, &a);
+    if (st != PKV_OK || n_seqs == 0) return st;
     int sms = 0;
     st = num_sms_of_current_device(&sms);
     if (st != PKV_OK) return st;
-    a.q = q;
-    a.n_q_heads = n_q_heads;
-    a.k_pool = k_pool;
-    a.v_pool = v_pool;
-    a.k_scales = k_scales;
-    a.v_scales = v_scales;
-    a.kv_dtype = kv_dtype;
-    a.dims = dims;
-    a.tables = block_tables;
-    a.max_blocks = max_blocks;
-    a.ctx_lens = ctx_lens;
-    a.n_seqs = n_seqs;
-    a.softmax_scale = softmax_scale;
-    a.split_tokens = split_tokens;
-    a.out = out;
-    a.lse_out = lse_out;
-    a.dev_status = dev_status;
     return cuda_status(launch_decode(a, sms, (cudaStream_t)stream));
+}
+
+int paged_decode_step(const pkv_bf16 *k_new, const pkv_bf16 *v_new, const int32_t *start_pos, int32_t n_new,
+                      const pkv_bf16 *q, int32_t n_q_heads, void *k_pool, void *v_pool, float *k_scales,
+                      float *v_scales, int32_t kv_dtype, pkv_dims dims, const int32_t *block_tables,
+                      int32_t max_blocks, const int32_t *ctx_lens, int32_t n_seqs, float softmax_scale,
+                      int32_t split_tokens, pkv_bf16 *out, float *lse_out, void *workspace,
+                      size_t workspace_bytes, int32_t *dev_status, pkv_stream_t stream)
+{
+    int st = write_common_checks(k_new, v_new, k_pool, v_pool, dims, block_tables, max_blocks, start_pos, n_seqs,
+                                 n_new);
+    if (st != PKV_OK) return st;
+    DecodeArgs a{};
+    st = prepare_decode(q, n_q_heads, k_pool, v_pool, k_scales, v_scales, kv_dtype, dims, block_tables, max_blocks,
+                        ctx_lens, n_seqs, softmax_scale, split_tokens, out, lse_out, workspace, workspace_bytes,
+                        dev_status, &a);
+    if (st != PKV_OK || n_seqs == 0) return st;
+    a.write_k_scales = k_scales;
+    a.write_v_scales = v_scales;
+    WriteArgs w{k_new, v_new, k_pool, v_pool, dims, block_tables, max_blocks, start_pos, n_seqs, n_new, dev_status};
+    int sms = 0;
+    st = num_sms_of_current_device(&sms);
+    if (st != PKV_OK) return st;
+    return cuda_status(launch_decode(a, sms, (cudaStream_t)stream, &w));
 }
 
 int paged_prefill_attention(const pkv_bf16 *q, int32_t n_q_heads, const pkv_bf16 *k_pool, const pkv_bf16 *v_pool,

@@ -37,6 +37,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "write_rows.cuh"
 
 namespace pkv {
 
@@ -171,16 +172,33 @@ __device__ int32_t block_exclusive_scan(int32_t v, int32_t *total, int32_t *scra
     return r;
 }
 
+// CTA 0 plans; in the fused decode step, CTAs 1.. also write this step's new
+// K/V rows into the pool (write_mode 1: bf16 copy, 2: int8 quantisation), so
+// the split kernel, which waits for this whole grid, reads them.
 __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t *__restrict__ ctx_lens,
                                                            int32_t n_seqs, int32_t split_tokens,
                                                            int32_t max_tokens, int32_t n_q_heads,
                                                            int32_t head_dim, int32_t n_kv_heads,
                                                            int32_t items_target, DecodeWorkspace ws,
                                                            __nv_bfloat16 *out, float *lse_out,
-                                                           int32_t *dev_status)
+                                                           int32_t *dev_status, const WriteArgs w, int32_t write_mode,
+                                                           float *k_scales, float *v_scales)
 {
     __shared__ int32_t scratch[33];
     grid_dependents_launch();   // the split kernel may start; it waits for this grid's results
+    if (blockIdx.x > 0) {
+        const int64_t wb = blockIdx.x - 1, nwb = gridDim.x - 1;
+        if (write_mode == 1) {
+            write_bf16_vectors(w, wb * blockDim.x + threadIdx.x, nwb * blockDim.x);
+        } else if (write_mode == 2) {
+            const int64_t warps = blockDim.x >> 5;
+            if (head_dim == 128)
+                write_int8_units<4>(w, k_scales, v_scales, wb * warps + (threadIdx.x >> 5), nwb * warps);
+            else
+                write_int8_units<2>(w, k_scales, v_scales, wb * warps + (threadIdx.x >> 5), nwb * warps);
+        }
+        return;
+    }
     const int tid = threadIdx.x;
     const bool balanced = split_tokens == 0;
     const int32_t unit = balanced ? kStageTokens : split_tokens;
@@ -202,8 +220,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t *__rest
             if (balanced) {
                 ws.seq_prefix[s] = ex;
             } else {
-                ws.seg_base[s] = ex;
-                ws.n_seg[s] = n;
+                ws.seg[s] = make_int2(ex, n);
                 for (int32_t k = 0; k < n; ++k)
                     if (ex + k < ws.capacity) ws.items[ex + k] = make_int2(s, k);
             }
@@ -239,8 +256,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t *__rest
             int32_t tot;
             const int32_t ex = running + block_exclusive_scan(n, &tot, scratch);
             if (s < n_seqs) {
-                ws.seg_base[s] = ex;
-                ws.n_seg[s] = n;
+                ws.seg[s] = make_int2(ex, n);
                 // items whose first stage lies in this sequence start with it
                 for (int32_t i = (pre + chunk - 1) / max(chunk, 1); st > 0 && i * chunk < pre + st; ++i)
                     ws.items[i] = make_int2(s, 0);
@@ -257,15 +273,16 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t *__rest
         ws.header[kHdrCounter] = 0u;
     }
     // Sequences no piece will cover (empty or invalid context, or every
-    // sequence when the work list overflowed) get o = 0 and lse = -inf here.
-    for (int32_t s = 0; s < n_seqs; ++s) {
+    // sequence when the work list overflowed) get o = 0 and lse = -inf here,
+    // one thread per such sequence.
+    for (int32_t s = tid; s < n_seqs; s += blockDim.x) {
         const int32_t ctx = ctx_lens[s];
         if (!overflow && ctx > 0 && ctx <= max_tokens) continue;
         const int64_t row = (int64_t)s * n_q_heads;
-        for (int32_t i = tid; i < n_q_heads * head_dim; i += blockDim.x)
-            out[row * head_dim + i] = __float2bfloat16_rn(0.f);
+        uint4 *o = reinterpret_cast<uint4 *>(out + row * head_dim);
+        for (int32_t i = 0; i < n_q_heads * head_dim / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
         if (lse_out)
-            for (int32_t i = tid; i < n_q_heads; i += blockDim.x) lse_out[row + i] = -INFINITY;
+            for (int32_t i = 0; i < n_q_heads; ++i) lse_out[row + i] = -INFINITY;
     }
 }
 
@@ -288,11 +305,9 @@ __device__ __forceinline__ void merge_pieces(const float2 *part_ml, const float 
     constexpr int BATCH = EPL >= 32 ? 2 : (EPL >= 16 ? 4 : 8);
     const int n = lane / LPH, sub = lane % LPH;
     const int64_t hrow = hbase + n;
+    // one pass with a running maximum: every load of a batch is in flight
+    // before any is used, and no separate pass over the maxima is needed
     float M = -INFINITY;
-    for (int32_t k = sub; k < n_pieces; k += LPH)
-        M = fmaxf(M, __ldcg(&part_ml[(int64_t)(base + k) * n_q_heads + hrow]).x);
-#pragma unroll
-    for (int off = 1; off < LPH; off <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     float o[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) o[e] = 0.f;
@@ -324,11 +339,13 @@ __device__ __forceinline__ void merge_pieces(const float2 *part_ml, const float 
         }
 #pragma unroll
         for (int i = 0; i < BATCH; ++i) {
-            if (k0 + i < n_pieces) {
-                const float w = M == -INFINITY ? 0.f : exp2f(ml[i].x - M);
-                Lsum += ml[i].y * w;
+            if (k0 + i < n_pieces && ml[i].x != -INFINITY) {
+                const float Mn = fmaxf(M, ml[i].x);
+                const float keep = exp2f(M - Mn), w = exp2f(ml[i].x - Mn);
+                Lsum = Lsum * keep + ml[i].y * w;
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) o[e] += a[i][e] * w;
+                for (int e = 0; e < EPL; ++e) o[e] = o[e] * keep + a[i][e] * w;
+                M = Mn;
             }
         }
     }
@@ -353,9 +370,9 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(DecodeWorkspace ws, i
     const int64_t idx = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (idx >= (int64_t)n_seqs * n_kv_heads) return;
     const int32_t s = (int32_t)(idx / n_kv_heads), kvh = (int32_t)(idx % n_kv_heads);
-    const int32_t n = ws.n_seg[s];
-    if (n < 2 || ws.header[kHdrOverflow] != 0) return;
-    merge_pieces<D, EPL>(ws.part_ml, ws.part_acc, out, lse_out, n_q_heads, s, kvh * group, ws.seg_base[s], n, lane);
+    const int2 sg = ws.seg[s];
+    if (sg.y < 2 || ws.header[kHdrOverflow] != 0) return;
+    merge_pieces<D, EPL>(ws.part_ml, ws.part_acc, out, lse_out, n_q_heads, s, kvh * group, sg.x, sg.y, lane);
 }
 
 // TMA copies of one 16-token stage (K and V tiles of hpc kv heads, int8 scales)
@@ -480,8 +497,9 @@ __global__ void __launch_bounds__(288, 1) decode_split_kernel(const __grid_const
                     seq = s;
                     t0 = (g0 - pre) * kStageTokens;
                     t1 = min((e - pre) * kStageTokens, __ldg(p.ctx_lens + s));
-                    slot = __ldg(p.ws.seg_base + s) + (item - pre / chunk);
-                    n_pieces = __ldg(p.ws.n_seg + s);
+                    const int2 sg = __ldg(p.ws.seg + s);
+                    slot = sg.x + (item - pre / chunk);
+                    n_pieces = sg.y;
                     g0 = e;
                     ++s;
                     more = g0 < g1;
@@ -490,7 +508,7 @@ __global__ void __launch_bounds__(288, 1) decode_split_kernel(const __grid_const
                     t0 = fixed_sk.y * p.split_tokens;
                     t1 = min(t0 + p.split_tokens, __ldg(p.ctx_lens + seq));
                     slot = item;
-                    n_pieces = __ldg(p.ws.n_seg + seq);
+                    n_pieces = __ldg(&p.ws.seg[seq].y);
                     more = false;
                 }
                 const bool final_out = n_pieces == 1;
@@ -869,7 +887,7 @@ size_t decode_workspace_bytes(int32_t n_seqs, int32_t n_q_heads, int32_t head_di
 {
     size_t b = 256;                                                    // header
     b += align_up((size_t)(n_seqs + 1) * sizeof(int32_t), 256);        // seq_prefix
-    b += 2 * align_up((size_t)n_seqs * sizeof(int32_t), 256);          // seg_base, n_seg
+    b += align_up((size_t)n_seqs * sizeof(int2), 256);                 // seg
     b += align_up((size_t)capacity * sizeof(int2), 256);               // items
     b += align_up((size_t)capacity * n_q_heads * sizeof(float2), 256);
     b += align_up((size_t)capacity * n_q_heads * head_dim * sizeof(float), 256);
@@ -891,10 +909,8 @@ bool carve_decode_workspace(void *ws, size_t bytes, int32_t n_seqs, int32_t n_q_
     p += 256;
     out->seq_prefix = reinterpret_cast<int32_t *>(p);
     p += align_up((size_t)(n_seqs + 1) * sizeof(int32_t), 256);
-    out->seg_base = reinterpret_cast<int32_t *>(p);
-    p += align_up((size_t)n_seqs * sizeof(int32_t), 256);
-    out->n_seg = reinterpret_cast<int32_t *>(p);
-    p += align_up((size_t)n_seqs * sizeof(int32_t), 256);
+    out->seg = reinterpret_cast<int2 *>(p);
+    p += align_up((size_t)n_seqs * sizeof(int2), 256);
     out->items = reinterpret_cast<int2 *>(p);
     p += align_up((size_t)cap * sizeof(int2), 256);
     out->part_ml = reinterpret_cast<float2 *>(p);
@@ -941,7 +957,7 @@ int encode_pool_map(CUtensorMap *map, const void *pool, CUtensorMapDataType dt, 
 }
 
 template <int D, bool INT8>
-cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream)
+cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream, const WriteArgs *write)
 {
     const pkv_dims &d = a.dims;
     const int G = a.n_q_heads / d.n_kv_heads;
@@ -1033,9 +1049,20 @@ cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream)
     if (items_per_cta < 1 || items_per_cta > 16) items_per_cta = 1;
     const int items_target = (grid * items_per_cta + p.n_hg - 1) / p.n_hg;
     const int32_t max_tokens = a.max_blocks * d.block_size;
-    decode_plan_kernel<<<1, 1024, 0, stream>>>(a.ctx_lens, a.n_seqs, a.split_tokens, max_tokens, a.n_q_heads, D,
-                                               d.n_kv_heads, items_target, a.ws, (__nv_bfloat16 *)a.out,
-                                               a.lse_out, a.dev_status);
+    // the fused step's write runs in extra CTAs of the plan launch
+    int write_mode = 0, write_ctas = 0;
+    WriteArgs wa{};
+    if (write && write->n_seqs > 0 && write->n_new > 0) {
+        wa = *write;
+        write_mode = INT8 ? 2 : 1;
+        const int64_t units = INT8 ? (int64_t)wa.n_seqs * wa.n_new * d.n_kv_heads * 2 / 32
+                                   : (int64_t)wa.n_seqs * wa.n_new * (d.n_kv_heads * D / 8) / 1024;
+        write_ctas = (int)(units < 1 ? 1 : (units > 2 * num_sms ? 2 * num_sms : units));
+    }
+    decode_plan_kernel<<<1 + write_ctas, 1024, 0, stream>>>(a.ctx_lens, a.n_seqs, a.split_tokens, max_tokens,
+                                                            a.n_q_heads, D, d.n_kv_heads, items_target, a.ws,
+                                                            (__nv_bfloat16 *)a.out, a.lse_out, a.dev_status, wa,
+                                                            write_mode, a.write_k_scales, a.write_v_scales);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     cudaLaunchAttribute pdl[1];
@@ -1069,12 +1096,13 @@ cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream)
 
 }  // namespace
 
-cudaError_t launch_decode(const DecodeArgs &a, int num_sms, cudaStream_t stream)
+cudaError_t launch_decode(const DecodeArgs &a, int num_sms, cudaStream_t stream, const WriteArgs *write)
 {
     const bool int8 = a.kv_dtype == PKV_KV_INT8;
     if (a.dims.head_dim == 128)
-        return int8 ? launch_split<128, true>(a, num_sms, stream) : launch_split<128, false>(a, num_sms, stream);
-    return int8 ? launch_split<64, true>(a, num_sms, stream) : launch_split<64, false>(a, num_sms, stream);
+        return int8 ? launch_split<128, true>(a, num_sms, stream, write)
+                    : launch_split<128, false>(a, num_sms, stream, write);
+    return int8 ? launch_split<64, true>(a, num_sms, stream, write) : launch_split<64, false>(a, num_sms, stream, write);
 }
 
 }  // namespace pkv

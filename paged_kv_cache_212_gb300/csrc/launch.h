@@ -35,16 +35,14 @@ struct GatherArgs {
 // Decode workspace layout (all offsets 256-byte aligned):
 //   header     : uint32 [64]        work counter, items, overflow flag, stages per item, total stages
 //   seq_prefix : int32 [n_seqs + 1] 16-token stages before each sequence (balanced mode)
-//   seg_base   : int32 [n_seqs]     first partial slot of each sequence
-//   n_seg      : int32 [n_seqs]     pieces (partial slots) of each sequence
+//   seg        : int2  [n_seqs]     (first partial slot, pieces) of each sequence
 //   items      : int2  [cap]        fixed splits: (sequence, split) per item; balanced: first sequence
 //   part_ml    : float2[cap][Hq]    (running max in log2 units, running sum)
 //   part_acc   : float [cap][Hq][D] unnormalised partial outputs
 struct DecodeWorkspace {
     uint32_t *header;
     int32_t *seq_prefix;
-    int32_t *seg_base;
-    int32_t *n_seg;
+    int2 *seg;
     int2 *items;
     float2 *part_ml;
     float *part_acc;
@@ -77,6 +75,7 @@ struct DecodeArgs {
     float *lse_out;
     DecodeWorkspace ws;
     int32_t *dev_status;
+    float *write_k_scales, *write_v_scales;  // int8 pools of a fused decode step
 };
 
 struct PrefillArgs {
@@ -98,7 +97,9 @@ cudaError_t launch_write_bf16(const WriteArgs &a, cudaStream_t stream);
 cudaError_t launch_write_int8(const WriteArgs &a, float *k_scales, float *v_scales,
                               cudaStream_t stream);
 cudaError_t launch_gather(const GatherArgs &a, int num_sms, cudaStream_t stream);
-cudaError_t launch_decode(const DecodeArgs &a, int num_sms, cudaStream_t stream);
+// write (nullable): this step's new rows, written by the first launch of the
+// decode (the fused decode step).
+cudaError_t launch_decode(const DecodeArgs &a, int num_sms, cudaStream_t stream, const WriteArgs *write = nullptr);
 cudaError_t launch_prefill(const PrefillArgs &a, int num_sms, cudaStream_t stream);
 
 // Driver entry point for tensor-map encoding (resolved once through cudart,

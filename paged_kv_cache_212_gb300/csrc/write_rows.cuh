@@ -1,0 +1,124 @@
+// write_rows.cuh -- the page-write work (bf16 copy and int8 quantisation) as
+// device functions over a flat index space, shared by the stand-alone write
+// kernels and by the fused decode step, which runs the write in the same launch
+// as its plan.
+#pragma once
+
+#include "common.cuh"
+#include "launch.h"
+
+namespace pkv {
+
+// Pool row of token t of the sequence whose table row is `table_row`, or -1
+// (and a status bit) when the block is outside the table or the id outside
+// [0, n_blocks].  tiny-llm paged_kv.py, module docstring: token t lives at
+// (table[t // block_size], t % block_size).
+__device__ __forceinline__ int64_t pool_row_of(const int32_t *table_row, int32_t max_blocks,
+                                               int32_t n_blocks, int32_t block_size, int64_t t,
+                                               int32_t *dev_status)
+{
+    if (t < 0 || t / block_size >= max_blocks) {
+        report(dev_status, PKV_DEV_BAD_POSITION);
+        return -1;
+    }
+    const int32_t b = __ldg(table_row + t / block_size);
+    if (b < 0 || b > n_blocks) {
+        report(dev_status, PKV_DEV_BAD_BLOCK_ID);
+        return -1;
+    }
+    return (int64_t)b * block_size + t % block_size;
+}
+
+// Native bf16 write: 16-byte vector i of the [n_seqs * n_new rows][Hkv * D]
+// new K and V rows goes to the same vector of its token's pool row.  Threads
+// take vectors first, first + stride, ...; a bad row is reported once (by the
+// thread holding its first vector) and skipped.
+__device__ __forceinline__ void write_bf16_vectors(const WriteArgs &a, int64_t first, int64_t stride)
+{
+    const int32_t row_vecs = a.dims.n_kv_heads * a.dims.head_dim / 8;
+    const int64_t n_vecs = (int64_t)a.n_seqs * a.n_new * row_vecs;
+    const uint4 *k_new = static_cast<const uint4 *>(a.k_new);
+    const uint4 *v_new = static_cast<const uint4 *>(a.v_new);
+    uint4 *k_pool = static_cast<uint4 *>(a.k_pool);
+    uint4 *v_pool = static_cast<uint4 *>(a.v_pool);
+    for (int64_t i = first; i < n_vecs; i += stride) {
+        const int64_t r = i / row_vecs;
+        const int32_t v = (int32_t)(i - r * row_vecs);
+        const int64_t s = r / a.n_new;
+        const int64_t t = (int64_t)__ldg(a.start_pos + s) + (r - s * a.n_new);
+        const int64_t row = pool_row_of(a.tables + s * a.max_blocks, a.max_blocks, a.dims.n_blocks,
+                                        a.dims.block_size, t, v == 0 ? a.dev_status : nullptr);
+        if (row < 0) continue;
+        const uint4 kx = __ldcs(k_new + i);
+        const uint4 vx = __ldcs(v_new + i);
+        k_pool[row * row_vecs + v] = kx;
+        v_pool[row * row_vecs + v] = vx;
+    }
+}
+
+// Symmetric int8 quantisation, one (token, kv head, K or V) row per warp, in
+// IEEE binary32 with round-to-nearest-even (libmir-metal paged/mod.rs,
+// KvPageFormat::Int8PerTokenHead): amax by a warp max-reduction, scale =
+// amax / 127 (correctly rounded division), code = clamp(rint(x / scale),
+// -127, 127).  Warps take units first, first + stride, ...; EPL = head_dim / 32.
+template <int EPL>
+__device__ __forceinline__ void write_int8_units(const WriteArgs &a, float *k_scales, float *v_scales,
+                                                 int64_t first, int64_t stride)
+{
+    constexpr int D = EPL * 32;
+    const int lane = threadIdx.x & 31;
+    const int32_t hkv = a.dims.n_kv_heads;
+    const int64_t n_units = (int64_t)a.n_seqs * a.n_new * hkv * 2;
+    // unit = ((s * n_new + j) * n_kv_heads + h) * 2 + (0: K, 1: V)
+    for (int64_t u = first; u < n_units; u += stride) {
+        const int which = (int)(u & 1);
+        const int64_t rh = u >> 1;
+        const int32_t h = (int32_t)(rh % hkv);
+        const int64_t r = rh / hkv;
+        const int64_t s = r / a.n_new;
+        const int64_t t = (int64_t)__ldg(a.start_pos + s) + (r - s * a.n_new);
+        const int64_t row = pool_row_of(a.tables + s * a.max_blocks, a.max_blocks, a.dims.n_blocks,
+                                        a.dims.block_size, t, lane == 0 && which == 0 && h == 0 ? a.dev_status : nullptr);
+        if (row < 0) continue;
+        const __nv_bfloat16 *src = static_cast<const __nv_bfloat16 *>(which ? a.v_new : a.k_new) + rh * D + lane * EPL;
+        float x[EPL];
+        if constexpr (EPL == 4) {
+            uint2 raw = __ldcs(reinterpret_cast<const uint2 *>(src));
+            __nv_bfloat162 p0 = *reinterpret_cast<__nv_bfloat162 *>(&raw.x);
+            __nv_bfloat162 p1 = *reinterpret_cast<__nv_bfloat162 *>(&raw.y);
+            x[0] = __low2float(p0);
+            x[1] = __high2float(p0);
+            x[2] = __low2float(p1);
+            x[3] = __high2float(p1);
+        } else {
+            uint32_t raw = __ldcs(reinterpret_cast<const unsigned int *>(src));
+            __nv_bfloat162 p0 = *reinterpret_cast<__nv_bfloat162 *>(&raw);
+            x[0] = __low2float(p0);
+            x[1] = __high2float(p0);
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) amax = fmaxf(amax, fabsf(x[e]));
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        const float scale = __fdiv_rn(amax, 127.0f);
+        uint32_t packed = 0;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+            int c = 0;
+            if (amax != 0.0f) {
+                c = __float2int_rn(__fdiv_rn(x[e], scale));
+                c = max(-127, min(127, c));
+            }
+            packed |= (uint32_t)(c & 0xff) << (8 * e);
+        }
+        int8_t *dst = static_cast<int8_t *>(which ? a.v_pool : a.k_pool) + (row * hkv + h) * D + lane * EPL;
+        if constexpr (EPL == 4)
+            *reinterpret_cast<uint32_t *>(dst) = packed;
+        else
+            *reinterpret_cast<uint16_t *>(dst) = (uint16_t)packed;
+        if (lane == 0) (which ? v_scales : k_scales)[row * hkv + h] = scale;
+    }
+}
+
+}  // namespace pkv

@@ -139,3 +139,32 @@ def test_decode_workspace_sizing(lib):
     # capacity grows with the number of splits: ceil(total / split) + n_seqs partial rows
     per_split = 8 + 32 * 8 + 32 * 128 * 4
     assert f(64, 32, 128, 150_000 + 512 * 100, 512) - small >= 100 * per_split - 4 * 256
+
+
+def test_binding_declares_every_signature(lib):
+    """Each exported call has argtypes and an int status return in the binding."""
+    from paged_kv_cache_212_gb300 import EXPORTS
+    for n in EXPORTS:
+        fn = getattr(lib, n)
+        assert fn.argtypes is not None, n
+    for n in ("paged_kv_write", "paged_kv_write_int8", "paged_kv_gather", "paged_decode_attention",
+              "paged_prefill_attention", "paged_decode_attention_noalloc", "paged_decode_step"):
+        assert getattr(lib, n).restype is ctypes.c_int, n
+
+
+def test_decode_step_argument_checks(lib):
+    import paged_kv_cache_212_gb300 as P
+    d = _dims(P, hkv=2)
+    f = lib.paged_decode_step
+    base = [FAKE, FAKE, FAKE, 1, FAKE, 8, FAKE, FAKE, None, None, 0, d, FAKE, 4, FAKE, 2, 0.125, 0, FAKE, None,
+            FAKE, 1 << 20, None, None]
+    args = list(base); args[15] = 0
+    assert f(*args) == 0                           # no sequences: nothing to do
+    args = list(base); args[0] = None
+    assert f(*args) == 1                           # the write's checks apply
+    args = list(base); args[3] = 65
+    assert f(*args) == 3                           # more new rows than a table row holds
+    args = list(base); args[5] = 7
+    assert f(*args) == 1                           # the decode's checks apply
+    args = list(base); args[20] = None
+    assert f(*args) == 4

@@ -392,3 +392,51 @@ def test_prefill_identity_vs_permuted_tables_bit_exact(P):
     t2 = torch.from_numpy(move[w.tables.numpy()]).to(torch.int32)
     out2, lse2, _ = run_prefill(P, w, kp2, vp2, tables=t2)
     assert torch.equal(out.view(torch.int16), out2.view(torch.int16)) and torch.equal(lse, lse2)
+
+
+# ---------------------------------------------------------------------------
+# the fused decode step: write + decode in one call
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["cfg0", "cfg1", "cfg2", "ragged_d64", "int8_small"])
+def test_fused_decode_step(P, name):
+    """paged_decode_step = paged_kv_write(_int8) then paged_decode_attention:
+    the pool bit-exact with the oracle's write, the output identical bit for
+    bit to the two-call path and within tolerance of the oracle."""
+    w = workload(name)
+    kp, vp, ks, vs = pools(name, after_step=False)
+    tables, start, ctx = i32(w.tables), i32(w.start_pos), i32(w.ctx_lens)
+    q, kn, vn = w.q.cuda(), w.k_new.cuda(), w.v_new.cuda()
+    int8 = w.kv_format == "int8"
+    # fused
+    gk, gv = dev(kp), dev(vp)
+    gks, gvs = (dev(ks), dev(vs)) if int8 else (None, None)
+    st = status_tensor()
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
+    out = P.paged_decode_step(kn, vn, start, q, gk, gv, tables, ctx, w.softmax_scale, k_scales=gks, v_scales=gvs,
+                              lse_out=lse, dev_status=st)
+    # two calls
+    gk2, gv2 = dev(kp), dev(vp)
+    if int8:
+        gks2, gvs2 = dev(ks), dev(vs)
+        P.paged_kv_write_int8(kn, vn, gk2, gv2, gks2, gvs2, tables, start)
+    else:
+        gks2 = gvs2 = None
+        P.paged_kv_write(kn, vn, gk2, gv2, tables, start)
+    lse2 = torch.empty_like(lse)
+    out2 = P.paged_decode_attention(q, gk2, gv2, tables, ctx, w.softmax_scale, k_scales=gks2, v_scales=gvs2,
+                                    lse_out=lse2)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    rk, rv, rks, rvs = pools(name, after_step=True)
+    assert np.array_equal(host(gk), rk) and np.array_equal(host(gv), rv)
+    if int8:
+        assert np.array_equal(host(gks).view(np.uint32), rks.view(np.uint32))
+        assert np.array_equal(host(gvs).view(np.uint32), rvs.view(np.uint32))
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16)) and torch.equal(lse, lse2)
+    ref, _ = oracle_decode(w, rk, rv, rks, rvs)
+    mx, mean = attention_errors(out, ref)
+    if int8:
+        assert mx <= INT8_MAX, mx
+    else:
+        assert mx <= BF16_MAX and mean <= BF16_MEAN, (mx, mean)
