@@ -394,7 +394,6 @@ def main():
 
     # ---- timed region: K steps, events around every decode call ----
     K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     uuid = None
     try:
@@ -406,17 +405,17 @@ def main():
     torch.cuda.synchronize()
     with ClockSampler(uuid) as clk:
         time.sleep(0.25)  # let the sampler start before the timed work
+        # one step is one paged_decode_step call; events bracket the K calls on
+        # their stream (no events in between, which would break the launch chaining)
         t_start.record(stream)
         for i in range(K):
-            ev[i][0].record(stream)
             step()
-            ev[i][1].record(stream)
         t_end.record(stream)
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
     elapsed_ms = t_start.elapsed_time(t_end)
-    decode_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    decode_ms = elapsed_ms / K
     if world > 1:
         tt = torch.tensor([elapsed_ms, decode_ms], dtype=torch.float64, device=device)
         dist.all_reduce(tt, op=dist.ReduceOp.MAX)

@@ -186,6 +186,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t *__rest
 {
     __shared__ int32_t scratch[33];
     grid_dependents_launch();   // the split kernel may start; it waits for this grid's results
+    grid_dependency_wait();     // launched as a dependent of the previous kernel: wait for its results
     if (blockIdx.x > 0) {
         const int64_t wb = blockIdx.x - 1, nwb = gridDim.x - 1;
         if (write_mode == 1) {
@@ -365,6 +366,7 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(DecodeWorkspace ws, i
                                                            int32_t n_q_heads, int32_t group, __nv_bfloat16 *out,
                                                            float *lse_out)
 {
+    grid_dependents_launch();   // the next step's plan may start; it waits for this grid
     grid_dependency_wait();
     const int lane = threadIdx.x & 31;
     const int64_t idx = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -1059,15 +1061,21 @@ cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream, 
                                    : (int64_t)wa.n_seqs * wa.n_new * (d.n_kv_heads * D / 8) / 1024;
         write_ctas = (int)(units < 1 ? 1 : (units > 2 * num_sms ? 2 * num_sms : units));
     }
-    decode_plan_kernel<<<1 + write_ctas, 1024, 0, stream>>>(a.ctx_lens, a.n_seqs, a.split_tokens, max_tokens,
-                                                            a.n_q_heads, D, d.n_kv_heads, items_target, a.ws,
-                                                            (__nv_bfloat16 *)a.out, a.lse_out, a.dev_status, wa,
-                                                            write_mode, a.write_k_scales, a.write_v_scales);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+    // all three launches are programmatic dependents of their predecessor on
+    // the stream; each waits (griddepcontrol.wait) before touching memory
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t pc{};
+    pc.gridDim = dim3((unsigned)(1 + write_ctas));
+    pc.blockDim = dim3(1024);
+    pc.stream = stream;
+    pc.attrs = pdl;
+    pc.numAttrs = 1;
+    e = cudaLaunchKernelEx(&pc, decode_plan_kernel, a.ctx_lens, a.n_seqs, a.split_tokens, max_tokens, a.n_q_heads,
+                           (int32_t)D, d.n_kv_heads, (int32_t)items_target, a.ws, (__nv_bfloat16 *)a.out, a.lse_out,
+                           a.dev_status, wa, (int32_t)write_mode, a.write_k_scales, a.write_v_scales);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t lc{};
     lc.gridDim = dim3((unsigned)grid);
     lc.blockDim = dim3((unsigned)threads);
