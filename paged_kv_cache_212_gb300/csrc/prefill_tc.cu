@@ -1,20 +1,28 @@
 // prefill_tc.cu -- chunked paged prefill attention on the 5th-generation tensor
 // cores (tcgen05 + TMEM), for head_dim 64 / 128 and GQA groups of 1..16.
 //
-// CTA = (sequence, kv head, tile of 128 query rows).  The rows of a tile pack
-// the G query heads of the kv head: row r is (chunk position p0 + r / G, query
-// head kvh * G + r % G), so each K/V tile serves all G heads.  Warp roles:
-//   warps 0-3  softmax: thread r owns query row r = TMEM lane r;
-//   warp 4     TMA producer: Q once, then K and V tiles of 128 keys, one
-//              {64 columns, 16 keys} box per 16-key group, addressed through
-//              the block table (groups past the last key read zeros);
-//   warp 5     TMEM allocator and MMA issuer (one elected lane).
-// Per key tile j:  S_j = Q K_j^T  (tcgen05.mma, M 128 x N 128, S in TMEM,
-// double-buffered), softmax in registers (log2 units, a stale row maximum is
-// kept unless it grows by more than 2^8, then the O row is rescaled in TMEM),
-// P_j (bf16) to shared memory, O += P_j V_j (tcgen05.mma, V read MN-major).
-// Query position P + p (P = prefix length) sees keys 0 .. P + p (metrale
-// impl_more.rs: a query at q_pos attends only slots <= q_pos of its block).
+// CTA = (sequence, kv head, two adjacent tiles of 128 query rows).  The rows of
+// a tile pack the G query heads of the kv head: row r is (chunk position
+// p0 + r / G, query head kvh * G + r % G), so every K/V tile serves 2 x 128
+// rows.  Warp roles (320 threads):
+//   warps 0-3, 4-7  softmax warpgroups of query tile 0 and 1: thread r of a
+//                   warpgroup owns row r of its tile (= TMEM lane r);
+//   warp 8          TMA producer: both Q tiles once, then K and V tiles of 64
+//                   keys into a 4-stage ring, one {64 columns, 1 head, 16 keys}
+//                   box per 16-key group and 64-column panel, addressed
+//                   through the block table (groups past the last key read the
+//                   zero fill of an out-of-range row);
+//   warp 9          TMEM allocator and MMA issuer (one lane).
+// TMEM (512 columns): per query tile, S double-buffered (2 x 64 columns) and
+// O (head_dim columns).  For key tile j and query tile i:
+//   S_ij = Q_i K_j^T (tcgen05.mma M 128, N 64), softmax in registers (log2
+//   units; a stale row maximum is kept unless it grows by more than 2^8, then
+//   the O row is rescaled in TMEM), P_ij (bf16) to shared memory, O_i += P_ij V_j
+//   (tcgen05.mma M 128, N head_dim, V read MN-major).
+// The MMA lane issues each product as soon as its inputs are ready, so one
+// warpgroup's softmax overlaps the other tile's products.  Query position
+// P + p (P = prefix length) sees keys 0 .. P + p (metrale impl_more.rs: a query
+// at q_pos attends only slots <= q_pos of its block).
 #include <math.h>
 
 #include "common.cuh"
@@ -24,10 +32,14 @@ namespace pkv {
 
 namespace {
 
-constexpr int kTM = 128;          // query rows per CTA (TMEM lanes)
-constexpr int kTN = 128;          // keys per tile
-constexpr int kKvStages = 2;
+constexpr int kTM = 128;           // query rows per tile (TMEM lanes)
+constexpr int kNQ = 2;             // query tiles per CTA
+constexpr int kTN = 64;            // keys per K/V tile
+constexpr int kStages = 4;         // K/V ring depth
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTileCols = 256;        // TMEM columns per query tile: S0, S1, O
+constexpr uint32_t kOCol = 128;            // O's column within a query tile's range
 
 struct PrefillTcParams {
     int32_t n_q_heads, group, chunk;
@@ -40,8 +52,8 @@ struct PrefillTcParams {
     __nv_bfloat16 *out;
     float *lse_out;
     int32_t *dev_status;
-    int32_t tiles_per_seq;
-    int32_t n_kv_heads;
+    int32_t tiles_per_seq;        // 128-row query tiles per (sequence, kv head)
+    int32_t pairs_per_seq;        // CTAs per (sequence, kv head)
 };
 
 // ---- tcgen05 helpers -------------------------------------------------------
@@ -87,24 +99,7 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar)
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// 32 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32])
-{
-    uint32_t r[32];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// Issue a load of 32 consecutive fp32 columns without waiting for it.
+// Issue a load of 32 consecutive fp32 columns of this thread's TMEM lane.
 __device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t *r)
 {
     asm volatile(
@@ -119,22 +114,15 @@ __device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t *r)
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32])
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *r)
 {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
         "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
-        "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-        "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-        "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-        "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-        "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-        "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
-        "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
-        "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
-        "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
-        "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
-        "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -147,46 +135,45 @@ __device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t chunk)
 }  // namespace
 
 template <int D>
-__global__ void __launch_bounds__(192, 1) prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
+__global__ void __launch_bounds__(320, 1) prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                                                             const __grid_constant__ CUtensorMap k_map,
                                                             const __grid_constant__ CUtensorMap v_map,
                                                             const PrefillTcParams p)
 {
-    constexpr int PANELS = D / 64;                    // 64-column (128-byte) panels of a bf16 row
-    constexpr uint32_t kQBytes = kTM * D * 2;         // 32 KiB at D 128
-    constexpr uint32_t kKBytes = kTN * D * 2;
-    constexpr uint32_t kPanelRows128 = 128u * 128u;   // one panel of 128 rows
-    constexpr uint32_t kStageBytes = 2 * kKBytes;     // K then V
-    constexpr uint32_t kPBytes = kTM * kTN * 2;       // P: 128 rows x 128 keys, 2 panels
-    constexpr uint32_t kTmemCols = 512;
-    constexpr uint32_t kOCol = 256;
+    constexpr int PANELS = D / 64;                          // 64-column (128-byte) panels of a bf16 row
+    constexpr uint32_t kQPanel = kTM * 128u;                // 16 KiB: one panel of a 128-row Q tile
+    constexpr uint32_t kQTile = PANELS * kQPanel;
+    constexpr uint32_t kKVPanel = kTN * 128u;               // 8 KiB: one panel of a 64-key tile
+    constexpr uint32_t kKTile = PANELS * kKVPanel;
+    constexpr uint32_t kStageBytes = 2 * kKTile;            // K then V
+    constexpr uint32_t kPTile = kTM * kTN * 2;              // 16 KiB: P of one query tile (one panel)
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *q_s = base;
-    uint8_t *kv_s = q_s + kQBytes;
-    uint8_t *p_s = kv_s + kKvStages * kStageBytes;   // after V: any descriptor overrun stays inside the CTA
-    uint64_t *bars = reinterpret_cast<uint64_t *>(p_s + kPBytes);
+    uint8_t *q_s = base;                                    // kNQ Q tiles
+    uint8_t *kv_s = q_s + kNQ * kQTile;                     // kStages x (K, V)
+    uint8_t *p_s = kv_s + kStages * kStageBytes;            // kNQ P tiles
+    uint64_t *bars = reinterpret_cast<uint64_t *>(p_s + kNQ * kPTile);
     uint64_t *q_full = bars + 0;
-    uint64_t *kv_full = bars + 1;                    // [2]
-    uint64_t *kv_empty = bars + 3;                   // [2]
-    uint64_t *s_full = bars + 5;                     // [2]
-    uint64_t *s_free = bars + 7;                     // [2]
-    uint64_t *p_full = bars + 9;
-    uint64_t *o_done = bars + 10;
-    uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(bars + 11);
-    volatile int32_t *abort_flag = reinterpret_cast<int32_t *>(bars + 12);
-    uint64_t *fin_bar = bars + 13;                  // all MMAs of this CTA retired
+    uint64_t *kv_full = bars + 1;                           // [kStages]
+    uint64_t *kv_empty = kv_full + kStages;                 // [kStages]
+    uint64_t *s_full = kv_empty + kStages;                  // [kNQ][2]
+    uint64_t *s_free = s_full + 2 * kNQ;                    // [kNQ][2]
+    uint64_t *p_full = s_free + 2 * kNQ;                    // [kNQ]
+    uint64_t *o_done = p_full + kNQ;                        // [kNQ]
+    uint64_t *fin_bar = o_done + kNQ;
+    uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(fin_bar + 1);
+    volatile int32_t *abort_flag = reinterpret_cast<int32_t *>(fin_bar + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int tiles = p.tiles_per_seq;
-    const int tile = tiles - 1 - (int)(blockIdx.x % tiles);   // heavy (late) tiles first
+    const int pairs = p.pairs_per_seq;
+    const int pair = pairs - 1 - (int)(blockIdx.x % pairs);   // heavy (late) tiles first
     const int kvh = blockIdx.y;
     const int s = blockIdx.z;
     const int G = p.group;
     const int pos_per_tile = kTM / G;
-    const int p0 = tile * pos_per_tile;
-    const int p_last = min(p0 + pos_per_tile, p.chunk) - 1;
+    const int p0 = pair * kNQ * pos_per_tile;
+    const int p_last = min(p0 + kNQ * pos_per_tile, p.chunk) - 1;
     const int32_t P = __ldg(p.prefix_lens + s);
     const int32_t n_keys = P + p_last + 1;
     const bool bad_len = P < 0 || (int64_t)n_keys > (int64_t)p.max_blocks * p.block_size;
@@ -194,20 +181,23 @@ __global__ void __launch_bounds__(192, 1) prefill_tc_kernel(const __grid_constan
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int i = 0; i < kKvStages; ++i) {
+        for (int i = 0; i < kStages; ++i) {
             mbar_init(&kv_full[i], 1);
             mbar_init(&kv_empty[i], 1);
+        }
+        for (int i = 0; i < 2 * kNQ; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&s_free[i], 4);
         }
-        mbar_init(p_full, 4);
-        mbar_init(o_done, 1);
+        for (int i = 0; i < kNQ; ++i) {
+            mbar_init(&p_full[i], 4);
+            mbar_init(&o_done[i], 1);
+        }
         mbar_init(fin_bar, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 5) {
-        // allocate TMEM: S double buffer (2 x 128 columns) + O (D columns), rounded to 512
+    if (warp == 9) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(tmem_base_s)),
                      "r"(kTmemCols)
                      : "memory");
@@ -219,26 +209,28 @@ __global__ void __launch_bounds__(192, 1) prefill_tc_kernel(const __grid_constan
     const uint32_t tmem = *tmem_base_s;
     if (bad_len && threadIdx.x == 0) report(p.dev_status, PKV_DEV_BAD_LENGTH);
 
-    if (warp == 4 && n_kt > 0) {
+    if (warp == 8 && n_kt > 0) {
         // ===================== TMA producer =====================
         if (lane == 0) {
             prefetch_tensormap(&q_map);
             prefetch_tensormap(&k_map);
             prefetch_tensormap(&v_map);
-            mbar_arrive_expect_tx(q_full, kQBytes);
-            for (int h = 0; h < PANELS; ++h)
-                tma_load_3d(q_s + h * kPanelRows128, &q_map, h * 64, kvh * G, s * p.chunk + p0, q_full);
+            mbar_arrive_expect_tx(q_full, kNQ * kQTile);
+            for (int i = 0; i < kNQ; ++i)
+                for (int h = 0; h < PANELS; ++h)
+                    tma_load_3d(q_s + i * kQTile + h * kQPanel, &q_map, h * 64, kvh * G,
+                                s * p.chunk + p0 + i * pos_per_tile, q_full);
         }
         const int32_t *trow = p.tables + (int64_t)s * p.max_blocks;
         int issued = 0;
         for (int j = 0; j < n_kt; ++j) {
-            const int st = j % kKvStages, use = j / kKvStages;
+            const int st = j % kStages, use = j / kStages;
             if (lane == 0 && !mbar_wait(&kv_empty[st], (use & 1) ^ 1, abort_flag)) {
                 report(p.dev_status, PKV_DEV_TIMEOUT);
                 *abort_flag = 1;
             }
             if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-            // lanes 0..7: the pool row of each 16-key group of this tile
+            // lanes 0..3: the pool row of each 16-key group of this tile
             int32_t row = p.pool_rows;  // out of range: the box reads zeros
             if (lane < kTN / 16) {
                 const int32_t key0 = j * kTN + lane * 16;
@@ -251,13 +243,13 @@ __global__ void __launch_bounds__(192, 1) prefill_tc_kernel(const __grid_constan
                 }
             }
             uint8_t *ks = kv_s + st * kStageBytes;
-            uint8_t *vs = ks + kKBytes;
+            uint8_t *vs = ks + kKTile;
             if (lane == 0) mbar_arrive_expect_tx(&kv_full[st], kStageBytes);
             for (int gq = 0; gq < kTN / 16; ++gq) {
                 const int32_t rr = __shfl_sync(0xffffffffu, row, gq);
                 if (lane == 0) {
                     for (int h = 0; h < PANELS; ++h) {
-                        const uint32_t off = h * kPanelRows128 + gq * 16 * 128;
+                        const uint32_t off = h * kKVPanel + gq * 16 * 128;
                         tma_load_3d(ks + off, &k_map, h * 64, kvh, rr, &kv_full[st]);
                         tma_load_3d(vs + off, &v_map, h * 64, kvh, rr, &kv_full[st]);
                     }
@@ -268,59 +260,70 @@ __global__ void __launch_bounds__(192, 1) prefill_tc_kernel(const __grid_constan
         // every copy this warp issued has landed before the CTA can exit
         if (lane == 0) {
             (void)mbar_wait(q_full, 0);
-            for (int i = issued > kKvStages ? issued - kKvStages : 0; i < issued; ++i)
-                (void)mbar_wait(&kv_full[i % kKvStages], (i / kKvStages) & 1);
+            for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
+                (void)mbar_wait(&kv_full[i % kStages], (i / kStages) & 1);
         }
-    } else if (warp == 5 && n_kt > 0) {
+    } else if (warp == 9 && n_kt > 0) {
         // ===================== MMA issuer =====================
-        // One lane issues S_j = Q K_j^T as soon as K_j has landed and S buffer
-        // j & 1 is free, and O += P_j V_j as soon as P_j is written, whichever
-        // is ready first (non-blocking polls, bounded by the wait limit).
+        // One lane issues every product as soon as its inputs are ready:
+        // S_ij = Q_i K_j^T when K_j has landed and S buffer j & 1 of tile i is
+        // free; O_i += P_ij V_j when P_ij is written.  A K/V stage returns to the
+        // producer once both tiles' P V products of it are issued (the commit
+        // arrives when they are done).
         const uint32_t idesc_s = umma_idesc_bf16(kTM, kTN, false, false);
         const uint32_t idesc_o = umma_idesc_bf16(kTM, D, false, true);
         bool ok = true;
         if (lane == 0) {
             ok = mbar_wait(q_full, 0, abort_flag);
-            const uint32_t q_addr = smem_u32(q_s), p_addr = smem_u32(p_s);
-            int js = 0, jp = 0;
+            int js[kNQ] = {0, 0}, jp[kNQ] = {0, 0};
+            int released = 0;
             unsigned long long t_last = global_timer_ns();
             uint32_t spin = 0;
-            while (ok && jp < n_kt) {
+            while (ok && (jp[0] < n_kt || jp[1] < n_kt)) {
                 bool progressed = false;
-                if (js < n_kt && js < jp + 2) {
-                    const int st = js % kKvStages, b = js & 1;
-                    if (mbar_test_wait(&kv_full[st], (js / kKvStages) & 1) &&
-                        mbar_test_wait(&s_free[b], ((js >> 1) & 1) ^ 1)) {
+#pragma unroll
+                for (int i = 0; i < kNQ; ++i) {
+                    const int j = js[i];
+                    if (j < n_kt && j < jp[i] + 2 && mbar_test_wait(&kv_full[j % kStages], (j / kStages) & 1) &&
+                        mbar_test_wait(&s_free[2 * i + (j & 1)], ((j >> 1) & 1) ^ 1)) {
                         tc_fence_after();
-                        const uint32_t k_addr = smem_u32(kv_s + st * kStageBytes);
+                        const uint32_t q_addr = smem_u32(q_s + i * kQTile);
+                        const uint32_t k_addr = smem_u32(kv_s + (j % kStages) * kStageBytes);
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
-                            const uint32_t off = (kk / 4) * kPanelRows128 + (kk % 4) * 32;
-                            umma_bf16(tmem + b * kTN, umma_desc_sw128(q_addr + off, 16, 1024),
-                                      umma_desc_sw128(k_addr + off, 16, 1024), idesc_s, kk > 0);
+                            umma_bf16(tmem + i * kTileCols + (j & 1) * kTN,
+                                      umma_desc_sw128(q_addr + (kk / 4) * kQPanel + (kk % 4) * 32, 16, 1024),
+                                      umma_desc_sw128(k_addr + (kk / 4) * kKVPanel + (kk % 4) * 32, 16, 1024),
+                                      idesc_s, kk > 0);
                         }
-                        umma_commit(&s_full[b]);
-                        ++js;
+                        umma_commit(&s_full[2 * i + (j & 1)]);
+                        ++js[i];
                         progressed = true;
                     }
                 }
-                if (jp < js && mbar_test_wait(p_full, jp & 1)) {
-                    tc_fence_after();
-                    const int st = jp % kKvStages;
-                    const uint32_t v_addr = smem_u32(kv_s + st * kStageBytes + kKBytes);
 #pragma unroll
-                    for (int kk = 0; kk < kTN / 16; ++kk) {
-                        // A = P (K-major, keys kk*16..), B = V (MN-major: 8-key groups 1024 B
-                        // apart, 64-column panels kPanelRows128 apart)
-                        const uint32_t a_off = (kk / 4) * kPanelRows128 + (kk % 4) * 32;
-                        umma_bf16(tmem + kOCol, umma_desc_sw128(p_addr + a_off, 16, 1024),
-                                  umma_desc_sw128(v_addr + kk * 2048, kPanelRows128, 1024), idesc_o,
-                                  (jp > 0 || kk > 0) ? 1u : 0u);
+                for (int i = 0; i < kNQ; ++i) {
+                    const int j = jp[i];
+                    if (j < js[i] && mbar_test_wait(&p_full[i], j & 1)) {
+                        tc_fence_after();
+                        const uint32_t p_addr = smem_u32(p_s + i * kPTile);
+                        const uint32_t v_addr = smem_u32(kv_s + (j % kStages) * kStageBytes + kKTile);
+#pragma unroll
+                        for (int kk = 0; kk < kTN / 16; ++kk) {
+                            // A = P (K-major, keys kk*16..), B = V (MN-major: 8-key groups 1024 B
+                            // apart, 64-column panels kKVPanel apart)
+                            umma_bf16(tmem + i * kTileCols + kOCol, umma_desc_sw128(p_addr + kk * 32, 16, 1024),
+                                      umma_desc_sw128(v_addr + kk * 2048, kKVPanel, 1024), idesc_o,
+                                      (j > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        umma_commit(&o_done[i]);
+                        ++jp[i];
+                        progressed = true;
                     }
-                    umma_commit(o_done);
-                    umma_commit(&kv_empty[st]);
-                    ++jp;
-                    progressed = true;
+                }
+                while (released < min(jp[0], jp[1])) {
+                    umma_commit(&kv_empty[released % kStages]);
+                    ++released;
                 }
                 if (progressed) {
                     spin = 0;
@@ -338,29 +341,30 @@ __global__ void __launch_bounds__(192, 1) prefill_tc_kernel(const __grid_constan
             (void)mbar_wait(fin_bar, 0);
         }
         __syncwarp();
-    } else if (warp < 4) {
-        // ===================== softmax warpgroup: row r = TMEM lane r =====================
-        const int r = threadIdx.x;
-        const int32_t qpos = P + p0 + r / G;
-        const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    } else if (warp < 4 * kNQ) {
+        // ===================== softmax warpgroups: row r of tile qt = TMEM lane r =====================
+        const int qt = warp / 4;
+        const int r = threadIdx.x % kTM;
+        const int32_t qpos = P + p0 + qt * pos_per_tile + r / G;
+        const uint32_t lane_base = tmem + ((uint32_t)((warp % 4) * 32) << 16) + qt * kTileCols;
+        uint8_t *p_tile = p_s + qt * kPTile;
         float m = -INFINITY, l = 0.f;
         bool ok = n_kt > 0;
         for (int j = 0; j < n_kt && ok; ++j) {
             const int b = j & 1;
-            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[b], (j >> 1) & 1, abort_flag));
+            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[2 * qt + b], (j >> 1) & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
             const int32_t key_base = j * kTN;
             const bool masked = key_base + kTN - 1 > qpos;
-            // one pass: the whole S row into registers (four loads, one wait)
             uint32_t sv[kTN];
 #pragma unroll
             for (int c = 0; c < kTN / 32; ++c) tmem_ld32_async(lane_base + b * kTN + c * 32, sv + c * 32);
             tmem_wait_ld();
-            // S buffer b is read: the MMA warp may overwrite it with S_{j+2}
+            // S buffer b of this tile is read: the MMA lane may overwrite it
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&s_free[b]);
+            if (lane == 0) mbar_arrive(&s_free[2 * qt + b]);
             float mx = -INFINITY;
 #pragma unroll
             for (int i = 0; i < kTN; ++i) {
@@ -368,94 +372,87 @@ __global__ void __launch_bounds__(192, 1) prefill_tc_kernel(const __grid_constan
                 mx = fmaxf(mx, valid ? __uint_as_float(sv[i]) : -INFINITY);
             }
             mx *= p.scale_log2;
-            // the previous P V product must be done: P is overwritten, O may be rescaled
+            // the previous P V product of this tile must be done: P is overwritten, O may be rescaled
             if (j > 0) {
-                ok = __all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, abort_flag));
+                ok = __all_sync(0xffffffffu, mbar_wait(&o_done[qt], (j - 1) & 1, abort_flag));
                 if (!ok) break;
                 tc_fence_after();
             }
             float alpha = 1.f;
             if (m == -INFINITY) {
-                m = mx;
+                m = mx;          // first tile: key 0 is always visible, so mx is finite
             } else if (mx > m + kRescaleThreshold) {
                 alpha = fast_exp2(m - mx);
                 m = mx;
             }
             l *= alpha;
-            // probabilities, row sum, P (bf16) to shared memory
+            // probabilities, row sum, P (bf16) of keys 0..63 = one 128-byte row of the P tile
 #pragma unroll
-            for (int c = 0; c < kTN / 32; ++c) {
-                uint32_t pk[16];
+            for (int q4 = 0; q4 < kTN / 8; ++q4) {
+                uint32_t pk[4];
 #pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    const int kidx = c * 32 + i;
+                for (int e = 0; e < 4; ++e) {
+                    const int kidx = q4 * 8 + 2 * e;
                     const bool v0 = !masked || key_base + kidx <= qpos;
                     const bool v1 = !masked || key_base + kidx + 1 <= qpos;
                     const float e0 = v0 ? fast_exp2(__uint_as_float(sv[kidx]) * p.scale_log2 - m) : 0.f;
                     const float e1 = v1 ? fast_exp2(__uint_as_float(sv[kidx + 1]) * p.scale_log2 - m) : 0.f;
                     l += e0 + e1;
-                    pk[i / 2] = pack_bf16x2(e0, e1);
+                    pk[e] = pack_bf16x2(e0, e1);
                 }
-                // keys c*32 .. c*32+31 of row r: panel c/2, 16-byte chunks (c%2)*4 .. +3
-                uint8_t *prow = p_s + (c / 2) * kPanelRows128;
-#pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4)
-                    *reinterpret_cast<uint4 *>(prow + swz128(r, (c % 2) * 4 + q4)) =
-                        make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+                *reinterpret_cast<uint4 *>(p_tile + swz128(r, q4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
-            // O row rescale (rare: the row maximum grew by more than 2^8), after the
-            // S row is dead; the next P V product is issued only after p_full below
+            // O row rescale (rare), after the S row is dead; the next P V product of
+            // this tile is issued only after p_full below
             if (__any_sync(0xffffffffu, alpha != 1.f) && j > 0) {
-                float v[32];
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
-                    tmem_ld32(lane_base + kOCol + c * 32, v);
+                    uint32_t v[32];
+                    tmem_ld32_async(lane_base + kOCol + c * 32, v);
+                    tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] *= alpha;
+                    for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
                     tmem_st32(lane_base + kOCol + c * 32, v);
                 }
             }
             // last tile: V rows of keys past the last one may hold anything; zero them
+            // (both warpgroups write the same zeros)
             if (j == n_kt - 1 && (n_keys & 15) != 0) {
                 const int first = n_keys - key_base, stop = ((n_keys + 15) & ~15) - key_base;
-                uint8_t *vs = kv_s + (j % kKvStages) * kStageBytes + kKBytes;
+                uint8_t *vs = kv_s + (j % kStages) * kStageBytes + kKTile;
                 for (int i = r; i < (stop - first) * PANELS * 8; i += kTM) {
                     const int row = first + i / (PANELS * 8), pc = i % (PANELS * 8);
-                    *reinterpret_cast<uint4 *>(vs + (pc / 8) * kPanelRows128 + swz128(row, pc % 8)) =
+                    *reinterpret_cast<uint4 *>(vs + (pc / 8) * kKVPanel + swz128(row, pc % 8)) =
                         make_uint4(0, 0, 0, 0);
                 }
             }
             fence_proxy_async_smem();   // P (and zeroed V rows) visible to the tensor core
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(p_full);
+            if (lane == 0) mbar_arrive(&p_full[qt]);
         }
         if (ok && n_kt > 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait(o_done, (n_kt - 1) & 1, abort_flag));
+            ok = __all_sync(0xffffffffu, mbar_wait(&o_done[qt], (n_kt - 1) & 1, abort_flag));
             tc_fence_after();
         }
         if (ok && n_kt > 0) {
-            const int pos = p0 + r / G, h = kvh * G + r % G;
+            const int pos = p0 + qt * pos_per_tile + r / G, h = kvh * G + r % G;
             const bool store = pos <= p_last;
             const float inv = 1.f / l;
             __nv_bfloat16 *o = p.out + (((int64_t)s * p.chunk + pos) * p.n_q_heads + h) * D;
-            uint32_t ov[D];
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) tmem_ld32_async(lane_base + kOCol + c * 32, ov + c * 32);
-            tmem_wait_ld();
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
-                float v[32];
-#pragma unroll
-                for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(ov[c * 32 + i]);
+                uint32_t v[32];
+                tmem_ld32_async(lane_base + kOCol + c * 32, v);
+                tmem_wait_ld();
                 if (store) {
 #pragma unroll
                     for (int q4 = 0; q4 < 4; ++q4) {
                         uint4 w;
-                        w.x = pack_bf16x2(v[8 * q4 + 0] * inv, v[8 * q4 + 1] * inv);
-                        w.y = pack_bf16x2(v[8 * q4 + 2] * inv, v[8 * q4 + 3] * inv);
-                        w.z = pack_bf16x2(v[8 * q4 + 4] * inv, v[8 * q4 + 5] * inv);
-                        w.w = pack_bf16x2(v[8 * q4 + 6] * inv, v[8 * q4 + 7] * inv);
+                        w.x = pack_bf16x2(__uint_as_float(v[8 * q4 + 0]) * inv, __uint_as_float(v[8 * q4 + 1]) * inv);
+                        w.y = pack_bf16x2(__uint_as_float(v[8 * q4 + 2]) * inv, __uint_as_float(v[8 * q4 + 3]) * inv);
+                        w.z = pack_bf16x2(__uint_as_float(v[8 * q4 + 4]) * inv, __uint_as_float(v[8 * q4 + 5]) * inv);
+                        w.w = pack_bf16x2(__uint_as_float(v[8 * q4 + 6]) * inv, __uint_as_float(v[8 * q4 + 7]) * inv);
                         *reinterpret_cast<uint4 *>(o + c * 32 + 8 * q4) = w;
                     }
                 }
@@ -470,21 +467,17 @@ __global__ void __launch_bounds__(192, 1) prefill_tc_kernel(const __grid_constan
     // everyone meets here before the TMEM is released
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
     }
 }
 
-}  // namespace pkv
-
-namespace pkv {
-
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream)
 {
     const pkv_dims &d = a.dims;
     const int G = a.n_q_heads / d.n_kv_heads;
-    if (G > 16 || 128 % G != 0) return cudaErrorInvalidValue;
+    if (G > 16 || kTM % G != 0) return cudaErrorInvalidValue;
     PrefillTcParams p{};
     p.n_q_heads = a.n_q_heads;
     p.group = G;
@@ -499,9 +492,9 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream)
     p.out = static_cast<__nv_bfloat16 *>(a.out);
     p.lse_out = a.lse_out;
     p.dev_status = a.dev_status;
-    p.n_kv_heads = d.n_kv_heads;
     const int pos_per_tile = kTM / G;
     p.tiles_per_seq = (a.chunk + pos_per_tile - 1) / pos_per_tile;
+    p.pairs_per_seq = (p.tiles_per_seq + kNQ - 1) / kNQ;
 
     CUtensorMap qmap, kmap, vmap;
     {
@@ -522,18 +515,18 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream)
                           box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
 
-    const size_t smem = 1024 + (size_t)kTM * d.head_dim * 2 + (size_t)kKvStages * 2 * kTN * d.head_dim * 2 +
-                        (size_t)kTM * kTN * 2 + 16 * sizeof(uint64_t);
-    dim3 grid((unsigned)p.tiles_per_seq, (unsigned)d.n_kv_heads, (unsigned)a.n_seqs);
+    const size_t smem = 1024 + (size_t)kNQ * kTM * d.head_dim * 2 + (size_t)kStages * 2 * kTN * d.head_dim * 2 +
+                        (size_t)kNQ * kTM * kTN * 2 + 32 * sizeof(uint64_t);
+    dim3 grid((unsigned)p.pairs_per_seq, (unsigned)d.n_kv_heads, (unsigned)a.n_seqs);
     cudaError_t e;
     if (d.head_dim == 128) {
         e = cudaFuncSetAttribute(prefill_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        prefill_tc_kernel<128><<<grid, 192, smem, stream>>>(qmap, kmap, vmap, p);
+        prefill_tc_kernel<128><<<grid, 320, smem, stream>>>(qmap, kmap, vmap, p);
     } else {
         e = cudaFuncSetAttribute(prefill_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        prefill_tc_kernel<64><<<grid, 192, smem, stream>>>(qmap, kmap, vmap, p);
+        prefill_tc_kernel<64><<<grid, 320, smem, stream>>>(qmap, kmap, vmap, p);
     }
     return cudaGetLastError();
 }
