@@ -265,30 +265,26 @@ __global__ void __launch_bounds__(320, 1) prefill_tc_kernel(const __grid_constan
         }
     } else if (warp == 9 && n_kt > 0) {
         // ===================== MMA issuer =====================
-        // One lane issues every product as soon as its inputs are ready:
-        // S_ij = Q_i K_j^T when K_j has landed and S buffer j & 1 of tile i is
-        // free; O_i += P_ij V_j when P_ij is written.  A K/V stage returns to the
-        // producer once both tiles' P V products of it are issued (the commit
-        // arrives when they are done).
+        // One lane issues, for key tile j, S_0j and S_1j, then the P V products
+        // of tile j - 1 of both query tiles, waiting (suspended) for each input:
+        // while a warpgroup's softmax works on S_ij the tensor core runs the
+        // other tile's products.  A K/V stage returns to the producer when both
+        // P V products of it are done.
         const uint32_t idesc_s = umma_idesc_bf16(kTM, kTN, false, false);
         const uint32_t idesc_o = umma_idesc_bf16(kTM, D, false, true);
         bool ok = true;
         if (lane == 0) {
             ok = mbar_wait(q_full, 0, abort_flag);
-            int js[kNQ] = {0, 0}, jp[kNQ] = {0, 0};
-            int released = 0;
-            unsigned long long t_last = global_timer_ns();
-            uint32_t spin = 0;
-            while (ok && (jp[0] < n_kt || jp[1] < n_kt)) {
-                bool progressed = false;
+            for (int j = 0; ok && j <= n_kt; ++j) {
+                if (j < n_kt) {
+                    ok = mbar_wait(&kv_full[j % kStages], (j / kStages) & 1, abort_flag);
+                    const uint32_t k_addr = smem_u32(kv_s + (j % kStages) * kStageBytes);
 #pragma unroll
-                for (int i = 0; i < kNQ; ++i) {
-                    const int j = js[i];
-                    if (j < n_kt && j < jp[i] + 2 && mbar_test_wait(&kv_full[j % kStages], (j / kStages) & 1) &&
-                        mbar_test_wait(&s_free[2 * i + (j & 1)], ((j >> 1) & 1) ^ 1)) {
+                    for (int i = 0; i < kNQ && ok; ++i) {
+                        ok = mbar_wait(&s_free[2 * i + (j & 1)], ((j >> 1) & 1) ^ 1, abort_flag);
+                        if (!ok) break;
                         tc_fence_after();
                         const uint32_t q_addr = smem_u32(q_s + i * kQTile);
-                        const uint32_t k_addr = smem_u32(kv_s + (j % kStages) * kStageBytes);
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk) {
                             umma_bf16(tmem + i * kTileCols + (j & 1) * kTN,
@@ -297,39 +293,28 @@ __global__ void __launch_bounds__(320, 1) prefill_tc_kernel(const __grid_constan
                                       idesc_s, kk > 0);
                         }
                         umma_commit(&s_full[2 * i + (j & 1)]);
-                        ++js[i];
-                        progressed = true;
                     }
                 }
+                if (j >= 1 && ok) {
+                    const int jp = j - 1;
+                    const uint32_t v_addr = smem_u32(kv_s + (jp % kStages) * kStageBytes + kKTile);
 #pragma unroll
-                for (int i = 0; i < kNQ; ++i) {
-                    const int j = jp[i];
-                    if (j < js[i] && mbar_test_wait(&p_full[i], j & 1)) {
+                    for (int i = 0; i < kNQ && ok; ++i) {
+                        ok = mbar_wait(&p_full[i], jp & 1, abort_flag);
+                        if (!ok) break;
                         tc_fence_after();
                         const uint32_t p_addr = smem_u32(p_s + i * kPTile);
-                        const uint32_t v_addr = smem_u32(kv_s + (j % kStages) * kStageBytes + kKTile);
 #pragma unroll
                         for (int kk = 0; kk < kTN / 16; ++kk) {
                             // A = P (K-major, keys kk*16..), B = V (MN-major: 8-key groups 1024 B
                             // apart, 64-column panels kKVPanel apart)
                             umma_bf16(tmem + i * kTileCols + kOCol, umma_desc_sw128(p_addr + kk * 32, 16, 1024),
                                       umma_desc_sw128(v_addr + kk * 2048, kKVPanel, 1024), idesc_o,
-                                      (j > 0 || kk > 0) ? 1u : 0u);
+                                      (jp > 0 || kk > 0) ? 1u : 0u);
                         }
                         umma_commit(&o_done[i]);
-                        ++jp[i];
-                        progressed = true;
                     }
-                }
-                while (released < min(jp[0], jp[1])) {
-                    umma_commit(&kv_empty[released % kStages]);
-                    ++released;
-                }
-                if (progressed) {
-                    spin = 0;
-                    t_last = global_timer_ns();
-                } else if ((++spin & 255u) == 0) {
-                    if (*abort_flag || global_timer_ns() - t_last > kWaitTimeoutNs) ok = false;
+                    if (ok) umma_commit(&kv_empty[jp % kStages]);
                 }
             }
             if (!ok) {
@@ -356,7 +341,8 @@ __global__ void __launch_bounds__(320, 1) prefill_tc_kernel(const __grid_constan
             if (!ok) break;
             tc_fence_after();
             const int32_t key_base = j * kTN;
-            const bool masked = key_base + kTN - 1 > qpos;
+            // rows whose keys in this tile are all visible need no per-key test
+            const bool masked = __any_sync(0xffffffffu, key_base + kTN - 1 > qpos);
             uint32_t sv[kTN];
 #pragma unroll
             for (int c = 0; c < kTN / 32; ++c) tmem_ld32_async(lane_base + b * kTN + c * 32, sv + c * 32);
