@@ -76,14 +76,13 @@ struct DecodeParams {
     int32_t *dev_status;
     int32_t n_stages;
     int32_t boxes_per_half;  // TMA boxes per (K or V, half): 1 (all heads) or hpc (one per head)
-    uint32_t stage_bytes, tx_bytes, kv_tile_bytes, scale_tile_bytes, q_slot_bytes, scratch_bytes;
+    uint32_t stage_bytes, tx_bytes, kv_tile_bytes, scale_tile_bytes, q_slot_bytes;
 };
 
 // Shared-memory carve-up (dynamic smem, base rounded up to 1024 bytes).
 struct SmemLayout {
     uint8_t *stages;     // n_stages * stage_bytes
     uint8_t *q_slots;    // 2 * q_slot_bytes
-    uint8_t *scratch;    // per-consumer-warp fp16 tiles (int8 pages only)
     uint64_t *full_bar, *empty_bar, *qfull_bar, *qempty_bar;
     StageMeta *meta;
     int32_t *abort_flag;
@@ -98,8 +97,6 @@ __device__ __forceinline__ SmemLayout carve(uint8_t *smem, const DecodeParams &p
     base += (size_t)p.n_stages * p.stage_bytes;
     L.q_slots = base;
     base += 2 * (size_t)p.q_slot_bytes;
-    L.scratch = base;
-    base += (size_t)p.hpc * p.scratch_bytes;
     L.full_bar = reinterpret_cast<uint64_t *>(base);
     L.empty_bar = L.full_bar + kMaxStages;
     L.qfull_bar = L.empty_bar + kMaxStages;
@@ -426,7 +423,6 @@ __global__ void __launch_bounds__(288, 1) decode_split_kernel(const __grid_const
                                                               const __grid_constant__ CUtensorMap vs_map,
                                                               const DecodeParams p)
 {
-    constexpr int HALVES = D / 64;      // 64-element (128-byte) column halves of a bf16 row
     constexpr int KSTEPS = D / 16;      // mma k-steps over head_dim (QK) = m-tiles (PV)
     extern __shared__ uint8_t smem_raw[];
     SmemLayout L = carve(smem_raw, p);
@@ -608,7 +604,6 @@ __global__ void __launch_bounds__(288, 1) decode_split_kernel(const __grid_const
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
     uint32_t stage_it = 0, item_it = 0;
     const uint32_t half_bytes = (uint32_t)hpc * kStageTokens * 128u;
-    uint8_t *scratch = L.scratch + (size_t)warp * p.scratch_bytes;
 
     while (true) {
         const uint32_t st = stage_it % p.n_stages;
@@ -629,9 +624,13 @@ __global__ void __launch_bounds__(288, 1) decode_split_kernel(const __grid_const
                 break;
             }
             // Rewrite this warp's G query rows in place: 16-byte chunk c of head row
-            // r moves to chunk c ^ r (so ldmatrix of 8 head rows is conflict-free),
-            // converted to fp16 for int8 pages.  The rows stay in the slot until
-            // the piece's last stage.
+            // r moves to chunk c ^ r (so ldmatrix of 8 head rows is conflict-free).
+            // For int8 pages the row is also converted to fp16 and its elements
+            // permuted so that k-step kk, lane q of the K^T Q contraction sees
+            // d = q * D/4 + 4 kk + {0, 1} (b0) and + {2, 3} (b1): the order in
+            // which each lane holds its K codes (a dot product does not depend
+            // on the order of its terms).  The rows stay in the slot until the
+            // piece's last stage.
             uint8_t *qrows = L.q_slots + qs * p.q_slot_bytes + (size_t)warp * G * D * 2;
             {
                 constexpr int CPR = D / 8;            // 16-byte chunks per head row
@@ -639,7 +638,21 @@ __global__ void __launch_bounds__(288, 1) decode_split_kernel(const __grid_const
 #pragma unroll
                 for (int i = 0; i < (8 * CPR + 31) / 32; ++i) {
                     const int idx = i * 32 + lane;
-                    if (idx < G * CPR) tmp[i] = *reinterpret_cast<const uint4 *>(qrows + idx * 16);
+                    if (idx < G * CPR) {
+                        if (!INT8) {
+                            tmp[i] = *reinterpret_cast<const uint4 *>(qrows + idx * 16);
+                        } else {
+                            const int r = idx / CPR, c = idx % CPR, kk = c / 2, h = c % 2;
+                            uint32_t *w = reinterpret_cast<uint32_t *>(&tmp[i]);
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) {
+                                const int d0 = q * (D / 4) + 4 * kk + 2 * h;
+                                const uint32_t bits = *reinterpret_cast<const uint32_t *>(qrows + (r * D + d0) * 2);
+                                const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&bits));
+                                w[q] = pack_f16x2(f.x, f.y);
+                            }
+                        }
+                    }
                 }
                 __syncwarp();
 #pragma unroll
@@ -647,16 +660,7 @@ __global__ void __launch_bounds__(288, 1) decode_split_kernel(const __grid_const
                     const int idx = i * 32 + lane;
                     if (idx < G * CPR) {
                         const int r = idx / CPR, c = idx % CPR;
-                        uint4 x = tmp[i];
-                        if (INT8) {
-                            uint32_t *w = reinterpret_cast<uint32_t *>(&x);
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                const float2 f = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&w[e]));
-                                w[e] = pack_f16x2(f.x, f.y);
-                            }
-                        }
-                        *reinterpret_cast<uint4 *>(qrows + (r * CPR + (c ^ (r & 7))) * 16) = x;
+                        *reinterpret_cast<uint4 *>(qrows + (r * CPR + (c ^ (r & 7))) * 16) = tmp[i];
                     }
                 }
                 __syncwarp();
@@ -669,49 +673,18 @@ __global__ void __launch_bounds__(288, 1) decode_split_kernel(const __grid_const
 
         if (!(meta.flags & kMetaBad)) {
             const int nv = meta.n_valid;
-            // --- tiles for this head: bf16 straight from the stage, int8 via fp16 scratch
+            // --- tiles for this head: bf16 through ldmatrix; int8 codes are read
+            // straight into mma fragments
             uint32_t k_base, v_base;     // smem address of half 0 of this head's K / V tile
             uint32_t half_stride;        // bytes between the two 64-column halves
             float sk0 = 1.f, sk1 = 1.f, sv0 = 1.f, sv1 = 1.f;
+            const uint8_t *kcodes = stg + (size_t)warp * kStageTokens * D;   // int8: this head's codes
             if (!INT8) {
                 k_base = smem_u32(stg) + warp * (kStageTokens * 128u);
                 v_base = k_base + p.kv_tile_bytes;
                 half_stride = half_bytes;
             } else {
-                // convert this head's codes to fp16 tiles laid out like the bf16 ones
-                const uint8_t *kc = stg + (size_t)warp * kStageTokens * D;
-                const uint8_t *vc = kc + p.kv_tile_bytes;
-                constexpr int CPR = D / 16;  // 16-code chunks per row
-#pragma unroll
-                for (int j = 0; j < (kStageTokens * CPR) / 32; ++j) {
-                    const int idx = j * 32 + lane;
-                    const int tok = idx / CPR, c = idx % CPR;
-                    const uint32_t src_off = D == 128 ? swz(tok, c) : (uint32_t)(tok * D + c * 16);
-                    const uint4 kw = *reinterpret_cast<const uint4 *>(kc + src_off);
-                    const uint4 vw = *reinterpret_cast<const uint4 *>(vc + src_off);
-                    uint4 klo, khi, vlo, vhi;
-                    int8x4_to_half2x2(kw.x, klo.x, klo.y);
-                    int8x4_to_half2x2(kw.y, klo.z, klo.w);
-                    int8x4_to_half2x2(kw.z, khi.x, khi.y);
-                    int8x4_to_half2x2(kw.w, khi.z, khi.w);
-                    int8x4_to_half2x2(vw.x, vlo.x, vlo.y);
-                    int8x4_to_half2x2(vw.y, vlo.z, vlo.w);
-                    int8x4_to_half2x2(vw.z, vhi.x, vhi.y);
-                    int8x4_to_half2x2(vw.w, vhi.z, vhi.w);
-                    // fp16 elements d = 16c .. 16c+15 -> half (16c)/64, chunks (c%4)*2, +1
-                    const uint32_t hoff = (uint32_t)((16 * c) / 64) * (kStageTokens * 128u);
-                    const uint32_t c0 = (uint32_t)((c % 4) * 2);
-                    uint8_t *ks_ = scratch + hoff;
-                    uint8_t *vs_ = scratch + HALVES * kStageTokens * 128u + hoff;
-                    *reinterpret_cast<uint4 *>(ks_ + swz(tok, c0)) = klo;
-                    *reinterpret_cast<uint4 *>(ks_ + swz(tok, c0 + 1)) = khi;
-                    *reinterpret_cast<uint4 *>(vs_ + swz(tok, c0)) = vlo;
-                    *reinterpret_cast<uint4 *>(vs_ + swz(tok, c0 + 1)) = vhi;
-                }
-                __syncwarp();
-                k_base = smem_u32(scratch);
-                v_base = k_base + HALVES * kStageTokens * 128u;
-                half_stride = kStageTokens * 128u;
+                k_base = v_base = half_stride = 0;
                 const float *sc = reinterpret_cast<const float *>(stg + 2 * p.kv_tile_bytes);
                 sk0 = sc[g * hpc + warp];
                 sk1 = sc[(g + 8) * hpc + warp];
@@ -727,6 +700,26 @@ __global__ void __launch_bounds__(288, 1) decode_split_kernel(const __grid_const
             const uint32_t q_base = smem_u32(L.q_slots + (item_it & 1u) * p.q_slot_bytes) + warp * G * D * 2;
             const uint32_t qrow = ri < G ? (uint32_t)ri : 0u;
             float s4[4] = {0.f, 0.f, 0.f, 0.f};
+            // int8: lane (g, qd) holds the D/4 codes d = qd * D/4 .. of token rows g and
+            // g + 8 (one or two conflict-free 16-byte loads per row); word kk of
+            // that run is k-step kk's A fragment (a0a1 | a4a5 from row g, a2a3 |
+            // a6a7 from row g + 8), converted exactly to fp16.
+            uint32_t kw[2][D / 16];
+            if (INT8) {
+#pragma unroll
+                for (int rr = 0; rr < 2; ++rr) {
+                    const int tok = g + 8 * rr;
+#pragma unroll
+                    for (int c = 0; c < D / 64; ++c) {
+                        const uint32_t off = D == 128 ? swz(tok, 2 * qd + c) : (uint32_t)(tok * D + qd * 16);
+                        const uint4 x = *reinterpret_cast<const uint4 *>(kcodes + off);
+                        kw[rr][4 * c] = x.x;
+                        kw[rr][4 * c + 1] = x.y;
+                        kw[rr][4 * c + 2] = x.z;
+                        kw[rr][4 * c + 3] = x.w;
+                    }
+                }
+            }
 #pragma unroll
             for (int kk = 0; kk < KSTEPS; kk += 2) {
                 uint32_t qb[4];  // b0, b1 of k-step kk, then of kk + 1
@@ -734,14 +727,17 @@ __global__ void __launch_bounds__(288, 1) decode_split_kernel(const __grid_const
 #pragma unroll
                 for (int k2 = 0; k2 < 2; ++k2) {
                     const int k = kk + k2;
-                    const int tok = ri + 8 * (mi & 1);
-                    const uint32_t chunk = (uint32_t)((k % 4) * 2 + (mi >> 1));
                     uint32_t a[4];
-                    ldmatrix_x4(a, k_base + (uint32_t)(k / 4) * half_stride + swz(tok, chunk));
-                    if (INT8)
+                    if (INT8) {
+                        int8x4_to_half2x2(kw[0][k], a[0], a[2]);
+                        int8x4_to_half2x2(kw[1][k], a[1], a[3]);
                         mma_f16_16816(s4, a, qb[2 * k2], qb[2 * k2 + 1]);
-                    else
+                    } else {
+                        const int tok = ri + 8 * (mi & 1);
+                        const uint32_t chunk = (uint32_t)((k % 4) * 2 + (mi >> 1));
+                        ldmatrix_x4(a, k_base + (uint32_t)(k / 4) * half_stride + swz(tok, chunk));
                         mma_bf16_16816(s4, a, qb[2 * k2], qb[2 * k2 + 1]);
+                    }
                 }
             }
             // scale to log2 units, dequantise K (int8), mask tokens past the context
@@ -790,15 +786,42 @@ __global__ void __launch_bounds__(288, 1) decode_split_kernel(const __grid_const
                 vmask0 = (ta < nv ? 0x0000ffffu : 0u) | (ta + 1 < nv ? 0xffff0000u : 0u);
                 vmask1 = (tb < nv ? 0x0000ffffu : 0u) | (tb + 1 < nv ? 0xffff0000u : 0u);
             }
+            if (INT8) {
+                // lane (g, qd) holds the D/8 codes d = g * D/8 .. of tokens 2qd, 2qd+1,
+                // 2qd+8, 2qd+9.  O^T rows are relabelled: m-tile mt row g is
+                // d = g * D/8 + 2 mt and row g + 8 is the next d, so byte pairs of
+                // two token rows interleave (prmt) into the A fragments.
+                uint32_t vw[4][D / 32];
 #pragma unroll
-            for (int mt = 0; mt < KSTEPS; ++mt) {
-                const int tok = ri + 8 * (mi >> 1);
-                const uint32_t chunk = (uint32_t)((mt % 4) * 2 + (mi & 1));
-                uint32_t a[4];
-                ldmatrix_x4_trans(a, v_base + (uint32_t)(mt / 4) * half_stride + swz(tok, chunk));
-                if (INT8) {
+                for (int t4 = 0; t4 < 4; ++t4) {
+                    const int tok = 2 * qd + (t4 & 1) + 8 * (t4 >> 1);
+                    if (D == 128) {
+                        const uint4 x = *reinterpret_cast<const uint4 *>(kcodes + p.kv_tile_bytes + swz(tok, g));
+                        vw[t4][0] = x.x;
+                        vw[t4][1] = x.y;
+                        vw[t4][2] = x.z;
+                        vw[t4][3] = x.w;
+                    } else {
+                        const uint2 x = *reinterpret_cast<const uint2 *>(kcodes + p.kv_tile_bytes + tok * D + g * 8);
+                        vw[t4][0] = x.x;
+                        vw[t4][1] = x.y;
+                    }
+                }
+#pragma unroll
+                for (int mt = 0; mt < KSTEPS; ++mt) {
+                    const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+                    uint32_t a[4];
+                    int8x4_to_half2x2(__byte_perm(vw[0][mt / 2], vw[1][mt / 2], sel), a[0], a[1]);
+                    int8x4_to_half2x2(__byte_perm(vw[2][mt / 2], vw[3][mt / 2], sel), a[2], a[3]);
                     mma_f16_16816(acc[mt], a, pb0, pb1);
-                } else {
+                }
+            } else {
+#pragma unroll
+                for (int mt = 0; mt < KSTEPS; ++mt) {
+                    const int tok = ri + 8 * (mi >> 1);
+                    const uint32_t chunk = (uint32_t)((mt % 4) * 2 + (mi & 1));
+                    uint32_t a[4];
+                    ldmatrix_x4_trans(a, v_base + (uint32_t)(mt / 4) * half_stride + swz(tok, chunk));
                     a[0] &= vmask0;
                     a[1] &= vmask0;
                     a[2] &= vmask1;
@@ -806,7 +829,6 @@ __global__ void __launch_bounds__(288, 1) decode_split_kernel(const __grid_const
                     mma_bf16_16816(acc[mt], a, pb0, pb1);
                 }
             }
-            if (INT8) __syncwarp();  // scratch is rewritten by the next stage
         }
 
         // the stage's tiles (and, at a piece's end, its query rows) are no longer
@@ -835,14 +857,24 @@ __global__ void __launch_bounds__(288, 1) decode_split_kernel(const __grid_const
                 __nv_bfloat16 *o = p.out + ((int64_t)s * p.n_q_heads + hbase) * D;
 #pragma unroll
                 for (int mt = 0; mt < KSTEPS; ++mt) {
-                    const int d = mt * 16 + g;
-                    if (n0 < G) {
-                        o[(size_t)n0 * D + d] = __float2bfloat16_rn(acc[mt][0] * inv0);
-                        o[(size_t)n0 * D + d + 8] = __float2bfloat16_rn(acc[mt][2] * inv0);
-                    }
-                    if (n1 < G) {
-                        o[(size_t)n1 * D + d] = __float2bfloat16_rn(acc[mt][1] * inv1);
-                        o[(size_t)n1 * D + d + 8] = __float2bfloat16_rn(acc[mt][3] * inv1);
+                    if (INT8) {  // rows g, g + 8 of m-tile mt are d, d + 1
+                        const int d = g * (D / 8) + 2 * mt;
+                        if (n0 < G)
+                            *reinterpret_cast<uint32_t *>(o + (size_t)n0 * D + d) =
+                                pack_bf16x2(acc[mt][0] * inv0, acc[mt][2] * inv0);
+                        if (n1 < G)
+                            *reinterpret_cast<uint32_t *>(o + (size_t)n1 * D + d) =
+                                pack_bf16x2(acc[mt][1] * inv1, acc[mt][3] * inv1);
+                    } else {     // rows g, g + 8 of m-tile mt are d, d + 8
+                        const int d = mt * 16 + g;
+                        if (n0 < G) {
+                            o[(size_t)n0 * D + d] = __float2bfloat16_rn(acc[mt][0] * inv0);
+                            o[(size_t)n0 * D + d + 8] = __float2bfloat16_rn(acc[mt][2] * inv0);
+                        }
+                        if (n1 < G) {
+                            o[(size_t)n1 * D + d] = __float2bfloat16_rn(acc[mt][1] * inv1);
+                            o[(size_t)n1 * D + d + 8] = __float2bfloat16_rn(acc[mt][3] * inv1);
+                        }
                     }
                 }
                 if (p.lse_out && g == 0) {
@@ -855,14 +887,20 @@ __global__ void __launch_bounds__(288, 1) decode_split_kernel(const __grid_const
                 float *pa = p.ws.part_acc + prow * D;
 #pragma unroll
                 for (int mt = 0; mt < KSTEPS; ++mt) {
-                    const int d = mt * 16 + g;
-                    if (n0 < G) {
-                        pa[(size_t)n0 * D + d] = acc[mt][0];
-                        pa[(size_t)n0 * D + d + 8] = acc[mt][2];
-                    }
-                    if (n1 < G) {
-                        pa[(size_t)n1 * D + d] = acc[mt][1];
-                        pa[(size_t)n1 * D + d + 8] = acc[mt][3];
+                    if (INT8) {
+                        const int d = g * (D / 8) + 2 * mt;
+                        if (n0 < G) *reinterpret_cast<float2 *>(pa + (size_t)n0 * D + d) = make_float2(acc[mt][0], acc[mt][2]);
+                        if (n1 < G) *reinterpret_cast<float2 *>(pa + (size_t)n1 * D + d) = make_float2(acc[mt][1], acc[mt][3]);
+                    } else {
+                        const int d = mt * 16 + g;
+                        if (n0 < G) {
+                            pa[(size_t)n0 * D + d] = acc[mt][0];
+                            pa[(size_t)n0 * D + d + 8] = acc[mt][2];
+                        }
+                        if (n1 < G) {
+                            pa[(size_t)n1 * D + d] = acc[mt][1];
+                            pa[(size_t)n1 * D + d + 8] = acc[mt][3];
+                        }
                     }
                 }
                 if (g == 0) {
@@ -991,12 +1029,10 @@ cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream, 
     if (!INT8) {
         p.kv_tile_bytes = (uint32_t)(D / 64) * hpc * 16u * 128u;
         p.scale_tile_bytes = 0;
-        p.scratch_bytes = 0;
         p.tx_bytes = 2 * p.kv_tile_bytes;
     } else {
         p.kv_tile_bytes = (uint32_t)hpc * 16u * D;
         p.scale_tile_bytes = (uint32_t)hpc * 16u * 4u;
-        p.scratch_bytes = 2u * (D / 64) * 16u * 128u;
         p.tx_bytes = 2 * p.kv_tile_bytes + 2 * p.scale_tile_bytes;
     }
     p.stage_bytes = (uint32_t)align_up(p.tx_bytes, 1024);
@@ -1028,7 +1064,7 @@ cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream, 
     // shared memory: stages fill what one CTA may hold at ctas_per_sm per SM
     const size_t max_smem = 232448;  // 227 KiB per CTA on sm_103
     const size_t per_cta = max_smem / ctas_per_sm - (ctas_per_sm > 1 ? 1024 : 0);
-    const size_t fixed = 1024 + 2 * (size_t)p.q_slot_bytes + (size_t)hpc * p.scratch_bytes + smem_tail_bytes();
+    const size_t fixed = 1024 + 2 * (size_t)p.q_slot_bytes + smem_tail_bytes();
     if (fixed + 2 * (size_t)p.stage_bytes > per_cta) return cudaErrorInvalidValue;
     int stages = (int)((per_cta - fixed) / p.stage_bytes);
     stages = stages > kMaxStages ? kMaxStages : stages;
