@@ -32,9 +32,10 @@ METRIC = "paged decode attention HBM GB/s (% of GB300 peak) and seq-steps/s per 
 FALLBACK_HBM_GBS = 6800.0
 
 # dram__bytes_read.sum + dram__bytes_write.sum per launch of decode_split_kernel
-# on the config-1 workload, from the ncu capture summarised in
-# profiles/decode_split_cfg1.txt, valid while the kernel source hashes match.
-NCU_TRAFFIC = {"source_sha": None, "bytes_per_launch": None}
+# (the dominant kernel of the decode step) on the config-1 workload, from the ncu
+# capture summarised in profiles/decode_cfg1_llama8b_batch64.md, valid while
+# the kernel sources hash to source_sha.
+NCU_TRAFFIC = {"source_sha": "3b735f5fa5cbec47", "bytes_per_launch": 544754432 + 4990976}
 
 
 def parse_args():
@@ -278,6 +279,36 @@ def bench_config(w, args):
             "l2": "inputs larger than L2 (K/V pages read per step far exceed the 129 MB L2); no flush"}
 
 
+def bench_gather(P, device, peak, reps=200):
+    """The bf16 gather timed beside config 2: 16 sequences of 2048 tokens into a
+    contiguous [16, 8, 2048, 128] view (K and V), CUDA events over `reps` calls.
+    Algorithmic bytes: every gathered K/V row read once and written once."""
+    import torch
+    from paged_kv_cache_212_gb300 import workloads as W
+    w = W.config2_gather(device=device)
+    kp, vp, _, _ = fill_pool(P, w, device)
+    tables, lens = w.tables.to(device), w.stored_lens.to(device)
+    out_tokens = w.extra["out_tokens"]
+    ko = torch.empty((w.n_seqs, w.n_kv_heads, out_tokens, w.head_dim), dtype=torch.bfloat16, device=device)
+    vo = torch.empty_like(ko)
+    for _ in range(5):
+        P.paged_kv_gather(kp, vp, tables, lens, out_tokens, k_out=ko, v_out=vo)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(reps):
+        P.paged_kv_gather(kp, vp, tables, lens, out_tokens, k_out=ko, v_out=vo)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    nbytes = 2 * 2 * int(w.stored_lens.sum()) * w.n_kv_heads * w.head_dim * 2
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"workload": w.name, "ms_per_call": round(ms, 5), "algorithmic_bytes": nbytes,
+            "achieved": round(gbs, 2), "unit": "GB/s", "frac": round(gbs / peak, 4), "calls": reps,
+            "l2": "268 MB moved per call, larger than the 129 MB L2"}
+
+
 def prefill_flops(w):
     """4 * Hq * D * sum over queries of the keys each attends (Q K^T and P V)."""
     import torch
@@ -485,6 +516,8 @@ def main():
         "gpu_launches": 3 * K,
         "clocks": clk.summary(),
     }
+    if args.config == 2:
+        line["gather"] = bench_gather(P, device, peak)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.config)
     if rank == 0:
