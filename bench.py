@@ -70,6 +70,23 @@ def kernel_source_sha():
     return h.hexdigest()[:16]
 
 
+def max_over_ranks(values, device):
+    """Element-wise maximum of a list of floats over all ranks (the slowest
+    rank's times); identity when no process group is initialised."""
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def weak_scaling_value(bytes_per_step_per_rank, world, ms_per_step):
+    """Whole-job throughput in GB/s: every rank moves its own step bytes in
+    the slowest rank's step time."""
+    return world * bytes_per_step_per_rank / (ms_per_step * 1e-3) / 1e9
+
+
 def make_workload(cfg, device):
     from paged_kv_cache_212_gb300 import workloads as W
     if cfg == 1:
@@ -445,12 +462,8 @@ def main():
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    elapsed_ms = t_start.elapsed_time(t_end)
+    elapsed_ms = max_over_ranks([t_start.elapsed_time(t_end)], device)[0]
     decode_ms = elapsed_ms / K
-    if world > 1:
-        tt = torch.tensor([elapsed_ms, decode_ms], dtype=torch.float64, device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms, decode_ms = float(tt[0]), float(tt[1])
     assert int(status.item()) == 0, f"device status {int(status.item())}"
     ms_per_step = elapsed_ms / K
 
@@ -483,16 +496,12 @@ def main():
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        tt = torch.tensor([e2e_ms], dtype=torch.float64, device=device)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        e2e_ms = float(tt[0])
+    e2e_ms = max_over_ranks([e0.elapsed_time(e1) / e2e_steps], device)[0]
 
     decode_b, write_b = algorithmic_bytes(w)
     step_b = decode_b + write_b
     peak, peak_kind = measured_peaks()
-    value = world * step_b / (ms_per_step * 1e-3) / 1e9
+    value = weak_scaling_value(step_b, world, ms_per_step)
     achieved = step_b / (decode_ms * 1e-3) / 1e9
     traffic = NCU_TRAFFIC["bytes_per_launch"] if NCU_TRAFFIC["source_sha"] == kernel_source_sha() else None
     line = {
@@ -510,7 +519,7 @@ def main():
                      "algorithmic_bytes_per_launch": step_b, "avg_launch_ms": round(decode_ms, 5),
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s"},
-        "e2e": {"value": round(world * step_b / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+        "e2e": {"value": round(weak_scaling_value(step_b, world, e2e_ms), 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5),
                 "steps": e2e_steps},
         "gpu_launches": 3 * K,
