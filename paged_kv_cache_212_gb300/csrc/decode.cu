@@ -1001,11 +1001,20 @@ cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream, 
 {
     const pkv_dims &d = a.dims;
     const int G = a.n_q_heads / d.n_kv_heads;
-    int hpc = env_int("PKV_DECODE_HPC", d.n_kv_heads <= 8 ? d.n_kv_heads : 8);
-    if (hpc <= 0 || hpc > 8 || d.n_kv_heads % hpc != 0) hpc = d.n_kv_heads <= 8 ? d.n_kv_heads : 8;
+    // Launch shape (measured on GB300): one CTA per SM serving up to 8 kv
+    // heads; with groups of 8 or more query heads per kv head the consumer
+    // warps carry twice the mma work per byte, and 4 kv heads per CTA with two
+    // CTAs per SM keep more loads in flight per unit of that work.
+    int hpc_default = d.n_kv_heads <= 8 ? d.n_kv_heads : 8, ctas_default = 1;
+    if (G >= 8 && d.n_kv_heads % 4 == 0) {
+        hpc_default = 4;
+        ctas_default = 2;
+    }
+    int hpc = env_int("PKV_DECODE_HPC", hpc_default);
+    if (hpc <= 0 || hpc > 8 || d.n_kv_heads % hpc != 0) hpc = hpc_default;
     if (INT8 && hpc % 4 != 0) return cudaErrorInvalidValue;
-    int ctas_per_sm = env_int("PKV_DECODE_CTAS_PER_SM", 1);
-    if (ctas_per_sm < 1 || ctas_per_sm > 4) ctas_per_sm = 1;
+    int ctas_per_sm = env_int("PKV_DECODE_CTAS_PER_SM", ctas_default);
+    if (ctas_per_sm < 1 || ctas_per_sm > 4) ctas_per_sm = ctas_default;
 
     DecodeParams p{};
     p.q = static_cast<const __nv_bfloat16 *>(a.q);
@@ -1067,7 +1076,9 @@ cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream, 
     const size_t fixed = 1024 + 2 * (size_t)p.q_slot_bytes + smem_tail_bytes();
     if (fixed + 2 * (size_t)p.stage_bytes > per_cta) return cudaErrorInvalidValue;
     int stages = (int)((per_cta - fixed) / p.stage_bytes);
-    stages = stages > kMaxStages ? kMaxStages : stages;
+    // int8 pages: at most four stages (measured faster on GB300 than deeper rings)
+    const int stage_cap = INT8 ? 4 : kMaxStages;
+    stages = stages > stage_cap ? stage_cap : stages;
     const int want = env_int("PKV_DECODE_STAGES", 0);
     if (want >= 2 && want < stages) stages = want;
     p.n_stages = stages;
