@@ -7,22 +7,29 @@
 // rows.  Warp roles (320 threads):
 //   warps 0-3, 4-7  softmax warpgroups of query tile 0 and 1: thread r of a
 //                   warpgroup owns row r of its tile (= TMEM lane r);
-//   warp 8          TMA producer: both Q tiles once, then K and V tiles of 64
-//                   keys into a 4-stage ring, one {64 columns, 1 head, 16 keys}
-//                   box per 16-key group and 64-column panel, addressed
-//                   through the block table (groups past the last key read the
-//                   zero fill of an out-of-range row);
+//   warp 8          TMA producer: both Q tiles once, then for every tile of
+//                   128 keys its K and then its V into a ring of single-tile
+//                   slots; lane g of lanes 0..7 issues the {64 columns, 1 head,
+//                   16 keys} boxes of 16-key group g (addressed through the
+//                   block table, looked up one tile ahead; groups past the last
+//                   key read the zero fill of an out-of-range row);
 //   warp 9          TMEM allocator and MMA issuer (one lane).
-// TMEM (512 columns): per query tile, S double-buffered (2 x 64 columns) and
-// O (head_dim columns).  For key tile j and query tile i:
-//   S_ij = Q_i K_j^T (tcgen05.mma M 128, N 64), softmax in registers (log2
-//   units; a stale row maximum is kept unless it grows by more than 2^8, then
-//   the O row is rescaled in TMEM), P_ij (bf16) to shared memory, O_i += P_ij V_j
-//   (tcgen05.mma M 128, N head_dim, V read MN-major).
-// The MMA lane issues each product as soon as its inputs are ready, so one
-// warpgroup's softmax overlaps the other tile's products.  Query position
-// P + p (P = prefix length) sees keys 0 .. P + p (metrale impl_more.rs: a query
-// at q_pos attends only slots <= q_pos of its block).
+// TMEM (512 columns): per query tile, S (128 fp32 columns; P overwrites its
+// first 64 columns as packed bf16 pairs) and O (head_dim columns).  For key
+// tile j and query tile i:
+//   S_ij = Q_i K_j^T (tcgen05.mma M 128, N 128, both operands in shared
+//   memory); softmax in registers (log2 units; a stale row maximum is kept
+//   unless it grows by more than 2^8, then the O row is rescaled in TMEM);
+//   P_ij (bf16) back into TMEM; O_i += P_ij V_j (tcgen05.mma with A = P read
+//   from TMEM, B = V MN-major in shared memory).
+// Issue order PV_0j, S_0,j+1, PV_1j, S_1,j+1: while one warpgroup computes the
+// softmax of its tile the tensor core runs the other tile's two products, and
+// the commit of S_i,j+1 also covers PV_ij, so O may be rescaled as soon as S is
+// ready.  Keeping P in TMEM spares the shared-memory port the P round trip
+// (the S and P V operand reads and the TMA writes already come close to its
+// bandwidth).  Query position P + p (P = prefix length) sees keys 0 .. P + p
+// (metrale impl_more.rs: a query at q_pos attends only slots <= q_pos of its
+// block).
 #include <math.h>
 
 #include "common.cuh"
@@ -34,12 +41,15 @@ namespace {
 
 constexpr int kTM = 128;           // query rows per tile (TMEM lanes)
 constexpr int kNQ = 2;             // query tiles per CTA
-constexpr int kTN = 64;            // keys per K/V tile
-constexpr int kStages = 4;         // K/V ring depth
+constexpr int kTN = 128;           // keys per K/V tile
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTileCols = 256;        // TMEM columns per query tile: S0, S1, O
+constexpr uint32_t kTileCols = 256;        // TMEM columns per query tile: S / P, O
 constexpr uint32_t kOCol = 128;            // O's column within a query tile's range
+
+// K/V ring slots (one 128-key K or V tile each) that fit beside the Q tiles.
+template <int D>
+constexpr int ring_slots() { return D == 128 ? 5 : 10; }
 
 struct PrefillTcParams {
     int32_t n_q_heads, group, chunk;
@@ -127,6 +137,33 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *r)
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// D (TMEM) += A (TMEM, M x 16, K-major: lane = row, column c = bf16 pair
+// 2c, 2c + 1) * B (shared-memory descriptor).
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Store 16 consecutive 32-bit columns of this thread's TMEM lane (completion
+// awaited separately with tmem_wait_st).
+__device__ __forceinline__ void tmem_st16_async(uint32_t taddr, const uint32_t *r)
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t chunk)
 {
     return row * 128u + ((chunk ^ (row & 7u)) << 4);
@@ -141,26 +178,23 @@ __global__ void __launch_bounds__(320, 1) prefill_tc_kernel(const __grid_constan
                                                             const PrefillTcParams p)
 {
     constexpr int PANELS = D / 64;                          // 64-column (128-byte) panels of a bf16 row
+    constexpr int NS = ring_slots<D>();
     constexpr uint32_t kQPanel = kTM * 128u;                // 16 KiB: one panel of a 128-row Q tile
     constexpr uint32_t kQTile = PANELS * kQPanel;
-    constexpr uint32_t kKVPanel = kTN * 128u;               // 8 KiB: one panel of a 64-key tile
-    constexpr uint32_t kKTile = PANELS * kKVPanel;
-    constexpr uint32_t kStageBytes = 2 * kKTile;            // K then V
-    constexpr uint32_t kPTile = kTM * kTN * 2;              // 16 KiB: P of one query tile (one panel)
+    constexpr uint32_t kKVPanel = kTN * 128u;               // 16 KiB: one panel of a 128-key tile
+    constexpr uint32_t kSlotBytes = PANELS * kKVPanel;      // one K or V tile
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *q_s = base;                                    // kNQ Q tiles
-    uint8_t *kv_s = q_s + kNQ * kQTile;                     // kStages x (K, V)
-    uint8_t *p_s = kv_s + kStages * kStageBytes;            // kNQ P tiles
-    uint64_t *bars = reinterpret_cast<uint64_t *>(p_s + kNQ * kPTile);
+    uint8_t *ring = q_s + kNQ * kQTile;                     // NS slots: K_0, V_0, K_1, V_1, ...
+    uint64_t *bars = reinterpret_cast<uint64_t *>(ring + NS * kSlotBytes);
     uint64_t *q_full = bars + 0;
-    uint64_t *kv_full = bars + 1;                           // [kStages]
-    uint64_t *kv_empty = kv_full + kStages;                 // [kStages]
-    uint64_t *s_full = kv_empty + kStages;                  // [kNQ][2]
-    uint64_t *s_free = s_full + 2 * kNQ;                    // [kNQ][2]
-    uint64_t *p_full = s_free + 2 * kNQ;                    // [kNQ]
-    uint64_t *o_done = p_full + kNQ;                        // [kNQ]
+    uint64_t *slot_full = bars + 1;                         // [NS]
+    uint64_t *slot_empty = slot_full + NS;                  // [NS]
+    uint64_t *s_full = slot_empty + NS;                     // [kNQ]: S_ij in TMEM (and PV_i,j-1 done)
+    uint64_t *p_full = s_full + kNQ;                        // [kNQ]: P_ij in TMEM
+    uint64_t *o_done = p_full + kNQ;                        // [kNQ]: last P V product done
     uint64_t *fin_bar = o_done + kNQ;
     uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(fin_bar + 1);
     volatile int32_t *abort_flag = reinterpret_cast<int32_t *>(fin_bar + 2);
@@ -181,15 +215,12 @@ __global__ void __launch_bounds__(320, 1) prefill_tc_kernel(const __grid_constan
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int i = 0; i < kStages; ++i) {
-            mbar_init(&kv_full[i], 1);
-            mbar_init(&kv_empty[i], 1);
-        }
-        for (int i = 0; i < 2 * kNQ; ++i) {
-            mbar_init(&s_full[i], 1);
-            mbar_init(&s_free[i], 4);
+        for (int i = 0; i < NS; ++i) {
+            mbar_init(&slot_full[i], 1);
+            mbar_init(&slot_empty[i], 1);
         }
         for (int i = 0; i < kNQ; ++i) {
+            mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], 4);
             mbar_init(&o_done[i], 1);
         }
@@ -222,100 +253,111 @@ __global__ void __launch_bounds__(320, 1) prefill_tc_kernel(const __grid_constan
                                 s * p.chunk + p0 + i * pos_per_tile, q_full);
         }
         const int32_t *trow = p.tables + (int64_t)s * p.max_blocks;
+        // lane g < 8 serves 16-key group g of a tile: its block id is read one
+        // tile ahead and turned into a pool row when the tile is issued
+        auto group_key = [&](int j) { return j * kTN + lane * 16; };
+        auto load_block = [&](int j) -> int32_t {
+            const int32_t key0 = group_key(j);
+            return (lane < kTN / 16 && key0 < n_keys) ? __ldg(trow + key0 / p.block_size) : 0;
+        };
+        int32_t blk = load_block(0);
         int issued = 0;
-        for (int j = 0; j < n_kt; ++j) {
-            const int st = j % kStages, use = j / kStages;
-            if (lane == 0 && !mbar_wait(&kv_empty[st], (use & 1) ^ 1, abort_flag)) {
-                report(p.dev_status, PKV_DEV_TIMEOUT);
-                *abort_flag = 1;
-            }
-            if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-            // lanes 0..3: the pool row of each 16-key group of this tile
+        bool stop = false;
+        for (int j = 0; j < n_kt && !stop; ++j) {
             int32_t row = p.pool_rows;  // out of range: the box reads zeros
-            if (lane < kTN / 16) {
-                const int32_t key0 = j * kTN + lane * 16;
-                if (key0 < n_keys) {
-                    const int32_t blk = __ldg(trow + key0 / p.block_size);
+            {
+                const int32_t key0 = group_key(j);
+                if (lane < kTN / 16 && key0 < n_keys) {
                     if (blk < 0 || blk > p.n_blocks)
                         report(p.dev_status, PKV_DEV_BAD_BLOCK_ID);
                     else
                         row = blk * p.block_size + key0 % p.block_size;
                 }
             }
-            uint8_t *ks = kv_s + st * kStageBytes;
-            uint8_t *vs = ks + kKTile;
-            if (lane == 0) mbar_arrive_expect_tx(&kv_full[st], kStageBytes);
-            for (int gq = 0; gq < kTN / 16; ++gq) {
-                const int32_t rr = __shfl_sync(0xffffffffu, row, gq);
-                if (lane == 0) {
-                    for (int h = 0; h < PANELS; ++h) {
-                        const uint32_t off = h * kKVPanel + gq * 16 * 128;
-                        tma_load_3d(ks + off, &k_map, h * 64, kvh, rr, &kv_full[st]);
-                        tma_load_3d(vs + off, &v_map, h * 64, kvh, rr, &kv_full[st]);
-                    }
+            if (j + 1 < n_kt) blk = load_block(j + 1);
+            for (int kv = 0; kv < 2; ++kv) {
+                const int i = 2 * j + kv, st = i % NS, use = i / NS;
+                if (lane == 0 && !mbar_wait(&slot_empty[st], (use & 1) ^ 1, abort_flag)) {
+                    report(p.dev_status, PKV_DEV_TIMEOUT);
+                    *abort_flag = 1;
                 }
+                if (__shfl_sync(0xffffffffu, *abort_flag, 0)) {
+                    stop = true;
+                    break;
+                }
+                uint8_t *dst = ring + st * kSlotBytes;
+                if (lane == 0) mbar_arrive_expect_tx(&slot_full[st], kSlotBytes);
+                __syncwarp();
+                // a TMA issue holds its thread for about a hundred cycles: the
+                // eight group lanes issue side by side
+                if (lane < kTN / 16) {
+#pragma unroll
+                    for (int h = 0; h < PANELS; ++h)
+                        tma_load_3d(dst + h * kKVPanel + lane * 16 * 128, kv ? &v_map : &k_map, h * 64, kvh, row,
+                                    &slot_full[st]);
+                }
+                ++issued;
             }
-            ++issued;
         }
         // every copy this warp issued has landed before the CTA can exit
         if (lane == 0) {
             (void)mbar_wait(q_full, 0);
-            for (int i = issued > kStages ? issued - kStages : 0; i < issued; ++i)
-                (void)mbar_wait(&kv_full[i % kStages], (i / kStages) & 1);
+            for (int i = issued > NS ? issued - NS : 0; i < issued; ++i)
+                (void)mbar_wait(&slot_full[i % NS], (i / NS) & 1);
         }
     } else if (warp == 9 && n_kt > 0) {
         // ===================== MMA issuer =====================
-        // One lane issues, for key tile j, S_0j and S_1j, then the P V products
-        // of tile j - 1 of both query tiles, waiting (suspended) for each input:
-        // while a warpgroup's softmax works on S_ij the tensor core runs the
-        // other tile's products.  A K/V stage returns to the producer when both
-        // P V products of it are done.
         const uint32_t idesc_s = umma_idesc_bf16(kTM, kTN, false, false);
         const uint32_t idesc_o = umma_idesc_bf16(kTM, D, false, true);
         bool ok = true;
         if (lane == 0) {
-            ok = mbar_wait(q_full, 0, abort_flag);
-            for (int j = 0; ok && j <= n_kt; ++j) {
-                if (j < n_kt) {
-                    ok = mbar_wait(&kv_full[j % kStages], (j / kStages) & 1, abort_flag);
-                    const uint32_t k_addr = smem_u32(kv_s + (j % kStages) * kStageBytes);
+            auto slot_addr = [&](int i) { return smem_u32(ring + (i % NS) * kSlotBytes); };
+            auto wait_slot = [&](int i) { return mbar_wait(&slot_full[i % NS], (i / NS) & 1, abort_flag); };
+            // S_tj = Q_t K_j^T, then the commit that hands S_tj to warpgroup t
+            auto issue_s = [&](int t, int j) {
+                const uint32_t k_addr = slot_addr(2 * j), q_addr = smem_u32(q_s + t * kQTile);
 #pragma unroll
-                    for (int i = 0; i < kNQ && ok; ++i) {
-                        ok = mbar_wait(&s_free[2 * i + (j & 1)], ((j >> 1) & 1) ^ 1, abort_flag);
-                        if (!ok) break;
-                        tc_fence_after();
-                        const uint32_t q_addr = smem_u32(q_s + i * kQTile);
+                for (int kk = 0; kk < D / 16; ++kk)
+                    umma_bf16(tmem + t * kTileCols, umma_desc_sw128(q_addr + (kk / 4) * kQPanel + (kk % 4) * 32, 16, 1024),
+                              umma_desc_sw128(k_addr + (kk / 4) * kKVPanel + (kk % 4) * 32, 16, 1024), idesc_s,
+                              kk > 0);
+                umma_commit(&s_full[t]);
+            };
+            ok = mbar_wait(q_full, 0, abort_flag) && wait_slot(0);
+            if (ok) {
+                tc_fence_after();
+                for (int t = 0; t < kNQ; ++t) issue_s(t, 0);
+                umma_commit(&slot_empty[0]);
+            }
+            for (int j = 0; ok && j < n_kt; ++j) {
+                ok = wait_slot(2 * j + 1);
+                if (!ok) break;
+                const uint32_t v_addr = slot_addr(2 * j + 1);
+                for (int t = 0; t < kNQ && ok; ++t) {
+                    ok = mbar_wait(&p_full[t], j & 1, abort_flag);
+                    if (!ok) break;
+                    tc_fence_after();
+                    // O_t += P_tj V_j: A = P (TMEM, 8 columns per 16 keys), B = V (MN-major:
+                    // 8-key groups 1024 B apart, 64-column panels kKVPanel apart)
 #pragma unroll
-                        for (int kk = 0; kk < D / 16; ++kk) {
-                            umma_bf16(tmem + i * kTileCols + (j & 1) * kTN,
-                                      umma_desc_sw128(q_addr + (kk / 4) * kQPanel + (kk % 4) * 32, 16, 1024),
-                                      umma_desc_sw128(k_addr + (kk / 4) * kKVPanel + (kk % 4) * 32, 16, 1024),
-                                      idesc_s, kk > 0);
+                    for (int kk = 0; kk < kTN / 16; ++kk)
+                        umma_bf16_ts(tmem + t * kTileCols + kOCol, tmem + t * kTileCols + kk * 8,
+                                     umma_desc_sw128(v_addr + kk * 2048, kKVPanel, 1024), idesc_o,
+                                     (j > 0 || kk > 0) ? 1u : 0u);
+                    if (j + 1 < n_kt) {
+                        if (t == 0) {
+                            ok = wait_slot(2 * j + 2);
+                            if (!ok) break;
+                            tc_fence_after();
                         }
-                        umma_commit(&s_full[2 * i + (j & 1)]);
+                        issue_s(t, j + 1);
+                    } else {
+                        umma_commit(&o_done[t]);
                     }
                 }
-                if (j >= 1 && ok) {
-                    const int jp = j - 1;
-                    const uint32_t v_addr = smem_u32(kv_s + (jp % kStages) * kStageBytes + kKTile);
-#pragma unroll
-                    for (int i = 0; i < kNQ && ok; ++i) {
-                        ok = mbar_wait(&p_full[i], jp & 1, abort_flag);
-                        if (!ok) break;
-                        tc_fence_after();
-                        const uint32_t p_addr = smem_u32(p_s + i * kPTile);
-#pragma unroll
-                        for (int kk = 0; kk < kTN / 16; ++kk) {
-                            // A = P (K-major, keys kk*16..), B = V (MN-major: 8-key groups 1024 B
-                            // apart, 64-column panels kKVPanel apart)
-                            umma_bf16(tmem + i * kTileCols + kOCol, umma_desc_sw128(p_addr + kk * 32, 16, 1024),
-                                      umma_desc_sw128(v_addr + kk * 2048, kKVPanel, 1024), idesc_o,
-                                      (jp > 0 || kk > 0) ? 1u : 0u);
-                        }
-                        umma_commit(&o_done[i]);
-                    }
-                    if (ok) umma_commit(&kv_empty[jp % kStages]);
-                }
+                if (!ok) break;
+                umma_commit(&slot_empty[(2 * j + 1) % NS]);
+                if (j + 1 < n_kt) umma_commit(&slot_empty[(2 * j + 2) % NS]);
             }
             if (!ok) {
                 report(p.dev_status, PKV_DEV_TIMEOUT);
@@ -332,12 +374,10 @@ __global__ void __launch_bounds__(320, 1) prefill_tc_kernel(const __grid_constan
         const int r = threadIdx.x % kTM;
         const int32_t qpos = P + p0 + qt * pos_per_tile + r / G;
         const uint32_t lane_base = tmem + ((uint32_t)((warp % 4) * 32) << 16) + qt * kTileCols;
-        uint8_t *p_tile = p_s + qt * kPTile;
         float m = -INFINITY, l = 0.f;
         bool ok = n_kt > 0;
         for (int j = 0; j < n_kt && ok; ++j) {
-            const int b = j & 1;
-            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[2 * qt + b], (j >> 1) & 1, abort_flag));
+            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[qt], j & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
             const int32_t key_base = j * kTN;
@@ -345,12 +385,8 @@ __global__ void __launch_bounds__(320, 1) prefill_tc_kernel(const __grid_constan
             const bool masked = __any_sync(0xffffffffu, key_base + kTN - 1 > qpos);
             uint32_t sv[kTN];
 #pragma unroll
-            for (int c = 0; c < kTN / 32; ++c) tmem_ld32_async(lane_base + b * kTN + c * 32, sv + c * 32);
+            for (int c = 0; c < kTN / 32; ++c) tmem_ld32_async(lane_base + c * 32, sv + c * 32);
             tmem_wait_ld();
-            // S buffer b of this tile is read: the MMA lane may overwrite it
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&s_free[2 * qt + b]);
             float mx = -INFINITY;
 #pragma unroll
             for (int i = 0; i < kTN; ++i) {
@@ -358,12 +394,6 @@ __global__ void __launch_bounds__(320, 1) prefill_tc_kernel(const __grid_constan
                 mx = fmaxf(mx, valid ? __uint_as_float(sv[i]) : -INFINITY);
             }
             mx *= p.scale_log2;
-            // the previous P V product of this tile must be done: P is overwritten, O may be rescaled
-            if (j > 0) {
-                ok = __all_sync(0xffffffffu, mbar_wait(&o_done[qt], (j - 1) & 1, abort_flag));
-                if (!ok) break;
-                tc_fence_after();
-            }
             float alpha = 1.f;
             if (m == -INFINITY) {
                 m = mx;          // first tile: key 0 is always visible, so mx is finite
@@ -372,24 +402,8 @@ __global__ void __launch_bounds__(320, 1) prefill_tc_kernel(const __grid_constan
                 m = mx;
             }
             l *= alpha;
-            // probabilities, row sum, P (bf16) of keys 0..63 = one 128-byte row of the P tile
-#pragma unroll
-            for (int q4 = 0; q4 < kTN / 8; ++q4) {
-                uint32_t pk[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int kidx = q4 * 8 + 2 * e;
-                    const bool v0 = !masked || key_base + kidx <= qpos;
-                    const bool v1 = !masked || key_base + kidx + 1 <= qpos;
-                    const float e0 = v0 ? fast_exp2(__uint_as_float(sv[kidx]) * p.scale_log2 - m) : 0.f;
-                    const float e1 = v1 ? fast_exp2(__uint_as_float(sv[kidx + 1]) * p.scale_log2 - m) : 0.f;
-                    l += e0 + e1;
-                    pk[e] = pack_bf16x2(e0, e1);
-                }
-                *reinterpret_cast<uint4 *>(p_tile + swz128(r, q4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-            }
-            // O row rescale (rare), after the S row is dead; the next P V product of
-            // this tile is issued only after p_full below
+            // O row rescale (rare): O holds P V up to tile j - 1, complete since
+            // S_j's commit came after it
             if (__any_sync(0xffffffffu, alpha != 1.f) && j > 0) {
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
@@ -401,24 +415,45 @@ __global__ void __launch_bounds__(320, 1) prefill_tc_kernel(const __grid_constan
                     tmem_st32(lane_base + kOCol + c * 32, v);
                 }
             }
-            // last tile: V rows of keys past the last one may hold anything; zero them
-            // (both warpgroups write the same zeros)
+            // probabilities and row sum; P (bf16 pairs) over S's first 64 columns,
+            // each 16-column store after the S columns it covers were read
+#pragma unroll
+            for (int c = 0; c < kTN / 32; ++c) {
+                uint32_t pk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int kidx = c * 32 + 2 * e;
+                    const bool v0 = !masked || key_base + kidx <= qpos;
+                    const bool v1 = !masked || key_base + kidx + 1 <= qpos;
+                    const float e0 = v0 ? fast_exp2(__uint_as_float(sv[kidx]) * p.scale_log2 - m) : 0.f;
+                    const float e1 = v1 ? fast_exp2(__uint_as_float(sv[kidx + 1]) * p.scale_log2 - m) : 0.f;
+                    l += e0 + e1;
+                    pk[e] = pack_bf16x2(e0, e1);
+                }
+                tmem_st16_async(lane_base + c * 16, pk);
+            }
+            tmem_wait_st();
+            // last tile: V rows of keys past the last one may hold anything; zero
+            // them once V_j has landed (both warpgroups write the same zeros)
             if (j == n_kt - 1 && (n_keys & 15) != 0) {
+                const int vi = 2 * j + 1;
+                ok = __all_sync(0xffffffffu, mbar_wait(&slot_full[vi % NS], (vi / NS) & 1, abort_flag));
+                if (!ok) break;
                 const int first = n_keys - key_base, stop = ((n_keys + 15) & ~15) - key_base;
-                uint8_t *vs = kv_s + (j % kStages) * kStageBytes + kKTile;
+                uint8_t *vs = ring + (vi % NS) * kSlotBytes;
                 for (int i = r; i < (stop - first) * PANELS * 8; i += kTM) {
                     const int row = first + i / (PANELS * 8), pc = i % (PANELS * 8);
                     *reinterpret_cast<uint4 *>(vs + (pc / 8) * kKVPanel + swz128(row, pc % 8)) =
                         make_uint4(0, 0, 0, 0);
                 }
+                fence_proxy_async_smem();   // zeroed V rows visible to the tensor core
             }
-            fence_proxy_async_smem();   // P (and zeroed V rows) visible to the tensor core
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[qt]);
         }
         if (ok && n_kt > 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&o_done[qt], (n_kt - 1) & 1, abort_flag));
+            ok = __all_sync(0xffffffffu, mbar_wait(&o_done[qt], 0, abort_flag));
             tc_fence_after();
         }
         if (ok && n_kt > 0) {
@@ -501,8 +536,9 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream)
                           box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
 
-    const size_t smem = 1024 + (size_t)kNQ * kTM * d.head_dim * 2 + (size_t)kStages * 2 * kTN * d.head_dim * 2 +
-                        (size_t)kNQ * kTM * kTN * 2 + 32 * sizeof(uint64_t);
+    const int slots = d.head_dim == 128 ? ring_slots<128>() : ring_slots<64>();
+    const size_t smem = 1024 + (size_t)kNQ * kTM * d.head_dim * 2 + (size_t)slots * kTN * d.head_dim * 2 +
+                        32 * sizeof(uint64_t);
     dim3 grid((unsigned)p.pairs_per_seq, (unsigned)d.n_kv_heads, (unsigned)a.n_seqs);
     cudaError_t e;
     if (d.head_dim == 128) {
