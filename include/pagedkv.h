@@ -164,6 +164,8 @@ size_t pkv_decode_workspace_bytes(int32_t n_seqs, int32_t n_q_heads, int32_t hea
  *            scores (nullable)
  * For every sequence s and query head h (kv head g = h / G):
  *   o = softmax(softmax_scale * q K^T) V over the ctx_lens[s] tokens of s.
+ * softmax_scale must be finite and positive (1/sqrt(head_dim) in the pages);
+ * anything else returns PKV_ERR_INVALID_ARG.
  * The context is cut into logical ranges of split_tokens tokens (a multiple
  * of 16; 0 = automatic), each range is reduced with an online softmax, and
  * the ranges are merged by their log-sum-exp.  ctx_lens[s] == 0 gives o = 0
@@ -208,7 +210,8 @@ int paged_decode_step(const pkv_bf16 *k_new, const pkv_bf16 *v_new, const int32_
  *   prefix_lens int32 [n_seqs]
  * Query i of sequence s sits at absolute position P = prefix_lens[s] + i and
  * attends keys 0 .. P: the whole resident prefix plus, causally, the chunk up
- * to itself.  Q K^T and P V run on the tcgen05 tensor cores.
+ * to itself.  softmax_scale: finite and positive, as for the decode.  Q K^T
+ * and P V run on the tcgen05 tensor cores.
  */
 int paged_prefill_attention(const pkv_bf16 *q, int32_t n_q_heads, const pkv_bf16 *k_pool,
                             const pkv_bf16 *v_pool, pkv_dims dims, const int32_t *block_tables,

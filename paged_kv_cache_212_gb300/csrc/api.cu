@@ -227,7 +227,7 @@ static int prepare_decode(const pkv_bf16 *q, int32_t n_q_heads, const void *k_po
     if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out)) return PKV_ERR_INVALID_ARG;
     if (kv_dtype == PKV_KV_INT8 && (!k_scales || !v_scales || !aligned16(k_scales) || !aligned16(v_scales)))
         return PKV_ERR_INVALID_ARG;
-    if (!std::isfinite(softmax_scale)) return PKV_ERR_INVALID_ARG;
+    if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.f)) return PKV_ERR_INVALID_ARG;
     if (!carve_decode_workspace(workspace, workspace_bytes, n_seqs, n_q_heads, dims.head_dim, &a->ws))
         return PKV_ERR_WORKSPACE;
     a->q = q;
@@ -308,7 +308,7 @@ int paged_prefill_attention(const pkv_bf16 *q, int32_t n_q_heads, const pkv_bf16
     if ((int64_t)n_seqs * chunk > 0x7fffffffLL) return PKV_ERR_OUT_OF_RANGE;
     if (!q || !k_pool || !v_pool || !block_tables || !prefix_lens || !out) return PKV_ERR_INVALID_ARG;
     if (!aligned16(q) || !aligned16(k_pool) || !aligned16(v_pool) || !aligned16(out)) return PKV_ERR_INVALID_ARG;
-    if (!std::isfinite(softmax_scale)) return PKV_ERR_INVALID_ARG;
+    if (!std::isfinite(softmax_scale) || !(softmax_scale > 0.f)) return PKV_ERR_INVALID_ARG;
     int sms = 0;
     st = num_sms_of_current_device(&sms);
     if (st != PKV_OK) return st;

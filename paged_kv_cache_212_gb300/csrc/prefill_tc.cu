@@ -49,7 +49,7 @@ constexpr uint32_t kOCol = 128;            // O's column within a query tile's r
 
 // K/V ring slots (one 128-key K or V tile each) that fit beside the Q tiles.
 template <int D>
-constexpr int ring_slots() { return D == 128 ? 5 : 10; }
+__host__ __device__ constexpr int ring_slots() { return D == 128 ? 5 : 10; }
 
 struct PrefillTcParams {
     int32_t n_q_heads, group, chunk;
@@ -163,6 +163,14 @@ __device__ __forceinline__ void tmem_st16_async(uint32_t taddr, const uint32_t *
 }
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// max(a, b, c) in one instruction (sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c)
+{
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
 
 __device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t chunk)
 {
@@ -387,13 +395,26 @@ __global__ void __launch_bounds__(320, 1) prefill_tc_kernel(const __grid_constan
 #pragma unroll
             for (int c = 0; c < kTN / 32; ++c) tmem_ld32_async(lane_base + c * 32, sv + c * 32);
             tmem_wait_ld();
-            float mx = -INFINITY;
+            // keys past this row's position get a score of -inf (exp2 gives 0);
+            // only tiles crossing the diagonal take this branch
+            if (masked) {
 #pragma unroll
-            for (int i = 0; i < kTN; ++i) {
-                const bool valid = !masked || key_base + i <= qpos;
-                mx = fmaxf(mx, valid ? __uint_as_float(sv[i]) : -INFINITY);
+                for (int i = 0; i < kTN; ++i)
+                    if (key_base + i > qpos) sv[i] = __float_as_uint(-INFINITY);
             }
-            mx *= p.scale_log2;
+            // row maximum: three-input max over four independent chains
+            float mx;
+            {
+                float a0 = -INFINITY, a1 = -INFINITY, a2 = -INFINITY, a3 = -INFINITY;
+#pragma unroll
+                for (int i = 0; i < kTN; i += 8) {
+                    a0 = fmax3(a0, __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]));
+                    a1 = fmax3(a1, __uint_as_float(sv[i + 2]), __uint_as_float(sv[i + 3]));
+                    a2 = fmax3(a2, __uint_as_float(sv[i + 4]), __uint_as_float(sv[i + 5]));
+                    a3 = fmax3(a3, __uint_as_float(sv[i + 6]), __uint_as_float(sv[i + 7]));
+                }
+                mx = fmax3(a0, a1, fmaxf(a2, a3)) * p.scale_log2;
+            }
             float alpha = 1.f;
             if (m == -INFINITY) {
                 m = mx;          // first tile: key 0 is always visible, so mx is finite
@@ -401,7 +422,6 @@ __global__ void __launch_bounds__(320, 1) prefill_tc_kernel(const __grid_constan
                 alpha = fast_exp2(m - mx);
                 m = mx;
             }
-            l *= alpha;
             // O row rescale (rare): O holds P V up to tile j - 1, complete since
             // S_j's commit came after it
             if (__any_sync(0xffffffffu, alpha != 1.f) && j > 0) {
@@ -415,23 +435,29 @@ __global__ void __launch_bounds__(320, 1) prefill_tc_kernel(const __grid_constan
                     tmem_st32(lane_base + kOCol + c * 32, v);
                 }
             }
-            // probabilities and row sum; P (bf16 pairs) over S's first 64 columns,
-            // each 16-column store after the S columns it covers were read
+            // probabilities (packed two-lane FMA for the exponent arguments) and
+            // two packed partial row sums; P (bf16 pairs) over S's first 64
+            // columns, each 16-column store after the S columns it covers were read
+            const float2 sc2 = make_float2(p.scale_log2, p.scale_log2), nm2 = make_float2(-m, -m);
+            float2 la = make_float2(0.f, 0.f), lb = make_float2(0.f, 0.f);
 #pragma unroll
             for (int c = 0; c < kTN / 32; ++c) {
                 uint32_t pk[16];
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                     const int kidx = c * 32 + 2 * e;
-                    const bool v0 = !masked || key_base + kidx <= qpos;
-                    const bool v1 = !masked || key_base + kidx + 1 <= qpos;
-                    const float e0 = v0 ? fast_exp2(__uint_as_float(sv[kidx]) * p.scale_log2 - m) : 0.f;
-                    const float e1 = v1 ? fast_exp2(__uint_as_float(sv[kidx + 1]) * p.scale_log2 - m) : 0.f;
-                    l += e0 + e1;
-                    pk[e] = pack_bf16x2(e0, e1);
+                    const float2 x = __ffma2_rn(make_float2(__uint_as_float(sv[kidx]), __uint_as_float(sv[kidx + 1])),
+                                                sc2, nm2);
+                    const float2 ee = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+                    if (e & 1)
+                        lb = __fadd2_rn(lb, ee);
+                    else
+                        la = __fadd2_rn(la, ee);
+                    pk[e] = pack_bf16x2(ee.x, ee.y);
                 }
                 tmem_st16_async(lane_base + c * 16, pk);
             }
+            l = l * alpha + ((la.x + la.y) + (lb.x + lb.y));
             tmem_wait_st();
             // last tile: V rows of keys past the last one may hold anything; zero
             // them once V_j has landed (both warpgroups write the same zeros)

@@ -98,7 +98,7 @@ def test_decode_argument_checks(lib):
     d = _dims(P, hkv=2)
     f = lib.paged_decode_attention
     args = lambda **kw: [kw.get("q", FAKE), kw.get("hq", 8), FAKE, FAKE, kw.get("ks", None), kw.get("vs", None),
-                         kw.get("dt", 0), kw.get("dims", d), FAKE, 4, FAKE, kw.get("n", 2), 0.125,
+                         kw.get("dt", 0), kw.get("dims", d), FAKE, 4, FAKE, kw.get("n", 2), kw.get("sc", 0.125),
                          kw.get("split", 0), FAKE, None, kw.get("ws", FAKE), kw.get("wsb", 1 << 20), None,
                          None]
     assert f(*args(n=0)) == 0
@@ -112,6 +112,8 @@ def test_decode_argument_checks(lib):
     assert f(*args(dt=1, ks=FAKE, vs=FAKE)) == 2   # int8 needs Hkv % 4 == 0
     assert f(*args(ws=None)) == 4
     assert f(*args(wsb=64)) == 4
+    for sc in (0.0, -0.125, float("nan"), float("inf")):  # the scale must be finite and positive
+        assert f(*args(sc=sc)) == 1, sc
 
 
 def test_prefill_and_gather_argument_checks(lib):
@@ -123,6 +125,8 @@ def test_prefill_and_gather_argument_checks(lib):
     assert f(FAKE, 6, FAKE, FAKE, d, FAKE, 4, FAKE, 1, 16, 0.1, FAKE, None, None, None) == 2  # G = 3
     assert f(FAKE, 8, FAKE, FAKE, d, FAKE, 4, FAKE, 1, 65, 0.1, FAKE, None, None, None) == 3
     assert f(None, 8, FAKE, FAKE, d, FAKE, 4, FAKE, 1, 16, 0.1, FAKE, None, None, None) == 1
+    for sc in (0.0, -0.1, float("nan")):
+        assert f(FAKE, 8, FAKE, FAKE, d, FAKE, 4, FAKE, 1, 16, sc, FAKE, None, None, None) == 1, sc
     g = lib.paged_kv_gather
     assert g(FAKE, FAKE, d, FAKE, 4, FAKE, 0, 16, FAKE, FAKE, None, None) == 0
     assert g(FAKE, FAKE, d, FAKE, 4, FAKE, 2, 16, None, FAKE, None, None) == 1
