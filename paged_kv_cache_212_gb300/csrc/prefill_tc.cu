@@ -64,7 +64,11 @@ struct PrefillTcParams {
     int32_t *dev_status;
     int32_t tiles_per_seq;        // 128-row query tiles per (sequence, kv head)
     int32_t pairs_per_seq;        // CTAs per (sequence, kv head)
+    int32_t n_seqs, n_kv_heads;
 };
+
+// Batches of at most this many sequences are scheduled longest prefix first.
+constexpr int kSortMaxSeqs = 32;
 
 // ---- tcgen05 helpers -------------------------------------------------------
 
@@ -206,12 +210,36 @@ __global__ void __launch_bounds__(320, 1) prefill_tc_kernel(const __grid_constan
     uint64_t *fin_bar = o_done + kNQ;
     uint32_t *tmem_base_s = reinterpret_cast<uint32_t *>(fin_bar + 1);
     volatile int32_t *abort_flag = reinterpret_cast<int32_t *>(fin_bar + 2);
+    int32_t *sched = reinterpret_cast<int32_t *>(bars + 32);  // [kSortMaxSeqs + 1]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // CTA order: sequence-major, the heavy (late) query pairs of a sequence
+    // first, its kv heads innermost.  Small batches take their sequences
+    // longest prefix first, so the longest CTAs start in the first wave
+    // rather than the last (the hardware hands out CTAs in index order);
+    // each CTA finds its sequence as the one of prefix-length rank
+    // blockIdx.x / units (ties by index).
     const int pairs = p.pairs_per_seq;
-    const int pair = pairs - 1 - (int)(blockIdx.x % pairs);   // heavy (late) tiles first
-    const int kvh = blockIdx.y;
-    const int s = blockIdx.z;
+    const int units = pairs * p.n_kv_heads;
+    const int unit = (int)(blockIdx.x % units);
+    const int pair = pairs - 1 - unit / p.n_kv_heads;
+    const int kvh = unit % p.n_kv_heads;
+    int s = (int)(blockIdx.x / units);
+    if (p.n_seqs <= kSortMaxSeqs) {
+        if (threadIdx.x < p.n_seqs) sched[threadIdx.x] = __ldg(p.prefix_lens + threadIdx.x);
+        __syncthreads();
+        if (threadIdx.x < p.n_seqs) {
+            const int32_t mine = sched[threadIdx.x];
+            int rank = 0;
+            for (int t = 0; t < p.n_seqs; ++t) {
+                const int32_t o = sched[t];
+                rank += (o > mine || (o == mine && t < (int)threadIdx.x)) ? 1 : 0;
+            }
+            if (rank == s) sched[kSortMaxSeqs] = threadIdx.x;
+        }
+        __syncthreads();
+        s = sched[kSortMaxSeqs];
+    }
     const int G = p.group;
     const int pos_per_tile = kTM / G;
     const int p0 = pair * kNQ * pos_per_tile;
@@ -542,6 +570,8 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream)
     const int pos_per_tile = kTM / G;
     p.tiles_per_seq = (a.chunk + pos_per_tile - 1) / pos_per_tile;
     p.pairs_per_seq = (p.tiles_per_seq + kNQ - 1) / kNQ;
+    p.n_seqs = a.n_seqs;
+    p.n_kv_heads = d.n_kv_heads;
 
     CUtensorMap qmap, kmap, vmap;
     {
@@ -564,8 +594,10 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream)
 
     const int slots = d.head_dim == 128 ? ring_slots<128>() : ring_slots<64>();
     const size_t smem = 1024 + (size_t)kNQ * kTM * d.head_dim * 2 + (size_t)slots * kTN * d.head_dim * 2 +
-                        32 * sizeof(uint64_t);
-    dim3 grid((unsigned)p.pairs_per_seq, (unsigned)d.n_kv_heads, (unsigned)a.n_seqs);
+                        32 * sizeof(uint64_t) + (kSortMaxSeqs + 1) * sizeof(int32_t);
+    const int64_t ctas = (int64_t)p.pairs_per_seq * d.n_kv_heads * a.n_seqs;
+    if (ctas > INT32_MAX) return cudaErrorInvalidValue;
+    dim3 grid((unsigned)ctas);
     cudaError_t e;
     if (d.head_dim == 128) {
         e = cudaFuncSetAttribute(prefill_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

@@ -53,6 +53,11 @@ def workload(name):
             "prefill_small": lambda: W.prefill_workload("p", 10, [0, 5, 16, 100, 250], 40, 8, 2, 64, 16),
             "prefill_g8": lambda: W.prefill_workload("p8", 11, [0, 33, 300], 37, 64, 8, 128, 16),
             "prefill_g1": lambda: W.prefill_workload("p1", 12, [7, 64], 70, 4, 4, 128, 32),
+            # more sequences than the kernel orders by prefix length (natural order)
+            "prefill_many": lambda: W.prefill_workload("pm", 13, [(37 * i) % 301 for i in range(40)], 9, 8, 2,
+                                                       64, 16),
+            # equal prefix lengths: the longest-first order breaks ties by index
+            "prefill_ties": lambda: W.prefill_workload("pt", 14, [100, 100, 0, 100, 37], 20, 16, 4, 128, 16),
         }
         _CACHE[name] = makers[name]()
     return _CACHE[name]
@@ -344,7 +349,7 @@ def run_prefill(P, w, kp, vp, tables=None):
     return out, lse, int(st.item())
 
 
-@pytest.mark.parametrize("name", ["prefill_small", "prefill_g8", "prefill_g1"])
+@pytest.mark.parametrize("name", ["prefill_small", "prefill_g8", "prefill_g1", "prefill_many", "prefill_ties"])
 def test_prefill_parity_all_rows(P, name):
     w = workload(name)
     kp, vp, _, _ = pools(name)
