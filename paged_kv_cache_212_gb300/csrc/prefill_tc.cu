@@ -4,16 +4,20 @@
 // CTA = (sequence, kv head, two adjacent tiles of 128 query rows).  The rows of
 // a tile pack the G query heads of the kv head: row r is (chunk position
 // p0 + r / G, query head kvh * G + r % G), so every K/V tile serves 2 x 128
-// rows.  Warp roles (320 threads):
+// rows.  Warp roles (384 threads):
 //   warps 0-3, 4-7  softmax warpgroups of query tile 0 and 1: thread r of a
 //                   warpgroup owns row r of its tile (= TMEM lane r);
-//   warp 8          TMA producer: both Q tiles once, then for every tile of
-//                   128 keys its K and then its V into a ring of single-tile
-//                   slots; lane g of lanes 0..7 issues the {64 columns, 1 head,
-//                   16 keys} boxes of 16-key group g (addressed through the
-//                   block table, looked up one tile ahead; groups past the last
-//                   key read the zero fill of an out-of-range row);
+//   warps 8, 10     TMA producers of K: both Q tiles once (warp 8), then for
+//                   every tile of 128 keys half of its 16-key groups each, one
+//                   {64 columns, 1 head, 16 keys} box per group and panel;
+//   warp 11         TMA producer of V: one {64 columns, 16 keys, all panels}
+//                   box per group (a panel-dimension view of the pool);
 //   warp 9          TMEM allocator and MMA issuer (one lane).
+// Groups are addressed through the block table, looked up one tile ahead;
+// groups past the last key read the zero fill of an out-of-range row.  A TMA
+// issue holds its warp for about a hundred cycles whatever the box size (the
+// lanes of one warp issue one after the other), so the boxes of a tile are
+// spread over three warps and V, whose layout allows it, takes 4 KiB boxes.
 // TMEM (512 columns): per query tile, S (128 fp32 columns; P overwrites its
 // first 64 columns as packed bf16 pairs) and O (head_dim columns).  For key
 // tile j and query tile i:
@@ -47,9 +51,11 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTileCols = 256;        // TMEM columns per query tile: S / P, O
 constexpr uint32_t kOCol = 128;            // O's column within a query tile's range
 
-// K/V ring slots (one 128-key K or V tile each) that fit beside the Q tiles.
+// Ring slots (one 128-key tile each) of K and of V that fit beside the Q tiles.
 template <int D>
-__host__ __device__ constexpr int ring_slots() { return D == 128 ? 5 : 10; }
+__host__ __device__ constexpr int k_slots() { return D == 128 ? 3 : 6; }
+template <int D>
+__host__ __device__ constexpr int v_slots() { return D == 128 ? 2 : 4; }
 
 struct PrefillTcParams {
     int32_t n_q_heads, group, chunk;
@@ -184,27 +190,32 @@ __device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t chunk)
 }  // namespace
 
 template <int D>
-__global__ void __launch_bounds__(320, 1) prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
+__global__ void __launch_bounds__(384, 1) prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                                                             const __grid_constant__ CUtensorMap k_map,
                                                             const __grid_constant__ CUtensorMap v_map,
                                                             const PrefillTcParams p)
 {
     constexpr int PANELS = D / 64;                          // 64-column (128-byte) panels of a bf16 row
-    constexpr int NS = ring_slots<D>();
+    constexpr int NK = k_slots<D>(), NV = v_slots<D>();
     constexpr uint32_t kQPanel = kTM * 128u;                // 16 KiB: one panel of a 128-row Q tile
     constexpr uint32_t kQTile = PANELS * kQPanel;
-    constexpr uint32_t kKVPanel = kTN * 128u;               // 16 KiB: one panel of a 128-key tile
+    constexpr uint32_t kKVPanel = kTN * 128u;               // 16 KiB: one panel of a 128-key K tile
     constexpr uint32_t kSlotBytes = PANELS * kKVPanel;      // one K or V tile
+    constexpr uint32_t kVGroup = PANELS * 2048u;            // one 16-key group of a V tile (all panels)
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *q_s = base;                                    // kNQ Q tiles
-    uint8_t *ring = q_s + kNQ * kQTile;                     // NS slots: K_0, V_0, K_1, V_1, ...
-    uint64_t *bars = reinterpret_cast<uint64_t *>(ring + NS * kSlotBytes);
+    // K tile: [panel][128 keys][128 B]; V tile: [16-key group][panel][16 keys][128 B]
+    uint8_t *k_ring = q_s + kNQ * kQTile;                   // NK K tiles
+    uint8_t *v_ring = k_ring + NK * kSlotBytes;             // NV V tiles
+    uint64_t *bars = reinterpret_cast<uint64_t *>(v_ring + NV * kSlotBytes);
     uint64_t *q_full = bars + 0;
-    uint64_t *slot_full = bars + 1;                         // [NS]
-    uint64_t *slot_empty = slot_full + NS;                  // [NS]
-    uint64_t *s_full = slot_empty + NS;                     // [kNQ]: S_ij in TMEM (and PV_i,j-1 done)
+    uint64_t *k_full = bars + 1;                            // [NK]
+    uint64_t *k_empty = k_full + NK;                        // [NK]
+    uint64_t *v_full = k_empty + NK;                        // [NV]
+    uint64_t *v_empty = v_full + NV;                        // [NV]
+    uint64_t *s_full = v_empty + NV;                        // [kNQ]: S_ij in TMEM (and PV_i,j-1 done)
     uint64_t *p_full = s_full + kNQ;                        // [kNQ]: P_ij in TMEM
     uint64_t *o_done = p_full + kNQ;                        // [kNQ]: last P V product done
     uint64_t *fin_bar = o_done + kNQ;
@@ -251,9 +262,13 @@ __global__ void __launch_bounds__(320, 1) prefill_tc_kernel(const __grid_constan
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int i = 0; i < NS; ++i) {
-            mbar_init(&slot_full[i], 1);
-            mbar_init(&slot_empty[i], 1);
+        for (int i = 0; i < NK; ++i) {
+            mbar_init(&k_full[i], 2);   // the two K producers
+            mbar_init(&k_empty[i], 1);
+        }
+        for (int i = 0; i < NV; ++i) {
+            mbar_init(&v_full[i], 1);
+            mbar_init(&v_empty[i], 1);
         }
         for (int i = 0; i < kNQ; ++i) {
             mbar_init(&s_full[i], 1);
@@ -276,34 +291,40 @@ __global__ void __launch_bounds__(320, 1) prefill_tc_kernel(const __grid_constan
     const uint32_t tmem = *tmem_base_s;
     if (bad_len && threadIdx.x == 0) report(p.dev_status, PKV_DEV_BAD_LENGTH);
 
-    if (warp == 8 && n_kt > 0) {
-        // ===================== TMA producer =====================
-        if (lane == 0) {
+    if ((warp == 8 || warp == 10 || warp == 11) && n_kt > 0) {
+        // ===================== TMA producers =====================
+        const bool is_v = warp == 11;
+        if (warp == 8 && lane == 0) {
             prefetch_tensormap(&q_map);
-            prefetch_tensormap(&k_map);
-            prefetch_tensormap(&v_map);
             mbar_arrive_expect_tx(q_full, kNQ * kQTile);
             for (int i = 0; i < kNQ; ++i)
                 for (int h = 0; h < PANELS; ++h)
                     tma_load_3d(q_s + i * kQTile + h * kQPanel, &q_map, h * 64, kvh * G,
                                 s * p.chunk + p0 + i * pos_per_tile, q_full);
         }
+        if (lane == 0) prefetch_tensormap(is_v ? &v_map : &k_map);
+        // this warp's 16-key groups: all eight (V) or four (each K warp)
+        const int n_grp = is_v ? kTN / 16 : kTN / 32;
+        const int grp = is_v ? lane : (warp == 10 ? kTN / 32 : 0) + lane;
+        const int NSL = is_v ? NV : NK;
+        uint64_t *full = is_v ? v_full : k_full;
+        uint64_t *empty = is_v ? v_empty : k_empty;
+        uint8_t *ring = is_v ? v_ring : k_ring;
+        const uint32_t bytes = is_v ? kSlotBytes : kSlotBytes / 2;
         const int32_t *trow = p.tables + (int64_t)s * p.max_blocks;
-        // lane g < 8 serves 16-key group g of a tile: its block id is read one
-        // tile ahead and turned into a pool row when the tile is issued
-        auto group_key = [&](int j) { return j * kTN + lane * 16; };
+        // block ids are read one tile ahead and turned into pool rows when the
+        // tile is issued
         auto load_block = [&](int j) -> int32_t {
-            const int32_t key0 = group_key(j);
-            return (lane < kTN / 16 && key0 < n_keys) ? __ldg(trow + key0 / p.block_size) : 0;
+            const int32_t key0 = j * kTN + grp * 16;
+            return (lane < n_grp && key0 < n_keys) ? __ldg(trow + key0 / p.block_size) : 0;
         };
         int32_t blk = load_block(0);
         int issued = 0;
-        bool stop = false;
-        for (int j = 0; j < n_kt && !stop; ++j) {
+        for (int j = 0; j < n_kt; ++j) {
             int32_t row = p.pool_rows;  // out of range: the box reads zeros
             {
-                const int32_t key0 = group_key(j);
-                if (lane < kTN / 16 && key0 < n_keys) {
+                const int32_t key0 = j * kTN + grp * 16;
+                if (lane < n_grp && key0 < n_keys) {
                     if (blk < 0 || blk > p.n_blocks)
                         report(p.dev_status, PKV_DEV_BAD_BLOCK_ID);
                     else
@@ -311,35 +332,31 @@ __global__ void __launch_bounds__(320, 1) prefill_tc_kernel(const __grid_constan
                 }
             }
             if (j + 1 < n_kt) blk = load_block(j + 1);
-            for (int kv = 0; kv < 2; ++kv) {
-                const int i = 2 * j + kv, st = i % NS, use = i / NS;
-                if (lane == 0 && !mbar_wait(&slot_empty[st], (use & 1) ^ 1, abort_flag)) {
-                    report(p.dev_status, PKV_DEV_TIMEOUT);
-                    *abort_flag = 1;
-                }
-                if (__shfl_sync(0xffffffffu, *abort_flag, 0)) {
-                    stop = true;
-                    break;
-                }
-                uint8_t *dst = ring + st * kSlotBytes;
-                if (lane == 0) mbar_arrive_expect_tx(&slot_full[st], kSlotBytes);
-                __syncwarp();
-                // a TMA issue holds its thread for about a hundred cycles: the
-                // eight group lanes issue side by side
-                if (lane < kTN / 16) {
+            const int st = j % NSL, use = j / NSL;
+            if (lane == 0 && !mbar_wait(&empty[st], (use & 1) ^ 1, abort_flag)) {
+                report(p.dev_status, PKV_DEV_TIMEOUT);
+                *abort_flag = 1;
+            }
+            if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+            uint8_t *dst = ring + st * kSlotBytes;
+            if (lane == 0) mbar_arrive_expect_tx(&full[st], bytes);
+            __syncwarp();
+            if (lane < n_grp) {
+                if (is_v) {
+                    tma_load_3d(dst + grp * kVGroup, &v_map, 0, row, kvh * PANELS, &full[st]);
+                } else {
 #pragma unroll
                     for (int h = 0; h < PANELS; ++h)
-                        tma_load_3d(dst + h * kKVPanel + lane * 16 * 128, kv ? &v_map : &k_map, h * 64, kvh, row,
-                                    &slot_full[st]);
+                        tma_load_3d(dst + h * kKVPanel + grp * 2048, &k_map, h * 64, kvh, row, &full[st]);
                 }
-                ++issued;
             }
+            ++issued;
         }
         // every copy this warp issued has landed before the CTA can exit
         if (lane == 0) {
-            (void)mbar_wait(q_full, 0);
-            for (int i = issued > NS ? issued - NS : 0; i < issued; ++i)
-                (void)mbar_wait(&slot_full[i % NS], (i / NS) & 1);
+            if (warp == 8) (void)mbar_wait(q_full, 0);
+            for (int i = issued > NSL ? issued - NSL : 0; i < issued; ++i)
+                (void)mbar_wait(&full[i % NSL], (i / NSL) & 1);
         }
     } else if (warp == 9 && n_kt > 0) {
         // ===================== MMA issuer =====================
@@ -347,11 +364,11 @@ __global__ void __launch_bounds__(320, 1) prefill_tc_kernel(const __grid_constan
         const uint32_t idesc_o = umma_idesc_bf16(kTM, D, false, true);
         bool ok = true;
         if (lane == 0) {
-            auto slot_addr = [&](int i) { return smem_u32(ring + (i % NS) * kSlotBytes); };
-            auto wait_slot = [&](int i) { return mbar_wait(&slot_full[i % NS], (i / NS) & 1, abort_flag); };
+            auto wait_k = [&](int j) { return mbar_wait(&k_full[j % NK], (j / NK) & 1, abort_flag); };
+            auto wait_v = [&](int j) { return mbar_wait(&v_full[j % NV], (j / NV) & 1, abort_flag); };
             // S_tj = Q_t K_j^T, then the commit that hands S_tj to warpgroup t
             auto issue_s = [&](int t, int j) {
-                const uint32_t k_addr = slot_addr(2 * j), q_addr = smem_u32(q_s + t * kQTile);
+                const uint32_t k_addr = smem_u32(k_ring + (j % NK) * kSlotBytes), q_addr = smem_u32(q_s + t * kQTile);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
                     umma_bf16(tmem + t * kTileCols, umma_desc_sw128(q_addr + (kk / 4) * kQPanel + (kk % 4) * 32, 16, 1024),
@@ -359,30 +376,31 @@ __global__ void __launch_bounds__(320, 1) prefill_tc_kernel(const __grid_constan
                               kk > 0);
                 umma_commit(&s_full[t]);
             };
-            ok = mbar_wait(q_full, 0, abort_flag) && wait_slot(0);
+            ok = mbar_wait(q_full, 0, abort_flag) && wait_k(0);
             if (ok) {
                 tc_fence_after();
                 for (int t = 0; t < kNQ; ++t) issue_s(t, 0);
-                umma_commit(&slot_empty[0]);
+                umma_commit(&k_empty[0]);
             }
             for (int j = 0; ok && j < n_kt; ++j) {
-                ok = wait_slot(2 * j + 1);
+                ok = wait_v(j);
                 if (!ok) break;
-                const uint32_t v_addr = slot_addr(2 * j + 1);
+                const uint32_t v_addr = smem_u32(v_ring + (j % NV) * kSlotBytes);
                 for (int t = 0; t < kNQ && ok; ++t) {
                     ok = mbar_wait(&p_full[t], j & 1, abort_flag);
                     if (!ok) break;
                     tc_fence_after();
                     // O_t += P_tj V_j: A = P (TMEM, 8 columns per 16 keys), B = V (MN-major:
-                    // 8-key groups 1024 B apart, 64-column panels kKVPanel apart)
+                    // 16-key group kk at kk * kVGroup, its two 8-key halves 1024 B
+                    // apart, 64-column panels 2048 B apart)
 #pragma unroll
                     for (int kk = 0; kk < kTN / 16; ++kk)
                         umma_bf16_ts(tmem + t * kTileCols + kOCol, tmem + t * kTileCols + kk * 8,
-                                     umma_desc_sw128(v_addr + kk * 2048, kKVPanel, 1024), idesc_o,
+                                     umma_desc_sw128(v_addr + kk * kVGroup, 2048, 1024), idesc_o,
                                      (j > 0 || kk > 0) ? 1u : 0u);
                     if (j + 1 < n_kt) {
                         if (t == 0) {
-                            ok = wait_slot(2 * j + 2);
+                            ok = wait_k(j + 1);
                             if (!ok) break;
                             tc_fence_after();
                         }
@@ -392,8 +410,8 @@ __global__ void __launch_bounds__(320, 1) prefill_tc_kernel(const __grid_constan
                     }
                 }
                 if (!ok) break;
-                umma_commit(&slot_empty[(2 * j + 1) % NS]);
-                if (j + 1 < n_kt) umma_commit(&slot_empty[(2 * j + 2) % NS]);
+                umma_commit(&v_empty[j % NV]);
+                if (j + 1 < n_kt) umma_commit(&k_empty[(j + 1) % NK]);
             }
             if (!ok) {
                 report(p.dev_status, PKV_DEV_TIMEOUT);
@@ -490,14 +508,13 @@ __global__ void __launch_bounds__(320, 1) prefill_tc_kernel(const __grid_constan
             // last tile: V rows of keys past the last one may hold anything; zero
             // them once V_j has landed (both warpgroups write the same zeros)
             if (j == n_kt - 1 && (n_keys & 15) != 0) {
-                const int vi = 2 * j + 1;
-                ok = __all_sync(0xffffffffu, mbar_wait(&slot_full[vi % NS], (vi / NS) & 1, abort_flag));
+                ok = __all_sync(0xffffffffu, mbar_wait(&v_full[j % NV], (j / NV) & 1, abort_flag));
                 if (!ok) break;
                 const int first = n_keys - key_base, stop = ((n_keys + 15) & ~15) - key_base;
-                uint8_t *vs = ring + (vi % NS) * kSlotBytes;
+                uint8_t *vs = v_ring + (j % NV) * kSlotBytes;
                 for (int i = r; i < (stop - first) * PANELS * 8; i += kTM) {
                     const int row = first + i / (PANELS * 8), pc = i % (PANELS * 8);
-                    *reinterpret_cast<uint4 *>(vs + (pc / 8) * kKVPanel + swz128(row, pc % 8)) =
+                    *reinterpret_cast<uint4 *>(vs + (row / 16) * kVGroup + (pc / 8) * 2048 + swz128(row % 16, pc % 8)) =
                         make_uint4(0, 0, 0, 0);
                 }
                 fence_proxy_async_smem();   // zeroed V rows visible to the tensor core
@@ -583,16 +600,29 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream)
             return cudaErrorInvalidValue;
     }
     const uint64_t rows = (uint64_t)(d.n_blocks + 1) * d.block_size;
-    const uint64_t dims[3] = {(uint64_t)d.head_dim, (uint64_t)d.n_kv_heads, rows};
-    const uint64_t strides[2] = {(uint64_t)d.head_dim * 2, (uint64_t)d.n_kv_heads * d.head_dim * 2};
-    const uint32_t box[3] = {64u, 1u, 16u};
-    if (encode_tensor_map(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(a.k_pool), dims, strides,
-                          box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS ||
-        encode_tensor_map(&vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(a.v_pool), dims, strides,
-                          box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
-        return cudaErrorInvalidValue;
+    const uint64_t row_bytes = (uint64_t)d.n_kv_heads * d.head_dim * 2;
+    {
+        // K: {64 columns, kv head, pool row}, one head and 16 rows per box
+        const uint64_t dims[3] = {(uint64_t)d.head_dim, (uint64_t)d.n_kv_heads, rows};
+        const uint64_t strides[2] = {(uint64_t)d.head_dim * 2, row_bytes};
+        const uint32_t box[3] = {64u, 1u, 16u};
+        if (encode_tensor_map(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(a.k_pool), dims, strides,
+                              box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    {
+        // V: {64 columns, pool row, 64-column panel of all heads}: a box of 16
+        // rows and a head's panels lands as [panel][row][128 B]
+        const uint32_t panels = (uint32_t)d.head_dim / 64u;
+        const uint64_t dims[3] = {64u, rows, (uint64_t)d.n_kv_heads * panels};
+        const uint64_t strides[2] = {row_bytes, 128u};
+        const uint32_t box[3] = {64u, 16u, panels};
+        if (encode_tensor_map(&vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(a.v_pool), dims, strides,
+                              box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
 
-    const int slots = d.head_dim == 128 ? ring_slots<128>() : ring_slots<64>();
+    const int slots = d.head_dim == 128 ? k_slots<128>() + v_slots<128>() : k_slots<64>() + v_slots<64>();
     const size_t smem = 1024 + (size_t)kNQ * kTM * d.head_dim * 2 + (size_t)slots * kTN * d.head_dim * 2 +
                         32 * sizeof(uint64_t) + (kSortMaxSeqs + 1) * sizeof(int32_t);
     const int64_t ctas = (int64_t)p.pairs_per_seq * d.n_kv_heads * a.n_seqs;
@@ -602,11 +632,11 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream)
     if (d.head_dim == 128) {
         e = cudaFuncSetAttribute(prefill_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        prefill_tc_kernel<128><<<grid, 320, smem, stream>>>(qmap, kmap, vmap, p);
+        prefill_tc_kernel<128><<<grid, 384, smem, stream>>>(qmap, kmap, vmap, p);
     } else {
         e = cudaFuncSetAttribute(prefill_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        prefill_tc_kernel<64><<<grid, 320, smem, stream>>>(qmap, kmap, vmap, p);
+        prefill_tc_kernel<64><<<grid, 384, smem, stream>>>(qmap, kmap, vmap, p);
     }
     return cudaGetLastError();
 }
