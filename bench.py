@@ -31,11 +31,16 @@ sys.path.insert(0, ROOT)
 METRIC = "paged decode attention HBM GB/s (% of GB300 peak) and seq-steps/s per layer"
 FALLBACK_HBM_GBS = 6800.0
 
-# dram__bytes_read.sum + dram__bytes_write.sum per launch of decode_split_kernel
-# (the dominant kernel of the decode step) on the config-1 workload, from the ncu
-# capture summarised in profiles/decode_cfg1_llama8b_batch64.md, valid while
-# the kernel sources hash to source_sha.
-NCU_TRAFFIC = {"source_sha": "3b735f5fa5cbec47", "bytes_per_launch": 544754432 + 4990976}
+# dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant
+# kernel per workload (decode_split_kernel for configs 1, 2, 4; prefill_tc_kernel
+# for config 3), from the ncu captures summarised under profiles/, valid while
+# the kernel's sources hash to source_sha.
+NCU_TRAFFIC = {
+    "decode": {"sources": ("decode.cu", "common.cuh", "launch.h"), "source_sha": "242eac3e195b354b",
+               "bytes_per_launch": {1: 544729856 + 4279552, 2: 310421504 + 3900160, 4: 1345788672 + 33092352}},
+    "prefill": {"sources": ("prefill_tc.cu", "common.cuh", "launch.h"), "source_sha": "2e84a4c06f67639b",
+                "bytes_per_launch": {3: 197249024 + 19143424}},
+}
 
 
 def parse_args():
@@ -61,10 +66,10 @@ def measured_peaks(key="hbm_gbs"):
         return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": 1900.0}[key], "fallback"
 
 
-def kernel_source_sha():
+def kernel_source_sha(names=("decode.cu", "common.cuh", "launch.h")):
     import hashlib
     h = hashlib.sha256()
-    for name in ("decode.cu", "common.cuh", "launch.h"):
+    for name in names:
         with open(os.path.join(ROOT, "paged_kv_cache_212_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -85,6 +90,15 @@ def weak_scaling_value(bytes_per_step_per_rank, world, ms_per_step):
     """Whole-job throughput in GB/s: every rank moves its own step bytes in
     the slowest rank's step time."""
     return world * bytes_per_step_per_rank / (ms_per_step * 1e-3) / 1e9
+
+
+def ncu_traffic(kind, cfg):
+    """Per-launch DRAM traffic of the dominant kernel from the committed ncu
+    capture, or None when its sources changed since (or no capture exists)."""
+    t = NCU_TRAFFIC[kind]
+    if t["source_sha"] != kernel_source_sha(t["sources"]):
+        return None
+    return t["bytes_per_launch"].get(cfg)
 
 
 def make_workload(cfg, device):
@@ -383,7 +397,8 @@ def run_prefill_bench(args, P, w, device, rank, world):
             "config": {"workload": w.name, "n_seqs": w.n_seqs, "chunk": w.n_new,
                        "prefix": [int(x) for x in w.stored_lens], "impl": os.environ.get("PKV_PREFILL_IMPL", "tcgen05")},
             "roofline": {"bound": "tensor", "kernel": "paged_prefill_attention", "achieved": round(ach, 2),
-                         "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4), "traffic": None,
+                         "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4),
+                         "traffic": ncu_traffic("prefill", 3),
                          "flops_per_launch": flops, "avg_launch_ms": round(pre_ms, 5),
                          "peak_source": f"{kind} bf16_tflops (burst)"},
             "gpu_launches": 2 * K, "clocks": clk.summary()}
@@ -503,7 +518,7 @@ def main():
     peak, peak_kind = measured_peaks()
     value = weak_scaling_value(step_b, world, ms_per_step)
     achieved = step_b / (decode_ms * 1e-3) / 1e9
-    traffic = NCU_TRAFFIC["bytes_per_launch"] if NCU_TRAFFIC["source_sha"] == kernel_source_sha() else None
+    traffic = ncu_traffic("decode", args.config)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
