@@ -53,6 +53,8 @@ def parse_args():
     ap.add_argument("--split", type=int, default=0, help="decode split_tokens (0 = library default)")
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--blocks", action="store_true",
+                    help="time the host-side block manager's per-step calls instead (no GPU)")
     return ap.parse_args()
 
 
@@ -406,6 +408,83 @@ def run_prefill_bench(args, P, w, device, rank, world):
         print(json.dumps(line), flush=True)
 
 
+def blocks_serving_loop(mgr, n_slots, steps, rng_seed=20265):
+    """A continuous-batching loop on a block manager (library or oracle: same
+    method names).  Every step: reserve_step (preemption), begin_step (growth,
+    copy-on-write pairs), export of the tables, end_step -- these four are
+    timed; then, untimed, sequences that ran out of tokens are released and
+    empty slots refilled with new prompts, a quarter of them as forks of a live
+    sequence (sharing its blocks).  Returns (seconds in the four calls,
+    copies, victims)."""
+    import random
+    rng = random.Random(rng_seed)
+    budget = [rng.randrange(64, 1024) for _ in range(n_slots)]   # tokens each sequence still generates
+    for s in range(n_slots):
+        mgr.admit(s, rng.randrange(16, 2048))
+    copies = victims = 0
+    busy = 0.0
+    for _ in range(steps):
+        t0 = time.perf_counter()
+        v = mgr.reserve_step()
+        c = mgr.begin_step()
+        mgr.export()
+        mgr.end_step()
+        busy += time.perf_counter() - t0
+        victims += len(v)
+        copies += len(c)
+        _, lens, active = mgr.export()
+        act = [int(x) for x in active]
+        ln = [int(x) for x in lens]
+        for s in range(n_slots):
+            if act[s]:
+                budget[s] -= 1
+                if budget[s] > 0:
+                    continue
+                mgr.release(s)
+                act[s] = 0
+            n = rng.randrange(16, 2048)
+            live = [t for t in range(n_slots) if act[t] and ln[t] < 2048]
+            if live and rng.random() < 0.25:
+                src = rng.choice(live)
+                mgr.fork(src, s)
+                act[s], ln[s] = 1, ln[src]
+            elif mgr.can_admit([n]):
+                mgr.admit(s, n)
+                act[s], ln[s] = 1, n
+            budget[s] = rng.randrange(64, 1024)
+    return busy, copies, victims
+
+
+def run_blocks_bench(args):
+    """Host-side block manager (pagedkv_blocks.h) per-step cost on a 256-slot
+    serving loop, the plain-Python oracle of the same rules timed beside it."""
+    import paged_kv_cache_212_gb300 as P
+    from paged_kv_cache_212_gb300 import build as B
+    B.build()
+    P.load_library()
+    n_slots, bs, max_blocks = 256, 16, 256
+    n_blocks = int(1.25 * n_slots * 2048 / bs)
+    steps = min(args.steps, 2000)
+    mgr = P.BlockManager(n_blocks, bs, n_slots, max_blocks)
+    busy, copies, victims = blocks_serving_loop(mgr, n_slots, steps)
+    line = {"metric": "block manager steps/s (256 slots: reserve_step, begin_step, export, end_step)",
+            "value": round(steps / busy, 1), "unit": "steps/s", "n_gpus": 0, "steps": steps, "warmup": 0,
+            "ms_per_step": round(1e3 * busy / steps, 4), "higher_is_better": True, "scaling": "none",
+            "vs_baseline": None, "dtype": "int32", "data": "synthetic",
+            "config": {"workload": "block manager serving loop", "n_slots": n_slots, "block_size": bs,
+                       "n_blocks": n_blocks, "max_blocks": max_blocks, "copies": copies, "victims": victims},
+            "note": "host code through the Python binding (ctypes call overhead included)"}
+    if not args.no_cpu_baseline:
+        sys.path.insert(0, ROOT)
+        from oracle.block_manager import BlockManagerOracle
+        osteps = max(1, min(steps, 200))
+        ref = BlockManagerOracle(n_blocks, bs, n_slots, max_blocks)
+        obusy, _, _ = blocks_serving_loop(ref, n_slots, osteps)
+        line["cpu_baseline"] = {"value": round(osteps / obusy, 1), "unit": "steps/s", "cores": 1, "kind": "oracle",
+                                "sample": f"first {osteps} steps of the same loop"}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     rank = int(os.environ.get("RANK", "0"))
@@ -413,6 +492,10 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         run_reference(args, rank, world)
+        return
+    if args.blocks:
+        if rank == 0:
+            run_blocks_bench(args)
         return
 
     import torch

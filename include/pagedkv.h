@@ -58,7 +58,9 @@ enum pkv_status {
     PKV_ERR_UNSUPPORTED = 2,  /* head_dim, block_size, group size or kv dtype not supported */
     PKV_ERR_OUT_OF_RANGE = 3, /* a host-checkable size is out of range (e.g. n_new > table) */
     PKV_ERR_WORKSPACE = 4,    /* workspace null or smaller than required */
-    PKV_ERR_CUDA = 5          /* a CUDA call failed; pkv_last_cuda_error() says which */
+    PKV_ERR_CUDA = 5,         /* a CUDA call failed; pkv_last_cuda_error() says which */
+    PKV_ERR_OUT_OF_BLOCKS = 6, /* block manager: not enough free blocks (nothing changed) */
+    PKV_ERR_STATE = 7         /* block manager: the call does not fit the current state */
 };
 
 /* Bits OR-ed into *dev_status by the kernels. */
@@ -136,6 +138,27 @@ int paged_kv_gather(const pkv_bf16 *k_pool, const pkv_bf16 *v_pool, pkv_dims dim
                     const int32_t *block_tables, int32_t max_blocks, const int32_t *lens,
                     int32_t n_seqs, int32_t out_tokens, pkv_bf16 *k_out, pkv_bf16 *v_out,
                     int32_t *dev_status, pkv_stream_t stream);
+
+/*
+ * paged_kv_copy_blocks -- copy whole pool blocks on the device: the device half
+ * of copy-on-write for blocks shared between sequences (libmir-metal
+ * paged/mod.rs, PagedStore::snapshot shares a sequence's pages by reference
+ * count; a page that is still shared gets a private copy before it is written
+ * -- pkv_bm_begin_step in pagedkv_blocks.h reports the pairs).
+ *   pairs    int32 [n_pairs][2] device, 8-byte aligned: (source, destination)
+ *            block ids in [0, n_blocks]
+ *   k_pool, v_pool  bf16 pools (PKV_KV_BF16) or int8 code pools (PKV_KV_INT8,
+ *            then k_scales / v_scales [n_blocks + 1][block_size][n_kv_heads]
+ *            are copied too, else ignored)
+ * For every pair, block destination becomes a bit-exact copy of block source
+ * (all block_size rows, every kv head, K and V).  Destinations must be
+ * distinct and no destination may be a source in the same call (the order of
+ * the copies is not defined).  A pair naming an id outside [0, n_blocks] is
+ * skipped (PKV_DEV_BAD_BLOCK_ID).  n_pairs == 0 is a no-op.
+ */
+int paged_kv_copy_blocks(const int32_t *pairs, int32_t n_pairs, void *k_pool, void *v_pool, float *k_scales,
+                         float *v_scales, int32_t kv_dtype, pkv_dims dims, int32_t *dev_status,
+                         pkv_stream_t stream);
 
 /*
  * pkv_decode_workspace_bytes -- size of the workspace paged_decode_attention

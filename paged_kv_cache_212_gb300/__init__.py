@@ -24,7 +24,12 @@ DEV_WORKSPACE_OVERFLOW, DEV_TIMEOUT = 8, 16
 
 EXPORTS = ("pkv_status_string", "pkv_last_cuda_error", "paged_kv_write", "paged_kv_write_int8",
            "paged_kv_gather", "pkv_decode_workspace_bytes", "paged_decode_attention",
-           "paged_prefill_attention", "paged_decode_attention_noalloc", "paged_decode_step")
+           "paged_prefill_attention", "paged_decode_attention_noalloc", "paged_decode_step",
+           "paged_kv_copy_blocks",
+           # host-side block manager (include/pagedkv_blocks.h)
+           "pkv_bm_create", "pkv_bm_destroy", "pkv_bm_alloc", "pkv_bm_free", "pkv_bm_num_free",
+           "pkv_bm_peak_used", "pkv_bm_refcount", "pkv_bm_can_admit", "pkv_bm_admit", "pkv_bm_release",
+           "pkv_bm_fork", "pkv_bm_reserve_step", "pkv_bm_begin_step", "pkv_bm_end_step", "pkv_bm_export")
 NOALLOC_DECODE_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
@@ -72,9 +77,31 @@ def load_library(path: str = LIB_PATH):
                                                    ctypes.c_float, i32, i64, P, P, P, P]
     lib.paged_decode_step.argtypes = [P, P, P, i32, P, i32, P, P, P, P, i32, Dims, P, i32, P, i32,
                                       ctypes.c_float, i32, P, P, P, sz, P, P]
+    lib.paged_kv_copy_blocks.argtypes = [P, i32, P, P, P, P, i32, Dims, P, P]
     for fn in ("paged_kv_write", "paged_kv_write_int8", "paged_kv_gather", "paged_decode_attention",
-               "paged_prefill_attention", "paged_decode_attention_noalloc", "paged_decode_step"):
+               "paged_prefill_attention", "paged_decode_attention_noalloc", "paged_decode_step",
+               "paged_kv_copy_blocks"):
         getattr(lib, fn).restype = ctypes.c_int
+    PP = ctypes.POINTER(ctypes.c_void_p)
+    lib.pkv_bm_create.argtypes = [i32, i32, i32, i32, PP]
+    lib.pkv_bm_destroy.argtypes = [P]
+    lib.pkv_bm_destroy.restype = None
+    lib.pkv_bm_alloc.argtypes = [P, P]
+    lib.pkv_bm_free.argtypes = [P, P, i32]
+    lib.pkv_bm_num_free.argtypes = [P]
+    lib.pkv_bm_peak_used.argtypes = [P]
+    lib.pkv_bm_refcount.argtypes = [P, i32]
+    lib.pkv_bm_can_admit.argtypes = [P, P, i32, P]
+    lib.pkv_bm_admit.argtypes = [P, i32, i32]
+    lib.pkv_bm_release.argtypes = [P, i32]
+    lib.pkv_bm_fork.argtypes = [P, i32, i32]
+    lib.pkv_bm_reserve_step.argtypes = [P, P, P]
+    lib.pkv_bm_begin_step.argtypes = [P, P, P]
+    lib.pkv_bm_end_step.argtypes = [P]
+    lib.pkv_bm_export.argtypes = [P, P, P, P]
+    for fn in EXPORTS:
+        if fn.startswith("pkv_bm_") and fn != "pkv_bm_destroy":
+            getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -177,6 +204,25 @@ def paged_kv_gather(k_pool, v_pool, block_tables, lens, out_tokens, k_out=None, 
                              _ptr(dev_status), _stream(stream))
     _check("paged_kv_gather", st)
     return k_out, v_out
+
+
+def paged_kv_copy_blocks(pairs, k_pool, v_pool, k_scales=None, v_scales=None, dev_status=None, stream=None):
+    """Copy whole pool blocks: pairs int32 [n, 2] of (source, destination) ids
+    on the device (the device half of copy-on-write)."""
+    lib = load_library()
+    dev = k_pool.device
+    _need(pairs, "pairs", torch.int32, 2, dev)
+    int8 = k_pool.dtype == torch.int8
+    if int8:
+        _need(k_scales, "k_scales", torch.float32, 3, dev)
+        _need(v_scales, "v_scales", torch.float32, 3, dev)
+    else:
+        _need(k_pool, "k_pool", torch.bfloat16, 4, dev)
+    _need(v_pool, "v_pool", k_pool.dtype, 4, dev)
+    st = lib.paged_kv_copy_blocks(_ptr(pairs), pairs.shape[0], _ptr(k_pool), _ptr(v_pool), _ptr(k_scales),
+                                  _ptr(v_scales), PKV_KV_INT8 if int8 else PKV_KV_BF16, pool_dims(k_pool),
+                                  _ptr(dev_status), _stream(stream))
+    _check("paged_kv_copy_blocks", st)
 
 
 def decode_workspace_bytes(n_seqs, n_q_heads, head_dim, max_total_ctx_tokens, split_tokens=0) -> int:
@@ -328,3 +374,89 @@ def paged_prefill_attention(q, k_pool, v_pool, block_tables, prefix_lens, softma
                                      _stream(stream))
     _check("paged_prefill_attention", st)
     return out
+
+
+class BlockManager:
+    """The library's host-side block manager (include/pagedkv_blocks.h): free
+    stack and reference counts of n_blocks blocks, n_slots sequence slots with
+    tables of max_blocks entries.  Methods mirror the C calls; failures raise
+    PagedKVError (nothing changed)."""
+
+    def __init__(self, n_blocks, block_size, n_slots, max_blocks):
+        self._lib = load_library()
+        h = ctypes.c_void_p()
+        _check("pkv_bm_create", self._lib.pkv_bm_create(int(n_blocks), int(block_size), int(n_slots),
+                                                          int(max_blocks), ctypes.byref(h)))
+        self._h = h
+        self.n_blocks, self.block_size, self.n_slots, self.max_blocks = n_blocks, block_size, n_slots, max_blocks
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            self._lib.pkv_bm_destroy(h)
+            self._h = None
+
+    def _call(self, fn, *args):
+        _check(fn, getattr(self._lib, fn)(self._h, *args))
+
+    @staticmethod
+    def _ints(values):
+        arr = (ctypes.c_int32 * max(1, len(values)))(*values)
+        return arr
+
+    def alloc(self) -> int:
+        b = ctypes.c_int32()
+        self._call("pkv_bm_alloc", ctypes.byref(b))
+        return b.value
+
+    def free(self, blocks):
+        self._call("pkv_bm_free", self._ints(list(blocks)), len(blocks))
+
+    @property
+    def num_free(self) -> int:
+        return self._lib.pkv_bm_num_free(self._h)
+
+    @property
+    def peak_used(self) -> int:
+        return self._lib.pkv_bm_peak_used(self._h)
+
+    def refcount(self, block) -> int:
+        return self._lib.pkv_bm_refcount(self._h, int(block))
+
+    def can_admit(self, lengths) -> bool:
+        ok = ctypes.c_int32()
+        self._call("pkv_bm_can_admit", self._ints(list(lengths)), len(lengths), ctypes.byref(ok))
+        return bool(ok.value)
+
+    def admit(self, slot, n_tokens):
+        self._call("pkv_bm_admit", int(slot), int(n_tokens))
+
+    def release(self, slot):
+        self._call("pkv_bm_release", int(slot))
+
+    def fork(self, src_slot, dst_slot):
+        self._call("pkv_bm_fork", int(src_slot), int(dst_slot))
+
+    def reserve_step(self):
+        victims = (ctypes.c_int32 * self.n_slots)()
+        n = ctypes.c_int32()
+        self._call("pkv_bm_reserve_step", victims, ctypes.byref(n))
+        return list(victims[:n.value])
+
+    def begin_step(self):
+        copies = (ctypes.c_int32 * (2 * self.n_slots))()
+        n = ctypes.c_int32()
+        self._call("pkv_bm_begin_step", copies, ctypes.byref(n))
+        return [(copies[2 * i], copies[2 * i + 1]) for i in range(n.value)]
+
+    def end_step(self):
+        self._call("pkv_bm_end_step")
+
+    def export(self):
+        """(tables [n_slots][max_blocks], lens [n_slots], active [n_slots]) as int32 CPU tensors."""
+        tables = torch.empty((self.n_slots, self.max_blocks), dtype=torch.int32)
+        lens = torch.empty(self.n_slots, dtype=torch.int32)
+        active = torch.empty(self.n_slots, dtype=torch.int32)
+        self._call("pkv_bm_export", ctypes.c_void_p(tables.data_ptr()), ctypes.c_void_p(lens.data_ptr()),
+                   ctypes.c_void_p(active.data_ptr()))
+        return tables, lens, active

@@ -1,6 +1,7 @@
 """Build libpagedkv.so in-tree with nvcc for sm_103a (GB300).
 
-Each .cu translation unit compiles in parallel to an object file, then one
+Each .cu (device) and .cpp (host-only) translation unit compiles in parallel
+to an object file, then one
 link step produces the shared library (cudart linked statically, so the
 library needs only the driver at run time).  Rebuilds only when a source or
 header is newer than the library.
@@ -30,12 +31,12 @@ def nvcc() -> str:
 
 
 def _sources():
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _deps():
     return _sources() + glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h")) + \
-        [os.path.join(ROOT, "include", "pagedkv.h"), os.path.abspath(__file__)]
+        glob.glob(os.path.join(ROOT, "include", "*.h")) + [os.path.abspath(__file__)]
 
 
 def up_to_date() -> bool:
@@ -56,7 +57,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
         flags += ["-Xptxas", "-v"]
 
     def compile_one(src):
-        obj = os.path.join(BUILD_DIR, os.path.basename(src).replace(".cu", ".o"))
+        obj = os.path.join(BUILD_DIR, os.path.splitext(os.path.basename(src))[0] + ".o")
         cmd = [cc, *flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:

@@ -127,6 +127,8 @@ const char *pkv_status_string(int status)
     case PKV_ERR_OUT_OF_RANGE: return "PKV_ERR_OUT_OF_RANGE";
     case PKV_ERR_WORKSPACE: return "PKV_ERR_WORKSPACE";
     case PKV_ERR_CUDA: return "PKV_ERR_CUDA";
+    case PKV_ERR_OUT_OF_BLOCKS: return "PKV_ERR_OUT_OF_BLOCKS";
+    case PKV_ERR_STATE: return "PKV_ERR_STATE";
     default: return "PKV_ERR_UNKNOWN";
     }
 }
@@ -193,6 +195,27 @@ int paged_kv_gather(const pkv_bf16 *k_pool, const pkv_bf16 *v_pool, pkv_dims dim
     GatherArgs a{k_pool, v_pool, dims, block_tables, max_blocks, lens, n_seqs, out_tokens, k_out, v_out,
                  dev_status};
     return cuda_status(launch_gather(a, sms, (cudaStream_t)stream));
+}
+
+int paged_kv_copy_blocks(const int32_t *pairs, int32_t n_pairs, void *k_pool, void *v_pool, float *k_scales,
+                         float *v_scales, int32_t kv_dtype, pkv_dims dims, int32_t *dev_status,
+                         pkv_stream_t stream)
+{
+    int st = check_dims(dims);
+    if (st != PKV_OK) return st;
+    if (n_pairs < 0) return PKV_ERR_INVALID_ARG;
+    if (kv_dtype != PKV_KV_BF16 && kv_dtype != PKV_KV_INT8) return PKV_ERR_UNSUPPORTED;
+    if (n_pairs == 0) return PKV_OK;
+    if (!pairs || !k_pool || !v_pool || !aligned16(k_pool) || !aligned16(v_pool)) return PKV_ERR_INVALID_ARG;
+    const bool int8 = kv_dtype == PKV_KV_INT8;
+    if (int8 && (!k_scales || !v_scales || !aligned16(k_scales) || !aligned16(v_scales)))
+        return PKV_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(pairs) % 8 != 0) return PKV_ERR_INVALID_ARG;
+    int sms = 0;
+    st = num_sms_of_current_device(&sms);
+    if (st != PKV_OK) return st;
+    return cuda_status(launch_copy_blocks(pairs, n_pairs, k_pool, v_pool, k_scales, v_scales, int8, dims,
+                                          dev_status, sms, (cudaStream_t)stream));
 }
 
 size_t pkv_decode_workspace_bytes(int32_t n_seqs, int32_t n_q_heads, int32_t head_dim,

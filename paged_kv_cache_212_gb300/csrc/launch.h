@@ -97,6 +97,9 @@ cudaError_t launch_write_bf16(const WriteArgs &a, cudaStream_t stream);
 cudaError_t launch_write_int8(const WriteArgs &a, float *k_scales, float *v_scales,
                               cudaStream_t stream);
 cudaError_t launch_gather(const GatherArgs &a, int num_sms, cudaStream_t stream);
+cudaError_t launch_copy_blocks(const int32_t *pairs, int32_t n_pairs, void *k_pool, void *v_pool, float *k_scales,
+                               float *v_scales, bool int8, const pkv_dims &d, int32_t *dev_status, int num_sms,
+                               cudaStream_t stream);
 // write (nullable): this step's new rows, written by the first launch of the
 // decode (the fused decode step).
 cudaError_t launch_decode(const DecodeArgs &a, int num_sms, cudaStream_t stream, const WriteArgs *write = nullptr);

@@ -82,6 +82,39 @@ __global__ void __launch_bounds__(256) gather_kernel(
     }
 }
 
+// Block copy (the device half of copy-on-write): the index space is, per
+// (source, destination) pair, the 16-byte vectors of the K block, the V block
+// and, for int8 pools, the K and V scale rows of the block.
+__global__ void __launch_bounds__(256) copy_blocks_kernel(uint4 *__restrict__ k_pool, uint4 *__restrict__ v_pool,
+                                                          uint4 *__restrict__ k_scales, uint4 *__restrict__ v_scales,
+                                                          const int2 *__restrict__ pairs, int32_t n_blocks,
+                                                          int64_t block_vecs, int64_t scale_vecs, int64_t n_vecs,
+                                                          int32_t *dev_status)
+{
+    const int64_t per_pair = 2 * block_vecs + 2 * scale_vecs;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_vecs; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t pr = i / per_pair, r = i % per_pair;
+        const int2 sd = __ldg(pairs + pr);
+        if (sd.x < 0 || sd.x > n_blocks || sd.y < 0 || sd.y > n_blocks) {
+            if (r == 0) report(dev_status, PKV_DEV_BAD_BLOCK_ID);
+            continue;
+        }
+        uint4 *base;
+        int64_t per_block, off;
+        if (r < 2 * block_vecs) {
+            base = r < block_vecs ? k_pool : v_pool;
+            per_block = block_vecs;
+            off = r % block_vecs;
+        } else {
+            const int64_t q = r - 2 * block_vecs;
+            base = q < scale_vecs ? k_scales : v_scales;
+            per_block = scale_vecs;
+            off = q % scale_vecs;
+        }
+        base[(int64_t)sd.y * per_block + off] = base[(int64_t)sd.x * per_block + off];
+    }
+}
+
 cudaError_t launch_write_bf16(const WriteArgs &a, cudaStream_t stream)
 {
     const int64_t n_vecs = (int64_t)a.n_seqs * a.n_new * (a.dims.n_kv_heads * a.dims.head_dim / 8);
@@ -116,6 +149,23 @@ cudaError_t launch_gather(const GatherArgs &a, int num_sms, cudaStream_t stream)
         (const uint4 *)a.k_pool, (const uint4 *)a.v_pool, a.dims.n_blocks, a.dims.block_size,
         a.dims.n_kv_heads, d_vecs, a.tables, a.max_blocks, a.lens, a.out_tokens, (uint4 *)a.k_out,
         (uint4 *)a.v_out, n_vecs, a.dev_status);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy_blocks(const int32_t *pairs, int32_t n_pairs, void *k_pool, void *v_pool, float *k_scales,
+                               float *v_scales, bool int8, const pkv_dims &d, int32_t *dev_status, int num_sms,
+                               cudaStream_t stream)
+{
+    const int64_t elems = (int64_t)d.block_size * d.n_kv_heads * d.head_dim;
+    const int64_t block_vecs = elems * (int8 ? 1 : 2) / 16;
+    const int64_t scale_vecs = int8 ? (int64_t)d.block_size * d.n_kv_heads * 4 / 16 : 0;
+    const int64_t n_vecs = (int64_t)n_pairs * (2 * block_vecs + 2 * scale_vecs);
+    if (n_vecs == 0) return cudaSuccess;
+    int64_t grid = (n_vecs + 255) / 256, cap = (int64_t)num_sms * 8;
+    if (grid > cap) grid = cap;
+    copy_blocks_kernel<<<(unsigned)grid, 256, 0, stream>>>((uint4 *)k_pool, (uint4 *)v_pool, (uint4 *)k_scales,
+                                                           (uint4 *)v_scales, (const int2 *)pairs, d.n_blocks,
+                                                           block_vecs, scale_vecs, n_vecs, dev_status);
     return cudaGetLastError();
 }
 
