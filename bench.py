@@ -36,9 +36,9 @@ FALLBACK_HBM_GBS = 6800.0
 # for config 3), from the ncu captures summarised under profiles/, valid while
 # the kernel's sources hash to source_sha.
 NCU_TRAFFIC = {
-    "decode": {"sources": ("decode.cu", "common.cuh", "launch.h"), "source_sha": "242eac3e195b354b",
+    "decode": {"sources": ("decode.cu", "common.cuh", "launch.h"), "source_sha": "3f5b4d465385e7e8",
                "bytes_per_launch": {1: 544729856 + 4279552, 2: 310421504 + 3900160, 4: 1345788672 + 33092352}},
-    "prefill": {"sources": ("prefill_tc.cu", "common.cuh", "launch.h"), "source_sha": "2e84a4c06f67639b",
+    "prefill": {"sources": ("prefill_tc.cu", "common.cuh", "launch.h"), "source_sha": "da1f86f79b1796a3",
                 "bytes_per_launch": {3: 197249024 + 19143424}},
 }
 
