@@ -55,6 +55,8 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--blocks", action="store_true",
                     help="time the host-side block manager's per-step calls instead (no GPU)")
+    ap.add_argument("--stream", type=int, default=0, metavar="N_SLOTS",
+                    help="decode config 1 from a pinned host tier through an N_SLOTS-block scratch pool")
     return ap.parse_args()
 
 
@@ -485,6 +487,67 @@ def run_blocks_bench(args):
     print(json.dumps(line), flush=True)
 
 
+def run_stream_bench(args, P, device):
+    """Config 1's decode with every K/V block in a pinned host tier, streamed
+    through a device scratch pool of args.stream blocks (pagedkv_stream.h).
+    When the batch has more blocks than the pool, the cyclic order evicts every
+    block before its reuse, so each call restages the whole context over the
+    CPU-GPU link: the link bounds this path."""
+    import torch
+    w = make_workload(1, device)
+    kp, vp, _, _ = fill_pool(P, w, device)
+    tables, start, ctx = w.tables.to(device), w.start_pos.to(device), w.ctx_lens.to(device)
+    q = w.q.to(device)
+    P.paged_kv_write(w.k_new.to(device), w.v_new.to(device), kp, vp, tables, start)
+    torch.cuda.synchronize()
+    host_k, host_v = kp.cpu().pin_memory(), vp.cpu().pin_memory()   # the tier: ids as in the tables
+    del kp, vp
+    n_slots = args.stream
+    pool_k = torch.zeros((n_slots + 1,) + tuple(host_k.shape[1:]), dtype=torch.bfloat16, device=device)
+    pool_v = torch.zeros_like(pool_k)
+    sp = P.ScratchPool(n_slots, w.n_seqs)
+    t_tab, t_len = w.tables.to(torch.int32), w.ctx_lens.to(torch.int32)
+    ws = torch.empty(P.streamed_workspace_bytes(w.n_seqs, w.n_q_heads, w.head_dim, n_slots, w.block_size),
+                     dtype=torch.uint8, device=device)
+    out = torch.empty_like(q)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        P.paged_decode_streamed(q, host_k, host_v, pool_k, pool_v, sp, t_tab, t_len, w.softmax_scale, out=out,
+                                workspace=ws, dev_status=status)
+
+    for _ in range(max(3, args.warmup)):
+        call()
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    # blocks staged per call (the plan is host bookkeeping: replay it on a copy)
+    blocks = sum(-(-int(L) // w.block_size) for L in w.ctx_lens)
+    steps = max(3, min(args.steps, 50))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    with ClockSampler(uuid) as clk:
+        time.sleep(0.25)
+        e0.record(stream)
+        for _ in range(steps):
+            call()
+        e1.record(stream)
+        torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    decode_b, _ = algorithmic_bytes(w)
+    block_bytes = 2 * w.block_size * w.n_kv_heads * w.head_dim * 2
+    staged = blocks * block_bytes if blocks > n_slots else 0
+    line = {"metric": "streamed paged decode GB/s (config 1 batch from a pinned host tier)",
+            "value": round(decode_b / (ms * 1e-3) / 1e9, 2), "unit": "GB/s", "n_gpus": 1, "steps": steps,
+            "warmup": max(3, args.warmup), "ms_per_step": round(ms, 4), "higher_is_better": True,
+            "scaling": "none", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "n_slots": n_slots, "blocks_per_call": blocks,
+                       "tiles_per_call": -(-blocks // n_slots), "host_tier_bytes": 2 * host_k.numel() * 2},
+            "staging": {"bytes_per_call": staged, "gbs": round(staged / (ms * 1e-3) / 1e9, 2)},
+            "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     rank = int(os.environ.get("RANK", "0"))
@@ -509,6 +572,10 @@ def main():
     import paged_kv_cache_212_gb300 as P
     P.load_library()
 
+    if args.stream:
+        if rank == 0:
+            run_stream_bench(args, P, device)
+        return
     w = make_workload(args.config, device)  # every rank owns an independent replica batch
     if args.config == 3:
         run_prefill_bench(args, P, w, device, rank, world)

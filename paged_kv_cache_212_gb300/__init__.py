@@ -29,7 +29,10 @@ EXPORTS = ("pkv_status_string", "pkv_last_cuda_error", "paged_kv_write", "paged_
            # host-side block manager (include/pagedkv_blocks.h)
            "pkv_bm_create", "pkv_bm_destroy", "pkv_bm_alloc", "pkv_bm_free", "pkv_bm_num_free",
            "pkv_bm_peak_used", "pkv_bm_refcount", "pkv_bm_can_admit", "pkv_bm_admit", "pkv_bm_release",
-           "pkv_bm_fork", "pkv_bm_reserve_step", "pkv_bm_begin_step", "pkv_bm_end_step", "pkv_bm_export")
+           "pkv_bm_fork", "pkv_bm_reserve_step", "pkv_bm_begin_step", "pkv_bm_end_step", "pkv_bm_export",
+           # decode streamed from a host tier (include/pagedkv_stream.h)
+           "pkv_sp_create", "pkv_sp_destroy", "pkv_sp_lookup", "pkv_sp_invalidate", "pkv_sp_plan_tile",
+           "paged_kv_stage_blocks", "pkv_streamed_workspace_bytes", "paged_decode_streamed")
 NOALLOC_DECODE_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
@@ -102,6 +105,20 @@ def load_library(path: str = LIB_PATH):
     for fn in EXPORTS:
         if fn.startswith("pkv_bm_") and fn != "pkv_bm_destroy":
             getattr(lib, fn).restype = ctypes.c_int
+    lib.pkv_sp_create.argtypes = [i32, i32, PP]
+    lib.pkv_sp_destroy.argtypes = [P]
+    lib.pkv_sp_destroy.restype = None
+    lib.pkv_sp_lookup.argtypes = [P, i32]
+    lib.pkv_sp_invalidate.argtypes = [P, i32]
+    lib.pkv_sp_plan_tile.argtypes = [P, P, i32, P, i32, i32, P, P, P, P, P, P]
+    lib.paged_kv_stage_blocks.argtypes = [P, i32, P, P, i32, P, P, Dims, P, P]
+    lib.pkv_streamed_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
+    lib.pkv_streamed_workspace_bytes.restype = sz
+    lib.paged_decode_streamed.argtypes = [P, i32, P, P, i32, P, P, Dims, P, P, i32, P, i32, ctypes.c_float, P, P,
+                                          P, sz, P, P]
+    for fn in ("pkv_sp_create", "pkv_sp_lookup", "pkv_sp_invalidate", "pkv_sp_plan_tile", "paged_kv_stage_blocks",
+               "paged_decode_streamed"):
+        getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -460,3 +477,105 @@ class BlockManager:
         self._call("pkv_bm_export", ctypes.c_void_p(tables.data_ptr()), ctypes.c_void_p(lens.data_ptr()),
                    ctypes.c_void_p(active.data_ptr()))
         return tables, lens, active
+
+
+class ScratchPool:
+    """Residency of a device scratch pool of n_slots blocks for decode streamed
+    from a host tier (include/pagedkv_stream.h)."""
+
+    def __init__(self, n_slots, max_seqs):
+        self._lib = load_library()
+        h = ctypes.c_void_p()
+        _check("pkv_sp_create", self._lib.pkv_sp_create(int(n_slots), int(max_seqs), ctypes.byref(h)))
+        self._h = h
+        self.n_slots, self.max_seqs = int(n_slots), int(max_seqs)
+
+    def __del__(self):
+        h = getattr(self, "_h", None)
+        if h is not None and h.value:
+            self._lib.pkv_sp_destroy(h)
+            self._h = None
+
+    def lookup(self, host_block) -> int:
+        return self._lib.pkv_sp_lookup(self._h, int(host_block))
+
+    def invalidate(self, host_block):
+        _check("pkv_sp_invalidate", self._lib.pkv_sp_invalidate(self._h, int(host_block)))
+
+    def plan_tile(self, host_tables, ctx_lens, block_size, cursor):
+        """Plan the next tile (host int32 tensors); returns (tile_tables, tile_lens,
+        pairs list, done) and advances cursor (a 2-element list)."""
+        host_tables = host_tables.to(torch.int32).contiguous()
+        ctx_lens = ctx_lens.to(torch.int32).contiguous()
+        n_seqs = ctx_lens.shape[0]
+        tt = torch.empty((n_seqs, self.n_slots), dtype=torch.int32)
+        tl = torch.empty(n_seqs, dtype=torch.int32)
+        pr = torch.empty((self.n_slots, 2), dtype=torch.int32)
+        cur = (ctypes.c_int32 * 2)(*cursor)
+        n, done = ctypes.c_int32(), ctypes.c_int32()
+        _check("pkv_sp_plan_tile", self._lib.pkv_sp_plan_tile(
+            self._h, ctypes.c_void_p(host_tables.data_ptr()), host_tables.shape[1],
+            ctypes.c_void_p(ctx_lens.data_ptr()), n_seqs, int(block_size), cur, ctypes.c_void_p(tt.data_ptr()),
+            ctypes.c_void_p(tl.data_ptr()), ctypes.c_void_p(pr.data_ptr()), ctypes.byref(n), ctypes.byref(done)))
+        cursor[0], cursor[1] = cur[0], cur[1]
+        return tt, tl, [tuple(x) for x in pr[:n.value].tolist()], bool(done.value)
+
+
+def paged_kv_stage_blocks(pairs, host_k, host_v, pool_k, pool_v, dev_status=None, stream=None):
+    """Copy host-tier blocks (pinned CPU tensors [n_host_blocks, bs, Hkv, D]
+    bf16) into scratch-pool slots (device [n_slots + 1, bs, Hkv, D]):
+    pairs int32 [n, 2] (host block, slot) on the device."""
+    lib = load_library()
+    dev = pool_k.device
+    _need(pairs, "pairs", torch.int32, 2, dev)
+    for t, n in ((host_k, "host_k"), (host_v, "host_v")):
+        if t.device.type != "cpu" or t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous bf16 CPU tensor [n_host_blocks, bs, Hkv, D]")
+    _need(pool_k, "pool_k", torch.bfloat16, 4, dev)
+    _need(pool_v, "pool_v", torch.bfloat16, 4, dev)
+    st = lib.paged_kv_stage_blocks(_ptr(pairs), pairs.shape[0], ctypes.c_void_p(host_k.data_ptr()),
+                                   ctypes.c_void_p(host_v.data_ptr()), host_k.shape[0], _ptr(pool_k), _ptr(pool_v),
+                                   pool_dims(pool_k), _ptr(dev_status), _stream(stream))
+    _check("paged_kv_stage_blocks", st)
+
+
+def streamed_workspace_bytes(n_seqs, n_q_heads, head_dim, n_slots, block_size) -> int:
+    n = load_library().pkv_streamed_workspace_bytes(int(n_seqs), int(n_q_heads), int(head_dim), int(n_slots),
+                                                    int(block_size))
+    if n == 0:
+        raise ValueError("invalid arguments to pkv_streamed_workspace_bytes")
+    return int(n)
+
+
+def paged_decode_streamed(q, host_k, host_v, pool_k, pool_v, scratch_pool, host_tables, ctx_lens, softmax_scale,
+                          out=None, lse_out=None, workspace=None, dev_status=None, stream=None):
+    """Decode attention over blocks in a host tier (pinned CPU tensors), streamed
+    through the device scratch pool (pool_k/pool_v [n_slots + 1, bs, Hkv, D]) one
+    tile of at most n_slots blocks at a time.  host_tables / ctx_lens: int32 CPU
+    tensors.  Returns out (bf16 [n_seqs, Hq, D])."""
+    lib = load_library()
+    dev = q.device
+    _need(q, "q", torch.bfloat16, 3, dev)
+    _need(pool_k, "pool_k", torch.bfloat16, 4, dev)
+    _need(pool_v, "pool_v", torch.bfloat16, 4, dev)
+    for t, n in ((host_k, "host_k"), (host_v, "host_v")):
+        if t.device.type != "cpu" or t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous bf16 CPU tensor [n_host_blocks, bs, Hkv, D]")
+    host_tables = host_tables.to(torch.int32).contiguous()
+    ctx_lens = ctx_lens.to(torch.int32).contiguous()
+    if host_tables.device.type != "cpu" or ctx_lens.device.type != "cpu":
+        raise ValueError("host_tables and ctx_lens are host (CPU) tensors")
+    n_seqs, n_q_heads, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if workspace is None:
+        workspace = torch.empty(streamed_workspace_bytes(n_seqs, n_q_heads, D, pool_k.shape[0] - 1,
+                                                         pool_k.shape[1]), dtype=torch.uint8, device=dev)
+    st = lib.paged_decode_streamed(
+        _ptr(q), n_q_heads, ctypes.c_void_p(host_k.data_ptr()), ctypes.c_void_p(host_v.data_ptr()),
+        host_k.shape[0], _ptr(pool_k), _ptr(pool_v), pool_dims(pool_k), scratch_pool._h,
+        ctypes.c_void_p(host_tables.data_ptr()), host_tables.shape[1], ctypes.c_void_p(ctx_lens.data_ptr()), n_seqs,
+        float(softmax_scale), _ptr(out), _ptr(lse_out), _ptr(workspace), workspace.numel(), _ptr(dev_status),
+        _stream(stream))
+    _check("paged_decode_streamed", st)
+    return out

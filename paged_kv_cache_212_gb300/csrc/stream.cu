@@ -1,0 +1,434 @@
+// stream.cu -- decode over a host tier streamed through a device scratch pool
+// (pagedkv_stream.h): the residency bookkeeping of the scratch pool (least
+// recently used slots are reused, slots of the current tile stay pinned), the
+// per-tile plan, the staging kernel that reads the host tier straight over the
+// CPU-GPU link, and the merge of each tile's attention into a float32 running
+// (output, log-sum-exp) state.
+#include <math.h>
+#include <string.h>
+
+#include <new>
+#include <unordered_map>
+#include <vector>
+
+#include "../../include/pagedkv_stream.h"
+#include "common.cuh"
+#include "launch.h"
+
+struct pkv_scratch_pool {
+    int32_t n_slots = 0, max_seqs = 0;
+    std::unordered_map<int32_t, int32_t> slot_of;   // host block -> slot
+    std::vector<int32_t> block_of;                  // slot -> host block (-1: empty)
+    // least recently used list over slots: head = next to reuse, tail = newest
+    std::vector<int32_t> prev, next;
+    int32_t head = -1, tail = -1;
+    std::vector<int64_t> pinned_tile;               // tile that last used the slot
+    int64_t tiles = 0;
+    // two pinned host staging buffers for tile plans, and their copy events
+    int32_t *stage[2] = {nullptr, nullptr};
+    cudaEvent_t copied[2] = {nullptr, nullptr};
+    size_t stage_ints = 0;
+
+    void unlink(int32_t s)
+    {
+        if (prev[s] >= 0) next[prev[s]] = next[s]; else head = next[s];
+        if (next[s] >= 0) prev[next[s]] = prev[s]; else tail = prev[s];
+        prev[s] = next[s] = -1;
+    }
+    void push_back(int32_t s)
+    {
+        prev[s] = tail;
+        next[s] = -1;
+        if (tail >= 0) next[tail] = s; else head = s;
+        tail = s;
+    }
+    void push_front(int32_t s)
+    {
+        next[s] = head;
+        prev[s] = -1;
+        if (head >= 0) prev[head] = s; else tail = s;
+        head = s;
+    }
+};
+
+namespace pkv {
+
+void record_cuda_error(int e);  // api.cu: the value pkv_last_cuda_error() reports
+
+namespace {
+
+constexpr int kPairsAlign = 2;   // pairs start at an even int offset (8-byte int2 loads)
+
+// plan layout in int32 units: tables [n_seqs][n_slots], lens [n_seqs], pairs [n_slots][2]
+size_t plan_ints(int32_t n_seqs, int32_t n_slots)
+{
+    size_t t = (size_t)n_seqs * n_slots + n_seqs;
+    t = (t + kPairsAlign - 1) / kPairsAlign * kPairsAlign;
+    return t + 2 * (size_t)n_slots;
+}
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+struct StreamWs {
+    void *decode_ws;
+    size_t decode_bytes;
+    int32_t *plan;              // device copy of the tile plan
+    __nv_bfloat16 *tile_out;
+    float *tile_lse, *acc, *acc_lse;
+};
+
+size_t stream_ws_bytes(int32_t n_seqs, int32_t n_q_heads, int32_t head_dim, int32_t n_slots, int32_t block_size,
+                       size_t *decode_bytes)
+{
+    const size_t d = pkv_decode_workspace_bytes(n_seqs, n_q_heads, head_dim,
+                                                (int64_t)n_slots * block_size, 0);
+    if (d == 0) return 0;
+    if (decode_bytes) *decode_bytes = d;
+    const size_t rows = (size_t)n_seqs * n_q_heads;
+    return align256(d) + align256(plan_ints(n_seqs, n_slots) * 4) + align256(rows * head_dim * 2) +
+           align256(rows * 4) + align256(rows * head_dim * 4) + align256(rows * 4);
+}
+
+// Host tier -> scratch pool: per (host block, slot) pair the 16-byte vectors of
+// the K block and the V block; the host tier is read through its device mapping.
+__global__ void __launch_bounds__(256) stage_blocks_kernel(const uint4 *__restrict__ host_k,
+                                                           const uint4 *__restrict__ host_v, uint4 *__restrict__ pool_k,
+                                                           uint4 *__restrict__ pool_v, const int2 *__restrict__ pairs,
+                                                           int32_t n_host, int32_t n_pool, int64_t block_vecs,
+                                                           int64_t n_vecs, int32_t *dev_status)
+{
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_vecs; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t pr = i / (2 * block_vecs), r = i % (2 * block_vecs);
+        const int2 hs = __ldg(pairs + pr);
+        if (hs.x < 0 || hs.x >= n_host || hs.y < 0 || hs.y > n_pool) {
+            if (r == 0) report(dev_status, PKV_DEV_BAD_BLOCK_ID);
+            continue;
+        }
+        const bool v = r >= block_vecs;
+        const int64_t off = v ? r - block_vecs : r;
+        const uint4 x = (v ? host_v : host_k)[(int64_t)hs.x * block_vecs + off];
+        (v ? pool_v : pool_k)[(int64_t)hs.y * block_vecs + off] = x;
+    }
+}
+
+// One warp per (sequence, query head) row: the tile's normalised output o_t and
+// log-sum-exp lse_t merge into the running (acc, lse) -- acc stays normalised:
+// acc = (acc e^(lse - M) + o_t e^(lse_t - M)) / (e^(lse - M) + e^(lse_t - M)).
+template <int D>
+__global__ void __launch_bounds__(256) merge_tile_kernel(const __nv_bfloat16 *__restrict__ tile_out,
+                                                         const float *__restrict__ tile_lse, float *__restrict__ acc,
+                                                         float *__restrict__ acc_lse, int64_t n_rows, int first)
+{
+    constexpr int EPL = D / 32;
+    const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= n_rows) return;
+    const float lt = tile_lse[row];
+    const __nv_bfloat16 *o = tile_out + row * D + lane * EPL;
+    float *a = acc + row * D + lane * EPL;
+    float ot[EPL];
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) ot[e] = __bfloat162float(o[e]);
+    if (first) {
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) a[e] = ot[e];
+        if (lane == 0) acc_lse[row] = lt;
+        return;
+    }
+    const float la = acc_lse[row];
+    const float M = fmaxf(la, lt);
+    if (M == -INFINITY) return;   // neither has any token yet
+    const float wa = expf(la - M), wt = expf(lt - M);
+    const float inv = 1.f / (wa + wt);
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) a[e] = (a[e] * wa + ot[e] * wt) * inv;
+    __syncwarp();
+    if (lane == 0) acc_lse[row] = M + logf(wa + wt);
+}
+
+template <int D>
+__global__ void __launch_bounds__(256) finalize_tiles_kernel(const float *__restrict__ acc,
+                                                             const float *__restrict__ acc_lse,
+                                                             __nv_bfloat16 *__restrict__ out, float *__restrict__ lse_out,
+                                                             int64_t n_rows)
+{
+    constexpr int EPL = D / 32;
+    const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (row >= n_rows) return;
+    const float *a = acc + row * D + lane * EPL;
+    __nv_bfloat16 *o = out + row * D + lane * EPL;
+#pragma unroll
+    for (int e = 0; e < EPL; e += 2) *reinterpret_cast<uint32_t *>(o + e) = pack_bf16x2(a[e], a[e + 1]);
+    if (lse_out && lane == 0) lse_out[row] = acc_lse[row];
+}
+
+int cuda_err(cudaError_t e)
+{
+    if (e == cudaSuccess) return PKV_OK;
+    record_cuda_error((int)e);
+    return PKV_ERR_CUDA;
+}
+
+// device pointer of pinned, mapped host memory (PKV_ERR_INVALID_ARG otherwise)
+int mapped(const void *host, const void **dev)
+{
+    void *d = nullptr;
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, host) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return PKV_ERR_INVALID_ARG;
+    }
+    if (at.type != cudaMemoryTypeHost) return PKV_ERR_INVALID_ARG;
+    if (cudaHostGetDevicePointer(&d, const_cast<void *>(host), 0) != cudaSuccess || !d) {
+        (void)cudaGetLastError();
+        return PKV_ERR_INVALID_ARG;
+    }
+    *dev = d;
+    return PKV_OK;
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+int pkv_sp_create(int32_t n_slots, int32_t max_seqs, pkv_scratch_pool **out)
+{
+    if (!out || n_slots <= 0 || max_seqs <= 0) return PKV_ERR_INVALID_ARG;
+    pkv_scratch_pool *sp = new (std::nothrow) pkv_scratch_pool();
+    if (!sp) return PKV_ERR_INVALID_ARG;
+    sp->n_slots = n_slots;
+    sp->max_seqs = max_seqs;
+    sp->block_of.assign(n_slots, -1);
+    sp->prev.assign(n_slots, -1);
+    sp->next.assign(n_slots, -1);
+    sp->pinned_tile.assign(n_slots, -1);
+    for (int32_t s = 0; s < n_slots; ++s) sp->push_back(s);   // slot 0 is reused first
+    sp->stage_ints = plan_ints(max_seqs, n_slots);
+    *out = sp;
+    return PKV_OK;
+}
+
+void pkv_sp_destroy(pkv_scratch_pool *sp)
+{
+    if (!sp) return;
+    for (int b = 0; b < 2; ++b) {
+        if (sp->copied[b]) {
+            (void)cudaEventSynchronize(sp->copied[b]);
+            (void)cudaEventDestroy(sp->copied[b]);
+        }
+        if (sp->stage[b]) (void)cudaFreeHost(sp->stage[b]);
+    }
+    delete sp;
+}
+
+int32_t pkv_sp_lookup(const pkv_scratch_pool *sp, int32_t host_block)
+{
+    if (!sp) return -1;
+    auto it = sp->slot_of.find(host_block);
+    return it == sp->slot_of.end() ? -1 : it->second;
+}
+
+int pkv_sp_invalidate(pkv_scratch_pool *sp, int32_t host_block)
+{
+    if (!sp) return PKV_ERR_INVALID_ARG;
+    auto it = sp->slot_of.find(host_block);
+    if (it == sp->slot_of.end()) return PKV_OK;
+    const int32_t s = it->second;
+    sp->slot_of.erase(it);
+    sp->block_of[s] = -1;
+    sp->unlink(s);
+    sp->push_front(s);   // an empty slot is reused first
+    return PKV_OK;
+}
+
+int pkv_sp_plan_tile(pkv_scratch_pool *sp, const int32_t *host_tables, int32_t max_blocks, const int32_t *ctx_lens,
+                     int32_t n_seqs, int32_t block_size, int32_t *cursor, int32_t *tile_tables, int32_t *tile_lens,
+                     int32_t *pairs, int32_t *n_pairs, int32_t *done)
+{
+    if (!sp || !cursor || !tile_tables || !tile_lens || !pairs || !n_pairs || !done || n_seqs < 0 ||
+        n_seqs > sp->max_seqs || block_size <= 0 || max_blocks <= 0 || (n_seqs > 0 && (!host_tables || !ctx_lens)))
+        return PKV_ERR_INVALID_ARG;
+    for (int32_t s = 0; s < n_seqs; ++s)
+        if (ctx_lens[s] < 0 || (int64_t)ctx_lens[s] > (int64_t)max_blocks * block_size) return PKV_ERR_OUT_OF_RANGE;
+    const int32_t n_slots = sp->n_slots;
+    for (int64_t i = 0; i < (int64_t)n_seqs * n_slots; ++i) tile_tables[i] = n_slots;   // the scratch slot
+    for (int32_t s = 0; s < n_seqs; ++s) tile_lens[s] = 0;
+    std::vector<int32_t> used(n_seqs, 0);
+    const int64_t tile = ++sp->tiles;
+    int32_t s = cursor[0], j = cursor[1], taken = 0, np = 0;
+    auto blocks_of = [&](int32_t q) { return (ctx_lens[q] + block_size - 1) / block_size; };
+    while (s < n_seqs && taken < n_slots) {
+        if (j >= blocks_of(s)) {
+            ++s;
+            j = 0;
+            continue;
+        }
+        const int32_t hb = host_tables[(int64_t)s * max_blocks + j];
+        int32_t slot;
+        auto it = sp->slot_of.find(hb);
+        if (it != sp->slot_of.end()) {
+            slot = it->second;
+        } else {
+            slot = sp->head;   // least recently used; every slot of this tile sits behind it
+            if (sp->pinned_tile[slot] == tile) return PKV_ERR_STATE;   // cannot happen: taken < n_slots
+            if (sp->block_of[slot] >= 0) sp->slot_of.erase(sp->block_of[slot]);
+            sp->block_of[slot] = hb;
+            sp->slot_of[hb] = slot;
+            pairs[2 * np] = hb;
+            pairs[2 * np + 1] = slot;
+            ++np;
+        }
+        sp->pinned_tile[slot] = tile;
+        sp->unlink(slot);
+        sp->push_back(slot);
+        tile_tables[(int64_t)s * n_slots + used[s]++] = slot;
+        tile_lens[s] += (int32_t)((int64_t)ctx_lens[s] - (int64_t)j * block_size < block_size
+                                      ? ctx_lens[s] - j * block_size : block_size);
+        ++j;
+        ++taken;
+    }
+    while (s < n_seqs && j >= blocks_of(s)) {
+        ++s;
+        j = 0;
+    }
+    cursor[0] = s;
+    cursor[1] = j;
+    *n_pairs = np;
+    *done = s >= n_seqs ? 1 : 0;
+    return PKV_OK;
+}
+
+int paged_kv_stage_blocks(const int32_t *pairs, int32_t n_pairs, const pkv_bf16 *host_k, const pkv_bf16 *host_v,
+                          int32_t n_host_blocks, pkv_bf16 *pool_k, pkv_bf16 *pool_v, pkv_dims pool_dims,
+                          int32_t *dev_status, pkv_stream_t stream)
+{
+    if (n_pairs < 0 || n_host_blocks < 0 || pool_dims.n_blocks < 0 || pool_dims.block_size <= 0 ||
+        pool_dims.n_kv_heads <= 0 || (pool_dims.head_dim != 64 && pool_dims.head_dim != 128))
+        return PKV_ERR_INVALID_ARG;
+    if (n_pairs == 0) return PKV_OK;
+    if (!pairs || !host_k || !host_v || !pool_k || !pool_v || (reinterpret_cast<uintptr_t>(pairs) & 7) != 0 ||
+        (reinterpret_cast<uintptr_t>(pool_k) & 15) != 0 || (reinterpret_cast<uintptr_t>(pool_v) & 15) != 0 ||
+        (reinterpret_cast<uintptr_t>(host_k) & 15) != 0 || (reinterpret_cast<uintptr_t>(host_v) & 15) != 0)
+        return PKV_ERR_INVALID_ARG;
+    const void *dk = nullptr, *dv = nullptr;
+    int st = mapped(host_k, &dk);
+    if (st == PKV_OK) st = mapped(host_v, &dv);
+    if (st != PKV_OK) return st;
+    const int64_t block_vecs = (int64_t)pool_dims.block_size * pool_dims.n_kv_heads * pool_dims.head_dim * 2 / 16;
+    const int64_t n_vecs = (int64_t)n_pairs * 2 * block_vecs;
+    int64_t grid = (n_vecs + 255) / 256;
+    if (grid > 4096) grid = 4096;
+    stage_blocks_kernel<<<(unsigned)grid, 256, 0, (cudaStream_t)stream>>>(
+        (const uint4 *)dk, (const uint4 *)dv, (uint4 *)pool_k, (uint4 *)pool_v, (const int2 *)pairs, n_host_blocks,
+        pool_dims.n_blocks, block_vecs, n_vecs, dev_status);
+    return cuda_err(cudaGetLastError());
+}
+
+size_t pkv_streamed_workspace_bytes(int32_t n_seqs, int32_t n_q_heads, int32_t head_dim, int32_t n_slots,
+                                    int32_t block_size)
+{
+    if (n_seqs <= 0 || n_q_heads <= 0 || (head_dim != 64 && head_dim != 128) || n_slots <= 0 || block_size <= 0)
+        return 0;
+    return stream_ws_bytes(n_seqs, n_q_heads, head_dim, n_slots, block_size, nullptr);
+}
+
+int paged_decode_streamed(const pkv_bf16 *q, int32_t n_q_heads, const pkv_bf16 *host_k, const pkv_bf16 *host_v,
+                          int32_t n_host_blocks, pkv_bf16 *pool_k, pkv_bf16 *pool_v, pkv_dims pool_dims,
+                          pkv_scratch_pool *sp, const int32_t *host_tables, int32_t max_blocks,
+                          const int32_t *ctx_lens, int32_t n_seqs, float softmax_scale, pkv_bf16 *out,
+                          float *lse_out, void *workspace, size_t workspace_bytes, int32_t *dev_status,
+                          pkv_stream_t stream)
+{
+    if (!sp || n_seqs < 0 || n_q_heads <= 0 || n_host_blocks < 0 || max_blocks <= 0) return PKV_ERR_INVALID_ARG;
+    if (n_seqs == 0) return PKV_OK;
+    if (pool_dims.n_blocks != sp->n_slots || n_seqs > sp->max_seqs) return PKV_ERR_INVALID_ARG;
+    if (!q || !out || !host_tables || !ctx_lens || !workspace) return PKV_ERR_INVALID_ARG;
+    const int32_t D = pool_dims.head_dim, bs = pool_dims.block_size, n_slots = sp->n_slots;
+    if (D != 64 && D != 128) return PKV_ERR_UNSUPPORTED;
+    for (int64_t i = 0; i < (int64_t)n_seqs; ++i) {
+        if (ctx_lens[i] < 0 || (int64_t)ctx_lens[i] > (int64_t)max_blocks * bs) return PKV_ERR_OUT_OF_RANGE;
+        for (int32_t j = 0; j < (ctx_lens[i] + bs - 1) / bs; ++j) {
+            const int32_t hb = host_tables[i * max_blocks + j];
+            if (hb < 0 || hb >= n_host_blocks) return PKV_ERR_OUT_OF_RANGE;
+        }
+    }
+    size_t decode_bytes = 0;
+    const size_t need = stream_ws_bytes(n_seqs, n_q_heads, D, n_slots, bs, &decode_bytes);
+    if (need == 0) return PKV_ERR_INVALID_ARG;
+    if (workspace_bytes < need) return PKV_ERR_WORKSPACE;
+    // check the host tier's device mapping once (staging would fail per tile)
+    const void *dk = nullptr, *dv = nullptr;
+    int st = mapped(host_k, &dk);
+    if (st == PKV_OK) st = mapped(host_v, &dv);
+    if (st != PKV_OK) return st;
+    // lazily: pinned staging buffers and their events
+    for (int b = 0; b < 2; ++b) {
+        if (!sp->stage[b]) {
+            void *p = nullptr;
+            if (cudaHostAlloc(&p, sp->stage_ints * 4, cudaHostAllocDefault) != cudaSuccess) return PKV_ERR_CUDA;
+            sp->stage[b] = static_cast<int32_t *>(p);
+        }
+        if (!sp->copied[b] && cudaEventCreateWithFlags(&sp->copied[b], cudaEventDisableTiming) != cudaSuccess)
+            return PKV_ERR_CUDA;
+    }
+    uint8_t *w = static_cast<uint8_t *>(workspace);
+    StreamWs ws;
+    ws.decode_ws = w;
+    ws.decode_bytes = decode_bytes;
+    w += align256(decode_bytes);
+    ws.plan = reinterpret_cast<int32_t *>(w);
+    const size_t pints = plan_ints(n_seqs, n_slots);
+    w += align256(pints * 4);
+    const size_t rows = (size_t)n_seqs * n_q_heads;
+    ws.tile_out = reinterpret_cast<__nv_bfloat16 *>(w);
+    w += align256(rows * D * 2);
+    ws.tile_lse = reinterpret_cast<float *>(w);
+    w += align256(rows * 4);
+    ws.acc = reinterpret_cast<float *>(w);
+    w += align256(rows * D * 4);
+    ws.acc_lse = reinterpret_cast<float *>(w);
+
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t lens_off = (size_t)n_seqs * n_slots;
+    const size_t pairs_off = (lens_off + n_seqs + kPairsAlign - 1) / kPairsAlign * kPairsAlign;
+    int32_t cursor[2] = {0, 0}, done = 0;
+    int first = 1;
+    for (int64_t t = 0; !done; ++t) {
+        const int b = (int)(t & 1);
+        if (cudaEventSynchronize(sp->copied[b]) != cudaSuccess) return cuda_err(cudaGetLastError());   // tile t - 2's copy read it
+        int32_t *plan = sp->stage[b];
+        int32_t np = 0;
+        st = pkv_sp_plan_tile(sp, host_tables, max_blocks, ctx_lens, n_seqs, bs, cursor, plan, plan + lens_off,
+                              plan + pairs_off, &np, &done);
+        if (st != PKV_OK) return st;
+        if (cudaMemcpyAsync(ws.plan, plan, pints * 4, cudaMemcpyHostToDevice, s) != cudaSuccess) return PKV_ERR_CUDA;
+        if (cudaEventRecord(sp->copied[b], s) != cudaSuccess) return PKV_ERR_CUDA;
+        st = paged_kv_stage_blocks(ws.plan + pairs_off, np, host_k, host_v, n_host_blocks, pool_k, pool_v, pool_dims,
+                                   dev_status, stream);
+        if (st != PKV_OK) return st;
+        st = paged_decode_attention(q, n_q_heads, pool_k, pool_v, nullptr, nullptr, PKV_KV_BF16, pool_dims, ws.plan,
+                                    n_slots, ws.plan + lens_off, n_seqs, softmax_scale, 0,
+                                    reinterpret_cast<pkv_bf16 *>(ws.tile_out), ws.tile_lse,
+                                    ws.decode_ws, ws.decode_bytes, dev_status, stream);
+        if (st != PKV_OK) return st;
+        const unsigned grid = (unsigned)((rows + 7) / 8);
+        if (D == 128)
+            merge_tile_kernel<128><<<grid, 256, 0, s>>>(ws.tile_out, ws.tile_lse, ws.acc, ws.acc_lse, (int64_t)rows, first);
+        else
+            merge_tile_kernel<64><<<grid, 256, 0, s>>>(ws.tile_out, ws.tile_lse, ws.acc, ws.acc_lse, (int64_t)rows, first);
+        if (cudaGetLastError() != cudaSuccess) return PKV_ERR_CUDA;
+        first = 0;
+    }
+    const unsigned grid = (unsigned)((rows + 7) / 8);
+    if (D == 128)
+        finalize_tiles_kernel<128><<<grid, 256, 0, s>>>(ws.acc, ws.acc_lse, (__nv_bfloat16 *)out, lse_out, (int64_t)rows);
+    else
+        finalize_tiles_kernel<64><<<grid, 256, 0, s>>>(ws.acc, ws.acc_lse, (__nv_bfloat16 *)out, lse_out, (int64_t)rows);
+    return cuda_err(cudaGetLastError());
+}
+
+}  // extern "C"

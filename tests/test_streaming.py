@@ -1,0 +1,60 @@
+"""The library's tile planner for decode streamed from a host tier
+(pkv_sp_plan_tile) against the oracle (oracle/streaming.py): same tiles, same
+staged pairs, same residency, over random batches, repeated calls and
+invalidations.  CPU only (no CUDA call)."""
+import random
+
+import pytest
+import torch
+
+from oracle.streaming import ScratchPoolOracle
+
+
+@pytest.fixture(scope="module")
+def P():
+    from paged_kv_cache_212_gb300 import build as B
+    try:
+        B.nvcc()
+    except RuntimeError:
+        pytest.skip("nvcc not available")
+    B.build()
+    import paged_kv_cache_212_gb300 as P
+    P.load_library()
+    return P
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_planner_matches_the_oracle(P, seed):
+    rng = random.Random(seed)
+    bs = rng.choice([16, 32])
+    n_slots = rng.randrange(1, 24)
+    max_seqs = 8
+    lib = P.ScratchPool(n_slots, max_seqs)
+    ref = ScratchPoolOracle(n_slots)
+    n_host = rng.randrange(4, 60)
+    for call in range(12):
+        n = rng.randrange(1, max_seqs + 1)
+        lens = [rng.randrange(0, 12 * bs) for _ in range(n)]
+        max_blocks = max(1, max(-(-L // bs) for L in lens))
+        tables = [[rng.randrange(0, n_host) for _ in range(max_blocks)] for _ in range(n)]
+        t_tab, t_len = torch.tensor(tables, dtype=torch.int32), torch.tensor(lens, dtype=torch.int32)
+        cl, cr = [0, 0], [0, 0]
+        while True:
+            tt, tl, pairs, done = lib.plan_tile(t_tab, t_len, bs, cl)
+            rtt, rtl, rpairs, rdone = ref.plan_tile(tables, lens, bs, cr)
+            assert tt.tolist() == rtt and tl.tolist() == rtl and pairs == rpairs and done == rdone
+            assert cl == cr
+            if done:
+                break
+        for b in range(n_host):
+            assert lib.lookup(b) == ref.lookup(b)
+        for _ in range(rng.randrange(0, 3)):
+            b = rng.randrange(0, n_host)
+            lib.invalidate(b)
+            ref.invalidate(b)
+
+
+def test_planner_rejects_lengths_past_the_table(P):
+    lib = P.ScratchPool(4, 2)
+    with pytest.raises(P.PagedKVError):
+        lib.plan_tile(torch.zeros((1, 2), dtype=torch.int32), torch.tensor([33], dtype=torch.int32), 16, [0, 0])
