@@ -49,7 +49,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", type=int, default=1, choices=[1, 2, 3, 4])
+    ap.add_argument("--config", type=int, default=1, choices=[0, 1, 2, 3, 4])
     ap.add_argument("--split", type=int, default=0, help="decode split_tokens (0 = library default)")
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -57,6 +57,9 @@ def parse_args():
                     help="time the host-side block manager's per-step calls instead (no GPU)")
     ap.add_argument("--stream", type=int, default=0, metavar="N_SLOTS",
                     help="decode config 1 from a pinned host tier through an N_SLOTS-block scratch pool")
+    ap.add_argument("--layers", type=int, default=0, metavar="L",
+                    help="time an L-layer decode step (write + decode per layer, each layer its own pools), "
+                         "eager launches against one CUDA graph of the whole step")
     return ap.parse_args()
 
 
@@ -107,7 +110,9 @@ def ncu_traffic(kind, cfg):
 
 def make_workload(cfg, device):
     from paged_kv_cache_212_gb300 import workloads as W
-    if cfg == 1:
+    if cfg == 0:
+        w = W.config0(device=device)
+    elif cfg == 1:
         w = W.config1(device=device)
     elif cfg == 3:
         w = W.config3(device=device)
@@ -521,6 +526,18 @@ def run_stream_bench(args, P, device):
         call()
     torch.cuda.synchronize()
     assert int(status.item()) == 0
+    # the link's copy rate on this machine, measured here: the copy engine moving the
+    # whole K tier (pinned host -> device, one contiguous copy), after one warm-up
+    link_dst = torch.empty_like(host_k, device=device)
+    l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    link_dst.copy_(host_k, non_blocking=True)
+    l0.record(stream)
+    for _ in range(3):
+        link_dst.copy_(host_k, non_blocking=True)
+    l1.record(stream)
+    torch.cuda.synchronize()
+    link_gbs = 3 * host_k.numel() * 2 / (l0.elapsed_time(l1) * 1e-3) / 1e9
+    del link_dst
     # blocks staged per call (the plan is host bookkeeping: replay it on a copy)
     blocks = sum(-(-int(L) // w.block_size) for L in w.ctx_lens)
     steps = max(3, min(args.steps, 50))
@@ -544,6 +561,90 @@ def run_stream_bench(args, P, device):
             "config": {"workload": w.name, "n_slots": n_slots, "blocks_per_call": blocks,
                        "tiles_per_call": -(-blocks // n_slots), "host_tier_bytes": 2 * host_k.numel() * 2},
             "staging": {"bytes_per_call": staged, "gbs": round(staged / (ms * 1e-3) / 1e9, 2)},
+            "roofline": ({"bound": "host-link", "achieved": round(staged / (ms * 1e-3) / 1e9, 2),
+                          "peak": round(link_gbs, 2), "unit": "GB/s",
+                          "frac": round(staged / (ms * 1e-3) / 1e9 / link_gbs, 4), "traffic": None,
+                          "peak_source": "pinned host -> device copy-engine rate measured in this run"}
+                         if staged else None),
+            "clocks": clk.summary()}
+    print(json.dumps(line), flush=True)
+
+
+def run_layers_bench(args, P, device):
+    """An args.layers-layer decode step of config 0 or 1 (int8 pools for config
+    2): per layer the page write of the step's new rows and the paged decode
+    over that layer's own pools (the tables are shared, as every layer of a
+    model stores the same token positions), timed as eager calls and as one
+    captured CUDA graph of the whole step."""
+    import torch
+    assert args.config in (0, 1, 2), "the layered step covers configs 0, 1 and 2"
+    w = make_workload(args.config, device)
+    L = args.layers
+    kp, vp, ks, vs = fill_pool(P, w, device)
+    layers = []
+    gen = torch.Generator().manual_seed(4242)
+    for l in range(L):
+        layers.append(dict(kp=kp if l == 0 else kp.clone(), vp=vp if l == 0 else vp.clone(),
+                           ks=None if ks is None else (ks if l == 0 else ks.clone()),
+                           vs=None if vs is None else (vs if l == 0 else vs.clone()),
+                           q=torch.randn(w.q.shape, generator=gen).to(torch.bfloat16).to(device),
+                           k_new=torch.randn(w.k_new.shape, generator=gen).to(torch.bfloat16).to(device),
+                           v_new=torch.randn(w.v_new.shape, generator=gen).to(torch.bfloat16).to(device),
+                           out=torch.empty(w.q.shape, dtype=torch.bfloat16, device=device)))
+    tables, start, ctx = w.tables.to(device), w.start_pos.to(device), w.ctx_lens.to(device)
+    ws = torch.empty(P.decode_workspace_bytes(w.n_seqs, w.n_q_heads, w.head_dim, int(w.ctx_lens.sum()),
+                                              w.split_tokens), dtype=torch.uint8, device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+
+    def step():
+        for x in layers:
+            P.paged_decode_step(x["k_new"], x["v_new"], start, x["q"], x["kp"], x["vp"], tables, ctx,
+                                w.softmax_scale, k_scales=x["ks"], v_scales=x["vs"], split_tokens=w.split_tokens,
+                                out=x["out"], workspace=ws, dev_status=status)
+
+    side = torch.cuda.Stream(device)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    steps = max(3, min(args.steps, 2000))
+    warm = max(3, args.warmup)
+
+    def timed(fn):
+        for _ in range(warm):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    with ClockSampler(uuid) as clk:
+        time.sleep(0.25)
+        ms_eager = timed(step)
+        ms_graph = timed(graph.replay)
+    assert int(status.item()) == 0
+    decode_b, write_b = algorithmic_bytes(w)
+    line = {"metric": f"{L}-layer decode step seq-steps/s", "value": round(w.n_seqs / (ms_graph * 1e-3), 1),
+            "unit": "seq-steps/s", "n_gpus": 1, "steps": steps, "warmup": warm, "ms_per_step": round(ms_graph, 4),
+            "higher_is_better": True, "scaling": "none", "vs_baseline": None,
+            "dtype": "int8" if w.kv_format == "int8" else "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "layers": L, "launch": "one CUDA graph per step",
+                       "gb_per_s": round(L * (decode_b + write_b) / (ms_graph * 1e-3) / 1e9, 2),
+                       "kernel_launches_per_step": L * 3},
+            "eager": {"ms_per_step": round(ms_eager, 4), "value": round(w.n_seqs / (ms_eager * 1e-3), 1),
+                      "gb_per_s": round(L * (decode_b + write_b) / (ms_eager * 1e-3) / 1e9, 2)},
             "clocks": clk.summary()}
     print(json.dumps(line), flush=True)
 
@@ -575,6 +676,10 @@ def main():
     if args.stream:
         if rank == 0:
             run_stream_bench(args, P, device)
+        return
+    if args.layers:
+        if rank == 0:
+            run_layers_bench(args, P, device)
         return
     w = make_workload(args.config, device)  # every rank owns an independent replica batch
     if args.config == 3:

@@ -35,8 +35,9 @@
  *
  * Supported geometry: head_dim in {64, 128}; block_size a multiple of 16, at
  * most 256; n_q_heads % n_kv_heads == 0 and G = n_q_heads / n_kv_heads in
- * {1, 2, 4, 8} for decode (1 .. 16 dividing 64 for prefill); query head h reads kv
- * head h / G.
+ * {1, 2, 4, 8} for decode (1 .. 16 dividing 64 for prefill); decode over int8
+ * pages also needs n_kv_heads % 4 == 0 (else PKV_ERR_UNSUPPORTED); query head h
+ * reads kv head h / G.
  */
 #ifndef PAGEDKV_H
 #define PAGEDKV_H

@@ -32,7 +32,9 @@ typedef struct pkv_scratch_pool pkv_scratch_pool;
  * blocks (slot ids 0 .. n_slots - 1; the device pool tensors have n_slots + 1
  * blocks, the last a scratch block) and per-tile plans for batches of up to
  * max_seqs sequences.  Holds two small pinned host staging buffers (the plan of
- * a tile is copied to the device from them).  Host only; not thread-safe.
+ * a tile is copied to the device from them) and, from the first
+ * paged_decode_streamed call on, a copy stream and events of the device that
+ * was current then (the pool serves that device only).  Not thread-safe.
  */
 int pkv_sp_create(int32_t n_slots, int32_t max_seqs, pkv_scratch_pool **out);
 void pkv_sp_destroy(pkv_scratch_pool *sp);
@@ -44,17 +46,19 @@ int pkv_sp_invalidate(pkv_scratch_pool *sp, int32_t host_block);
 /*
  * pkv_sp_plan_tile -- the plan of the next tile (host only; paged_decode_streamed
  * calls it per tile): starting at cursor[0] = sequence, cursor[1] = block of
- * that sequence, take the batch's blocks in order until n_slots blocks or the
- * end.  Each block reuses its resident slot, or takes the least recently used
- * slot not yet used by this tile (its old block is forgotten) and adds
- * (host block, slot) to pairs [n_slots][2] (*n_pairs of them).  tile_tables
+ * that sequence, take the batch's blocks in order until tile_blocks blocks
+ * (<= 0 or > n_slots: n_slots) or the end.  Each block reuses its resident
+ * slot, or takes the least recently used slot not yet used by this tile (its
+ * old block is forgotten) and adds (host block, slot) to pairs [n_slots][2]
+ * (*n_pairs of them).  With tile_blocks <= n_slots / 2 a tile never stages
+ * into a slot the tile before it uses (those are the most recently used).  tile_tables
  * [n_seqs][n_slots] receives each sequence's slots in token order (unused
  * entries = n_slots, the scratch slot), tile_lens [n_seqs] its tokens in this
  * tile.  Advances cursor; *done = 1 when no block is left.
  */
 int pkv_sp_plan_tile(pkv_scratch_pool *sp, const int32_t *host_tables, int32_t max_blocks, const int32_t *ctx_lens,
-                     int32_t n_seqs, int32_t block_size, int32_t *cursor, int32_t *tile_tables, int32_t *tile_lens,
-                     int32_t *pairs, int32_t *n_pairs, int32_t *done);
+                     int32_t n_seqs, int32_t block_size, int32_t tile_blocks, int32_t *cursor, int32_t *tile_tables,
+                     int32_t *tile_lens, int32_t *pairs, int32_t *n_pairs, int32_t *done);
 
 /*
  * paged_kv_stage_blocks -- copy host-tier blocks into scratch-pool slots on the
@@ -76,19 +80,25 @@ size_t pkv_streamed_workspace_bytes(int32_t n_seqs, int32_t n_q_heads, int32_t h
  * paged_decode_streamed -- o = softmax(softmax_scale * q K^T) V over the
  * ctx_lens[s] tokens of each sequence, whose blocks are host_tables[s][j]
  * (HOST int32 [n_seqs][max_blocks], ids into the host tier).  The tokens of
- * the batch are taken in order (sequence by sequence) in tiles of at most
- * n_slots = pool_dims.n_blocks blocks; for each tile the resident blocks are
- * reused, the missing ones staged (paged_kv_stage_blocks), the tile attended
- * by the split-KV decode of pagedkv.h over the scratch pool, and its result
- * merged into a float32 running (output, log-sum-exp) state; the last step
+ * the batch are taken in order (sequence by sequence) in tiles of
+ * n_slots = pool_dims.n_blocks blocks when the batch fits the scratch pool,
+ * else of n_slots / 2 blocks; for each tile the resident blocks are reused,
+ * the missing ones staged (paged_kv_stage_blocks, on the pool's copy stream,
+ * overlapping the attention of the tile before), the tile attended by the
+ * split-KV decode of pagedkv.h over the scratch pool, and its result merged
+ * into a float32 running (output, log-sum-exp) state; the last step
  * writes out (bf16 [n_seqs][n_q_heads][head_dim]) and lse_out (fp32
  * [n_seqs][n_q_heads], natural log; nullable).  ctx_lens is HOST int32
  * [n_seqs]; q, out, lse_out device.  workspace: device memory of
  * pkv_streamed_workspace_bytes(...) bytes; the residency state in sp carries
- * over between calls (a later call reuses what is still resident).  Work is
- * enqueued on stream; the call returns once every tile is enqueued (it waits
- * only for the staging buffer of the tile two before).  The scratch pool and
- * workspace must not be used by other work meanwhile.
+ * over between calls (a later call reuses what is still resident).  The
+ * attention and merges are enqueued on stream, the plan copies and staging on
+ * the pool's copy stream, ordered against stream by events (the staging waits
+ * for the work enqueued on stream before the call; the result is complete
+ * when stream reaches the end of the call).  The call returns once every tile
+ * is enqueued (it waits on the host only until the plan of the tile two
+ * before has been copied).  The scratch pool and workspace must not be used by
+ * other work meanwhile.
  */
 int paged_decode_streamed(const pkv_bf16 *q, int32_t n_q_heads, const pkv_bf16 *host_k, const pkv_bf16 *host_v,
                           int32_t n_host_blocks, pkv_bf16 *pool_k, pkv_bf16 *pool_v, pkv_dims pool_dims,

@@ -15,7 +15,9 @@ used by the current tile is never taken); empty slots are used first, in id
 order; a tile takes the blocks of the whole batch in order, sequence after
 sequence, so one tile may hold the end of one sequence and the start of the
 next; a sequence's tokens in a tile are its tokens of the blocks taken (the
-last block of a sequence may be partial).
+last block of a sequence may be partial).  A tile may be capped below the
+pool size (the library caps it at half the pool when the batch does not fit,
+so that staging the next tile never overwrites a slot the current one reads).
 
 The attention itself is checked against oracle.decode over the whole context:
 tiling, like split-KV, does not change the result beyond rounding.
@@ -45,10 +47,12 @@ class ScratchPoolOracle:
         self.order.remove(slot)
         self.order.insert(0, slot)            # reused first
 
-    def plan_tile(self, host_tables, ctx_lens, block_size: int, cursor):
-        """Next tile from cursor = [sequence, block]; returns (tile_tables as
-        lists padded with n_slots, tile_lens, pairs [(host block, slot)], done)
-        and advances cursor."""
+    def plan_tile(self, host_tables, ctx_lens, block_size: int, cursor, tile_blocks: int = 0):
+        """Next tile of at most tile_blocks blocks (0 or more than n_slots: all
+        slots) from cursor = [sequence, block]; returns (tile_tables as lists
+        padded with n_slots, tile_lens, pairs [(host block, slot)], done) and
+        advances cursor."""
+        cap = self.n_slots if tile_blocks <= 0 or tile_blocks > self.n_slots else tile_blocks
         n = len(ctx_lens)
         nb = [-(-int(L) // block_size) for L in ctx_lens]
         tables = [[] for _ in range(n)]
@@ -57,7 +61,7 @@ class ScratchPoolOracle:
         used = set()
         s, j = cursor
         taken = 0
-        while s < n and taken < self.n_slots:
+        while s < n and taken < cap:
             if j >= nb[s]:
                 s, j = s + 1, 0
                 continue

@@ -110,7 +110,7 @@ def load_library(path: str = LIB_PATH):
     lib.pkv_sp_destroy.restype = None
     lib.pkv_sp_lookup.argtypes = [P, i32]
     lib.pkv_sp_invalidate.argtypes = [P, i32]
-    lib.pkv_sp_plan_tile.argtypes = [P, P, i32, P, i32, i32, P, P, P, P, P, P]
+    lib.pkv_sp_plan_tile.argtypes = [P, P, i32, P, i32, i32, i32, P, P, P, P, P, P]
     lib.paged_kv_stage_blocks.argtypes = [P, i32, P, P, i32, P, P, Dims, P, P]
     lib.pkv_streamed_workspace_bytes.argtypes = [i32, i32, i32, i32, i32]
     lib.pkv_streamed_workspace_bytes.restype = sz
@@ -502,9 +502,10 @@ class ScratchPool:
     def invalidate(self, host_block):
         _check("pkv_sp_invalidate", self._lib.pkv_sp_invalidate(self._h, int(host_block)))
 
-    def plan_tile(self, host_tables, ctx_lens, block_size, cursor):
-        """Plan the next tile (host int32 tensors); returns (tile_tables, tile_lens,
-        pairs list, done) and advances cursor (a 2-element list)."""
+    def plan_tile(self, host_tables, ctx_lens, block_size, cursor, tile_blocks=0):
+        """Plan the next tile of at most tile_blocks blocks (0: n_slots) from host
+        int32 tensors; returns (tile_tables, tile_lens, pairs list, done) and
+        advances cursor (a 2-element list)."""
         host_tables = host_tables.to(torch.int32).contiguous()
         ctx_lens = ctx_lens.to(torch.int32).contiguous()
         n_seqs = ctx_lens.shape[0]
@@ -515,7 +516,8 @@ class ScratchPool:
         n, done = ctypes.c_int32(), ctypes.c_int32()
         _check("pkv_sp_plan_tile", self._lib.pkv_sp_plan_tile(
             self._h, ctypes.c_void_p(host_tables.data_ptr()), host_tables.shape[1],
-            ctypes.c_void_p(ctx_lens.data_ptr()), n_seqs, int(block_size), cur, ctypes.c_void_p(tt.data_ptr()),
+            ctypes.c_void_p(ctx_lens.data_ptr()), n_seqs, int(block_size), int(tile_blocks), cur,
+            ctypes.c_void_p(tt.data_ptr()),
             ctypes.c_void_p(tl.data_ptr()), ctypes.c_void_p(pr.data_ptr()), ctypes.byref(n), ctypes.byref(done)))
         cursor[0], cursor[1] = cur[0], cur[1]
         return tt, tl, [tuple(x) for x in pr[:n.value].tolist()], bool(done.value)

@@ -28,6 +28,11 @@ struct pkv_scratch_pool {
     int32_t *stage[2] = {nullptr, nullptr};
     cudaEvent_t copied[2] = {nullptr, nullptr};
     size_t stage_ints = 0;
+    // the copy stream the staging runs on (created at the first streamed call,
+    // on the device current then), and the events that order it against the
+    // caller's stream: entry (work before the call), staged / decoded per tile parity
+    cudaStream_t copy_stream = nullptr;
+    cudaEvent_t entry = nullptr, staged[2] = {nullptr, nullptr}, decoded[2] = {nullptr, nullptr};
 
     void unlink(int32_t s)
     {
@@ -72,7 +77,7 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 struct StreamWs {
     void *decode_ws;
     size_t decode_bytes;
-    int32_t *plan;              // device copy of the tile plan
+    int32_t *plan[2];           // device copies of the tile plans (by tile parity)
     __nv_bfloat16 *tile_out;
     float *tile_lse, *acc, *acc_lse;
 };
@@ -85,29 +90,43 @@ size_t stream_ws_bytes(int32_t n_seqs, int32_t n_q_heads, int32_t head_dim, int3
     if (d == 0) return 0;
     if (decode_bytes) *decode_bytes = d;
     const size_t rows = (size_t)n_seqs * n_q_heads;
-    return align256(d) + align256(plan_ints(n_seqs, n_slots) * 4) + align256(rows * head_dim * 2) +
+    return align256(d) + 2 * align256(plan_ints(n_seqs, n_slots) * 4) + align256(rows * head_dim * 2) +
            align256(rows * 4) + align256(rows * head_dim * 4) + align256(rows * 4);
 }
 
-// Host tier -> scratch pool: per (host block, slot) pair the 16-byte vectors of
-// the K block and the V block; the host tier is read through its device mapping.
+// Host tier -> scratch pool.  A warp copies one segment of kSegVecs 16-byte
+// vectors of the K or the V half of one (host block, slot) pair, all its loads
+// issued before its stores; the host tier is read through its device mapping.
+// The CPU-GPU link bounds the kernel, so a small grid (two CTAs per SM) keeps
+// enough bytes in flight and leaves the SMs to the attention it overlaps.
+constexpr int kSegUnroll = 4, kSegVecs = 32 * kSegUnroll;
+
 __global__ void __launch_bounds__(256) stage_blocks_kernel(const uint4 *__restrict__ host_k,
                                                            const uint4 *__restrict__ host_v, uint4 *__restrict__ pool_k,
                                                            uint4 *__restrict__ pool_v, const int2 *__restrict__ pairs,
                                                            int32_t n_host, int32_t n_pool, int64_t block_vecs,
-                                                           int64_t n_vecs, int32_t *dev_status)
+                                                           int64_t segs_per_half, int64_t n_segs, int32_t *dev_status)
 {
-    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_vecs; i += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t pr = i / (2 * block_vecs), r = i % (2 * block_vecs);
+    const int lane = threadIdx.x & 31;
+    const int64_t n_warps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    for (int64_t seg = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5; seg < n_segs; seg += n_warps) {
+        const int64_t half = seg / segs_per_half, pr = half >> 1;
+        const int64_t off = (seg - half * segs_per_half) * kSegVecs;
         const int2 hs = __ldg(pairs + pr);
         if (hs.x < 0 || hs.x >= n_host || hs.y < 0 || hs.y > n_pool) {
-            if (r == 0) report(dev_status, PKV_DEV_BAD_BLOCK_ID);
+            if (lane == 0 && off == 0 && (half & 1) == 0) report(dev_status, PKV_DEV_BAD_BLOCK_ID);
             continue;
         }
-        const bool v = r >= block_vecs;
-        const int64_t off = v ? r - block_vecs : r;
-        const uint4 x = (v ? host_v : host_k)[(int64_t)hs.x * block_vecs + off];
-        (v ? pool_v : pool_k)[(int64_t)hs.y * block_vecs + off] = x;
+        const uint4 *src = ((half & 1) ? host_v : host_k) + (int64_t)hs.x * block_vecs + off;
+        uint4 *dst = ((half & 1) ? pool_v : pool_k) + (int64_t)hs.y * block_vecs + off;
+        const int64_t left = block_vecs - off;
+        uint4 x[kSegUnroll];
+#pragma unroll
+        for (int u = 0; u < kSegUnroll; ++u)
+            if (u * 32 + lane < left) x[u] = src[u * 32 + lane];
+#pragma unroll
+        for (int u = 0; u < kSegUnroll; ++u)
+            if (u * 32 + lane < left) dst[u * 32 + lane] = x[u];
     }
 }
 
@@ -215,13 +234,21 @@ int pkv_sp_create(int32_t n_slots, int32_t max_seqs, pkv_scratch_pool **out)
 void pkv_sp_destroy(pkv_scratch_pool *sp)
 {
     if (!sp) return;
+    if (sp->copy_stream) (void)cudaStreamSynchronize(sp->copy_stream);
     for (int b = 0; b < 2; ++b) {
         if (sp->copied[b]) {
             (void)cudaEventSynchronize(sp->copied[b]);
             (void)cudaEventDestroy(sp->copied[b]);
         }
+        if (sp->staged[b]) (void)cudaEventDestroy(sp->staged[b]);
+        if (sp->decoded[b]) {
+            (void)cudaEventSynchronize(sp->decoded[b]);
+            (void)cudaEventDestroy(sp->decoded[b]);
+        }
         if (sp->stage[b]) (void)cudaFreeHost(sp->stage[b]);
     }
+    if (sp->entry) (void)cudaEventDestroy(sp->entry);
+    if (sp->copy_stream) (void)cudaStreamDestroy(sp->copy_stream);
     delete sp;
 }
 
@@ -246,8 +273,8 @@ int pkv_sp_invalidate(pkv_scratch_pool *sp, int32_t host_block)
 }
 
 int pkv_sp_plan_tile(pkv_scratch_pool *sp, const int32_t *host_tables, int32_t max_blocks, const int32_t *ctx_lens,
-                     int32_t n_seqs, int32_t block_size, int32_t *cursor, int32_t *tile_tables, int32_t *tile_lens,
-                     int32_t *pairs, int32_t *n_pairs, int32_t *done)
+                     int32_t n_seqs, int32_t block_size, int32_t tile_blocks, int32_t *cursor, int32_t *tile_tables,
+                     int32_t *tile_lens, int32_t *pairs, int32_t *n_pairs, int32_t *done)
 {
     if (!sp || !cursor || !tile_tables || !tile_lens || !pairs || !n_pairs || !done || n_seqs < 0 ||
         n_seqs > sp->max_seqs || block_size <= 0 || max_blocks <= 0 || (n_seqs > 0 && (!host_tables || !ctx_lens)))
@@ -255,13 +282,14 @@ int pkv_sp_plan_tile(pkv_scratch_pool *sp, const int32_t *host_tables, int32_t m
     for (int32_t s = 0; s < n_seqs; ++s)
         if (ctx_lens[s] < 0 || (int64_t)ctx_lens[s] > (int64_t)max_blocks * block_size) return PKV_ERR_OUT_OF_RANGE;
     const int32_t n_slots = sp->n_slots;
+    const int32_t cap = tile_blocks <= 0 || tile_blocks > n_slots ? n_slots : tile_blocks;
     for (int64_t i = 0; i < (int64_t)n_seqs * n_slots; ++i) tile_tables[i] = n_slots;   // the scratch slot
     for (int32_t s = 0; s < n_seqs; ++s) tile_lens[s] = 0;
     std::vector<int32_t> used(n_seqs, 0);
     const int64_t tile = ++sp->tiles;
     int32_t s = cursor[0], j = cursor[1], taken = 0, np = 0;
     auto blocks_of = [&](int32_t q) { return (ctx_lens[q] + block_size - 1) / block_size; };
-    while (s < n_seqs && taken < n_slots) {
+    while (s < n_seqs && taken < cap) {
         if (j >= blocks_of(s)) {
             ++s;
             j = 0;
@@ -319,12 +347,16 @@ int paged_kv_stage_blocks(const int32_t *pairs, int32_t n_pairs, const pkv_bf16 
     if (st == PKV_OK) st = mapped(host_v, &dv);
     if (st != PKV_OK) return st;
     const int64_t block_vecs = (int64_t)pool_dims.block_size * pool_dims.n_kv_heads * pool_dims.head_dim * 2 / 16;
-    const int64_t n_vecs = (int64_t)n_pairs * 2 * block_vecs;
-    int64_t grid = (n_vecs + 255) / 256;
-    if (grid > 4096) grid = 4096;
+    const int64_t segs_per_half = (block_vecs + kSegVecs - 1) / kSegVecs;
+    const int64_t n_segs = (int64_t)n_pairs * 2 * segs_per_half;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return cuda_err(cudaGetLastError());
+    int64_t grid = (n_segs + 7) / 8;
+    if (grid > 2 * (int64_t)sms) grid = 2 * (int64_t)sms;
     stage_blocks_kernel<<<(unsigned)grid, 256, 0, (cudaStream_t)stream>>>(
         (const uint4 *)dk, (const uint4 *)dv, (uint4 *)pool_k, (uint4 *)pool_v, (const int2 *)pairs, n_host_blocks,
-        pool_dims.n_blocks, block_vecs, n_vecs, dev_status);
+        pool_dims.n_blocks, block_vecs, segs_per_half, n_segs, dev_status);
     return cuda_err(cudaGetLastError());
 }
 
@@ -365,24 +397,29 @@ int paged_decode_streamed(const pkv_bf16 *q, int32_t n_q_heads, const pkv_bf16 *
     int st = mapped(host_k, &dk);
     if (st == PKV_OK) st = mapped(host_v, &dv);
     if (st != PKV_OK) return st;
-    // lazily: pinned staging buffers and their events
+    // lazily: pinned staging buffers, the copy stream and the events
     for (int b = 0; b < 2; ++b) {
         if (!sp->stage[b]) {
             void *p = nullptr;
             if (cudaHostAlloc(&p, sp->stage_ints * 4, cudaHostAllocDefault) != cudaSuccess) return PKV_ERR_CUDA;
             sp->stage[b] = static_cast<int32_t *>(p);
         }
-        if (!sp->copied[b] && cudaEventCreateWithFlags(&sp->copied[b], cudaEventDisableTiming) != cudaSuccess)
-            return PKV_ERR_CUDA;
+        for (cudaEvent_t *e : {&sp->copied[b], &sp->staged[b], &sp->decoded[b]})
+            if (!*e && cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return PKV_ERR_CUDA;
     }
+    if (!sp->entry && cudaEventCreateWithFlags(&sp->entry, cudaEventDisableTiming) != cudaSuccess) return PKV_ERR_CUDA;
+    if (!sp->copy_stream && cudaStreamCreateWithFlags(&sp->copy_stream, cudaStreamNonBlocking) != cudaSuccess)
+        return PKV_ERR_CUDA;
     uint8_t *w = static_cast<uint8_t *>(workspace);
     StreamWs ws;
     ws.decode_ws = w;
     ws.decode_bytes = decode_bytes;
     w += align256(decode_bytes);
-    ws.plan = reinterpret_cast<int32_t *>(w);
     const size_t pints = plan_ints(n_seqs, n_slots);
-    w += align256(pints * 4);
+    for (int b = 0; b < 2; ++b) {
+        ws.plan[b] = reinterpret_cast<int32_t *>(w);
+        w += align256(pints * 4);
+    }
     const size_t rows = (size_t)n_seqs * n_q_heads;
     ws.tile_out = reinterpret_cast<__nv_bfloat16 *>(w);
     w += align256(rows * D * 2);
@@ -392,7 +429,17 @@ int paged_decode_streamed(const pkv_bf16 *q, int32_t n_q_heads, const pkv_bf16 *
     w += align256(rows * D * 4);
     ws.acc_lse = reinterpret_cast<float *>(w);
 
-    cudaStream_t s = (cudaStream_t)stream;
+    // Tiles of at most n_slots / 2 blocks when the batch does not fit the pool:
+    // the least recently used slots a tile stages into are then never those
+    // of the tile before it, so the staging of tile t + 1 (copy stream) only
+    // waits for the attention of tile t - 1 and overlaps that of tile t.
+    int64_t total_blocks = 0;
+    for (int32_t i = 0; i < n_seqs; ++i) total_blocks += (ctx_lens[i] + bs - 1) / bs;
+    const bool overlap = total_blocks > n_slots && n_slots >= 2;
+    const int32_t tile_blocks = overlap ? n_slots / 2 : n_slots;
+    cudaStream_t s = (cudaStream_t)stream, c = sp->copy_stream;
+    if (cudaEventRecord(sp->entry, s) != cudaSuccess || cudaStreamWaitEvent(c, sp->entry, 0) != cudaSuccess)
+        return cuda_err(cudaGetLastError());
     const size_t lens_off = (size_t)n_seqs * n_slots;
     const size_t pairs_off = (lens_off + n_seqs + kPairsAlign - 1) / kPairsAlign * kPairsAlign;
     int32_t cursor[2] = {0, 0}, done = 0;
@@ -402,19 +449,29 @@ int paged_decode_streamed(const pkv_bf16 *q, int32_t n_q_heads, const pkv_bf16 *
         if (cudaEventSynchronize(sp->copied[b]) != cudaSuccess) return cuda_err(cudaGetLastError());   // tile t - 2's copy read it
         int32_t *plan = sp->stage[b];
         int32_t np = 0;
-        st = pkv_sp_plan_tile(sp, host_tables, max_blocks, ctx_lens, n_seqs, bs, cursor, plan, plan + lens_off,
-                              plan + pairs_off, &np, &done);
+        st = pkv_sp_plan_tile(sp, host_tables, max_blocks, ctx_lens, n_seqs, bs, tile_blocks, cursor, plan,
+                              plan + lens_off, plan + pairs_off, &np, &done);
         if (st != PKV_OK) return st;
-        if (cudaMemcpyAsync(ws.plan, plan, pints * 4, cudaMemcpyHostToDevice, s) != cudaSuccess) return PKV_ERR_CUDA;
-        if (cudaEventRecord(sp->copied[b], s) != cudaSuccess) return PKV_ERR_CUDA;
-        st = paged_kv_stage_blocks(ws.plan + pairs_off, np, host_k, host_v, n_host_blocks, pool_k, pool_v, pool_dims,
-                                   dev_status, stream);
+        // copy stream: wait until no earlier tile still reads the slots (and the
+        // device plan buffer) this tile overwrites, then plan copy and staging
+        const int64_t need = overlap ? t - 2 : t - 1;
+        if (need >= 0 && cudaStreamWaitEvent(c, sp->decoded[need & 1], 0) != cudaSuccess)
+            return cuda_err(cudaGetLastError());
+        if (cudaMemcpyAsync(ws.plan[b], plan, pints * 4, cudaMemcpyHostToDevice, c) != cudaSuccess ||
+            cudaEventRecord(sp->copied[b], c) != cudaSuccess)
+            return cuda_err(cudaGetLastError());
+        st = paged_kv_stage_blocks(ws.plan[b] + pairs_off, np, host_k, host_v, n_host_blocks, pool_k, pool_v,
+                                   pool_dims, dev_status, c);
         if (st != PKV_OK) return st;
-        st = paged_decode_attention(q, n_q_heads, pool_k, pool_v, nullptr, nullptr, PKV_KV_BF16, pool_dims, ws.plan,
-                                    n_slots, ws.plan + lens_off, n_seqs, softmax_scale, 0,
+        if (cudaEventRecord(sp->staged[b], c) != cudaSuccess || cudaStreamWaitEvent(s, sp->staged[b], 0) != cudaSuccess)
+            return cuda_err(cudaGetLastError());
+        // caller's stream: attention over the tile, then its merge into the running state
+        st = paged_decode_attention(q, n_q_heads, pool_k, pool_v, nullptr, nullptr, PKV_KV_BF16, pool_dims, ws.plan[b],
+                                    n_slots, ws.plan[b] + lens_off, n_seqs, softmax_scale, 0,
                                     reinterpret_cast<pkv_bf16 *>(ws.tile_out), ws.tile_lse,
                                     ws.decode_ws, ws.decode_bytes, dev_status, stream);
         if (st != PKV_OK) return st;
+        if (cudaEventRecord(sp->decoded[b], s) != cudaSuccess) return cuda_err(cudaGetLastError());
         const unsigned grid = (unsigned)((rows + 7) / 8);
         if (D == 128)
             merge_tile_kernel<128><<<grid, 256, 0, s>>>(ws.tile_out, ws.tile_lse, ws.acc, ws.acc_lse, (int64_t)rows, first);

@@ -61,10 +61,13 @@ def test_unpinned_host_tier_is_refused(P):
     assert e.value.status == 1
 
 
-def run_streamed(P, sp, q, hk, hv, n_slots, tables, lens, scale):
-    bs, hkv, d = hk.shape[1], hk.shape[2], hk.shape[3]
-    pool_k = torch.zeros((n_slots + 1, bs, hkv, d), dtype=torch.bfloat16, device="cuda")
-    pool_v = torch.zeros_like(pool_k)
+def scratch(hk, n_slots):
+    pool_k = torch.zeros((n_slots + 1,) + tuple(hk.shape[1:]), dtype=torch.bfloat16, device="cuda")
+    return pool_k, torch.zeros_like(pool_k)
+
+
+def run_streamed(P, sp, q, hk, hv, pools, tables, lens, scale):
+    pool_k, pool_v = pools
     lse = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
     out = P.paged_decode_streamed(q, hk, hv, pool_k, pool_v, sp, torch.tensor(tables, dtype=torch.int32),
@@ -82,7 +85,10 @@ def oracle_ref(q, hk, hv, tables, lens, scale):
     return ref, ref_lse
 
 
-@pytest.mark.parametrize("n_slots,head_dim,g", [(24, 128, 4), (7, 64, 8), (400, 128, 2)])
+# 24 and 7 slots: the batch (100 blocks) does not fit, tiles of half the pool
+# stage on the copy stream while the tile before is attended; 2 slots: tiles of
+# one block; 400 slots: one tile
+@pytest.mark.parametrize("n_slots,head_dim,g", [(24, 128, 4), (7, 64, 8), (2, 128, 4), (400, 128, 2)])
 def test_streamed_decode_matches_the_oracle(P, n_slots, head_dim, g):
     gen = torch.Generator().manual_seed(9 + n_slots)
     bs, hkv, n_host, n = 16, 4, 90, 6
@@ -95,13 +101,17 @@ def test_streamed_decode_matches_the_oracle(P, n_slots, head_dim, g):
     q = torch.randn((n, hkv * g, head_dim), generator=gen).to(torch.bfloat16).cuda()
     scale = 1.0 / head_dim ** 0.5
     sp = P.ScratchPool(n_slots, n)
-    out, lse, _ = run_streamed(P, sp, q, hk, hv, n_slots, tables, lens, scale)
+    pools = scratch(hk, n_slots)
+    out, lse, _ = run_streamed(P, sp, q, hk, hv, pools, tables, lens, scale)
     ref, ref_lse = oracle_ref(q, hk, hv, tables, lens, scale)
     mx, mean = attention_errors(out, ref)
     assert mx <= BF16_MAX and mean <= BF16_MEAN, (mx, mean)
     live = np.array(lens) > 0
     assert np.abs(lse.cpu().numpy()[live] - ref_lse[live]).max() <= LSE_TOL
     assert np.all(out.float().cpu().numpy()[~live] == 0) and np.all(np.isneginf(lse.cpu().numpy()[~live]))
+    # a second call on the same scratch pool (residency left by the first) gives the same bits
+    again, lse2, _ = run_streamed(P, sp, q, hk, hv, pools, tables, lens, scale)
+    assert torch.equal(again, out) and torch.equal(lse2, lse)
 
 
 def test_residency_carries_over_and_invalidation_restages(P):

@@ -83,3 +83,39 @@ def test_tiles_cover_every_block_once_in_order():
                 assert all(x == sp.n_slots for x in tt[s][k:])
         assert tok == lens
         assert [len(x) for x in seen] == [len(t) for t in tables]
+
+
+def test_capped_tiles_take_at_most_tile_blocks():
+    sp = ScratchPoolOracle(6)
+    cursor, sizes = [0, 0], []
+    while True:
+        tt, tl, pairs, done = sp.plan_tile([[0, 1, 2, 3, 4, 5, 6]], [112], 16, cursor, tile_blocks=3)
+        sizes.append(sum(1 for x in tt[0] if x != 6))
+        if done:
+            break
+    assert sizes == [3, 3, 1]
+
+
+def test_half_pool_tiles_never_stage_into_the_previous_tiles_slots():
+    # least recently used: with tiles of at most n_slots // 2 blocks the slots a
+    # tile stages into are never the slots the tile before it reads, whatever
+    # the residency left by earlier calls and invalidations
+    rng = random.Random(11)
+    for _ in range(200):
+        n_slots = rng.randrange(2, 12)
+        sp = ScratchPoolOracle(n_slots)
+        for call in range(3):
+            n = rng.randrange(1, 5)
+            bs = 16
+            lens = [rng.randrange(0, 300) for _ in range(n)]
+            tables = [[rng.randrange(0, 40) for _ in range(-(-L // bs))] for L in lens]
+            cursor, prev = [0, 0], set()
+            while True:
+                tt, tl, pairs, done = sp.plan_tile(tables, lens, bs, cursor, tile_blocks=n_slots // 2)
+                used = {x for row in tt for x in row if x != n_slots}
+                assert not ({slot for _, slot in pairs} & prev)
+                prev = used
+                if done:
+                    break
+            if rng.random() < 0.5:
+                sp.invalidate(rng.randrange(0, 40))

@@ -23,7 +23,7 @@ def P():
     return P
 
 
-@pytest.mark.parametrize("seed", range(6))
+@pytest.mark.parametrize("seed", range(10))
 def test_planner_matches_the_oracle(P, seed):
     rng = random.Random(seed)
     bs = rng.choice([16, 32])
@@ -39,9 +39,10 @@ def test_planner_matches_the_oracle(P, seed):
         tables = [[rng.randrange(0, n_host) for _ in range(max_blocks)] for _ in range(n)]
         t_tab, t_len = torch.tensor(tables, dtype=torch.int32), torch.tensor(lens, dtype=torch.int32)
         cl, cr = [0, 0], [0, 0]
+        cap = rng.choice([0, 0, n_slots // 2, rng.randrange(1, n_slots + 2)])
         while True:
-            tt, tl, pairs, done = lib.plan_tile(t_tab, t_len, bs, cl)
-            rtt, rtl, rpairs, rdone = ref.plan_tile(tables, lens, bs, cr)
+            tt, tl, pairs, done = lib.plan_tile(t_tab, t_len, bs, cl, tile_blocks=cap)
+            rtt, rtl, rpairs, rdone = ref.plan_tile(tables, lens, bs, cr, tile_blocks=cap)
             assert tt.tolist() == rtt and tl.tolist() == rtl and pairs == rpairs and done == rdone
             assert cl == cr
             if done:
