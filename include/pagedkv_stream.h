@@ -51,10 +51,13 @@ int pkv_sp_invalidate(pkv_scratch_pool *sp, int32_t host_block);
  * slot, or takes the least recently used slot not yet used by this tile (its
  * old block is forgotten) and adds (host block, slot) to pairs [n_slots][2]
  * (*n_pairs of them).  With tile_blocks <= n_slots / 2 a tile never stages
- * into a slot the tile before it uses (those are the most recently used).  tile_tables
- * [n_seqs][n_slots] receives each sequence's slots in token order (unused
- * entries = n_slots, the scratch slot), tile_lens [n_seqs] its tokens in this
- * tile.  Advances cursor; *done = 1 when no block is left.
+ * into a slot the tile before it uses (those are the most recently used).
+ * tile_tables [n_seqs][W], W = min(tile cap, max_blocks), receives each
+ * sequence's slots in token order (unused entries = n_slots, the scratch
+ * slot), tile_lens [n_seqs] its tokens in this tile.  Advances cursor; *done =
+ * 1 when no block is left.  A negative host id among the tile's blocks returns
+ * PKV_ERR_OUT_OF_RANGE before any state changes.  The residency index takes
+ * 4 bytes per host block up to the largest id seen.
  */
 int pkv_sp_plan_tile(pkv_scratch_pool *sp, const int32_t *host_tables, int32_t max_blocks, const int32_t *ctx_lens,
                      int32_t n_seqs, int32_t block_size, int32_t tile_blocks, int32_t *cursor, int32_t *tile_tables,

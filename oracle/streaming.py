@@ -47,12 +47,16 @@ class ScratchPoolOracle:
         self.order.remove(slot)
         self.order.insert(0, slot)            # reused first
 
-    def plan_tile(self, host_tables, ctx_lens, block_size: int, cursor, tile_blocks: int = 0):
+    def plan_tile(self, host_tables, ctx_lens, block_size: int, cursor, tile_blocks: int = 0, max_blocks=None):
         """Next tile of at most tile_blocks blocks (0 or more than n_slots: all
         slots) from cursor = [sequence, block]; returns (tile_tables as lists
-        padded with n_slots, tile_lens, pairs [(host block, slot)], done) and
-        advances cursor."""
+        padded with n_slots to min(tile size, max_blocks) entries, tile_lens,
+        pairs [(host block, slot)], done) and advances cursor.  max_blocks
+        defaults to the longest table row (at least 1)."""
         cap = self.n_slots if tile_blocks <= 0 or tile_blocks > self.n_slots else tile_blocks
+        if max_blocks is None:
+            max_blocks = max([1] + [len(r) for r in host_tables])
+        width = min(cap, max_blocks)
         n = len(ctx_lens)
         nb = [-(-int(L) // block_size) for L in ctx_lens]
         tables = [[] for _ in range(n)]
@@ -84,5 +88,5 @@ class ScratchPoolOracle:
         while s < n and j >= nb[s]:
             s, j = s + 1, 0
         cursor[0], cursor[1] = s, j
-        padded = [t + [self.n_slots] * (self.n_slots - len(t)) for t in tables]
+        padded = [t + [self.n_slots] * (width - len(t)) for t in tables]
         return padded, lens, pairs, s >= n

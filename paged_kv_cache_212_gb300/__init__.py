@@ -509,7 +509,8 @@ class ScratchPool:
         host_tables = host_tables.to(torch.int32).contiguous()
         ctx_lens = ctx_lens.to(torch.int32).contiguous()
         n_seqs = ctx_lens.shape[0]
-        tt = torch.empty((n_seqs, self.n_slots), dtype=torch.int32)
+        cap = self.n_slots if tile_blocks <= 0 or tile_blocks > self.n_slots else int(tile_blocks)
+        tt = torch.empty((n_seqs, min(cap, host_tables.shape[1])), dtype=torch.int32)
         tl = torch.empty(n_seqs, dtype=torch.int32)
         pr = torch.empty((self.n_slots, 2), dtype=torch.int32)
         cur = (ctypes.c_int32 * 2)(*cursor)

@@ -8,7 +8,6 @@
 #include <string.h>
 
 #include <new>
-#include <unordered_map>
 #include <vector>
 
 #include "../../include/pagedkv_stream.h"
@@ -17,7 +16,9 @@
 
 struct pkv_scratch_pool {
     int32_t n_slots = 0, max_seqs = 0;
-    std::unordered_map<int32_t, int32_t> slot_of;   // host block -> slot
+    // host block -> slot (-1: not resident); grown to the largest id seen (4 bytes
+    // per host block, against a host tier of kilobytes per block)
+    std::vector<int32_t> slot_of;
     std::vector<int32_t> block_of;                  // slot -> host block (-1: empty)
     // least recently used list over slots: head = next to reuse, tail = newest
     std::vector<int32_t> prev, next;
@@ -47,6 +48,12 @@ struct pkv_scratch_pool {
         if (tail >= 0) next[tail] = s; else head = s;
         tail = s;
     }
+    int32_t resident(int32_t hb) const { return hb >= 0 && (size_t)hb < slot_of.size() ? slot_of[hb] : -1; }
+    void set_resident(int32_t hb, int32_t slot)
+    {
+        if ((size_t)hb >= slot_of.size()) slot_of.resize((size_t)hb + 1 + slot_of.size() / 2, -1);
+        slot_of[hb] = slot;
+    }
     void push_front(int32_t s)
     {
         next[s] = head;
@@ -64,13 +71,14 @@ namespace {
 
 constexpr int kPairsAlign = 2;   // pairs start at an even int offset (8-byte int2 loads)
 
-// plan layout in int32 units: tables [n_seqs][n_slots], lens [n_seqs], pairs [n_slots][2]
-size_t plan_ints(int32_t n_seqs, int32_t n_slots)
+// plan layout in int32 units: tables [n_seqs][width], lens [n_seqs], pairs [cap][2]
+// (width = min(cap, max_blocks): a sequence has at most that many blocks in a tile)
+size_t pairs_offset(int32_t n_seqs, int32_t width)
 {
-    size_t t = (size_t)n_seqs * n_slots + n_seqs;
-    t = (t + kPairsAlign - 1) / kPairsAlign * kPairsAlign;
-    return t + 2 * (size_t)n_slots;
+    const size_t t = (size_t)n_seqs * width + n_seqs;
+    return (t + kPairsAlign - 1) / kPairsAlign * kPairsAlign;
 }
+size_t plan_ints(int32_t n_seqs, int32_t width, int32_t cap) { return pairs_offset(n_seqs, width) + 2 * (size_t)cap; }
 
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
@@ -90,7 +98,7 @@ size_t stream_ws_bytes(int32_t n_seqs, int32_t n_q_heads, int32_t head_dim, int3
     if (d == 0) return 0;
     if (decode_bytes) *decode_bytes = d;
     const size_t rows = (size_t)n_seqs * n_q_heads;
-    return align256(d) + 2 * align256(plan_ints(n_seqs, n_slots) * 4) + align256(rows * head_dim * 2) +
+    return align256(d) + 2 * align256(plan_ints(n_seqs, n_slots, n_slots) * 4) + align256(rows * head_dim * 2) +
            align256(rows * 4) + align256(rows * head_dim * 4) + align256(rows * 4);
 }
 
@@ -226,7 +234,7 @@ int pkv_sp_create(int32_t n_slots, int32_t max_seqs, pkv_scratch_pool **out)
     sp->next.assign(n_slots, -1);
     sp->pinned_tile.assign(n_slots, -1);
     for (int32_t s = 0; s < n_slots; ++s) sp->push_back(s);   // slot 0 is reused first
-    sp->stage_ints = plan_ints(max_seqs, n_slots);
+    sp->stage_ints = plan_ints(max_seqs, n_slots, n_slots);
     *out = sp;
     return PKV_OK;
 }
@@ -254,18 +262,15 @@ void pkv_sp_destroy(pkv_scratch_pool *sp)
 
 int32_t pkv_sp_lookup(const pkv_scratch_pool *sp, int32_t host_block)
 {
-    if (!sp) return -1;
-    auto it = sp->slot_of.find(host_block);
-    return it == sp->slot_of.end() ? -1 : it->second;
+    return sp ? sp->resident(host_block) : -1;
 }
 
 int pkv_sp_invalidate(pkv_scratch_pool *sp, int32_t host_block)
 {
     if (!sp) return PKV_ERR_INVALID_ARG;
-    auto it = sp->slot_of.find(host_block);
-    if (it == sp->slot_of.end()) return PKV_OK;
-    const int32_t s = it->second;
-    sp->slot_of.erase(it);
+    const int32_t s = sp->resident(host_block);
+    if (s < 0) return PKV_OK;
+    sp->slot_of[host_block] = -1;
     sp->block_of[s] = -1;
     sp->unlink(s);
     sp->push_front(s);   // an empty slot is reused first
@@ -283,12 +288,28 @@ int pkv_sp_plan_tile(pkv_scratch_pool *sp, const int32_t *host_tables, int32_t m
         if (ctx_lens[s] < 0 || (int64_t)ctx_lens[s] > (int64_t)max_blocks * block_size) return PKV_ERR_OUT_OF_RANGE;
     const int32_t n_slots = sp->n_slots;
     const int32_t cap = tile_blocks <= 0 || tile_blocks > n_slots ? n_slots : tile_blocks;
-    for (int64_t i = 0; i < (int64_t)n_seqs * n_slots; ++i) tile_tables[i] = n_slots;   // the scratch slot
+    const int32_t width = cap < max_blocks ? cap : max_blocks;
+    auto blocks_of = [&](int32_t q) { return (ctx_lens[q] + block_size - 1) / block_size; };
+    // the tile's host ids are checked before any state changes
+    {
+        int32_t s = cursor[0], j = cursor[1], taken = 0;
+        if (s < 0 || j < 0) return PKV_ERR_INVALID_ARG;
+        while (s < n_seqs && taken < cap) {
+            if (j >= blocks_of(s)) {
+                ++s;
+                j = 0;
+                continue;
+            }
+            if (host_tables[(int64_t)s * max_blocks + j] < 0) return PKV_ERR_OUT_OF_RANGE;
+            ++j;
+            ++taken;
+        }
+    }
+    for (int64_t i = 0; i < (int64_t)n_seqs * width; ++i) tile_tables[i] = n_slots;   // the scratch slot
     for (int32_t s = 0; s < n_seqs; ++s) tile_lens[s] = 0;
     std::vector<int32_t> used(n_seqs, 0);
     const int64_t tile = ++sp->tiles;
     int32_t s = cursor[0], j = cursor[1], taken = 0, np = 0;
-    auto blocks_of = [&](int32_t q) { return (ctx_lens[q] + block_size - 1) / block_size; };
     while (s < n_seqs && taken < cap) {
         if (j >= blocks_of(s)) {
             ++s;
@@ -296,16 +317,13 @@ int pkv_sp_plan_tile(pkv_scratch_pool *sp, const int32_t *host_tables, int32_t m
             continue;
         }
         const int32_t hb = host_tables[(int64_t)s * max_blocks + j];
-        int32_t slot;
-        auto it = sp->slot_of.find(hb);
-        if (it != sp->slot_of.end()) {
-            slot = it->second;
-        } else {
+        int32_t slot = sp->resident(hb);
+        if (slot < 0) {
             slot = sp->head;   // least recently used; every slot of this tile sits behind it
             if (sp->pinned_tile[slot] == tile) return PKV_ERR_STATE;   // cannot happen: taken < n_slots
-            if (sp->block_of[slot] >= 0) sp->slot_of.erase(sp->block_of[slot]);
+            if (sp->block_of[slot] >= 0) sp->slot_of[sp->block_of[slot]] = -1;
             sp->block_of[slot] = hb;
-            sp->slot_of[hb] = slot;
+            sp->set_resident(hb, slot);
             pairs[2 * np] = hb;
             pairs[2 * np + 1] = slot;
             ++np;
@@ -313,7 +331,7 @@ int pkv_sp_plan_tile(pkv_scratch_pool *sp, const int32_t *host_tables, int32_t m
         sp->pinned_tile[slot] = tile;
         sp->unlink(slot);
         sp->push_back(slot);
-        tile_tables[(int64_t)s * n_slots + used[s]++] = slot;
+        tile_tables[(int64_t)s * width + used[s]++] = slot;
         tile_lens[s] += (int32_t)((int64_t)ctx_lens[s] - (int64_t)j * block_size < block_size
                                       ? ctx_lens[s] - j * block_size : block_size);
         ++j;
@@ -415,10 +433,9 @@ int paged_decode_streamed(const pkv_bf16 *q, int32_t n_q_heads, const pkv_bf16 *
     ws.decode_ws = w;
     ws.decode_bytes = decode_bytes;
     w += align256(decode_bytes);
-    const size_t pints = plan_ints(n_seqs, n_slots);
     for (int b = 0; b < 2; ++b) {
         ws.plan[b] = reinterpret_cast<int32_t *>(w);
-        w += align256(pints * 4);
+        w += align256(plan_ints(n_seqs, n_slots, n_slots) * 4);
     }
     const size_t rows = (size_t)n_seqs * n_q_heads;
     ws.tile_out = reinterpret_cast<__nv_bfloat16 *>(w);
@@ -440,8 +457,9 @@ int paged_decode_streamed(const pkv_bf16 *q, int32_t n_q_heads, const pkv_bf16 *
     cudaStream_t s = (cudaStream_t)stream, c = sp->copy_stream;
     if (cudaEventRecord(sp->entry, s) != cudaSuccess || cudaStreamWaitEvent(c, sp->entry, 0) != cudaSuccess)
         return cuda_err(cudaGetLastError());
-    const size_t lens_off = (size_t)n_seqs * n_slots;
-    const size_t pairs_off = (lens_off + n_seqs + kPairsAlign - 1) / kPairsAlign * kPairsAlign;
+    const int32_t width = tile_blocks < max_blocks ? tile_blocks : max_blocks;   // tile table row length
+    const size_t lens_off = (size_t)n_seqs * width, pairs_off = pairs_offset(n_seqs, width);
+    const size_t pints = plan_ints(n_seqs, width, tile_blocks);
     int32_t cursor[2] = {0, 0}, done = 0;
     int first = 1;
     for (int64_t t = 0; !done; ++t) {
@@ -465,13 +483,16 @@ int paged_decode_streamed(const pkv_bf16 *q, int32_t n_q_heads, const pkv_bf16 *
         if (st != PKV_OK) return st;
         if (cudaEventRecord(sp->staged[b], c) != cudaSuccess || cudaStreamWaitEvent(s, sp->staged[b], 0) != cudaSuccess)
             return cuda_err(cudaGetLastError());
-        // caller's stream: attention over the tile, then its merge into the running state
+        // caller's stream: attention over the tile, then its merge into the running
+        // state (a batch in one tile is attended straight into out and lse_out)
+        const bool only = first && done;
         st = paged_decode_attention(q, n_q_heads, pool_k, pool_v, nullptr, nullptr, PKV_KV_BF16, pool_dims, ws.plan[b],
-                                    n_slots, ws.plan[b] + lens_off, n_seqs, softmax_scale, 0,
-                                    reinterpret_cast<pkv_bf16 *>(ws.tile_out), ws.tile_lse,
-                                    ws.decode_ws, ws.decode_bytes, dev_status, stream);
+                                    width, ws.plan[b] + lens_off, n_seqs, softmax_scale, 0,
+                                    only ? out : reinterpret_cast<pkv_bf16 *>(ws.tile_out),
+                                    only ? lse_out : ws.tile_lse, ws.decode_ws, ws.decode_bytes, dev_status, stream);
         if (st != PKV_OK) return st;
         if (cudaEventRecord(sp->decoded[b], s) != cudaSuccess) return cuda_err(cudaGetLastError());
+        if (only) return PKV_OK;
         const unsigned grid = (unsigned)((rows + 7) / 8);
         if (D == 128)
             merge_tile_kernel<128><<<grid, 256, 0, s>>>(ws.tile_out, ws.tile_lse, ws.acc, ws.acc_lse, (int64_t)rows, first);

@@ -137,7 +137,7 @@ def test_write_to_bad_slots_is_flagged_and_skipped(P):
     assert np.array_equal(host(gk), rk) and np.array_equal(host(gv), rv)
 
 
-@pytest.mark.parametrize("name,extra", [("cfg2_gather", 0), ("cfg0", 13), ("ragged_d64", 1)])
+@pytest.mark.parametrize("name,extra", [("cfg2_gather", 0), ("cfg0", 13), ("ragged_d64", 1), ("ragged_g8_bs32", 7)])
 def test_gather_bit_exact(P, name, extra):
     w = workload(name)
     kp, vp, _, _ = pools(name, after_step=w.kind != "gather")

@@ -43,7 +43,7 @@ def test_a_block_shared_by_two_sequences_is_staged_once():
 def test_tiles_cross_sequence_boundaries():
     sp = ScratchPoolOracle(4)
     tiles = run_all(sp, [[0, 1, 2], [3, 4]], [48, 17], 16)
-    assert tiles[0][0] == [[0, 1, 2, 4], [3, 4, 4, 4]] and tiles[0][1] == [48, 16]
+    assert tiles[0][0] == [[0, 1, 2], [3, 4, 4]] and tiles[0][1] == [48, 16]   # rows: min(4 slots, 3 blocks)
     assert tiles[1][1] == [0, 1] and tiles[1][0][1][0] == 0    # block 4 takes the oldest slot
 
 

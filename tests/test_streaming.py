@@ -42,7 +42,7 @@ def test_planner_matches_the_oracle(P, seed):
         cap = rng.choice([0, 0, n_slots // 2, rng.randrange(1, n_slots + 2)])
         while True:
             tt, tl, pairs, done = lib.plan_tile(t_tab, t_len, bs, cl, tile_blocks=cap)
-            rtt, rtl, rpairs, rdone = ref.plan_tile(tables, lens, bs, cr, tile_blocks=cap)
+            rtt, rtl, rpairs, rdone = ref.plan_tile(tables, lens, bs, cr, tile_blocks=cap, max_blocks=max_blocks)
             assert tt.tolist() == rtt and tl.tolist() == rtl and pairs == rpairs and done == rdone
             assert cl == cr
             if done:
@@ -59,3 +59,13 @@ def test_planner_rejects_lengths_past_the_table(P):
     lib = P.ScratchPool(4, 2)
     with pytest.raises(P.PagedKVError):
         lib.plan_tile(torch.zeros((1, 2), dtype=torch.int32), torch.tensor([33], dtype=torch.int32), 16, [0, 0])
+
+
+def test_planner_rejects_a_negative_host_id_without_changing_state(P):
+    lib = P.ScratchPool(4, 2)
+    tab = torch.tensor([[3, -1]], dtype=torch.int32)
+    with pytest.raises(P.PagedKVError):
+        lib.plan_tile(tab, torch.tensor([20], dtype=torch.int32), 16, [0, 0])
+    assert lib.lookup(3) == -1
+    tt, tl, pairs, done = lib.plan_tile(tab, torch.tensor([16], dtype=torch.int32), 16, [0, 0])
+    assert pairs == [(3, 0)] and tt.tolist() == [[0, 4]] and done
