@@ -766,9 +766,11 @@ def main():
     d_views = [views(b) for b in d_arena]
     d_out = [torch.empty_like(q) for _ in range(2)]
     h_outs = [torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(2)]
-    copy_stream = torch.cuda.Stream(device=device)
+    copy_stream = torch.cuda.Stream(device=device)     # inputs, host -> device
+    out_stream = torch.cuda.Stream(device=device)      # outputs, device -> host (not behind the next inputs)
     ev_in = [torch.cuda.Event() for _ in range(2)]
     ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_drained = [torch.cuda.Event() for _ in range(2)]
     ev_out = torch.cuda.Event()
 
     def e2e_run(n):
@@ -780,14 +782,17 @@ def main():
                 d_arena[b].copy_(h_arena, non_blocking=True)
                 ev_in[b].record(copy_stream)
             stream.wait_event(ev_in[b])
+            if i >= 2:
+                stream.wait_event(ev_drained[b])               # output i - 2 has left d_out[b]
             dk, dv, dq, dtab, dstart, dctx = d_views[b]
             P.paged_decode_step(dk, dv, dstart, dq, kp, vp, dtab, dctx, w.softmax_scale, k_scales=ks,
                                 v_scales=vs, split_tokens=split, out=d_out[b], workspace=ws, dev_status=status)
             ev_done[b].record(stream)
-            with torch.cuda.stream(copy_stream):
-                copy_stream.wait_event(ev_done[b])
+            with torch.cuda.stream(out_stream):
+                out_stream.wait_event(ev_done[b])
                 h_outs[b].copy_(d_out[b], non_blocking=True)
-        ev_out.record(copy_stream)
+                ev_drained[b].record(out_stream)
+        ev_out.record(out_stream)
         stream.wait_event(ev_out)                          # the last output has reached the host
 
     e2e_run(3)
@@ -797,6 +802,7 @@ def main():
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     copy_stream.wait_event(e0)
+    out_stream.wait_event(e0)
     e2e_run(e2e_steps)
     e1.record(stream)
     torch.cuda.synchronize()
