@@ -29,6 +29,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "paged decode attention HBM GB/s (% of GB300 peak) and seq-steps/s per layer"
+PREFILL_METRIC = "chunked paged prefill attention TFLOP/s (config 3)"
 FALLBACK_HBM_GBS = 6800.0
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant
@@ -252,6 +253,76 @@ def cpu_baseline(cfg, budget_s=12.0, threads=None):
             "seq_steps_per_s": round(reps * w.n_seqs / el, 2)}
 
 
+def prefill_row_flops(w):
+    """Flops of each query row of the chunk: 4 Hq D (P_s + i + 1) per (s, i)."""
+    import numpy as np
+    P = np.asarray(w.stored_lens, np.int64)[:, None]
+    i = np.arange(w.n_new, dtype=np.int64)[None, :]
+    return 4 * w.n_q_heads * w.head_dim * (P + i + 1)
+
+
+def oracle_prefill_sample(w, budget_s, threads):
+    """The float64 oracle's chunk write + prefill over an evenly strided sample
+    of the chunk's query rows (every sequence, rows i = 0, k, 2k, ...), k chosen
+    so that one pass takes about budget_s.  Returns (flops per pass, a pass
+    callable, description)."""
+    import numpy as np
+    import oracle
+    from oracle_pools import dims_of, empty_pools, write_prefix
+    kp, vp, _, _ = empty_pools(w, poison=False)
+    write_prefix(w, kp, vp)
+    d = dims_of(w)
+    rowf = prefill_row_flops(w)
+
+    def select(stride):
+        sel = np.zeros((w.n_seqs, w.n_new), bool)
+        sel[:, ::stride] = True
+        return sel
+
+    def one(sel):
+        oracle.write_bf16(w.k_new, w.v_new, kp, vp, d, w.tables, w.start_pos)
+        code, _, _ = oracle.prefill(w.q, kp, vp, d, w.tables, w.stored_lens, w.softmax_scale, row_select=sel,
+                                    n_threads=threads)
+        assert code == oracle.OK
+
+    probe = select(w.n_new)                     # row 0 of every sequence
+    t0 = time.perf_counter()
+    one(probe)
+    t_probe = time.perf_counter() - t0
+    rate = float(rowf[probe].sum()) / max(t_probe, 1e-9)
+    if t_probe <= budget_s:
+        stride = max(1, int(np.ceil(float(rowf.sum()) / (rate * budget_s))))
+        sel = select(stride)
+        what = f"one query row in {stride} ({int(sel.sum())} of {w.n_seqs * w.n_new} rows, all heads)"
+    else:
+        # below one row per sequence: the single row whose key count best fits the budget
+        want = rate * budget_s
+        flat = rowf.reshape(-1)
+        fits = np.flatnonzero(flat <= want)
+        k = int(fits[np.argmax(flat[fits])]) if fits.size else int(np.argmin(flat))
+        sel = np.zeros(flat.shape, bool)
+        sel[k] = True
+        sel = sel.reshape(rowf.shape)
+        what = f"query row {k % w.n_new} of sequence {k // w.n_new} (all heads)"
+    return float(rowf[sel].sum()), (lambda: one(sel)), "the chunk write + float64 prefill of " + what
+
+
+def cpu_baseline_prefill(budget_s=12.0, threads=None):
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    w = make_workload(3, "cpu")
+    threads = threads or (os.cpu_count() or 1)
+    flops, run, what = oracle_prefill_sample(w, budget_s / 2, threads)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        run()
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s / 2:
+            break
+    return {"value": round(reps * flops / el / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{reps} passes of {what} in {el:.1f} s"}
+
+
 def run_reference(args, rank, world):
     """The reference arm: the float64 oracle on the host cores, same metric and
     workload; each step is a bounded sample (the first n sequences)."""
@@ -263,48 +334,87 @@ def run_reference(args, rank, world):
     from oracle_pools import dims_of, empty_pools, write_prefix
     w = make_workload(args.config, "cpu")
     threads = os.cpu_count() or 1
+    if args.config == 3:
+        flops, run, what = oracle_prefill_sample(w, 150.0 / max(1, args.steps + args.warmup), threads)
+        for _ in range(args.warmup):
+            run()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            run()
+        el = time.perf_counter() - t0
+        tf = args.steps * flops / el / 1e12
+        print(json.dumps({
+            "impl": "reference", "metric": PREFILL_METRIC, "value": round(tf, 6), "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(el / args.steps * 1e3, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "n_seqs": w.n_seqs, "chunk": w.n_new},
+            "cpu_baseline": {"value": round(tf, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": "each step: " + what},
+            "e2e": {"value": round(tf, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}),
+            flush=True)
+        return
     kp, vp, ks, vs = empty_pools(w, poison=False)
     write_prefix(w, kp, vp, ks, vs)
     d = dims_of(w)
 
-    def step(n):
+    def step(n, ctx0=None):
         sl = slice(0, n)
         if w.kv_format == "int8":
             oracle.write_int8(w.k_new[sl], w.v_new[sl], kp, vp, ks, vs, d, w.tables[sl], w.start_pos[sl])
         else:
             oracle.write_bf16(w.k_new[sl], w.v_new[sl], kp, vp, d, w.tables[sl], w.start_pos[sl])
-        oracle.decode(w.q[sl], kp, vp, d, w.tables[sl], w.ctx_lens[sl], w.softmax_scale, ks, vs,
-                      n_threads=threads)
+        ctx = w.ctx_lens[sl].clone()
+        if ctx0 is not None:
+            ctx[0] = ctx0
+        oracle.decode(w.q[sl], kp, vp, d, w.tables[sl], ctx, w.softmax_scale, ks, vs, n_threads=threads)
 
-    t0 = time.perf_counter()
-    step(w.n_seqs)
-    t_full = time.perf_counter() - t0
+    def timed(*a):
+        t0 = time.perf_counter()
+        step(*a)
+        return time.perf_counter() - t0
+
+    # each step's sample fits 150 s / (steps + warmup): the first n sequences,
+    # or, below one sequence, sequence 0 attending only its first ctx0 tokens
     budget = 150.0 / max(1, args.steps + args.warmup)
+    t_full = timed(w.n_seqs)
     n = max(1, min(w.n_seqs, int(w.n_seqs * budget / max(t_full, 1e-9))))
+    ctx0 = None
+    if n == 1:
+        full0 = int(w.ctx_lens[0])
+        t_one = timed(1)
+        if t_one > budget:
+            ctx0 = max(w.n_new, min(full0, int(full0 * budget / t_one)))
     for _ in range(args.warmup):
-        step(n)
+        step(n, ctx0)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        step(n)
+        step(n, ctx0)
     el = time.perf_counter() - t0
-    sub = make_sub_bytes(w, n)
+    sub = make_sub_bytes(w, n, ctx0)
     gbs = args.steps * sub / el / 1e9
     line = {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "config": bench_config(w, args),
             "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-                             "sample": f"each step: write + float64 decode of the first {n} of {w.n_seqs} "
-                                       "sequences"},
+                             "sample": (f"each step: write + float64 decode of the first {n} of {w.n_seqs} "
+                                        "sequences" if ctx0 is None else
+                                        f"each step: write + float64 decode of sequence 0 over its first {ctx0} "
+                                        f"of {int(w.ctx_lens[0])} tokens")},
             "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
-def make_sub_bytes(w, n):
+def make_sub_bytes(w, n, ctx0=None):
+    """Algorithmic bytes of the step restricted to the first n sequences (and,
+    with ctx0, sequence 0 attending only its first ctx0 tokens)."""
     import copy
     sub = copy.copy(w)
     sub.n_seqs = n
-    sub.stored_lens = w.stored_lens[:n]
+    sub.stored_lens = w.stored_lens[:n].clone()
+    if ctx0 is not None:
+        sub.stored_lens[0] = ctx0 - w.n_new
     sub.tables = w.tables[:n]
     dec, wr = algorithmic_bytes(sub)
     return dec + wr
@@ -395,12 +505,38 @@ def run_prefill_bench(args, P, w, device, rank, world):
             step(ev[i])
         t1.record(stream)
         torch.cuda.synchronize()
-    ms = t0.elapsed_time(t1) / K
+    ms = max_over_ranks([t0.elapsed_time(t1) / K], device)[0]
     pre_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
     flops = prefill_flops(w)
     peak, kind = measured_peaks("bf16_tflops")
     ach = flops / (pre_ms * 1e-3) / 1e12
-    line = {"metric": "chunked paged prefill attention TFLOP/s (config 3)", "value": round(world * flops / (ms * 1e-3) / 1e12, 2),
+    # end to end: the chunk's rows, queries, tables and prefix lengths from pinned
+    # host memory every step, the output back to pinned host memory
+    h_in = tuple(x.cpu().pin_memory() for x in (w.k_new, w.v_new, w.q, w.tables, w.start_pos))
+    h2d = sum(x.numel() * x.element_size() for x in h_in)
+    d2h = q.numel() * q.element_size()
+
+    def call(views, o):
+        dk, dv, dq, dtab, dstart = views
+        P.paged_kv_write(dk, dv, kp, vp, dtab, dstart, dev_status=status)
+        P.paged_prefill_attention(dq, kp, vp, dtab, dstart, w.softmax_scale, out=o, dev_status=status)
+
+    e2e_run, cs, osm = pipelined_e2e(h_in, q, call, device, stream)
+    e2e_steps = args.e2e_steps or max(10, min(K, 200))
+    e2e_run(3)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    cs.wait_event(e0)
+    osm.wait_event(e0)
+    e2e_run(e2e_steps)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    e2e_ms = max_over_ranks([e0.elapsed_time(e1) / e2e_steps], device)[0]
+    line = {"metric": PREFILL_METRIC, "value": round(world * flops / (ms * 1e-3) / 1e12, 2),
             "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "n_seqs": w.n_seqs, "chunk": w.n_new,
@@ -410,7 +546,12 @@ def run_prefill_bench(args, P, w, device, rank, world):
                          "traffic": ncu_traffic("prefill", 3),
                          "flops_per_launch": flops, "avg_launch_ms": round(pre_ms, 5),
                          "peak_source": f"{kind} bf16_tflops (burst)"},
+            "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5),
+                    "steps": e2e_steps},
             "gpu_launches": 2 * K, "clocks": clk.summary()}
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_prefill()
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -649,6 +790,61 @@ def run_layers_bench(args, P, device):
     print(json.dumps(line), flush=True)
 
 
+def pipelined_e2e(ins, out_like, call, device, stream):
+    """End-to-end steps through the public API: the step's inputs sit in one
+    pinned host arena and are copied with one H2D per step into one of two
+    device arenas (views feed call(views, out)); the output goes back to one
+    of two pinned host buffers.  Input copies and output copies each run on
+    their own stream, so step i + 1's inputs land while step i computes and
+    step i's output drains while step i + 1 runs; every step still moves its
+    own inputs and output.  Returns (run(n), input stream, output stream);
+    run(n) ends with the caller's stream waiting for the last output."""
+    import torch
+    offs, total = [], 0
+    for t in ins:
+        offs.append(total)
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    h_arena = torch.empty(total, dtype=torch.uint8).pin_memory()
+    for t, o in zip(ins, offs):
+        h_arena[o:o + t.numel() * t.element_size()].copy_(t.contiguous().view(-1).view(torch.uint8))
+    d_arena = [torch.empty(total, dtype=torch.uint8, device=device) for _ in range(2)]
+
+    def views(buf):
+        return [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for t, o in zip(ins, offs)]
+
+    d_views = [views(b) for b in d_arena]
+    d_out = [torch.empty_like(out_like) for _ in range(2)]
+    h_outs = [torch.empty(out_like.shape, dtype=out_like.dtype).pin_memory() for _ in range(2)]
+    copy_stream = torch.cuda.Stream(device=device)     # inputs, host -> device
+    out_stream = torch.cuda.Stream(device=device)      # outputs, device -> host (not behind the next inputs)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_drained = [torch.cuda.Event() for _ in range(2)]
+    ev_out = torch.cuda.Event()
+
+    def run(n):
+        for i in range(n):
+            b = i % 2
+            with torch.cuda.stream(copy_stream):
+                if i >= 2:
+                    copy_stream.wait_event(ev_done[b])     # compute i - 2 no longer reads buffer b
+                d_arena[b].copy_(h_arena, non_blocking=True)
+                ev_in[b].record(copy_stream)
+            stream.wait_event(ev_in[b])
+            if i >= 2:
+                stream.wait_event(ev_drained[b])           # output i - 2 has left d_out[b]
+            call(d_views[b], d_out[b])
+            ev_done[b].record(stream)
+            with torch.cuda.stream(out_stream):
+                out_stream.wait_event(ev_done[b])
+                h_outs[b].copy_(d_out[b], non_blocking=True)
+                ev_drained[b].record(out_stream)
+        ev_out.record(out_stream)
+        stream.wait_event(ev_out)                          # the last output has reached the host
+
+    return run, copy_stream, out_stream
+
+
 def main():
     args = parse_args()
     rank = int(os.environ.get("RANK", "0"))
@@ -745,56 +941,13 @@ def main():
     h2d = sum(x.numel() * x.element_size() for x in (h_k, h_v, h_q, h_tab, h_start, h_ctx))
     d2h = h_out.numel() * h_out.element_size()
 
-    # The step's inputs sit in one pinned host arena and are copied with one
-    # H2D per step into one of two device arenas (views feed the call); copies
-    # run on their own stream, so step i + 1's inputs land while step i
-    # computes and step i's output drains while step i + 1 runs.  Every step
-    # still moves its own inputs and output inside the timed region.
-    ins = (h_k, h_v, h_q, h_tab, h_start, h_ctx)
-    offs, total = [], 0
-    for t in ins:
-        offs.append(total)
-        total += (t.numel() * t.element_size() + 255) // 256 * 256
-    h_arena = torch.empty(total, dtype=torch.uint8).pin_memory()
-    for t, o in zip(ins, offs):
-        h_arena[o:o + t.numel() * t.element_size()].copy_(t.contiguous().view(-1).view(torch.uint8))
-    d_arena = [torch.empty(total, dtype=torch.uint8, device=device) for _ in range(2)]
+    def call(views, out):
+        dk, dv, dq, dtab, dstart, dctx = views
+        P.paged_decode_step(dk, dv, dstart, dq, kp, vp, dtab, dctx, w.softmax_scale, k_scales=ks,
+                            v_scales=vs, split_tokens=split, out=out, workspace=ws, dev_status=status)
 
-    def views(buf):
-        return [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape) for t, o in zip(ins, offs)]
-
-    d_views = [views(b) for b in d_arena]
-    d_out = [torch.empty_like(q) for _ in range(2)]
-    h_outs = [torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(2)]
-    copy_stream = torch.cuda.Stream(device=device)     # inputs, host -> device
-    out_stream = torch.cuda.Stream(device=device)      # outputs, device -> host (not behind the next inputs)
-    ev_in = [torch.cuda.Event() for _ in range(2)]
-    ev_done = [torch.cuda.Event() for _ in range(2)]
-    ev_drained = [torch.cuda.Event() for _ in range(2)]
-    ev_out = torch.cuda.Event()
-
-    def e2e_run(n):
-        for i in range(n):
-            b = i % 2
-            with torch.cuda.stream(copy_stream):
-                if i >= 2:
-                    copy_stream.wait_event(ev_done[b])     # compute i - 2 no longer reads buffer b
-                d_arena[b].copy_(h_arena, non_blocking=True)
-                ev_in[b].record(copy_stream)
-            stream.wait_event(ev_in[b])
-            if i >= 2:
-                stream.wait_event(ev_drained[b])               # output i - 2 has left d_out[b]
-            dk, dv, dq, dtab, dstart, dctx = d_views[b]
-            P.paged_decode_step(dk, dv, dstart, dq, kp, vp, dtab, dctx, w.softmax_scale, k_scales=ks,
-                                v_scales=vs, split_tokens=split, out=d_out[b], workspace=ws, dev_status=status)
-            ev_done[b].record(stream)
-            with torch.cuda.stream(out_stream):
-                out_stream.wait_event(ev_done[b])
-                h_outs[b].copy_(d_out[b], non_blocking=True)
-                ev_drained[b].record(out_stream)
-        ev_out.record(out_stream)
-        stream.wait_event(ev_out)                          # the last output has reached the host
-
+    e2e_run, copy_stream, out_stream = pipelined_e2e((h_k, h_v, h_q, h_tab, h_start, h_ctx), q, call, device,
+                                                     stream)
     e2e_run(3)
     torch.cuda.synchronize()
     if world > 1:
