@@ -32,7 +32,9 @@ __device__ __forceinline__ int64_t pool_row_of(const int32_t *table_row, int32_t
 // Native bf16 write: 16-byte vector i of the [n_seqs * n_new rows][Hkv * D]
 // new K and V rows goes to the same vector of its token's pool row.  Threads
 // take vectors first, first + stride, ...; a bad row is reported once (by the
-// thread holding its first vector) and skipped.
+// thread holding its first vector) and skipped.  The new row is loaded before
+// the table lookup so that its latency overlaps the lookup's two dependent
+// loads (position, then table entry).
 __device__ __forceinline__ void write_bf16_vectors(const WriteArgs &a, int64_t first, int64_t stride)
 {
     const int32_t row_vecs = a.dims.n_kv_heads * a.dims.head_dim / 8;
@@ -45,12 +47,12 @@ __device__ __forceinline__ void write_bf16_vectors(const WriteArgs &a, int64_t f
         const int64_t r = i / row_vecs;
         const int32_t v = (int32_t)(i - r * row_vecs);
         const int64_t s = r / a.n_new;
+        const uint4 kx = __ldcs(k_new + i);
+        const uint4 vx = __ldcs(v_new + i);
         const int64_t t = (int64_t)__ldg(a.start_pos + s) + (r - s * a.n_new);
         const int64_t row = pool_row_of(a.tables + s * a.max_blocks, a.max_blocks, a.dims.n_blocks,
                                         a.dims.block_size, t, v == 0 ? a.dev_status : nullptr);
         if (row < 0) continue;
-        const uint4 kx = __ldcs(k_new + i);
-        const uint4 vx = __ldcs(v_new + i);
         k_pool[row * row_vecs + v] = kx;
         v_pool[row * row_vecs + v] = vx;
     }
