@@ -70,8 +70,8 @@ def run_streamed(P, sp, q, hk, hv, pools, tables, lens, scale):
     pool_k, pool_v = pools
     lse = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
-    out = P.paged_decode_streamed(q, hk, hv, pool_k, pool_v, sp, torch.tensor(tables, dtype=torch.int32),
-                                  torch.tensor(lens, dtype=torch.int32), scale, lse_out=lse, dev_status=st)
+    out = P.paged_decode_streamed(q, hk, hv, pool_k, pool_v, sp, torch.as_tensor(tables, dtype=torch.int32),
+                                  torch.as_tensor(lens, dtype=torch.int32), scale, lse_out=lse, dev_status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     return out, lse, (pool_k, pool_v)
@@ -147,3 +147,26 @@ def test_residency_carries_over_and_invalidation_restages(P):
     mx, mean = attention_errors(out2, ref)
     assert mx <= BF16_MAX and mean <= BF16_MEAN, (mx, mean)
     assert not torch.equal(out1, out2)
+
+
+def test_config1_batch_streamed_in_the_benchmarked_shape(P):
+    """The config 1 batch (8,296 blocks) from a host tier holding the oracle's
+    pools, through the 2048-slot scratch pool bench.py --stream 2048 times:
+    every output against the oracle's decode over the whole context."""
+    from oracle_pools import dims_of, oracle_pools_after_step
+    from gpu_support import NTHREADS
+    from paged_kv_cache_212_gb300 import workloads as W
+    w = W.config1()
+    kp, vp, _, _ = oracle_pools_after_step(w, poison=True)
+    code, ref, ref_lse = oracle.decode(w.q, kp, vp, dims_of(w), w.tables, w.ctx_lens, w.softmax_scale,
+                                       n_threads=NTHREADS)
+    assert code == 0
+    hk = torch.from_numpy(kp.view(np.int16)).view(torch.bfloat16).pin_memory()
+    hv = torch.from_numpy(vp.view(np.int16)).view(torch.bfloat16).pin_memory()
+    sp = P.ScratchPool(2048, w.n_seqs)
+    pools = scratch(hk, 2048)
+    q = w.q.cuda()
+    out, lse, _ = run_streamed(P, sp, q, hk, hv, pools, w.tables, w.ctx_lens, w.softmax_scale)
+    mx, mean = attention_errors(out, ref)
+    assert mx <= BF16_MAX and mean <= BF16_MEAN, (mx, mean)
+    assert np.abs(lse.cpu().numpy() - ref_lse).max() <= LSE_TOL
