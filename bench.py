@@ -711,6 +711,66 @@ def run_stream_bench(args, P, device):
     print(json.dumps(line), flush=True)
 
 
+def run_small_bench(args, P, w, device):
+    """Config 0 (4 sequences, all data in L2): the decode step (write + decode)
+    timed call by call with CUDA events, median of the reps, once with the
+    data warm in L2 and once with a buffer of twice the L2 size rewritten
+    between reps outside the timed pair (flushed)."""
+    import torch
+    kp, vp, ks, vs = fill_pool(P, w, device)
+    tables, start, ctx = w.tables.to(device), w.start_pos.to(device), w.ctx_lens.to(device)
+    k_new, v_new, q = w.k_new.to(device), w.v_new.to(device), w.q.to(device)
+    out = torch.empty_like(q)
+    ws = torch.empty(P.decode_workspace_bytes(w.n_seqs, w.n_q_heads, w.head_dim, int(w.ctx_lens.sum())),
+                     dtype=torch.uint8, device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream()
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1, dtype=torch.float32, device=device)
+
+    def step():
+        P.paged_decode_step(k_new, v_new, start, q, kp, vp, tables, ctx, w.softmax_scale, out=out, workspace=ws,
+                            dev_status=status)
+
+    reps = max(50, min(args.steps, 2000))
+    warm_n = max(5, args.warmup)
+
+    def median_us(flushed):
+        for _ in range(warm_n):
+            step()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        for a, b in evs:
+            if flushed:
+                flush.fill_(1.0)
+            # a short GPU wait before each timed pair lets the host enqueue the
+            # step ahead of the GPU, so the pair times the GPU, not the launches
+            torch.cuda._sleep(100_000)
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize()
+        t = sorted(a.elapsed_time(b) * 1e3 for a, b in evs)
+        return {"median_us": round(t[len(t) // 2], 3), "p10_us": round(t[len(t) // 10], 3),
+                "p90_us": round(t[(9 * len(t)) // 10], 3)}
+
+    uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    with ClockSampler(uuid) as clk:
+        time.sleep(0.25)
+        warm = median_us(False)
+        cold = median_us(True)
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    decode_b, write_b = algorithmic_bytes(w)
+    us = cold["median_us"]
+    print(json.dumps({
+        "metric": METRIC, "value": round((decode_b + write_b) / (us * 1e-6) / 1e9, 3), "unit": "GB/s",
+        "n_gpus": 1, "steps": reps, "warmup": warm_n, "ms_per_step": round(us * 1e-3, 5), "higher_is_better": True,
+        "scaling": "none", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": dict(bench_config(w, args), l2=f"data fits in L2: value from the flushed median ({2 * l2 >> 20} "
+                                                  "MiB rewritten between reps)"),
+        "seq_steps_per_s_per_layer": round(w.n_seqs / (us * 1e-6), 1),
+        "warm_l2": warm, "flushed_l2": cold, "gpu_launches": 3 * reps * 2, "clocks": clk.summary()}), flush=True)
+
+
 def run_layers_bench(args, P, device):
     """An args.layers-layer decode step of config 0 or 1 (int8 pools for config
     2): per layer the page write of the step's new rows and the paged decode
@@ -878,6 +938,12 @@ def main():
             run_layers_bench(args, P, device)
         return
     w = make_workload(args.config, device)  # every rank owns an independent replica batch
+    if args.config == 0:
+        if rank == 0:
+            run_small_bench(args, P, w, device)
+        if world > 1:
+            dist.destroy_process_group()
+        return
     if args.config == 3:
         run_prefill_bench(args, P, w, device, rank, world)
         if world > 1:
