@@ -69,7 +69,10 @@ int pkv_sp_plan_tile(pkv_scratch_pool *sp, const int32_t *host_tables, int32_t m
  * slot in [0, pool_dims.n_blocks]); host_k / host_v pinned host memory
  * [n_host_blocks][block_size][n_kv_heads][head_dim] bf16; pool_k / pool_v
  * device [pool_dims.n_blocks + 1][...] bf16.  Destination slots must be
- * distinct.  Out-of-range ids are skipped (PKV_DEV_BAD_BLOCK_ID).
+ * distinct.  Out-of-range ids are skipped (PKV_DEV_BAD_BLOCK_ID).  Returns
+ * PKV_ERR_INVALID_ARG for a negative count or size, a null or misaligned
+ * pointer (pairs 8-byte, the rest 16-byte aligned) or host memory that is not
+ * pinned and mapped; PKV_ERR_UNSUPPORTED for head_dim outside {64, 128}.
  */
 int paged_kv_stage_blocks(const int32_t *pairs, int32_t n_pairs, const pkv_bf16 *host_k, const pkv_bf16 *host_v,
                           int32_t n_host_blocks, pkv_bf16 *pool_k, pkv_bf16 *pool_v, pkv_dims pool_dims,

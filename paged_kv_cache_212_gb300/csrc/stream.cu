@@ -353,8 +353,9 @@ int paged_kv_stage_blocks(const int32_t *pairs, int32_t n_pairs, const pkv_bf16 
                           int32_t *dev_status, pkv_stream_t stream)
 {
     if (n_pairs < 0 || n_host_blocks < 0 || pool_dims.n_blocks < 0 || pool_dims.block_size <= 0 ||
-        pool_dims.n_kv_heads <= 0 || (pool_dims.head_dim != 64 && pool_dims.head_dim != 128))
+        pool_dims.n_kv_heads <= 0)
         return PKV_ERR_INVALID_ARG;
+    if (pool_dims.head_dim != 64 && pool_dims.head_dim != 128) return PKV_ERR_UNSUPPORTED;
     if (n_pairs == 0) return PKV_OK;
     if (!pairs || !host_k || !host_v || !pool_k || !pool_v || (reinterpret_cast<uintptr_t>(pairs) & 7) != 0 ||
         (reinterpret_cast<uintptr_t>(pool_k) & 15) != 0 || (reinterpret_cast<uintptr_t>(pool_v) & 15) != 0 ||
@@ -397,6 +398,7 @@ int paged_decode_streamed(const pkv_bf16 *q, int32_t n_q_heads, const pkv_bf16 *
     if (n_seqs == 0) return PKV_OK;
     if (pool_dims.n_blocks != sp->n_slots || n_seqs > sp->max_seqs) return PKV_ERR_INVALID_ARG;
     if (!q || !out || !host_tables || !ctx_lens || !workspace) return PKV_ERR_INVALID_ARG;
+    if (!(softmax_scale > 0.f) || !isfinite(softmax_scale)) return PKV_ERR_INVALID_ARG;   // as the decode itself
     const int32_t D = pool_dims.head_dim, bs = pool_dims.block_size, n_slots = sp->n_slots;
     if (D != 64 && D != 128) return PKV_ERR_UNSUPPORTED;
     for (int64_t i = 0; i < (int64_t)n_seqs; ++i) {

@@ -69,3 +69,53 @@ def test_planner_rejects_a_negative_host_id_without_changing_state(P):
     assert lib.lookup(3) == -1
     tt, tl, pairs, done = lib.plan_tile(tab, torch.tensor([16], dtype=torch.int32), 16, [0, 0])
     assert pairs == [(3, 0)] and tt.tolist() == [[0, 4]] and done
+
+
+def test_streamed_decode_host_checks(P):
+    """paged_decode_streamed returns its host-checkable errors before any CUDA
+    call (device pointers here are placeholders that are never dereferenced)."""
+    import ctypes
+    lib = P.load_library()
+    sp = P.ScratchPool(4, 2)
+    fake = ctypes.c_void_p(0x1000)
+    d = P.Dims(4, 16, 2, 64)                     # the scratch pool: n_blocks = n_slots = 4
+    tables = (ctypes.c_int32 * 4)(0, 1, 2, 3)    # [2 sequences][2 blocks]
+    lens = (ctypes.c_int32 * 2)(20, 32)
+    need = P.streamed_workspace_bytes(2, 8, 64, 4, 16)
+
+    def call(**kw):
+        return lib.paged_decode_streamed(
+            kw.get("q", fake), 8, fake, fake, kw.get("n_host", 10), fake, fake, kw.get("dims", d),
+            kw.get("sp", sp._h), kw.get("tables", tables), 2, kw.get("lens", lens), kw.get("n", 2),
+            kw.get("scale", 0.125), fake, None, fake, kw.get("wsb", need), None, None)
+
+    assert call(n=0) == 0
+    assert call(sp=None) == 1
+    assert call(dims=P.Dims(5, 16, 2, 64)) == 1            # pool size is not the scratch pool's
+    assert call(n=3) == 1                                    # more sequences than the pool plans for
+    assert call(q=None) == 1
+    for sc in (0.0, -1.0, float("nan"), float("inf")):
+        assert call(scale=sc) == 1
+    assert call(dims=P.Dims(4, 16, 2, 96)) == 2              # head_dim
+    assert call(lens=(ctypes.c_int32 * 2)(20, 33)) == 3      # past the table (2 blocks of 16)
+    assert call(n_host=3) == 3                               # host id 3 outside a 3-block tier
+    assert call(wsb=need - 1) == 4
+    assert need > 0
+
+
+def test_stage_blocks_host_checks(P):
+    import ctypes
+    lib = P.load_library()
+    fake, odd = ctypes.c_void_p(0x1000), ctypes.c_void_p(0x1004)
+    d = P.Dims(4, 16, 2, 64)
+
+    def call(**kw):
+        return lib.paged_kv_stage_blocks(kw.get("pairs", fake), kw.get("n", 3), kw.get("hk", fake), fake, 10,
+                                         fake, fake, kw.get("dims", d), None, None)
+
+    assert call(n=0) == 0
+    assert call(n=-1) == 1
+    assert call(pairs=None) == 1
+    assert call(pairs=odd) == 1                          # pairs are read as 8-byte int2
+    assert call(hk=ctypes.c_void_p(0x1008)) == 1         # 16-byte vectors
+    assert call(dims=P.Dims(4, 16, 2, 96)) == 2
