@@ -929,13 +929,11 @@ def main():
     import paged_kv_cache_212_gb300 as P
     P.load_library()
 
-    if args.stream:
+    if args.stream or args.layers:
         if rank == 0:
-            run_stream_bench(args, P, device)
-        return
-    if args.layers:
-        if rank == 0:
-            run_layers_bench(args, P, device)
+            (run_stream_bench if args.stream else run_layers_bench)(args, P, device)
+        if world > 1:
+            dist.destroy_process_group()
         return
     w = make_workload(args.config, device)  # every rank owns an independent replica batch
     if args.config == 0:

@@ -7,9 +7,12 @@
  * --------------------------------
  *  - Every pointer argument is a caller-owned DEVICE pointer (allocated by the
  *    caller, e.g. through PyTorch) unless stated otherwise, 16-byte aligned.
- *    The library never allocates, frees or synchronises; work is enqueued on
- *    `stream` (the last argument; NULL = the legacy default stream) and the
- *    call returns as soon as it is enqueued.
+ *    The calls of this header never allocate, free or synchronise; work is
+ *    enqueued on `stream` (the last argument; NULL = the legacy default
+ *    stream) and the call returns as soon as it is enqueued.  (The host-side
+ *    block manager of pagedkv_blocks.h and the scratch pool of
+ *    pagedkv_stream.h own host memory, and the latter a copy stream and
+ *    events; their headers say so.)
  *  - Every call returns a PKV_* status.  Host-checkable argument errors are
  *    reported before anything is enqueued.  Errors that depend on device data
  *    (a table id outside [0, n_blocks], a position outside the table, a
