@@ -1,10 +1,13 @@
 // api.cu -- the extern "C" entry points of libpagedkv.so: argument checks on
 // the host, then kernel launches on the caller's stream.  No allocation, no
 // synchronisation, no exception crosses the ABI.
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
 #include "launch.h"
+#include "decode_small.h"
 
 namespace pkv {
 
@@ -228,6 +231,17 @@ size_t pkv_decode_workspace_bytes(int32_t n_seqs, int32_t n_q_heads, int32_t hea
                                   (int64_t)decode_capacity_for(n_seqs, max_total_ctx_tokens, split_tokens));
 }
 
+// Small batches (one wave of (sequence, kv head) units, short contexts, bf16
+// pages, automatic splitting) take the one-launch path of decode_small.cu;
+// PKV_DECODE_IMPL=split in the environment keeps every call on the split-KV
+// path (for comparisons).
+static bool use_small_decode(const DecodeArgs &a, int sms)
+{
+    const char *impl = getenv("PKV_DECODE_IMPL");
+    if (impl && strcmp(impl, "split") == 0) return false;
+    return decode_small_eligible(a, sms);
+}
+
 // Host checks of a decode call; on success fills *a (workspace carved).
 static int prepare_decode(const pkv_bf16 *q, int32_t n_q_heads, const void *k_pool, const void *v_pool,
                           const float *k_scales, const float *v_scales, int32_t kv_dtype, const pkv_dims &dims,
@@ -288,6 +302,7 @@ int paged_decode_attention(const pkv_bf16 *q, int32_t n_q_heads, const void *k_p
     int sms = 0;
     st = num_sms_of_current_device(&sms);
     if (st != PKV_OK) return st;
+    if (use_small_decode(a, sms)) return cuda_status(launch_decode_small(a, nullptr, (cudaStream_t)stream));
     return cuda_status(launch_decode(a, sms, (cudaStream_t)stream));
 }
 
@@ -312,6 +327,7 @@ int paged_decode_step(const pkv_bf16 *k_new, const pkv_bf16 *v_new, const int32_
     int sms = 0;
     st = num_sms_of_current_device(&sms);
     if (st != PKV_OK) return st;
+    if (use_small_decode(a, sms)) return cuda_status(launch_decode_small(a, &w, (cudaStream_t)stream));
     return cuda_status(launch_decode(a, sms, (cudaStream_t)stream, &w));
 }
 

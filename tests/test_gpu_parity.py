@@ -46,6 +46,10 @@ def workload(name):
             "ragged_d64": lambda: W.decode_workload("ragged", 5, [1, 15, 16, 17, 31, 33, 200, 511], 16, 4, 64, 16),
             "ragged_g8_bs32": lambda: W.decode_workload("g8", 6, [1, 31, 32, 33, 100, 700, 1500], 64, 8, 128, 32),
             "ragged_g1": lambda: W.decode_workload("g1", 7, [3, 40, 129], 4, 4, 128, 16),
+            # at the one-launch path's limits (the context in shared memory): 512 tokens at
+            # head_dim 64 (block size 32), 256 at head_dim 128; G = 8
+            "small_limits": lambda: W.decode_workload("sl", 15, [0, 1, 511, 300, 511], 64, 8, 64, 32),
+            "small_limits_d128": lambda: W.decode_workload("sl128", 16, [255, 0, 100, 17, 255], 64, 8, 128, 16),
             "int8_small": lambda: W.decode_workload("i8", 8, [0, 1, 15, 16, 100, 333], 16, 4, 128, 16, n_new=3,
                                                     kv_format="int8"),
             "int8_d64": lambda: W.decode_workload("i8d64", 9, [5, 77, 300], 8, 4, 64, 32, n_new=2,
@@ -202,8 +206,21 @@ def check_lse(lse_gpu, lse_ref):
         assert np.abs(g[fin] - lse_ref[fin]).max() <= LSE_TOL
 
 
-@pytest.mark.parametrize("name", ["cfg0", "cfg1", "cfg4", "ragged_d64", "ragged_g8_bs32", "ragged_g1"])
-def test_decode_bf16_parity(P, name):
+@pytest.fixture(params=["auto", "split"])
+def decode_impl(request, monkeypatch):
+    """auto: small batches take the one-launch path (one CTA per (sequence,
+    kv head)), larger ones the split-KV path; split: every call takes the
+    split-KV path."""
+    if request.param == "split":
+        monkeypatch.setenv("PKV_DECODE_IMPL", "split")
+    else:
+        monkeypatch.delenv("PKV_DECODE_IMPL", raising=False)
+    return request.param
+
+
+@pytest.mark.parametrize("name", ["cfg0", "cfg1", "cfg4", "ragged_d64", "ragged_g8_bs32", "ragged_g1", "small_limits",
+                                  "small_limits_d128"])
+def test_decode_bf16_parity(P, name, decode_impl):
     w = workload(name)
     kp, vp, _, _ = pools(name)
     out, lse, st = run_decode(P, w, kp, vp)
@@ -238,8 +255,8 @@ def test_decode_split_sizes(P, split):
     check_lse(lse, ref_lse)
 
 
-@pytest.mark.parametrize("name", ["cfg1", "int8_small"])
-def test_decode_identity_vs_permuted_tables_bit_exact(P, name):
+@pytest.mark.parametrize("name", ["cfg1", "int8_small", "ragged_d64"])
+def test_decode_identity_vs_permuted_tables_bit_exact(P, name, decode_impl):
     """Results do not depend on which physical pages the table names."""
     w = workload(name)
     kp, vp, ks, vs = pools(name)
@@ -258,7 +275,7 @@ def test_decode_identity_vs_permuted_tables_bit_exact(P, name):
     assert torch.equal(lse, lse2)
 
 
-def test_decode_edge_lengths(P):
+def test_decode_edge_lengths(P, decode_impl):
     w = workload("ragged_d64")
     kp, vp, _, _ = pools("ragged_d64")
     ctx = w.ctx_lens.clone()
@@ -274,7 +291,7 @@ def test_decode_edge_lengths(P):
     check_lse(lse, ref_lse)
 
 
-def test_decode_bad_table_and_length_are_flagged(P):
+def test_decode_bad_table_and_length_are_flagged(P, decode_impl):
     w = workload("ragged_d64")
     kp, vp, _, _ = pools("ragged_d64")
     tables = w.tables.clone()
@@ -404,7 +421,7 @@ def test_prefill_identity_vs_permuted_tables_bit_exact(P):
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("name", ["cfg0", "cfg1", "cfg2", "ragged_d64", "int8_small"])
-def test_fused_decode_step(P, name):
+def test_fused_decode_step(P, name, decode_impl):
     """paged_decode_step = paged_kv_write(_int8) then paged_decode_attention:
     the pool bit-exact with the oracle's write, the output identical bit for
     bit to the two-call path and within tolerance of the oracle."""
