@@ -199,6 +199,11 @@ size_t pkv_decode_workspace_bytes(int32_t n_seqs, int32_t n_q_heads, int32_t hea
  * and lse = -inf.  workspace: device memory of at least
  * pkv_decode_workspace_bytes(...) bytes, contents need not be initialised,
  * and it must not be shared by concurrently running calls.
+ * With split_tokens = 0 and bf16 pages, a batch of at most one (sequence,
+ * kv head) pair per SM whose table spans at most 256 tokens (head_dim 128) or
+ * 512 (head_dim 64) is attended whole by one CTA per pair in a single launch
+ * (same results within the tolerances; PKV_DECODE_IMPL=split in the
+ * environment keeps the split-KV path).
  */
 int paged_decode_attention(const pkv_bf16 *q, int32_t n_q_heads, const void *k_pool,
                            const void *v_pool, const float *k_scales, const float *v_scales,
