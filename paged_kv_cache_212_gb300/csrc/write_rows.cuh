@@ -104,15 +104,36 @@ __device__ __forceinline__ void write_int8_units(const WriteArgs &a, float *k_sc
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
         const float scale = __fdiv_rn(amax, 127.0f);
+        // code = rint(fl(x / scale)) without a division per element: with the
+        // correctly rounded reciprocal rcp = fl(1 / scale) (scale normal), the
+        // product q = fl(x * rcp) is within |x / scale| * (2^-23 + 2^-48) <= 1.53e-5
+        // of x / scale (|x / scale| < 128), and fl(x / scale) within half an ulp
+        // (<= 3.8e-6) of it; so when q is farther than 3e-5 from every
+        // half-integer, q and fl(x / scale) round to the same integer.  The
+        // rare q closer than that (a tie or a near-tie) takes the division.
+        const bool fast = scale >= 1.17549435e-38f;            // normal: rcp is finite and within 2^-24
+        const float rcp = fast ? __frcp_rn(scale) : 0.0f;
+        int c[EPL];
+        bool need_div = false;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) {
+            const float q = __fmul_rn(x[e], rcp);
+            const float frac = q - floorf(q);                   // exact for |q| < 2^23
+            c[e] = __float2int_rn(q);
+            need_div |= !(fast && fabsf(frac - 0.5f) > 3.0e-5f);
+        }
+        if (__any_sync(0xffffffffu, need_div && amax != 0.0f)) {    // rare: a (near-)tie in the warp's row
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) {
+                const float q = __fmul_rn(x[e], rcp);
+                if (!(fast && fabsf(q - floorf(q) - 0.5f) > 3.0e-5f)) c[e] = __float2int_rn(__fdiv_rn(x[e], scale));
+            }
+        }
         uint32_t packed = 0;
 #pragma unroll
         for (int e = 0; e < EPL; ++e) {
-            int c = 0;
-            if (amax != 0.0f) {
-                c = __float2int_rn(__fdiv_rn(x[e], scale));
-                c = max(-127, min(127, c));
-            }
-            packed |= (uint32_t)(c & 0xff) << (8 * e);
+            const int ce = amax != 0.0f ? max(-127, min(127, c[e])) : 0;
+            packed |= (uint32_t)(ce & 0xff) << (8 * e);
         }
         int8_t *dst = static_cast<int8_t *>(which ? a.v_pool : a.k_pool) + (row * hkv + h) * D + lane * EPL;
         if constexpr (EPL == 4)

@@ -462,3 +462,49 @@ def test_fused_decode_step(P, name, decode_impl):
         assert mx <= INT8_MAX, mx
     else:
         assert mx <= BF16_MAX and mean <= BF16_MEAN, (mx, mean)
+
+
+def test_int8_write_near_ties_bit_exact(P):
+    """Rows whose codes sit at or next to a half-integer quotient -- where a
+    reciprocal multiply and the IEEE division by the stored scale can round
+    differently -- are quantised exactly as the oracle's division says."""
+    u = np.arange(0x3e00, 0x4100, dtype=np.uint32)
+    vals = (u << 16).view(np.float32)
+    rows = []
+    for amax in vals:
+        scale = np.float32(amax) / np.float32(127)
+        rcp = np.float32(1) / scale
+        xs = vals[vals <= amax]
+        q = xs * rcp
+        near = np.abs(q - np.floor(q) - np.float32(0.5)) <= np.float32(1e-4)
+        picked = xs[near][:63]
+        if len(picked):
+            row = np.zeros(128, np.float32)
+            row[0] = amax
+            row[1:1 + len(picked)] = picked
+            row[64:64 + len(picked)] = -picked
+            rows.append(row)
+    assert len(rows) >= 64
+    Hkv, D, bs = 4, 128, 16
+    n_tok = -(-len(rows) // Hkv)
+    data = np.zeros((n_tok * Hkv, D), np.float32)
+    data[:len(rows)] = np.stack(rows)
+    new = torch.from_numpy(data.reshape(1, n_tok, Hkv, D)).to(torch.bfloat16)
+    kn = new.view(torch.int16).numpy().view(np.uint16)
+    vn = (-new).view(torch.int16).numpy().view(np.uint16)
+    nb = -(-n_tok // bs)
+    d = oracle.Dims(nb, bs, Hkv, D)
+    tables = np.arange(nb, dtype=np.int32)[None]
+    start = np.zeros(1, np.int32)
+    okp, ovp = np.zeros(d.pool_shape, np.int8), np.zeros(d.pool_shape, np.int8)
+    oks, ovs = np.zeros(d.scale_shape, np.float32), np.zeros(d.scale_shape, np.float32)
+    assert oracle.write_int8(kn, vn, okp, ovp, oks, ovs, d, tables, start) == oracle.OK
+    gk, gv = dev(okp * 0), dev(ovp * 0)
+    gks, gvs = dev(oks * 0), dev(ovs * 0)
+    st = status_tensor()
+    P.paged_kv_write_int8(dev(kn), dev(vn), gk, gv, gks, gvs, i32(tables), i32(start), dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    assert np.array_equal(host(gk), okp) and np.array_equal(host(gv), ovp)
+    assert np.array_equal(host(gks).view(np.uint32), oks.view(np.uint32))
+    assert np.array_equal(host(gvs).view(np.uint32), ovs.view(np.uint32))
