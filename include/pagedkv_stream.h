@@ -104,7 +104,10 @@ size_t pkv_streamed_workspace_bytes(int32_t n_seqs, int32_t n_q_heads, int32_t h
  * when stream reaches the end of the call).  The call returns once every tile
  * is enqueued (it waits on the host only until the plan of the tile two
  * before has been copied).  The scratch pool and workspace must not be used by
- * other work meanwhile.
+ * other work meanwhile.  An error return after the first tile was planned
+ * (PKV_ERR_CUDA) leaves the residency bookkeeping ahead of what reached the
+ * device: destroy the scratch pool (or invalidate every block) before
+ * reusing it.
  */
 int paged_decode_streamed(const pkv_bf16 *q, int32_t n_q_heads, const pkv_bf16 *host_k, const pkv_bf16 *host_v,
                           int32_t n_host_blocks, pkv_bf16 *pool_k, pkv_bf16 *pool_v, pkv_dims pool_dims,

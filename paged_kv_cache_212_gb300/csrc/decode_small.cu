@@ -10,8 +10,6 @@
 // (visible to the block after a barrier); no CTA depends on another.
 #include <math.h>
 
-#include <mutex>
-
 #include "common.cuh"
 #include "decode_small.h"
 
@@ -271,20 +269,17 @@ cudaError_t launch_decode_small(const DecodeArgs &a, const WriteArgs *write, cud
     const unsigned grid = (unsigned)(a.n_seqs * a.dims.n_kv_heads);
     const WriteArgs w = write ? *write : WriteArgs{};
     const int cap = a.max_blocks * a.dims.block_size;      // tokens the buffers hold
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [] {
-        attr_err = cudaFuncSetAttribute(decode_small_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        (int)small_smem_bytes<128>(kSmallKVBytes / (4 * 128)));
-        if (attr_err == cudaSuccess)
-            attr_err = cudaFuncSetAttribute(decode_small_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                            (int)small_smem_bytes<64>(kSmallKVBytes / (4 * 64)));
-    });
+    // per call, as the other kernels: the attribute belongs to the current device
+    const size_t smem = a.dims.head_dim == 128 ? small_smem_bytes<128>(cap) : small_smem_bytes<64>(cap);
+    const cudaError_t attr_err =
+        a.dims.head_dim == 128
+            ? cudaFuncSetAttribute(decode_small_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
+            : cudaFuncSetAttribute(decode_small_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (attr_err != cudaSuccess) return attr_err;
     if (a.dims.head_dim == 128)
-        decode_small_kernel<128><<<grid, kThreads, small_smem_bytes<128>(cap), stream>>>(a, w, write ? 1 : 0, cap);
+        decode_small_kernel<128><<<grid, kThreads, smem, stream>>>(a, w, write ? 1 : 0, cap);
     else
-        decode_small_kernel<64><<<grid, kThreads, small_smem_bytes<64>(cap), stream>>>(a, w, write ? 1 : 0, cap);
+        decode_small_kernel<64><<<grid, kThreads, smem, stream>>>(a, w, write ? 1 : 0, cap);
     return cudaGetLastError();
 }
 
