@@ -367,13 +367,16 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(const __grid_constan
             auto wait_k = [&](int j) { return mbar_wait(&k_full[j % NK], (j / NK) & 1, abort_flag); };
             auto wait_v = [&](int j) { return mbar_wait(&v_full[j % NV], (j / NV) & 1, abort_flag); };
             // S_tj = Q_t K_j^T, then the commit that hands S_tj to warpgroup t
+            // Descriptors of a tile are built once and stepped by constants: the
+            // start-address field is addr / 16 (14 bits, shared addresses < 256 KiB),
+            // so desc(addr + off) = desc(addr) + off / 16 for 16-byte multiples off.
             auto issue_s = [&](int t, int j) {
-                const uint32_t k_addr = smem_u32(k_ring + (j % NK) * kSlotBytes), q_addr = smem_u32(q_s + t * kQTile);
+                const uint64_t q_desc = umma_desc_sw128(smem_u32(q_s + t * kQTile), 16, 1024);
+                const uint64_t k_desc = umma_desc_sw128(smem_u32(k_ring + (j % NK) * kSlotBytes), 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    umma_bf16(tmem + t * kTileCols, umma_desc_sw128(q_addr + (kk / 4) * kQPanel + (kk % 4) * 32, 16, 1024),
-                              umma_desc_sw128(k_addr + (kk / 4) * kKVPanel + (kk % 4) * 32, 16, 1024), idesc_s,
-                              kk > 0);
+                    umma_bf16(tmem + t * kTileCols, q_desc + (uint64_t)(((kk / 4) * kQPanel + (kk % 4) * 32) >> 4),
+                              k_desc + (uint64_t)(((kk / 4) * kKVPanel + (kk % 4) * 32) >> 4), idesc_s, kk > 0);
                 umma_commit(&s_full[t]);
             };
             ok = mbar_wait(q_full, 0, abort_flag) && wait_k(0);
@@ -385,7 +388,7 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(const __grid_constan
             for (int j = 0; ok && j < n_kt; ++j) {
                 ok = wait_v(j);
                 if (!ok) break;
-                const uint32_t v_addr = smem_u32(v_ring + (j % NV) * kSlotBytes);
+                const uint64_t v_desc = umma_desc_sw128(smem_u32(v_ring + (j % NV) * kSlotBytes), 2048, 1024);
                 for (int t = 0; t < kNQ && ok; ++t) {
                     ok = mbar_wait(&p_full[t], j & 1, abort_flag);
                     if (!ok) break;
@@ -396,8 +399,7 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(const __grid_constan
 #pragma unroll
                     for (int kk = 0; kk < kTN / 16; ++kk)
                         umma_bf16_ts(tmem + t * kTileCols + kOCol, tmem + t * kTileCols + kk * 8,
-                                     umma_desc_sw128(v_addr + kk * kVGroup, 2048, 1024), idesc_o,
-                                     (j > 0 || kk > 0) ? 1u : 0u);
+                                     v_desc + (uint64_t)((kk * kVGroup) >> 4), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
                     if (j + 1 < n_kt) {
                         if (t == 0) {
                             ok = wait_k(j + 1);
