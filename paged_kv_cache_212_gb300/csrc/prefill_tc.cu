@@ -109,6 +109,16 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
         : "memory");
 }
 
+// desc + off / 16 on the low word only: the start-address field never carries
+// out (shared addresses < 256 KiB), so the high word stays as it is.
+__device__ __forceinline__ uint64_t desc_step(uint64_t desc, uint32_t off_bytes)
+{
+    const uint32_t lo = (uint32_t)desc + (off_bytes >> 4), hi = (uint32_t)(desc >> 32);
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+
 __device__ __forceinline__ void umma_commit(uint64_t *bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -375,8 +385,8 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(const __grid_constan
                 const uint64_t k_desc = umma_desc_sw128(smem_u32(k_ring + (j % NK) * kSlotBytes), 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk)
-                    umma_bf16(tmem + t * kTileCols, q_desc + (uint64_t)(((kk / 4) * kQPanel + (kk % 4) * 32) >> 4),
-                              k_desc + (uint64_t)(((kk / 4) * kKVPanel + (kk % 4) * 32) >> 4), idesc_s, kk > 0);
+                    umma_bf16(tmem + t * kTileCols, desc_step(q_desc, (kk / 4) * kQPanel + (kk % 4) * 32),
+                              desc_step(k_desc, (kk / 4) * kKVPanel + (kk % 4) * 32), idesc_s, kk > 0);
                 umma_commit(&s_full[t]);
             };
             ok = mbar_wait(q_full, 0, abort_flag) && wait_k(0);
@@ -399,7 +409,7 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(const __grid_constan
 #pragma unroll
                     for (int kk = 0; kk < kTN / 16; ++kk)
                         umma_bf16_ts(tmem + t * kTileCols + kOCol, tmem + t * kTileCols + kk * 8,
-                                     v_desc + (uint64_t)((kk * kVGroup) >> 4), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                                     desc_step(v_desc, kk * kVGroup), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
                     if (j + 1 < n_kt) {
                         if (t == 0) {
                             ok = wait_k(j + 1);
