@@ -119,6 +119,54 @@ __device__ __forceinline__ uint64_t desc_step(uint64_t desc, uint32_t off_bytes)
     return r;
 }
 
+// The 8 products of one 128-row tile step in one asm block, so that the
+// predicates are set once (first product: accumulate_first; the rest
+// accumulate) rather than once per instruction.  A and B shared-memory
+// descriptors (SS form).
+__device__ __forceinline__ void umma_bf16_x8(uint32_t d_tmem, const uint64_t (&a)[8], const uint64_t (&b)[8],
+                                             uint32_t idesc, uint32_t accumulate_first)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %17, 0;\n\t"
+        "setp.eq.b32 q, %17, %17;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %9, %18, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %10, %18, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %11, %18, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %12, %18, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %5, %13, %18, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %6, %14, %18, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %7, %15, %18, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %8, %16, %18, q;\n\t}" ::"r"(d_tmem),
+        "l"(a[0]), "l"(a[1]), "l"(a[2]), "l"(a[3]), "l"(a[4]), "l"(a[5]), "l"(a[6]), "l"(a[7]), "l"(b[0]),
+        "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]), "r"(accumulate_first),
+        "r"(idesc)
+        : "memory");
+}
+
+// The same for the TS form (A from TMEM at a_tmem + 8 k for product k).
+__device__ __forceinline__ void umma_bf16_ts_x8(uint32_t d_tmem, uint32_t a_tmem, const uint64_t (&b)[8],
+                                                uint32_t idesc, uint32_t accumulate_first)
+{
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t.reg .b32 a1, a2, a3, a4, a5, a6, a7;\n\t"
+        "setp.ne.b32 p, %10, 0;\n\t"
+        "setp.eq.b32 q, %10, %10;\n\t"
+        "add.u32 a1, %1, 8;\n\tadd.u32 a2, %1, 16;\n\tadd.u32 a3, %1, 24;\n\tadd.u32 a4, %1, 32;\n\t"
+        "add.u32 a5, %1, 40;\n\tadd.u32 a6, %1, 48;\n\tadd.u32 a7, %1, 56;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %11, p;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a1], %3, %11, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a2], %4, %11, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a3], %5, %11, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a4], %6, %11, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a5], %7, %11, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a6], %8, %11, q;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a7], %9, %11, q;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b[0]), "l"(b[1]), "l"(b[2]), "l"(b[3]), "l"(b[4]), "l"(b[5]), "l"(b[6]), "l"(b[7]),
+        "r"(accumulate_first), "r"(idesc)
+        : "memory");
+}
+
 __device__ __forceinline__ void umma_commit(uint64_t *bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -383,10 +431,20 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(const __grid_constan
             auto issue_s = [&](int t, int j) {
                 const uint64_t q_desc = umma_desc_sw128(smem_u32(q_s + t * kQTile), 16, 1024);
                 const uint64_t k_desc = umma_desc_sw128(smem_u32(k_ring + (j % NK) * kSlotBytes), 16, 1024);
+                if constexpr (D == 128) {
+                    uint64_t ad[8], bd[8];
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    umma_bf16(tmem + t * kTileCols, desc_step(q_desc, (kk / 4) * kQPanel + (kk % 4) * 32),
-                              desc_step(k_desc, (kk / 4) * kKVPanel + (kk % 4) * 32), idesc_s, kk > 0);
+                    for (int kk = 0; kk < 8; ++kk) {
+                        ad[kk] = desc_step(q_desc, (kk / 4) * kQPanel + (kk % 4) * 32);
+                        bd[kk] = desc_step(k_desc, (kk / 4) * kKVPanel + (kk % 4) * 32);
+                    }
+                    umma_bf16_x8(tmem + t * kTileCols, ad, bd, idesc_s, 0u);
+                } else {
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        umma_bf16(tmem + t * kTileCols, desc_step(q_desc, (kk / 4) * kQPanel + (kk % 4) * 32),
+                                  desc_step(k_desc, (kk / 4) * kKVPanel + (kk % 4) * 32), idesc_s, kk > 0);
+                }
                 umma_commit(&s_full[t]);
             };
             ok = mbar_wait(q_full, 0, abort_flag) && wait_k(0);
@@ -406,10 +464,14 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(const __grid_constan
                     // O_t += P_tj V_j: A = P (TMEM, 8 columns per 16 keys), B = V (MN-major:
                     // 16-key group kk at kk * kVGroup, its two 8-key halves 1024 B
                     // apart, 64-column panels 2048 B apart)
+                    {
+                        static_assert(kTN / 16 == 8, "eight 16-key products per tile");
+                        uint64_t bd[8];
 #pragma unroll
-                    for (int kk = 0; kk < kTN / 16; ++kk)
-                        umma_bf16_ts(tmem + t * kTileCols + kOCol, tmem + t * kTileCols + kk * 8,
-                                     desc_step(v_desc, kk * kVGroup), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < 8; ++kk) bd[kk] = desc_step(v_desc, kk * kVGroup);
+                        umma_bf16_ts_x8(tmem + t * kTileCols + kOCol, tmem + t * kTileCols, bd, idesc_o,
+                                        j > 0 ? 1u : 0u);
+                    }
                     if (j + 1 < n_kt) {
                         if (t == 0) {
                             ok = wait_k(j + 1);
