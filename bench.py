@@ -39,8 +39,8 @@ FALLBACK_HBM_GBS = 6800.0
 NCU_TRAFFIC = {
     "decode": {"sources": ("decode.cu", "common.cuh", "launch.h"), "source_sha": "3f5b4d465385e7e8",
                "bytes_per_launch": {1: 544729856 + 4279552, 2: 310421504 + 3900160, 4: 1345788672 + 33092352}},
-    "prefill": {"sources": ("prefill_tc.cu", "common.cuh", "launch.h"), "source_sha": "da1f86f79b1796a3",
-                "bytes_per_launch": {3: 197249024 + 19143424}},
+    "prefill": {"sources": ("prefill_tc.cu", "common.cuh", "launch.h"), "source_sha": "fd9d2a8e26d35f66",
+                "bytes_per_launch": {3: 199709952 + 19170048}},
 }
 
 
