@@ -37,6 +37,9 @@ NOALLOC_DECODE_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
 class PagedKVError(RuntimeError):
+    """A library call returned a non-zero PKV_* status (``status``; for
+    PKV_ERR_CUDA the CUDA error code is in the message)."""
+
     def __init__(self, fn, status, name, cuda_error=0):
         msg = f"{fn} returned {name} ({status})"
         if cuda_error:
@@ -46,6 +49,8 @@ class PagedKVError(RuntimeError):
 
 
 class Dims(ctypes.Structure):
+    """pkv_dims: pool geometry (n_blocks physical blocks, the pool tensors have
+    n_blocks + 1 with the scratch block last)."""
     _fields_ = [("n_blocks", ctypes.c_int32), ("block_size", ctypes.c_int32),
                 ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32)]
 
@@ -243,6 +248,8 @@ def paged_kv_copy_blocks(pairs, k_pool, v_pool, k_scales=None, v_scales=None, de
 
 
 def decode_workspace_bytes(n_seqs, n_q_heads, head_dim, max_total_ctx_tokens, split_tokens=0) -> int:
+    """Device workspace a decode call needs for batches of n_seqs sequences whose
+    contexts sum to at most max_total_ctx_tokens (pkv_decode_workspace_bytes)."""
     n = load_library().pkv_decode_workspace_bytes(int(n_seqs), int(n_q_heads), int(head_dim),
                                                   int(max_total_ctx_tokens), int(split_tokens))
     if n == 0:
@@ -543,6 +550,7 @@ def paged_kv_stage_blocks(pairs, host_k, host_v, pool_k, pool_v, dev_status=None
 
 
 def streamed_workspace_bytes(n_seqs, n_q_heads, head_dim, n_slots, block_size) -> int:
+    """Device workspace paged_decode_streamed needs (pkv_streamed_workspace_bytes)."""
     n = load_library().pkv_streamed_workspace_bytes(int(n_seqs), int(n_q_heads), int(head_dim), int(n_slots),
                                                     int(block_size))
     if n == 0:
