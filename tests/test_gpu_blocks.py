@@ -71,7 +71,7 @@ def test_copy_blocks_bad_ids_are_flagged_and_skipped(P):
 
 
 @pytest.mark.parametrize("int8", [False, True])
-def test_serving_loop_driven_by_the_block_manager(P, int8):
+def test_serving_loop_driven_by_the_block_manager(P, int8, decode_impl):
     gen = torch.Generator().manual_seed(77 + int8)
     n_blocks, bs, n_slots, max_blocks = 22, 16, 8, 8
     Hkv, G, D = 4, 4, 128

@@ -26,7 +26,7 @@ def P():
 
 
 @pytest.mark.parametrize("int8", [False, True])
-def test_layer_step_graph_replays_the_eager_bits(P, int8):
+def test_layer_step_graph_replays_the_eager_bits(P, int8, decode_impl):
     n_layers, n, Hkv, G, D, bs, n_blocks, max_blocks = 4, 5, 4, 4, 128, 16, 60, 10   # int8 decode: Hkv % 4 == 0
     Hq = Hkv * G
     gen = torch.Generator().manual_seed(303 + int8)

@@ -206,18 +206,6 @@ def check_lse(lse_gpu, lse_ref):
         assert np.abs(g[fin] - lse_ref[fin]).max() <= LSE_TOL
 
 
-@pytest.fixture(params=["auto", "split"])
-def decode_impl(request, monkeypatch):
-    """auto: small batches take the one-launch path (one CTA per (sequence,
-    kv head)), larger ones the split-KV path; split: every call takes the
-    split-KV path."""
-    if request.param == "split":
-        monkeypatch.setenv("PKV_DECODE_IMPL", "split")
-    else:
-        monkeypatch.delenv("PKV_DECODE_IMPL", raising=False)
-    return request.param
-
-
 @pytest.mark.parametrize("name", ["cfg0", "cfg1", "cfg4", "ragged_d64", "ragged_g8_bs32", "ragged_g1", "small_limits",
                                   "small_limits_d128"])
 def test_decode_bf16_parity(P, name, decode_impl):
