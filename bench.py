@@ -12,7 +12,16 @@ steps.
 
 Prints one JSON line (rank 0).  Under torchrun every rank runs its own replica
 (independent sequences, no collective in the data path: weak scaling) and the
-time is the max over ranks.
+time is the max over ranks.  Other modes (each prints its own JSON line):
+
+  --config 2 / 4     int8 pages with 16 new tokens (and the gather beside it) /
+                     256 skewed sequences sharing prefixes, 512-token splits
+  --config 3         chunked prefill on the tensor cores (TFLOP/s)
+  --config 0         the tiny, L2-resident decode step: per-call medians, warm and flushed
+  --layers L         an L-layer decode step, eager launches against one CUDA graph
+  --stream N_SLOTS   config 1 decoded from a pinned host tier through N_SLOTS scratch blocks
+  --blocks           the host-side block manager's serving loop (no GPU)
+  --impl reference   the float64 oracle on the host cores, bounded samples
 """
 from __future__ import annotations
 
