@@ -48,7 +48,7 @@ FALLBACK_HBM_GBS = 6800.0
 NCU_TRAFFIC = {
     "decode": {"sources": ("decode.cu", "common.cuh", "launch.h"), "source_sha": "3f5b4d465385e7e8",
                "bytes_per_launch": {1: 544729856 + 4279552, 2: 310421504 + 3900160, 4: 1345788672 + 33092352}},
-    "prefill": {"sources": ("prefill_tc.cu", "common.cuh", "launch.h"), "source_sha": "fd9d2a8e26d35f66",
+    "prefill": {"sources": ("prefill_tc.cu", "common.cuh", "launch.h"), "source_sha": "afce10efbd08fc2c",
                 "bytes_per_launch": {3: 199709952 + 19170048}},
 }
 

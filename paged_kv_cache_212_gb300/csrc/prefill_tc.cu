@@ -144,7 +144,9 @@ __device__ __forceinline__ void umma_bf16_x8(uint32_t d_tmem, const uint64_t (&a
         : "memory");
 }
 
-// The same for the TS form (A from TMEM at a_tmem + 8 k for product k).
+// The 8 products of one tile step in the TS form: D (TMEM) += A (TMEM, M x 16,
+// K-major: lane = row, column c = bf16 pair 2c, 2c + 1; product k at a_tmem +
+// 8 k) * B (shared-memory descriptor), predicates set once as above.
 __device__ __forceinline__ void umma_bf16_ts_x8(uint32_t d_tmem, uint32_t a_tmem, const uint64_t (&b)[8],
                                                 uint32_t idesc, uint32_t accumulate_first)
 {
@@ -203,19 +205,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *r)
         "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-}
-
-// D (TMEM) += A (TMEM, M x 16, K-major: lane = row, column c = bf16 pair
-// 2c, 2c + 1) * B (shared-memory descriptor).
-__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                             uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
 }
 
 // Store 16 consecutive 32-bit columns of this thread's TMEM lane (completion
