@@ -12,7 +12,12 @@ steps.
 
 Prints one JSON line (rank 0).  Under torchrun every rank runs its own replica
 (independent sequences, no collective in the data path: weak scaling) and the
-time is the max over ranks.  Other modes (each prints its own JSON line):
+time is the max over ranks.  The K timed steps follow the warm-up directly;
+each timed region starts after a GPU-side hold during which the host enqueues
+the K steps, and short regions are repeated (median reported) so that the
+timed work adds up to ~150 ms.  The default single-GPU run also nests short
+runs of the other four scenarios and of the page writes in the line
+(`other_configs`).  Other modes (each prints its own JSON line):
 
   --config 2 / 4     int8 pages with 16 new tokens (and the gather beside it) /
                      256 skewed sequences sharing prefixes, 512-token splits
@@ -63,6 +68,8 @@ def parse_args():
     ap.add_argument("--split", type=int, default=0, help="decode split_tokens (0 = library default)")
     ap.add_argument("--e2e-steps", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-configs", action="store_true",
+                    help="default run: skip the short runs of the other scenarios nested in the line")
     ap.add_argument("--blocks", action="store_true",
                     help="time the host-side block manager's per-step calls instead (no GPU)")
     ap.add_argument("--stream", type=int, default=0, metavar="N_SLOTS",
@@ -101,6 +108,73 @@ def max_over_ranks(values, device):
     if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return [float(x) for x in t]
+
+
+def gpu_hold(ms):
+    """Puts a GPU-side wait of about `ms` on the current stream, so that the
+    host enqueues the timed steps while the GPU waits: the timed region that
+    starts after it then measures the GPU, not the host's launch rate."""
+    import torch
+    torch.cuda._sleep(max(1, int(ms * 1e-3 * 2.0e9)))     # clock cycles at ~2 GHz
+
+
+def device_timed(step, K, stream, world, device, host_ms_per_step, est_ms_per_step,
+                 min_total_ms=150.0, max_repeats=50):
+    """Times exactly K steps on the device, R times over.  Every repeat is
+    bracketed by a barrier and a synchronize on both sides; a GPU-side hold
+    that covers the host's enqueue of the K steps sits before the start event,
+    so the GPU runs the K steps back to back.  R is chosen so that the timed
+    regions add up to about min_total_ms (at most max_repeats).  Returns the
+    per-repeat elapsed ms (max over ranks for each repeat)."""
+    import torch
+    import torch.distributed as dist
+    R = max(1, min(max_repeats, math.ceil(min_total_ms / max(K * est_ms_per_step, 1e-6))))
+    hold = min(50.0, 0.3 + 1.25 * K * host_ms_per_step)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(R)]
+    per = []
+    for t0, t1 in evs:
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+        gpu_hold(hold)
+        t0.record(stream)
+        for _ in range(K):
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        per.append(t0.elapsed_time(t1))
+    return max_over_ranks(per, device)
+
+
+def warm_up(step, W):
+    """W untimed steps; returns (host ms per step spent enqueueing, GPU ms per
+    step of the last half, both measured here)."""
+    import torch
+    for _ in range(max(1, W // 2)):
+        step()
+    torch.cuda.synchronize()
+    n = max(1, W - W // 2)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    h0 = time.perf_counter()
+    e0.record()
+    for _ in range(n):
+        step()
+    e1.record()
+    host = (time.perf_counter() - h0) * 1e3 / n
+    torch.cuda.synchronize()
+    return host, e0.elapsed_time(e1) / n
+
+
+def timing_note(per_repeat_ms, K, hold_note=True):
+    return {"repeats": len(per_repeat_ms), "steps_per_repeat": K,
+            "ms_per_step_median": round(statistics.median(per_repeat_ms) / K, 5),
+            "ms_per_step_min": round(min(per_repeat_ms) / K, 5),
+            "ms_per_step_max": round(max(per_repeat_ms) / K, 5),
+            "how": ("each repeat: barrier + synchronize, a GPU-side hold while the host enqueues the K steps, "
+                    "CUDA events around the K steps on the launching stream, synchronize + barrier; "
+                    "ms_per_step is the median repeat / K" if hold_note else "")}
 
 
 def weak_scaling_value(bytes_per_step_per_rank, world, ms_per_step):
@@ -232,34 +306,49 @@ def fill_pool(P, w, device):
     return kp, vp, ks, vs
 
 
-def cpu_baseline(cfg, budget_s=12.0, threads=None):
+def cpu_baseline(cfg, budget_s=8.0):
     """The float64 oracle, as it stands, on the host cores: write + decode of
-    the same workload's sequences, repeated until ~budget_s of wall time."""
+    the same workload's sequences, repeated until ~budget_s of wall time, once
+    with one thread per host core and once single-threaded."""
     sys.path.insert(0, os.path.join(ROOT, "tests"))
-    import numpy as np
     import oracle
     from oracle_pools import dims_of, empty_pools, write_prefix
     w = make_workload(cfg, "cpu")
-    threads = threads or (os.cpu_count() or 1)
     kp, vp, ks, vs = empty_pools(w, poison=False)
     write_prefix(w, kp, vp, ks, vs)
     decode_b, write_b = algorithmic_bytes(w)
     d = dims_of(w)
-    reps, t0 = 0, time.perf_counter()
-    while True:
-        if w.kv_format == "int8":
-            oracle.write_int8(w.k_new, w.v_new, kp, vp, ks, vs, d, w.tables, w.start_pos)
-        else:
-            oracle.write_bf16(w.k_new, w.v_new, kp, vp, d, w.tables, w.start_pos)
-        oracle.decode(w.q, kp, vp, d, w.tables, w.ctx_lens, w.softmax_scale, ks, vs, n_threads=threads)
-        reps += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s:
-            break
+
+    def run(threads, n):
+        sl = slice(0, n)
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            if w.kv_format == "int8":
+                oracle.write_int8(w.k_new[sl], w.v_new[sl], kp, vp, ks, vs, d, w.tables[sl], w.start_pos[sl])
+            else:
+                oracle.write_bf16(w.k_new[sl], w.v_new[sl], kp, vp, d, w.tables[sl], w.start_pos[sl])
+            oracle.decode(w.q[sl], kp, vp, d, w.tables[sl], w.ctx_lens[sl], w.softmax_scale, ks, vs,
+                          n_threads=threads)
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= budget_s:
+                return reps, el
+
+    threads = os.cpu_count() or 1
+    reps, el = run(threads, w.n_seqs)
     gbs = reps * (decode_b + write_b) / el / 1e9
+    # single-threaded: the first n sequences, n such that a pass takes about a
+    # quarter of the budget (the bytes counted are those of the n sequences)
+    n1 = max(1, min(w.n_seqs, int(w.n_seqs * (budget_s / 4) / max(el / reps * threads, 1e-9))))
+    reps1, el1 = run(1, n1)
+    sub = make_sub_bytes(w, n1)
+    gbs1 = reps1 * sub / el1 / 1e9
     return {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
             "sample": f"{reps} full steps (write + float64 decode of all {w.n_seqs} sequences) in {el:.1f} s",
-            "seq_steps_per_s": round(reps * w.n_seqs / el, 2)}
+            "seq_steps_per_s": round(reps * w.n_seqs / el, 2),
+            "single_thread": {"value": round(gbs1, 4), "unit": "GB/s", "cores": 1,
+                              "sample": f"{reps1} steps of the first {n1} sequences in {el1:.1f} s",
+                              "seq_steps_per_s": round(reps1 * n1 / el1, 2)}}
 
 
 def prefill_row_flops(w):
@@ -316,20 +405,28 @@ def oracle_prefill_sample(w, budget_s, threads):
     return float(rowf[sel].sum()), (lambda: one(sel)), "the chunk write + float64 prefill of " + what
 
 
-def cpu_baseline_prefill(budget_s=12.0, threads=None):
+def cpu_baseline_prefill(budget_s=12.0):
+    """The float64 oracle's chunk write + prefill over a row sample, with one
+    thread per host core and single-threaded."""
     sys.path.insert(0, os.path.join(ROOT, "tests"))
     w = make_workload(3, "cpu")
-    threads = threads or (os.cpu_count() or 1)
-    flops, run, what = oracle_prefill_sample(w, budget_s / 2, threads)
-    reps, t0 = 0, time.perf_counter()
-    while True:
-        run()
-        reps += 1
-        el = time.perf_counter() - t0
-        if el >= budget_s / 2:
-            break
-    return {"value": round(reps * flops / el / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
-            "sample": f"{reps} passes of {what} in {el:.1f} s"}
+    res = {}
+    for threads in (os.cpu_count() or 1, 1):
+        flops, run, what = oracle_prefill_sample(w, budget_s / 4, threads)
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            run()
+            reps += 1
+            el = time.perf_counter() - t0
+            if el >= budget_s / 4:
+                break
+        res[threads] = {"value": round(reps * flops / el / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
+                        "sample": f"{reps} passes of {what} in {el:.1f} s"}
+    many = os.cpu_count() or 1
+    line = dict(res[many], kind="oracle")
+    if many != 1:
+        line["single_thread"] = res[1]
+    return line
 
 
 def run_reference(args, rank, world):
@@ -434,7 +531,7 @@ def bench_config(w, args):
     return {"workload": w.name, "n_seqs": w.n_seqs, "ctx_min": int(ctx.min()), "ctx_max": int(ctx.max()),
             "ctx_total": int(ctx.sum()), "n_q_heads": w.n_q_heads, "n_kv_heads": w.n_kv_heads,
             "head_dim": w.head_dim, "block_size": w.block_size, "kv_pages": w.kv_format,
-            "n_blocks": w.n_blocks, "layers_timed": 1, "split_tokens": args.split or "library default",
+            "n_blocks": w.n_blocks, "layers_timed": 1, "split_tokens": args.split or w.split_tokens or "library default",
             "l2": "inputs larger than L2 (K/V pages read per step far exceed the 129 MB L2); no flush"}
 
 
@@ -476,9 +573,11 @@ def prefill_flops(w):
     return 4 * w.n_q_heads * w.head_dim * keys
 
 
-def run_prefill_bench(args, P, w, device, rank, world):
+def run_prefill_bench(args, P, w, device, rank, world, K, W, with_e2e=True):
     """Config 3: paged write of each sequence's 512-token chunk, then chunked
-    paged prefill attention over prefix + chunk (tensor-core bound)."""
+    paged prefill attention over prefix + chunk (tensor-core bound).  The
+    step (write + prefill) and the prefill call alone are each timed as K
+    calls on the device (see device_timed).  Returns the JSON line."""
     import torch
     import torch.distributed as dist
     kp, vp, _, _ = fill_pool(P, w, device)
@@ -488,37 +587,41 @@ def run_prefill_bench(args, P, w, device, rank, world):
     status = torch.zeros(1, dtype=torch.int32, device=device)
     stream = torch.cuda.current_stream()
 
-    def step(ev=None):
-        P.paged_kv_write(k_new, v_new, kp, vp, tables, start, dev_status=status)
-        if ev is not None:
-            ev[0].record(stream)
+    def prefill():
         P.paged_prefill_attention(q, kp, vp, tables, start, w.softmax_scale, out=out, dev_status=status)
-        if ev is not None:
-            ev[1].record(stream)
 
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize()
-    assert int(status.item()) == 0, f"device status {int(status.item())}"
-    K = args.steps
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
-    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
+    def step():
+        P.paged_kv_write(k_new, v_new, kp, vp, tables, start, dev_status=status)
+        prefill()
+
+    uuid = gpu_uuid(device)
     with ClockSampler(uuid) as clk:
         time.sleep(0.25)
-        t0.record(stream)
-        for i in range(K):
-            step(ev[i])
-        t1.record(stream)
-        torch.cuda.synchronize()
-    ms = max_over_ranks([t0.elapsed_time(t1) / K], device)[0]
-    pre_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+        host_ms, est_ms = warm_up(step, max(3, W))
+        assert int(status.item()) == 0, f"device status {int(status.item())}"
+        per = device_timed(step, K, stream, world, device, host_ms, est_ms)
+        host_p, est_p = warm_up(prefill, 3)
+        per_p = device_timed(prefill, K, stream, world, device, host_p, est_p)
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
+    ms = statistics.median(per) / K
+    pre_ms = statistics.median(per_p) / K
     flops = prefill_flops(w)
     peak, kind = measured_peaks("bf16_tflops")
     ach = flops / (pre_ms * 1e-3) / 1e12
+    line = {"metric": PREFILL_METRIC, "value": round(world * flops / (ms * 1e-3) / 1e12, 2),
+            "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": W, "ms_per_step": round(ms, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": w.name, "n_seqs": w.n_seqs, "chunk": w.n_new,
+                       "prefix": [int(x) for x in w.stored_lens]},
+            "timing": timing_note(per, K),
+            "roofline": {"bound": "tensor", "kernel": "paged_prefill_attention", "achieved": round(ach, 2),
+                         "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4),
+                         "traffic": ncu_traffic("prefill", 3),
+                         "flops_per_launch": flops, "avg_launch_ms": round(pre_ms, 5),
+                         "peak_source": f"{kind} bf16_tflops (burst)"},
+            "gpu_launches": 2 * K * len(per) + K * len(per_p), "clocks": clk.summary()}
+    if not with_e2e:
+        return line
     # end to end: the chunk's rows, queries, tables and prefix lengths from pinned
     # host memory every step, the output back to pinned host memory
     h_in = tuple(x.cpu().pin_memory() for x in (w.k_new, w.v_new, w.q, w.tables, w.start_pos))
@@ -545,24 +648,10 @@ def run_prefill_bench(args, P, w, device, rank, world):
     torch.cuda.synchronize()
     assert int(status.item()) == 0, f"device status {int(status.item())}"
     e2e_ms = max_over_ranks([e0.elapsed_time(e1) / e2e_steps], device)[0]
-    line = {"metric": PREFILL_METRIC, "value": round(world * flops / (ms * 1e-3) / 1e12, 2),
-            "unit": "TFLOP/s", "n_gpus": world, "steps": K, "warmup": args.warmup, "ms_per_step": round(ms, 5),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": w.name, "n_seqs": w.n_seqs, "chunk": w.n_new,
-                       "prefix": [int(x) for x in w.stored_lens], "impl": os.environ.get("PKV_PREFILL_IMPL", "tcgen05")},
-            "roofline": {"bound": "tensor", "kernel": "paged_prefill_attention", "achieved": round(ach, 2),
-                         "peak": peak, "unit": "TFLOP/s", "frac": round(ach / peak, 4),
-                         "traffic": ncu_traffic("prefill", 3),
-                         "flops_per_launch": flops, "avg_launch_ms": round(pre_ms, 5),
-                         "peak_source": f"{kind} bf16_tflops (burst)"},
-            "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
-                    "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5),
-                    "steps": e2e_steps},
-            "gpu_launches": 2 * K, "clocks": clk.summary()}
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline_prefill()
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+    line["e2e"] = {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                   "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5),
+                   "steps": e2e_steps}
+    return line
 
 
 def blocks_serving_loop(mgr, n_slots, steps, rng_seed=20265):
@@ -695,6 +784,9 @@ def run_stream_bench(args, P, device):
     uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
     with ClockSampler(uuid) as clk:
         time.sleep(0.25)
+        for _ in range(3):          # busy again right before the timed calls
+            call()
+        torch.cuda.synchronize()
         e0.record(stream)
         for _ in range(steps):
             call()
@@ -720,7 +812,7 @@ def run_stream_bench(args, P, device):
     print(json.dumps(line), flush=True)
 
 
-def run_small_bench(args, P, w, device):
+def run_small_bench(args, P, w, device, reps=None):
     """Config 0 (4 sequences, all data in L2): the decode step (write + decode)
     timed call by call with CUDA events, median of the reps, once with the
     data warm in L2 and once with a buffer of twice the L2 size rewritten
@@ -741,7 +833,7 @@ def run_small_bench(args, P, w, device):
         P.paged_decode_step(k_new, v_new, start, q, kp, vp, tables, ctx, w.softmax_scale, out=out, workspace=ws,
                             dev_status=status)
 
-    reps = max(50, min(args.steps, 2000))
+    reps = reps or max(50, min(args.steps, 2000))
     warm_n = max(5, args.warmup)
 
     def median_us(flushed):
@@ -770,14 +862,17 @@ def run_small_bench(args, P, w, device):
     assert int(status.item()) == 0, f"device status {int(status.item())}"
     decode_b, write_b = algorithmic_bytes(w)
     us = cold["median_us"]
-    print(json.dumps({
+    return {
         "metric": METRIC, "value": round((decode_b + write_b) / (us * 1e-6) / 1e9, 3), "unit": "GB/s",
         "n_gpus": 1, "steps": reps, "warmup": warm_n, "ms_per_step": round(us * 1e-3, 5), "higher_is_better": True,
         "scaling": "none", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": dict(bench_config(w, args), l2=f"data fits in L2: value from the flushed median ({2 * l2 >> 20} "
                                                   "MiB rewritten between reps)"),
         "seq_steps_per_s_per_layer": round(w.n_seqs / (us * 1e-6), 1),
-        "warm_l2": warm, "flushed_l2": cold, "gpu_launches": 3 * reps * 2, "clocks": clk.summary()}), flush=True)
+        "warm_l2": warm, "flushed_l2": cold,
+        # one launch per step: this shape takes the small-batch path unless PKV_DECODE_IMPL=split
+        "gpu_launches": (3 if os.environ.get("PKV_DECODE_IMPL") == "split" else 1) * reps * 2,
+        "clocks": clk.summary()}
 
 
 def run_layers_bench(args, P, device):
@@ -947,15 +1042,40 @@ def main():
     w = make_workload(args.config, device)  # every rank owns an independent replica batch
     if args.config == 0:
         if rank == 0:
-            run_small_bench(args, P, w, device)
+            print(json.dumps(run_small_bench(args, P, w, device)), flush=True)
         if world > 1:
             dist.destroy_process_group()
         return
     if args.config == 3:
-        run_prefill_bench(args, P, w, device, rank, world)
+        line = run_prefill_bench(args, P, w, device, rank, world, args.steps, args.warmup)
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline_prefill()
+        if rank == 0:
+            print(json.dumps(line), flush=True)
         if world > 1:
             dist.destroy_process_group()
         return
+    line = run_decode_bench(args, P, w, device, rank, world, args.steps, args.warmup)
+    if args.config == 2:
+        line["gather"] = bench_gather(P, device, measured_peaks()[0])
+    del w
+    torch.cuda.empty_cache()
+    if world == 1 and args.config == 1 and not args.no_other_configs:
+        line["other_configs"] = other_configs(args, P, device)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.config)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def run_decode_bench(args, P, w, device, rank, world, K, W, with_e2e=True):
+    """One decode step (paged write of the step's new rows + paged decode
+    attention, one paged_decode_step call) of workload w, timed as K steps
+    on the device (see device_timed), then end to end through the Python API
+    with per-step host copies.  Returns the JSON line (a dict)."""
+    import torch
     kp, vp, ks, vs = fill_pool(P, w, device)
     tables = w.tables.to(device)
     start = w.start_pos.to(device)
@@ -974,39 +1094,70 @@ def main():
         P.paged_decode_step(k_new, v_new, start, q, kp, vp, tables, ctx, w.softmax_scale, k_scales=ks,
                             v_scales=vs, split_tokens=split, out=out, workspace=ws, dev_status=status)
 
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize()
-    assert int(status.item()) == 0, f"device status {int(status.item())}"
-
-    # ---- timed region: K steps, events around every decode call ----
-    K = args.steps
-    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    uuid = None
-    try:
-        uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
-    except Exception:
-        pass
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
+    uuid = gpu_uuid(device)
     with ClockSampler(uuid) as clk:
-        time.sleep(0.25)  # let the sampler start before the timed work
-        # one step is one paged_decode_step call; events bracket the K calls on
-        # their stream (no events in between, which would break the launch chaining)
-        t_start.record(stream)
-        for i in range(K):
-            step()
-        t_end.record(stream)
-        torch.cuda.synchronize()
-    if world > 1:
-        dist.barrier()
-    elapsed_ms = max_over_ranks([t_start.elapsed_time(t_end)], device)[0]
-    decode_ms = elapsed_ms / K
+        time.sleep(0.25)  # the sampler is running before the warm-up starts
+        host_ms, est_ms = warm_up(step, max(3, W))
+        assert int(status.item()) == 0, f"device status {int(status.item())}"
+        # the timed region follows the warm-up directly: no idle gap before it
+        per = device_timed(step, K, stream, world, device, host_ms, est_ms)
     assert int(status.item()) == 0, f"device status {int(status.item())}"
-    ms_per_step = elapsed_ms / K
+    ms_per_step = statistics.median(per) / K
+    decode_b, write_b = algorithmic_bytes(w)
+    step_b = decode_b + write_b
+    peak, peak_kind = measured_peaks()
+    value = weak_scaling_value(step_b, world, ms_per_step)
+    achieved = step_b / (ms_per_step * 1e-3) / 1e9
+    traffic = ncu_traffic("decode", w_index(w))
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "u8" if int8 else "bf16", "data": "synthetic",
+        "config": bench_config(w, args),
+        "pct_of_peak": round(100 * value / world / peak, 2),
+        "seq_steps_per_s_per_layer": round(world * w.n_seqs / (ms_per_step * 1e-3), 1),
+        "ms_per_32_layer_step": round(32 * ms_per_step, 4),
+        "timing": timing_note(per, K),
+        "roofline": {"bound": "hbm",
+                     "kernel": "paged_decode_step (plan + write, split, merge launches; split kernel dominant)",
+                     "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "algorithmic_bytes_per_launch": step_b, "avg_launch_ms": round(ms_per_step, 5),
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                     else "fallback 6.8 TB/s"},
+        "gpu_launches": 3 * K * len(per),
+        "clocks": clk.summary(),
+    }
+    if with_e2e:
+        line["e2e"] = decode_e2e(P, w, kp, vp, ks, vs, split, ws, status, q, K, world, device, stream, args)
+    return line
 
-    # ---- end to end through the public API with pinned host buffers ----
+
+def W_CONFIGS():
+    from paged_kv_cache_212_gb300 import workloads as W
+    return W.CONFIGS
+
+
+def w_index(w):
+    """The scenario number of a workload (from its seed)."""
+    from paged_kv_cache_212_gb300 import workloads as W
+    return w.seed - W.SEED_BASE
+
+
+def gpu_uuid(device):
+    import torch
+    try:
+        return "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        return None
+
+
+def decode_e2e(P, w, kp, vp, ks, vs, split, ws, status, q, K, world, device, stream, args):
+    """The decode step end to end through the public API with pinned host
+    buffers: per step the new rows, queries, tables, positions and lengths go
+    host -> device and the output device -> host, inside the timed region."""
+    import torch
+    import torch.distributed as dist
     e2e_steps = args.e2e_steps or max(10, min(K, 2000))
     h_k, h_v, h_q = (x.cpu().pin_memory() for x in (w.k_new, w.v_new, w.q))
     h_tab, h_start, h_ctx = (x.cpu().pin_memory() for x in (w.tables, w.start_pos, w.ctx_lens))
@@ -1032,43 +1183,121 @@ def main():
     e2e_run(e2e_steps)
     e1.record(stream)
     torch.cuda.synchronize()
+    assert int(status.item()) == 0, f"device status {int(status.item())}"
     e2e_ms = max_over_ranks([e0.elapsed_time(e1) / e2e_steps], device)[0]
-
     decode_b, write_b = algorithmic_bytes(w)
-    step_b = decode_b + write_b
-    peak, peak_kind = measured_peaks()
-    value = weak_scaling_value(step_b, world, ms_per_step)
-    achieved = step_b / (decode_ms * 1e-3) / 1e9
-    traffic = ncu_traffic("decode", args.config)
-    line = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
-        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "u8" if int8 else "bf16", "data": "synthetic",
-        "config": bench_config(w, args),
-        "pct_of_peak": round(100 * value / world / peak, 2),
-        "seq_steps_per_s_per_layer": round(world * w.n_seqs / (ms_per_step * 1e-3), 1),
-        "ms_per_32_layer_step": round(32 * ms_per_step, 4),
-        "roofline": {"bound": "hbm",
-                     "kernel": "paged_decode_step (plan + write, split, merge launches; split kernel dominant)",
-                     "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "algorithmic_bytes_per_launch": step_b, "avg_launch_ms": round(decode_ms, 5),
-                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
-                     else "fallback 6.8 TB/s"},
-        "e2e": {"value": round(weak_scaling_value(step_b, world, e2e_ms), 2), "unit": "GB/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5),
-                "steps": e2e_steps},
-        "gpu_launches": 3 * K,
-        "clocks": clk.summary(),
-    }
-    if args.config == 2:
-        line["gather"] = bench_gather(P, device, peak)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(args.config)
-    if rank == 0:
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        dist.destroy_process_group()
+    return {"value": round(weak_scaling_value(decode_b + write_b, world, e2e_ms), 2), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5),
+            "steps": e2e_steps}
+
+
+def bench_writes(P, device, peak):
+    """The page writes on their own: paged_kv_write_int8 at the int8
+    workload's 64 x 16-token shape and paged_kv_write of the prefill
+    workload's 8 x 512-token chunk, per-call CUDA events (median of 200),
+    warm and with twice the L2 rewritten before each call."""
+    import torch
+    res = {}
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush = torch.empty(2 * l2 // 4 + 1, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream()
+    for cfg in (2, 3):
+        w = make_workload(cfg, device)
+        int8 = cfg == 2
+        nb1 = w.n_blocks + 1
+        shape = (nb1, w.block_size, w.n_kv_heads, w.head_dim)
+        kp = torch.zeros(shape, dtype=torch.int8 if int8 else torch.bfloat16, device=device)
+        vp = torch.zeros_like(kp)
+        ks = torch.zeros(shape[:3], dtype=torch.float32, device=device) if int8 else None
+        vs = torch.zeros_like(ks) if int8 else None
+        tables, start = w.tables.to(device), w.start_pos.to(device)
+        k_new, v_new = w.k_new.to(device), w.v_new.to(device)
+
+        def call():
+            if int8:
+                P.paged_kv_write_int8(k_new, v_new, kp, vp, ks, vs, tables, start)
+            else:
+                P.paged_kv_write(k_new, v_new, kp, vp, tables, start)
+
+        rows = w.n_seqs * w.n_new * w.n_kv_heads
+        nbytes = (2 * rows * w.head_dim * 2 + 2 * rows * (w.head_dim + 4)) if int8 else 2 * 2 * rows * w.head_dim * 2
+        nbytes += w.n_seqs * 4 + int(((w.start_pos + w.n_new + w.block_size - 1) // w.block_size).sum()) * 4
+        out = {"workload": w.name, "call": "paged_kv_write_int8" if int8 else "paged_kv_write",
+               "rows": rows, "algorithmic_bytes": nbytes}
+        for name, flushed in (("warm", False), ("flushed", True)):
+            for _ in range(5):
+                call()
+            reps = 200
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+            for a, b in evs:
+                if flushed:
+                    flush.fill_(1.0)
+                gpu_hold(0.05)
+                a.record(stream)
+                call()
+                b.record(stream)
+            torch.cuda.synchronize()
+            t = sorted(a.elapsed_time(b) for a, b in evs)
+            ms = t[len(t) // 2]
+            out[name] = {"median_us": round(ms * 1e3, 3), "gbs": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                         "frac": round(nbytes / (ms * 1e-3) / 1e9 / peak, 4)}
+        res[str(cfg)] = out
+        del kp, vp, ks, vs, w
+        torch.cuda.empty_cache()
+    return res
+
+
+def other_configs(args, P, device):
+    """Short runs of the other four scenarios, reported beside the headline
+    (the headline's metric, value and config stay those of the Llama-3-8B
+    decode): the int8 decode step with its gather, the chunked prefill, the
+    skewed shared-prefix decode and the tiny L2-resident step, plus the page
+    writes on their own."""
+    import torch
+    res = {}
+    peak = measured_peaks()[0]
+    keep = ("value", "unit", "ms_per_step", "steps", "warmup", "dtype", "pct_of_peak",
+            "seq_steps_per_s_per_layer", "timing", "roofline", "clocks", "config", "gpu_launches")
+    for cfg in (2, 4):
+        w = make_workload(cfg, device)
+        line = run_decode_bench(args, P, w, device, 0, 1, 200, 5, with_e2e=False)
+        sub = {k: line[k] for k in keep if k in line}
+        sub["metric"] = METRIC
+        if cfg == 2:
+            sub["gather"] = bench_gather(P, device, peak)
+        if cfg == 4:
+            # shared prefix blocks are read by every member: report the unique bytes too
+            sub["unique_kv_bytes_per_step"] = unique_kv_bytes(w)
+        res[str(cfg)] = sub
+        del w, line
+        torch.cuda.empty_cache()
+    w = make_workload(3, device)
+    line = run_prefill_bench(args, P, w, device, 0, 1, 20, 5, with_e2e=False)
+    res["3"] = {k: line[k] for k in ("metric",) + keep if k in line}
+    del w, line
+    torch.cuda.empty_cache()
+    w = make_workload(0, device)
+    line = run_small_bench(args, P, w, device, reps=300)
+    res["0"] = {k: line[k] for k in ("metric", "value", "unit", "ms_per_step", "warm_l2", "flushed_l2",
+                                     "seq_steps_per_s_per_layer", "clocks", "config") if k in line}
+    del w, line
+    torch.cuda.empty_cache()
+    res["writes"] = bench_writes(P, device, peak)
+    return res
+
+
+def unique_kv_bytes(w):
+    """K/V bytes of the blocks the step reads, each physical block once
+    (valid tokens of each distinct block)."""
+    bs = w.block_size
+    per_tok = 2 * w.n_kv_heads * w.head_dim * 2
+    seen = {}
+    for s in range(w.n_seqs):
+        L = int(w.ctx_lens[s])
+        for j in range(-(-L // bs)):
+            b = int(w.tables[s, j])
+            seen[b] = max(seen.get(b, 0), min(bs, L - j * bs))
+    return sum(seen.values()) * per_tok
 
 
 if __name__ == "__main__":
