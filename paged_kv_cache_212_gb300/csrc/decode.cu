@@ -125,6 +125,18 @@ __device__ __forceinline__ void int8x4_to_half2x2(uint32_t w, uint32_t &lo, uint
     hi = *reinterpret_cast<uint32_t *>(&hb);
 }
 
+// int8 -> fp16 for four packed codes with a bias: (0x6400 | (b ^ 0x80)) is
+// the fp16 value 1152 + b, exact for every code b.  Products of the biased
+// codes are corrected once per score (S - 1152 sum_d q_d) and once per output
+// (O - 1152 sum_t p_t) instead of subtracting the bias from every element.
+constexpr float kCodeBias = 1152.0f;
+__device__ __forceinline__ void int8x4_to_biased_half2x2(uint32_t w, uint32_t &lo, uint32_t &hi)
+{
+    const uint32_t u = w ^ 0x80808080u;
+    lo = __byte_perm(u, 0x64646464u, 0x4140);
+    hi = __byte_perm(u, 0x64646464u, 0x4342);
+}
+
 // Byte offset of the 16-byte chunk `chunk` (0..7) of row `row` in a
 // 128-byte-swizzled tile of 128-byte rows.
 __device__ __forceinline__ uint32_t swz(uint32_t row, uint32_t chunk)
@@ -191,9 +203,9 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t *__rest
         } else if (write_mode == 2) {
             const int64_t warps = blockDim.x >> 5;
             if (head_dim == 128)
-                write_int8_units<4>(w, k_scales, v_scales, wb * warps + (threadIdx.x >> 5), nwb * warps);
+                write_int8_units<16>(w, k_scales, v_scales, wb * warps + (threadIdx.x >> 5), nwb * warps);
             else
-                write_int8_units<2>(w, k_scales, v_scales, wb * warps + (threadIdx.x >> 5), nwb * warps);
+                write_int8_units<8>(w, k_scales, v_scales, wb * warps + (threadIdx.x >> 5), nwb * warps);
         }
         return;
     }
@@ -416,8 +428,8 @@ __device__ __forceinline__ void issue_stage_loads(uint8_t *stg, const DecodePara
 // ---------------------------------------------------------------------------
 // 2. split kernel
 // ---------------------------------------------------------------------------
-template <int D, bool INT8>
-__global__ void __launch_bounds__(288, 1) decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
+template <int D, bool INT8, int MINB>
+__global__ void __launch_bounds__(288, MINB) decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
                                                               const __grid_constant__ CUtensorMap v_map,
                                                               const __grid_constant__ CUtensorMap ks_map,
                                                               const __grid_constant__ CUtensorMap vs_map,
@@ -602,6 +614,10 @@ __global__ void __launch_bounds__(288, 1) decode_split_kernel(const __grid_const
     const int mi = lane >> 3, ri = lane & 7;  // ldmatrix matrix index / row within it
     float acc[KSTEPS][4];                     // O^T accumulators: rows d, columns query heads
     float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    // int8 pages: bias corrections of this lane's columns n0 = 2qd, n1 = 2qd + 1
+    // (qb: 1152 * sum_d q_d of the piece's query heads; ps: running sum of
+    // the fp16 P' fed to the P V product, rescaled with acc)
+    float qb0 = 0.f, qb1 = 0.f, ps0 = 0.f, ps1 = 0.f;
     uint32_t stage_it = 0, item_it = 0;
     const uint32_t half_bytes = (uint32_t)hpc * kStageTokens * 128u;
 
@@ -665,6 +681,35 @@ __global__ void __launch_bounds__(288, 1) decode_split_kernel(const __grid_const
                 }
                 __syncwarp();
             }
+            if (INT8) {
+                // sum_d q_d of the fp16 query rows of columns n0, n1 (padding
+                // columns read row 0): lane (g, qd) adds its share of the
+                // chunks (the swizzle only permutes chunks within a row)
+                constexpr int CPR = D / 8;
+                const int r0 = 2 * qd < G ? 2 * qd : 0, r1 = 2 * qd + 1 < G ? 2 * qd + 1 : 0;
+                float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+                for (int c = g; c < CPR; c += 8) {
+                    const uint4 x0 = *reinterpret_cast<const uint4 *>(qrows + (r0 * CPR + c) * 16);
+                    const uint4 x1 = *reinterpret_cast<const uint4 *>(qrows + (r1 * CPR + c) * 16);
+                    const uint32_t w0[4] = {x0.x, x0.y, x0.z, x0.w}, w1[4] = {x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&w0[k]));
+                        const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&w1[k]));
+                        a0 += f0.x + f0.y;
+                        a1 += f1.x + f1.y;
+                    }
+                }
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    a0 += __shfl_xor_sync(0xffffffffu, a0, off);
+                    a1 += __shfl_xor_sync(0xffffffffu, a1, off);
+                }
+                qb0 = kCodeBias * a0;
+                qb1 = kCodeBias * a1;
+                ps0 = ps1 = 0.f;
+            }
 #pragma unroll
             for (int mt = 0; mt < KSTEPS; ++mt) acc[mt][0] = acc[mt][1] = acc[mt][2] = acc[mt][3] = 0.f;
             m0 = m1 = -INFINITY;
@@ -720,6 +765,39 @@ __global__ void __launch_bounds__(288, 1) decode_split_kernel(const __grid_const
                     }
                 }
             }
+            // int8: V codes for O^T += V^T P^T, loaded and converted (biased) up
+            // front so the conversion overlaps the K Q^T chain.  Lane (g, qd) holds
+            // the D/8 codes d = g * D/8 .. of tokens 2qd, 2qd+1, 2qd+8, 2qd+9;
+            // O^T rows are relabelled: m-tile mt row g is d = g * D/8 + 2 mt and
+            // row g + 8 is the next d, so byte pairs of two token rows interleave
+            // (prmt) into the A fragments.
+            uint32_t va[INT8 ? KSTEPS : 1][4];
+            if constexpr (INT8) {
+                uint32_t vw[4][D / 32];
+#pragma unroll
+                for (int t4 = 0; t4 < 4; ++t4) {
+                    const int tok = 2 * qd + (t4 & 1) + 8 * (t4 >> 1);
+                    if (D == 128) {
+                        const uint4 x = *reinterpret_cast<const uint4 *>(kcodes + p.kv_tile_bytes + swz(tok, g));
+                        vw[t4][0] = x.x;
+                        vw[t4][1] = x.y;
+                        vw[t4][2] = x.z;
+                        vw[t4][3] = x.w;
+                    } else {
+                        const uint2 x = *reinterpret_cast<const uint2 *>(kcodes + p.kv_tile_bytes + tok * D + g * 8);
+                        vw[t4][0] = x.x;
+                        vw[t4][1] = x.y;
+                    }
+                }
+#pragma unroll
+                for (int mt = 0; mt < KSTEPS; ++mt) {
+                    const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
+                    int8x4_to_biased_half2x2(__byte_perm(vw[0][mt / 2], vw[1][mt / 2], sel), va[mt][0], va[mt][1]);
+                    int8x4_to_biased_half2x2(__byte_perm(vw[2][mt / 2], vw[3][mt / 2], sel), va[mt][2], va[mt][3]);
+                }
+            }
+            // K Q^T; int8 pages in two accumulator chains (even and odd k-steps)
+            float s4b[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int kk = 0; kk < KSTEPS; kk += 2) {
                 uint32_t qb[4];  // b0, b1 of k-step kk, then of kk + 1
@@ -728,10 +806,10 @@ __global__ void __launch_bounds__(288, 1) decode_split_kernel(const __grid_const
                 for (int k2 = 0; k2 < 2; ++k2) {
                     const int k = kk + k2;
                     uint32_t a[4];
-                    if (INT8) {
-                        int8x4_to_half2x2(kw[0][k], a[0], a[2]);
-                        int8x4_to_half2x2(kw[1][k], a[1], a[3]);
-                        mma_f16_16816(s4, a, qb[2 * k2], qb[2 * k2 + 1]);
+                    if constexpr (INT8) {
+                        int8x4_to_biased_half2x2(kw[0][k], a[0], a[2]);
+                        int8x4_to_biased_half2x2(kw[1][k], a[1], a[3]);
+                        mma_f16_16816(k2 ? s4b : s4, a, qb[2 * k2], qb[2 * k2 + 1]);
                     } else {
                         const int tok = ri + 8 * (mi & 1);
                         const uint32_t chunk = (uint32_t)((k % 4) * 2 + (mi >> 1));
@@ -740,12 +818,22 @@ __global__ void __launch_bounds__(288, 1) decode_split_kernel(const __grid_const
                     }
                 }
             }
-            // scale to log2 units, dequantise K (int8), mask tokens past the context
+            // scale to log2 units, dequantise K (int8: remove the code bias
+            // 1152 sum_d q_d first), mask tokens past the context
             const bool v0 = g < nv, v1 = g + 8 < nv;
-            float x0 = v0 ? s4[0] * sk0 * p.scale_log2 : -INFINITY;
-            float x1 = v0 ? s4[1] * sk0 * p.scale_log2 : -INFINITY;
-            float x2 = v1 ? s4[2] * sk1 * p.scale_log2 : -INFINITY;
-            float x3 = v1 ? s4[3] * sk1 * p.scale_log2 : -INFINITY;
+            float x0, x1, x2, x3;
+            if constexpr (INT8) {
+                const float c0 = sk0 * p.scale_log2, c1 = sk1 * p.scale_log2;
+                x0 = v0 ? ((s4[0] + s4b[0]) - qb0) * c0 : -INFINITY;
+                x1 = v0 ? ((s4[1] + s4b[1]) - qb1) * c0 : -INFINITY;
+                x2 = v1 ? ((s4[2] + s4b[2]) - qb0) * c1 : -INFINITY;
+                x3 = v1 ? ((s4[3] + s4b[3]) - qb1) * c1 : -INFINITY;
+            } else {
+                x0 = v0 ? s4[0] * p.scale_log2 : -INFINITY;
+                x1 = v0 ? s4[1] * p.scale_log2 : -INFINITY;
+                x2 = v1 ? s4[2] * p.scale_log2 : -INFINITY;
+                x3 = v1 ? s4[3] * p.scale_log2 : -INFINITY;
+            }
             float bm0 = fmaxf(x0, x2), bm1 = fmaxf(x1, x3);
 #pragma unroll
             for (int off = 4; off < 32; off <<= 1) {
@@ -768,54 +856,34 @@ __global__ void __launch_bounds__(288, 1) decode_split_kernel(const __grid_const
                     acc[mt][2] *= al0;
                     acc[mt][3] *= al1;
                 }
+                ps0 *= al0;
+                ps1 *= al1;
             }
-            // P^T as the B operand of O^T += V^T P^T (int8: fold the V scale into P)
+            // P^T as the B operand of O^T += V^T P^T (int8: fold the V scale into
+            // P, and add the fp16 P' actually used to the bias correction's sum)
             uint32_t pb0, pb1;
-            if (INT8) {
-                pb0 = movmatrix_trans(pack_f16x2(v0 ? p0 * sv0 : 0.f, v0 ? p1 * sv0 : 0.f));
-                pb1 = movmatrix_trans(pack_f16x2(v1 ? p2 * sv1 : 0.f, v1 ? p3 * sv1 : 0.f));
+            if constexpr (INT8) {
+                const uint32_t pk0 = pack_f16x2(v0 ? p0 * sv0 : 0.f, v0 ? p1 * sv0 : 0.f);
+                const uint32_t pk1 = pack_f16x2(v1 ? p2 * sv1 : 0.f, v1 ? p3 * sv1 : 0.f);
+                const float2 f0 = __half22float2(*reinterpret_cast<const __half2 *>(&pk0));
+                const float2 f1 = __half22float2(*reinterpret_cast<const __half2 *>(&pk1));
+                ps0 += f0.x + f1.x;
+                ps1 += f0.y + f1.y;
+                pb0 = movmatrix_trans(pk0);
+                pb1 = movmatrix_trans(pk1);
+#pragma unroll
+                for (int mt = 0; mt < KSTEPS; ++mt) mma_f16_16816(acc[mt], va[mt], pb0, pb1);
             } else {
                 pb0 = movmatrix_trans(pack_bf16x2(p0, p1));
                 pb1 = movmatrix_trans(pack_bf16x2(p2, p3));
-            }
-            // V rows past the context may hold anything (even NaN): zero them in the
-            // A fragments of a partial stage so 0 * NaN never reaches the sum.
-            uint32_t vmask0 = 0xffffffffu, vmask1 = 0xffffffffu;
-            if (!INT8 && nv < kStageTokens) {
-                const int ta = 2 * qd, tb = 2 * qd + 8;
-                vmask0 = (ta < nv ? 0x0000ffffu : 0u) | (ta + 1 < nv ? 0xffff0000u : 0u);
-                vmask1 = (tb < nv ? 0x0000ffffu : 0u) | (tb + 1 < nv ? 0xffff0000u : 0u);
-            }
-            if (INT8) {
-                // lane (g, qd) holds the D/8 codes d = g * D/8 .. of tokens 2qd, 2qd+1,
-                // 2qd+8, 2qd+9.  O^T rows are relabelled: m-tile mt row g is
-                // d = g * D/8 + 2 mt and row g + 8 is the next d, so byte pairs of
-                // two token rows interleave (prmt) into the A fragments.
-                uint32_t vw[4][D / 32];
-#pragma unroll
-                for (int t4 = 0; t4 < 4; ++t4) {
-                    const int tok = 2 * qd + (t4 & 1) + 8 * (t4 >> 1);
-                    if (D == 128) {
-                        const uint4 x = *reinterpret_cast<const uint4 *>(kcodes + p.kv_tile_bytes + swz(tok, g));
-                        vw[t4][0] = x.x;
-                        vw[t4][1] = x.y;
-                        vw[t4][2] = x.z;
-                        vw[t4][3] = x.w;
-                    } else {
-                        const uint2 x = *reinterpret_cast<const uint2 *>(kcodes + p.kv_tile_bytes + tok * D + g * 8);
-                        vw[t4][0] = x.x;
-                        vw[t4][1] = x.y;
-                    }
+                // V rows past the context may hold anything (even NaN): zero them in
+                // the A fragments of a partial stage so 0 * NaN never reaches the sum.
+                uint32_t vmask0 = 0xffffffffu, vmask1 = 0xffffffffu;
+                if (nv < kStageTokens) {
+                    const int ta = 2 * qd, tb = 2 * qd + 8;
+                    vmask0 = (ta < nv ? 0x0000ffffu : 0u) | (ta + 1 < nv ? 0xffff0000u : 0u);
+                    vmask1 = (tb < nv ? 0x0000ffffu : 0u) | (tb + 1 < nv ? 0xffff0000u : 0u);
                 }
-#pragma unroll
-                for (int mt = 0; mt < KSTEPS; ++mt) {
-                    const uint32_t sel = (mt & 1) ? 0x7362u : 0x5140u;
-                    uint32_t a[4];
-                    int8x4_to_half2x2(__byte_perm(vw[0][mt / 2], vw[1][mt / 2], sel), a[0], a[1]);
-                    int8x4_to_half2x2(__byte_perm(vw[2][mt / 2], vw[3][mt / 2], sel), a[2], a[3]);
-                    mma_f16_16816(acc[mt], a, pb0, pb1);
-                }
-            } else {
 #pragma unroll
                 for (int mt = 0; mt < KSTEPS; ++mt) {
                     const int tok = ri + 8 * (mi >> 1);
@@ -829,6 +897,7 @@ __global__ void __launch_bounds__(288, 1) decode_split_kernel(const __grid_const
                     mma_bf16_16816(acc[mt], a, pb0, pb1);
                 }
             }
+            (void)va;
         }
 
         // the stage's tiles (and, at a piece's end, its query rows) are no longer
@@ -846,6 +915,23 @@ __global__ void __launch_bounds__(288, 1) decode_split_kernel(const __grid_const
             for (int off = 4; off < 32; off <<= 1) {
                 L0 += __shfl_xor_sync(0xffffffffu, L0, off);
                 L1 += __shfl_xor_sync(0xffffffffu, L1, off);
+            }
+            if constexpr (INT8) {
+                // remove the code bias: O^T = (V + 1152)^T P'^T - 1152 sum_t P'_t
+                float P0 = ps0, P1 = ps1;
+#pragma unroll
+                for (int off = 4; off < 32; off <<= 1) {
+                    P0 += __shfl_xor_sync(0xffffffffu, P0, off);
+                    P1 += __shfl_xor_sync(0xffffffffu, P1, off);
+                }
+                const float B0 = kCodeBias * P0, B1 = kCodeBias * P1;
+#pragma unroll
+                for (int mt = 0; mt < KSTEPS; ++mt) {
+                    acc[mt][0] -= B0;
+                    acc[mt][1] -= B1;
+                    acc[mt][2] -= B0;
+                    acc[mt][3] -= B1;
+                }
             }
             const int32_t s = meta.seq;
             const int32_t kvh = meta.head_group * hpc + warp;
@@ -1084,7 +1170,7 @@ cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream, 
     p.n_stages = stages;
     const size_t smem = fixed + (size_t)stages * p.stage_bytes;
 
-    auto kern = decode_split_kernel<D, INT8>;
+    auto kern = env_int("PKV_DECODE_LB", 1) == 2 ? decode_split_kernel<D, INT8, 2> : decode_split_kernel<D, INT8, 1>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int threads = 32 * (hpc + 1);
@@ -1104,7 +1190,7 @@ cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream, 
     if (write && write->n_seqs > 0 && write->n_new > 0) {
         wa = *write;
         write_mode = INT8 ? 2 : 1;
-        const int64_t units = INT8 ? (int64_t)wa.n_seqs * wa.n_new * d.n_kv_heads * 2 / 32
+        const int64_t units = INT8 ? ((int64_t)wa.n_seqs * wa.n_new * 2 * ((d.n_kv_heads + 3) / 4) + 31) / 32
                                    : (int64_t)wa.n_seqs * wa.n_new * (d.n_kv_heads * D / 8) / 1024;
         write_ctas = (int)(units < 1 ? 1 : (units > 2 * num_sms ? 2 * num_sms : units));
     }

@@ -19,7 +19,8 @@ __global__ void __launch_bounds__(256) write_bf16_kernel(const WriteArgs a)
     write_bf16_vectors(a, (int64_t)blockIdx.x * blockDim.x + threadIdx.x, (int64_t)gridDim.x * blockDim.x);
 }
 
-// Quantised write: one (token, kv head, K or V) row per warp (write_rows.cuh).
+// Quantised write: four kv heads of one token's K or V row per warp unit
+// (write_rows.cuh).
 template <int EPL>
 __global__ void __launch_bounds__(256) write_int8_kernel(const WriteArgs a, float *k_scales, float *v_scales)
 {
@@ -140,13 +141,13 @@ cudaError_t launch_write_bf16(const WriteArgs &a, cudaStream_t stream)
 
 cudaError_t launch_write_int8(const WriteArgs &a, float *k_scales, float *v_scales, cudaStream_t stream)
 {
-    const int64_t n_units = (int64_t)a.n_seqs * a.n_new * a.dims.n_kv_heads * 2;
+    const int64_t n_units = (int64_t)a.n_seqs * a.n_new * 2 * ((a.dims.n_kv_heads + 3) / 4);
     int64_t grid = (n_units + 7) / 8;
     if (grid > 4096) grid = 4096;
     if (a.dims.head_dim == 128)
-        write_int8_kernel<4><<<(unsigned)grid, 256, 0, stream>>>(a, k_scales, v_scales);
+        write_int8_kernel<16><<<(unsigned)grid, 256, 0, stream>>>(a, k_scales, v_scales);
     else
-        write_int8_kernel<2><<<(unsigned)grid, 256, 0, stream>>>(a, k_scales, v_scales);
+        write_int8_kernel<8><<<(unsigned)grid, 256, 0, stream>>>(a, k_scales, v_scales);
     return cudaGetLastError();
 }
 

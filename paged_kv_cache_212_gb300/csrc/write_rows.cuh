@@ -58,51 +58,64 @@ __device__ __forceinline__ void write_bf16_vectors(const WriteArgs &a, int64_t f
     }
 }
 
-// Symmetric int8 quantisation, one (token, kv head, K or V) row per warp, in
-// IEEE binary32 with round-to-nearest-even (libmir-metal paged/mod.rs,
-// KvPageFormat::Int8PerTokenHead): amax by a warp max-reduction, scale =
-// amax / 127 (correctly rounded division), code = clamp(rint(x / scale),
-// -127, 127).  Warps take units first, first + stride, ...; EPL = head_dim / 32.
+// Symmetric int8 quantisation in IEEE binary32 with round-to-nearest-even
+// (libmir-metal paged/mod.rs, KvPageFormat::Int8PerTokenHead): per (token,
+// kv head) row of K or of V, amax by a max-reduction, scale = amax / 127
+// (correctly rounded division), code = clamp(rint(x / scale), -127, 127).
+//
+// A warp unit is four kv heads of one token's K or V row: eight lanes per
+// head, each lane holding EPL = head_dim / 8 consecutive elements.  The
+// unit's new rows are loaded before the table lookup (position, then table
+// entry: two dependent loads), so the three loads overlap.  Warps take units
+// first, first + stride, ...; unit = (row * 2 + K/V) * head_quads + quad.
 template <int EPL>
 __device__ __forceinline__ void write_int8_units(const WriteArgs &a, float *k_scales, float *v_scales,
                                                  int64_t first, int64_t stride)
 {
-    constexpr int D = EPL * 32;
+    constexpr int D = EPL * 8;
+    constexpr int VECS = EPL / 8;                      // 16-byte vectors of bf16 per lane
     const int lane = threadIdx.x & 31;
     const int32_t hkv = a.dims.n_kv_heads;
-    const int64_t n_units = (int64_t)a.n_seqs * a.n_new * hkv * 2;
-    // unit = ((s * n_new + j) * n_kv_heads + h) * 2 + (0: K, 1: V)
+    const int32_t quads = (hkv + 3) / 4;
+    const int64_t n_units = (int64_t)a.n_seqs * a.n_new * 2 * quads;
     for (int64_t u = first; u < n_units; u += stride) {
-        const int which = (int)(u & 1);
-        const int64_t rh = u >> 1;
-        const int32_t h = (int32_t)(rh % hkv);
-        const int64_t r = rh / hkv;
+        const int32_t quad = (int32_t)(u % quads);
+        const int64_t rw = u / quads;
+        const int which = (int)(rw & 1);
+        const int64_t r = rw >> 1;                     // r = s * n_new + j
+        const int32_t h = quad * 4 + (lane >> 3);
+        const bool active = h < hkv;
+        const int32_t part = lane & 7;                 // elements [part * EPL, (part + 1) * EPL) of the row
+        float x[EPL];
+        if (active) {
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                static_cast<const __nv_bfloat16 *>(which ? a.v_new : a.k_new) + (r * hkv + h) * D + part * EPL);
+#pragma unroll
+            for (int v = 0; v < VECS; ++v) {
+                const uint4 raw = __ldcs(src + v);
+                const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const __nv_bfloat162 p2 = *reinterpret_cast<const __nv_bfloat162 *>(&w4[k]);
+                    x[8 * v + 2 * k] = __low2float(p2);
+                    x[8 * v + 2 * k + 1] = __high2float(p2);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < EPL; ++e) x[e] = 0.0f;
+        }
         const int64_t s = r / a.n_new;
         const int64_t t = (int64_t)__ldg(a.start_pos + s) + (r - s * a.n_new);
         const int64_t row = pool_row_of(a.tables + s * a.max_blocks, a.max_blocks, a.dims.n_blocks,
-                                        a.dims.block_size, t, lane == 0 && which == 0 && h == 0 ? a.dev_status : nullptr);
-        if (row < 0) continue;
-        const __nv_bfloat16 *src = static_cast<const __nv_bfloat16 *>(which ? a.v_new : a.k_new) + rh * D + lane * EPL;
-        float x[EPL];
-        if constexpr (EPL == 4) {
-            uint2 raw = __ldcs(reinterpret_cast<const uint2 *>(src));
-            __nv_bfloat162 p0 = *reinterpret_cast<__nv_bfloat162 *>(&raw.x);
-            __nv_bfloat162 p1 = *reinterpret_cast<__nv_bfloat162 *>(&raw.y);
-            x[0] = __low2float(p0);
-            x[1] = __high2float(p0);
-            x[2] = __low2float(p1);
-            x[3] = __high2float(p1);
-        } else {
-            uint32_t raw = __ldcs(reinterpret_cast<const unsigned int *>(src));
-            __nv_bfloat162 p0 = *reinterpret_cast<__nv_bfloat162 *>(&raw);
-            x[0] = __low2float(p0);
-            x[1] = __high2float(p0);
-        }
+                                        a.dims.block_size, t,
+                                        lane == 0 && which == 0 && quad == 0 ? a.dev_status : nullptr);
+        if (row < 0) continue;                         // the same token for the whole warp
         float amax = 0.0f;
 #pragma unroll
         for (int e = 0; e < EPL; ++e) amax = fmaxf(amax, fabsf(x[e]));
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        for (int off = 1; off < 8; off <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
         const float scale = __fdiv_rn(amax, 127.0f);
         // code = rint(fl(x / scale)) without a division per element: with the
         // correctly rounded reciprocal rcp = fl(1 / scale) (scale normal), the
@@ -122,25 +135,30 @@ __device__ __forceinline__ void write_int8_units(const WriteArgs &a, float *k_sc
             c[e] = __float2int_rn(q);
             need_div |= !(fast && fabsf(frac - 0.5f) > 3.0e-5f);
         }
-        if (__any_sync(0xffffffffu, need_div && amax != 0.0f)) {    // rare: a (near-)tie in the warp's row
+        if (__any_sync(0xffffffffu, need_div && amax != 0.0f)) {    // rare: a (near-)tie in the warp's rows
 #pragma unroll
             for (int e = 0; e < EPL; ++e) {
                 const float q = __fmul_rn(x[e], rcp);
                 if (!(fast && fabsf(q - floorf(q) - 0.5f) > 3.0e-5f)) c[e] = __float2int_rn(__fdiv_rn(x[e], scale));
             }
         }
-        uint32_t packed = 0;
+        if (!active) continue;
+        uint32_t packed[EPL / 4];
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) {
-            const int ce = amax != 0.0f ? max(-127, min(127, c[e])) : 0;
-            packed |= (uint32_t)(ce & 0xff) << (8 * e);
+        for (int w = 0; w < EPL / 4; ++w) {
+            packed[w] = 0;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int ce = amax != 0.0f ? max(-127, min(127, c[4 * w + k])) : 0;
+                packed[w] |= (uint32_t)(ce & 0xff) << (8 * k);
+            }
         }
-        int8_t *dst = static_cast<int8_t *>(which ? a.v_pool : a.k_pool) + (row * hkv + h) * D + lane * EPL;
-        if constexpr (EPL == 4)
-            *reinterpret_cast<uint32_t *>(dst) = packed;
+        int8_t *dst = static_cast<int8_t *>(which ? a.v_pool : a.k_pool) + (row * hkv + h) * D + part * EPL;
+        if constexpr (EPL == 16)
+            *reinterpret_cast<uint4 *>(dst) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
         else
-            *reinterpret_cast<uint16_t *>(dst) = (uint16_t)packed;
-        if (lane == 0) (which ? v_scales : k_scales)[row * hkv + h] = scale;
+            *reinterpret_cast<uint2 *>(dst) = make_uint2(packed[0], packed[1]);
+        if (part == 0) (which ? v_scales : k_scales)[row * hkv + h] = scale;
     }
 }
 
