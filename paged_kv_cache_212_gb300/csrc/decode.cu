@@ -428,8 +428,12 @@ __device__ __forceinline__ void issue_stage_loads(uint8_t *stg, const DecodePara
 // ---------------------------------------------------------------------------
 // 2. split kernel
 // ---------------------------------------------------------------------------
-template <int D, bool INT8, int MINB>
-__global__ void __launch_bounds__(288, MINB) decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
+// Register budget (measured on GB300): bf16 pages compile for two resident
+// CTAs per SM (at most ~112 registers; fewer registers measured faster even at
+// one CTA per SM), int8 pages for one (the fp16 fragments of the in-register
+// code conversion need ~168 registers; the two-CTA budget spills).
+template <int D, bool INT8>
+__global__ void __launch_bounds__(288, INT8 ? 1 : 2) decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
                                                               const __grid_constant__ CUtensorMap v_map,
                                                               const __grid_constant__ CUtensorMap ks_map,
                                                               const __grid_constant__ CUtensorMap vs_map,
@@ -461,34 +465,40 @@ __global__ void __launch_bounds__(288, MINB) decode_split_kernel(const __grid_co
     volatile int32_t *abort_flag = L.abort_flag;
 
     if (warp == hpc) {
-        // ===================== producer warp =====================
-        if (lane == 0) {
-            prefetch_tensormap(&k_map);
-            prefetch_tensormap(&v_map);
-            if (INT8) {
-                prefetch_tensormap(&ks_map);
-                prefetch_tensormap(&vs_map);
-            }
+        // ===================== producer (one thread) =====================
+        // Lane 0 alone walks the work list and issues the copies: no per-stage
+        // warp shuffles or divergent branches, ring position and block
+        // position advanced by counters, the next table entry loaded one stage
+        // ahead of its use.
+        if (lane != 0) return;
+        prefetch_tensormap(&k_map);
+        prefetch_tensormap(&v_map);
+        if (INT8) {
+            prefetch_tensormap(&ks_map);
+            prefetch_tensormap(&vs_map);
         }
-        uint32_t stage_it = 0, item_it = 0;
-        uint32_t next = 0;
-        if (lane == 0) next = atomicAdd(&p.ws.header[kHdrCounter], 1u);
-        next = __shfl_sync(0xffffffffu, next, 0);
+        uint32_t st = 0, phase = 0;          // ring slot and its parity
+        uint32_t item_it = 0;
         bool ok = true;
         const bool balanced = p.split_tokens == 0;
         const int32_t chunk = (int32_t)p.ws.header[kHdrChunk];
         const int32_t total_stages = (int32_t)p.ws.header[kHdrStages];
-        while (ok && next < total_items) {
-            const uint32_t it = next;
-            if (lane == 0) next = atomicAdd(&p.ws.header[kHdrCounter], 1u);
+        // Balanced items are all the same size and number at most the grid:
+        // CTA b takes units b, b + grid, ...  Fixed splits differ in size: a
+        // CTA takes the next unit from the counter when it starts one (no id
+        // is taken ahead, which would let early CTAs hold two units while late
+        // ones get none).
+        uint32_t it = balanced ? blockIdx.x : atomicAdd(&p.ws.header[kHdrCounter], 1u);
+        for (; ok && it < total_items;
+             it = balanced ? it + gridDim.x : atomicAdd(&p.ws.header[kHdrCounter], 1u)) {
             const int32_t item = (int32_t)(it / p.n_hg), hg = (int32_t)(it % p.n_hg);
             // balanced: the item is the stage range [g0, g1) of the concatenated sequences
-            int32_t g0 = 0, g1 = 0, s = 0;
+            int32_t g0 = 0, g1 = 0, sq = 0;
             int2 fixed_sk = make_int2(0, 0);
             if (balanced) {
                 g0 = item * chunk;
                 g1 = min(g0 + chunk, total_stages);
-                s = __ldg(&p.ws.items[item].x);
+                sq = __ldg(&p.ws.items[item].x);
             } else {
                 fixed_sk = __ldg(&p.ws.items[item]);
             }
@@ -497,21 +507,21 @@ __global__ void __launch_bounds__(288, MINB) decode_split_kernel(const __grid_co
                 // the next piece: sequence, token range, partial slot, pieces of that sequence
                 int32_t seq, t0, t1, slot, n_pieces;
                 if (balanced) {
-                    int32_t pre = __ldg(p.ws.seq_prefix + s), pre1 = __ldg(p.ws.seq_prefix + s + 1);
+                    int32_t pre = __ldg(p.ws.seq_prefix + sq), pre1 = __ldg(p.ws.seq_prefix + sq + 1);
                     while (pre1 == pre) {  // sequences without tokens
-                        ++s;
+                        ++sq;
                         pre = pre1;
-                        pre1 = __ldg(p.ws.seq_prefix + s + 1);
+                        pre1 = __ldg(p.ws.seq_prefix + sq + 1);
                     }
                     const int32_t e = min(g1, pre1);
-                    seq = s;
+                    seq = sq;
                     t0 = (g0 - pre) * kStageTokens;
-                    t1 = min((e - pre) * kStageTokens, __ldg(p.ctx_lens + s));
-                    const int2 sg = __ldg(p.ws.seg + s);
+                    t1 = min((e - pre) * kStageTokens, __ldg(p.ctx_lens + sq));
+                    const int2 sg = __ldg(p.ws.seg + sq);
                     slot = sg.x + (item - pre / chunk);
                     n_pieces = sg.y;
                     g0 = e;
-                    ++s;
+                    ++sq;
                     more = g0 < g1;
                 } else {
                     seq = fixed_sk.x;
@@ -523,74 +533,73 @@ __global__ void __launch_bounds__(288, MINB) decode_split_kernel(const __grid_co
                 }
                 const bool final_out = n_pieces == 1;
                 const int32_t *trow = p.tables + (int64_t)seq * p.max_blocks;
-                const int32_t blk0 = t0 / p.block_size;
                 // this piece's queries: heads [hg*hpc*G, (hg+1)*hpc*G) of sequence seq
                 const uint32_t qs = item_it & 1u;
-                if (lane == 0) {
-                    if (!mbar_wait(&L.qempty_bar[qs], ((item_it >> 1) & 1u) ^ 1u, abort_flag)) {
+                if (!mbar_wait(&L.qempty_bar[qs], ((item_it >> 1) & 1u) ^ 1u, abort_flag)) {
+                    report(p.dev_status, PKV_DEV_TIMEOUT);
+                    *abort_flag = 1;
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&L.qfull_bar[qs], p.q_slot_bytes);
+                bulk_g2s(L.q_slots + qs * p.q_slot_bytes,
+                         p.q + ((int64_t)seq * p.n_q_heads + (int64_t)hg * hpc * p.group) * D, p.q_slot_bytes,
+                         &L.qfull_bar[qs]);
+                // block position of t0, and its table entry; later entries are
+                // loaded one stage ahead
+                int32_t lb = t0 / p.block_size, off = t0 - lb * p.block_size;
+                int32_t blk = lb < p.max_blocks ? __ldg(trow + lb) : -1;
+                for (int32_t t = t0; t < t1; t += kStageTokens) {
+                    const bool last_of_block = off + kStageTokens >= p.block_size;
+                    const bool more_stages = t + kStageTokens < t1;
+                    int32_t blk_next = blk;
+                    if (last_of_block && more_stages) blk_next = lb + 1 < p.max_blocks ? __ldg(trow + lb + 1) : -1;
+                    if (!mbar_wait(&L.empty_bar[st], phase ^ 1u, abort_flag)) {
                         report(p.dev_status, PKV_DEV_TIMEOUT);
                         *abort_flag = 1;
+                        ok = false;
+                        break;
                     }
-                    if (!*abort_flag) {
-                        mbar_arrive_expect_tx(&L.qfull_bar[qs], p.q_slot_bytes);
-                        bulk_g2s(L.q_slots + qs * p.q_slot_bytes,
-                                 p.q + ((int64_t)seq * p.n_q_heads + (int64_t)hg * hpc * p.group) * D,
-                                 p.q_slot_bytes, &L.qfull_bar[qs]);
+                    StageMeta m;
+                    m.seq = seq;
+                    m.split_index = slot;
+                    m.n_valid = min(kStageTokens, t1 - t);
+                    m.flags = (t == t0 ? kMetaFirst : 0) | (more_stages ? 0 : kMetaLast) | (final_out ? kMetaFinal : 0);
+                    m.head_group = hg;
+                    m.n_splits = n_pieces;
+                    const bool bad = blk < 0 || blk > p.n_blocks;
+                    if (bad) {
+                        m.flags |= kMetaBad;
+                        report(p.dev_status, PKV_DEV_BAD_BLOCK_ID);
                     }
-                }
-                ok = !__shfl_sync(0xffffffffu, *abort_flag, 0);
-                int32_t tbl = 0, tbl_base = -1;
-                for (int32_t t = t0; ok && t < t1; t += kStageTokens) {
-                    const int32_t lb = t / p.block_size;
-                    if (lb - blk0 >= tbl_base + 32 || tbl_base < 0) {
-                        tbl_base = lb - blk0;
-                        const int32_t j = blk0 + tbl_base + lane;
-                        tbl = j < p.max_blocks ? __ldg(trow + j) : -1;
+                    L.meta[st] = m;
+                    if (bad) {
+                        mbar_arrive(&L.full_bar[st]);
+                    } else {
+                        uint8_t *stg = L.stages + (size_t)st * p.stage_bytes;
+                        const int32_t row0 = blk * p.block_size + off;
+                        mbar_arrive_expect_tx(&L.full_bar[st], p.tx_bytes);
+                        issue_stage_loads<D, INT8>(stg, p, k_map, v_map, ks_map, vs_map, row0, hg * hpc,
+                                                   &L.full_bar[st]);
                     }
-                    const int32_t blk = __shfl_sync(0xffffffffu, tbl, lb - blk0 - tbl_base);
-                    if (lane == 0) {
-                        const uint32_t st = stage_it % p.n_stages;
-                        if (!mbar_wait(&L.empty_bar[st], ((stage_it / p.n_stages) & 1u) ^ 1u, abort_flag)) {
-                            report(p.dev_status, PKV_DEV_TIMEOUT);
-                            *abort_flag = 1;
-                        } else {
-                            StageMeta m;
-                            m.seq = seq;
-                            m.split_index = slot;
-                            m.n_valid = min(kStageTokens, t1 - t);
-                            m.flags = (t == t0 ? kMetaFirst : 0) | (t + kStageTokens >= t1 ? kMetaLast : 0) |
-                                      (final_out ? kMetaFinal : 0);
-                            m.head_group = hg;
-                            m.n_splits = n_pieces;
-                            const bool bad = blk < 0 || blk > p.n_blocks;
-                            if (bad) {
-                                m.flags |= kMetaBad;
-                                report(p.dev_status, PKV_DEV_BAD_BLOCK_ID);
-                            }
-                            L.meta[st] = m;
-                            if (bad) {
-                                mbar_arrive(&L.full_bar[st]);
-                            } else {
-                                uint8_t *stg = L.stages + (size_t)st * p.stage_bytes;
-                                const int32_t row0 = blk * p.block_size + (t % p.block_size);
-                                const int32_t head0 = hg * hpc;
-                                mbar_arrive_expect_tx(&L.full_bar[st], p.tx_bytes);
-                                issue_stage_loads<D, INT8>(stg, p, k_map, v_map, ks_map, vs_map, row0, head0,
-                                                           &L.full_bar[st]);
-                            }
-                        }
+                    if (++st == (uint32_t)p.n_stages) {
+                        st = 0;
+                        phase ^= 1u;
                     }
-                    ok = !__shfl_sync(0xffffffffu, *abort_flag, 0);
-                    ++stage_it;
+                    if (last_of_block) {
+                        ++lb;
+                        off = 0;
+                        blk = blk_next;
+                    } else {
+                        off += kStageTokens;
+                    }
                 }
                 ++item_it;
             }
-            next = __shfl_sync(0xffffffffu, next, 0);
         }
         // stop marker
-        if (lane == 0 && !*abort_flag) {
-            const uint32_t st = stage_it % p.n_stages;
-            if (mbar_wait(&L.empty_bar[st], ((stage_it / p.n_stages) & 1u) ^ 1u, abort_flag)) {
+        if (ok && !*abort_flag) {
+            if (mbar_wait(&L.empty_bar[st], phase ^ 1u, abort_flag)) {
                 L.meta[st].flags = kMetaStop;
                 mbar_arrive(&L.full_bar[st]);
             } else {
@@ -598,11 +607,18 @@ __global__ void __launch_bounds__(288, MINB) decode_split_kernel(const __grid_co
                 *abort_flag = 1;
             }
         }
-        if (lane == 0 && *abort_flag) {
+        if (*abort_flag) {
             // wind down: let every load already issued land before the CTA exits
-            const uint32_t first = stage_it > (uint32_t)p.n_stages ? stage_it - p.n_stages : 0;
-            for (uint32_t i = first; i < stage_it; ++i)
-                (void)mbar_wait(&L.full_bar[i % p.n_stages], (i / p.n_stages) & 1u);
+            // (the last n_stages slots, in issue order)
+            uint32_t ws_ = st, wp = phase;
+            for (int i = 0; i < p.n_stages; ++i) {
+                if (ws_ == 0) {
+                    ws_ = (uint32_t)p.n_stages;
+                    wp ^= 1u;
+                }
+                --ws_;
+                (void)mbar_wait(&L.full_bar[ws_], wp);
+            }
         }
         return;
     }
@@ -618,12 +634,11 @@ __global__ void __launch_bounds__(288, MINB) decode_split_kernel(const __grid_co
     // (qb: 1152 * sum_d q_d of the piece's query heads; ps: running sum of
     // the fp16 P' fed to the P V product, rescaled with acc)
     float qb0 = 0.f, qb1 = 0.f, ps0 = 0.f, ps1 = 0.f;
-    uint32_t stage_it = 0, item_it = 0;
+    uint32_t st = 0, phase = 0, item_it = 0;   // ring slot and its parity
     const uint32_t half_bytes = (uint32_t)hpc * kStageTokens * 128u;
 
     while (true) {
-        const uint32_t st = stage_it % p.n_stages;
-        if (!__all_sync(0xffffffffu, mbar_wait(&L.full_bar[st], (stage_it / p.n_stages) & 1u, abort_flag))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&L.full_bar[st], phase, abort_flag))) {
             if (lane == 0) report(p.dev_status, PKV_DEV_TIMEOUT);
             *abort_flag = 1;
             break;
@@ -907,7 +922,10 @@ __global__ void __launch_bounds__(288, MINB) decode_split_kernel(const __grid_co
             mbar_arrive(&L.empty_bar[st]);
             if (meta.flags & kMetaLast) mbar_arrive(&L.qempty_bar[item_it & 1u]);
         }
-        ++stage_it;
+        if (++st == (uint32_t)p.n_stages) {
+            st = 0;
+            phase ^= 1u;
+        }
 
         if (meta.flags & kMetaLast) {
             float L0 = l0, L1 = l1;
@@ -1170,7 +1188,7 @@ cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream, 
     p.n_stages = stages;
     const size_t smem = fixed + (size_t)stages * p.stage_bytes;
 
-    auto kern = env_int("PKV_DECODE_LB", 1) == 2 ? decode_split_kernel<D, INT8, 2> : decode_split_kernel<D, INT8, 1>;
+    auto kern = decode_split_kernel<D, INT8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     const int threads = 32 * (hpc + 1);
