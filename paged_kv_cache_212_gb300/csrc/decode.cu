@@ -181,6 +181,119 @@ __device__ int32_t block_exclusive_scan(int32_t v, int32_t *total, int32_t *scra
     return r;
 }
 
+// Inclusive warp scan.
+__device__ __forceinline__ int32_t warp_inclusive_scan(int32_t v, int lane)
+{
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int32_t u = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += u;
+    }
+    return v;
+}
+
+// The plan of a batch of at most kSmallPlanSeqs sequences, made by one warp:
+// lane l holds sequences 4l .. 4l + 3, and each pass is one warp scan (no
+// block barrier, ctx_lens read once).  Same results as the block-wide plan.
+constexpr int32_t kSmallPlanSeqs = 128;
+__device__ void plan_small(const int32_t *__restrict__ ctx_lens, int32_t n_seqs, int32_t split_tokens,
+                           int32_t max_tokens, int32_t n_q_heads, int32_t head_dim, int32_t items_target,
+                           DecodeWorkspace ws, __nv_bfloat16 *out, float *lse_out, int32_t *dev_status)
+{
+    const int lane = threadIdx.x & 31;
+    const bool balanced = split_tokens == 0;
+    const int32_t unit = balanced ? kStageTokens : split_tokens;
+    int32_t ctx[4], n[4], pre[4];
+    int32_t loc = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int32_t sq = 4 * lane + j;
+        ctx[j] = sq < n_seqs ? ctx_lens[sq] : -1;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int32_t sq = 4 * lane + j;
+        n[j] = 0;
+        if (sq < n_seqs) {
+            if (ctx[j] < 0 || ctx[j] > max_tokens)
+                report(dev_status, PKV_DEV_BAD_LENGTH);
+            else
+                n[j] = (ctx[j] + unit - 1) / unit;
+        }
+        loc += n[j];
+    }
+    const int32_t incl = warp_inclusive_scan(loc, lane);
+    const int32_t total = __shfl_sync(0xffffffffu, incl, 31);
+    int32_t ex = incl - loc;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        pre[j] = ex;
+        ex += n[j];
+    }
+    int32_t n_items = 0, chunk = 0;
+    bool overflow = false;
+    if (!balanced) {
+        n_items = total;
+        overflow = total > ws.capacity;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int32_t sq = 4 * lane + j;
+            if (sq >= n_seqs) continue;
+            ws.seg[sq] = make_int2(pre[j], n[j]);
+            for (int32_t k = 0; k < n[j]; ++k)
+                if (pre[j] + k < ws.capacity) ws.items[pre[j] + k] = make_int2(sq, k);
+        }
+    } else {
+        if (lane == 0) ws.seq_prefix[n_seqs] = total;
+        const int32_t room = ws.capacity - n_seqs;
+        overflow = room < 1 && total > 0;
+        if (total > 0 && !overflow) {
+            const int32_t want = max(1, min(items_target, room));
+            chunk = max(kMinChunkStages, (total + want - 1) / want);
+            n_items = (total + chunk - 1) / chunk;
+        }
+        int32_t np[4], loc2 = 0;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            np[j] = chunk > 0 && n[j] > 0 ? (pre[j] + n[j] - 1) / chunk - pre[j] / chunk + 1 : 0;
+            loc2 += np[j];
+        }
+        const int32_t incl2 = warp_inclusive_scan(loc2, lane);
+        int32_t ex2 = incl2 - loc2;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int32_t sq = 4 * lane + j;
+            if (sq < n_seqs) {
+                ws.seq_prefix[sq] = pre[j];
+                ws.seg[sq] = make_int2(ex2, np[j]);
+                // items whose first stage lies in this sequence start with it
+                for (int32_t i = (pre[j] + chunk - 1) / max(chunk, 1); n[j] > 0 && i * chunk < pre[j] + n[j]; ++i)
+                    ws.items[i] = make_int2(sq, 0);
+            }
+            ex2 += np[j];
+        }
+    }
+    if (lane == 0) {
+        if (overflow) report(dev_status, PKV_DEV_WORKSPACE_OVERFLOW);
+        ws.header[kHdrTotal] = overflow ? 0u : (uint32_t)n_items;
+        ws.header[kHdrOverflow] = overflow ? 1u : 0u;
+        ws.header[kHdrChunk] = (uint32_t)chunk;
+        ws.header[kHdrStages] = balanced && !overflow ? (uint32_t)total : 0u;
+        ws.header[kHdrCounter] = 0u;
+    }
+    // sequences no piece will cover get o = 0 and lse = -inf
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        const int32_t sq = 4 * lane + j;
+        if (sq >= n_seqs || (!overflow && ctx[j] > 0 && ctx[j] <= max_tokens)) continue;
+        const int64_t row = (int64_t)sq * n_q_heads;
+        uint4 *o = reinterpret_cast<uint4 *>(out + row * head_dim);
+        for (int32_t i = 0; i < n_q_heads * head_dim / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
+        if (lse_out)
+            for (int32_t i = 0; i < n_q_heads; ++i) lse_out[row + i] = -INFINITY;
+    }
+}
+
 // CTA 0 plans; in the fused decode step, CTAs 1.. also write this step's new
 // K/V rows into the pool (write_mode 1: bf16 copy, 2: int8 quantisation), so
 // the split kernel, which waits for this whole grid, reads them.
@@ -209,35 +322,56 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t *__rest
         }
         return;
     }
+    if (n_seqs <= kSmallPlanSeqs) {
+        if (threadIdx.x < 32)
+            plan_small(ctx_lens, n_seqs, split_tokens, max_tokens, n_q_heads, head_dim, items_target, ws, out,
+                       lse_out, dev_status);
+        return;
+    }
     const int tid = threadIdx.x;
     const bool balanced = split_tokens == 0;
     const int32_t unit = balanced ? kStageTokens : split_tokens;
+    // Each thread keeps the lengths and prefixes of its first kCache sequences
+    // (s = tid + c * blockDim.x) in registers across the passes, so a batch of
+    // up to kCache * blockDim.x sequences reads ctx_lens once and never reads
+    // back what the plan wrote; larger batches re-read the rest.
+    constexpr int kCache = 4;
+    int32_t ctx_c[kCache], ex_c[kCache];
+    auto ctx_of = [&](int c, int32_t s) { return c < kCache ? ctx_c[c] : (s < n_seqs ? ctx_lens[s] : -1); };
     // pass 1: units (16-token stages, or fixed splits) per sequence and their prefix
     int32_t running = 0;
-    for (int32_t c0 = 0; c0 < n_seqs; c0 += blockDim.x) {
-        const int32_t s = c0 + tid;
-        int32_t n = 0;
-        if (s < n_seqs) {
-            const int32_t ctx = ctx_lens[s];
-            if (ctx < 0 || ctx > max_tokens)
-                report(dev_status, PKV_DEV_BAD_LENGTH);
-            else
-                n = (ctx + unit - 1) / unit;
-        }
-        int32_t tot;
-        const int32_t ex = running + block_exclusive_scan(n, &tot, scratch);
-        if (s < n_seqs) {
-            if (balanced) {
-                ws.seq_prefix[s] = ex;
-            } else {
-                ws.seg[s] = make_int2(ex, n);
-                for (int32_t k = 0; k < n; ++k)
-                    if (ex + k < ws.capacity) ws.items[ex + k] = make_int2(s, k);
+#pragma unroll
+    for (int c = 0; c < kCache + 1; ++c) {
+        for (int32_t c0 = c * (int32_t)blockDim.x; c0 < n_seqs; c0 += (c < kCache ? n_seqs : (int32_t)blockDim.x)) {
+            const int32_t s = c0 + tid;
+            const int32_t ctx = s < n_seqs ? ctx_lens[s] : -1;
+            int32_t n = 0;
+            if (s < n_seqs) {
+                if (ctx < 0 || ctx > max_tokens)
+                    report(dev_status, PKV_DEV_BAD_LENGTH);
+                else
+                    n = (ctx + unit - 1) / unit;
             }
+            int32_t tot;
+            const int32_t ex = running + block_exclusive_scan(n, &tot, scratch);
+            if (c < kCache) {
+                ctx_c[c] = ctx;
+                ex_c[c] = ex;
+            }
+            if (s < n_seqs) {
+                if (balanced) {
+                    ws.seq_prefix[s] = ex;
+                } else {
+                    ws.seg[s] = make_int2(ex, n);
+                    for (int32_t k = 0; k < n; ++k)
+                        if (ex + k < ws.capacity) ws.items[ex + k] = make_int2(s, k);
+                }
+            }
+            running += tot;
         }
-        running += tot;
     }
     int32_t n_items = 0, chunk = 0;
+    const int32_t total_stages = running;
     bool overflow = false;
     if (!balanced) {
         n_items = running;
@@ -254,24 +388,27 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t *__rest
         }
         // pass 2: pieces per sequence, their slots, and the first sequence of every item
         running = 0;
-        for (int32_t c0 = 0; c0 < n_seqs; c0 += blockDim.x) {
-            const int32_t s = c0 + tid;
-            int32_t n = 0, pre = 0, st = 0;
-            if (s < n_seqs && chunk > 0) {
-                pre = ws.seq_prefix[s];
-                const int32_t ctx = ctx_lens[s];
-                st = (ctx < 0 || ctx > max_tokens) ? 0 : (ctx + kStageTokens - 1) / kStageTokens;
-                if (st > 0) n = (pre + st - 1) / chunk - pre / chunk + 1;
+#pragma unroll
+        for (int c = 0; c < kCache + 1; ++c) {
+            for (int32_t c0 = c * (int32_t)blockDim.x; c0 < n_seqs; c0 += (c < kCache ? n_seqs : (int32_t)blockDim.x)) {
+                const int32_t s = c0 + tid;
+                int32_t n = 0, pre = 0, st = 0;
+                if (s < n_seqs && chunk > 0) {
+                    pre = c < kCache ? ex_c[c] : ws.seq_prefix[s];
+                    const int32_t ctx = ctx_of(c, s);
+                    st = (ctx < 0 || ctx > max_tokens) ? 0 : (ctx + kStageTokens - 1) / kStageTokens;
+                    if (st > 0) n = (pre + st - 1) / chunk - pre / chunk + 1;
+                }
+                int32_t tot;
+                const int32_t ex = running + block_exclusive_scan(n, &tot, scratch);
+                if (s < n_seqs) {
+                    ws.seg[s] = make_int2(ex, n);
+                    // items whose first stage lies in this sequence start with it
+                    for (int32_t i = (pre + chunk - 1) / max(chunk, 1); st > 0 && i * chunk < pre + st; ++i)
+                        ws.items[i] = make_int2(s, 0);
+                }
+                running += tot;
             }
-            int32_t tot;
-            const int32_t ex = running + block_exclusive_scan(n, &tot, scratch);
-            if (s < n_seqs) {
-                ws.seg[s] = make_int2(ex, n);
-                // items whose first stage lies in this sequence start with it
-                for (int32_t i = (pre + chunk - 1) / max(chunk, 1); st > 0 && i * chunk < pre + st; ++i)
-                    ws.items[i] = make_int2(s, 0);
-            }
-            running += tot;
         }
     }
     if (tid == 0) {
@@ -279,111 +416,124 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t *__rest
         ws.header[kHdrTotal] = overflow ? 0u : (uint32_t)n_items;
         ws.header[kHdrOverflow] = overflow ? 1u : 0u;
         ws.header[kHdrChunk] = (uint32_t)chunk;
-        ws.header[kHdrStages] = balanced && !overflow ? (uint32_t)ws.seq_prefix[n_seqs] : 0u;
+        ws.header[kHdrStages] = balanced && !overflow ? (uint32_t)total_stages : 0u;
         ws.header[kHdrCounter] = 0u;
     }
     // Sequences no piece will cover (empty or invalid context, or every
     // sequence when the work list overflowed) get o = 0 and lse = -inf here,
     // one thread per such sequence.
-    for (int32_t s = tid; s < n_seqs; s += blockDim.x) {
-        const int32_t ctx = ctx_lens[s];
-        if (!overflow && ctx > 0 && ctx <= max_tokens) continue;
-        const int64_t row = (int64_t)s * n_q_heads;
-        uint4 *o = reinterpret_cast<uint4 *>(out + row * head_dim);
-        for (int32_t i = 0; i < n_q_heads * head_dim / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
-        if (lse_out)
-            for (int32_t i = 0; i < n_q_heads; ++i) lse_out[row + i] = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < kCache + 1; ++c) {
+        for (int32_t c0 = c * (int32_t)blockDim.x; c0 < n_seqs; c0 += (c < kCache ? n_seqs : (int32_t)blockDim.x)) {
+            const int32_t s = c0 + tid;
+            if (s >= n_seqs) continue;
+            const int32_t ctx = ctx_of(c, s);
+            if (!overflow && ctx > 0 && ctx <= max_tokens) continue;
+            const int64_t row = (int64_t)s * n_q_heads;
+            uint4 *o = reinterpret_cast<uint4 *>(out + row * head_dim);
+            for (int32_t i = 0; i < n_q_heads * head_dim / 8; ++i) o[i] = make_uint4(0, 0, 0, 0);
+            if (lse_out)
+                for (int32_t i = 0; i < n_q_heads; ++i) lse_out[row + i] = -INFINITY;
+        }
     }
 }
 
 // ---------------------------------------------------------------------------
 // 3. merge of the pieces of a sequence
 // ---------------------------------------------------------------------------
-// The G query heads are merged side by side: 32 / G lanes per head, each lane
-// owning EPL = D * G / 32 consecutive elements of its head's output.  The
-// partials of a batch of pieces are all loaded before any is used, so a merge
-// costs about two L2 round trips.  Partials are read with ld.global.cg (L2):
-// other SMs wrote them.
-template <int D, int EPL>
-__device__ __forceinline__ void merge_pieces(const float2 *part_ml, const float *part_acc, __nv_bfloat16 *out,
-                                          float *lse_out, int32_t n_q_heads, int32_t s, int32_t hbase,
-                                          int32_t base, int32_t n_pieces, int lane)
+// One warp per (sequence, query head) of every sequence cut into two or more
+// pieces: o = sum_k 2^(m_k - M) acc_k / sum_k 2^(m_k - M) l_k with M = max_k
+// m_k (the finalize step of the tiled attention), lse = ln 2 (M + log2 L).
+// First the lanes read the pieces' (m, l) side by side (one load each for up
+// to 32 pieces) and reduce M; then every lane streams its D / 32 elements of
+// kBatch pieces' partial rows at a time, all loads of a batch in flight
+// together, each weighted by its piece's factor broadcast from the lane that
+// read it.  Partials are read with ld.global.cg (L2): other SMs wrote them.
+// Launched after the split kernel as a programmatic dependent; it reads the
+// plan's piece counts before waiting for the split kernel's partials.
+template <int D>
+__global__ void __launch_bounds__(256, 3) decode_merge_kernel(DecodeWorkspace ws, int32_t n_seqs,
+                                                              int32_t n_q_heads, __nv_bfloat16 *out, float *lse_out)
 {
-    constexpr int LPH = D / EPL;                     // lanes per head
-    constexpr int VEC = EPL >= 4 ? 4 : 2;            // floats per load
-    constexpr int NV = EPL / VEC;                    // loads per piece and lane
-    constexpr int BATCH = EPL >= 32 ? 2 : (EPL >= 16 ? 4 : 8);
-    const int n = lane / LPH, sub = lane % LPH;
-    const int64_t hrow = hbase + n;
-    // one pass with a running maximum: every load of a batch is in flight
-    // before any is used, and no separate pass over the maxima is needed
+    constexpr int EPL = D / 32;                      // output elements per lane
+    constexpr int kBatch = 8;                        // pieces in flight per lane
+    grid_dependents_launch();   // the next step's plan may start; it waits for this grid
+    const int lane = threadIdx.x & 31;
+    const int64_t idx = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    const bool mine = idx < (int64_t)n_seqs * n_q_heads;
+    const int32_t s = mine ? (int32_t)(idx / n_q_heads) : 0, h = mine ? (int32_t)(idx % n_q_heads) : 0;
+    // The plan's results (pieces per sequence, overflow flag) are complete:
+    // the split kernel lets this grid start only after its own wait for the
+    // plan.  Only the partials need the wait for the split kernel.
+    const int2 sg = mine ? ws.seg[s] : make_int2(0, 0);
+    const uint32_t overflow = mine ? ws.header[kHdrOverflow] : 1u;
+    grid_dependency_wait();
+    if (!mine || sg.y < 2 || overflow != 0) return;
+    const int32_t n = sg.y;
+    const int64_t row0 = (int64_t)sg.x * n_q_heads + h;       // piece k's row: row0 + k * n_q_heads
+    // (m, l) of pieces lane, lane + 32, ...: the maximum over all pieces
+    float2 ml_own = make_float2(-INFINITY, 0.f);
     float M = -INFINITY;
+    for (int32_t k = lane; k < n; k += 32) {
+        const float2 ml = __ldcg(&ws.part_ml[row0 + (int64_t)k * n_q_heads]);
+        if (k < 32) ml_own = ml;
+        M = fmaxf(M, ml.x);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     float o[EPL];
 #pragma unroll
     for (int e = 0; e < EPL; ++e) o[e] = 0.f;
     float Lsum = 0.f;
-    for (int32_t k0 = 0; k0 < n_pieces; k0 += BATCH) {
-        float2 ml[BATCH];
-        float a[BATCH][EPL];
+    for (int32_t k0 = 0; k0 < n; k0 += 32) {
+        // this lane's piece k0 + lane: its weight and its share of the sum
+        const float2 ml = k0 == 0 ? ml_own
+                                  : (k0 + lane < n ? __ldcg(&ws.part_ml[row0 + (int64_t)(k0 + lane) * n_q_heads])
+                                                   : make_float2(-INFINITY, 0.f));
+        const float wk = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
+        Lsum += wk * ml.y;
+        const int32_t cnt = min(32, n - k0);
+        const float *base = ws.part_acc + (row0 + (int64_t)k0 * n_q_heads) * D + lane * EPL;
+        const int32_t stride = n_q_heads * D;                  // floats from one piece's row to the next
+        for (int32_t i0 = 0; i0 < cnt; i0 += kBatch) {
+            float a[kBatch][EPL];
 #pragma unroll
-        for (int i = 0; i < BATCH; ++i) {
-            if (k0 + i < n_pieces) {
-                const int64_t row = (int64_t)(base + k0 + i) * n_q_heads + hrow;
-                ml[i] = __ldcg(&part_ml[row]);
-                const float *src = part_acc + row * D + sub * EPL;
-#pragma unroll
-                for (int v = 0; v < NV; ++v) {
-                    if constexpr (VEC == 4) {
-                        const float4 x = __ldcg(reinterpret_cast<const float4 *>(src) + v);
-                        a[i][4 * v] = x.x;
-                        a[i][4 * v + 1] = x.y;
-                        a[i][4 * v + 2] = x.z;
-                        a[i][4 * v + 3] = x.w;
+            for (int i = 0; i < kBatch; ++i) {
+                if (i0 + i < cnt) {
+                    const float *src = base + (i0 + i) * stride;
+                    if constexpr (EPL == 4) {
+                        const float4 x = __ldcg(reinterpret_cast<const float4 *>(src));
+                        a[i][0] = x.x;
+                        a[i][1] = x.y;
+                        a[i][2] = x.z;
+                        a[i][3] = x.w;
                     } else {
-                        const float2 x = __ldcg(reinterpret_cast<const float2 *>(src) + v);
-                        a[i][2 * v] = x.x;
-                        a[i][2 * v + 1] = x.y;
+                        const float2 x = __ldcg(reinterpret_cast<const float2 *>(src));
+                        a[i][0] = x.x;
+                        a[i][1] = x.y;
                     }
                 }
             }
-        }
 #pragma unroll
-        for (int i = 0; i < BATCH; ++i) {
-            if (k0 + i < n_pieces && ml[i].x != -INFINITY) {
-                const float Mn = fmaxf(M, ml[i].x);
-                const float keep = exp2f(M - Mn), w = exp2f(ml[i].x - Mn);
-                Lsum = Lsum * keep + ml[i].y * w;
+            for (int i = 0; i < kBatch; ++i) {
+                const float w = __shfl_sync(0xffffffffu, wk, (i0 + i) & 31);
+                if (i0 + i < cnt) {
 #pragma unroll
-                for (int e = 0; e < EPL; ++e) o[e] = o[e] * keep + a[i][e] * w;
-                M = Mn;
+                    for (int e = 0; e < EPL; ++e) o[e] = fmaf(w, a[i][e], o[e]);
+                }
             }
         }
     }
-    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-    __nv_bfloat16 *dst = out + ((int64_t)s * n_q_heads + hrow) * D + sub * EPL;
 #pragma unroll
-    for (int e = 0; e < EPL; e += 2) *reinterpret_cast<uint32_t *>(dst + e) = pack_bf16x2(o[e] * inv, o[e + 1] * inv);
-    if (lse_out && sub == 0)
-        lse_out[(int64_t)s * n_q_heads + hrow] = Lsum > 0.f ? (M + __log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
-}
-
-// One warp per (sequence, kv head) of every sequence cut into two or more
-// pieces; EPL = D * G / 32.  Launched after the split kernel as a programmatic
-// dependent: it waits for the split kernel's results before reading them.
-template <int D, int EPL>
-__global__ void __launch_bounds__(128) decode_merge_kernel(DecodeWorkspace ws, int32_t n_seqs, int32_t n_kv_heads,
-                                                           int32_t n_q_heads, int32_t group, __nv_bfloat16 *out,
-                                                           float *lse_out)
-{
-    grid_dependents_launch();   // the next step's plan may start; it waits for this grid
-    grid_dependency_wait();
-    const int lane = threadIdx.x & 31;
-    const int64_t idx = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    if (idx >= (int64_t)n_seqs * n_kv_heads) return;
-    const int32_t s = (int32_t)(idx / n_kv_heads), kvh = (int32_t)(idx % n_kv_heads);
-    const int2 sg = ws.seg[s];
-    if (sg.y < 2 || ws.header[kHdrOverflow] != 0) return;
-    merge_pieces<D, EPL>(ws.part_ml, ws.part_acc, out, lse_out, n_q_heads, s, kvh * group, sg.x, sg.y, lane);
+    for (int off = 16; off > 0; off >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, off);
+    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+    __nv_bfloat16 *dst = out + ((int64_t)s * n_q_heads + h) * D + lane * EPL;
+    if constexpr (EPL == 4)
+        *reinterpret_cast<uint2 *>(dst) = make_uint2(pack_bf16x2(o[0] * inv, o[1] * inv), pack_bf16x2(o[2] * inv, o[3] * inv));
+    else
+        *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(o[0] * inv, o[1] * inv);
+    if (lse_out && lane == 0)
+        lse_out[(int64_t)s * n_q_heads + h] = Lsum > 0.f ? (M + __log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
 }
 
 // TMA copies of one 16-token stage (K and V tiles of hpc kv heads, int8 scales)
@@ -458,8 +608,9 @@ __global__ void __launch_bounds__(288, INT8 ? 1 : 2) decode_split_kernel(const _
         fence_mbar_init();
     }
     __syncthreads();
-    grid_dependents_launch();
     grid_dependency_wait();     // the plan kernel's work list is complete and visible
+    // the merge may start now: the plan it reads first is complete
+    grid_dependents_launch();
 
     const uint32_t total_items = p.ws.header[kHdrTotal] * (uint32_t)p.n_hg;
     volatile int32_t *abort_flag = L.abort_flag;
@@ -1236,21 +1387,16 @@ cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream, 
     lc.numAttrs = 1;
     e = cudaLaunchKernelEx(&lc, kern, kmap, vmap, ksmap, vsmap, p);
     if (e != cudaSuccess) return e;
-    // merge of multi-piece sequences: one warp per (sequence, kv head)
-    const int64_t warps = (int64_t)a.n_seqs * d.n_kv_heads;
+    // merge of multi-piece sequences: one warp per (sequence, query head)
+    const int64_t warps = (int64_t)a.n_seqs * a.n_q_heads;
     cudaLaunchConfig_t mc{};
-    mc.gridDim = dim3((unsigned)((warps + 3) / 4));
-    mc.blockDim = dim3(128);
+    mc.gridDim = dim3((unsigned)((warps + 7) / 8));
+    mc.blockDim = dim3(256);
     mc.stream = stream;
     mc.attrs = pdl;
     mc.numAttrs = 1;
-    __nv_bfloat16 *out = static_cast<__nv_bfloat16 *>(a.out);
-    switch (G) {
-    case 1: return cudaLaunchKernelEx(&mc, decode_merge_kernel<D, D / 32>, a.ws, a.n_seqs, d.n_kv_heads, a.n_q_heads, G, out, a.lse_out);
-    case 2: return cudaLaunchKernelEx(&mc, decode_merge_kernel<D, D / 16>, a.ws, a.n_seqs, d.n_kv_heads, a.n_q_heads, G, out, a.lse_out);
-    case 4: return cudaLaunchKernelEx(&mc, decode_merge_kernel<D, D / 8>, a.ws, a.n_seqs, d.n_kv_heads, a.n_q_heads, G, out, a.lse_out);
-    default: return cudaLaunchKernelEx(&mc, decode_merge_kernel<D, D / 4>, a.ws, a.n_seqs, d.n_kv_heads, a.n_q_heads, G, out, a.lse_out);
-    }
+    return cudaLaunchKernelEx(&mc, decode_merge_kernel<D>, a.ws, a.n_seqs, a.n_q_heads,
+                              static_cast<__nv_bfloat16 *>(a.out), a.lse_out);
 }
 
 }  // namespace
