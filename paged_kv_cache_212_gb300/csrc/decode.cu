@@ -294,10 +294,15 @@ __device__ void plan_small(const int32_t *__restrict__ ctx_lens, int32_t n_seqs,
     }
 }
 
+// 256-thread CTAs for the plan launch: small enough to be placed on an SM
+// beside the previous kernels' CTAs, so they are resident and waiting when
+// their predecessor completes.
+constexpr int kPlanThreads = 256;
+
 // CTA 0 plans; in the fused decode step, CTAs 1.. also write this step's new
 // K/V rows into the pool (write_mode 1: bf16 copy, 2: int8 quantisation), so
 // the split kernel, which waits for this whole grid, reads them.
-__global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t *__restrict__ ctx_lens,
+__global__ void __launch_bounds__(kPlanThreads, 4) decode_plan_kernel(const int32_t *__restrict__ ctx_lens,
                                                            int32_t n_seqs, int32_t split_tokens,
                                                            int32_t max_tokens, int32_t n_q_heads,
                                                            int32_t head_dim, int32_t n_kv_heads,
@@ -452,7 +457,7 @@ __global__ void __launch_bounds__(1024) decode_plan_kernel(const int32_t *__rest
 // Launched after the split kernel as a programmatic dependent; it reads the
 // plan's piece counts before waiting for the split kernel's partials.
 template <int D>
-__global__ void __launch_bounds__(256, 3) decode_merge_kernel(DecodeWorkspace ws, int32_t n_seqs,
+__global__ void __launch_bounds__(128) decode_merge_kernel(DecodeWorkspace ws, int32_t n_seqs,
                                                               int32_t n_q_heads, __nv_bfloat16 *out, float *lse_out)
 {
     constexpr int EPL = D / 32;                      // output elements per lane
@@ -1359,9 +1364,12 @@ cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream, 
     if (write && write->n_seqs > 0 && write->n_new > 0) {
         wa = *write;
         write_mode = INT8 ? 2 : 1;
-        const int64_t units = INT8 ? ((int64_t)wa.n_seqs * wa.n_new * 2 * ((d.n_kv_heads + 3) / 4) + 31) / 32
-                                   : (int64_t)wa.n_seqs * wa.n_new * (d.n_kv_heads * D / 8) / 1024;
-        write_ctas = (int)(units < 1 ? 1 : (units > 2 * num_sms ? 2 * num_sms : units));
+        constexpr int64_t warps_per_cta = kPlanThreads / 32;
+        const int64_t units = INT8 ? ((int64_t)wa.n_seqs * wa.n_new * 2 * ((d.n_kv_heads + 3) / 4) + warps_per_cta - 1) /
+                                         warps_per_cta
+                                   : ((int64_t)wa.n_seqs * wa.n_new * (d.n_kv_heads * D / 8) + kPlanThreads - 1) /
+                                         kPlanThreads;
+        write_ctas = (int)(units < 1 ? 1 : (units > 8 * num_sms ? 8 * num_sms : units));
     }
     // all three launches are programmatic dependents of their predecessor on
     // the stream; each waits (griddepcontrol.wait) before touching memory
@@ -1370,7 +1378,7 @@ cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream, 
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t pc{};
     pc.gridDim = dim3((unsigned)(1 + write_ctas));
-    pc.blockDim = dim3(1024);
+    pc.blockDim = dim3(kPlanThreads);
     pc.stream = stream;
     pc.attrs = pdl;
     pc.numAttrs = 1;
@@ -1390,8 +1398,8 @@ cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream, 
     // merge of multi-piece sequences: one warp per (sequence, query head)
     const int64_t warps = (int64_t)a.n_seqs * a.n_q_heads;
     cudaLaunchConfig_t mc{};
-    mc.gridDim = dim3((unsigned)((warps + 7) / 8));
-    mc.blockDim = dim3(256);
+    mc.gridDim = dim3((unsigned)((warps + 3) / 4));
+    mc.blockDim = dim3(128);   // small CTAs: resident beside the split kernel's before it ends
     mc.stream = stream;
     mc.attrs = pdl;
     mc.numAttrs = 1;
