@@ -111,20 +111,6 @@ __host__ __device__ constexpr size_t smem_tail_bytes()
     return (2 * kMaxStages + 4) * sizeof(uint64_t) + kMaxStages * sizeof(StageMeta) + 16;
 }
 
-// Exact int8 -> fp16 for four packed codes: (0x6400 | (b ^ 0x80)) is the fp16
-// value 1024 + b + 128, so subtracting 1152 leaves b exactly.
-__device__ __forceinline__ void int8x4_to_half2x2(uint32_t w, uint32_t &lo, uint32_t &hi)
-{
-    const uint32_t u = w ^ 0x80808080u;
-    uint32_t a = __byte_perm(u, 0x64646464u, 0x4140);
-    uint32_t b = __byte_perm(u, 0x64646464u, 0x4342);
-    const __half2 bias = __half2half2(__ushort_as_half((unsigned short)0x6480));  // 1152
-    __half2 ha = __hsub2(*reinterpret_cast<__half2 *>(&a), bias);
-    __half2 hb = __hsub2(*reinterpret_cast<__half2 *>(&b), bias);
-    lo = *reinterpret_cast<uint32_t *>(&ha);
-    hi = *reinterpret_cast<uint32_t *>(&hb);
-}
-
 // int8 -> fp16 for four packed codes with a bias: (0x6400 | (b ^ 0x80)) is
 // the fp16 value 1152 + b, exact for every code b.  Products of the biased
 // codes are corrected once per score (S - 1152 sum_d q_d) and once per output
@@ -341,7 +327,7 @@ __global__ void __launch_bounds__(kPlanThreads, 4) decode_plan_kernel(const int3
     // up to kCache * blockDim.x sequences reads ctx_lens once and never reads
     // back what the plan wrote; larger batches re-read the rest.
     constexpr int kCache = 4;
-    int32_t ctx_c[kCache], ex_c[kCache];
+    int32_t ctx_c[kCache] = {}, ex_c[kCache] = {};
     auto ctx_of = [&](int c, int32_t s) { return c < kCache ? ctx_c[c] : (s < n_seqs ? ctx_lens[s] : -1); };
     // pass 1: units (16-token stages, or fixed splits) per sequence and their prefix
     int32_t running = 0;
