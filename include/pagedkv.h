@@ -94,6 +94,20 @@ const char *pkv_status_string(int status);
 int pkv_last_cuda_error(void);
 
 /*
+ * pkv_set_pipeline_wait_ns -- the limit of the kernels' pipeline waits, for
+ * every launch prepared after the call (process-wide; 0 restores the default
+ * of 4 s).  A wait that runs out sets PKV_DEV_TIMEOUT in dev_status and its
+ * CTA winds down: the copies and tensor-core operations it already issued
+ * finish (those waits keep the default limit) before it releases shared
+ * memory or TMEM, and the call's outputs are then undefined.  The failure
+ * path of the pages' Result-returning calls (libmir-metal paged/mod.rs,
+ * PagedStore::update and context return errors instead of aborting); a short
+ * limit makes that path run on purpose, for tests.  Returns the previous
+ * limit.
+ */
+uint64_t pkv_set_pipeline_wait_ns(uint64_t ns);
+
+/*
  * paged_kv_write -- native bf16 page write (tiny-llm paged_kv.py,
  * PagedLayerKV.update; AstrAI cache.py, PagedCache.write; libmir-metal
  * paged/mod.rs, write::native).

@@ -22,7 +22,8 @@ PKV_KV_BF16, PKV_KV_INT8 = 0, 1
 DEV_BAD_BLOCK_ID, DEV_BAD_POSITION, DEV_BAD_LENGTH = 1, 2, 4
 DEV_WORKSPACE_OVERFLOW, DEV_TIMEOUT = 8, 16
 
-EXPORTS = ("pkv_status_string", "pkv_last_cuda_error", "paged_kv_write", "paged_kv_write_int8",
+EXPORTS = ("pkv_status_string", "pkv_last_cuda_error", "pkv_set_pipeline_wait_ns", "paged_kv_write",
+           "paged_kv_write_int8",
            "paged_kv_gather", "pkv_decode_workspace_bytes", "paged_decode_attention",
            "paged_prefill_attention", "paged_decode_attention_noalloc", "paged_decode_step",
            "paged_kv_copy_blocks",
@@ -72,6 +73,8 @@ def load_library(path: str = LIB_PATH):
     lib.pkv_status_string.restype = ctypes.c_char_p
     lib.pkv_last_cuda_error.argtypes = []
     lib.pkv_last_cuda_error.restype = ctypes.c_int
+    lib.pkv_set_pipeline_wait_ns.argtypes = [ctypes.c_uint64]
+    lib.pkv_set_pipeline_wait_ns.restype = ctypes.c_uint64
     lib.paged_kv_write.argtypes = [P, P, P, P, Dims, P, i32, P, i32, i32, P, P]
     lib.paged_kv_write_int8.argtypes = [P, P, P, P, P, P, Dims, P, i32, P, i32, i32, P, P]
     lib.paged_kv_gather.argtypes = [P, P, Dims, P, i32, P, i32, i32, P, P, P, P]

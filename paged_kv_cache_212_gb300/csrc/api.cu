@@ -1,6 +1,7 @@
 // api.cu -- the extern "C" entry points of libpagedkv.so: argument checks on
 // the host, then kernel launches on the caller's stream.  No allocation, no
 // synchronisation, no exception crosses the ABI.
+#include <atomic>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
@@ -11,12 +12,12 @@
 
 namespace pkv {
 
-cudaError_t launch_prefill_mma(const PrefillArgs &a, cudaStream_t stream);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream);
 
 namespace {
 
 thread_local int g_last_cuda_error = 0;
+std::atomic<uint64_t> g_pipeline_wait_ns{kWaitTimeoutNs};
 
 int cuda_status(cudaError_t e)
 {
@@ -90,6 +91,8 @@ size_t decode_capacity_for(int32_t n_seqs, int64_t max_total_ctx_tokens, int32_t
 
 void record_cuda_error(int e) { g_last_cuda_error = e; }
 
+unsigned long long pipeline_wait_ns() { return g_pipeline_wait_ns.load(); }
+
 CUresult encode_tensor_map(CUtensorMap *map, CUtensorMapDataType dtype, uint32_t rank, void *base,
                            const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box,
                            CUtensorMapSwizzle swizzle)
@@ -103,15 +106,10 @@ CUresult encode_tensor_map(CUtensorMap *map, CUtensorMapDataType dtype, uint32_t
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-// Prefill runs on the tcgen05 kernel; PKV_PREFILL_IMPL=mma selects the
-// warp-level mma.sync kernel instead (kept for comparison and for group sizes
-// the tcgen05 tiling does not take).
+// Prefill runs on the tcgen05 kernel (prefill_tc.cu).
 cudaError_t launch_prefill(const PrefillArgs &a, int num_sms, cudaStream_t stream)
 {
     (void)num_sms;
-    const char *impl = getenv("PKV_PREFILL_IMPL");
-    const int G = a.n_q_heads / a.dims.n_kv_heads;
-    if ((impl && impl[0] == 'm') || G > 16 || 128 % G != 0) return launch_prefill_mma(a, stream);
     return launch_prefill_tc(a, stream);
 }
 
@@ -137,6 +135,12 @@ const char *pkv_status_string(int status)
 }
 
 int pkv_last_cuda_error(void) { return g_last_cuda_error; }
+
+uint64_t pkv_set_pipeline_wait_ns(uint64_t ns)
+{
+    const uint64_t prev = g_pipeline_wait_ns.exchange(ns == 0 ? (uint64_t)kWaitTimeoutNs : ns);
+    return prev;
+}
 
 static int write_common_checks(const void *k_new, const void *v_new, const void *k_pool, const void *v_pool,
                                const pkv_dims &dims, const int32_t *tables, int32_t max_blocks,

@@ -86,18 +86,33 @@ __device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity)
 }
 
 // Waits for the phase with the given parity to complete.  Returns false when
-// the wait ran out of time or another warp of the CTA raised *abort (the
-// caller then reports PKV_DEV_TIMEOUT and winds down).
+// the wait ran out of time (timeout_ns of %globaltimer) or another warp of the
+// CTA raised *abort (the caller then reports PKV_DEV_TIMEOUT and winds down).
+// Pipeline waits take the launch's limit (settable from the host, see
+// pkv_set_pipeline_wait_ns); the waits of a wind-down, which let copies and
+// tensor-core operations already issued finish before shared memory or TMEM
+// is released, always keep the default.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
-                                          volatile int32_t *abort = nullptr)
+                                          volatile int32_t *abort = nullptr,
+                                          unsigned long long timeout_ns = kWaitTimeoutNs)
 {
+    if (timeout_ns < kWaitTimeoutNs) {
+        // a short limit: poll with test_wait, which never suspends the thread
+        // (try_wait may block until the phase completes)
+        const unsigned long long t0 = global_timer_ns();
+        while (true) {
+            if (mbar_test_wait(bar, parity)) return true;
+            if (abort && *abort) return false;
+            if (global_timer_ns() - t0 > timeout_ns) return false;
+        }
+    }
     if (mbar_try_wait(bar, parity)) return true;
     unsigned long long t0 = global_timer_ns();
     for (uint32_t spin = 1;; ++spin) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((spin & 255u) == 0) {
             if (abort && *abort) return false;
-            if (global_timer_ns() - t0 > kWaitTimeoutNs) return false;
+            if (global_timer_ns() - t0 > timeout_ns) return false;
         }
     }
 }

@@ -77,6 +77,7 @@ struct DecodeParams {
     int32_t n_stages;
     int32_t boxes_per_half;  // TMA boxes per (K or V, half): 1 (all heads) or hpc (one per head)
     uint32_t stage_bytes, tx_bytes, kv_tile_bytes, scale_tile_bytes, q_slot_bytes;
+    unsigned long long wait_ns;   // limit of the pipeline waits
 };
 
 // Shared-memory carve-up (dynamic smem, base rounded up to 1024 bytes).
@@ -677,7 +678,7 @@ __global__ void __launch_bounds__(288, INT8 ? 1 : 2) decode_split_kernel(const _
                 const int32_t *trow = p.tables + (int64_t)seq * p.max_blocks;
                 // this piece's queries: heads [hg*hpc*G, (hg+1)*hpc*G) of sequence seq
                 const uint32_t qs = item_it & 1u;
-                if (!mbar_wait(&L.qempty_bar[qs], ((item_it >> 1) & 1u) ^ 1u, abort_flag)) {
+                if (!mbar_wait(&L.qempty_bar[qs], ((item_it >> 1) & 1u) ^ 1u, abort_flag, p.wait_ns)) {
                     report(p.dev_status, PKV_DEV_TIMEOUT);
                     *abort_flag = 1;
                     ok = false;
@@ -696,7 +697,7 @@ __global__ void __launch_bounds__(288, INT8 ? 1 : 2) decode_split_kernel(const _
                     const bool more_stages = t + kStageTokens < t1;
                     int32_t blk_next = blk;
                     if (last_of_block && more_stages) blk_next = lb + 1 < p.max_blocks ? __ldg(trow + lb + 1) : -1;
-                    if (!mbar_wait(&L.empty_bar[st], phase ^ 1u, abort_flag)) {
+                    if (!mbar_wait(&L.empty_bar[st], phase ^ 1u, abort_flag, p.wait_ns)) {
                         report(p.dev_status, PKV_DEV_TIMEOUT);
                         *abort_flag = 1;
                         ok = false;
@@ -741,7 +742,7 @@ __global__ void __launch_bounds__(288, INT8 ? 1 : 2) decode_split_kernel(const _
         }
         // stop marker
         if (ok && !*abort_flag) {
-            if (mbar_wait(&L.empty_bar[st], phase ^ 1u, abort_flag)) {
+            if (mbar_wait(&L.empty_bar[st], phase ^ 1u, abort_flag, p.wait_ns)) {
                 L.meta[st].flags = kMetaStop;
                 mbar_arrive(&L.full_bar[st]);
             } else {
@@ -750,8 +751,9 @@ __global__ void __launch_bounds__(288, INT8 ? 1 : 2) decode_split_kernel(const _
             }
         }
         if (*abort_flag) {
-            // wind down: let every load already issued land before the CTA exits
-            // (the last n_stages slots, in issue order)
+            // wind down: let every copy already issued land before the CTA exits
+            // (the last n_stages slots and the last two query copies; a phase
+            // never issued counts as complete), with the default limit
             uint32_t ws_ = st, wp = phase;
             for (int i = 0; i < p.n_stages; ++i) {
                 if (ws_ == 0) {
@@ -761,6 +763,8 @@ __global__ void __launch_bounds__(288, INT8 ? 1 : 2) decode_split_kernel(const _
                 --ws_;
                 (void)mbar_wait(&L.full_bar[ws_], wp);
             }
+            for (uint32_t i = item_it > 2u ? item_it - 2u : 0u; i < item_it; ++i)
+                (void)mbar_wait(&L.qfull_bar[i & 1u], (i >> 1) & 1u);
         }
         return;
     }
@@ -780,7 +784,7 @@ __global__ void __launch_bounds__(288, INT8 ? 1 : 2) decode_split_kernel(const _
     const uint32_t half_bytes = (uint32_t)hpc * kStageTokens * 128u;
 
     while (true) {
-        if (!__all_sync(0xffffffffu, mbar_wait(&L.full_bar[st], phase, abort_flag))) {
+        if (!__all_sync(0xffffffffu, mbar_wait(&L.full_bar[st], phase, abort_flag, p.wait_ns))) {
             if (lane == 0) report(p.dev_status, PKV_DEV_TIMEOUT);
             *abort_flag = 1;
             break;
@@ -791,7 +795,7 @@ __global__ void __launch_bounds__(288, INT8 ? 1 : 2) decode_split_kernel(const _
 
         if (meta.flags & kMetaFirst) {
             const uint32_t qs = item_it & 1u;
-            if (!__all_sync(0xffffffffu, mbar_wait(&L.qfull_bar[qs], (item_it >> 1) & 1u, abort_flag))) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&L.qfull_bar[qs], (item_it >> 1) & 1u, abort_flag, p.wait_ns))) {
                 if (lane == 0) report(p.dev_status, PKV_DEV_TIMEOUT);
                 *abort_flag = 1;
                 break;
@@ -1208,12 +1212,6 @@ bool carve_decode_workspace(void *ws, size_t bytes, int32_t n_seqs, int32_t n_q_
 
 namespace {
 
-int env_int(const char *name, int fallback)
-{
-    const char *v = getenv(name);
-    return (v && *v) ? atoi(v) : fallback;
-}
-
 // Pool tile map for TMA: preferred is a 3-D view {col, row, head} whose box
 // {box_cols, 16, hpc} fetches 16 token rows of hpc heads in one copy; if the
 // driver rejects the non-monotonic strides, a {col, head, row} view with one
@@ -1251,16 +1249,16 @@ cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream, 
     // heads; with groups of 8 or more query heads per kv head the consumer
     // warps carry twice the mma work per byte, and 4 kv heads per CTA with two
     // CTAs per SM keep more loads in flight per unit of that work.
-    int hpc_default = d.n_kv_heads <= 8 ? d.n_kv_heads : 8, ctas_default = 1;
+    // (kv heads per CTA: the largest divisor of n_kv_heads up to 8, a multiple
+    // of 4 for int8 pages, whose scale rows are copied 16 bytes at a time)
+    int hpc = 0, ctas_per_sm = 1;
+    for (int c = 8; c >= 1 && hpc == 0; --c)
+        if (d.n_kv_heads % c == 0 && (!INT8 || c % 4 == 0)) hpc = c;
     if (G >= 8 && d.n_kv_heads % 4 == 0) {
-        hpc_default = 4;
-        ctas_default = 2;
+        hpc = 4;
+        ctas_per_sm = 2;
     }
-    int hpc = env_int("PKV_DECODE_HPC", hpc_default);
-    if (hpc <= 0 || hpc > 8 || d.n_kv_heads % hpc != 0) hpc = hpc_default;
-    if (INT8 && hpc % 4 != 0) return cudaErrorInvalidValue;
-    int ctas_per_sm = env_int("PKV_DECODE_CTAS_PER_SM", ctas_default);
-    if (ctas_per_sm < 1 || ctas_per_sm > 4) ctas_per_sm = ctas_default;
+    if (hpc == 0) return cudaErrorInvalidValue;
 
     DecodeParams p{};
     p.q = static_cast<const __nv_bfloat16 *>(a.q);
@@ -1281,6 +1279,7 @@ cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream, 
     p.lse_out = a.lse_out;
     p.ws = a.ws;
     p.dev_status = a.dev_status;
+    p.wait_ns = pipeline_wait_ns();
     if (!INT8) {
         p.kv_tile_bytes = (uint32_t)(D / 64) * hpc * 16u * 128u;
         p.scale_tile_bytes = 0;
@@ -1325,8 +1324,6 @@ cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream, 
     // int8 pages: at most four stages (measured faster on GB300 than deeper rings)
     const int stage_cap = INT8 ? 4 : kMaxStages;
     stages = stages > stage_cap ? stage_cap : stages;
-    const int want = env_int("PKV_DECODE_STAGES", 0);
-    if (want >= 2 && want < stages) stages = want;
     p.n_stages = stages;
     const size_t smem = fixed + (size_t)stages * p.stage_bytes;
 
@@ -1339,10 +1336,8 @@ cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream, 
     if (e != cudaSuccess) return e;
     if (occ < 1) return cudaErrorInvalidConfiguration;
     const int grid = num_sms * (occ < ctas_per_sm ? occ : ctas_per_sm);
-    // balanced pieces: about items_per_cta items per CTA and kv-head group
-    int items_per_cta = env_int("PKV_DECODE_ITEMS_PER_CTA", 1);
-    if (items_per_cta < 1 || items_per_cta > 16) items_per_cta = 1;
-    const int items_target = (grid * items_per_cta + p.n_hg - 1) / p.n_hg;
+    // balanced pieces: about one item per CTA and kv-head group
+    const int items_target = (grid + p.n_hg - 1) / p.n_hg;
     const int32_t max_tokens = a.max_blocks * d.block_size;
     // the fused step's write runs in extra CTAs of the plan launch
     int write_mode = 0, write_ctas = 0;

@@ -105,6 +105,10 @@ cudaError_t launch_copy_blocks(const int32_t *pairs, int32_t n_pairs, void *k_po
 cudaError_t launch_decode(const DecodeArgs &a, int num_sms, cudaStream_t stream, const WriteArgs *write = nullptr);
 cudaError_t launch_prefill(const PrefillArgs &a, int num_sms, cudaStream_t stream);
 
+// The limit in nanoseconds of the kernels' pipeline waits (default 4 s; see
+// pkv_set_pipeline_wait_ns in pagedkv.h), read when a launch is prepared.
+unsigned long long pipeline_wait_ns();
+
 // Driver entry point for tensor-map encoding (resolved once through cudart,
 // so the library does not link libcuda directly).  Returns CUDA_SUCCESS or
 // the driver error.

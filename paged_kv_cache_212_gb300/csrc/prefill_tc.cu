@@ -71,6 +71,7 @@ struct PrefillTcParams {
     int32_t tiles_per_seq;        // 128-row query tiles per (sequence, kv head)
     int32_t pairs_per_seq;        // CTAs per (sequence, kv head)
     int32_t n_seqs, n_kv_heads;
+    unsigned long long wait_ns;   // limit of the pipeline waits
 };
 
 // Batches of at most this many sequences are scheduled longest prefix first.
@@ -380,7 +381,7 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(const __grid_constan
             }
             if (j + 1 < n_kt) blk = load_block(j + 1);
             const int st = j % NSL, use = j / NSL;
-            if (lane == 0 && !mbar_wait(&empty[st], (use & 1) ^ 1, abort_flag)) {
+            if (lane == 0 && !mbar_wait(&empty[st], (use & 1) ^ 1, abort_flag, p.wait_ns)) {
                 report(p.dev_status, PKV_DEV_TIMEOUT);
                 *abort_flag = 1;
             }
@@ -411,8 +412,8 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(const __grid_constan
         const uint32_t idesc_o = umma_idesc_bf16(kTM, D, false, true);
         bool ok = true;
         if (lane == 0) {
-            auto wait_k = [&](int j) { return mbar_wait(&k_full[j % NK], (j / NK) & 1, abort_flag); };
-            auto wait_v = [&](int j) { return mbar_wait(&v_full[j % NV], (j / NV) & 1, abort_flag); };
+            auto wait_k = [&](int j) { return mbar_wait(&k_full[j % NK], (j / NK) & 1, abort_flag, p.wait_ns); };
+            auto wait_v = [&](int j) { return mbar_wait(&v_full[j % NV], (j / NV) & 1, abort_flag, p.wait_ns); };
             // S_tj = Q_t K_j^T, then the commit that hands S_tj to warpgroup t
             // Descriptors of a tile are built once and stepped by constants: the
             // start-address field is addr / 16 (14 bits, shared addresses < 256 KiB),
@@ -436,7 +437,7 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(const __grid_constan
                 }
                 umma_commit(&s_full[t]);
             };
-            ok = mbar_wait(q_full, 0, abort_flag) && wait_k(0);
+            ok = mbar_wait(q_full, 0, abort_flag, p.wait_ns) && wait_k(0);
             if (ok) {
                 tc_fence_after();
                 for (int t = 0; t < kNQ; ++t) issue_s(t, 0);
@@ -447,7 +448,7 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(const __grid_constan
                 if (!ok) break;
                 const uint64_t v_desc = umma_desc_sw128(smem_u32(v_ring + (j % NV) * kSlotBytes), 2048, 1024);
                 for (int t = 0; t < kNQ && ok; ++t) {
-                    ok = mbar_wait(&p_full[t], j & 1, abort_flag);
+                    ok = mbar_wait(&p_full[t], j & 1, abort_flag, p.wait_ns);
                     if (!ok) break;
                     tc_fence_after();
                     // O_t += P_tj V_j: A = P (TMEM, 8 columns per 16 keys), B = V (MN-major:
@@ -494,7 +495,7 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(const __grid_constan
         float m = -INFINITY, l = 0.f;
         bool ok = n_kt > 0;
         for (int j = 0; j < n_kt && ok; ++j) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[qt], j & 1, abort_flag));
+            ok = __all_sync(0xffffffffu, mbar_wait(&s_full[qt], j & 1, abort_flag, p.wait_ns));
             if (!ok) break;
             tc_fence_after();
             const int32_t key_base = j * kTN;
@@ -571,7 +572,7 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(const __grid_constan
             // last tile: V rows of keys past the last one may hold anything; zero
             // them once V_j has landed (both warpgroups write the same zeros)
             if (j == n_kt - 1 && (n_keys & 15) != 0) {
-                ok = __all_sync(0xffffffffu, mbar_wait(&v_full[j % NV], (j / NV) & 1, abort_flag));
+                ok = __all_sync(0xffffffffu, mbar_wait(&v_full[j % NV], (j / NV) & 1, abort_flag, p.wait_ns));
                 if (!ok) break;
                 const int first = n_keys - key_base, stop = ((n_keys + 15) & ~15) - key_base;
                 uint8_t *vs = v_ring + (j % NV) * kSlotBytes;
@@ -587,7 +588,7 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(const __grid_constan
             if (lane == 0) mbar_arrive(&p_full[qt]);
         }
         if (ok && n_kt > 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&o_done[qt], 0, abort_flag));
+            ok = __all_sync(0xffffffffu, mbar_wait(&o_done[qt], 0, abort_flag, p.wait_ns));
             tc_fence_after();
         }
         if (ok && n_kt > 0) {
@@ -647,6 +648,7 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream)
     p.out = static_cast<__nv_bfloat16 *>(a.out);
     p.lse_out = a.lse_out;
     p.dev_status = a.dev_status;
+    p.wait_ns = pipeline_wait_ns();
     const int pos_per_tile = kTM / G;
     p.tiles_per_seq = (a.chunk + pos_per_tile - 1) / pos_per_tile;
     p.pairs_per_seq = (p.tiles_per_seq + kNQ - 1) / kNQ;

@@ -176,3 +176,11 @@ def test_decode_step_argument_checks(lib):
     assert f(*args) == 1                           # the decode's checks apply
     args = list(base); args[20] = None
     assert f(*args) == 4
+
+
+def test_pipeline_wait_limit_setter(lib):
+    """pkv_set_pipeline_wait_ns (host state only): returns the previous limit;
+    0 restores the 4 s default."""
+    assert lib.pkv_set_pipeline_wait_ns(123) == 4_000_000_000
+    assert lib.pkv_set_pipeline_wait_ns(0) == 123
+    assert lib.pkv_set_pipeline_wait_ns(0) == 4_000_000_000
