@@ -184,7 +184,8 @@ int paged_kv_copy_blocks(const int32_t *pairs, int32_t n_pairs, void *k_pool, vo
  * PagedAttentionScratch).  max_total_ctx_tokens bounds sum_s ctx_lens[s];
  * split_tokens as passed to paged_decode_attention (0 = automatic: the size
  * then covers every split the automatic choice can make).  Returns 0 on
- * invalid arguments.
+ * invalid arguments, a max_total_ctx_tokens above n_seqs * INT32_MAX among
+ * them.
  */
 size_t pkv_decode_workspace_bytes(int32_t n_seqs, int32_t n_q_heads, int32_t head_dim,
                                   int64_t max_total_ctx_tokens, int32_t split_tokens);
@@ -283,7 +284,9 @@ int paged_prefill_attention(const pkv_bf16 *q, int32_t n_q_heads, const pkv_bf16
  *       array, the call returns PKV_ERR_WORKSPACE and enqueues nothing.
  * The first call on a device looks up the array's device address (one
  * cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture.  All calls share the one array and it keeps the
+ * before any stream capture.  The address is kept for the life of the
+ * process, so a cudaDeviceReset after the first call is not supported.  A
+ * max_total_ctx_tokens above n_seqs * INT32_MAX is PKV_ERR_INVALID_ARG.  All calls share the one array and it keeps the
  * last call's contents (nothing in it needs to start at zero: each call
  * rewrites what it reads).  Calls whose work overlaps on the GPU -- on
  * different streams, or from different threads without ordering -- race on

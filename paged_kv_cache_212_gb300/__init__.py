@@ -163,6 +163,32 @@ def _need(t, name, dtype=None, ndim=None, device=None):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _shape(t, name, shape):
+    """A tensor of the wrong shape would become an out-of-bounds device access:
+    refuse it here."""
+    if t is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _check_status(dev_status, device):
+    if dev_status is not None:
+        _need(dev_status, "dev_status", torch.int32, None, device)
+        if dev_status.numel() < 1:
+            raise ValueError("dev_status needs at least one int32")
+
+
+def _check_pools(k_pool, v_pool, k_scales=None, v_scales=None):
+    _shape(v_pool, "v_pool", k_pool.shape)
+    _shape(k_scales, "k_scales", k_pool.shape[:3])
+    _shape(v_scales, "v_scales", k_pool.shape[:3])
+
+
+def _check_batch(n_seqs, block_tables, lens, lens_name):
+    if block_tables.shape[0] != n_seqs:
+        raise ValueError(f"block_tables has {block_tables.shape[0]} rows for {n_seqs} sequences")
+    _shape(lens, lens_name, (n_seqs,))
+
+
 def pool_dims(k_pool: torch.Tensor) -> Dims:
     """Geometry of a [n_blocks + 1, block_size, n_kv_heads, head_dim] pool (the
     last row is the scratch block)."""
@@ -178,8 +204,11 @@ def paged_kv_write(k_new, v_new, k_pool, v_pool, block_tables, start_pos, dev_st
         _need(t, n, torch.bfloat16, 4, k_pool.device)
     _need(block_tables, "block_tables", torch.int32, 2, k_pool.device)
     _need(start_pos, "start_pos", torch.int32, 1, k_pool.device)
-    if dev_status is not None:
-        _need(dev_status, "dev_status", torch.int32, None, k_pool.device)
+    _check_status(dev_status, k_pool.device)
+    _check_pools(k_pool, v_pool)
+    _shape(k_new, "k_new", (k_new.shape[0], k_new.shape[1]) + tuple(k_pool.shape[2:]))
+    _shape(v_new, "v_new", k_new.shape)
+    _check_batch(k_new.shape[0], block_tables, start_pos, "start_pos")
     st = lib.paged_kv_write(_ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool), pool_dims(k_pool),
                             _ptr(block_tables), block_tables.shape[1], _ptr(start_pos), k_new.shape[0],
                             k_new.shape[1], _ptr(dev_status), _stream(stream))
@@ -199,6 +228,11 @@ def paged_kv_write_int8(k_new, v_new, k_pool, v_pool, k_scales, v_scales, block_
     _need(v_scales, "v_scales", torch.float32, 3, dev)
     _need(block_tables, "block_tables", torch.int32, 2, dev)
     _need(start_pos, "start_pos", torch.int32, 1, dev)
+    _check_status(dev_status, dev)
+    _check_pools(k_pool, v_pool, k_scales, v_scales)
+    _shape(k_new, "k_new", (k_new.shape[0], k_new.shape[1]) + tuple(k_pool.shape[2:]))
+    _shape(v_new, "v_new", k_new.shape)
+    _check_batch(k_new.shape[0], block_tables, start_pos, "start_pos")
     st = lib.paged_kv_write_int8(_ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool), _ptr(k_scales),
                                  _ptr(v_scales), pool_dims(k_pool), _ptr(block_tables), block_tables.shape[1],
                                  _ptr(start_pos), k_new.shape[0], k_new.shape[1], _ptr(dev_status),
@@ -224,6 +258,11 @@ def paged_kv_gather(k_pool, v_pool, block_tables, lens, out_tokens, k_out=None, 
         v_out = torch.empty(shape, dtype=torch.bfloat16, device=dev)
     _need(k_out, "k_out", torch.bfloat16, 4, dev)
     _need(v_out, "v_out", torch.bfloat16, 4, dev)
+    _check_status(dev_status, dev)
+    _check_pools(k_pool, v_pool)
+    _check_batch(n_seqs, block_tables, lens, "lens")
+    _shape(k_out, "k_out", shape)
+    _shape(v_out, "v_out", shape)
     st = lib.paged_kv_gather(_ptr(k_pool), _ptr(v_pool), pool_dims(k_pool), _ptr(block_tables),
                              block_tables.shape[1], _ptr(lens), n_seqs, int(out_tokens), _ptr(k_out), _ptr(v_out),
                              _ptr(dev_status), _stream(stream))
@@ -244,6 +283,10 @@ def paged_kv_copy_blocks(pairs, k_pool, v_pool, k_scales=None, v_scales=None, de
     else:
         _need(k_pool, "k_pool", torch.bfloat16, 4, dev)
     _need(v_pool, "v_pool", k_pool.dtype, 4, dev)
+    _check_status(dev_status, dev)
+    _check_pools(k_pool, v_pool, k_scales if int8 else None, v_scales if int8 else None)
+    if pairs.shape[1] != 2:
+        raise ValueError(f"pairs must be [n, 2], got {tuple(pairs.shape)}")
     st = lib.paged_kv_copy_blocks(_ptr(pairs), pairs.shape[0], _ptr(k_pool), _ptr(v_pool), _ptr(k_scales),
                                   _ptr(v_scales), PKV_KV_INT8 if int8 else PKV_KV_BF16, pool_dims(k_pool),
                                   _ptr(dev_status), _stream(stream))
@@ -258,6 +301,18 @@ def decode_workspace_bytes(n_seqs, n_q_heads, head_dim, max_total_ctx_tokens, sp
     if n == 0:
         raise ValueError("invalid arguments to pkv_decode_workspace_bytes")
     return int(n)
+
+
+def _check_decode(q, k_pool, v_pool, k_scales, v_scales, block_tables, ctx_lens, out, lse_out, dev_status):
+    """Shapes of a decode call's tensors against q [n_seqs, Hq, D] and the pool."""
+    n_seqs, n_q_heads, D = q.shape
+    _check_status(dev_status, q.device)
+    _check_pools(k_pool, v_pool, k_scales, v_scales)
+    if k_pool.shape[3] != D:
+        raise ValueError(f"q has head_dim {D}, the pool {k_pool.shape[3]}")
+    _check_batch(n_seqs, block_tables, ctx_lens, "ctx_lens")
+    _shape(out, "out", q.shape)
+    _shape(lse_out, "lse_out", (n_seqs, n_q_heads))
 
 
 def paged_decode_attention(q, k_pool, v_pool, block_tables, ctx_lens, softmax_scale, k_scales=None,
@@ -284,6 +339,7 @@ def paged_decode_attention(q, k_pool, v_pool, block_tables, ctx_lens, softmax_sc
     _need(out, "out", torch.bfloat16, 3, dev)
     if lse_out is not None:
         _need(lse_out, "lse_out", torch.float32, 2, dev)
+    _check_decode(q, k_pool, v_pool, k_scales, v_scales, block_tables, ctx_lens, out, lse_out, dev_status)
     if workspace is None:
         if max_total_ctx_tokens is None:
             max_total_ctx_tokens = n_seqs * block_tables.shape[1] * k_pool.shape[1]
@@ -328,6 +384,10 @@ def paged_decode_step(k_new, v_new, start_pos, q, k_pool, v_pool, block_tables, 
     _need(out, "out", torch.bfloat16, 3, dev)
     if lse_out is not None:
         _need(lse_out, "lse_out", torch.float32, 2, dev)
+    _check_decode(q, k_pool, v_pool, k_scales, v_scales, block_tables, ctx_lens, out, lse_out, dev_status)
+    _shape(k_new, "k_new", (n_seqs, k_new.shape[1]) + tuple(k_pool.shape[2:]))
+    _shape(v_new, "v_new", k_new.shape)
+    _shape(start_pos, "start_pos", (n_seqs,))
     if workspace is None:
         if max_total_ctx_tokens is None:
             max_total_ctx_tokens = n_seqs * block_tables.shape[1] * k_pool.shape[1]
@@ -367,6 +427,7 @@ def paged_decode_attention_noalloc(q, k_pool, v_pool, block_tables, ctx_lens, so
     _need(out, "out", torch.bfloat16, 3, dev)
     if lse_out is not None:
         _need(lse_out, "lse_out", torch.float32, 2, dev)
+    _check_decode(q, k_pool, v_pool, k_scales, v_scales, block_tables, ctx_lens, out, lse_out, dev_status)
     n_seqs, n_q_heads, _ = q.shape
     st = lib.paged_decode_attention_noalloc(_ptr(q), n_q_heads, _ptr(k_pool), _ptr(v_pool), _ptr(k_scales),
                                             _ptr(v_scales), PKV_KV_INT8 if int8 else PKV_KV_BF16,
@@ -395,6 +456,13 @@ def paged_prefill_attention(q, k_pool, v_pool, block_tables, prefix_lens, softma
     _need(out, "out", torch.bfloat16, 4, dev)
     if lse_out is not None:
         _need(lse_out, "lse_out", torch.float32, 3, dev)
+    _check_status(dev_status, dev)
+    _check_pools(k_pool, v_pool)
+    if k_pool.shape[3] != q.shape[3]:
+        raise ValueError(f"q has head_dim {q.shape[3]}, the pool {k_pool.shape[3]}")
+    _check_batch(n_seqs, block_tables, prefix_lens, "prefix_lens")
+    _shape(out, "out", q.shape)
+    _shape(lse_out, "lse_out", q.shape[:3])
     st = lib.paged_prefill_attention(_ptr(q), n_q_heads, _ptr(k_pool), _ptr(v_pool), pool_dims(k_pool),
                                      _ptr(block_tables), block_tables.shape[1], _ptr(prefix_lens), n_seqs,
                                      chunk, float(softmax_scale), _ptr(out), _ptr(lse_out), _ptr(dev_status),
@@ -546,6 +614,12 @@ def paged_kv_stage_blocks(pairs, host_k, host_v, pool_k, pool_v, dev_status=None
             raise ValueError(f"{n} must be a contiguous bf16 CPU tensor [n_host_blocks, bs, Hkv, D]")
     _need(pool_k, "pool_k", torch.bfloat16, 4, dev)
     _need(pool_v, "pool_v", torch.bfloat16, 4, dev)
+    _check_status(dev_status, dev)
+    _check_pools(pool_k, pool_v)
+    if pairs.shape[1] != 2:
+        raise ValueError(f"pairs must be [n, 2], got {tuple(pairs.shape)}")
+    if tuple(host_k.shape[1:]) != tuple(pool_k.shape[1:]) or host_v.shape != host_k.shape:
+        raise ValueError("host_k / host_v blocks must match the scratch pool's [bs, Hkv, D]")
     st = lib.paged_kv_stage_blocks(_ptr(pairs), pairs.shape[0], ctypes.c_void_p(host_k.data_ptr()),
                                    ctypes.c_void_p(host_v.data_ptr()), host_k.shape[0], _ptr(pool_k), _ptr(pool_v),
                                    pool_dims(pool_k), _ptr(dev_status), _stream(stream))
@@ -582,6 +656,18 @@ def paged_decode_streamed(q, host_k, host_v, pool_k, pool_v, scratch_pool, host_
     n_seqs, n_q_heads, D = q.shape
     if out is None:
         out = torch.empty_like(q)
+    _need(out, "out", torch.bfloat16, 3, dev)
+    if lse_out is not None:
+        _need(lse_out, "lse_out", torch.float32, 2, dev)
+    _check_status(dev_status, dev)
+    _check_pools(pool_k, pool_v)
+    if tuple(host_k.shape[1:]) != tuple(pool_k.shape[1:]) or host_v.shape != host_k.shape:
+        raise ValueError("host_k / host_v blocks must match the scratch pool's [bs, Hkv, D]")
+    if pool_k.shape[3] != D:
+        raise ValueError(f"q has head_dim {D}, the pool {pool_k.shape[3]}")
+    _check_batch(n_seqs, host_tables, ctx_lens, "ctx_lens")
+    _shape(out, "out", q.shape)
+    _shape(lse_out, "lse_out", (n_seqs, n_q_heads))
     if workspace is None:
         workspace = torch.empty(streamed_workspace_bytes(n_seqs, n_q_heads, D, pool_k.shape[0] - 1,
                                                          pool_k.shape[1]), dtype=torch.uint8, device=dev)

@@ -231,6 +231,9 @@ size_t pkv_decode_workspace_bytes(int32_t n_seqs, int32_t n_q_heads, int32_t hea
     if (n_seqs < 0 || n_q_heads <= 0 || head_dim <= 0 || max_total_ctx_tokens < 0 || split_tokens < 0 ||
         (split_tokens > 0 && split_tokens % 16 != 0))
         return 0;
+    // no sequence attends more than INT32_MAX tokens: a larger bound is an
+    // error (and keeps the slot arithmetic below far from overflow)
+    if (max_total_ctx_tokens > (int64_t)n_seqs * 0x7fffffffLL) return 0;
     return decode_workspace_bytes(n_seqs, n_q_heads, head_dim,
                                   (int64_t)decode_capacity_for(n_seqs, max_total_ctx_tokens, split_tokens));
 }

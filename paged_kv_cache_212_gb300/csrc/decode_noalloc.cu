@@ -27,6 +27,9 @@ static __device__ __align__(256) uint8_t g_decode_scratch[kNoAllocScratchBytes];
 // Device address of g_decode_scratch per device ordinal.  In host code the
 // array's name is only a host-side stand-in, so the real address comes from
 // cudaGetSymbolAddress, looked up once per device with that device current.
+// The address is kept for the life of the process: a cudaDeviceReset (or
+// anything else that destroys the device's primary context) after the first
+// call is not supported, since the array may then live at another address.
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mutex;
 void *g_scratch_addr[kMaxDevices];
@@ -65,7 +68,8 @@ extern "C" int paged_decode_attention_noalloc(const pkv_bf16 *q, int32_t n_q_hea
                                               int64_t max_total_ctx_tokens, pkv_bf16 *out, float *lse_out,
                                               int32_t *dev_status, pkv_stream_t stream)
 {
-    if (n_seqs < 0 || n_q_heads <= 0 || dims.head_dim <= 0 || max_total_ctx_tokens < 0 || split_tokens < 0)
+    if (n_seqs < 0 || n_q_heads <= 0 || dims.head_dim <= 0 || max_total_ctx_tokens < 0 || split_tokens < 0 ||
+        max_total_ctx_tokens > (int64_t)n_seqs * 0x7fffffffLL)
         return PKV_ERR_INVALID_ARG;
     if (n_seqs == 0) return PKV_OK;
     // Reject requests whose scratch would not fit in the static array.

@@ -45,13 +45,30 @@ def _errors(a, b):
     return float(d.max()), float(d.mean())
 
 
-@pytest.mark.parametrize("make,tol_max,tol_mean", [
-    (lambda: W.decode_workload("ragged", 31, [1, 15, 16, 17, 300, 777, 2000], 32, 8, 128, 16), BF16_MAX,
-     BF16_MEAN),
-    (lambda: W.decode_workload("int8", 32, [5, 90, 1200], 16, 4, 128, 32, n_new=2, kv_format="int8"), INT8_MAX,
-     None),
+def _ragged():
+    return W.decode_workload("ragged", 31, [1, 15, 16, 17, 300, 777, 2000], 32, 8, 128, 16)
+
+
+def _int8():
+    return W.decode_workload("int8", 32, [5, 90, 1200], 16, 4, 128, 32, n_new=2, kv_format="int8")
+
+
+def _tiny():
+    # one wave of (sequence, kv head) units with contexts of at most 256 tokens:
+    # automatic splitting takes the one-launch path, which uses no scratch
+    return W.decode_workload("tiny", 34, [10, 100, 255], 16, 4, 128, 16)
+
+
+# split 64: several fixed splits per sequence, so the shared scratch carries
+# partials; split 0: the automatic balanced split over the whole array
+@pytest.mark.parametrize("make,split,tol_max,tol_mean", [
+    (_ragged, 64, BF16_MAX, BF16_MEAN),
+    (_int8, 64, INT8_MAX, None),
+    (_ragged, 0, BF16_MAX, BF16_MEAN),
+    (_int8, 0, INT8_MAX, None),
+    (_tiny, 0, BF16_MAX, BF16_MEAN),
 ])
-def test_noalloc_matches_workspace_entry_point_on_two_calls(P, make, tol_max, tol_mean):
+def test_noalloc_matches_workspace_entry_point_on_two_calls(P, make, split, tol_max, tol_mean):
     w = make()
     kp, vp, ks, vs = oracle_pools_after_step(w)
     gk, gv = _dev(kp), _dev(vp)
@@ -61,7 +78,6 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(P, make, tol_max, to
     q = w.q.cuda()
     tables, ctx = w.tables.cuda(), w.ctx_lens.cuda()
     total = int(w.ctx_lens.sum())
-    split = 64  # several splits per sequence, so the shared scratch carries partials
     ref_lse = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
     ref = P.paged_decode_attention(q, gk, gv, tables, ctx, w.softmax_scale, k_scales=gks, v_scales=gvs,
                                    split_tokens=split, lse_out=ref_lse)
