@@ -412,8 +412,12 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(const __grid_constan
         const uint32_t idesc_o = umma_idesc_bf16(kTM, D, false, true);
         bool ok = true;
         if (lane == 0) {
-            auto wait_k = [&](int j) { return mbar_wait(&k_full[j % NK], (j / NK) & 1, abort_flag, p.wait_ns); };
-            auto wait_v = [&](int j) { return mbar_wait(&v_full[j % NV], (j / NV) & 1, abort_flag, p.wait_ns); };
+            // The issuing thread bounds the prefill: its waits keep the default
+            // limit, which compiles to the plain wait (the settable limit is
+            // taken by the producers and the softmax warps; when theirs runs
+            // out, the abort flag ends these waits too).
+            auto wait_k = [&](int j) { return mbar_wait(&k_full[j % NK], (j / NK) & 1, abort_flag); };
+            auto wait_v = [&](int j) { return mbar_wait(&v_full[j % NV], (j / NV) & 1, abort_flag); };
             // S_tj = Q_t K_j^T, then the commit that hands S_tj to warpgroup t
             // Descriptors of a tile are built once and stepped by constants: the
             // start-address field is addr / 16 (14 bits, shared addresses < 256 KiB),
@@ -437,7 +441,7 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(const __grid_constan
                 }
                 umma_commit(&s_full[t]);
             };
-            ok = mbar_wait(q_full, 0, abort_flag, p.wait_ns) && wait_k(0);
+            ok = mbar_wait(q_full, 0, abort_flag) && wait_k(0);
             if (ok) {
                 tc_fence_after();
                 for (int t = 0; t < kNQ; ++t) issue_s(t, 0);
@@ -448,7 +452,7 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(const __grid_constan
                 if (!ok) break;
                 const uint64_t v_desc = umma_desc_sw128(smem_u32(v_ring + (j % NV) * kSlotBytes), 2048, 1024);
                 for (int t = 0; t < kNQ && ok; ++t) {
-                    ok = mbar_wait(&p_full[t], j & 1, abort_flag, p.wait_ns);
+                    ok = mbar_wait(&p_full[t], j & 1, abort_flag);
                     if (!ok) break;
                     tc_fence_after();
                     // O_t += P_tj V_j: A = P (TMEM, 8 columns per 16 keys), B = V (MN-major:
