@@ -25,6 +25,7 @@ runs of the other four scenarios and of the page writes in the line
   --config 0         the tiny, L2-resident decode step: per-call medians, warm and flushed
   --layers L         an L-layer decode step, eager launches against one CUDA graph
   --stream N_SLOTS   config 1 decoded from a pinned host tier through N_SLOTS scratch blocks
+  --writes           the page writes alone: int8 at 64 x 16 tokens, bf16 at 8 x 512-token chunks
   --blocks           the host-side block manager's serving loop (no GPU)
   --impl reference   the float64 oracle on the host cores, bounded samples
 """
@@ -51,10 +52,10 @@ FALLBACK_HBM_GBS = 6800.0
 # for config 3), from the ncu captures summarised under profiles/, valid while
 # the kernel's sources hash to source_sha.
 NCU_TRAFFIC = {
-    "decode": {"sources": ("decode.cu", "common.cuh", "launch.h"), "source_sha": "3f5b4d465385e7e8",
-               "bytes_per_launch": {1: 544729856 + 4279552, 2: 310421504 + 3900160, 4: 1345788672 + 33092352}},
-    "prefill": {"sources": ("prefill_tc.cu", "common.cuh", "launch.h"), "source_sha": "afce10efbd08fc2c",
-                "bytes_per_launch": {3: 199709952 + 19170048}},
+    "decode": {"sources": ("decode.cu", "common.cuh", "launch.h"), "source_sha": "97f1ea42c27b8e34",
+               "bytes_per_launch": {1: 544745472 + 3934464, 2: 310416896 + 3853312, 4: 1317263360 + 32973312}},
+    "prefill": {"sources": ("prefill_tc.cu", "common.cuh", "launch.h"), "source_sha": "c163eb2119b9c314",
+                "bytes_per_launch": {3: 197486848 + 18785792}},
 }
 
 
@@ -74,6 +75,8 @@ def parse_args():
                     help="time the host-side block manager's per-step calls instead (no GPU)")
     ap.add_argument("--stream", type=int, default=0, metavar="N_SLOTS",
                     help="decode config 1 from a pinned host tier through an N_SLOTS-block scratch pool")
+    ap.add_argument("--writes", action="store_true",
+                    help="time the page writes alone (int8 write at 64 x 16 tokens, bf16 write of 8 x 512-token chunks)")
     ap.add_argument("--layers", type=int, default=0, metavar="L",
                     help="time an L-layer decode step (write + decode per layer, each layer its own pools), "
                          "eager launches against one CUDA graph of the whole step")
@@ -1033,6 +1036,13 @@ def main():
     import paged_kv_cache_212_gb300 as P
     P.load_library()
 
+    if args.writes:
+        if rank == 0:
+            print(json.dumps({"metric": "page write GB/s", "unit": "GB/s", "n_gpus": 1, "data": "synthetic",
+                              "writes": bench_writes(P, device, measured_peaks()[0])}), flush=True)
+        if world > 1:
+            dist.destroy_process_group()
+        return
     if args.stream or args.layers:
         if rank == 0:
             (run_stream_bench if args.stream else run_layers_bench)(args, P, device)

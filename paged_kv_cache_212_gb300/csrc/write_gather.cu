@@ -20,9 +20,10 @@ __global__ void __launch_bounds__(256) write_bf16_kernel(const WriteArgs a)
 }
 
 // Quantised write: four kv heads of one token's K or V row per warp unit
-// (write_rows.cuh).
+// (write_rows.cuh).  At most 64 registers: four resident CTAs per SM, so a
+// 64 x 16-token write (512 CTAs) runs in one wave.
 template <int EPL>
-__global__ void __launch_bounds__(256) write_int8_kernel(const WriteArgs a, float *k_scales, float *v_scales)
+__global__ void __launch_bounds__(256, 4) write_int8_kernel(const WriteArgs a, float *k_scales, float *v_scales)
 {
     const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     write_int8_units<EPL>(a, k_scales, v_scales, warp, (int64_t)gridDim.x * (blockDim.x >> 5));
