@@ -45,6 +45,9 @@ namespace {
 
 constexpr int kStageTokens = 16;
 constexpr int kMaxStages = 8;
+// the running maximum of the online softmax lags the true one by at most this
+// (log2 units): probabilities stay at most 2^8
+constexpr float kLazyMax = 8.0f;
 constexpr uint32_t kHdrCounter = 0, kHdrTotal = 1, kHdrOverflow = 2, kHdrChunk = 3, kHdrStages = 4;
 constexpr int32_t kMinChunkStages = 4;   // balanced items hold at least 64 tokens
 
@@ -995,21 +998,24 @@ __global__ void __launch_bounds__(288, INT8 ? 1 : 2) decode_split_kernel(const _
                 x2 = v1 ? s4[2] * p.scale_log2 : -INFINITY;
                 x3 = v1 ? s4[3] * p.scale_log2 : -INFINITY;
             }
-            float bm0 = fmaxf(x0, x2), bm1 = fmaxf(x1, x3);
+            // Lazy running maximum (log2 units): it moves only when a score of
+            // the stage passes it by more than kLazyMax, so the probabilities
+            // stay at most 2^kLazyMax, and the row reduction and the rescale of
+            // the accumulators run only then (o = acc / l and lse = m + log2 l
+            // do not depend on which m was used).
+            if (__any_sync(0xffffffffu, fmaxf(x0, x2) > m0 + kLazyMax || fmaxf(x1, x3) > m1 + kLazyMax)) {
+                float bm0 = fmaxf(x0, x2), bm1 = fmaxf(x1, x3);
 #pragma unroll
-            for (int off = 4; off < 32; off <<= 1) {
-                bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
-                bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
-            }
-            const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
-            const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
-            const float p0 = fast_exp2(x0 - mn0), p1 = fast_exp2(x1 - mn1);
-            const float p2 = fast_exp2(x2 - mn0), p3 = fast_exp2(x3 - mn1);
-            m0 = mn0;
-            m1 = mn1;
-            l0 = l0 * al0 + p0 + p2;
-            l1 = l1 * al1 + p1 + p3;
-            if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+                for (int off = 4; off < 32; off <<= 1) {
+                    bm0 = fmaxf(bm0, __shfl_xor_sync(0xffffffffu, bm0, off));
+                    bm1 = fmaxf(bm1, __shfl_xor_sync(0xffffffffu, bm1, off));
+                }
+                const float mn0 = fmaxf(m0, bm0), mn1 = fmaxf(m1, bm1);
+                const float al0 = fast_exp2(m0 - mn0), al1 = fast_exp2(m1 - mn1);
+                m0 = mn0;
+                m1 = mn1;
+                l0 *= al0;
+                l1 *= al1;
 #pragma unroll
                 for (int mt = 0; mt < KSTEPS; ++mt) {
                     acc[mt][0] *= al0;
@@ -1020,6 +1026,10 @@ __global__ void __launch_bounds__(288, INT8 ? 1 : 2) decode_split_kernel(const _
                 ps0 *= al0;
                 ps1 *= al1;
             }
+            const float p0 = fast_exp2(x0 - m0), p1 = fast_exp2(x1 - m1);
+            const float p2 = fast_exp2(x2 - m0), p3 = fast_exp2(x3 - m1);
+            l0 += p0 + p2;
+            l1 += p1 + p3;
             // P^T as the B operand of O^T += V^T P^T (int8: fold the V scale into
             // P, and add the fp16 P' actually used to the bias correction's sum)
             uint32_t pb0, pb1;
