@@ -8,7 +8,7 @@ len + 1 tokens.  Inputs are resident in HBM; the decode reads ~604 MB of K/V
 pages per step, far more than the 129 MB L2, so no flush is needed between
 steps.
 
-  python bench.py [--gpus N --steps K --warmup W] [--config 1] [--impl reference]
+  python bench.py [--gpus N --steps K --warmup W] [--config C] [--impl reference]
 
 Prints one JSON line (rank 0).  Under torchrun every rank runs its own replica
 (independent sequences, no collective in the data path: weak scaling) and the
@@ -17,14 +17,17 @@ each timed region starts after a GPU-side hold during which the host enqueues
 the K steps, and short regions are repeated (median reported) so that the
 timed work adds up to ~150 ms.  The default single-GPU run also nests short
 runs of the other four scenarios and of the page writes in the line
-(`other_configs`).  Other modes (each prints its own JSON line):
+(`other_configs`).  `--config C` picks the workload (workloads.WORKLOADS):
+1 the Llama-3-8B-shaped decode above (the default), 2 the same shapes with int8
+pages and 16 new tokens per sequence (the gather of 16 x 2048 tokens timed
+beside it), 4 256 skewed sequences sharing prefixes with 512-token splits,
+3 chunked prefill (8 sequences, 512-token chunks) on the tensor cores
+(TFLOP/s), 0 the tiny L2-resident decode step (per-call medians, warm and
+flushed).  Other modes (each prints its own JSON line):
 
-  --config 2 / 4     int8 pages with 16 new tokens (and the gather beside it) /
-                     256 skewed sequences sharing prefixes, 512-token splits
-  --config 3         chunked prefill on the tensor cores (TFLOP/s)
-  --config 0         the tiny, L2-resident decode step: per-call medians, warm and flushed
   --layers L         an L-layer decode step, eager launches against one CUDA graph
-  --stream N_SLOTS   config 1 decoded from a pinned host tier through N_SLOTS scratch blocks
+  --stream N_SLOTS   the Llama-3-8B-shaped batch decoded from a pinned host tier
+                     through N_SLOTS scratch blocks
   --writes           the page writes alone: int8 at 64 x 16 tokens, bf16 at 8 x 512-token chunks
   --blocks           the host-side block manager's serving loop (no GPU)
   --impl reference   the float64 oracle on the host cores, bounded samples
@@ -44,16 +47,17 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "paged decode attention HBM GB/s (% of GB300 peak) and seq-steps/s per layer"
-PREFILL_METRIC = "chunked paged prefill attention TFLOP/s (config 3)"
+PREFILL_METRIC = "chunked paged prefill attention TFLOP/s (8 sequences, 512-token chunks)"
 FALLBACK_HBM_GBS = 6800.0
 
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch of the dominant
-# kernel per workload (decode_split_kernel for configs 1, 2, 4; prefill_tc_kernel
-# for config 3), from the ncu captures summarised under profiles/, valid while
+# kernel per workload number (decode_split_kernel for the decode workloads 1, 2
+# and 4; prefill_tc_kernel for the prefill, 3), from the ncu captures summarised
+# under profiles/, valid while
 # the kernel's sources hash to source_sha.
 NCU_TRAFFIC = {
-    "decode": {"sources": ("decode.cu", "common.cuh", "launch.h"), "source_sha": "97f1ea42c27b8e34",
-               "bytes_per_launch": {1: 544745472 + 3934464, 2: 310416896 + 3853312, 4: 1317263360 + 32973312}},
+    "decode": {"sources": ("decode.cu", "common.cuh", "launch.h"), "source_sha": "b1b74ce85e3b596a",
+               "bytes_per_launch": {1: 544749568 + 3998464, 2: 310413312 + 3869440, 4: 1316489472 + 32868096}},
     "prefill": {"sources": ("prefill_tc.cu", "common.cuh", "launch.h"), "source_sha": "c163eb2119b9c314",
                 "bytes_per_launch": {3: 197486848 + 18785792}},
 }
@@ -74,7 +78,8 @@ def parse_args():
     ap.add_argument("--blocks", action="store_true",
                     help="time the host-side block manager's per-step calls instead (no GPU)")
     ap.add_argument("--stream", type=int, default=0, metavar="N_SLOTS",
-                    help="decode config 1 from a pinned host tier through an N_SLOTS-block scratch pool")
+                    help="decode the Llama-3-8B-shaped batch from a pinned host tier through an "
+                         "N_SLOTS-block scratch pool")
     ap.add_argument("--writes", action="store_true",
                     help="time the page writes alone (int8 write at 64 x 16 tokens, bf16 write of 8 x 512-token chunks)")
     ap.add_argument("--layers", type=int, default=0, metavar="L",
@@ -198,15 +203,15 @@ def ncu_traffic(kind, cfg):
 def make_workload(cfg, device):
     from paged_kv_cache_212_gb300 import workloads as W
     if cfg == 0:
-        w = W.config0(device=device)
+        w = W.tiny_decode(device=device)
     elif cfg == 1:
-        w = W.config1(device=device)
+        w = W.llama8b_decode(device=device)
     elif cfg == 3:
-        w = W.config3(device=device)
+        w = W.chunked_prefill(device=device)
     elif cfg == 2:
-        w = W.config2(device=device)
+        w = W.llama8b_decode_int8(device=device)
     else:
-        w = W.config4(device=device)
+        w = W.skewed_prefix_decode(device=device)
     return w
 
 
@@ -539,12 +544,12 @@ def bench_config(w, args):
 
 
 def bench_gather(P, device, peak, reps=200):
-    """The bf16 gather timed beside config 2: 16 sequences of 2048 tokens into a
+    """The bf16 gather timed beside the int8 decode: 16 sequences of 2048 tokens into a
     contiguous [16, 8, 2048, 128] view (K and V), CUDA events over `reps` calls.
     Algorithmic bytes: every gathered K/V row read once and written once."""
     import torch
     from paged_kv_cache_212_gb300 import workloads as W
-    w = W.config2_gather(device=device)
+    w = W.gather_16x2048(device=device)
     kp, vp, _, _ = fill_pool(P, w, device)
     tables, lens = w.tables.to(device), w.stored_lens.to(device)
     out_tokens = w.extra["out_tokens"]
@@ -577,8 +582,9 @@ def prefill_flops(w):
 
 
 def run_prefill_bench(args, P, w, device, rank, world, K, W, with_e2e=True):
-    """Config 3: paged write of each sequence's 512-token chunk, then chunked
-    paged prefill attention over prefix + chunk (tensor-core bound).  The
+    """Chunked prefill (8 sequences): paged write of each sequence's 512-token
+    chunk, then chunked paged prefill attention over prefix + chunk
+    (tensor-core bound).  The
     step (write + prefill) and the prefill call alone are each timed as K
     calls on the device (see device_timed).  Returns the JSON line."""
     import torch
@@ -735,8 +741,8 @@ def run_blocks_bench(args):
 
 
 def run_stream_bench(args, P, device):
-    """Config 1's decode with every K/V block in a pinned host tier, streamed
-    through a device scratch pool of args.stream blocks (pagedkv_stream.h).
+    """The Llama-3-8B-shaped decode with every K/V block in a pinned host tier,
+    streamed through a device scratch pool of args.stream blocks (pagedkv_stream.h).
     When the batch has more blocks than the pool, the cyclic order evicts every
     block before its reuse, so each call restages the whole context over the
     CPU-GPU link: the link bounds this path."""
@@ -799,12 +805,14 @@ def run_stream_bench(args, P, device):
     decode_b, _ = algorithmic_bytes(w)
     block_bytes = 2 * w.block_size * w.n_kv_heads * w.head_dim * 2
     staged = blocks * block_bytes if blocks > n_slots else 0
-    line = {"metric": "streamed paged decode GB/s (config 1 batch from a pinned host tier)",
+    line = {"metric": "streamed paged decode GB/s (Llama-3-8B-shaped batch 64 from a pinned host tier)",
             "value": round(decode_b / (ms * 1e-3) / 1e9, 2), "unit": "GB/s", "n_gpus": 1, "steps": steps,
             "warmup": max(3, args.warmup), "ms_per_step": round(ms, 4), "higher_is_better": True,
             "scaling": "none", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": w.name, "n_slots": n_slots, "blocks_per_call": blocks,
-                       "tiles_per_call": -(-blocks // n_slots), "host_tier_bytes": 2 * host_k.numel() * 2},
+                       # a batch larger than the pool goes in tiles of half the pool
+                       "tiles_per_call": -(-blocks // (n_slots // 2)) if blocks > n_slots else 1,
+                       "host_tier_bytes": 2 * host_k.numel() * 2},
             "staging": {"bytes_per_call": staged, "gbs": round(staged / (ms * 1e-3) / 1e9, 2)},
             "roofline": ({"bound": "host-link", "achieved": round(staged / (ms * 1e-3) / 1e9, 2),
                           "peak": round(link_gbs, 2), "unit": "GB/s",
@@ -816,8 +824,8 @@ def run_stream_bench(args, P, device):
 
 
 def run_small_bench(args, P, w, device, reps=None):
-    """Config 0 (4 sequences, all data in L2): the decode step (write + decode)
-    timed call by call with CUDA events, median of the reps, once with the
+    """The tiny decode (4 sequences, all data in L2): the decode step (write +
+    decode) timed call by call with CUDA events, median of the reps, once with the
     data warm in L2 and once with a buffer of twice the L2 size rewritten
     between reps outside the timed pair (flushed)."""
     import torch
@@ -879,13 +887,13 @@ def run_small_bench(args, P, w, device, reps=None):
 
 
 def run_layers_bench(args, P, device):
-    """An args.layers-layer decode step of config 0 or 1 (int8 pools for config
-    2): per layer the page write of the step's new rows and the paged decode
+    """An args.layers-layer decode step of workload 0, 1 or 2 (tiny, Llama-3-8B
+    shaped, its int8 variant): per layer the page write of the step's new rows and the paged decode
     over that layer's own pools (the tables are shared, as every layer of a
     model stores the same token positions), timed as eager calls and as one
     captured CUDA graph of the whole step."""
     import torch
-    assert args.config in (0, 1, 2), "the layered step covers configs 0, 1 and 2"
+    assert args.config in (0, 1, 2), "the layered step covers workloads 0, 1 and 2"
     w = make_workload(args.config, device)
     L = args.layers
     kp, vp, ks, vs = fill_pool(P, w, device)
@@ -950,7 +958,9 @@ def run_layers_bench(args, P, device):
             "dtype": "int8" if w.kv_format == "int8" else "bf16", "data": "synthetic",
             "config": {"workload": w.name, "layers": L, "launch": "one CUDA graph per step",
                        "gb_per_s": round(L * (decode_b + write_b) / (ms_graph * 1e-3) / 1e9, 2),
-                       "kernel_launches_per_step": L * 3},
+                       # the tiny decode takes the one-launch small-batch path unless PKV_DECODE_IMPL=split
+                       "kernel_launches_per_step": L * (1 if args.config == 0 and
+                                                        os.environ.get("PKV_DECODE_IMPL") != "split" else 3)},
             "eager": {"ms_per_step": round(ms_eager, 4), "value": round(w.n_seqs / (ms_eager * 1e-3), 1),
                       "gb_per_s": round(L * (decode_b + write_b) / (ms_eager * 1e-3) / 1e9, 2)},
             "clocks": clk.summary()}
@@ -1145,7 +1155,7 @@ def run_decode_bench(args, P, w, device, rank, world, K, W, with_e2e=True):
 
 def W_CONFIGS():
     from paged_kv_cache_212_gb300 import workloads as W
-    return W.CONFIGS
+    return W.WORKLOADS
 
 
 def w_index(w):

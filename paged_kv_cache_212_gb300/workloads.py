@@ -236,7 +236,7 @@ def gather_workload(name, seed, lens, n_kv_heads, head_dim, block_size, out_toke
 # sequences / shorter lengths, for oracle-sized test cases.
 # ---------------------------------------------------------------------------
 
-def config0(device="cpu") -> Workload:
+def tiny_decode(device="cpu") -> Workload:
     """Tiny decode step: stored lengths {17, 64, 100, 255}, Hq 8, Hkv 2, D 64,
     bs 16, 64 physical blocks + scratch, one new token, attend len + 1."""
     return decode_workload("tiny decode (4 seqs, Hq8/Hkv2/D64/bs16)", SEED_BASE + 0,
@@ -248,7 +248,7 @@ def _uniform_lens(gen, n, lo, hi):
     return [int(x) for x in torch.randint(lo, hi + 1, (n,), generator=gen)]
 
 
-def config1(device="cpu", n_seqs=64, lo=512, hi=4096) -> Workload:
+def llama8b_decode(device="cpu", n_seqs=64, lo=512, hi=4096) -> Workload:
     """Llama-3-8B-shaped decode: batch 64, stored lengths U[512, 4096], Hq 32,
     Hkv 8 (GQA 4), D 128, bs 16, pool 1.25x the blocks needed, one new token."""
     seed = SEED_BASE + 1
@@ -258,10 +258,10 @@ def config1(device="cpu", n_seqs=64, lo=512, hi=4096) -> Workload:
                            max_blocks=-(-(hi + 1) // 16), device=device)
 
 
-def config2(device="cpu", n_seqs=64, lo=512, hi=4096) -> Workload:
-    """Config 1 shapes with int8 pages (fp32 absmax/127 scale per token and kv
-    head); 16 new tokens per sequence are quantised, then one decode query at
-    the last position attends stored + 16 tokens."""
+def llama8b_decode_int8(device="cpu", n_seqs=64, lo=512, hi=4096) -> Workload:
+    """The Llama-3-8B-shaped decode with int8 pages (fp32 absmax/127 scale per
+    token and kv head); 16 new tokens per sequence are quantised, then one
+    decode query at the last position attends stored + 16 tokens."""
     seed = SEED_BASE + 2
     lens = _uniform_lens(torch.Generator().manual_seed(seed ^ 0x5EED), n_seqs, lo, hi)
     return decode_workload(f"int8 decode (batch {n_seqs}, ctx U[{lo + 16},{hi + 16}], "
@@ -269,14 +269,14 @@ def config2(device="cpu", n_seqs=64, lo=512, hi=4096) -> Workload:
                            max_blocks=-(-(hi + 16) // 16), kv_format="int8", device=device)
 
 
-def config2_gather(device="cpu", n_seqs=16, length=2048) -> Workload:
-    """The bf16 gather timed beside config 2: 16 sequences of 2048 tokens,
+def gather_16x2048(device="cpu", n_seqs=16, length=2048) -> Workload:
+    """The bf16 gather timed beside the int8 decode: 16 sequences of 2048 tokens,
     Hkv 8, D 128, bs 16, into a [16, 8, 2048, 128] contiguous view."""
     return gather_workload(f"gather ({n_seqs} x {length}, Hkv8/D128/bs16)", SEED_BASE + 2 + 100,
                            [length] * n_seqs, 8, 128, 16, out_tokens=length, device=device)
 
 
-def config3(device="cpu", n_seqs=8, chunk=512, prefix_hi=8192) -> Workload:
+def chunked_prefill(device="cpu", n_seqs=8, chunk=512, prefix_hi=8192) -> Workload:
     """Chunked prefill: 8 sequences with resident prefix U{0 .. 8191}, each
     appends a 512-token chunk (paged write) attended causally within the chunk
     and fully over the prefix; Hq 32, Hkv 8, D 128, bs 16."""
@@ -288,7 +288,7 @@ def config3(device="cpu", n_seqs=8, chunk=512, prefix_hi=8192) -> Workload:
                             max_blocks=-(-(prefix_hi - 1 + chunk) // 16), device=device)
 
 
-def config4(device="cpu", n_seqs=256, median=1024, max_len=32768, group=16,
+def skewed_prefix_decode(device="cpu", n_seqs=256, median=1024, max_len=32768, group=16,
             shared_tokens=512) -> Workload:
     """Long skewed decode with shared prefixes: batch 256, stored lengths
     lognormal (median 1024, sigma 1 in log space) clipped to [16, 32768] and
@@ -305,4 +305,5 @@ def config4(device="cpu", n_seqs=256, median=1024, max_len=32768, group=16,
                            group_size=group, shared_tokens=shared_tokens, device=device)
 
 
-CONFIGS = {0: config0, 1: config1, 2: config2, 3: config3, 4: config4}
+WORKLOADS = {0: tiny_decode, 1: llama8b_decode, 2: llama8b_decode_int8, 3: chunked_prefill,
+             4: skewed_prefix_decode}

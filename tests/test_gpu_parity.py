@@ -41,8 +41,9 @@ def workload(name):
     """Full-size named workloads are drawn once per session."""
     if name not in _CACHE:
         makers = {
-            "cfg0": W.config0, "cfg1": W.config1, "cfg2": W.config2, "cfg3": W.config3, "cfg4": W.config4,
-            "cfg2_gather": W.config2_gather,
+            "tiny": W.tiny_decode, "llama8b": W.llama8b_decode, "llama8b_int8": W.llama8b_decode_int8,
+            "chunked_prefill": W.chunked_prefill, "skewed_prefix": W.skewed_prefix_decode,
+            "gather_16x2048": W.gather_16x2048,
             "ragged_d64": lambda: W.decode_workload("ragged", 5, [1, 15, 16, 17, 31, 33, 200, 511], 16, 4, 64, 16),
             "ragged_g8_bs32": lambda: W.decode_workload("g8", 6, [1, 31, 32, 33, 100, 700, 1500], 64, 8, 128, 32),
             "ragged_g1": lambda: W.decode_workload("g1", 7, [3, 40, 129], 4, 4, 128, 16),
@@ -91,7 +92,7 @@ def status_tensor():
 # writes and gather: bit-exact
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("name", ["cfg0", "cfg1", "cfg3", "cfg4", "ragged_d64"])
+@pytest.mark.parametrize("name", ["tiny", "llama8b", "chunked_prefill", "skewed_prefix", "ragged_d64"])
 def test_write_bf16_bit_exact(P, name):
     w = workload(name)
     kp, vp, _, _ = pools(name, after_step=False)
@@ -105,7 +106,7 @@ def test_write_bf16_bit_exact(P, name):
     assert np.array_equal(host(gv), rv)
 
 
-@pytest.mark.parametrize("name", ["cfg2", "int8_small", "int8_d64"])
+@pytest.mark.parametrize("name", ["llama8b_int8", "int8_small", "int8_d64"])
 def test_write_int8_bit_exact(P, name):
     w = workload(name)
     kp, vp, ks, vs = pools(name, after_step=False)
@@ -123,8 +124,8 @@ def test_write_int8_bit_exact(P, name):
 
 
 def test_write_to_bad_slots_is_flagged_and_skipped(P):
-    w = workload("cfg0")
-    kp, vp, _, _ = pools("cfg0", after_step=False)
+    w = workload("tiny")
+    kp, vp, _, _ = pools("tiny", after_step=False)
     gk, gv = dev(kp), dev(vp)
     tables = w.tables.clone()
     tables[1, int(w.start_pos[1]) // w.block_size] = w.n_blocks + 5      # id out of range
@@ -141,7 +142,7 @@ def test_write_to_bad_slots_is_flagged_and_skipped(P):
     assert np.array_equal(host(gk), rk) and np.array_equal(host(gv), rv)
 
 
-@pytest.mark.parametrize("name,extra", [("cfg2_gather", 0), ("cfg0", 13), ("ragged_d64", 1), ("ragged_g8_bs32", 7)])
+@pytest.mark.parametrize("name,extra", [("gather_16x2048", 0), ("tiny", 13), ("ragged_d64", 1), ("ragged_g8_bs32", 7)])
 def test_gather_bit_exact(P, name, extra):
     w = workload(name)
     kp, vp, _, _ = pools(name, after_step=w.kind != "gather")
@@ -156,8 +157,8 @@ def test_gather_bit_exact(P, name, extra):
 
 
 def test_gather_zero_length_and_bad_length(P):
-    w = workload("cfg0")
-    kp, vp, _, _ = pools("cfg0")
+    w = workload("tiny")
+    kp, vp, _, _ = pools("tiny")
     lens = torch.tensor([0, 5, 10**6, 65], dtype=torch.int32)
     st = status_tensor()
     ko, vo = P.paged_kv_gather(dev(kp), dev(vp), i32(w.tables), i32(lens), 70, dev_status=st)
@@ -206,7 +207,7 @@ def check_lse(lse_gpu, lse_ref):
         assert np.abs(g[fin] - lse_ref[fin]).max() <= LSE_TOL
 
 
-@pytest.mark.parametrize("name", ["cfg0", "cfg1", "cfg4", "ragged_d64", "ragged_g8_bs32", "ragged_g1", "small_limits",
+@pytest.mark.parametrize("name", ["tiny", "llama8b", "skewed_prefix", "ragged_d64", "ragged_g8_bs32", "ragged_g1", "small_limits",
                                   "small_limits_d128"])
 def test_decode_bf16_parity(P, name, decode_impl):
     w = workload(name)
@@ -219,7 +220,7 @@ def test_decode_bf16_parity(P, name, decode_impl):
     check_lse(lse, ref_lse)
 
 
-@pytest.mark.parametrize("name", ["cfg2", "int8_small", "int8_d64"])
+@pytest.mark.parametrize("name", ["llama8b_int8", "int8_small", "int8_d64"])
 def test_decode_int8_parity(P, name):
     w = workload(name)
     kp, vp, ks, vs = pools(name)
@@ -243,7 +244,7 @@ def test_decode_split_sizes(P, split):
     check_lse(lse, ref_lse)
 
 
-@pytest.mark.parametrize("name", ["cfg1", "int8_small", "ragged_d64"])
+@pytest.mark.parametrize("name", ["llama8b", "int8_small", "ragged_d64"])
 def test_decode_identity_vs_permuted_tables_bit_exact(P, name, decode_impl):
     """Results do not depend on which physical pages the table names."""
     w = workload(name)
@@ -313,7 +314,7 @@ def test_decode_workspace_overflow_is_flagged(P):
 # the decode step as the benchmark runs it: GPU write, then GPU decode
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("name", ["cfg1", "cfg2"])
+@pytest.mark.parametrize("name", ["llama8b", "llama8b_int8"])
 def test_step_write_then_decode_full_size(P, name):
     w = workload(name)
     kp, vp, ks, vs = pools(name, after_step=False)
@@ -368,11 +369,11 @@ def test_prefill_parity_all_rows(P, name):
 
 
 def test_prefill_full_size_sampled_rows(P):
-    """Config 3 at full size: the GPU computes every row; the oracle checks a
-    sample of chunk rows (first, last, block boundaries, random) of every
-    sequence and head."""
-    w = workload("cfg3")
-    kp, vp, _, _ = pools("cfg3")
+    """The chunked prefill (8 sequences x 512-token chunks) at full size: the
+    GPU computes every row; the oracle checks a sample of chunk rows (first,
+    last, block boundaries, random) of every sequence and head."""
+    w = workload("chunked_prefill")
+    kp, vp, _, _ = pools("chunked_prefill")
     out, lse, st = run_prefill(P, w, kp, vp)
     assert st == 0
     rng = np.random.default_rng(0)
@@ -408,7 +409,7 @@ def test_prefill_identity_vs_permuted_tables_bit_exact(P):
 # the fused decode step: write + decode in one call
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("name", ["cfg0", "cfg1", "cfg2", "ragged_d64", "int8_small"])
+@pytest.mark.parametrize("name", ["tiny", "llama8b", "llama8b_int8", "ragged_d64", "int8_small"])
 def test_fused_decode_step(P, name, decode_impl):
     """paged_decode_step = paged_kv_write(_int8) then paged_decode_attention:
     the pool bit-exact with the oracle's write, the output identical bit for

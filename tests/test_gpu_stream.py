@@ -150,13 +150,13 @@ def test_residency_carries_over_and_invalidation_restages(P):
 
 
 def test_config1_batch_streamed_in_the_benchmarked_shape(P):
-    """The config 1 batch (8,296 blocks) from a host tier holding the oracle's
+    """The Llama-3-8B-shaped batch (8,296 blocks) from a host tier holding the oracle's
     pools, through the 2048-slot scratch pool bench.py --stream 2048 times:
     every output against the oracle's decode over the whole context."""
     from oracle_pools import dims_of, oracle_pools_after_step
     from gpu_support import NTHREADS
     from paged_kv_cache_212_gb300 import workloads as W
-    w = W.config1()
+    w = W.llama8b_decode()
     kp, vp, _, _ = oracle_pools_after_step(w, poison=True)
     code, ref, ref_lse = oracle.decode(w.q, kp, vp, dims_of(w), w.tables, w.ctx_lens, w.softmax_scale,
                                        n_threads=NTHREADS)

@@ -91,7 +91,7 @@ def _sdpa_decode(w, kp, vp):
     return o[:, :, 0].numpy()
 
 
-@pytest.mark.parametrize("make", [W.config0, lambda: _small_decode(hq=16, hkv=4, d=64, bs=32)])
+@pytest.mark.parametrize("make", [W.tiny_decode, lambda: _small_decode(hq=16, hkv=4, d=64, bs=32)])
 def test_decode_equals_sdpa_on_gathered_view(make):
     w = make()
     kp, vp, _, _ = oracle_pools_after_step(w)

@@ -149,7 +149,7 @@ def _tiny_llm_gather(pool: torch.Tensor, table: torch.Tensor) -> torch.Tensor:
 @pytest.mark.parametrize("cfg", ["tiny", "ragged"])
 def test_gather_matches_tiny_llm_view_and_zero_tail(cfg):
     if cfg == "tiny":
-        w = W.config0()
+        w = W.tiny_decode()
     else:
         w = W.gather_workload("g", 7, [1, 15, 16, 17, 70, 0], 3, 32, 16, out_tokens=80)
     kp, vp, _, _ = oracle_pools_after_step(w, poison=True)
@@ -167,7 +167,7 @@ def test_gather_matches_tiny_llm_view_and_zero_tail(cfg):
 
 
 def test_gather_round_trips_logical_rows():
-    w = W.config0()
+    w = W.tiny_decode()
     kp, vp, _, _ = oracle_pools_after_step(w)
     lens = w.ctx_lens
     st, ko, vo = oracle.gather(kp, vp, dims_of(w), w.tables, lens, int(lens.max()))
@@ -180,13 +180,13 @@ def test_gather_round_trips_logical_rows():
 
 
 def test_gather_length_beyond_view_is_reported():
-    w = W.config0()
+    w = W.tiny_decode()
     kp, vp, _, _ = oracle_pools_after_step(w)
     st, _, _ = oracle.gather(kp, vp, dims_of(w), w.tables, w.ctx_lens, 10)
     assert st == oracle.BAD_INDEX
 
 
-@pytest.mark.parametrize("make", [W.config0, lambda: W.config4(n_seqs=32, median=600,
+@pytest.mark.parametrize("make", [W.tiny_decode, lambda: W.skewed_prefix_decode(n_seqs=32, median=600,
                                                                  max_len=2000)])
 def test_tables_waste_at_most_block_size_minus_one(make):
     """tiny-llm paged_kv.py docstring: at most block_size - 1 wasted slots per
@@ -205,7 +205,7 @@ def test_tables_waste_at_most_block_size_minus_one(make):
 
 
 def test_shared_prefix_blocks_hold_one_copy():
-    w = W.config4(n_seqs=32, median=600, max_len=2000)
+    w = W.skewed_prefix_decode(n_seqs=32, median=600, max_len=2000)
     kp, vp, _, _ = oracle_pools_after_step(w)
     lens = w.ctx_lens
     st, ko, _ = oracle.gather(kp, vp, dims_of(w), w.tables, lens, int(lens.max()))
