@@ -58,8 +58,8 @@ FALLBACK_HBM_GBS = 6800.0
 NCU_TRAFFIC = {
     "decode": {"sources": ("decode.cu", "common.cuh", "launch.h"), "source_sha": "b1b74ce85e3b596a",
                "bytes_per_launch": {1: 544749568 + 3998464, 2: 310413312 + 3869440, 4: 1316489472 + 32868096}},
-    "prefill": {"sources": ("prefill_tc.cu", "common.cuh", "launch.h"), "source_sha": "c163eb2119b9c314",
-                "bytes_per_launch": {3: 197486848 + 18785792}},
+    "prefill": {"sources": ("prefill_tc.cu", "common.cuh", "launch.h"), "source_sha": "28292c3087c95780",
+                "bytes_per_launch": {3: 199506688 + 17285632}},
 }
 
 

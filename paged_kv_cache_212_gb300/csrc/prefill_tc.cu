@@ -77,6 +77,16 @@ struct PrefillTcParams {
 // Batches of at most this many sequences are scheduled longest prefix first.
 constexpr int kSortMaxSeqs = 32;
 
+// Register split (setmaxnreg): the block is launched with kLaunchRegs per
+// thread; warpgroup 2 (TMA producers, MMA issuer) keeps kRegsIssue and hands
+// the rest to the two softmax warpgroups, whose rows of 128 scores stay in
+// registers.  The sum must not exceed what the block was launched with, or the
+// increase would wait for registers that never come free.
+constexpr int kLaunchRegs = 168;             // 65536 / 384, rounded down to a multiple of 8
+constexpr int kRegsIssue = 72;
+constexpr int kRegsSoftmax = 216;
+static_assert(128 * kRegsIssue + 256 * kRegsSoftmax <= 384 * kLaunchRegs, "register split above the launch");
+
 // ---- tcgen05 helpers -------------------------------------------------------
 
 // Shared-memory matrix descriptor: start address, leading / stride byte
@@ -339,158 +349,162 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(const __grid_constan
     const uint32_t tmem = *tmem_base_s;
     if (bad_len && threadIdx.x == 0) report(p.dev_status, PKV_DEV_BAD_LENGTH);
 
-    if ((warp == 8 || warp == 10 || warp == 11) && n_kt > 0) {
-        // ===================== TMA producers =====================
-        const bool is_v = warp == 11;
-        if (warp == 8 && lane == 0) {
-            prefetch_tensormap(&q_map);
-            mbar_arrive_expect_tx(q_full, kNQ * kQTile);
-            for (int i = 0; i < kNQ; ++i)
-                for (int h = 0; h < PANELS; ++h)
-                    tma_load_3d(q_s + i * kQTile + h * kQPanel, &q_map, h * 64, kvh * G,
-                                s * p.chunk + p0 + i * pos_per_tile, q_full);
-        }
-        if (lane == 0) prefetch_tensormap(is_v ? &v_map : &k_map);
-        // this warp's 16-key groups: all eight (V) or four (each K warp)
-        const int n_grp = is_v ? kTN / 16 : kTN / 32;
-        const int grp = is_v ? lane : (warp == 10 ? kTN / 32 : 0) + lane;
-        const int NSL = is_v ? NV : NK;
-        uint64_t *full = is_v ? v_full : k_full;
-        uint64_t *empty = is_v ? v_empty : k_empty;
-        uint8_t *ring = is_v ? v_ring : k_ring;
-        const uint32_t bytes = is_v ? kSlotBytes : kSlotBytes / 2;
-        const int32_t *trow = p.tables + (int64_t)s * p.max_blocks;
-        // block ids are read one tile ahead and turned into pool rows when the
-        // tile is issued
-        auto load_block = [&](int j) -> int32_t {
-            const int32_t key0 = j * kTN + grp * 16;
-            return (lane < n_grp && key0 < n_keys) ? __ldg(trow + key0 / p.block_size) : 0;
-        };
-        int32_t blk = load_block(0);
-        int issued = 0;
-        for (int j = 0; j < n_kt; ++j) {
-            int32_t row = p.pool_rows;  // out of range: the box reads zeros
-            {
-                const int32_t key0 = j * kTN + grp * 16;
-                if (lane < n_grp && key0 < n_keys) {
-                    if (blk < 0 || blk > p.n_blocks)
-                        report(p.dev_status, PKV_DEV_BAD_BLOCK_ID);
-                    else
-                        row = blk * p.block_size + key0 % p.block_size;
-                }
-            }
-            if (j + 1 < n_kt) blk = load_block(j + 1);
-            const int st = j % NSL, use = j / NSL;
-            if (lane == 0 && !mbar_wait(&empty[st], (use & 1) ^ 1, abort_flag, p.wait_ns)) {
-                report(p.dev_status, PKV_DEV_TIMEOUT);
-                *abort_flag = 1;
-            }
-            if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
-            uint8_t *dst = ring + st * kSlotBytes;
-            if (lane == 0) mbar_arrive_expect_tx(&full[st], bytes);
-            __syncwarp();
-            if (lane < n_grp) {
-                if (is_v) {
-                    tma_load_3d(dst + grp * kVGroup, &v_map, 0, row, kvh * PANELS, &full[st]);
-                } else {
-#pragma unroll
+    if (warp >= 4 * kNQ) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsIssue) : "memory");
+        if (warp != 9 && n_kt > 0) {
+            // ===================== TMA producers =====================
+            const bool is_v = warp == 11;
+            if (warp == 8 && lane == 0) {
+                prefetch_tensormap(&q_map);
+                mbar_arrive_expect_tx(q_full, kNQ * kQTile);
+                for (int i = 0; i < kNQ; ++i)
                     for (int h = 0; h < PANELS; ++h)
-                        tma_load_3d(dst + h * kKVPanel + grp * 2048, &k_map, h * 64, kvh, row, &full[st]);
-                }
+                        tma_load_3d(q_s + i * kQTile + h * kQPanel, &q_map, h * 64, kvh * G,
+                                    s * p.chunk + p0 + i * pos_per_tile, q_full);
             }
-            ++issued;
-        }
-        // every copy this warp issued has landed before the CTA can exit
-        if (lane == 0) {
-            if (warp == 8) (void)mbar_wait(q_full, 0);
-            for (int i = issued > NSL ? issued - NSL : 0; i < issued; ++i)
-                (void)mbar_wait(&full[i % NSL], (i / NSL) & 1);
-        }
-    } else if (warp == 9 && n_kt > 0) {
-        // ===================== MMA issuer =====================
-        const uint32_t idesc_s = umma_idesc_bf16(kTM, kTN, false, false);
-        const uint32_t idesc_o = umma_idesc_bf16(kTM, D, false, true);
-        bool ok = true;
-        if (lane == 0) {
-            // The issuing thread bounds the prefill: its waits keep the default
-            // limit, which compiles to the plain wait (the settable limit is
-            // taken by the producers and the softmax warps; when theirs runs
-            // out, the abort flag ends these waits too).
-            auto wait_k = [&](int j) { return mbar_wait(&k_full[j % NK], (j / NK) & 1, abort_flag); };
-            auto wait_v = [&](int j) { return mbar_wait(&v_full[j % NV], (j / NV) & 1, abort_flag); };
-            // S_tj = Q_t K_j^T, then the commit that hands S_tj to warpgroup t
-            // Descriptors of a tile are built once and stepped by constants: the
-            // start-address field is addr / 16 (14 bits, shared addresses < 256 KiB),
-            // so desc(addr + off) = desc(addr) + off / 16 for 16-byte multiples off.
-            auto issue_s = [&](int t, int j) {
-                const uint64_t q_desc = umma_desc_sw128(smem_u32(q_s + t * kQTile), 16, 1024);
-                const uint64_t k_desc = umma_desc_sw128(smem_u32(k_ring + (j % NK) * kSlotBytes), 16, 1024);
-                if constexpr (D == 128) {
-                    uint64_t ad[8], bd[8];
-#pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        ad[kk] = desc_step(q_desc, (kk / 4) * kQPanel + (kk % 4) * 32);
-                        bd[kk] = desc_step(k_desc, (kk / 4) * kKVPanel + (kk % 4) * 32);
-                    }
-                    umma_bf16_x8(tmem + t * kTileCols, ad, bd, idesc_s, 0u);
-                } else {
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        umma_bf16(tmem + t * kTileCols, desc_step(q_desc, (kk / 4) * kQPanel + (kk % 4) * 32),
-                                  desc_step(k_desc, (kk / 4) * kKVPanel + (kk % 4) * 32), idesc_s, kk > 0);
-                }
-                umma_commit(&s_full[t]);
+            if (lane == 0) prefetch_tensormap(is_v ? &v_map : &k_map);
+            // this warp's 16-key groups: all eight (V) or four (each K warp)
+            const int n_grp = is_v ? kTN / 16 : kTN / 32;
+            const int grp = is_v ? lane : (warp == 10 ? kTN / 32 : 0) + lane;
+            const int NSL = is_v ? NV : NK;
+            uint64_t *full = is_v ? v_full : k_full;
+            uint64_t *empty = is_v ? v_empty : k_empty;
+            uint8_t *ring = is_v ? v_ring : k_ring;
+            const uint32_t bytes = is_v ? kSlotBytes : kSlotBytes / 2;
+            const int32_t *trow = p.tables + (int64_t)s * p.max_blocks;
+            // block ids are read one tile ahead and turned into pool rows when the
+            // tile is issued
+            auto load_block = [&](int j) -> int32_t {
+                const int32_t key0 = j * kTN + grp * 16;
+                return (lane < n_grp && key0 < n_keys) ? __ldg(trow + key0 / p.block_size) : 0;
             };
-            ok = mbar_wait(q_full, 0, abort_flag) && wait_k(0);
-            if (ok) {
-                tc_fence_after();
-                for (int t = 0; t < kNQ; ++t) issue_s(t, 0);
-                umma_commit(&k_empty[0]);
-            }
-            for (int j = 0; ok && j < n_kt; ++j) {
-                ok = wait_v(j);
-                if (!ok) break;
-                const uint64_t v_desc = umma_desc_sw128(smem_u32(v_ring + (j % NV) * kSlotBytes), 2048, 1024);
-                for (int t = 0; t < kNQ && ok; ++t) {
-                    ok = mbar_wait(&p_full[t], j & 1, abort_flag);
-                    if (!ok) break;
-                    tc_fence_after();
-                    // O_t += P_tj V_j: A = P (TMEM, 8 columns per 16 keys), B = V (MN-major:
-                    // 16-key group kk at kk * kVGroup, its two 8-key halves 1024 B
-                    // apart, 64-column panels 2048 B apart)
-                    {
-                        static_assert(kTN / 16 == 8, "eight 16-key products per tile");
-                        uint64_t bd[8];
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) bd[kk] = desc_step(v_desc, kk * kVGroup);
-                        umma_bf16_ts_x8(tmem + t * kTileCols + kOCol, tmem + t * kTileCols, bd, idesc_o,
-                                        j > 0 ? 1u : 0u);
-                    }
-                    if (j + 1 < n_kt) {
-                        if (t == 0) {
-                            ok = wait_k(j + 1);
-                            if (!ok) break;
-                            tc_fence_after();
-                        }
-                        issue_s(t, j + 1);
-                    } else {
-                        umma_commit(&o_done[t]);
+            int32_t blk = load_block(0);
+            int issued = 0;
+            for (int j = 0; j < n_kt; ++j) {
+                int32_t row = p.pool_rows;  // out of range: the box reads zeros
+                {
+                    const int32_t key0 = j * kTN + grp * 16;
+                    if (lane < n_grp && key0 < n_keys) {
+                        if (blk < 0 || blk > p.n_blocks)
+                            report(p.dev_status, PKV_DEV_BAD_BLOCK_ID);
+                        else
+                            row = blk * p.block_size + key0 % p.block_size;
                     }
                 }
-                if (!ok) break;
-                umma_commit(&v_empty[j % NV]);
-                if (j + 1 < n_kt) umma_commit(&k_empty[(j + 1) % NK]);
+                if (j + 1 < n_kt) blk = load_block(j + 1);
+                const int st = j % NSL, use = j / NSL;
+                if (lane == 0 && !mbar_wait(&empty[st], (use & 1) ^ 1, abort_flag, p.wait_ns)) {
+                    report(p.dev_status, PKV_DEV_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+                uint8_t *dst = ring + st * kSlotBytes;
+                if (lane == 0) mbar_arrive_expect_tx(&full[st], bytes);
+                __syncwarp();
+                if (lane < n_grp) {
+                    if (is_v) {
+                        tma_load_3d(dst + grp * kVGroup, &v_map, 0, row, kvh * PANELS, &full[st]);
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < PANELS; ++h)
+                            tma_load_3d(dst + h * kKVPanel + grp * 2048, &k_map, h * 64, kvh, row, &full[st]);
+                    }
+                }
+                ++issued;
             }
-            if (!ok) {
-                report(p.dev_status, PKV_DEV_TIMEOUT);
-                *abort_flag = 1;
+            // every copy this warp issued has landed before the CTA can exit
+            if (lane == 0) {
+                if (warp == 8) (void)mbar_wait(q_full, 0);
+                for (int i = issued > NSL ? issued - NSL : 0; i < issued; ++i)
+                    (void)mbar_wait(&full[i % NSL], (i / NSL) & 1);
             }
-            // every MMA issued has retired before the TMEM is released
-            umma_commit(fin_bar);
-            (void)mbar_wait(fin_bar, 0);
+        } else if (warp == 9 && n_kt > 0) {
+            // ===================== MMA issuer =====================
+            const uint32_t idesc_s = umma_idesc_bf16(kTM, kTN, false, false);
+            const uint32_t idesc_o = umma_idesc_bf16(kTM, D, false, true);
+            bool ok = true;
+            if (lane == 0) {
+                // The issuing thread bounds the prefill: its waits keep the default
+                // limit, which compiles to the plain wait (the settable limit is
+                // taken by the producers and the softmax warps; when theirs runs
+                // out, the abort flag ends these waits too).
+                auto wait_k = [&](int j) { return mbar_wait(&k_full[j % NK], (j / NK) & 1, abort_flag); };
+                auto wait_v = [&](int j) { return mbar_wait(&v_full[j % NV], (j / NV) & 1, abort_flag); };
+                // S_tj = Q_t K_j^T, then the commit that hands S_tj to warpgroup t
+                // Descriptors of a tile are built once and stepped by constants: the
+                // start-address field is addr / 16 (14 bits, shared addresses < 256 KiB),
+                // so desc(addr + off) = desc(addr) + off / 16 for 16-byte multiples off.
+                auto issue_s = [&](int t, int j) {
+                    const uint64_t q_desc = umma_desc_sw128(smem_u32(q_s + t * kQTile), 16, 1024);
+                    const uint64_t k_desc = umma_desc_sw128(smem_u32(k_ring + (j % NK) * kSlotBytes), 16, 1024);
+                    if constexpr (D == 128) {
+                        uint64_t ad[8], bd[8];
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            ad[kk] = desc_step(q_desc, (kk / 4) * kQPanel + (kk % 4) * 32);
+                            bd[kk] = desc_step(k_desc, (kk / 4) * kKVPanel + (kk % 4) * 32);
+                        }
+                        umma_bf16_x8(tmem + t * kTileCols, ad, bd, idesc_s, 0u);
+                    } else {
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk)
+                            umma_bf16(tmem + t * kTileCols, desc_step(q_desc, (kk / 4) * kQPanel + (kk % 4) * 32),
+                                      desc_step(k_desc, (kk / 4) * kKVPanel + (kk % 4) * 32), idesc_s, kk > 0);
+                    }
+                    umma_commit(&s_full[t]);
+                };
+                ok = mbar_wait(q_full, 0, abort_flag) && wait_k(0);
+                if (ok) {
+                    tc_fence_after();
+                    for (int t = 0; t < kNQ; ++t) issue_s(t, 0);
+                    umma_commit(&k_empty[0]);
+                }
+                for (int j = 0; ok && j < n_kt; ++j) {
+                    ok = wait_v(j);
+                    if (!ok) break;
+                    const uint64_t v_desc = umma_desc_sw128(smem_u32(v_ring + (j % NV) * kSlotBytes), 2048, 1024);
+                    for (int t = 0; t < kNQ && ok; ++t) {
+                        ok = mbar_wait(&p_full[t], j & 1, abort_flag);
+                        if (!ok) break;
+                        tc_fence_after();
+                        // O_t += P_tj V_j: A = P (TMEM, 8 columns per 16 keys), B = V (MN-major:
+                        // 16-key group kk at kk * kVGroup, its two 8-key halves 1024 B
+                        // apart, 64-column panels 2048 B apart)
+                        {
+                            static_assert(kTN / 16 == 8, "eight 16-key products per tile");
+                            uint64_t bd[8];
+#pragma unroll
+                            for (int kk = 0; kk < 8; ++kk) bd[kk] = desc_step(v_desc, kk * kVGroup);
+                            umma_bf16_ts_x8(tmem + t * kTileCols + kOCol, tmem + t * kTileCols, bd, idesc_o,
+                                            j > 0 ? 1u : 0u);
+                        }
+                        if (j + 1 < n_kt) {
+                            if (t == 0) {
+                                ok = wait_k(j + 1);
+                                if (!ok) break;
+                                tc_fence_after();
+                            }
+                            issue_s(t, j + 1);
+                        } else {
+                            umma_commit(&o_done[t]);
+                        }
+                    }
+                    if (!ok) break;
+                    umma_commit(&v_empty[j % NV]);
+                    if (j + 1 < n_kt) umma_commit(&k_empty[(j + 1) % NK]);
+                }
+                if (!ok) {
+                    report(p.dev_status, PKV_DEV_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                // every MMA issued has retired before the TMEM is released
+                umma_commit(fin_bar);
+                (void)mbar_wait(fin_bar, 0);
+            }
+            __syncwarp();
         }
-        __syncwarp();
-    } else if (warp < 4 * kNQ) {
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax) : "memory");
         // ===================== softmax warpgroups: row r of tile qt = TMEM lane r =====================
         const int qt = warp / 4;
         const int r = threadIdx.x % kTM;
@@ -697,6 +711,15 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream)
     const int64_t ctas = (int64_t)p.pairs_per_seq * d.n_kv_heads * a.n_seqs;
     if (ctas > INT32_MAX) return cudaErrorInvalidValue;
     dim3 grid((unsigned)ctas);
+    // The register split assumes the block gets kLaunchRegs per thread: refuse
+    // a build whose kernel was given fewer (its setmaxnreg.inc could not complete).
+    static const bool regs_ok = [] {
+        cudaFuncAttributes fa128{}, fa64{};
+        return cudaFuncGetAttributes(&fa128, prefill_tc_kernel<128>) == cudaSuccess &&
+               cudaFuncGetAttributes(&fa64, prefill_tc_kernel<64>) == cudaSuccess && fa128.numRegs >= kLaunchRegs &&
+               fa64.numRegs >= kLaunchRegs;
+    }();
+    if (!regs_ok) return cudaErrorInvalidConfiguration;
     cudaError_t e;
     if (d.head_dim == 128) {
         e = cudaFuncSetAttribute(prefill_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
