@@ -1062,7 +1062,10 @@ def main():
     w = make_workload(args.config, device)  # every rank owns an independent replica batch
     if args.config == 0:
         if rank == 0:
-            print(json.dumps(run_small_bench(args, P, w, device)), flush=True)
+            line = run_small_bench(args, P, w, device)
+            if world == 1 and not args.no_cpu_baseline:
+                line["cpu_baseline"] = cpu_baseline(0)
+            print(json.dumps(line), flush=True)
         if world > 1:
             dist.destroy_process_group()
         return
