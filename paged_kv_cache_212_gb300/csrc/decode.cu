@@ -34,9 +34,12 @@
 // (16-byte chunk c of row r stored at chunk c ^ (r & 7)), so ldmatrix reads of
 // eight consecutive tokens hit eight different bank groups.
 #include <math.h>
+#include <stdlib.h>
+#include <string.h>
 
 #include "common.cuh"
 #include "launch.h"
+#include "tcgen05.cuh"
 #include "write_rows.cuh"
 
 namespace pkv {
@@ -51,7 +54,7 @@ constexpr float kLazyMax = 8.0f;
 constexpr uint32_t kHdrCounter = 0, kHdrTotal = 1, kHdrOverflow = 2, kHdrChunk = 3, kHdrStages = 4;
 constexpr int32_t kMinChunkStages = 4;   // balanced items hold at least 64 tokens
 
-enum : int32_t { kMetaFirst = 1, kMetaLast = 2, kMetaBad = 4, kMetaStop = 8, kMetaFinal = 16 };
+enum : int32_t { kMetaFirst = 1, kMetaLast = 2, kMetaBad = 4, kMetaStop = 8, kMetaFinal = 16, kMetaPad = 32 };
 
 struct StageMeta {
     int32_t seq;
@@ -80,6 +83,8 @@ struct DecodeParams {
     int32_t n_stages;
     int32_t boxes_per_half;  // TMA boxes per (K or V, half): 1 (all heads) or hpc (one per head)
     uint32_t stage_bytes, tx_bytes, kv_tile_bytes, scale_tile_bytes, q_slot_bytes;
+    int32_t scale_heads;          // int8: kv heads per scale box (a multiple of 4: 16-byte rows)
+    int32_t tile_stages;          // > 1: each piece is padded to a multiple of this many stages
     unsigned long long wait_ns;   // limit of the pipeline waits
 };
 
@@ -564,9 +569,200 @@ __device__ __forceinline__ void issue_stage_loads(uint8_t *stg, const DecodePara
                 tma_load_3d(stg + p.kv_tile_bytes + off, &v_map, 0, head0 + b, row0, bar);
             }
         }
+        // the scale box starts at a multiple of scale_heads heads (its first
+        // coordinate times 4 bytes must be a multiple of 16)
         uint8_t *sc = stg + 2 * p.kv_tile_bytes;
-        tma_load_2d(sc, &ks_map, head0, row0, bar);
-        tma_load_2d(sc + p.scale_tile_bytes, &vs_map, head0, row0, bar);
+        const int32_t sh0 = head0 / p.scale_heads * p.scale_heads;
+        tma_load_2d(sc, &ks_map, sh0, row0, bar);
+        tma_load_2d(sc + p.scale_tile_bytes, &vs_map, sh0, row0, bar);
+    }
+}
+
+// The producer of the split kernels (one thread): walks this CTA's units of
+// the work list, streams their pages stage by stage into the ring and ends it
+// with a stop marker.
+template <int D, bool INT8>
+__device__ __forceinline__ void run_producer(const SmemLayout &L, const DecodeParams &p, const CUtensorMap &k_map,
+                                             const CUtensorMap &v_map, const CUtensorMap &ks_map,
+                                             const CUtensorMap &vs_map, volatile int32_t *abort_flag,
+                                             uint32_t total_items)
+{
+    const int hpc = p.hpc;
+    // ===================== producer (one thread) =====================
+    // Lane 0 alone walks the work list and issues the copies: no per-stage
+    // warp shuffles or divergent branches, ring position and block
+    // position advanced by counters, the next table entry loaded one stage
+    // ahead of its use.
+    prefetch_tensormap(&k_map);
+    prefetch_tensormap(&v_map);
+    if (INT8) {
+        prefetch_tensormap(&ks_map);
+        prefetch_tensormap(&vs_map);
+    }
+    uint32_t st = 0, phase = 0;          // ring slot and its parity
+    uint32_t item_it = 0;
+    bool ok = true;
+    const bool balanced = p.split_tokens == 0;
+    const int32_t chunk = (int32_t)p.ws.header[kHdrChunk];
+    const int32_t total_stages = (int32_t)p.ws.header[kHdrStages];
+    // Balanced items are all the same size and number at most the grid:
+    // CTA b takes units b, b + grid, ...  Fixed splits differ in size: a
+    // CTA takes the next unit from the counter when it starts one (no id
+    // is taken ahead, which would let early CTAs hold two units while late
+    // ones get none).
+    uint32_t it = balanced ? blockIdx.x : atomicAdd(&p.ws.header[kHdrCounter], 1u);
+    for (; ok && it < total_items;
+         it = balanced ? it + gridDim.x : atomicAdd(&p.ws.header[kHdrCounter], 1u)) {
+        const int32_t item = (int32_t)(it / p.n_hg), hg = (int32_t)(it % p.n_hg);
+        // balanced: the item is the stage range [g0, g1) of the concatenated sequences
+        int32_t g0 = 0, g1 = 0, sq = 0;
+        int2 fixed_sk = make_int2(0, 0);
+        if (balanced) {
+            g0 = item * chunk;
+            g1 = min(g0 + chunk, total_stages);
+            sq = __ldg(&p.ws.items[item].x);
+        } else {
+            fixed_sk = __ldg(&p.ws.items[item]);
+        }
+        bool more = true;
+        while (ok && more) {
+            // the next piece: sequence, token range, partial slot, pieces of that sequence
+            int32_t seq, t0, t1, slot, n_pieces;
+            if (balanced) {
+                int32_t pre = __ldg(p.ws.seq_prefix + sq), pre1 = __ldg(p.ws.seq_prefix + sq + 1);
+                while (pre1 == pre) {  // sequences without tokens
+                    ++sq;
+                    pre = pre1;
+                    pre1 = __ldg(p.ws.seq_prefix + sq + 1);
+                }
+                const int32_t e = min(g1, pre1);
+                seq = sq;
+                t0 = (g0 - pre) * kStageTokens;
+                t1 = min((e - pre) * kStageTokens, __ldg(p.ctx_lens + sq));
+                const int2 sg = __ldg(p.ws.seg + sq);
+                slot = sg.x + (item - pre / chunk);
+                n_pieces = sg.y;
+                g0 = e;
+                ++sq;
+                more = g0 < g1;
+            } else {
+                seq = fixed_sk.x;
+                t0 = fixed_sk.y * p.split_tokens;
+                t1 = min(t0 + p.split_tokens, __ldg(p.ctx_lens + seq));
+                slot = item;
+                n_pieces = __ldg(&p.ws.seg[seq].y);
+                more = false;
+            }
+            const bool final_out = n_pieces == 1;
+            const int32_t *trow = p.tables + (int64_t)seq * p.max_blocks;
+            // this piece's queries: heads [hg*hpc*G, (hg+1)*hpc*G) of sequence seq
+            const uint32_t qs = item_it & 1u;
+            if (!mbar_wait(&L.qempty_bar[qs], ((item_it >> 1) & 1u) ^ 1u, abort_flag, p.wait_ns)) {
+                report(p.dev_status, PKV_DEV_TIMEOUT);
+                *abort_flag = 1;
+                ok = false;
+                break;
+            }
+            mbar_arrive_expect_tx(&L.qfull_bar[qs], p.q_slot_bytes);
+            bulk_g2s(L.q_slots + qs * p.q_slot_bytes,
+                     p.q + ((int64_t)seq * p.n_q_heads + (int64_t)hg * hpc * p.group) * D, p.q_slot_bytes,
+                     &L.qfull_bar[qs]);
+            // block position of t0, and its table entry; later entries are
+            // loaded one stage ahead
+            int32_t lb = t0 / p.block_size, off = t0 - lb * p.block_size;
+            int32_t blk = lb < p.max_blocks ? __ldg(trow + lb) : -1;
+            for (int32_t t = t0; t < t1; t += kStageTokens) {
+                const bool last_of_block = off + kStageTokens >= p.block_size;
+                const bool more_stages = t + kStageTokens < t1;
+                int32_t blk_next = blk;
+                if (last_of_block && more_stages) blk_next = lb + 1 < p.max_blocks ? __ldg(trow + lb + 1) : -1;
+                if (!mbar_wait(&L.empty_bar[st], phase ^ 1u, abort_flag, p.wait_ns)) {
+                    report(p.dev_status, PKV_DEV_TIMEOUT);
+                    *abort_flag = 1;
+                    ok = false;
+                    break;
+                }
+                StageMeta m;
+                m.seq = seq;
+                m.split_index = slot;
+                m.n_valid = min(kStageTokens, t1 - t);
+                m.flags = (t == t0 ? kMetaFirst : 0) | (more_stages ? 0 : kMetaLast) | (final_out ? kMetaFinal : 0);
+                m.head_group = hg;
+                m.n_splits = n_pieces;
+                const bool bad = blk < 0 || blk > p.n_blocks;
+                if (bad) {
+                    m.flags |= kMetaBad;
+                    report(p.dev_status, PKV_DEV_BAD_BLOCK_ID);
+                }
+                L.meta[st] = m;
+                if (bad) {
+                    mbar_arrive(&L.full_bar[st]);
+                } else {
+                    uint8_t *stg = L.stages + (size_t)st * p.stage_bytes;
+                    const int32_t row0 = blk * p.block_size + off;
+                    mbar_arrive_expect_tx(&L.full_bar[st], p.tx_bytes);
+                    issue_stage_loads<D, INT8>(stg, p, k_map, v_map, ks_map, vs_map, row0, hg * hpc,
+                                               &L.full_bar[st]);
+                }
+                if (++st == (uint32_t)p.n_stages) {
+                    st = 0;
+                    phase ^= 1u;
+                }
+                if (last_of_block) {
+                    ++lb;
+                    off = 0;
+                    blk = blk_next;
+                } else {
+                    off += kStageTokens;
+                }
+            }
+            if (ok && p.tile_stages > 1) {
+                // the tensor-core kernel takes whole tiles of tile_stages stages:
+                // the piece is padded with empty stages up to the next tile
+                const int32_t used = (t1 - t0 + kStageTokens - 1) / kStageTokens;
+                for (int32_t k = (p.tile_stages - used % p.tile_stages) % p.tile_stages; k > 0; --k) {
+                    if (!mbar_wait(&L.empty_bar[st], phase ^ 1u, abort_flag, p.wait_ns)) {
+                        report(p.dev_status, PKV_DEV_TIMEOUT);
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    L.meta[st].flags = kMetaPad;
+                    mbar_arrive(&L.full_bar[st]);
+                    if (++st == (uint32_t)p.n_stages) {
+                        st = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            ++item_it;
+        }
+    }
+    // stop marker
+    if (ok && !*abort_flag) {
+        if (mbar_wait(&L.empty_bar[st], phase ^ 1u, abort_flag, p.wait_ns)) {
+            L.meta[st].flags = kMetaStop;
+            mbar_arrive(&L.full_bar[st]);
+        } else {
+            report(p.dev_status, PKV_DEV_TIMEOUT);
+            *abort_flag = 1;
+        }
+    }
+    if (*abort_flag) {
+        // wind down: let every copy already issued land before the CTA exits
+        // (the last n_stages slots and the last two query copies; a phase
+        // never issued counts as complete), with the default limit
+        uint32_t ws_ = st, wp = phase;
+        for (int i = 0; i < p.n_stages; ++i) {
+            if (ws_ == 0) {
+                ws_ = (uint32_t)p.n_stages;
+                wp ^= 1u;
+            }
+            --ws_;
+            (void)mbar_wait(&L.full_bar[ws_], wp);
+        }
+        for (uint32_t i = item_it > 2u ? item_it - 2u : 0u; i < item_it; ++i)
+            (void)mbar_wait(&L.qfull_bar[i & 1u], (i >> 1) & 1u);
     }
 }
 
@@ -611,164 +807,7 @@ __global__ void __launch_bounds__(288, INT8 ? 1 : 2) decode_split_kernel(const _
     volatile int32_t *abort_flag = L.abort_flag;
 
     if (warp == hpc) {
-        // ===================== producer (one thread) =====================
-        // Lane 0 alone walks the work list and issues the copies: no per-stage
-        // warp shuffles or divergent branches, ring position and block
-        // position advanced by counters, the next table entry loaded one stage
-        // ahead of its use.
-        if (lane != 0) return;
-        prefetch_tensormap(&k_map);
-        prefetch_tensormap(&v_map);
-        if (INT8) {
-            prefetch_tensormap(&ks_map);
-            prefetch_tensormap(&vs_map);
-        }
-        uint32_t st = 0, phase = 0;          // ring slot and its parity
-        uint32_t item_it = 0;
-        bool ok = true;
-        const bool balanced = p.split_tokens == 0;
-        const int32_t chunk = (int32_t)p.ws.header[kHdrChunk];
-        const int32_t total_stages = (int32_t)p.ws.header[kHdrStages];
-        // Balanced items are all the same size and number at most the grid:
-        // CTA b takes units b, b + grid, ...  Fixed splits differ in size: a
-        // CTA takes the next unit from the counter when it starts one (no id
-        // is taken ahead, which would let early CTAs hold two units while late
-        // ones get none).
-        uint32_t it = balanced ? blockIdx.x : atomicAdd(&p.ws.header[kHdrCounter], 1u);
-        for (; ok && it < total_items;
-             it = balanced ? it + gridDim.x : atomicAdd(&p.ws.header[kHdrCounter], 1u)) {
-            const int32_t item = (int32_t)(it / p.n_hg), hg = (int32_t)(it % p.n_hg);
-            // balanced: the item is the stage range [g0, g1) of the concatenated sequences
-            int32_t g0 = 0, g1 = 0, sq = 0;
-            int2 fixed_sk = make_int2(0, 0);
-            if (balanced) {
-                g0 = item * chunk;
-                g1 = min(g0 + chunk, total_stages);
-                sq = __ldg(&p.ws.items[item].x);
-            } else {
-                fixed_sk = __ldg(&p.ws.items[item]);
-            }
-            bool more = true;
-            while (ok && more) {
-                // the next piece: sequence, token range, partial slot, pieces of that sequence
-                int32_t seq, t0, t1, slot, n_pieces;
-                if (balanced) {
-                    int32_t pre = __ldg(p.ws.seq_prefix + sq), pre1 = __ldg(p.ws.seq_prefix + sq + 1);
-                    while (pre1 == pre) {  // sequences without tokens
-                        ++sq;
-                        pre = pre1;
-                        pre1 = __ldg(p.ws.seq_prefix + sq + 1);
-                    }
-                    const int32_t e = min(g1, pre1);
-                    seq = sq;
-                    t0 = (g0 - pre) * kStageTokens;
-                    t1 = min((e - pre) * kStageTokens, __ldg(p.ctx_lens + sq));
-                    const int2 sg = __ldg(p.ws.seg + sq);
-                    slot = sg.x + (item - pre / chunk);
-                    n_pieces = sg.y;
-                    g0 = e;
-                    ++sq;
-                    more = g0 < g1;
-                } else {
-                    seq = fixed_sk.x;
-                    t0 = fixed_sk.y * p.split_tokens;
-                    t1 = min(t0 + p.split_tokens, __ldg(p.ctx_lens + seq));
-                    slot = item;
-                    n_pieces = __ldg(&p.ws.seg[seq].y);
-                    more = false;
-                }
-                const bool final_out = n_pieces == 1;
-                const int32_t *trow = p.tables + (int64_t)seq * p.max_blocks;
-                // this piece's queries: heads [hg*hpc*G, (hg+1)*hpc*G) of sequence seq
-                const uint32_t qs = item_it & 1u;
-                if (!mbar_wait(&L.qempty_bar[qs], ((item_it >> 1) & 1u) ^ 1u, abort_flag, p.wait_ns)) {
-                    report(p.dev_status, PKV_DEV_TIMEOUT);
-                    *abort_flag = 1;
-                    ok = false;
-                    break;
-                }
-                mbar_arrive_expect_tx(&L.qfull_bar[qs], p.q_slot_bytes);
-                bulk_g2s(L.q_slots + qs * p.q_slot_bytes,
-                         p.q + ((int64_t)seq * p.n_q_heads + (int64_t)hg * hpc * p.group) * D, p.q_slot_bytes,
-                         &L.qfull_bar[qs]);
-                // block position of t0, and its table entry; later entries are
-                // loaded one stage ahead
-                int32_t lb = t0 / p.block_size, off = t0 - lb * p.block_size;
-                int32_t blk = lb < p.max_blocks ? __ldg(trow + lb) : -1;
-                for (int32_t t = t0; t < t1; t += kStageTokens) {
-                    const bool last_of_block = off + kStageTokens >= p.block_size;
-                    const bool more_stages = t + kStageTokens < t1;
-                    int32_t blk_next = blk;
-                    if (last_of_block && more_stages) blk_next = lb + 1 < p.max_blocks ? __ldg(trow + lb + 1) : -1;
-                    if (!mbar_wait(&L.empty_bar[st], phase ^ 1u, abort_flag, p.wait_ns)) {
-                        report(p.dev_status, PKV_DEV_TIMEOUT);
-                        *abort_flag = 1;
-                        ok = false;
-                        break;
-                    }
-                    StageMeta m;
-                    m.seq = seq;
-                    m.split_index = slot;
-                    m.n_valid = min(kStageTokens, t1 - t);
-                    m.flags = (t == t0 ? kMetaFirst : 0) | (more_stages ? 0 : kMetaLast) | (final_out ? kMetaFinal : 0);
-                    m.head_group = hg;
-                    m.n_splits = n_pieces;
-                    const bool bad = blk < 0 || blk > p.n_blocks;
-                    if (bad) {
-                        m.flags |= kMetaBad;
-                        report(p.dev_status, PKV_DEV_BAD_BLOCK_ID);
-                    }
-                    L.meta[st] = m;
-                    if (bad) {
-                        mbar_arrive(&L.full_bar[st]);
-                    } else {
-                        uint8_t *stg = L.stages + (size_t)st * p.stage_bytes;
-                        const int32_t row0 = blk * p.block_size + off;
-                        mbar_arrive_expect_tx(&L.full_bar[st], p.tx_bytes);
-                        issue_stage_loads<D, INT8>(stg, p, k_map, v_map, ks_map, vs_map, row0, hg * hpc,
-                                                   &L.full_bar[st]);
-                    }
-                    if (++st == (uint32_t)p.n_stages) {
-                        st = 0;
-                        phase ^= 1u;
-                    }
-                    if (last_of_block) {
-                        ++lb;
-                        off = 0;
-                        blk = blk_next;
-                    } else {
-                        off += kStageTokens;
-                    }
-                }
-                ++item_it;
-            }
-        }
-        // stop marker
-        if (ok && !*abort_flag) {
-            if (mbar_wait(&L.empty_bar[st], phase ^ 1u, abort_flag, p.wait_ns)) {
-                L.meta[st].flags = kMetaStop;
-                mbar_arrive(&L.full_bar[st]);
-            } else {
-                report(p.dev_status, PKV_DEV_TIMEOUT);
-                *abort_flag = 1;
-            }
-        }
-        if (*abort_flag) {
-            // wind down: let every copy already issued land before the CTA exits
-            // (the last n_stages slots and the last two query copies; a phase
-            // never issued counts as complete), with the default limit
-            uint32_t ws_ = st, wp = phase;
-            for (int i = 0; i < p.n_stages; ++i) {
-                if (ws_ == 0) {
-                    ws_ = (uint32_t)p.n_stages;
-                    wp ^= 1u;
-                }
-                --ws_;
-                (void)mbar_wait(&L.full_bar[ws_], wp);
-            }
-            for (uint32_t i = item_it > 2u ? item_it - 2u : 0u; i < item_it; ++i)
-                (void)mbar_wait(&L.qfull_bar[i & 1u], (i >> 1) & 1u);
-        }
+        if (lane == 0) run_producer<D, INT8>(L, p, k_map, v_map, ks_map, vs_map, abort_flag, total_items);
         return;
     }
     if (warp > hpc) return;
@@ -1173,6 +1212,525 @@ __global__ void __launch_bounds__(288, INT8 ? 1 : 2) decode_split_kernel(const _
     }
 }
 
+// ---------------------------------------------------------------------------
+// 2b. tensor-core split kernel: int8 pages, head_dim 128, up to 8 query heads
+//     per kv head (tcgen05 with TMEM accumulators)
+// ---------------------------------------------------------------------------
+// The same work list, producer and partial slots as decode_split_kernel, two
+// kv heads per CTA, and tiles of 128 tokens (eight stages; each piece is
+// padded to whole tiles).  Per kv head one warpgroup converts the tile's codes
+// to fp16 in shared memory (the exact biased form 1152 + b, corrected once
+// per score and once per output as in the mma.sync kernel), and one thread of
+// the issuing warp runs the contractions on the 5th-generation tensor cores:
+//   S^T = K Q^T    tcgen05.mma M 128 (tokens), N 16 (query heads, padded),
+//                  K-major A (the converted K tile) and B (the query rows);
+//   O^T += V^T P'  M 128 (head_dim), N 16, A = the converted V tile read
+//                  MN-major, B = P' (fp16, written by the softmax threads).
+// S^T and O^T live in TMEM (16 columns each per kv head).  Thread t of the
+// warpgroup owns token t of S^T (the online softmax over tokens: running
+// maximum per query head, shared by the warpgroup's threads, with the lazy
+// rule of the mma.sync kernel) and row d = t of O^T at the end of a piece.
+constexpr int kTcHeads = 2;                                 // kv heads per CTA
+constexpr int kTcTokens = 128;                              // tokens per tile (M of S^T)
+constexpr int kTcStages = kTcTokens / kStageTokens;         // stages per tile
+constexpr int kTcN = 16;                                    // padded query heads (N: 16 at M 128)
+constexpr int kTcMaxGroup = 8;                              // query slots of 8 heads fit beside the tiles
+constexpr int kTcThreads = 32 * (4 * kTcHeads + 2);         // warpgroups, producer, issuer
+constexpr int kTcProducerWarp = 4 * kTcHeads, kTcIssuerWarp = 4 * kTcHeads + 1;
+constexpr uint32_t kTcTmemCols = 64;                        // per head: S^T 16 + O^T 16 columns (32)
+constexpr uint32_t kTcKTile = kTcTokens * 128u * 2u;        // fp16 K tile: 2 panels x 128 rows x 128 B
+constexpr uint32_t kTcVTile = kTcTokens * 128u * 2u;        // fp16 V tile (MN-major for the product)
+constexpr uint32_t kTcQTile = kTcN * 128u * 2u;             // fp16 query rows: 2 panels x 16 rows x 128 B
+constexpr uint32_t kTcPTile = kTcN * 128u * 2u;             // P': 2 panels (64 tokens each) x 16 rows x 128 B
+constexpr uint32_t kTcRegion = kTcHeads * (kTcKTile + kTcVTile + kTcQTile + kTcPTile);
+constexpr uint32_t kTcRedBytes = kTcHeads * 4 * kTcN * 4;   // cross-warp reductions
+enum : uint32_t { kTcInfoFirst = 1, kTcInfoStop = 2 };
+
+struct TcSmem {
+    uint8_t *kt, *vt, *qt, *pt;   // head 0; head h at + h * size
+    float *red;                   // [kTcHeads][4][kTcN]
+    uint64_t *conv_full, *s_full, *p_full, *pv_done, *o_free, *fin;
+    uint32_t *info;               // [kTcHeads]: the tile's flags, for the issuer
+    uint32_t *tmem_base;
+};
+
+__device__ __forceinline__ TcSmem tc_carve(const SmemLayout &L)
+{
+    TcSmem T;
+    uint8_t *b = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(L.full_bar) + smem_tail_bytes() + 1023) & ~uintptr_t(1023));
+    T.kt = b;
+    T.vt = T.kt + kTcHeads * kTcKTile;
+    T.qt = T.vt + kTcHeads * kTcVTile;
+    T.pt = T.qt + kTcHeads * kTcQTile;
+    T.red = reinterpret_cast<float *>(T.pt + kTcHeads * kTcPTile);
+    T.conv_full = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(T.red) + kTcRedBytes);
+    T.s_full = T.conv_full + kTcHeads;
+    T.p_full = T.s_full + kTcHeads;
+    T.pv_done = T.p_full + kTcHeads;
+    T.o_free = T.pv_done + kTcHeads;
+    T.fin = T.o_free + kTcHeads;
+    T.info = reinterpret_cast<uint32_t *>(T.fin + 1);
+    T.tmem_base = T.info + kTcHeads;
+    return T;
+}
+
+// Bytes after the (1024-aligned) end of the split kernel's layout.
+__host__ __device__ constexpr size_t tc_smem_extra()
+{
+    return kTcRegion + kTcRedBytes + (5 * kTcHeads + 1) * sizeof(uint64_t) + (kTcHeads + 1) * 4 + 16;
+}
+
+// Named barrier of one warpgroup (ids 1 + h) that also returns the OR of a
+// predicate over its threads.
+__device__ __forceinline__ bool wg_bar_or(uint32_t id, bool v)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, %2, 128, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ void wg_bar(uint32_t id) { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); }
+
+// Named barrier of one warpgroup returning the AND of a predicate: a wait that
+// ran out for some warp ends the loop for the whole warpgroup at the same
+// point, so no warp is left at a barrier the others never reach.
+__device__ __forceinline__ bool wg_all(uint32_t id, bool v)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.and.pred p, %2, 128, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id)
+        : "memory");
+    return r != 0;
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_constant__ CUtensorMap k_map,
+                                                                 const __grid_constant__ CUtensorMap v_map,
+                                                                 const __grid_constant__ CUtensorMap ks_map,
+                                                                 const __grid_constant__ CUtensorMap vs_map,
+                                                                 const DecodeParams p)
+{
+    constexpr int D = 128;
+    extern __shared__ uint8_t smem_raw[];
+    SmemLayout L = carve(smem_raw, p);
+    TcSmem T = tc_carve(L);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < p.n_stages; ++i) {
+            mbar_init(&L.full_bar[i], 1);
+            mbar_init(&L.empty_bar[i], kTcHeads);   // one warp of each warpgroup converts a stage
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&L.qfull_bar[i], 1);
+            mbar_init(&L.qempty_bar[i], kTcHeads);
+        }
+        for (int h = 0; h < kTcHeads; ++h) {
+            mbar_init(&T.conv_full[h], 1);
+            mbar_init(&T.s_full[h], 1);
+            mbar_init(&T.p_full[h], 1);
+            mbar_init(&T.pv_done[h], 1);
+            mbar_init(&T.o_free[h], 1);
+        }
+        mbar_init(T.fin, 1);
+        *L.abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == kTcIssuerWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(T.tmem_base)),
+                     "r"(kTcTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *T.tmem_base;
+    grid_dependency_wait();     // the plan kernel's work list is complete and visible
+    grid_dependents_launch();   // the merge may start: the plan it reads first is complete
+
+    const uint32_t total_items = p.ws.header[kHdrTotal] * (uint32_t)p.n_hg;
+    volatile int32_t *abort_flag = L.abort_flag;
+    const int G = p.group;
+
+    if (warp == kTcProducerWarp) {
+        if (lane == 0) run_producer<D, true>(L, p, k_map, v_map, ks_map, vs_map, abort_flag, total_items);
+    } else if (warp == kTcIssuerWarp) {
+        // ===================== MMA issuer (one thread) =====================
+        if (lane == 0) {
+            const uint32_t idesc_s = umma_idesc_f16(kTcTokens, kTcN, false, false);
+            const uint32_t idesc_o = umma_idesc_f16(D, kTcN, true, false);
+            bool ok = true;
+            uint32_t tile = 0, pieces[kTcHeads] = {};
+            while (ok) {
+                uint32_t info[kTcHeads];
+                for (int h = 0; h < kTcHeads && ok; ++h) {
+                    ok = mbar_wait(&T.conv_full[h], tile & 1, abort_flag);
+                    info[h] = ok ? T.info[h] : 0u;
+                }
+                if (!ok || (info[0] & kTcInfoStop)) break;
+                tc_fence_after();
+                // S^T = K Q^T: k-step kk covers head_dim 16 kk .. 16 kk + 15 (32 bytes of
+                // a 128-byte panel row; panels of 64 columns)
+                for (int h = 0; h < kTcHeads; ++h) {
+                    const uint64_t a0 = umma_desc_sw128(smem_u32(T.kt + h * kTcKTile), 16, 1024);
+                    const uint64_t b0 = umma_desc_sw128(smem_u32(T.qt + h * kTcQTile), 16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        umma_bf16(tmem + h * 32u, desc_step(a0, (kk / 4) * (kTcTokens * 128u) + (kk % 4) * 32),
+                                  desc_step(b0, (kk / 4) * (kTcN * 128u) + (kk % 4) * 32), idesc_s, kk > 0);
+                    umma_commit(&T.s_full[h]);
+                }
+                // O^T += V^T P': k-step kk covers tokens 16 kk .. 16 kk + 15 (V: group kk of
+                // 4 KiB, 64-column panels 2 KiB apart, 8-token halves 1 KiB apart; P': 32
+                // bytes of a row, panels of 64 tokens)
+                for (int h = 0; h < kTcHeads && ok; ++h) {
+                    ok = mbar_wait(&T.p_full[h], tile & 1, abort_flag);
+                    const bool first = (info[h] & kTcInfoFirst) != 0;
+                    // the first product of a piece overwrites O^T: the warpgroup has read
+                    // out the previous piece's
+                    if (ok && first && pieces[h] > 0) ok = mbar_wait(&T.o_free[h], (pieces[h] - 1) & 1, abort_flag);
+                    if (!ok) break;
+                    if (first) ++pieces[h];
+                    tc_fence_after();
+                    const uint64_t a0 = umma_desc_sw128(smem_u32(T.vt + h * kTcVTile), 2048, 1024);
+                    const uint64_t b0 = umma_desc_sw128(smem_u32(T.pt + h * kTcPTile), 16, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < kTcTokens / 16; ++kk)
+                        umma_bf16(tmem + h * 32u + 16u, desc_step(a0, kk * 4096u),
+                                  desc_step(b0, (kk / 4) * (kTcN * 128u) + (kk % 4) * 32), idesc_o,
+                                  (kk > 0 || !first) ? 1u : 0u);
+                    umma_commit(&T.pv_done[h]);
+                }
+                ++tile;
+            }
+            if (!ok) {
+                report(p.dev_status, PKV_DEV_TIMEOUT);
+                *abort_flag = 1;
+            }
+            // every product issued has retired before the TMEM is released
+            umma_commit(T.fin);
+            (void)mbar_wait(T.fin, 0);
+        }
+        __syncwarp();
+    } else {
+        // ===================== conversion / softmax warpgroup of kv head h =====================
+        const int h = warp / 4, wq = warp % 4;        // warpgroup, its warp (TMEM lanes 32 wq ..)
+        const int t = threadIdx.x % 128;              // token row of the tile; row d = t of O^T
+        const uint32_t bar_id = 1 + h;
+        const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16) + h * 32u;
+        uint8_t *kt = T.kt + h * kTcKTile, *vt = T.vt + h * kTcVTile, *qt = T.qt + h * kTcQTile,
+                *pt = T.pt + h * kTcPTile;
+        float *red = T.red + h * 4 * kTcN;
+        const float c_lazy = kLazyMax;
+        float m[kTcN], lp[kTcN], pp[kTcN], qb[kTcN];
+#pragma unroll
+        for (int q = 0; q < kTcN; ++q) m[q] = -INFINITY, lp[q] = 0.f, pp[q] = 0.f, qb[q] = 0.f;
+        // P' rows of padding query heads stay zero
+        for (int i = t; i < (int)(kTcPTile / 16); i += 128)
+            *reinterpret_cast<uint4 *>(pt + i * 16) = make_uint4(0, 0, 0, 0);
+        uint32_t tile = 0, pieces = 0, phase = 0;
+        bool ok = true;
+        // this thread's stage of the tile: slot j = t / 16 of the eight, token t % 16
+        const int j = t / kStageTokens, tt = t % kStageTokens;
+        while (true) {
+            // --- stage 0 tells the piece or the stop (every wait is followed by a
+            // warpgroup-wide AND, so the warpgroup leaves the loop as one)
+            bool w = __all_sync(0xffffffffu, mbar_wait(&L.full_bar[0], phase, abort_flag, p.wait_ns));
+            if (!wg_all(bar_id, w)) {
+                ok = false;
+                break;
+            }
+            const StageMeta m0 = L.meta[0];
+            if (m0.flags & kMetaStop) {
+                if (t == 0) {
+                    T.info[h] = kTcInfoStop;
+                    mbar_arrive(&T.conv_full[h]);
+                }
+                break;
+            }
+            const bool first = (m0.flags & kMetaFirst) != 0;
+            // own stage; the V and P' tiles are free once the previous tile's
+            // product is done; a piece's first tile needs its query rows
+            w = __all_sync(0xffffffffu, mbar_wait(&L.full_bar[j], phase, abort_flag, p.wait_ns));
+            if (w && tile > 0)
+                w = __all_sync(0xffffffffu, mbar_wait(&T.pv_done[h], (tile - 1) & 1, abort_flag, p.wait_ns));
+            if (w && first)
+                w = __all_sync(0xffffffffu,
+                               mbar_wait(&L.qfull_bar[pieces & 1u], (pieces >> 1) & 1u, abort_flag, p.wait_ns));
+            if (!wg_all(bar_id, w)) {
+                ok = false;
+                break;
+            }
+            const StageMeta mj = L.meta[j];
+            const bool have = !(mj.flags & (kMetaPad | kMetaBad));
+            const bool valid = have && tt < mj.n_valid;
+            const uint8_t *stg = L.stages + (size_t)j * p.stage_bytes;
+            float sk = 0.f, sv = 0.f;
+            if (first) {
+                // the piece's query rows: fp16, K-major, 128-byte swizzle, rows >= G zero;
+                // qb = 1152 sum_d q_d of the fp16 rows
+                const uint32_t qs = pieces & 1u;
+                const __nv_bfloat16 *qrows =
+                    reinterpret_cast<const __nv_bfloat16 *>(L.q_slots + qs * p.q_slot_bytes) + (size_t)h * G * D;
+                float qpart[2] = {0.f, 0.f};
+#pragma unroll
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    const int c = 2 * t + c2, r = c / 16, ch = c % 16;     // 16-byte chunk ch of row r
+                    uint4 w = make_uint4(0, 0, 0, 0);
+                    if (r < G) {
+                        const uint4 x = *reinterpret_cast<const uint4 *>(qrows + r * D + ch * 8);
+                        const uint32_t xs[4] = {x.x, x.y, x.z, x.w};
+                        uint32_t ys[4];
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&xs[k]));
+                            ys[k] = pack_f16x2(f.x, f.y);
+                            const float2 g2 = __half22float2(*reinterpret_cast<const __half2 *>(&ys[k]));
+                            qpart[c2] += g2.x + g2.y;
+                        }
+                        w = make_uint4(ys[0], ys[1], ys[2], ys[3]);
+                    }
+                    *reinterpret_cast<uint4 *>(qt + (ch / 8) * (kTcN * 128u) + swz(r, ch % 8)) = w;
+                }
+                // row sums: the 8 threads of a row are consecutive (2 chunks each)
+                float rs = qpart[0] + qpart[1];
+                rs += __shfl_xor_sync(0xffffffffu, rs, 1);
+                rs += __shfl_xor_sync(0xffffffffu, rs, 2);
+                rs += __shfl_xor_sync(0xffffffffu, rs, 4);
+                if ((t & 7) == 0) red[t / 8] = rs;                      // row r = t / 8 (16 rows)
+#pragma unroll
+                for (int q = 0; q < kTcN; ++q) m[q] = -INFINITY, lp[q] = 0.f, pp[q] = 0.f;
+            }
+            // --- this thread's token row: K codes -> fp16 K tile (K-major, swizzled),
+            // V codes -> fp16 V tile (MN-major), scales
+            if (have) {
+                const uint8_t *kc = stg + (size_t)h * kStageTokens * D;
+                const uint8_t *vc = kc + p.kv_tile_bytes;
+                const float *scl = reinterpret_cast<const float *>(stg + 2 * p.kv_tile_bytes);
+                const int hoff = ((int)mj.head_group * kTcHeads + h) % p.scale_heads;
+                if (valid) {
+                    sk = scl[tt * p.scale_heads + hoff];
+                    sv = scl[p.scale_tile_bytes / 4 + tt * p.scale_heads + hoff];
+                }
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {              // 16 codes = two 16-byte fp16 chunks
+                    const uint4 xk = *reinterpret_cast<const uint4 *>(kc + swz(tt, ch));
+                    const uint4 xv = *reinterpret_cast<const uint4 *>(vc + swz(tt, ch));
+                    uint4 ka, kb, va_, vb;
+                    int8x4_to_biased_half2x2(xk.x, ka.x, ka.y);
+                    int8x4_to_biased_half2x2(xk.y, ka.z, ka.w);
+                    int8x4_to_biased_half2x2(xk.z, kb.x, kb.y);
+                    int8x4_to_biased_half2x2(xk.w, kb.z, kb.w);
+                    int8x4_to_biased_half2x2(xv.x, va_.x, va_.y);
+                    int8x4_to_biased_half2x2(xv.y, va_.z, va_.w);
+                    int8x4_to_biased_half2x2(xv.z, vb.x, vb.y);
+                    int8x4_to_biased_half2x2(xv.w, vb.z, vb.w);
+                    // d = 16 ch .. 16 ch + 15: fp16 chunks 2 ch and 2 ch + 1
+                    const int c0 = 2 * ch, c1 = 2 * ch + 1;
+                    *reinterpret_cast<uint4 *>(kt + (c0 / 8) * (kTcTokens * 128u) + swz(t, c0 % 8)) = ka;
+                    *reinterpret_cast<uint4 *>(kt + (c1 / 8) * (kTcTokens * 128u) + swz(t, c1 % 8)) = kb;
+                    // V tile: 16-token group t / 16 at 4 KiB, panel d / 64 at 2 KiB, 8-token
+                    // half at 1 KiB, row t % 8
+                    uint8_t *vg = vt + (t / 16) * 4096u + ((t / 8) & 1) * 1024u;
+                    *reinterpret_cast<uint4 *>(vg + (c0 / 8) * 2048u + swz(t % 8, c0 % 8)) = va_;
+                    *reinterpret_cast<uint4 *>(vg + (c1 / 8) * 2048u + swz(t % 8, c1 % 8)) = vb;
+                }
+            } else {
+                // absent rows: zero V (0 x NaN must not reach O); K rows are masked
+                uint8_t *vg = vt + (t / 16) * 4096u + ((t / 8) & 1) * 1024u;
+#pragma unroll
+                for (int c = 0; c < 16; ++c)
+                    *reinterpret_cast<uint4 *>(vg + (c / 8) * 2048u + swz(t % 8, c % 8)) = make_uint4(0, 0, 0, 0);
+            }
+            // the stage (and at a piece's end the query slot) is converted: hand it back
+            const bool last_here = have && (mj.flags & kMetaLast) != 0;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&L.empty_bar[j]);
+            if (lane == 16) mbar_arrive(&L.empty_bar[j]);
+            fence_proxy_async_smem();                 // generic writes -> tensor-core reads
+            const bool last = wg_bar_or(bar_id, last_here);
+            if (first) {
+                // qb from the 16 row sums (written before the barrier)
+#pragma unroll
+                for (int q = 0; q < kTcN; ++q) qb[q] = kCodeBias * red[q];
+            }
+            if (t == 0) {
+                T.info[h] = first ? kTcInfoFirst : 0u;
+                mbar_arrive(&T.conv_full[h]);
+            }
+            phase ^= 1u;                              // all eight slots consumed once
+            // --- softmax over the tile's tokens
+            w = __all_sync(0xffffffffu, mbar_wait(&T.s_full[h], tile & 1, abort_flag, p.wait_ns));
+            if (!wg_all(bar_id, w)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t sr[kTcN];
+            tmem_ld16_async(lane_base, sr);
+            tmem_wait_ld();
+            float x[kTcN];
+            const float c = sk * p.scale_log2;
+#pragma unroll
+            for (int q = 0; q < kTcN; ++q) x[q] = (valid && q < G) ? (__uint_as_float(sr[q]) - qb[q]) * c : -INFINITY;
+            bool up = false;
+#pragma unroll
+            for (int q = 0; q < kTcN; ++q) up |= x[q] > m[q] + c_lazy;
+            if (wg_bar_or(bar_id, up)) {
+                // the running maximum moves: the tile's maximum per query head
+                float mt[kTcN];
+#pragma unroll
+                for (int q = 0; q < kTcN; ++q) {
+                    float v = x[q];
+#pragma unroll
+                    for (int off = 16; off >= 1; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+                    mt[q] = v;
+                }
+                wg_bar(bar_id);                        // red is free (qb was read)
+                if (lane == 0)
+#pragma unroll
+                    for (int q = 0; q < kTcN; ++q) red[wq * kTcN + q] = mt[q];
+                wg_bar(bar_id);
+                float al[kTcN];
+#pragma unroll
+                for (int q = 0; q < kTcN; ++q) {
+                    const float tm = fmaxf(fmaxf(red[q], red[kTcN + q]), fmaxf(red[2 * kTcN + q], red[3 * kTcN + q]));
+                    const float mn = fmaxf(m[q], tm);
+                    al[q] = (mn == -INFINITY) ? 1.f : fast_exp2(m[q] - mn);
+                    m[q] = mn;
+                    lp[q] *= al[q];
+                    pp[q] *= al[q];
+                }
+                if (!first) {
+                    // O^T columns of this head hold the piece so far (the previous
+                    // tile's product is done): rescale row d = t
+                    uint32_t o[kTcN];
+                    tmem_ld16_async(lane_base + 16u, o);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int q = 0; q < kTcN; ++q) o[q] = __float_as_uint(__uint_as_float(o[q]) * al[q]);
+                    tmem_st16_async(lane_base + 16u, o);
+                    tmem_wait_st();
+                }
+            }
+            // P' = p * v_scale (fp16) into the B tile: row q, token t
+            {
+                const uint32_t prow = (t / 64) * (kTcN * 128u) + (t % 8) * 2u;
+                const uint32_t pch = (t % 64) / 8;
+#pragma unroll
+                for (int q = 0; q < kTcN; ++q) {
+                    const float pr = x[q] == -INFINITY ? 0.f : fast_exp2(x[q] - m[q]);
+                    lp[q] += pr;
+                    const __half hv = __float2half_rn(pr * sv);
+                    pp[q] += __half2float(hv);
+                    if (q < G)
+                        *reinterpret_cast<__half *>(pt + prow + swz(q, pch)) = hv;
+                }
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            wg_bar(bar_id);
+            if (t == 0) mbar_arrive(&T.p_full[h]);
+            if (last) {
+                // --- end of the piece: row sums over the tokens, then O^T row d = t
+                w = __all_sync(0xffffffffu, mbar_wait(&T.pv_done[h], tile & 1, abort_flag, p.wait_ns));
+                if (!wg_all(bar_id, w)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                uint32_t o[kTcN];
+                tmem_ld16_async(lane_base + 16u, o);
+                tmem_wait_ld();
+                tc_fence_before();
+                float Ls[kTcN], Ps[kTcN];
+#pragma unroll
+                for (int q = 0; q < kTcN; ++q) {
+                    float a = lp[q], b = pp[q];
+#pragma unroll
+                    for (int off = 16; off >= 1; off >>= 1) {
+                        a += __shfl_xor_sync(0xffffffffu, a, off);
+                        b += __shfl_xor_sync(0xffffffffu, b, off);
+                    }
+                    Ls[q] = a;
+                    Ps[q] = b;
+                }
+                if (lane == 0)
+#pragma unroll
+                    for (int q = 0; q < kTcN; ++q) red[wq * kTcN + q] = Ls[q];
+                wg_bar(bar_id);
+#pragma unroll
+                for (int q = 0; q < kTcN; ++q) Ls[q] = red[q] + red[kTcN + q] + red[2 * kTcN + q] + red[3 * kTcN + q];
+                wg_bar(bar_id);
+                if (lane == 0)
+#pragma unroll
+                    for (int q = 0; q < kTcN; ++q) red[wq * kTcN + q] = Ps[q];
+                wg_bar(bar_id);
+#pragma unroll
+                for (int q = 0; q < kTcN; ++q) Ps[q] = red[q] + red[kTcN + q] + red[2 * kTcN + q] + red[3 * kTcN + q];
+                // O^T is read out: the next piece's first product may overwrite it
+                if (t == 0) mbar_arrive(&T.o_free[h]);
+                const int32_t s = m0.seq;
+                const int32_t hq0 = (m0.head_group * kTcHeads + h) * G;
+                if (m0.flags & kMetaFinal) {
+                    __nv_bfloat16 *o_out = p.out + ((int64_t)s * p.n_q_heads + hq0) * D + t;
+#pragma unroll
+                    for (int q = 0; q < kTcN; ++q)
+                        if (q < G)
+                            o_out[(size_t)q * D] =
+                                __float2bfloat16_rn((__uint_as_float(o[q]) - kCodeBias * Ps[q]) / Ls[q]);
+                    if (p.lse_out && t < G) {
+                        float mm = 0.f, ll = 1.f;
+#pragma unroll
+                        for (int q = 0; q < kTcN; ++q)
+                            if (q == t) mm = m[q], ll = Ls[q];
+                        p.lse_out[(int64_t)s * p.n_q_heads + hq0 + t] = (mm + __log2f(ll)) * 0.69314718055994531f;
+                    }
+                } else {
+                    const int64_t prow = (int64_t)m0.split_index * p.n_q_heads + hq0;
+#pragma unroll
+                    for (int q = 0; q < kTcN; ++q)
+                        if (q < G) p.ws.part_acc[(prow + q) * D + t] = __uint_as_float(o[q]) - kCodeBias * Ps[q];
+                    if (t < G) {
+                        float mm = 0.f, ll = 1.f;
+#pragma unroll
+                        for (int q = 0; q < kTcN; ++q)
+                            if (q == t) mm = m[q], ll = Ls[q];
+                        p.ws.part_ml[prow + t] = make_float2(mm, ll);
+                    }
+                }
+                if (t == 0) mbar_arrive(&L.qempty_bar[pieces & 1u]);
+                ++pieces;
+            }
+            ++tile;
+        }
+        if (!ok) {
+            if (lane == 0) report(p.dev_status, PKV_DEV_TIMEOUT);
+            *abort_flag = 1;
+        }
+    }
+    // everyone meets here before the TMEM is released
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kTcIssuerWarp) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTcTmemCols) : "memory");
+    }
+}
+
 }  // namespace pkv
 
 namespace pkv {
@@ -1250,9 +1808,23 @@ int encode_pool_map(CUtensorMap *map, const void *pool, CUtensorMapDataType dt, 
     return -1;
 }
 
-template <int D, bool INT8>
+// int8 pages of head_dim 128 with up to 8 query heads per kv head (and kv
+// heads in multiples of 4) can take the tensor-core kernel; PKV_DECODE_IMPL=tc
+// selects it.
+bool use_tc_decode(const DecodeArgs &a)
+{
+    const int G = a.n_q_heads / a.dims.n_kv_heads;
+    if (G > kTcMaxGroup || a.dims.n_kv_heads % 4 != 0) return false;
+    const char *impl = getenv("PKV_DECODE_IMPL");
+    return impl && strcmp(impl, "tc") == 0;
+}
+
+// TC: the tensor-core kernel (int8 pages, head_dim 128, G <= 8): two kv
+// heads per CTA, one CTA per SM, a ring of exactly one 128-token tile.
+template <int D, bool INT8, bool TC = false>
 cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream, const WriteArgs *write)
 {
+    static_assert(!TC || (INT8 && D == 128), "the tensor-core kernel takes int8 pages of head_dim 128");
     const pkv_dims &d = a.dims;
     const int G = a.n_q_heads / d.n_kv_heads;
     // Launch shape (measured on GB300): one CTA per SM serving up to 8 kv
@@ -1267,6 +1839,11 @@ cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream, 
     if (G >= 8 && d.n_kv_heads % 4 == 0) {
         hpc = 4;
         ctas_per_sm = 2;
+    }
+    if (TC) {
+        if (G > kTcMaxGroup || d.n_kv_heads % 4 != 0) return cudaErrorInvalidValue;
+        hpc = kTcHeads;
+        ctas_per_sm = 1;
     }
     if (hpc == 0) return cudaErrorInvalidValue;
 
@@ -1290,13 +1867,15 @@ cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream, 
     p.ws = a.ws;
     p.dev_status = a.dev_status;
     p.wait_ns = pipeline_wait_ns();
+    p.scale_heads = TC ? 4 : hpc;
+    p.tile_stages = TC ? kTcStages : 0;
     if (!INT8) {
         p.kv_tile_bytes = (uint32_t)(D / 64) * hpc * 16u * 128u;
         p.scale_tile_bytes = 0;
         p.tx_bytes = 2 * p.kv_tile_bytes;
     } else {
         p.kv_tile_bytes = (uint32_t)hpc * 16u * D;
-        p.scale_tile_bytes = (uint32_t)hpc * 16u * 4u;
+        p.scale_tile_bytes = (uint32_t)p.scale_heads * 16u * 4u;
         p.tx_bytes = 2 * p.kv_tile_bytes + 2 * p.scale_tile_bytes;
     }
     p.stage_bytes = (uint32_t)align_up(p.tx_bytes, 1024);
@@ -1317,7 +1896,7 @@ cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream, 
         const uint64_t rows = (uint64_t)(d.n_blocks + 1) * d.block_size;
         const uint64_t dims[2] = {(uint64_t)d.n_kv_heads, rows};
         const uint64_t strides[1] = {(uint64_t)d.n_kv_heads * 4};
-        const uint32_t box[2] = {(uint32_t)hpc, 16u};
+        const uint32_t box[2] = {(uint32_t)p.scale_heads, 16u};
         if (encode_tensor_map(&ksmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, (void *)a.k_scales, dims, strides,
                               box, CU_TENSOR_MAP_SWIZZLE_NONE) != CUDA_SUCCESS ||
             encode_tensor_map(&vsmap, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, (void *)a.v_scales, dims, strides,
@@ -1334,13 +1913,20 @@ cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream, 
     // int8 pages: at most four stages (measured faster on GB300 than deeper rings)
     const int stage_cap = INT8 ? 4 : kMaxStages;
     stages = stages > stage_cap ? stage_cap : stages;
+    size_t smem = fixed + (size_t)stages * p.stage_bytes;
+    if (TC) {
+        // exactly one tile of stages, then the fp16 tiles from a 1024-byte boundary
+        stages = kTcStages;
+        smem = 1024 + align_up((size_t)stages * p.stage_bytes + 2 * (size_t)p.q_slot_bytes + smem_tail_bytes(), 1024) +
+               tc_smem_extra();
+        if (smem > max_smem) return cudaErrorInvalidValue;
+    }
     p.n_stages = stages;
-    const size_t smem = fixed + (size_t)stages * p.stage_bytes;
 
-    auto kern = decode_split_kernel<D, INT8>;
+    auto kern = TC ? decode_tc_kernel : decode_split_kernel<D, INT8>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    const int threads = 32 * (hpc + 1);
+    const int threads = TC ? kTcThreads : 32 * (hpc + 1);
     int occ = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
     if (e != cudaSuccess) return e;
@@ -1403,6 +1989,8 @@ cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream, 
 cudaError_t launch_decode(const DecodeArgs &a, int num_sms, cudaStream_t stream, const WriteArgs *write)
 {
     const bool int8 = a.kv_dtype == PKV_KV_INT8;
+    if (a.dims.head_dim == 128 && int8 && use_tc_decode(a))
+        return launch_split<128, true, true>(a, num_sms, stream, write);
     if (a.dims.head_dim == 128)
         return int8 ? launch_split<128, true>(a, num_sms, stream, write)
                     : launch_split<128, false>(a, num_sms, stream, write);
