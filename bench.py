@@ -1288,6 +1288,19 @@ def other_configs(args, P, device):
         sub["metric"] = METRIC
         if cfg == 2:
             sub["gather"] = bench_gather(P, device, peak)
+            # the same step on the tensor-core (tcgen05) decode kernel, selected
+            # per call with PKV_DECODE_IMPL=tc
+            prev = os.environ.get("PKV_DECODE_IMPL")
+            os.environ["PKV_DECODE_IMPL"] = "tc"
+            try:
+                tc = run_decode_bench(args, P, w, device, 0, 1, 50, 5, with_e2e=False)
+            finally:
+                if prev is None:
+                    os.environ.pop("PKV_DECODE_IMPL", None)
+                else:
+                    os.environ["PKV_DECODE_IMPL"] = prev
+            sub["tensor_core_decode"] = {k: tc[k] for k in ("value", "unit", "ms_per_step", "pct_of_peak", "timing",
+                                                            "gpu_launches") if k in tc}
         if cfg == 4:
             # shared prefix blocks are read by every member: report the unique bytes too
             sub["unique_kv_bytes_per_step"] = unique_kv_bytes(w)
