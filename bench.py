@@ -918,6 +918,15 @@ def run_layers_bench(args, P, device):
                                 w.softmax_scale, k_scales=x["ks"], v_scales=x["vs"], split_tokens=w.split_tokens,
                                 out=x["out"], workspace=ws, dev_status=status)
 
+    # the same calls through one DecodePlan per layer (the fixed arguments checked once)
+    plans = [P.DecodePlan(x["kp"], x["vp"], tables, ctx, w.softmax_scale, w.n_q_heads, k_scales=x["ks"],
+                          v_scales=x["vs"], split_tokens=w.split_tokens, out=x["out"], workspace=ws,
+                          dev_status=status) for x in layers]
+
+    def step_planned():
+        for x, plan in zip(layers, plans):
+            plan.run(x["q"], x["k_new"], x["v_new"], start)
+
     side = torch.cuda.Stream(device)
     side.wait_stream(torch.cuda.current_stream())
     with torch.cuda.stream(side):
@@ -949,6 +958,7 @@ def run_layers_bench(args, P, device):
     with ClockSampler(uuid) as clk:
         time.sleep(0.25)
         ms_eager = timed(step)
+        ms_planned = timed(step_planned)
         ms_graph = timed(graph.replay)
     assert int(status.item()) == 0
     decode_b, write_b = algorithmic_bytes(w)
@@ -963,6 +973,10 @@ def run_layers_bench(args, P, device):
                                                         os.environ.get("PKV_DECODE_IMPL") != "split" else 3)},
             "eager": {"ms_per_step": round(ms_eager, 4), "value": round(w.n_seqs / (ms_eager * 1e-3), 1),
                       "gb_per_s": round(L * (decode_b + write_b) / (ms_eager * 1e-3) / 1e9, 2)},
+            "eager_planned": {"ms_per_step": round(ms_planned, 4),
+                              "value": round(w.n_seqs / (ms_planned * 1e-3), 1),
+                              "gb_per_s": round(L * (decode_b + write_b) / (ms_planned * 1e-3) / 1e9, 2),
+                              "how": "one DecodePlan per layer, run(q, k_new, v_new, start_pos) per call"},
             "clocks": clk.summary()}
     print(json.dumps(line), flush=True)
 

@@ -139,34 +139,65 @@ def _check(fn, status):
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # ctypes turns an int into the void * argument
+    return None if t is None else t.data_ptr()
+
+
+try:
+    from torch._C import _cuda_getCurrentRawStream as _raw_stream, _cuda_getDevice as _current_device
+except ImportError:      # pragma: no cover - older PyTorch builds
+    _raw_stream = _current_device = None
 
 
 def _stream(stream):
-    if stream is None:
-        stream = torch.cuda.current_stream()
-    return ctypes.c_void_p(stream.cuda_stream)
+    """The cudaStream_t of `stream`, or of the current stream of the current
+    device (as an int)."""
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None:
+        return _raw_stream(_current_device())
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _device_of(t, name):
+    """CUDA device index of the tensor the other arguments must share."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    d = t.get_device()
+    if d < 0:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    return d
 
 
 def _need(t, name, dtype=None, ndim=None, device=None):
+    """A contiguous CUDA tensor of the given dtype, rank and device index; the
+    common case is one test, the messages come from _refuse."""
+    if (isinstance(t, torch.Tensor) and (dtype is None or t.dtype is dtype) and (ndim is None or t.dim() == ndim)
+            and t.is_contiguous() and (t.get_device() == device if device is not None else t.is_cuda)):
+        return
+    _refuse(t, name, dtype, ndim, device)
+
+
+def _refuse(t, name, dtype, ndim, device):
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if not t.is_cuda:
         raise ValueError(f"{name} must be a CUDA tensor")
-    if device is not None and t.device != device:
-        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if device is not None and t.get_device() != device:
+        raise ValueError(f"{name} is on {t.device}, expected cuda:{device}")
     if dtype is not None and t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
     if ndim is not None and t.dim() != ndim:
         raise ValueError(f"{name} must have {ndim} dims, got {tuple(t.shape)}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+    raise ValueError(f"{name} was refused")
 
 
 def _shape(t, name, shape):
     """A tensor of the wrong shape would become an out-of-bounds device access:
     refuse it here."""
-    if t is not None and tuple(t.shape) != tuple(shape):
+    if t is not None and t.shape != shape:
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
 
 
@@ -196,20 +227,34 @@ def pool_dims(k_pool: torch.Tensor) -> Dims:
     return Dims(nb1 - 1, bs, hkv, d)
 
 
+_dims_cache = {}
+
+
+def _dims(k_pool):
+    """pool_dims, one shared (never modified) structure per pool shape."""
+    d = _dims_cache.get(k_pool.shape)
+    if d is None:
+        if len(_dims_cache) > 64:
+            _dims_cache.clear()
+        d = _dims_cache[k_pool.shape] = pool_dims(k_pool)
+    return d
+
+
 def paged_kv_write(k_new, v_new, k_pool, v_pool, block_tables, start_pos, dev_status=None, stream=None):
     """Native bf16 page write: k_new/v_new [n_seqs, n_new, Hkv, D] to positions
     start_pos[s] .. of each sequence."""
     lib = load_library()
+    dev = _device_of(k_pool, "k_pool")
     for t, n in ((k_new, "k_new"), (v_new, "v_new"), (k_pool, "k_pool"), (v_pool, "v_pool")):
-        _need(t, n, torch.bfloat16, 4, k_pool.device)
-    _need(block_tables, "block_tables", torch.int32, 2, k_pool.device)
-    _need(start_pos, "start_pos", torch.int32, 1, k_pool.device)
-    _check_status(dev_status, k_pool.device)
+        _need(t, n, torch.bfloat16, 4, dev)
+    _need(block_tables, "block_tables", torch.int32, 2, dev)
+    _need(start_pos, "start_pos", torch.int32, 1, dev)
+    _check_status(dev_status, dev)
     _check_pools(k_pool, v_pool)
     _shape(k_new, "k_new", (k_new.shape[0], k_new.shape[1]) + tuple(k_pool.shape[2:]))
     _shape(v_new, "v_new", k_new.shape)
     _check_batch(k_new.shape[0], block_tables, start_pos, "start_pos")
-    st = lib.paged_kv_write(_ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool), pool_dims(k_pool),
+    st = lib.paged_kv_write(_ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool), _dims(k_pool),
                             _ptr(block_tables), block_tables.shape[1], _ptr(start_pos), k_new.shape[0],
                             k_new.shape[1], _ptr(dev_status), _stream(stream))
     _check("paged_kv_write", st)
@@ -219,7 +264,7 @@ def paged_kv_write_int8(k_new, v_new, k_pool, v_pool, k_scales, v_scales, block_
                         dev_status=None, stream=None):
     """Quantised page write: int8 pools [NB+1, bs, Hkv, D], fp32 scales [NB+1, bs, Hkv]."""
     lib = load_library()
-    dev = k_pool.device
+    dev = _device_of(k_pool, "k_pool")
     _need(k_new, "k_new", torch.bfloat16, 4, dev)
     _need(v_new, "v_new", torch.bfloat16, 4, dev)
     _need(k_pool, "k_pool", torch.int8, 4, dev)
@@ -234,7 +279,7 @@ def paged_kv_write_int8(k_new, v_new, k_pool, v_pool, k_scales, v_scales, block_
     _shape(v_new, "v_new", k_new.shape)
     _check_batch(k_new.shape[0], block_tables, start_pos, "start_pos")
     st = lib.paged_kv_write_int8(_ptr(k_new), _ptr(v_new), _ptr(k_pool), _ptr(v_pool), _ptr(k_scales),
-                                 _ptr(v_scales), pool_dims(k_pool), _ptr(block_tables), block_tables.shape[1],
+                                 _ptr(v_scales), _dims(k_pool), _ptr(block_tables), block_tables.shape[1],
                                  _ptr(start_pos), k_new.shape[0], k_new.shape[1], _ptr(dev_status),
                                  _stream(stream))
     _check("paged_kv_write_int8", st)
@@ -245,7 +290,7 @@ def paged_kv_gather(k_pool, v_pool, block_tables, lens, out_tokens, k_out=None, 
     """Contiguous copy [n_seqs, Hkv, out_tokens, D] of every sequence's pages
     (zeros past its length).  Returns (k_out, v_out)."""
     lib = load_library()
-    dev = k_pool.device
+    dev = _device_of(k_pool, "k_pool")
     _need(k_pool, "k_pool", torch.bfloat16, 4, dev)
     _need(v_pool, "v_pool", torch.bfloat16, 4, dev)
     _need(block_tables, "block_tables", torch.int32, 2, dev)
@@ -263,7 +308,7 @@ def paged_kv_gather(k_pool, v_pool, block_tables, lens, out_tokens, k_out=None, 
     _check_batch(n_seqs, block_tables, lens, "lens")
     _shape(k_out, "k_out", shape)
     _shape(v_out, "v_out", shape)
-    st = lib.paged_kv_gather(_ptr(k_pool), _ptr(v_pool), pool_dims(k_pool), _ptr(block_tables),
+    st = lib.paged_kv_gather(_ptr(k_pool), _ptr(v_pool), _dims(k_pool), _ptr(block_tables),
                              block_tables.shape[1], _ptr(lens), n_seqs, int(out_tokens), _ptr(k_out), _ptr(v_out),
                              _ptr(dev_status), _stream(stream))
     _check("paged_kv_gather", st)
@@ -274,7 +319,7 @@ def paged_kv_copy_blocks(pairs, k_pool, v_pool, k_scales=None, v_scales=None, de
     """Copy whole pool blocks: pairs int32 [n, 2] of (source, destination) ids
     on the device (the device half of copy-on-write)."""
     lib = load_library()
-    dev = k_pool.device
+    dev = _device_of(k_pool, "k_pool")
     _need(pairs, "pairs", torch.int32, 2, dev)
     int8 = k_pool.dtype == torch.int8
     if int8:
@@ -288,7 +333,7 @@ def paged_kv_copy_blocks(pairs, k_pool, v_pool, k_scales=None, v_scales=None, de
     if pairs.shape[1] != 2:
         raise ValueError(f"pairs must be [n, 2], got {tuple(pairs.shape)}")
     st = lib.paged_kv_copy_blocks(_ptr(pairs), pairs.shape[0], _ptr(k_pool), _ptr(v_pool), _ptr(k_scales),
-                                  _ptr(v_scales), PKV_KV_INT8 if int8 else PKV_KV_BF16, pool_dims(k_pool),
+                                  _ptr(v_scales), PKV_KV_INT8 if int8 else PKV_KV_BF16, _dims(k_pool),
                                   _ptr(dev_status), _stream(stream))
     _check("paged_kv_copy_blocks", st)
 
@@ -306,7 +351,7 @@ def decode_workspace_bytes(n_seqs, n_q_heads, head_dim, max_total_ctx_tokens, sp
 def _check_decode(q, k_pool, v_pool, k_scales, v_scales, block_tables, ctx_lens, out, lse_out, dev_status):
     """Shapes of a decode call's tensors against q [n_seqs, Hq, D] and the pool."""
     n_seqs, n_q_heads, D = q.shape
-    _check_status(dev_status, q.device)
+    _check_status(dev_status, q.get_device())
     _check_pools(k_pool, v_pool, k_scales, v_scales)
     if k_pool.shape[3] != D:
         raise ValueError(f"q has head_dim {D}, the pool {k_pool.shape[3]}")
@@ -323,7 +368,7 @@ def paged_decode_attention(q, k_pool, v_pool, block_tables, ctx_lens, softmax_sc
     ``workspace`` (uint8 CUDA tensor) is allocated when not given, sized from
     max_total_ctx_tokens (default: every table entry full)."""
     lib = load_library()
-    dev = q.device
+    dev = _device_of(q, "q")
     _need(q, "q", torch.bfloat16, 3, dev)
     int8 = k_pool.dtype == torch.int8
     _need(k_pool, "k_pool", torch.int8 if int8 else torch.bfloat16, 4, dev)
@@ -347,7 +392,7 @@ def paged_decode_attention(q, k_pool, v_pool, block_tables, ctx_lens, softmax_sc
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     _need(workspace, "workspace", torch.uint8, 1, dev)
     st = lib.paged_decode_attention(_ptr(q), n_q_heads, _ptr(k_pool), _ptr(v_pool), _ptr(k_scales),
-                                    _ptr(v_scales), PKV_KV_INT8 if int8 else PKV_KV_BF16, pool_dims(k_pool),
+                                    _ptr(v_scales), PKV_KV_INT8 if int8 else PKV_KV_BF16, _dims(k_pool),
                                     _ptr(block_tables), block_tables.shape[1], _ptr(ctx_lens), n_seqs,
                                     float(softmax_scale), int(split_tokens), _ptr(out), _ptr(lse_out),
                                     _ptr(workspace), workspace.numel(), _ptr(dev_status), _stream(stream))
@@ -363,7 +408,7 @@ def paged_decode_step(k_new, v_new, start_pos, q, k_pool, v_pool, block_tables, 
     decode attention over ctx_lens tokens (which count the new rows), in one
     call.  Returns out [n_seqs, Hq, D] bf16."""
     lib = load_library()
-    dev = q.device
+    dev = _device_of(q, "q")
     _need(q, "q", torch.bfloat16, 3, dev)
     _need(k_new, "k_new", torch.bfloat16, 4, dev)
     _need(v_new, "v_new", torch.bfloat16, 4, dev)
@@ -396,12 +441,91 @@ def paged_decode_step(k_new, v_new, start_pos, q, k_pool, v_pool, block_tables, 
     _need(workspace, "workspace", torch.uint8, 1, dev)
     st = lib.paged_decode_step(_ptr(k_new), _ptr(v_new), _ptr(start_pos), k_new.shape[1], _ptr(q), n_q_heads,
                                _ptr(k_pool), _ptr(v_pool), _ptr(k_scales), _ptr(v_scales),
-                               PKV_KV_INT8 if int8 else PKV_KV_BF16, pool_dims(k_pool), _ptr(block_tables),
+                               PKV_KV_INT8 if int8 else PKV_KV_BF16, _dims(k_pool), _ptr(block_tables),
                                block_tables.shape[1], _ptr(ctx_lens), n_seqs, float(softmax_scale),
                                int(split_tokens), _ptr(out), _ptr(lse_out), _ptr(workspace), workspace.numel(),
                                _ptr(dev_status), _stream(stream))
     _check("paged_decode_step", st)
     return out
+
+
+class DecodePlan:
+    """paged_decode_attention / paged_decode_step with the arguments that stay
+    the same from call to call checked once: the pools (and int8 scales), the
+    block tables and lengths, the workspace, out, lse_out and dev_status.
+    ``run(q)`` then checks only q (and, for a step, k_new / v_new / start_pos)
+    before the library call, which keeps the host's cost per call low where
+    the GPU work is short (small batches, one call per layer).
+
+    The plan keeps references to its tensors and reads their contents at every
+    call (so block tables and lengths may be rewritten in place between calls);
+    they must keep their shapes and storage: resizing one after planning is not
+    allowed.  ``max_total_ctx_tokens`` bounds sum(ctx_lens) over every call.
+    Returns ``out`` from ``run``."""
+
+    def __init__(self, k_pool, v_pool, block_tables, ctx_lens, softmax_scale, n_q_heads, k_scales=None,
+                 v_scales=None, split_tokens=0, out=None, lse_out=None, workspace=None, max_total_ctx_tokens=None,
+                 dev_status=None):
+        dev = _device_of(k_pool, "k_pool")
+        self._lib = load_library()
+        n_seqs, D = block_tables.shape[0], k_pool.shape[3]
+        q_like = torch.empty((n_seqs, int(n_q_heads), D), dtype=torch.bfloat16, device=dev)
+        if out is None:
+            out = torch.empty_like(q_like)
+        # the one-call checks against a query of the planned shape
+        self.int8 = k_pool.dtype is torch.int8
+        _need(k_pool, "k_pool", torch.int8 if self.int8 else torch.bfloat16, 4, dev)
+        _need(v_pool, "v_pool", torch.int8 if self.int8 else torch.bfloat16, 4, dev)
+        if self.int8:
+            _need(k_scales, "k_scales", torch.float32, 3, dev)
+            _need(v_scales, "v_scales", torch.float32, 3, dev)
+        _need(block_tables, "block_tables", torch.int32, 2, dev)
+        _need(ctx_lens, "ctx_lens", torch.int32, 1, dev)
+        _need(out, "out", torch.bfloat16, 3, dev)
+        if lse_out is not None:
+            _need(lse_out, "lse_out", torch.float32, 2, dev)
+        _check_decode(q_like, k_pool, v_pool, k_scales, v_scales, block_tables, ctx_lens, out, lse_out, dev_status)
+        if workspace is None:
+            if max_total_ctx_tokens is None:
+                max_total_ctx_tokens = n_seqs * block_tables.shape[1] * k_pool.shape[1]
+            workspace = torch.empty(decode_workspace_bytes(n_seqs, n_q_heads, D, max_total_ctx_tokens,
+                                                           split_tokens), dtype=torch.uint8, device=dev)
+        _need(workspace, "workspace", torch.uint8, 1, dev)
+        self.device, self.q_shape, self.out = dev, q_like.shape, out
+        self.new_shape_tail = tuple(k_pool.shape[2:])
+        # held so that the pointers below stay valid
+        self._tensors = (k_pool, v_pool, k_scales, v_scales, block_tables, ctx_lens, out, lse_out, workspace,
+                         dev_status)
+        self._pools = (_ptr(k_pool), _ptr(v_pool), _ptr(k_scales), _ptr(v_scales),
+                       PKV_KV_INT8 if self.int8 else PKV_KV_BF16, pool_dims(k_pool), _ptr(block_tables),
+                       block_tables.shape[1], _ptr(ctx_lens), n_seqs, float(softmax_scale), int(split_tokens),
+                       _ptr(out), _ptr(lse_out), _ptr(workspace), workspace.numel(), _ptr(dev_status))
+        self.n_q_heads, self.n_seqs = int(n_q_heads), n_seqs
+
+    def run(self, q, k_new=None, v_new=None, start_pos=None, stream=None):
+        """Decode attention of q [n_seqs, Hq, D] (bf16) over the planned pools;
+        with k_new / v_new [n_seqs, n_new, Hkv, D] and start_pos [n_seqs] the
+        step's page write runs first, in the same call (paged_decode_step)."""
+        dev = self.device
+        _need(q, "q", torch.bfloat16, 3, dev)
+        _shape(q, "q", self.q_shape)
+        if k_new is None:
+            if v_new is not None or start_pos is not None:
+                raise ValueError("v_new and start_pos come with k_new")
+            st = self._lib.paged_decode_attention(q.data_ptr(), self.n_q_heads, *self._pools, _stream(stream))
+            _check("paged_decode_attention", st)
+            return self.out
+        _need(k_new, "k_new", torch.bfloat16, 4, dev)
+        _need(v_new, "v_new", torch.bfloat16, 4, dev)
+        _need(start_pos, "start_pos", torch.int32, 1, dev)
+        n_new = k_new.shape[1]
+        _shape(k_new, "k_new", (self.n_seqs, n_new) + self.new_shape_tail)
+        _shape(v_new, "v_new", k_new.shape)
+        _shape(start_pos, "start_pos", (self.n_seqs,))
+        st = self._lib.paged_decode_step(k_new.data_ptr(), v_new.data_ptr(), start_pos.data_ptr(), n_new,
+                                         q.data_ptr(), self.n_q_heads, *self._pools, _stream(stream))
+        _check("paged_decode_step", st)
+        return self.out
 
 
 def paged_decode_attention_noalloc(q, k_pool, v_pool, block_tables, ctx_lens, softmax_scale,
@@ -414,7 +538,7 @@ def paged_decode_attention_noalloc(q, k_pool, v_pool, block_tables, ctx_lens, so
     scratch would not fit raises (PKV_ERR_WORKSPACE).  Calls share the one
     array: do not let two of them overlap on the GPU."""
     lib = load_library()
-    dev = q.device
+    dev = _device_of(q, "q")
     _need(q, "q", torch.bfloat16, 3, dev)
     int8 = k_pool.dtype == torch.int8
     _need(k_pool, "k_pool", torch.int8 if int8 else torch.bfloat16, 4, dev)
@@ -431,7 +555,7 @@ def paged_decode_attention_noalloc(q, k_pool, v_pool, block_tables, ctx_lens, so
     n_seqs, n_q_heads, _ = q.shape
     st = lib.paged_decode_attention_noalloc(_ptr(q), n_q_heads, _ptr(k_pool), _ptr(v_pool), _ptr(k_scales),
                                             _ptr(v_scales), PKV_KV_INT8 if int8 else PKV_KV_BF16,
-                                            pool_dims(k_pool), _ptr(block_tables), block_tables.shape[1],
+                                            _dims(k_pool), _ptr(block_tables), block_tables.shape[1],
                                             _ptr(ctx_lens), n_seqs, float(softmax_scale), int(split_tokens),
                                             int(max_total_ctx_tokens), _ptr(out), _ptr(lse_out),
                                             _ptr(dev_status), _stream(stream))
@@ -444,7 +568,7 @@ def paged_prefill_attention(q, k_pool, v_pool, block_tables, prefix_lens, softma
     """Chunked paged prefill: q [n_seqs, chunk, Hq, D] bf16 (the chunk's K/V
     already written at prefix_lens[s] ..).  Returns out, same shape as q."""
     lib = load_library()
-    dev = q.device
+    dev = _device_of(q, "q")
     _need(q, "q", torch.bfloat16, 4, dev)
     _need(k_pool, "k_pool", torch.bfloat16, 4, dev)
     _need(v_pool, "v_pool", torch.bfloat16, 4, dev)
@@ -463,7 +587,7 @@ def paged_prefill_attention(q, k_pool, v_pool, block_tables, prefix_lens, softma
     _check_batch(n_seqs, block_tables, prefix_lens, "prefix_lens")
     _shape(out, "out", q.shape)
     _shape(lse_out, "lse_out", q.shape[:3])
-    st = lib.paged_prefill_attention(_ptr(q), n_q_heads, _ptr(k_pool), _ptr(v_pool), pool_dims(k_pool),
+    st = lib.paged_prefill_attention(_ptr(q), n_q_heads, _ptr(k_pool), _ptr(v_pool), _dims(k_pool),
                                      _ptr(block_tables), block_tables.shape[1], _ptr(prefix_lens), n_seqs,
                                      chunk, float(softmax_scale), _ptr(out), _ptr(lse_out), _ptr(dev_status),
                                      _stream(stream))
@@ -607,7 +731,7 @@ def paged_kv_stage_blocks(pairs, host_k, host_v, pool_k, pool_v, dev_status=None
     bf16) into scratch-pool slots (device [n_slots + 1, bs, Hkv, D]):
     pairs int32 [n, 2] (host block, slot) on the device."""
     lib = load_library()
-    dev = pool_k.device
+    dev = _device_of(pool_k, "pool_k")
     _need(pairs, "pairs", torch.int32, 2, dev)
     for t, n in ((host_k, "host_k"), (host_v, "host_v")):
         if t.device.type != "cpu" or t.dtype != torch.bfloat16 or t.dim() != 4 or not t.is_contiguous():
@@ -622,7 +746,7 @@ def paged_kv_stage_blocks(pairs, host_k, host_v, pool_k, pool_v, dev_status=None
         raise ValueError("host_k / host_v blocks must match the scratch pool's [bs, Hkv, D]")
     st = lib.paged_kv_stage_blocks(_ptr(pairs), pairs.shape[0], ctypes.c_void_p(host_k.data_ptr()),
                                    ctypes.c_void_p(host_v.data_ptr()), host_k.shape[0], _ptr(pool_k), _ptr(pool_v),
-                                   pool_dims(pool_k), _ptr(dev_status), _stream(stream))
+                                   _dims(pool_k), _ptr(dev_status), _stream(stream))
     _check("paged_kv_stage_blocks", st)
 
 
@@ -642,7 +766,7 @@ def paged_decode_streamed(q, host_k, host_v, pool_k, pool_v, scratch_pool, host_
     tile of at most n_slots blocks at a time.  host_tables / ctx_lens: int32 CPU
     tensors.  Returns out (bf16 [n_seqs, Hq, D])."""
     lib = load_library()
-    dev = q.device
+    dev = _device_of(q, "q")
     _need(q, "q", torch.bfloat16, 3, dev)
     _need(pool_k, "pool_k", torch.bfloat16, 4, dev)
     _need(pool_v, "pool_v", torch.bfloat16, 4, dev)
@@ -673,7 +797,7 @@ def paged_decode_streamed(q, host_k, host_v, pool_k, pool_v, scratch_pool, host_
                                                          pool_k.shape[1]), dtype=torch.uint8, device=dev)
     st = lib.paged_decode_streamed(
         _ptr(q), n_q_heads, ctypes.c_void_p(host_k.data_ptr()), ctypes.c_void_p(host_v.data_ptr()),
-        host_k.shape[0], _ptr(pool_k), _ptr(pool_v), pool_dims(pool_k), scratch_pool._h,
+        host_k.shape[0], _ptr(pool_k), _ptr(pool_v), _dims(pool_k), scratch_pool._h,
         ctypes.c_void_p(host_tables.data_ptr()), host_tables.shape[1], ctypes.c_void_p(ctx_lens.data_ptr()), n_seqs,
         float(softmax_scale), _ptr(out), _ptr(lse_out), _ptr(workspace), workspace.numel(), _ptr(dev_status),
         _stream(stream))

@@ -93,17 +93,120 @@ void record_cuda_error(int e) { g_last_cuda_error = e; }
 
 unsigned long long pipeline_wait_ns() { return g_pipeline_wait_ns.load(); }
 
+namespace {
+
+// A tensor map depends only on its arguments, so the maps of recent calls are
+// kept and a call whose arguments match one reuses it (a model's pools give
+// the same few maps at every step); the key is zero-filled so that whole keys
+// compare byte for byte.
+struct MapKey {
+    const void *base;
+    uint64_t dims[5];
+    uint64_t strides[4];
+    uint32_t box[5];
+    int32_t dtype, rank, swizzle, pad;
+};
+struct MapEntry {
+    MapKey key;
+    CUtensorMap map;
+    bool used;
+};
+constexpr int kMapCacheEntries = 32;
+MapEntry g_maps[kMapCacheEntries];
+int g_map_next = 0;
+std::mutex g_map_mu;
+
+// Per kernel and device: the largest dynamic shared memory size set so far (the
+// attribute only grows, so every earlier size stays launchable) and the
+// occupancy of the (threads, smem) combinations seen.
+struct KernelEntry {
+    const void *kern;
+    int device, threads;
+    size_t smem, smem_set;
+    int occupancy;
+};
+constexpr int kKernelCacheEntries = 64;
+KernelEntry g_kernels[kKernelCacheEntries];
+int g_kernels_used = 0;
+std::mutex g_kernel_mu;
+
+}  // namespace
+
 CUresult encode_tensor_map(CUtensorMap *map, CUtensorMapDataType dtype, uint32_t rank, void *base,
                            const uint64_t *dims, const uint64_t *strides_bytes, const uint32_t *box,
                            CUtensorMapSwizzle swizzle)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return CUDA_ERROR_NOT_FOUND;
+    if (rank < 1 || rank > 5) return CUDA_ERROR_INVALID_VALUE;
+    MapKey key;
+    memset(&key, 0, sizeof key);
+    key.base = base;
+    for (uint32_t i = 0; i < rank; ++i) {
+        key.dims[i] = dims[i];
+        key.box[i] = box[i];
+        if (i + 1 < rank) key.strides[i] = strides_bytes[i];
+    }
+    key.dtype = (int32_t)dtype;
+    key.rank = (int32_t)rank;
+    key.swizzle = (int32_t)swizzle;
+    {
+        std::lock_guard<std::mutex> lock(g_map_mu);
+        for (const MapEntry &e : g_maps)
+            if (e.used && memcmp(&e.key, &key, sizeof key) == 0) {
+                *map = e.map;
+                return CUDA_SUCCESS;
+            }
+    }
     cuuint32_t elem_strides[5] = {1, 1, 1, 1, 1};
-    return fn(map, dtype, rank, base, reinterpret_cast<const cuuint64_t *>(dims),
-              reinterpret_cast<const cuuint64_t *>(strides_bytes), reinterpret_cast<const cuuint32_t *>(box),
-              elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    const CUresult r = fn(map, dtype, rank, base, reinterpret_cast<const cuuint64_t *>(dims),
+                          reinterpret_cast<const cuuint64_t *>(strides_bytes), reinterpret_cast<const cuuint32_t *>(box),
+                          elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r == CUDA_SUCCESS) {
+        std::lock_guard<std::mutex> lock(g_map_mu);
+        MapEntry &e = g_maps[g_map_next];
+        g_map_next = (g_map_next + 1) % kMapCacheEntries;
+        e.key = key;
+        e.map = *map;
+        e.used = true;
+    }
+    return r;
+}
+
+cudaError_t prepare_kernel(const void *kern, int threads, size_t smem, int *occupancy)
+{
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    std::lock_guard<std::mutex> lock(g_kernel_mu);
+    size_t smem_set = 0;
+    for (int i = 0; i < g_kernels_used; ++i) {
+        const KernelEntry &e = g_kernels[i];
+        if (e.kern != kern || e.device != dev) continue;
+        if (e.smem_set > smem_set) smem_set = e.smem_set;
+        if (e.threads == threads && e.smem == smem && (occupancy == nullptr || e.occupancy >= 0)) {
+            if (occupancy) *occupancy = e.occupancy;
+            return cudaSuccess;
+        }
+    }
+    if (smem > smem_set) {
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (err != cudaSuccess) return err;
+        smem_set = smem;
+    }
+    int occ = -1;
+    if (occupancy) {
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
+        if (err != cudaSuccess) return err;
+        *occupancy = occ;
+    }
+    // remember the combination, and the size now set, for every entry of this kernel and device
+    for (int i = 0; i < g_kernels_used; ++i)
+        if (g_kernels[i].kern == kern && g_kernels[i].device == dev) g_kernels[i].smem_set = smem_set;
+    if (g_kernels_used < kKernelCacheEntries)
+        g_kernels[g_kernels_used++] = KernelEntry{kern, dev, threads, smem, smem_set, occ};
+    return cudaSuccess;
 }
 
 // Prefill runs on the tcgen05 kernel (prefill_tc.cu).

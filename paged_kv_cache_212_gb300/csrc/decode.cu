@@ -1924,11 +1924,9 @@ cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream, 
     p.n_stages = stages;
 
     auto kern = TC ? decode_tc_kernel : decode_split_kernel<D, INT8>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
     const int threads = TC ? kTcThreads : 32 * (hpc + 1);
     int occ = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
+    cudaError_t e = prepare_kernel(reinterpret_cast<const void *>(kern), threads, smem, &occ);
     if (e != cudaSuccess) return e;
     if (occ < 1) return cudaErrorInvalidConfiguration;
     const int grid = num_sms * (occ < ctas_per_sm ? occ : ctas_per_sm);

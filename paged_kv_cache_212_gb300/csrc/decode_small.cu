@@ -269,12 +269,12 @@ cudaError_t launch_decode_small(const DecodeArgs &a, const WriteArgs *write, cud
     const unsigned grid = (unsigned)(a.n_seqs * a.dims.n_kv_heads);
     const WriteArgs w = write ? *write : WriteArgs{};
     const int cap = a.max_blocks * a.dims.block_size;      // tokens the buffers hold
-    // per call, as the other kernels: the attribute belongs to the current device
+    // the shared memory limit belongs to the current device: set per device
     const size_t smem = a.dims.head_dim == 128 ? small_smem_bytes<128>(cap) : small_smem_bytes<64>(cap);
     const cudaError_t attr_err =
         a.dims.head_dim == 128
-            ? cudaFuncSetAttribute(decode_small_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)
-            : cudaFuncSetAttribute(decode_small_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            ? prepare_kernel(reinterpret_cast<const void *>(decode_small_kernel<128>), kThreads, smem, nullptr)
+            : prepare_kernel(reinterpret_cast<const void *>(decode_small_kernel<64>), kThreads, smem, nullptr);
     if (attr_err != cudaSuccess) return attr_err;
     if (a.dims.head_dim == 128)
         decode_small_kernel<128><<<grid, kThreads, smem, stream>>>(a, w, write ? 1 : 0, cap);

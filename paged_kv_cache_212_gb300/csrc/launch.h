@@ -111,9 +111,16 @@ unsigned long long pipeline_wait_ns();
 
 // Driver entry point for tensor-map encoding (resolved once through cudart,
 // so the library does not link libcuda directly).  Returns CUDA_SUCCESS or
-// the driver error.
+// the driver error.  Maps of recent calls with the same arguments are reused.
 CUresult encode_tensor_map(CUtensorMap *map, CUtensorMapDataType dtype, uint32_t rank,
                            void *base, const uint64_t *dims, const uint64_t *strides_bytes,
                            const uint32_t *box, CUtensorMapSwizzle swizzle);
+
+// Before a launch of `kern` with `smem` bytes of dynamic shared memory on the
+// current device: raises the kernel's dynamic shared memory limit when smem
+// exceeds what was set before (it never lowers it) and, if occupancy is not
+// null, returns the resident CTAs per SM at (threads, smem).  Both are done
+// once per kernel, device and combination.
+cudaError_t prepare_kernel(const void *kern, int threads, size_t smem, int *occupancy);
 
 }  // namespace pkv

@@ -630,11 +630,11 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream)
     if (!regs_ok) return cudaErrorInvalidConfiguration;
     cudaError_t e;
     if (d.head_dim == 128) {
-        e = cudaFuncSetAttribute(prefill_tc_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        e = prepare_kernel(reinterpret_cast<const void *>(prefill_tc_kernel<128>), 384, smem, nullptr);
         if (e != cudaSuccess) return e;
         prefill_tc_kernel<128><<<grid, 384, smem, stream>>>(qmap, kmap, vmap, p);
     } else {
-        e = cudaFuncSetAttribute(prefill_tc_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        e = prepare_kernel(reinterpret_cast<const void *>(prefill_tc_kernel<64>), 384, smem, nullptr);
         if (e != cudaSuccess) return e;
         prefill_tc_kernel<64><<<grid, 384, smem, stream>>>(qmap, kmap, vmap, p);
     }

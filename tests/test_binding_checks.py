@@ -49,6 +49,12 @@ def test_int8_scale_shape_mismatch_raises(name):
         P._check_decode(**t)
 
 
+def test_decode_plan_refuses_host_tensors():
+    t = _decode_tensors()
+    with pytest.raises(ValueError):
+        P.DecodePlan(t["k_pool"], t["v_pool"], t["block_tables"], t["ctx_lens"], 0.125, 8)
+
+
 def test_head_dim_mismatch_raises():
     t = _decode_tensors()
     t["q"] = torch.zeros((3, 8, 128), dtype=torch.bfloat16)

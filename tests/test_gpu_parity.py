@@ -453,6 +453,61 @@ def test_fused_decode_step(P, name, decode_impl):
         assert mx <= BF16_MAX and mean <= BF16_MEAN, (mx, mean)
 
 
+@pytest.mark.parametrize("name", ["tiny", "int8_small", "ragged_d64"])
+def test_decode_plan_matches_calls(P, name, decode_impl):
+    """DecodePlan.run (the fixed arguments checked once): the step (write +
+    decode) bit for bit the result of paged_decode_step, the decode alone over
+    the written pools the same bits again, and both within tolerance of the
+    oracle."""
+    w = workload(name)
+    kp, vp, ks, vs = pools(name, after_step=False)
+    tables, start, ctx = i32(w.tables), i32(w.start_pos), i32(w.ctx_lens)
+    q, kn, vn = w.q.cuda(), w.k_new.cuda(), w.v_new.cuda()
+    int8 = w.kv_format == "int8"
+    gk, gv = dev(kp), dev(vp)
+    gks, gvs = (dev(ks), dev(vs)) if int8 else (None, None)
+    st = status_tensor()
+    lse = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
+    plan = P.DecodePlan(gk, gv, tables, ctx, w.softmax_scale, q.shape[1], k_scales=gks, v_scales=gvs, lse_out=lse,
+                        dev_status=st)
+    out_step = plan.run(q, kn, vn, start).clone()
+    lse_step = lse.clone()
+    out_decode = plan.run(q).clone()
+    gk2, gv2 = dev(kp), dev(vp)
+    gks2, gvs2 = (dev(ks), dev(vs)) if int8 else (None, None)
+    lse2 = torch.empty_like(lse)
+    out2 = P.paged_decode_step(kn, vn, start, q, gk2, gv2, tables, ctx, w.softmax_scale, k_scales=gks2,
+                               v_scales=gvs2, lse_out=lse2)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    rk, rv, rks, rvs = pools(name, after_step=True)
+    assert np.array_equal(host(gk), rk) and np.array_equal(host(gv), rv)
+    assert torch.equal(out_step.view(torch.int16), out2.view(torch.int16)) and torch.equal(lse_step, lse2)
+    assert torch.equal(out_decode.view(torch.int16), out2.view(torch.int16)) and torch.equal(lse, lse2)
+    ref, _ = oracle_decode(w, rk, rv, rks, rvs)
+    mx, mean = attention_errors(out_step, ref)
+    if int8:
+        assert mx <= INT8_MAX, mx
+    else:
+        assert mx <= BF16_MAX and mean <= BF16_MEAN, (mx, mean)
+
+
+def test_decode_plan_refuses_mismatched_calls(P):
+    w = workload("tiny")
+    kp, vp, _, _ = pools("tiny", after_step=False)
+    tables, ctx = i32(w.tables), i32(w.ctx_lens)
+    plan = P.DecodePlan(dev(kp), dev(vp), tables, ctx, w.softmax_scale, w.q.shape[1])
+    q = w.q.cuda()
+    with pytest.raises(ValueError):
+        plan.run(q[:-1].contiguous())                       # fewer sequences than planned
+    with pytest.raises(ValueError):
+        plan.run(q, v_new=w.v_new.cuda())                   # v_new without k_new
+    with pytest.raises(ValueError):
+        plan.run(q, w.k_new.cuda()[:, :, :1].contiguous(), w.v_new.cuda(), i32(w.start_pos))   # wrong kv heads
+    with pytest.raises(ValueError):
+        plan.run(q.float())                                 # wrong dtype
+
+
 def test_int8_write_near_ties_bit_exact(P):
     """Rows whose codes sit at or next to a half-integer quotient -- where a
     reciprocal multiply and the IEEE division by the stored scale can round
