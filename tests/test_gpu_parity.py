@@ -368,27 +368,20 @@ def test_prefill_parity_all_rows(P, name):
     assert np.abs(lse.cpu().numpy() - ref_lse).max() <= LSE_TOL
 
 
-def test_prefill_full_size_sampled_rows(P):
-    """The chunked prefill (8 sequences x 512-token chunks) at full size: the
-    GPU computes every row; the oracle checks a sample of chunk rows (first,
-    last, block boundaries, random) of every sequence and head."""
+def test_prefill_full_size_all_rows(P):
+    """The chunked prefill (8 sequences x 512-token chunks, prefixes up to
+    5549 tokens) at full size, every row of every sequence and query head
+    against the float64 oracle (about a minute of CPU time on 16 cores)."""
     w = workload("chunked_prefill")
     kp, vp, _, _ = pools("chunked_prefill")
     out, lse, st = run_prefill(P, w, kp, vp)
     assert st == 0
-    rng = np.random.default_rng(0)
-    sel = np.zeros((w.n_seqs, w.n_new), bool)
-    for s in range(w.n_seqs):
-        rows = {0, 1, 15, 16, 17, 63, 64, 255, 256, w.n_new - 2, w.n_new - 1}
-        rows |= set(rng.integers(0, w.n_new, 6).tolist())
-        sel[s, sorted(r for r in rows if r < w.n_new)] = True
     code, ref, ref_lse = oracle.prefill(w.q, kp, vp, dims_of(w), w.tables, w.stored_lens, w.softmax_scale,
-                                        row_select=sel, n_threads=NTHREADS)
+                                        n_threads=NTHREADS)
     assert code == 0
-    g = out.cpu().to(torch.float64).numpy()[sel]
-    err = np.abs(g - ref[sel])
-    assert err.max() <= BF16_MAX and err.mean() <= BF16_MEAN, (err.max(), err.mean())
-    assert np.abs(lse.cpu().numpy()[sel] - ref_lse[sel]).max() <= LSE_TOL
+    mx, mean = attention_errors(out, ref)
+    assert mx <= BF16_MAX and mean <= BF16_MEAN, (mx, mean)
+    assert np.abs(lse.cpu().numpy() - ref_lse).max() <= LSE_TOL
     assert torch.isfinite(out).all()
 
 

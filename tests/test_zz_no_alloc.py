@@ -3,19 +3,20 @@ not allocate device memory (a plugin whose host owns all device memory, a
 runtime with a fixed memory budget).  Its split-KV scratch is the library's
 static device array instead of a caller workspace.
 
-Checked on the GPU against paged_decode_attention (caller workspace), on two
-calls in a row -- the second call finds the first call's leftovers in the
-shared array -- within the parity tolerances of the other decode tests.  This
-file is collected last so that a run stopping at the first failure has already
-run every other test; it also passes alone in a fresh process.
+Checked against the float64 CPU oracle and against paged_decode_attention
+(caller workspace) on the GPU, on two calls in a row -- the second call finds
+the first call's leftovers in the shared array -- within the parity tolerances
+of the other decode tests.  This file is collected last so that a run stopping
+at the first failure has already run every other test; it also passes alone in
+a fresh process.
 """
-import ctypes
-
 import numpy as np
 import pytest
 import torch
 
-from oracle_pools import oracle_pools_after_step
+import oracle
+from gpu_support import NTHREADS, attention_errors
+from oracle_pools import dims_of, oracle_pools_after_step
 from paged_kv_cache_212_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
@@ -81,6 +82,9 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(P, make, split, tol_
     ref_lse = torch.empty(q.shape[:2], dtype=torch.float32, device="cuda")
     ref = P.paged_decode_attention(q, gk, gv, tables, ctx, w.softmax_scale, k_scales=gks, v_scales=gvs,
                                    split_tokens=split, lse_out=ref_lse)
+    code, oref, olse = oracle.decode(w.q, kp, vp, dims_of(w), w.tables, w.ctx_lens, w.softmax_scale, ks, vs,
+                                     n_threads=NTHREADS)
+    assert code == oracle.OK
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     for call in range(2):
         out = torch.full_like(q, float("nan"))
@@ -89,11 +93,16 @@ def test_noalloc_matches_workspace_entry_point_on_two_calls(P, make, split, tol_
                                          v_scales=gvs, split_tokens=split, lse_out=lse, dev_status=status)
         torch.cuda.synchronize()
         assert int(status.item()) == 0, call
-        mx, mean = _errors(out, ref)
-        assert mx <= tol_max, (call, mx)
-        if tol_mean is not None:
-            assert mean <= tol_mean, (call, mean)
+        for against in (ref, oref):
+            mx, mean = _errors(out, against) if isinstance(against, torch.Tensor) else attention_errors(out, against)
+            assert mx <= tol_max, (call, mx)
+            if tol_mean is not None:
+                assert mean <= tol_mean, (call, mean)
         assert float((lse - ref_lse).abs().max()) <= 2e-3, call
+        g = lse.cpu().numpy().astype(np.float64)
+        fin = np.isfinite(olse)
+        assert np.array_equal(np.isneginf(g), np.isneginf(olse)), call
+        assert not fin.any() or np.abs(g[fin] - olse[fin]).max() <= 2e-3, call
 
 
 def test_noalloc_rejects_requests_larger_than_its_scratch(P):
