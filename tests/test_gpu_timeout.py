@@ -1,13 +1,14 @@
 """Failure detection without a GPU fault: a bounded pipeline wait that runs out.
 
-Every pipeline wait of the split-KV decode and of the tcgen05 prefill gives up
-after a limit the host sets (pkv_set_pipeline_wait_ns, 4 s by default).  With a
-1 ns limit the waits that are not already satisfied run out at once: the
-kernel reports PKV_DEV_TIMEOUT in dev_status, its CTAs wind down (the copies
-and tensor-core operations already issued finish before shared memory or TMEM
-is released) and the call returns.  The next call on the same stream, with the
-default limit back, matches the float64 oracle.  (libmir-metal paged/mod.rs:
-the store's calls return errors instead of aborting.)
+Every pipeline wait of the split-KV decode (mma.sync and tensor-core kernels)
+and of the tcgen05 prefill gives up after a limit the host sets
+(pkv_set_pipeline_wait_ns, 4 s by default).  With a 1 ns limit the waits that
+are not already satisfied run out at once: the kernel reports PKV_DEV_TIMEOUT
+in dev_status, its CTAs wind down (the copies and tensor-core operations
+already issued finish before shared memory or TMEM is released) and the call
+returns.  The next call on the same stream, with the default limit back,
+matches the float64 oracle.  (libmir-metal paged/mod.rs: the store's calls
+return errors instead of aborting.)
 """
 import numpy as np
 import pytest
@@ -48,9 +49,11 @@ class short_waits:
         self.lib.pkv_set_pipeline_wait_ns(0)
 
 
-@pytest.mark.parametrize("kv_format", ["bf16", "int8"])
-def test_decode_wait_runs_out_then_recovers(P, kv_format, monkeypatch):
-    monkeypatch.setenv("PKV_DECODE_IMPL", "split")          # the pipelined kernels
+# split: the mma.sync split-KV kernels; tc: the tensor-core kernel (int8 pages),
+# whose warpgroups leave their loop as one after any wait that gives up
+@pytest.mark.parametrize("kv_format,impl", [("bf16", "split"), ("int8", "split"), ("int8", "tc")])
+def test_decode_wait_runs_out_then_recovers(P, kv_format, impl, monkeypatch):
+    monkeypatch.setenv("PKV_DECODE_IMPL", impl)             # the pipelined kernels
     w = W.decode_workload("timeout", 31, [300, 700, 1500, 64, 2000, 5], 32, 8, 128, 16, n_new=1,
                           kv_format=kv_format)
     kp, vp, ks, vs = oracle_pools_after_step(w, poison=True)
