@@ -218,7 +218,11 @@ size_t pkv_decode_workspace_bytes(int32_t n_seqs, int32_t n_q_heads, int32_t hea
  * kv head) pair per SM whose table spans at most 256 tokens (head_dim 128) or
  * 512 (head_dim 64) is attended whole by one CTA per pair in a single launch
  * (same results within the tolerances; PKV_DECODE_IMPL=split in the
- * environment keeps the split-KV path).
+ * environment keeps the split-KV path).  PKV_DECODE_IMPL=tc runs int8 pages of
+ * head_dim 128 with at most 8 query heads per kv head (n_kv_heads a multiple
+ * of 4) on the tcgen05 tensor-core kernel instead of the mma.sync one (same
+ * results within the int8 tolerance; slower on GB300 today).  The variable is
+ * read at every call.
  */
 int paged_decode_attention(const pkv_bf16 *q, int32_t n_q_heads, const void *k_pool,
                            const void *v_pool, const float *k_scales, const float *v_scales,
