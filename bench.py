@@ -56,10 +56,10 @@ FALLBACK_HBM_GBS = 6800.0
 # under profiles/, valid while
 # the kernel's sources hash to source_sha.
 NCU_TRAFFIC = {
-    "decode": {"sources": ("decode.cu", "common.cuh", "launch.h", "tcgen05.cuh"), "source_sha": "f3968406105cbb8c",
-               "bytes_per_launch": {1: 544754432 + 4414976, 2: 310416896 + 3837696, 4: 1317703680 + 32872960}},
-    "prefill": {"sources": ("prefill_tc.cu", "common.cuh", "launch.h", "tcgen05.cuh"), "source_sha": "e91a9d8a4a03d93e",
-                "bytes_per_launch": {3: 199506688 + 17285632}},
+    "decode": {"sources": ("decode.cu", "common.cuh", "launch.h", "tcgen05.cuh"), "source_sha": "2470dfdc132bc43a",
+               "bytes_per_launch": {1: 544751360 + 4061696, 2: 310420224 + 3874048, 4: 1317381120 + 32879872}},
+    "prefill": {"sources": ("prefill_tc.cu", "common.cuh", "launch.h", "tcgen05.cuh"), "source_sha": "ae6c11aa76dcda31",
+                "bytes_per_launch": {3: 196737280 + 16645632}},
 }
 
 
@@ -1202,10 +1202,18 @@ def decode_e2e(P, w, kp, vp, ks, vs, split, ws, status, q, K, world, device, str
     h2d = sum(x.numel() * x.element_size() for x in (h_k, h_v, h_q, h_tab, h_start, h_ctx))
     d2h = h_out.numel() * h_out.element_size()
 
+    # one DecodePlan per device arena (its tables, lengths and output bound once);
+    # each step runs it on that arena's queries, new rows and positions
+    plans = {}
+
     def call(views, out):
         dk, dv, dq, dtab, dstart, dctx = views
-        P.paged_decode_step(dk, dv, dstart, dq, kp, vp, dtab, dctx, w.softmax_scale, k_scales=ks,
-                            v_scales=vs, split_tokens=split, out=out, workspace=ws, dev_status=status)
+        plan = plans.get(out.data_ptr())
+        if plan is None:
+            plan = plans[out.data_ptr()] = P.DecodePlan(kp, vp, dtab, dctx, w.softmax_scale, w.n_q_heads,
+                                                        k_scales=ks, v_scales=vs, split_tokens=split, out=out,
+                                                        workspace=ws, dev_status=status)
+        plan.run(dq, dk, dv, dstart)
 
     e2e_run, copy_stream, out_stream = pipelined_e2e((h_k, h_v, h_q, h_tab, h_start, h_ctx), q, call, device,
                                                      stream)
@@ -1225,7 +1233,7 @@ def decode_e2e(P, w, kp, vp, ks, vs, split, ws, status, q, K, world, device, str
     decode_b, write_b = algorithmic_bytes(w)
     return {"value": round(weak_scaling_value(decode_b + write_b, world, e2e_ms), 2), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 5),
-            "steps": e2e_steps}
+            "steps": e2e_steps, "api": "DecodePlan.run (write + decode per step) on the copied inputs"}
 
 
 def bench_writes(P, device, peak):
