@@ -1,7 +1,8 @@
 """GPU test of a multi-layer decode step captured as one CUDA graph: every
-layer's write + decode (paged_decode_step, three launches chained by
-programmatic dependent launch) replays from the graph with the same bits as
-the eager calls, and layer outputs match the oracle's write + decode."""
+layer's write + decode (paged_decode_step, or DecodePlan.run with one plan per
+layer; three launches chained by programmatic dependent launch) replays from
+the graph with the same bits as the eager calls, and layer outputs match the
+oracle's write + decode."""
 import numpy as np
 import pytest
 import torch
@@ -25,8 +26,9 @@ def P():
     return P
 
 
+@pytest.mark.parametrize("use_plan", [False, True])
 @pytest.mark.parametrize("int8", [False, True])
-def test_layer_step_graph_replays_the_eager_bits(P, int8, decode_impl):
+def test_layer_step_graph_replays_the_eager_bits(P, int8, use_plan, decode_impl):
     n_layers, n, Hkv, G, D, bs, n_blocks, max_blocks = 4, 5, 4, 4, 128, 16, 60, 10   # int8 decode: Hkv % 4 == 0
     Hq = Hkv * G
     gen = torch.Generator().manual_seed(303 + int8)
@@ -67,7 +69,14 @@ def test_layer_step_graph_replays_the_eager_bits(P, int8, decode_impl):
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     scale = 1.0 / D ** 0.5
 
+    plans = [P.DecodePlan(x["kp"], x["vp"], t_tab, t_ctx, scale, Hq, k_scales=x["ks"], v_scales=x["vs"],
+                          out=x["out"], workspace=ws, dev_status=st) for x in layers] if use_plan else None
+
     def step():
+        if use_plan:
+            for x, plan in zip(layers, plans):
+                plan.run(x["q"], x["k_new"], x["v_new"], t_start)
+            return
         for x in layers:
             P.paged_decode_step(x["k_new"], x["v_new"], t_start, x["q"], x["kp"], x["vp"], t_tab, t_ctx, scale,
                                 k_scales=x["ks"], v_scales=x["vs"], out=x["out"], workspace=ws, dev_status=st)
