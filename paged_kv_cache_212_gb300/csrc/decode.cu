@@ -37,6 +37,8 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 #include "launch.h"
 #include "tcgen05.cuh"
@@ -441,66 +443,62 @@ __global__ void __launch_bounds__(kPlanThreads, 4) decode_plan_kernel(const int3
 // ---------------------------------------------------------------------------
 // 3. merge of the pieces of a sequence
 // ---------------------------------------------------------------------------
-// One warp per (sequence, query head) of every sequence cut into two or more
-// pieces: o = sum_k 2^(m_k - M) acc_k / sum_k 2^(m_k - M) l_k with M = max_k
-// m_k (the finalize step of the tiled attention), lse = ln 2 (M + log2 L).
-// First the lanes read the pieces' (m, l) side by side (one load each for up
-// to 32 pieces) and reduce M; then every lane streams its D / 32 elements of
-// kBatch pieces' partial rows at a time, all loads of a batch in flight
-// together, each weighted by its piece's factor broadcast from the lane that
-// read it.  Partials are read with ld.global.cg (L2): other SMs wrote them.
-// Launched after the split kernel as a programmatic dependent; it reads the
-// plan's piece counts before waiting for the split kernel's partials.
+// Merge of the pieces of a sequence, per (sequence, query head):
+// o = sum_k 2^(m_k - M) acc_k / sum_k 2^(m_k - M) l_k with M = max_k m_k (the
+// finalize step of the tiled attention), lse = ln 2 (M + log2 L).  A warp
+// merges one (sequence, query head) pair at a time, the pairs of the grid
+// taken in a grid-stride loop (the grid is a few CTAs per SM, so no wave of
+// short-lived CTAs waits behind another).  Per pair, the pieces go kRound at a
+// time: lane i < kRound reads piece k0 + i's (m, l) while every lane reads its
+// D / 32 elements of the round's partial rows, all in flight together (a pair
+// of up to kRound pieces costs one memory round trip); the round's maximum
+// rescales the running sums (an online merge) and each row is weighted by its
+// piece's factor broadcast from the lane that read it.  Partials are read with
+// ld.global.cg (L2): other SMs wrote them.  Launched after the split kernel as
+// a programmatic dependent: the plan's results are complete when it starts
+// (the split kernel releases it only after its own wait for the plan); only
+// the partials need the wait for the split kernel.
+constexpr int kMergeCtasPerSm = 6;
+
 template <int D>
-__global__ void __launch_bounds__(128) decode_merge_kernel(DecodeWorkspace ws, int32_t n_seqs,
-                                                              int32_t n_q_heads, __nv_bfloat16 *out, float *lse_out)
+__global__ void __launch_bounds__(128, kMergeCtasPerSm) decode_merge_kernel(DecodeWorkspace ws, int32_t n_seqs,
+                                                                           int32_t n_q_heads, __nv_bfloat16 *out,
+                                                                           float *lse_out)
 {
     constexpr int EPL = D / 32;                      // output elements per lane
-    constexpr int kBatch = 8;                        // pieces in flight per lane
+    constexpr int kRound = 8;                        // pieces per round
     grid_dependents_launch();   // the next step's plan may start; it waits for this grid
     const int lane = threadIdx.x & 31;
-    const int64_t idx = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-    const bool mine = idx < (int64_t)n_seqs * n_q_heads;
-    const int32_t s = mine ? (int32_t)(idx / n_q_heads) : 0, h = mine ? (int32_t)(idx % n_q_heads) : 0;
-    // The plan's results (pieces per sequence, overflow flag) are complete:
-    // the split kernel lets this grid start only after its own wait for the
-    // plan.  Only the partials need the wait for the split kernel.
-    const int2 sg = mine ? ws.seg[s] : make_int2(0, 0);
-    const uint32_t overflow = mine ? ws.header[kHdrOverflow] : 1u;
+    const int64_t n_pairs = (int64_t)n_seqs * n_q_heads;
+    const int64_t n_warps = (int64_t)gridDim.x * (blockDim.x >> 5);
+    const int64_t idx0 = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    // the plan's results are read before the wait: the first pair's pieces
+    // (with one pair per warp, the only ones) and the overflow flag
+    const uint32_t overflow = ws.header[kHdrOverflow];
+    const int2 sg0 = idx0 < n_pairs ? ws.seg[idx0 / n_q_heads] : make_int2(0, 0);
     grid_dependency_wait();
-    if (!mine || sg.y < 2 || overflow != 0) return;
-    const int32_t n = sg.y;
-    const int64_t row0 = (int64_t)sg.x * n_q_heads + h;       // piece k's row: row0 + k * n_q_heads
-    // (m, l) of pieces lane, lane + 32, ...: the maximum over all pieces
-    float2 ml_own = make_float2(-INFINITY, 0.f);
-    float M = -INFINITY;
-    for (int32_t k = lane; k < n; k += 32) {
-        const float2 ml = __ldcg(&ws.part_ml[row0 + (int64_t)k * n_q_heads]);
-        if (k < 32) ml_own = ml;
-        M = fmaxf(M, ml.x);
-    }
+    if (overflow != 0) return;
+    for (int64_t idx = idx0; idx < n_pairs; idx += n_warps) {
+        const int32_t s = (int32_t)(idx / n_q_heads), h = (int32_t)(idx % n_q_heads);
+        const int2 sg = idx == idx0 ? sg0 : ws.seg[s];
+        if (sg.y < 2) continue;
+        const int32_t n = sg.y;
+        const int64_t row0 = (int64_t)sg.x * n_q_heads + h;   // piece k's row: row0 + k * n_q_heads
+        const int64_t stride = (int64_t)n_q_heads * D;         // floats from one piece's row to the next
+        const float *base = ws.part_acc + row0 * D + lane * EPL;
+        float M = -INFINITY, Lsum = 0.f;                       // Lsum: lanes < kRound, scaled to 2^-M
+        float o[EPL];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    float o[EPL];
+        for (int e = 0; e < EPL; ++e) o[e] = 0.f;
+        for (int32_t k0 = 0; k0 < n; k0 += kRound) {
+            const int32_t cnt = min(kRound, n - k0);
+            const float2 ml = lane < cnt ? __ldcg(&ws.part_ml[row0 + (int64_t)(k0 + lane) * n_q_heads])
+                                         : make_float2(-INFINITY, 0.f);
+            float a[kRound][EPL];
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) o[e] = 0.f;
-    float Lsum = 0.f;
-    for (int32_t k0 = 0; k0 < n; k0 += 32) {
-        // this lane's piece k0 + lane: its weight and its share of the sum
-        const float2 ml = k0 == 0 ? ml_own
-                                  : (k0 + lane < n ? __ldcg(&ws.part_ml[row0 + (int64_t)(k0 + lane) * n_q_heads])
-                                                   : make_float2(-INFINITY, 0.f));
-        const float wk = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
-        Lsum += wk * ml.y;
-        const int32_t cnt = min(32, n - k0);
-        const float *base = ws.part_acc + (row0 + (int64_t)k0 * n_q_heads) * D + lane * EPL;
-        const int32_t stride = n_q_heads * D;                  // floats from one piece's row to the next
-        for (int32_t i0 = 0; i0 < cnt; i0 += kBatch) {
-            float a[kBatch][EPL];
-#pragma unroll
-            for (int i = 0; i < kBatch; ++i) {
-                if (i0 + i < cnt) {
-                    const float *src = base + (i0 + i) * stride;
+            for (int i = 0; i < kRound; ++i) {
+                if (i < cnt) {
+                    const float *src = base + (int64_t)(k0 + i) * stride;
                     if constexpr (EPL == 4) {
                         const float4 x = __ldcg(reinterpret_cast<const float4 *>(src));
                         a[i][0] = x.x;
@@ -514,26 +512,43 @@ __global__ void __launch_bounds__(128) decode_merge_kernel(DecodeWorkspace ws, i
                     }
                 }
             }
+            float mr = ml.x;
 #pragma unroll
-            for (int i = 0; i < kBatch; ++i) {
-                const float w = __shfl_sync(0xffffffffu, wk, (i0 + i) & 31);
-                if (i0 + i < cnt) {
+            for (int off = kRound / 2; off > 0; off >>= 1) mr = fmaxf(mr, __shfl_xor_sync(0xffffffffu, mr, off));
+            mr = __shfl_sync(0xffffffffu, mr, 0);        // lanes >= kRound held -inf
+            const float Mn = fmaxf(M, mr);
+            if (Mn != -INFINITY && Mn != M) {             // the maximum moved: rescale what was summed
+                const float alpha = exp2f(M - Mn);        // M = -inf gives 0 (nothing summed yet)
+                Lsum *= alpha;
+#pragma unroll
+                for (int e = 0; e < EPL; ++e) o[e] *= alpha;
+                M = Mn;
+            }
+            const float wk = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
+            Lsum += wk * ml.y;
+#pragma unroll
+            for (int i = 0; i < kRound; ++i) {
+                const float w = __shfl_sync(0xffffffffu, wk, i);
+                if (i < cnt) {
 #pragma unroll
                     for (int e = 0; e < EPL; ++e) o[e] = fmaf(w, a[i][e], o[e]);
                 }
             }
         }
-    }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, off);
-    const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
-    __nv_bfloat16 *dst = out + ((int64_t)s * n_q_heads + h) * D + lane * EPL;
-    if constexpr (EPL == 4)
-        *reinterpret_cast<uint2 *>(dst) = make_uint2(pack_bf16x2(o[0] * inv, o[1] * inv), pack_bf16x2(o[2] * inv, o[3] * inv));
-    else
-        *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(o[0] * inv, o[1] * inv);
-    if (lse_out && lane == 0)
-        lse_out[(int64_t)s * n_q_heads + h] = Lsum > 0.f ? (M + __log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
+        for (int off = kRound / 2; off > 0; off >>= 1) Lsum += __shfl_xor_sync(0xffffffffu, Lsum, off);
+        Lsum = __shfl_sync(0xffffffffu, Lsum, 0);
+        const float inv = Lsum > 0.f ? 1.f / Lsum : 0.f;
+        __nv_bfloat16 *dst = out + ((int64_t)s * n_q_heads + h) * D + lane * EPL;
+        if constexpr (EPL == 4)
+            *reinterpret_cast<uint2 *>(dst) =
+                make_uint2(pack_bf16x2(o[0] * inv, o[1] * inv), pack_bf16x2(o[2] * inv, o[3] * inv));
+        else
+            *reinterpret_cast<uint32_t *>(dst) = pack_bf16x2(o[0] * inv, o[1] * inv);
+        if (lse_out && lane == 0)
+            lse_out[(int64_t)s * n_q_heads + h] =
+                Lsum > 0.f ? (M + __log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
+    }
 }
 
 // TMA copies of one 16-token stage (K and V tiles of hpc kv heads, int8 scales)
@@ -1970,10 +1985,12 @@ cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream, 
     lc.numAttrs = 1;
     e = cudaLaunchKernelEx(&lc, kern, kmap, vmap, ksmap, vsmap, p);
     if (e != cudaSuccess) return e;
-    // merge of multi-piece sequences: one warp per (sequence, query head)
+    // merge of multi-piece sequences: a warp per (sequence, query head) pair at
+    // a time, at most kMergeCtasPerSm CTAs of four warps per SM
     const int64_t warps = (int64_t)a.n_seqs * a.n_q_heads;
+    const int64_t merge_ctas = std::min<int64_t>((warps + 3) / 4, (int64_t)num_sms * kMergeCtasPerSm);
     cudaLaunchConfig_t mc{};
-    mc.gridDim = dim3((unsigned)((warps + 3) / 4));
+    mc.gridDim = dim3((unsigned)std::max<int64_t>(merge_ctas, 1));
     mc.blockDim = dim3(128);   // small CTAs: resident beside the split kernel's before it ends
     mc.stream = stream;
     mc.attrs = pdl;
