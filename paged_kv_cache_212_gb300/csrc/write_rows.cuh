@@ -17,16 +17,26 @@ __device__ __forceinline__ int64_t pool_row_of(const int32_t *table_row, int32_t
                                                int32_t n_blocks, int32_t block_size, int64_t t,
                                                int32_t *dev_status)
 {
-    if (t < 0 || t / block_size >= max_blocks) {
+    if (t < 0 || t >= (int64_t)max_blocks * block_size) {
         report(dev_status, PKV_DEV_BAD_POSITION);
         return -1;
     }
-    const int32_t b = __ldg(table_row + t / block_size);
+    // 0 <= t < 2^32 (an int32 start position plus an int32 row index): 32-bit division
+    const uint32_t tt = (uint32_t)t, blk = tt / (uint32_t)block_size;
+    const int32_t b = __ldg(table_row + blk);
     if (b < 0 || b > n_blocks) {
         report(dev_status, PKV_DEV_BAD_BLOCK_ID);
         return -1;
     }
-    return (int64_t)b * block_size + t % block_size;
+    return (int64_t)b * block_size + (tt - blk * (uint32_t)block_size);
+}
+
+// x / d for a non-negative flat index x and a positive d, in 32 bits when the
+// whole index space is below 2^31 (narrow, the same for every thread), else
+// in 64.
+__device__ __forceinline__ int64_t index_div(int64_t x, int32_t d, bool narrow)
+{
+    return narrow ? (int64_t)((uint32_t)x / (uint32_t)d) : x / d;
 }
 
 // Native bf16 write: 16-byte vector i of the [n_seqs * n_new rows][Hkv * D]
@@ -43,10 +53,11 @@ __device__ __forceinline__ void write_bf16_vectors(const WriteArgs &a, int64_t f
     const uint4 *v_new = static_cast<const uint4 *>(a.v_new);
     uint4 *k_pool = static_cast<uint4 *>(a.k_pool);
     uint4 *v_pool = static_cast<uint4 *>(a.v_pool);
+    const bool narrow = n_vecs <= 0x7fffffffLL;
     for (int64_t i = first; i < n_vecs; i += stride) {
-        const int64_t r = i / row_vecs;
+        const int64_t r = index_div(i, row_vecs, narrow);
         const int32_t v = (int32_t)(i - r * row_vecs);
-        const int64_t s = r / a.n_new;
+        const int64_t s = index_div(r, a.n_new, narrow);
         const uint4 kx = __ldcs(k_new + i);
         const uint4 vx = __ldcs(v_new + i);
         const int64_t t = (int64_t)__ldg(a.start_pos + s) + (r - s * a.n_new);
@@ -78,9 +89,10 @@ __device__ __forceinline__ void write_int8_units(const WriteArgs &a, float *k_sc
     const int32_t hkv = a.dims.n_kv_heads;
     const int32_t quads = (hkv + 3) / 4;
     const int64_t n_units = (int64_t)a.n_seqs * a.n_new * 2 * quads;
+    const bool narrow = n_units <= 0x7fffffffLL;
     for (int64_t u = first; u < n_units; u += stride) {
-        const int32_t quad = (int32_t)(u % quads);
-        const int64_t rw = u / quads;
+        const int64_t rw = index_div(u, quads, narrow);
+        const int32_t quad = (int32_t)(u - rw * quads);
         const int which = (int)(rw & 1);
         const int64_t r = rw >> 1;                     // r = s * n_new + j
         const int32_t h = quad * 4 + (lane >> 3);
@@ -105,7 +117,7 @@ __device__ __forceinline__ void write_int8_units(const WriteArgs &a, float *k_sc
 #pragma unroll
             for (int e = 0; e < EPL; ++e) x[e] = 0.0f;
         }
-        const int64_t s = r / a.n_new;
+        const int64_t s = index_div(r, a.n_new, narrow);
         const int64_t t = (int64_t)__ldg(a.start_pos + s) + (r - s * a.n_new);
         const int64_t row = pool_row_of(a.tables + s * a.max_blocks, a.max_blocks, a.dims.n_blocks,
                                         a.dims.block_size, t,
