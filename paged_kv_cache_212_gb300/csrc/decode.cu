@@ -264,7 +264,9 @@ __device__ void plan_small(const int32_t *__restrict__ ctx_lens, int32_t n_seqs,
                 ws.seq_prefix[sq] = pre[j];
                 ws.seg[sq] = make_int2(ex2, np[j]);
                 // items whose first stage lies in this sequence start with it
-                for (int32_t i = (pre[j] + chunk - 1) / max(chunk, 1); n[j] > 0 && i * chunk < pre[j] + n[j]; ++i)
+                // (none when the work list overflowed: chunk is then 0)
+                for (int32_t i = (pre[j] + chunk - 1) / max(chunk, 1);
+                     chunk > 0 && n[j] > 0 && i * chunk < pre[j] + n[j]; ++i)
                     ws.items[i] = make_int2(sq, 0);
             }
             ex2 += np[j];

@@ -310,6 +310,25 @@ def test_decode_workspace_overflow_is_flagged(P):
     assert (out == 0).all()
 
 
+def test_decode_balanced_overflow_is_flagged(P, monkeypatch):
+    # automatic splitting with a workspace of exactly n_seqs partial slots (the
+    # size pkv_decode_workspace_bytes gives for 16-token splits of no tokens):
+    # no room for the balanced items, so the plan flags the overflow, writes no
+    # item and leaves o = 0
+    monkeypatch.setenv("PKV_DECODE_IMPL", "split")
+    w = workload("ragged_d64")
+    kp, vp, _, _ = pools("ragged_d64")
+    q = w.q.cuda()
+    ws = torch.empty(P.decode_workspace_bytes(w.n_seqs, w.n_q_heads, w.head_dim, 0, 16), dtype=torch.uint8,
+                     device="cuda")
+    st = status_tensor()
+    out = P.paged_decode_attention(q, dev(kp), dev(vp), i32(w.tables), i32(w.ctx_lens), w.softmax_scale,
+                                   workspace=ws, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & P.DEV_WORKSPACE_OVERFLOW
+    assert (out == 0).all()
+
+
 # ---------------------------------------------------------------------------
 # the decode step as the benchmark runs it: GPU write, then GPU decode
 # ---------------------------------------------------------------------------
