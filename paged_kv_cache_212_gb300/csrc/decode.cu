@@ -787,9 +787,11 @@ __device__ __forceinline__ void run_producer(const SmemLayout &L, const DecodePa
 // 2. split kernel
 // ---------------------------------------------------------------------------
 // Register budget (measured on GB300): bf16 pages compile for two resident
-// CTAs per SM (at most ~112 registers; fewer registers measured faster even at
-// one CTA per SM), int8 pages for one (the fp16 fragments of the in-register
-// code conversion need ~168 registers; the two-CTA budget spills).
+// 288-thread CTAs per SM (at most ~112 registers; fewer registers measured
+// faster even at one CTA per SM), int8 pages for one (the fp16 fragments of the
+// in-register code conversion need ~168 registers; the two-CTA budget spills).
+// int8 pages launch 160-thread CTAs (four kv heads), two of which fit an SM at
+// that register count.
 template <int D, bool INT8>
 __global__ void __launch_bounds__(288, INT8 ? 1 : 2) decode_split_kernel(const __grid_constant__ CUtensorMap k_map,
                                                               const __grid_constant__ CUtensorMap v_map,
@@ -1847,13 +1849,17 @@ cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream, 
     // Launch shape (measured on GB300): one CTA per SM serving up to 8 kv
     // heads; with groups of 8 or more query heads per kv head the consumer
     // warps carry twice the mma work per byte, and 4 kv heads per CTA with two
-    // CTAs per SM keep more loads in flight per unit of that work.
+    // CTAs per SM keep more loads in flight per unit of that work.  int8 pages
+    // take 4 kv heads per CTA and two CTAs per SM as well: the consumer warps'
+    // in-register code conversion holds ~166 registers, so eight of them fit
+    // an SM either way, and two CTAs give two producers and rings (64.6 against
+    // 66.1 us on the int8 batch-64 step).
     // (kv heads per CTA: the largest divisor of n_kv_heads up to 8, a multiple
     // of 4 for int8 pages, whose scale rows are copied 16 bytes at a time)
     int hpc = 0, ctas_per_sm = 1;
     for (int c = 8; c >= 1 && hpc == 0; --c)
         if (d.n_kv_heads % c == 0 && (!INT8 || c % 4 == 0)) hpc = c;
-    if (G >= 8 && d.n_kv_heads % 4 == 0) {
+    if ((G >= 8 || INT8) && d.n_kv_heads % 4 == 0) {
         hpc = 4;
         ctas_per_sm = 2;
     }
@@ -1927,8 +1933,9 @@ cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream, 
     const size_t fixed = 1024 + 2 * (size_t)p.q_slot_bytes + smem_tail_bytes();
     if (fixed + 2 * (size_t)p.stage_bytes > per_cta) return cudaErrorInvalidValue;
     int stages = (int)((per_cta - fixed) / p.stage_bytes);
-    // int8 pages: at most four stages (measured faster on GB300 than deeper rings)
-    const int stage_cap = INT8 ? 4 : kMaxStages;
+    // int8 pages: at most five stages per CTA (measured on GB300: 4, 5 and 6
+    // stages of 17 KiB at two CTAs per SM: 64.6, 64.3 and 65.4 us per step)
+    const int stage_cap = INT8 ? 5 : kMaxStages;
     stages = stages > stage_cap ? stage_cap : stages;
     size_t smem = fixed + (size_t)stages * p.stage_bytes;
     if (TC) {
