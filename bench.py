@@ -56,8 +56,8 @@ FALLBACK_HBM_GBS = 6800.0
 # under profiles/, valid while
 # the kernel's sources hash to source_sha.
 NCU_TRAFFIC = {
-    "decode": {"sources": ("decode.cu", "common.cuh", "launch.h", "tcgen05.cuh"), "source_sha": "2470dfdc132bc43a",
-               "bytes_per_launch": {1: 544751360 + 4061696, 2: 310420224 + 3874048, 4: 1317381120 + 32879872}},
+    "decode": {"sources": ("decode.cu", "common.cuh", "launch.h", "tcgen05.cuh"), "source_sha": "512a4382b82296aa",
+               "bytes_per_launch": {1: 544752384 + 3997696, 2: 310419200 + 3858176, 4: 1317187840 + 33266176}},
     "prefill": {"sources": ("prefill_tc.cu", "common.cuh", "launch.h", "tcgen05.cuh"), "source_sha": "ae6c11aa76dcda31",
                 "bytes_per_launch": {3: 196737280 + 16645632}},
 }
