@@ -11,10 +11,12 @@
 //      cut into equal contiguous ranges, about one per CTA, so every CTA gets
 //      the same amount of work; a range may cover the end of one sequence and
 //      the start of the next.  Each (sequence, item) piece owns one partial
-//      slot.  The plan also resets the work counter and the merge counters.
-//   2. decode_split_kernel (persistent, one or two CTAs per SM): a producer
-//      warp takes (item, kv-head group) units from the counter and streams the
-//      item's pages, 16 tokens per stage, into a shared-memory ring with TMA
+//      slot.  The plan also resets the work counter.
+//   2. decode_split_kernel (persistent, one or two CTAs per SM): lane 0 of a
+//      producer warp takes (item, kv-head group) units (CTA b: units b,
+//      b + grid, ... when the items are the equal balanced ones; the next from
+//      the counter for fixed splits) and streams the item's pages, 16 tokens
+//      per stage, into a shared-memory ring with TMA
 //      (cp.async.bulk.tensor, 128-byte swizzle), addressed through the block
 //      table.  One consumer warp per kv head contracts the stage with its GQA
 //      query group on the tensor cores (mma.sync m16n8k16: S^T = K Q^T with the
@@ -22,7 +24,8 @@
 //      an online softmax (running max and sum in log2 units).  A sequence in
 //      one piece writes its output directly; otherwise each piece writes its
 //      partial (m, l, acc) to the workspace.
-//   3. decode_merge_kernel, for sequences in two or more pieces:
+//   3. decode_merge_kernel, for sequences in two or more pieces (a warp per
+//      (sequence, query head) pair at a time):
 //      o = sum_k 2^(m_k - M) acc_k / sum_k 2^(m_k - M) l_k (the finalize step
 //      of the tiled attention) and lse = ln 2 (M + log2 L).
 // The split and merge kernels are programmatic dependent launches: each
