@@ -68,7 +68,8 @@ struct StageMeta {
     int32_t flags;
     int32_t head_group;   // which group of hpc kv heads the item covers
     int32_t n_splits;     // pieces of this sequence
-    int32_t pad[2];
+    int32_t row0;         // pool row of the stage's first token (when its block is valid)
+    int32_t pad;
 };
 
 struct DecodeParams {
@@ -89,6 +90,9 @@ struct DecodeParams {
     int32_t boxes_per_half;  // TMA boxes per (K or V, half): 1 (all heads) or hpc (one per head)
     uint32_t stage_bytes, tx_bytes, kv_tile_bytes, scale_tile_bytes, q_slot_bytes;
     int32_t scale_heads;          // int8: kv heads per scale box (a multiple of 4: 16-byte rows)
+    int32_t scales_in_stage;      // int8: 1 = the scale rows come with each stage (TMA), 0 = the
+                                  // consumers read them from k_scales / v_scales themselves
+    const float *k_scales, *v_scales;
     int32_t tile_stages;          // > 1: each piece is padded to a multiple of this many stages
     unsigned long long wait_ns;   // limit of the pipeline waits
 };
@@ -591,10 +595,12 @@ __device__ __forceinline__ void issue_stage_loads(uint8_t *stg, const DecodePara
         }
         // the scale box starts at a multiple of scale_heads heads (its first
         // coordinate times 4 bytes must be a multiple of 16)
-        uint8_t *sc = stg + 2 * p.kv_tile_bytes;
-        const int32_t sh0 = head0 / p.scale_heads * p.scale_heads;
-        tma_load_2d(sc, &ks_map, sh0, row0, bar);
-        tma_load_2d(sc + p.scale_tile_bytes, &vs_map, sh0, row0, bar);
+        if (p.scales_in_stage) {
+            uint8_t *sc = stg + 2 * p.kv_tile_bytes;
+            const int32_t sh0 = head0 / p.scale_heads * p.scale_heads;
+            tma_load_2d(sc, &ks_map, sh0, row0, bar);
+            tma_load_2d(sc + p.scale_tile_bytes, &vs_map, sh0, row0, bar);
+        }
     }
 }
 
@@ -714,12 +720,14 @@ __device__ __forceinline__ void run_producer(const SmemLayout &L, const DecodePa
                     m.flags |= kMetaBad;
                     report(p.dev_status, PKV_DEV_BAD_BLOCK_ID);
                 }
+                const int32_t row0 = bad ? 0 : blk * p.block_size + off;
+                m.row0 = row0;
+                m.pad = 0;
                 L.meta[st] = m;
                 if (bad) {
                     mbar_arrive(&L.full_bar[st]);
                 } else {
                     uint8_t *stg = L.stages + (size_t)st * p.stage_bytes;
-                    const int32_t row0 = blk * p.block_size + off;
                     mbar_arrive_expect_tx(&L.full_bar[st], p.tx_bytes);
                     issue_stage_loads<D, INT8>(stg, p, k_map, v_map, ks_map, vs_map, row0, hg * hpc,
                                                &L.full_bar[st]);
@@ -1541,11 +1549,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) decode_tc_kernel(const __grid_c
             if (have) {
                 const uint8_t *kc = stg + (size_t)h * kStageTokens * D;
                 const uint8_t *vc = kc + p.kv_tile_bytes;
-                const float *scl = reinterpret_cast<const float *>(stg + 2 * p.kv_tile_bytes);
-                const int hoff = ((int)mj.head_group * kTcHeads + h) % p.scale_heads;
+                // this token's scales, read here so that their latency overlaps the
+                // conversion (the stages carry only the codes)
                 if (valid) {
-                    sk = scl[tt * p.scale_heads + hoff];
-                    sv = scl[p.scale_tile_bytes / 4 + tt * p.scale_heads + hoff];
+                    const int64_t srow =
+                        (int64_t)(mj.row0 + tt) * p.n_kv_heads + ((int)mj.head_group * kTcHeads + h);
+                    sk = __ldg(p.k_scales + srow);
+                    sv = __ldg(p.v_scales + srow);
                 }
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {              // 16 codes = two 16-byte fp16 chunks
@@ -1895,6 +1905,9 @@ cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream, 
     p.wait_ns = pipeline_wait_ns();
     p.scale_heads = TC ? 4 : hpc;
     p.tile_stages = TC ? kTcStages : 0;
+    p.scales_in_stage = TC ? 0 : 1;
+    p.k_scales = a.k_scales;
+    p.v_scales = a.v_scales;
     if (!INT8) {
         p.kv_tile_bytes = (uint32_t)(D / 64) * hpc * 16u * 128u;
         p.scale_tile_bytes = 0;
@@ -1902,7 +1915,7 @@ cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream, 
     } else {
         p.kv_tile_bytes = (uint32_t)hpc * 16u * D;
         p.scale_tile_bytes = (uint32_t)p.scale_heads * 16u * 4u;
-        p.tx_bytes = 2 * p.kv_tile_bytes + 2 * p.scale_tile_bytes;
+        p.tx_bytes = 2 * p.kv_tile_bytes + (p.scales_in_stage ? 2 * p.scale_tile_bytes : 0u);
     }
     p.stage_bytes = (uint32_t)align_up(p.tx_bytes, 1024);
     p.q_slot_bytes = (uint32_t)(hpc * G * D * 2);
