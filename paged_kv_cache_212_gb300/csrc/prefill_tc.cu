@@ -26,6 +26,10 @@
 //   unless it grows by more than 2^8, then the O row is rescaled in TMEM);
 //   P_ij (bf16) back into TMEM; O_i += P_ij V_j (tcgen05.mma with A = P read
 //   from TMEM, B = V MN-major in shared memory).
+// At the end each softmax warpgroup writes its normalised O tile into shared
+// memory (the K ring, free once the last S products have retired) and one
+// thread stores it with a TMA copy per 64-column panel: one bulk operation
+// instead of each thread storing its scattered 256-byte row.
 // Issue order PV_0j, S_0,j+1, PV_1j, S_1,j+1: while one warpgroup computes the
 // softmax of its tile the tensor core runs the other tile's two products, and
 // the commit of S_i,j+1 also covers PV_ij, so O may be rescaled as soon as S is
@@ -153,12 +157,47 @@ __device__ __forceinline__ uint32_t swz128(uint32_t row, uint32_t chunk)
     return row * 128u + ((chunk ^ (row & 7u)) << 4);
 }
 
+// Shared memory -> global through a 4-D tensor map (elements past the map's
+// extent are not written), then the commit of the bulk group.
+__device__ __forceinline__ void tma_store_4d(const CUtensorMap *map, const void *src, int32_t c0, int32_t c1,
+                                             int32_t c2, int32_t c3)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.4d.global.shared::cta.bulk_group [%0, {%2, %3, %4, %5}], [%1];\n\t"
+        "cp.async.bulk.commit_group;" ::"l"(reinterpret_cast<uint64_t>(map)),
+        "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
+// The bulk copies this thread committed have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all()
+{
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// AND of v over the 128 threads of a warpgroup (named barrier id); every
+// thread of the warpgroup must reach it.
+__device__ __forceinline__ bool wg_and(uint32_t id, bool v)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id)
+        : "memory");
+    return r != 0;
+}
+
 }  // namespace
 
 template <int D>
 __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                                                             const __grid_constant__ CUtensorMap k_map,
                                                             const __grid_constant__ CUtensorMap v_map,
+                                                            const __grid_constant__ CUtensorMap o_map,
                                                             const PrefillTcParams p)
 {
     constexpr int PANELS = D / 64;                          // 64-column (128-byte) panels of a bf16 row
@@ -517,29 +556,43 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(const __grid_constan
             ok = __all_sync(0xffffffffu, mbar_wait(&o_done[qt], 0, abort_flag, p.wait_ns));
             tc_fence_after();
         }
-        if (ok && n_kt > 0) {
+        // the warpgroup agrees before its named barriers (every warp gets here)
+        const bool go = wg_and(1 + qt, ok && n_kt > 0);
+        if (go) {
+            // Row r of O, normalised, into a staging tile laid out like a Q tile
+            // ([panel][row][128 B], 128-byte swizzle; the K ring is free: the last S
+            // of both tiles retired before either tile's last P V), then one TMA
+            // store per panel (positions past the chunk are outside the map).
             const int pos = p0 + qt * pos_per_tile + r / G, h = kvh * G + r % G;
-            const bool store = pos <= p_last;
             const float inv = 1.f / l;
-            __nv_bfloat16 *o = p.out + (((int64_t)s * p.chunk + pos) * p.n_q_heads + h) * D;
+            uint8_t *stage = k_ring + qt * kQTile;
 #pragma unroll
             for (int c = 0; c < D / 32; ++c) {
                 uint32_t v[32];
                 tmem_ld32_async(lane_base + kOCol + c * 32, v);
                 tmem_wait_ld();
-                if (store) {
 #pragma unroll
-                    for (int q4 = 0; q4 < 4; ++q4) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(v[8 * q4 + 0]) * inv, __uint_as_float(v[8 * q4 + 1]) * inv);
-                        w.y = pack_bf16x2(__uint_as_float(v[8 * q4 + 2]) * inv, __uint_as_float(v[8 * q4 + 3]) * inv);
-                        w.z = pack_bf16x2(__uint_as_float(v[8 * q4 + 4]) * inv, __uint_as_float(v[8 * q4 + 5]) * inv);
-                        w.w = pack_bf16x2(__uint_as_float(v[8 * q4 + 6]) * inv, __uint_as_float(v[8 * q4 + 7]) * inv);
-                        *reinterpret_cast<uint4 *>(o + c * 32 + 8 * q4) = w;
-                    }
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    uint4 w;
+                    w.x = pack_bf16x2(__uint_as_float(v[8 * q4 + 0]) * inv, __uint_as_float(v[8 * q4 + 1]) * inv);
+                    w.y = pack_bf16x2(__uint_as_float(v[8 * q4 + 2]) * inv, __uint_as_float(v[8 * q4 + 3]) * inv);
+                    w.z = pack_bf16x2(__uint_as_float(v[8 * q4 + 4]) * inv, __uint_as_float(v[8 * q4 + 5]) * inv);
+                    w.w = pack_bf16x2(__uint_as_float(v[8 * q4 + 6]) * inv, __uint_as_float(v[8 * q4 + 7]) * inv);
+                    const uint32_t chunk = (uint32_t)((c % 2) * 4 + q4);
+                    *reinterpret_cast<uint4 *>(stage + (c / 2) * kQPanel + swz128((uint32_t)r, chunk)) = w;
                 }
             }
-            if (store && p.lse_out)
+            fence_proxy_async_smem();     // generic writes -> the TMA's reads
+            asm volatile("bar.sync %0, 128;" ::"r"(1 + qt) : "memory");
+            // a tile whose first position is past the chunk stores nothing; a tile
+            // that crosses the chunk's end is clipped by the map
+            if (r == 0 && p0 + qt * pos_per_tile <= p_last) {
+#pragma unroll
+                for (int hp = 0; hp < PANELS; ++hp)
+                    tma_store_4d(&o_map, stage + hp * kQPanel, hp * 64, kvh * G, p0 + qt * pos_per_tile, s);
+                bulk_wait_read_all();
+            }
+            if (pos <= p_last && p.lse_out)
                 p.lse_out[((int64_t)s * p.chunk + pos) * p.n_q_heads + h] = (m + __log2f(l)) * 0.69314718055994531f;
         } else if (!ok) {
             if (lane == 0) report(p.dev_status, PKV_DEV_TIMEOUT);
@@ -581,13 +634,25 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream)
     p.n_seqs = a.n_seqs;
     p.n_kv_heads = d.n_kv_heads;
 
-    CUtensorMap qmap, kmap, vmap;
+    CUtensorMap qmap, kmap, vmap, omap;
     {
         const uint64_t dims[3] = {(uint64_t)d.head_dim, (uint64_t)a.n_q_heads, (uint64_t)a.n_seqs * a.chunk};
         const uint64_t strides[2] = {(uint64_t)d.head_dim * 2, (uint64_t)a.n_q_heads * d.head_dim * 2};
         const uint32_t box[3] = {64u, (uint32_t)G, (uint32_t)pos_per_tile};
         if (encode_tensor_map(&qmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(a.q), dims, strides,
                               box, CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
+            return cudaErrorInvalidValue;
+    }
+    {
+        // out: {64 columns, query head, chunk position, sequence}; the box of a
+        // query tile is the Q box, and positions past the chunk are not written
+        const uint64_t dims[4] = {(uint64_t)d.head_dim, (uint64_t)a.n_q_heads, (uint64_t)a.chunk,
+                                  (uint64_t)a.n_seqs};
+        const uint64_t strides[3] = {(uint64_t)d.head_dim * 2, (uint64_t)a.n_q_heads * d.head_dim * 2,
+                                     (uint64_t)a.chunk * a.n_q_heads * d.head_dim * 2};
+        const uint32_t box[4] = {64u, (uint32_t)G, (uint32_t)pos_per_tile, 1u};
+        if (encode_tensor_map(&omap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, a.out, dims, strides, box,
+                              CU_TENSOR_MAP_SWIZZLE_128B) != CUDA_SUCCESS)
             return cudaErrorInvalidValue;
     }
     const uint64_t rows = (uint64_t)(d.n_blocks + 1) * d.block_size;
@@ -632,11 +697,11 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream)
     if (d.head_dim == 128) {
         e = prepare_kernel(reinterpret_cast<const void *>(prefill_tc_kernel<128>), 384, smem, nullptr);
         if (e != cudaSuccess) return e;
-        prefill_tc_kernel<128><<<grid, 384, smem, stream>>>(qmap, kmap, vmap, p);
+        prefill_tc_kernel<128><<<grid, 384, smem, stream>>>(qmap, kmap, vmap, omap, p);
     } else {
         e = prepare_kernel(reinterpret_cast<const void *>(prefill_tc_kernel<64>), 384, smem, nullptr);
         if (e != cudaSuccess) return e;
-        prefill_tc_kernel<64><<<grid, 384, smem, stream>>>(qmap, kmap, vmap, p);
+        prefill_tc_kernel<64><<<grid, 384, smem, stream>>>(qmap, kmap, vmap, omap, p);
     }
     return cudaGetLastError();
 }
