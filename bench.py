@@ -58,8 +58,8 @@ FALLBACK_HBM_GBS = 6800.0
 NCU_TRAFFIC = {
     "decode": {"sources": ("decode.cu", "common.cuh", "launch.h", "tcgen05.cuh"), "source_sha": "b3f49d6e92f89e4e",
                "bytes_per_launch": {1: 544765952 + 4051200, 2: 310420736 + 3940864, 4: 1317307648 + 32826624}},
-    "prefill": {"sources": ("prefill_tc.cu", "common.cuh", "launch.h", "tcgen05.cuh"), "source_sha": "4b59c2f46c0e3928",
-                "bytes_per_launch": {3: 196737280 + 16645632}},
+    "prefill": {"sources": ("prefill_tc.cu", "common.cuh", "launch.h", "tcgen05.cuh"), "source_sha": "fa0f065aebf6992a",
+                "bytes_per_launch": {3: 198451712 + 17734144}},
 }
 
 
