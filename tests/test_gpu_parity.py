@@ -504,6 +504,31 @@ def test_decode_plan_matches_calls(P, name, decode_impl):
         assert mx <= BF16_MAX and mean <= BF16_MEAN, (mx, mean)
 
 
+def test_calls_run_on_the_current_stream(P):
+    """Without an explicit stream the calls enqueue on the caller's current
+    stream: under torch.cuda.stream(side), a decode step whose inputs are
+    produced on that stream gives the default-stream result, and the default
+    stream sees it only after waiting for the side stream."""
+    w = workload("tiny")
+    kp, vp, _, _ = pools("tiny", after_step=False)
+    tables, start, ctx = i32(w.tables), i32(w.start_pos), i32(w.ctx_lens)
+    gk, gv = dev(kp), dev(vp)
+    ref = P.paged_decode_step(w.k_new.cuda(), w.v_new.cuda(), start, w.q.cuda(), gk, gv, tables, ctx,
+                              w.softmax_scale)
+    torch.cuda.synchronize()
+    gk2, gv2 = dev(kp), dev(vp)
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        torch.cuda._sleep(2_000_000)                        # the side stream is busy for a while
+        q = w.q.cuda()                                      # produced on the side stream
+        plan = P.DecodePlan(gk2, gv2, tables, ctx, w.softmax_scale, q.shape[1])
+        out = plan.run(q, w.k_new.cuda(), w.v_new.cuda(), start)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+
+
 def test_decode_plan_refuses_mismatched_calls(P):
     w = workload("tiny")
     kp, vp, _, _ = pools("tiny", after_step=False)
