@@ -61,7 +61,7 @@ enum pkv_status {
     PKV_ERR_INVALID_ARG = 1,  /* null / misaligned pointer, non-positive size, Hq % Hkv != 0 */
     PKV_ERR_UNSUPPORTED = 2,  /* head_dim, block_size, group size or kv dtype not supported */
     PKV_ERR_OUT_OF_RANGE = 3, /* a host-checkable size is out of range (e.g. n_new > table) */
-    PKV_ERR_WORKSPACE = 4,    /* workspace null or smaller than required */
+    PKV_ERR_WORKSPACE = 4,    /* workspace null, smaller than required or not 256-byte aligned */
     PKV_ERR_CUDA = 5,         /* a CUDA call failed; pkv_last_cuda_error() says which */
     PKV_ERR_OUT_OF_BLOCKS = 6, /* block manager: not enough free blocks (nothing changed) */
     PKV_ERR_STATE = 7         /* block manager: the call does not fit the current state */
@@ -212,8 +212,9 @@ size_t pkv_decode_workspace_bytes(int32_t n_seqs, int32_t n_q_heads, int32_t hea
  * of 16; 0 = automatic), each range is reduced with an online softmax, and
  * the ranges are merged by their log-sum-exp.  ctx_lens[s] == 0 gives o = 0
  * and lse = -inf.  workspace: device memory of at least
- * pkv_decode_workspace_bytes(...) bytes, contents need not be initialised,
- * and it must not be shared by concurrently running calls.
+ * pkv_decode_workspace_bytes(...) bytes, 256-byte aligned (else
+ * PKV_ERR_WORKSPACE; the CUDA allocators return such addresses), contents need
+ * not be initialised, and it must not be shared by concurrently running calls.
  * With split_tokens = 0 and bf16 pages, a batch of at most one (sequence,
  * kv head) pair per SM whose table spans at most 256 tokens (head_dim 128) or
  * 512 (head_dim 64) is attended whole by one CTA per pair in a single launch

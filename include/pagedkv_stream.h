@@ -96,7 +96,8 @@ size_t pkv_streamed_workspace_bytes(int32_t n_seqs, int32_t n_q_heads, int32_t h
  * writes out (bf16 [n_seqs][n_q_heads][head_dim]) and lse_out (fp32
  * [n_seqs][n_q_heads], natural log; nullable).  ctx_lens is HOST int32
  * [n_seqs]; q, out, lse_out device.  workspace: device memory of
- * pkv_streamed_workspace_bytes(...) bytes; the residency state in sp carries
+ * pkv_streamed_workspace_bytes(...) bytes, 256-byte aligned (else
+ * PKV_ERR_WORKSPACE); the residency state in sp carries
  * over between calls (a later call reuses what is still resident).  The
  * attention and merges are enqueued on stream, the plan copies and staging on
  * the pool's copy stream, ordered against stream by events (the staging waits

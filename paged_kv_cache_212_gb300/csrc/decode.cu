@@ -1787,7 +1787,8 @@ size_t decode_workspace_bytes(int32_t n_seqs, int32_t n_q_heads, int32_t head_di
 bool carve_decode_workspace(void *ws, size_t bytes, int32_t n_seqs, int32_t n_q_heads,
                             int32_t head_dim, DecodeWorkspace *out)
 {
-    if (!ws) return false;
+    // every array is carved at a multiple of 256 bytes from a 256-byte aligned base
+    if (!ws || reinterpret_cast<uintptr_t>(ws) % 256 != 0) return false;
     if (bytes < decode_workspace_bytes(n_seqs, n_q_heads, head_dim, 1)) return false;
     const size_t per = sizeof(int2) + (size_t)n_q_heads * sizeof(float2) +
                        (size_t)n_q_heads * head_dim * sizeof(float);

@@ -411,7 +411,7 @@ int paged_decode_streamed(const pkv_bf16 *q, int32_t n_q_heads, const pkv_bf16 *
     size_t decode_bytes = 0;
     const size_t need = stream_ws_bytes(n_seqs, n_q_heads, D, n_slots, bs, &decode_bytes);
     if (need == 0) return PKV_ERR_INVALID_ARG;
-    if (workspace_bytes < need) return PKV_ERR_WORKSPACE;
+    if (workspace_bytes < need || reinterpret_cast<uintptr_t>(workspace) % 256 != 0) return PKV_ERR_WORKSPACE;
     // check the host tier's device mapping once (staging would fail per tile)
     const void *dk = nullptr, *dv = nullptr;
     int st = mapped(host_k, &dk);

@@ -116,6 +116,7 @@ def test_decode_argument_checks(lib):
     assert f(*args(dt=1, ks=FAKE, vs=FAKE)) == 2   # int8 needs Hkv % 4 == 0
     assert f(*args(ws=None)) == 4
     assert f(*args(wsb=64)) == 4
+    assert f(*args(ws=ctypes.c_void_p(0x1010))) == 4  # not 256-byte aligned
     for sc in (0.0, -0.125, float("nan"), float("inf")):  # the scale must be finite and positive
         assert f(*args(sc=sc)) == 1, sc
 

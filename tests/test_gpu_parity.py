@@ -545,6 +545,26 @@ def test_decode_plan_refuses_mismatched_calls(P):
         plan.run(q.float())                                 # wrong dtype
 
 
+def test_decode_refuses_an_unaligned_workspace(P):
+    """A workspace that does not start on a 256-byte boundary is refused on the
+    host (PKV_ERR_WORKSPACE, nothing enqueued); the same bytes one slice
+    later, aligned, give the workspace-allocating call's result."""
+    w = workload("int8_small")
+    kp, vp, ks, vs = pools("int8_small")
+    args = (w.q.cuda(), dev(kp), dev(vp), i32(w.tables), i32(w.ctx_lens), w.softmax_scale)
+    kw = dict(k_scales=dev(ks), v_scales=dev(vs), split_tokens=64)
+    need = P.decode_workspace_bytes(w.n_seqs, w.n_q_heads, w.head_dim, int(w.ctx_lens.sum()), 64)
+    buf = torch.empty(need + 256, dtype=torch.uint8, device="cuda")
+    assert buf.data_ptr() % 256 == 0
+    with pytest.raises(P.PagedKVError) as e:
+        P.paged_decode_attention(*args, workspace=buf[16:16 + need], **kw)
+    assert e.value.status == 4
+    got = P.paged_decode_attention(*args, workspace=buf[256:256 + need], **kw)
+    ref = P.paged_decode_attention(*args, **kw)
+    torch.cuda.synchronize()
+    assert torch.equal(got, ref)
+
+
 def test_int8_write_near_ties_bit_exact(P):
     """Rows whose codes sit at or next to a half-integer quotient -- where a
     reciprocal multiply and the IEEE division by the stored scale can round

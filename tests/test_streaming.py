@@ -87,7 +87,7 @@ def test_streamed_decode_host_checks(P):
         return lib.paged_decode_streamed(
             kw.get("q", fake), 8, fake, fake, kw.get("n_host", 10), fake, fake, kw.get("dims", d),
             kw.get("sp", sp._h), kw.get("tables", tables), 2, kw.get("lens", lens), kw.get("n", 2),
-            kw.get("scale", 0.125), fake, None, fake, kw.get("wsb", need), None, None)
+            kw.get("scale", 0.125), fake, None, kw.get("ws", fake), kw.get("wsb", need), None, None)
 
     assert call(n=0) == 0
     assert call(sp=None) == 1
@@ -100,6 +100,7 @@ def test_streamed_decode_host_checks(P):
     assert call(lens=(ctypes.c_int32 * 2)(20, 33)) == 3      # past the table (2 blocks of 16)
     assert call(n_host=3) == 3                               # host id 3 outside a 3-block tier
     assert call(wsb=need - 1) == 4
+    assert call(ws=ctypes.c_void_p(0x1010)) == 4               # not 256-byte aligned
     assert need > 0
 
 
