@@ -61,6 +61,52 @@ constexpr int32_t kMinChunkStages = 4;   // balanced items hold at least 64 toke
 
 enum : int32_t { kMetaFirst = 1, kMetaLast = 2, kMetaBad = 4, kMetaStop = 8, kMetaFinal = 16, kMetaPad = 32 };
 
+// L2 eviction priorities for the split-KV partials: the split kernel stores
+// them to be evicted last, so that they are still in L2 when the merge reads
+// them after the whole context has streamed through; the merge's reads mark
+// them to be evicted first (they are dead until the next call writes them).
+__device__ __forceinline__ uint64_t l2_evict_last_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ uint64_t l2_evict_first_policy()
+{
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void st_kept(float *a, float v, uint64_t pol)
+{
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(a), "f"(v), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void st_kept(float2 *a, float2 v, uint64_t pol)
+{
+    asm volatile("st.global.L2::cache_hint.v2.f32 [%0], {%1, %2}, %3;" ::"l"(a), "f"(v.x), "f"(v.y), "l"(pol)
+                 : "memory");
+}
+__device__ __forceinline__ float2 ld_last_use(const float2 *a, uint64_t pol)
+{
+    float2 v;
+    asm volatile("ld.global.cg.L2::cache_hint.v2.f32 {%0, %1}, [%2], %3;" : "=f"(v.x), "=f"(v.y) : "l"(a), "l"(pol));
+    return v;
+}
+// drops a 128-byte L2 line without writing it back (its contents become
+// undefined): partial rows the merge has read are dead until the next call
+__device__ __forceinline__ void l2_discard_line(const void *a)
+{
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(a) : "memory");
+}
+__device__ __forceinline__ float4 ld_last_use(const float4 *a, uint64_t pol)
+{
+    float4 v;
+    asm volatile("ld.global.cg.L2::cache_hint.v4.f32 {%0, %1, %2, %3}, [%4], %5;"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "l"(a), "l"(pol));
+    return v;
+}
+
 struct StageMeta {
     int32_t seq;
     int32_t split_index;  // the piece's partial slot
@@ -463,16 +509,19 @@ __global__ void __launch_bounds__(kPlanThreads, 4) decode_plan_kernel(const int3
 // of up to kRound pieces costs one memory round trip); the round's maximum
 // rescales the running sums (an online merge) and each row is weighted by its
 // piece's factor broadcast from the lane that read it.  Partials are read with
-// ld.global.cg (L2): other SMs wrote them.  Launched after the split kernel as
-// a programmatic dependent: the plan's results are complete when it starts
-// (the split kernel releases it only after its own wait for the plan); only
-// the partials need the wait for the split kernel.
+// ld.global.cg (L2: other SMs wrote them), marked to be evicted first; with
+// drop_partials (fixed splits, whose partials grow with the context) a pair's
+// rows are then discarded from L2, so the dead lines are never written back.
+// Launched after the split kernel as a programmatic dependent: the plan's
+// results are complete when it starts (the split kernel releases it only after
+// its own wait for the plan); only the partials need the wait for the split
+// kernel.
 constexpr int kMergeCtasPerSm = 6;
 
 template <int D>
 __global__ void __launch_bounds__(128, kMergeCtasPerSm) decode_merge_kernel(DecodeWorkspace ws, int32_t n_seqs,
                                                                            int32_t n_q_heads, __nv_bfloat16 *out,
-                                                                           float *lse_out)
+                                                                           float *lse_out, int32_t drop_partials)
 {
     constexpr int EPL = D / 32;                      // output elements per lane
     constexpr int kRound = 8;                        // pieces per round
@@ -487,6 +536,7 @@ __global__ void __launch_bounds__(128, kMergeCtasPerSm) decode_merge_kernel(Deco
     const int2 sg0 = idx0 < n_pairs ? ws.seg[idx0 / n_q_heads] : make_int2(0, 0);
     grid_dependency_wait();
     if (overflow != 0) return;
+    const uint64_t drop = l2_evict_first_policy();
     for (int64_t idx = idx0; idx < n_pairs; idx += n_warps) {
         const int32_t s = (int32_t)(idx / n_q_heads), h = (int32_t)(idx % n_q_heads);
         const int2 sg = idx == idx0 ? sg0 : ws.seg[s];
@@ -501,7 +551,7 @@ __global__ void __launch_bounds__(128, kMergeCtasPerSm) decode_merge_kernel(Deco
         for (int e = 0; e < EPL; ++e) o[e] = 0.f;
         for (int32_t k0 = 0; k0 < n; k0 += kRound) {
             const int32_t cnt = min(kRound, n - k0);
-            const float2 ml = lane < cnt ? __ldcg(&ws.part_ml[row0 + (int64_t)(k0 + lane) * n_q_heads])
+            const float2 ml = lane < cnt ? ld_last_use(&ws.part_ml[row0 + (int64_t)(k0 + lane) * n_q_heads], drop)
                                          : make_float2(-INFINITY, 0.f);
             float a[kRound][EPL];
 #pragma unroll
@@ -509,13 +559,13 @@ __global__ void __launch_bounds__(128, kMergeCtasPerSm) decode_merge_kernel(Deco
                 if (i < cnt) {
                     const float *src = base + (int64_t)(k0 + i) * stride;
                     if constexpr (EPL == 4) {
-                        const float4 x = __ldcg(reinterpret_cast<const float4 *>(src));
+                        const float4 x = ld_last_use(reinterpret_cast<const float4 *>(src), drop);
                         a[i][0] = x.x;
                         a[i][1] = x.y;
                         a[i][2] = x.z;
                         a[i][3] = x.w;
                     } else {
-                        const float2 x = __ldcg(reinterpret_cast<const float2 *>(src));
+                        const float2 x = ld_last_use(reinterpret_cast<const float2 *>(src), drop);
                         a[i][0] = x.x;
                         a[i][1] = x.y;
                     }
@@ -557,6 +607,15 @@ __global__ void __launch_bounds__(128, kMergeCtasPerSm) decode_merge_kernel(Deco
         if (lse_out && lane == 0)
             lse_out[(int64_t)s * n_q_heads + h] =
                 Lsum > 0.f ? (M + __log2f(Lsum)) * 0.69314718055994531f : -INFINITY;
+        // the pair's partial rows are dead (every lane has used its values):
+        // their L2 lines are dropped without a write-back, lane l taking lines
+        // l, l + 32, ... (row i / LINES, line i % LINES)
+        if (drop_partials) {
+            __syncwarp();
+            constexpr int LINES = D / 32;   // 128-byte lines per row of D floats
+            for (int i = lane; i < n * LINES; i += 32)
+                l2_discard_line(ws.part_acc + (row0 + (int64_t)(i / LINES) * n_q_heads) * D + (i % LINES) * 32);
+        }
     }
 }
 
@@ -1214,27 +1273,32 @@ __global__ void __launch_bounds__(288, INT8 ? 1 : 2) decode_split_kernel(const _
             } else {
                 const int64_t prow = (int64_t)meta.split_index * p.n_q_heads + hbase;
                 float *pa = p.ws.part_acc + prow * D;
+                const uint64_t keep = l2_evict_last_policy();
 #pragma unroll
                 for (int mt = 0; mt < KSTEPS; ++mt) {
                     if (INT8) {
                         const int d = g * (D / 8) + 2 * mt;
-                        if (n0 < G) *reinterpret_cast<float2 *>(pa + (size_t)n0 * D + d) = make_float2(acc[mt][0], acc[mt][2]);
-                        if (n1 < G) *reinterpret_cast<float2 *>(pa + (size_t)n1 * D + d) = make_float2(acc[mt][1], acc[mt][3]);
+                        if (n0 < G)
+                            st_kept(reinterpret_cast<float2 *>(pa + (size_t)n0 * D + d), make_float2(acc[mt][0], acc[mt][2]),
+                                    keep);
+                        if (n1 < G)
+                            st_kept(reinterpret_cast<float2 *>(pa + (size_t)n1 * D + d), make_float2(acc[mt][1], acc[mt][3]),
+                                    keep);
                     } else {
                         const int d = mt * 16 + g;
                         if (n0 < G) {
-                            pa[(size_t)n0 * D + d] = acc[mt][0];
-                            pa[(size_t)n0 * D + d + 8] = acc[mt][2];
+                            st_kept(pa + (size_t)n0 * D + d, acc[mt][0], keep);
+                            st_kept(pa + (size_t)n0 * D + d + 8, acc[mt][2], keep);
                         }
                         if (n1 < G) {
-                            pa[(size_t)n1 * D + d] = acc[mt][1];
-                            pa[(size_t)n1 * D + d + 8] = acc[mt][3];
+                            st_kept(pa + (size_t)n1 * D + d, acc[mt][1], keep);
+                            st_kept(pa + (size_t)n1 * D + d + 8, acc[mt][3], keep);
                         }
                     }
                 }
                 if (g == 0) {
-                    if (n0 < G) p.ws.part_ml[prow + n0] = make_float2(m0, L0);
-                    if (n1 < G) p.ws.part_ml[prow + n1] = make_float2(m1, L1);
+                    if (n0 < G) st_kept(p.ws.part_ml + prow + n0, make_float2(m0, L0), keep);
+                    if (n1 < G) st_kept(p.ws.part_ml + prow + n1, make_float2(m1, L1), keep);
                 }
             }
             ++item_it;
@@ -2021,8 +2085,10 @@ cudaError_t launch_split(const DecodeArgs &a, int num_sms, cudaStream_t stream, 
     mc.stream = stream;
     mc.attrs = pdl;
     mc.numAttrs = 1;
+    // fixed splits write partials in proportion to the context (balanced ones
+    // about one piece per CTA): only theirs are worth dropping from L2
     return cudaLaunchKernelEx(&mc, decode_merge_kernel<D>, a.ws, a.n_seqs, a.n_q_heads,
-                              static_cast<__nv_bfloat16 *>(a.out), a.lse_out);
+                              static_cast<__nv_bfloat16 *>(a.out), a.lse_out, (int32_t)(a.split_tokens > 0));
 }
 
 }  // namespace
