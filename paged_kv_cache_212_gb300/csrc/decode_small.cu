@@ -9,7 +9,10 @@
 // in fp32, then V^T P^T on mma.sync (P rounded to bf16, as in the split-KV
 // kernel).  Every CTA reads
 // only its own kv head, so the rows it wrote are the only new ones it reads
-// (visible to the block after a barrier); no CTA depends on another.
+// (visible to the block after a barrier); no CTA depends on another.  The
+// launch is a programmatic dependent of the previous kernel on the stream (its
+// CTAs are placed while that kernel drains and read nothing before it has
+// completed), and lets the next one be placed the same way.
 #include <math.h>
 
 #include "common.cuh"
@@ -71,6 +74,12 @@ __global__ void __launch_bounds__(kThreads) decode_small_kernel(const DecodeArgs
     const int g4 = lane >> 2, q4 = lane & 3;          // mma fragment row group / column pair
     const int mi = lane >> 3, ri = lane & 7;          // ldmatrix matrix / row within it
     const int32_t *trow = a.tables + (int64_t)s * a.max_blocks;
+
+    // launched as a programmatic dependent: the next kernel on the stream may
+    // become resident now (it waits for this grid itself); nothing is read
+    // before the preceding grid has completed
+    grid_dependents_launch();
+    grid_dependency_wait();
 
     // 1. context length, table row (bad ids mark their block's tokens as
     //    absent) and query rows; they do not depend on this step's rows
@@ -293,11 +302,21 @@ cudaError_t launch_decode_small(const DecodeArgs &a, const WriteArgs *write, cud
             ? prepare_kernel(reinterpret_cast<const void *>(decode_small_kernel<128>), kThreads, smem, nullptr)
             : prepare_kernel(reinterpret_cast<const void *>(decode_small_kernel<64>), kThreads, smem, nullptr);
     if (attr_err != cudaSuccess) return attr_err;
-    if (a.dims.head_dim == 128)
-        decode_small_kernel<128><<<grid, kThreads, smem, stream>>>(a, w, write ? 1 : 0, cap);
-    else
-        decode_small_kernel<64><<<grid, kThreads, smem, stream>>>(a, w, write ? 1 : 0, cap);
-    return cudaGetLastError();
+    // a programmatic dependent of the previous kernel on the stream: its CTAs
+    // are placed while that kernel drains and wait for it in the kernel
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t lc{};
+    lc.gridDim = dim3(grid);
+    lc.blockDim = dim3(kThreads);
+    lc.dynamicSmemBytes = smem;
+    lc.stream = stream;
+    lc.attrs = pdl;
+    lc.numAttrs = 1;
+    const int do_write = write ? 1 : 0;
+    if (a.dims.head_dim == 128) return cudaLaunchKernelEx(&lc, decode_small_kernel<128>, a, w, do_write, cap);
+    return cudaLaunchKernelEx(&lc, decode_small_kernel<64>, a, w, do_write, cap);
 }
 
 }  // namespace pkv
