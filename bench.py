@@ -58,8 +58,8 @@ FALLBACK_HBM_GBS = 6800.0
 NCU_TRAFFIC = {
     "decode": {"sources": ("decode.cu", "common.cuh", "launch.h", "tcgen05.cuh"), "source_sha": "49d4ee397a96c233",
                "bytes_per_launch": {1: 544752640 + 3192320, 2: 310436096 + 3242496, 4: 1318916864 + 12018944}},
-    "prefill": {"sources": ("prefill_tc.cu", "common.cuh", "launch.h", "tcgen05.cuh"), "source_sha": "fa0f065aebf6992a",
-                "bytes_per_launch": {3: 198451712 + 17734144}},
+    "prefill": {"sources": ("prefill_tc.cu", "common.cuh", "launch.h", "tcgen05.cuh"), "source_sha": "6734f6fa468fbe1b",
+                "bytes_per_launch": {3: 197949952 + 17204224}},
 }
 
 

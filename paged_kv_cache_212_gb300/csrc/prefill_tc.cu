@@ -229,6 +229,11 @@ __global__ void __launch_bounds__(384, 1) prefill_tc_kernel(const __grid_constan
     int32_t *sched = reinterpret_cast<int32_t *>(bars + 32);  // [kSortMaxSeqs + 1]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // launched as a programmatic dependent: the next kernel on the stream may
+    // be placed once every CTA of this one has started (it waits for this grid
+    // itself); nothing is read before the preceding grid has completed
+    grid_dependents_launch();
+    grid_dependency_wait();
     // CTA order: sequence-major, the heavy (late) query pairs of a sequence
     // first, its kv heads innermost.  Small batches take their sequences
     // longest prefix first, so the longest CTAs start in the first wave
@@ -693,17 +698,27 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t stream)
                fa64.numRegs >= kLaunchRegs;
     }();
     if (!regs_ok) return cudaErrorInvalidConfiguration;
+    // a programmatic dependent of the previous kernel on the stream: its CTAs
+    // are placed on SMs as that kernel's CTAs leave them
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t lc{};
+    lc.gridDim = grid;
+    lc.blockDim = dim3(384);
+    lc.dynamicSmemBytes = smem;
+    lc.stream = stream;
+    lc.attrs = pdl;
+    lc.numAttrs = 1;
     cudaError_t e;
     if (d.head_dim == 128) {
         e = prepare_kernel(reinterpret_cast<const void *>(prefill_tc_kernel<128>), 384, smem, nullptr);
         if (e != cudaSuccess) return e;
-        prefill_tc_kernel<128><<<grid, 384, smem, stream>>>(qmap, kmap, vmap, omap, p);
-    } else {
-        e = prepare_kernel(reinterpret_cast<const void *>(prefill_tc_kernel<64>), 384, smem, nullptr);
-        if (e != cudaSuccess) return e;
-        prefill_tc_kernel<64><<<grid, 384, smem, stream>>>(qmap, kmap, vmap, omap, p);
+        return cudaLaunchKernelEx(&lc, prefill_tc_kernel<128>, qmap, kmap, vmap, omap, p);
     }
-    return cudaGetLastError();
+    e = prepare_kernel(reinterpret_cast<const void *>(prefill_tc_kernel<64>), 384, smem, nullptr);
+    if (e != cudaSuccess) return e;
+    return cudaLaunchKernelEx(&lc, prefill_tc_kernel<64>, qmap, kmap, vmap, omap, p);
 }
 
 }  // namespace pkv

@@ -12,10 +12,29 @@
 
 namespace pkv {
 
+// Launch configuration of a programmatic dependent of the previous kernel on
+// the stream (its CTAs are placed while that kernel drains; the kernel waits
+// for it before reading anything).
+static cudaLaunchConfig_t dependent_launch(cudaLaunchAttribute (&pdl)[1], unsigned grid, unsigned threads,
+                                           cudaStream_t stream)
+{
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t lc{};
+    lc.gridDim = dim3(grid);
+    lc.blockDim = dim3(threads);
+    lc.stream = stream;
+    lc.attrs = pdl;
+    lc.numAttrs = 1;
+    return lc;
+}
+
 // Native bf16 write: the flat 16-byte-vector space of the new rows,
 // grid-strided (write_rows.cuh).
 __global__ void __launch_bounds__(256) write_bf16_kernel(const WriteArgs a)
 {
+    grid_dependents_launch();   // a programmatic dependent: nothing is read before the wait
+    grid_dependency_wait();
     write_bf16_vectors(a, (int64_t)blockIdx.x * blockDim.x + threadIdx.x, (int64_t)gridDim.x * blockDim.x);
 }
 
@@ -25,6 +44,8 @@ __global__ void __launch_bounds__(256) write_bf16_kernel(const WriteArgs a)
 template <int EPL>
 __global__ void __launch_bounds__(256, 4) write_int8_kernel(const WriteArgs a, float *k_scales, float *v_scales)
 {
+    grid_dependents_launch();   // a programmatic dependent: nothing is read before the wait
+    grid_dependency_wait();
     const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     write_int8_units<EPL>(a, k_scales, v_scales, warp, (int64_t)gridDim.x * (blockDim.x >> 5));
 }
@@ -136,8 +157,9 @@ cudaError_t launch_write_bf16(const WriteArgs &a, cudaStream_t stream)
     const int64_t n_vecs = (int64_t)a.n_seqs * a.n_new * (a.dims.n_kv_heads * a.dims.head_dim / 8);
     int64_t grid = (n_vecs + 255) / 256;
     if (grid > 4096) grid = 4096;
-    write_bf16_kernel<<<(unsigned)grid, 256, 0, stream>>>(a);
-    return cudaGetLastError();
+    cudaLaunchAttribute pdl[1];
+    cudaLaunchConfig_t lc = dependent_launch(pdl, (unsigned)grid, 256, stream);
+    return cudaLaunchKernelEx(&lc, write_bf16_kernel, a);
 }
 
 cudaError_t launch_write_int8(const WriteArgs &a, float *k_scales, float *v_scales, cudaStream_t stream)
@@ -145,11 +167,10 @@ cudaError_t launch_write_int8(const WriteArgs &a, float *k_scales, float *v_scal
     const int64_t n_units = (int64_t)a.n_seqs * a.n_new * 2 * ((a.dims.n_kv_heads + 3) / 4);
     int64_t grid = (n_units + 7) / 8;
     if (grid > 4096) grid = 4096;
-    if (a.dims.head_dim == 128)
-        write_int8_kernel<16><<<(unsigned)grid, 256, 0, stream>>>(a, k_scales, v_scales);
-    else
-        write_int8_kernel<8><<<(unsigned)grid, 256, 0, stream>>>(a, k_scales, v_scales);
-    return cudaGetLastError();
+    cudaLaunchAttribute pdl[1];
+    cudaLaunchConfig_t lc = dependent_launch(pdl, (unsigned)grid, 256, stream);
+    if (a.dims.head_dim == 128) return cudaLaunchKernelEx(&lc, write_int8_kernel<16>, a, k_scales, v_scales);
+    return cudaLaunchKernelEx(&lc, write_int8_kernel<8>, a, k_scales, v_scales);
 }
 
 cudaError_t launch_gather(const GatherArgs &a, int num_sms, cudaStream_t stream)
