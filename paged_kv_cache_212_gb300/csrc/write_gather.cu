@@ -58,7 +58,9 @@ __global__ void __launch_bounds__(256, 4) write_int8_kernel(const WriteArgs a, f
 // scheduler balances the equal-sized units, so no warp ends with one more
 // unit than the others; 128-thread CTAs measured ~1 % faster than 256 or 512
 // (16 sequences x 2048 tokens: 6012 GB/s, above a device-to-device cudaMemcpy
-// of the same bytes at 5770).
+// of the same bytes at 5770).  Launched as a programmatic dependent, so the
+// next call's CTAs take the SMs this one's last wave leaves (6430 GB/s back
+// to back).
 template <int UNROLL>
 __global__ void __launch_bounds__(128) gather_kernel(
     const uint4 *__restrict__ k_pool, const uint4 *__restrict__ v_pool, int32_t n_blocks,
@@ -66,6 +68,8 @@ __global__ void __launch_bounds__(128) gather_kernel(
     int32_t max_blocks, const int32_t *__restrict__ lens, int32_t out_tokens,
     uint4 *__restrict__ k_out, uint4 *__restrict__ v_out, int32_t blocks_out, int64_t n_units, int32_t *dev_status)
 {
+    grid_dependents_launch();   // a programmatic dependent: nothing is read before the wait
+    grid_dependency_wait();
     const int lane = threadIdx.x & 31;
     const int64_t n_warps = (int64_t)gridDim.x * (blockDim.x >> 5);
     const int32_t limit = min(out_tokens, max_blocks * block_size);
@@ -128,6 +132,8 @@ __global__ void __launch_bounds__(256) copy_blocks_kernel(uint4 *__restrict__ k_
                                                           int64_t block_vecs, int64_t scale_vecs, int64_t n_vecs,
                                                           int32_t *dev_status)
 {
+    grid_dependents_launch();   // a programmatic dependent: nothing is read before the wait
+    grid_dependency_wait();
     const int64_t per_pair = 2 * block_vecs + 2 * scale_vecs;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_vecs; i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t pr = i / per_pair, r = i % per_pair;
@@ -183,11 +189,12 @@ cudaError_t launch_gather(const GatherArgs &a, int num_sms, cudaStream_t stream)
     (void)num_sms;
     int64_t grid = (n_units + 3) / 4;                         // one unit per warp, four warps per CTA
     if (grid > 0x7fffffffLL) grid = 0x7fffffffLL;
-    gather_kernel<kUnroll><<<(unsigned)grid, 128, 0, stream>>>(
-        (const uint4 *)a.k_pool, (const uint4 *)a.v_pool, a.dims.n_blocks, a.dims.block_size,
-        a.dims.n_kv_heads, d_shift, a.tables, a.max_blocks, a.lens, a.out_tokens, (uint4 *)a.k_out,
-        (uint4 *)a.v_out, blocks_out, n_units, a.dev_status);
-    return cudaGetLastError();
+    cudaLaunchAttribute pdl[1];
+    cudaLaunchConfig_t lc = dependent_launch(pdl, (unsigned)grid, 128, stream);
+    return cudaLaunchKernelEx(&lc, gather_kernel<kUnroll>, (const uint4 *)a.k_pool, (const uint4 *)a.v_pool,
+                              a.dims.n_blocks, a.dims.block_size, a.dims.n_kv_heads, d_shift, a.tables,
+                              a.max_blocks, a.lens, a.out_tokens, (uint4 *)a.k_out, (uint4 *)a.v_out, blocks_out,
+                              n_units, a.dev_status);
 }
 
 cudaError_t launch_copy_blocks(const int32_t *pairs, int32_t n_pairs, void *k_pool, void *v_pool, float *k_scales,
@@ -201,10 +208,11 @@ cudaError_t launch_copy_blocks(const int32_t *pairs, int32_t n_pairs, void *k_po
     if (n_vecs == 0) return cudaSuccess;
     int64_t grid = (n_vecs + 255) / 256, cap = (int64_t)num_sms * 8;
     if (grid > cap) grid = cap;
-    copy_blocks_kernel<<<(unsigned)grid, 256, 0, stream>>>((uint4 *)k_pool, (uint4 *)v_pool, (uint4 *)k_scales,
-                                                           (uint4 *)v_scales, (const int2 *)pairs, d.n_blocks,
-                                                           block_vecs, scale_vecs, n_vecs, dev_status);
-    return cudaGetLastError();
+    cudaLaunchAttribute pdl[1];
+    cudaLaunchConfig_t lc = dependent_launch(pdl, (unsigned)grid, 256, stream);
+    return cudaLaunchKernelEx(&lc, copy_blocks_kernel, (uint4 *)k_pool, (uint4 *)v_pool, (uint4 *)k_scales,
+                              (uint4 *)v_scales, (const int2 *)pairs, d.n_blocks, block_vecs, scale_vecs, n_vecs,
+                              dev_status);
 }
 
 }  // namespace pkv
