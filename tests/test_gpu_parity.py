@@ -417,6 +417,43 @@ def test_prefill_identity_vs_permuted_tables_bit_exact(P):
     assert torch.equal(out.view(torch.int16), out2.view(torch.int16)) and torch.equal(lse, lse2)
 
 
+def test_write_prefill_gather_back_to_back_on_one_stream(P):
+    """Library kernels launched back to back on one stream with no host
+    synchronisation, each a programmatic dependent of the one before: the
+    chunk write, the prefill that attends the rows just written, a gather of
+    the same pages, a second write of the same rows and a second prefill.
+    Pools and gather are the oracle's bit for bit, both prefills within the
+    parity tolerances (and identical to each other)."""
+    w = workload("prefill_small")
+    kp, vp, _, _ = empty_pools(w, poison=True)
+    write_prefix(w, kp, vp, None, None)
+    gk, gv = dev(kp), dev(vp)
+    tables, prefix = i32(w.tables), i32(w.stored_lens)
+    k_new, v_new, q = w.k_new.cuda(), w.v_new.cuda(), w.q.cuda()
+    total = w.stored_lens + w.n_new
+    lens = i32(total)
+    T = int(total.max())
+    st = status_tensor()
+    P.paged_kv_write(k_new, v_new, gk, gv, tables, i32(w.start_pos), dev_status=st)
+    out1 = P.paged_prefill_attention(q, gk, gv, tables, prefix, w.softmax_scale, dev_status=st)
+    ko, vo = P.paged_kv_gather(gk, gv, tables, lens, T, dev_status=st)
+    P.paged_kv_write(k_new, v_new, gk, gv, tables, i32(w.start_pos), dev_status=st)
+    out2 = P.paged_prefill_attention(q, gk, gv, tables, prefix, w.softmax_scale, dev_status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    rk, rv, _, _ = oracle_pools_after_step(w, poison=True)
+    assert np.array_equal(host(gk), rk) and np.array_equal(host(gv), rv)
+    code, gk_ref, gv_ref = oracle.gather(rk, rv, dims_of(w), w.tables, total, T)
+    assert code == oracle.OK
+    assert np.array_equal(host(ko), gk_ref) and np.array_equal(host(vo), gv_ref)
+    code, ref, _ = oracle.prefill(w.q, rk, rv, dims_of(w), w.tables, w.stored_lens, w.softmax_scale,
+                                  n_threads=NTHREADS)
+    assert code == 0
+    mx, mean = attention_errors(out1, ref)
+    assert mx <= BF16_MAX and mean <= BF16_MEAN, (mx, mean)
+    assert torch.equal(out1.view(torch.int16), out2.view(torch.int16))
+
+
 # ---------------------------------------------------------------------------
 # the fused decode step: write + decode in one call
 # ---------------------------------------------------------------------------
